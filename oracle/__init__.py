@@ -1,0 +1,196 @@
+"""CPU oracle for the lightning indexer -- TEST INFRASTRUCTURE ONLY.
+
+Only the tests, the package smoke check and the benchmark's CPU-baseline leg
+may import this package.  The product path (the CUDA library and its Python
+binding) never imports, links or calls it.
+
+The arithmetic lives in ``idx_oracle.c`` (scalar C, fp64); this module only
+compiles it with gcc and passes numpy arrays to it through ctypes.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "idx_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "libidx_oracle.so")
+_lib = None
+_lock = threading.Lock()
+
+FMT_FP8 = 0
+FMT_MXFP4 = 1
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle to a shared object (gcc, -O2, no fast-math)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    stale = (not os.path.exists(_LIB_PATH)
+             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+    if force or stale:
+        tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+                               "-fno-fast-math", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = ctypes.CDLL(build())
+            _declare(_lib)
+    return _lib
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_L = ctypes.c_int64
+
+
+def _declare(L):
+    L.orc_e4m3_to_double.argtypes = [ctypes.c_uint8]
+    L.orc_e4m3_to_double.restype = ctypes.c_double
+    L.orc_e2m1_to_double.argtypes = [ctypes.c_uint8]
+    L.orc_e2m1_to_double.restype = ctypes.c_double
+    L.orc_e8m0_to_double.argtypes = [ctypes.c_uint8]
+    L.orc_e8m0_to_double.restype = ctypes.c_double
+    L.orc_default_threads.restype = _I
+    L.orc_row_end.argtypes = [_P, _I, _I, _I]
+    L.orc_row_end.restype = _I
+    L.orc_mqa_logits.argtypes = [_I, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _L, _I]
+    L.orc_mqa_logits.restype = _I
+    L.orc_paged_mqa_logits.argtypes = [_I, _P, _P, _P, _P, _L, _I, _P, _L, _I, _P, _I, _P,
+                                       _I, _I, _I, _I, _I, _P, _L, _I, _I]
+    L.orc_paged_mqa_logits.restype = _I
+    L.orc_apply_candidate_mask.argtypes = [_P, _L, _I, _I, _P, _P, _P, _L, _I, _I, _I, _I]
+    L.orc_apply_candidate_mask.restype = _I
+    L.orc_topk.argtypes = [_P, _L, _I, _I, _P, _I, _P, _L, _I]
+    L.orc_topk.restype = _I
+    L.orc_topk_to_ragged_slots.argtypes = [_P, _L, _I, _I, _P, _I, _P, _L, _I, _I, _I,
+                                           _P, _P, _P]
+    L.orc_topk_to_ragged_slots.restype = _I
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    assert a.flags["C_CONTIGUOUS"], "oracle inputs must be C-contiguous"
+    return a.ctypes.data
+
+
+def _c(a, dtype):
+    return None if a is None else np.ascontiguousarray(a, dtype=dtype)
+
+
+def default_threads() -> int:
+    return lib().orc_default_threads()
+
+
+def e4m3_to_double(code: int) -> float:
+    return lib().orc_e4m3_to_double(code)
+
+
+def e2m1_to_double(code: int) -> float:
+    return lib().orc_e2m1_to_double(code)
+
+
+def e8m0_to_double(code: int) -> float:
+    return lib().orc_e8m0_to_double(code)
+
+
+def mqa_logits(fmt, q, q_scale, weights, k, k_scale, ks, ke, M, N, H, D,
+               ld=None, nthreads=0) -> np.ndarray:
+    """Non-paged logits [M, ld] (columns [0, N) defined)."""
+    ld = N if ld is None else ld
+    out = np.full((M, max(ld, 1)), np.nan, dtype=np.float32)
+    q, k = _c(q, np.uint8), _c(k, np.uint8)
+    if fmt == FMT_FP8:
+        q_scale, k_scale = _c(q_scale, np.float32), _c(k_scale, np.float32)
+    else:
+        q_scale, k_scale = _c(q_scale, np.uint8), _c(k_scale, np.uint8)
+    w, ks, ke = _c(weights, np.float32), _c(ks, np.int32), _c(ke, np.int32)
+    rc = lib().orc_mqa_logits(fmt, _ptr(q), _ptr(q_scale), _ptr(w), _ptr(k), _ptr(k_scale),
+                              _ptr(ks), _ptr(ke), M, N, H, D, _ptr(out), ld, nthreads)
+    if rc != 0:
+        raise ValueError("oracle mqa_logits rejected its arguments")
+    return out[:, :ld]
+
+
+def paged_mqa_logits(fmt, q, q_scale, weights, pages, page_stride, num_pages, block_table,
+                     context_lens, ctx_per_row, row_ks, B, next_n, H, D, page_size, width,
+                     out=None, nthreads=0):
+    """Paged logits [B*next_n, width]; columns [ke_r, width) keep ``out``'s
+    contents (NaN when ``out`` is None).  Returns (logits, bad_key_count)."""
+    rows = B * next_n
+    if out is None:
+        out = np.full((rows, width), np.nan, dtype=np.float32)
+    q = _c(q, np.uint8)
+    q_scale = _c(q_scale, np.float32 if fmt == FMT_FP8 else np.uint8)
+    bt = _c(block_table, np.int32)
+    ctx = _c(context_lens, np.int32)
+    rks = _c(row_ks, np.int32)
+    w = _c(weights, np.float32)
+    pages = _c(pages, np.uint8)
+    bad = lib().orc_paged_mqa_logits(fmt, _ptr(q), _ptr(q_scale), _ptr(w), _ptr(pages),
+                                     page_stride, num_pages, _ptr(bt), bt.shape[1],
+                                     bt.shape[1], _ptr(ctx), int(ctx_per_row), _ptr(rks),
+                                     B, next_n, H, D, page_size, _ptr(out), out.shape[1],
+                                     width, nthreads)
+    if bad < 0:
+        raise ValueError("oracle paged_mqa_logits rejected its arguments")
+    return out, bad
+
+
+def row_end(context_lens, ctx_per_row, next_n, r) -> int:
+    ctx = _c(context_lens, np.int32)
+    return lib().orc_row_end(_ptr(ctx), int(ctx_per_row), next_n, r)
+
+
+def apply_candidate_mask(logits, row_ks, row_ke, cand, block_size, row_repeat=1,
+                         nthreads=0):
+    """In place on a C-contiguous float32 [rows, width] array."""
+    assert logits.dtype == np.float32 and logits.flags["C_CONTIGUOUS"]
+    rows, width = logits.shape
+    rks, rke, cand = _c(row_ks, np.int32), _c(row_ke, np.int32), _c(cand, np.int32)
+    rc = lib().orc_apply_candidate_mask(_ptr(logits), width, rows, width, _ptr(rks),
+                                        _ptr(rke), _ptr(cand), cand.shape[1], cand.shape[1],
+                                        block_size, row_repeat, nthreads)
+    if rc != 0:
+        raise ValueError("oracle apply_candidate_mask rejected its arguments")
+    return logits
+
+
+def topk(logits, lengths, k, nthreads=0) -> np.ndarray:
+    """[rows, k] int32, largest first (ties: lower index first), -1 padded."""
+    logits = _c(logits, np.float32)
+    rows, width = logits.shape
+    lengths = _c(lengths, np.int32)
+    out = np.empty((rows, k), dtype=np.int32)
+    rc = lib().orc_topk(_ptr(logits), width, rows, width, _ptr(lengths), k, _ptr(out), k,
+                        nthreads)
+    if rc != 0:
+        raise ValueError("oracle topk rejected its arguments")
+    return out
+
+
+def topk_to_ragged_slots(topk_idx, block_table, page_size, num_pages, next_n=1,
+                         row_to_seq=None):
+    """Returns (slots [nnz], indptr [rows+1], lens [rows], invalid_count)."""
+    t = _c(topk_idx, np.int32)
+    rows, k = t.shape
+    bt = _c(block_table, np.int32)
+    r2s = _c(row_to_seq, np.int32)
+    slots = np.empty(max(rows * k, 1), dtype=np.int32)
+    indptr = np.empty(rows + 1, dtype=np.int32)
+    lens = np.empty(max(rows, 1), dtype=np.int32)
+    bad = lib().orc_topk_to_ragged_slots(_ptr(t), k, rows, k, _ptr(r2s), next_n, _ptr(bt),
+                                         bt.shape[1], bt.shape[1], page_size, num_pages,
+                                         _ptr(slots), _ptr(indptr), _ptr(lens))
+    return slots[:indptr[rows]], indptr, lens[:rows], bad
