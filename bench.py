@@ -1,0 +1,414 @@
+"""Benchmark of one indexer step on synthetic data.
+
+Default workload: paged FP8 MTP decode with a candidate mask (B=128
+sequences, next_n=2, lognormal contexts with median 16384, 64 candidate
+blocks of 128 keys per row, top-2048 mapped to ragged cache slots).  A step
+is the whole hot path: paged logits with the candidate mask fused in, per-row
+top-k, and the top-k -> slot map.
+
+Metric: indexer keys scored per second (sum over rows of ke - ks, per step
+time), whole job over all ranks.  Every rank runs its own independent batch
+(weak scaling; the path has no exchange step).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..5]
+                  [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "indexer Gkeys scored/s (paged FP8 decode) + top-k rows/s; % of HBM/TC roofline"
+UNIT = "Gkeys/s"
+WORKLOAD_NAMES = {
+    1: "non-paged FP8 logits+top-256, M=16 N=1024 H=64 D=128",
+    2: "prefill chunk FP8 logits+top-2048, 2048 rows x 8192 keys, H=64 D=128",
+    3: "paged FP8 decode, B=64 next_n=1 ctx U[4096,32768], page 64, top-2048 + slots",
+    4: "paged FP8 MTP decode, B=128 next_n=2 lognormal ctx (median 16384), 64 candidate blocks "
+       "of 128 per row, top-2048 + ragged slots",
+    5: "paged MXFP4 decode, B=32 ctx 131072, page 64, top-2048 + slots",
+}
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+class Clocks:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        self.proc.wait()
+        sms, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sms.append(float(parts[1]))
+                    maxes.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sms) if sms else None,
+                "sm_max_mhz": max(maxes) if maxes else None,
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+def _case(cfg: int):
+    from sparse_attention_indexer_mxfp4_gb300 import synth
+    return synth.CONFIGS[cfg]()
+
+
+def logits_bytes(case) -> float:
+    """Algorithmic bytes of one logits launch: every live key's values and
+    scale read once per sequence, the group's queries, weights and candidate
+    ids read once, one fp32 logit written per scored (row, key), block-table
+    entries read once per page."""
+    from sparse_attention_indexer_mxfp4_gb300.synth import FMT_FP8, PagedCase
+    D, H = case.D, case.H
+    per_key = (D + 4) if case.fmt == FMT_FP8 else (D // 2 + D // 32)
+    per_q = H * ((D if case.fmt == FMT_FP8 else D // 2 + D // 32) + 4)
+    if isinstance(case, PagedCase):
+        ke = np.clip(case.row_ends(), 0, case.width)
+        seq_keys = ke.reshape(case.B, case.next_n).max(axis=1)
+        b = float(seq_keys.sum()) * per_key
+        b += case.rows * per_q
+        b += float(ke.sum()) * 4
+        b += float(np.ceil(seq_keys / case.page_size).sum()) * 4
+        if case.cand is not None:
+            b += case.cand.size * 4
+        return b
+    # contiguous: K read once per row group (it stays in L2), Q once, every
+    # column of [0, N) of every row written
+    b = case.N * per_key + case.M * per_q + case.M * case.N * 4.0
+    return b
+
+
+def logits_flops(case) -> float:
+    return 2.0 * case.H * case.D * case.keys_scored
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from sparse_attention_indexer_mxfp4_gb300 import IndexerStep, idx_get_device_status
+    from sparse_attention_indexer_mxfp4_gb300.synth import PagedCase
+
+    world, rank, local = _dist()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    case = _case(args.config)
+    step = IndexerStep(case, device=dev)
+    stream = torch.cuda.current_stream()
+
+    # warm-up (also builds and loads the library)
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+    assert idx_get_device_status() == 0, "device status set during warm-up"
+
+    # L2: the K pages read per step exceed the 129 MB L2 for the paged
+    # workloads; for the contiguous ones a 256 MB buffer is rewritten
+    # between steps.
+    flush = None
+    if not isinstance(case, PagedCase):
+        flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = Clocks(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    total_ms = 0.0
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    flush_ms = 0.0
+    for i in range(args.steps):
+        if flush is not None:
+            f0 = torch.cuda.Event(enable_timing=True)
+            f1 = torch.cuda.Event(enable_timing=True)
+            f0.record(stream)
+            flush.fill_(float(i))
+            f1.record(stream)
+        if i == 0:
+            t0.record(stream)
+        a, b, c, d = ev[i]
+        a.record(stream)
+        step.logits_stage()
+        b.record(stream)
+        step.topk_stage()
+        c.record(stream)
+        step.slots_stage()
+        d.record(stream)
+        if flush is not None:
+            torch.cuda.synchronize()
+            flush_ms += f0.elapsed_time(f1)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if world > 1:
+        dist.barrier()
+    total_ms = t0.elapsed_time(t1) - flush_ms
+    logit_ms = [a.elapsed_time(b) for a, b, _, _ in ev]
+    topk_ms = [b.elapsed_time(c) for _, b, c, _ in ev]
+    step_ms = [a.elapsed_time(d) for a, _, _, d in ev]
+    ms_per_step = sum(step_ms) / len(step_ms)
+    if flush is None:
+        ms_per_step = total_ms / args.steps
+
+    t = torch.tensor([ms_per_step, sum(logit_ms) / len(logit_ms), sum(topk_ms) / len(topk_ms)],
+                     device=dev, dtype=torch.float64)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_per_step, logit_avg, topk_avg = t.tolist()
+
+    keys = case.keys_scored
+    rows = case.rows if isinstance(case, PagedCase) else case.M
+    e2e = run_e2e(step, case, args, dev) if rank == 0 else None
+
+    hbm, bf16, src = _peaks()
+    lb = logits_bytes(case)
+    achieved_gbs = lb / (logit_avg * 1e-3) / 1e9
+    if args.config == 2:
+        fp8_peak = 2.0 * bf16  # dense fp8 rate = 2x bf16 on this part
+        ach = logits_flops(case) / (logit_avg * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": fp8_peak,
+                "unit": "TFLOP/s", "frac": round(ach / fp8_peak, 4),
+                "traffic": None, "peak_source": f"{src} bf16 x 2 (fp8 dense)"}
+    else:
+        roof = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved_gbs / hbm, 4), "traffic": None,
+                "peak_source": f"{src} hbm_gbs", "kernel": "logits_kernel",
+                "algorithmic_bytes_per_launch": lb, "avg_launch_ms": round(logit_avg, 5)}
+    out = {
+        "metric": METRIC, "value": round(world * keys / (ms_per_step * 1e-3) / 1e9, 4),
+        "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32" if case.fmt == 0 else
+        "e2m1 x e2m1 (e8m0 block scales) -> f32",
+        "data": "synthetic (seeded; shapes and distributions of the workload description)",
+        "config": {"workload": WORKLOAD_NAMES[args.config], "config_id": args.config,
+                   "rows": rows, "keys_scored_per_step": keys,
+                   "l2": "flushed between steps" if flush is not None else
+                   "K pages read per step exceed L2"},
+        "topk_rows_per_s": round(world * rows / (topk_avg * 1e-3), 1),
+        "logits_ms": round(logit_avg, 5), "topk_ms": round(topk_avg, 5),
+        "roofline": roof, "clocks": clk,
+        "gpu_launches": step.launches_per_step * args.steps,
+        "e2e": e2e,
+    }
+    if rank == 0:
+        out["cpu_baseline"] = cpu_baseline(case, args) if world == 1 and not args.no_cpu else None
+        print(json.dumps(out))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(step, case, args, dev):
+    """Same metric through the public API with host buffers: each step copies
+    the step's inputs (queries, weights, lengths, block table, candidates)
+    from pinned host memory and reads the top-k indices and ragged slots
+    back.  The K cache itself is resident device state (it is written by the
+    cache producer, not per step)."""
+    import torch
+    from sparse_attention_indexer_mxfp4_gb300.synth import PagedCase
+
+    names = ["q", "weights", "lengths"]
+    if isinstance(case, PagedCase):
+        names += ["block_table", "context_lens"] + (["cand"] if case.cand is not None else [])
+    else:
+        names += ["ks", "ke"]
+    host = {n: getattr(step, n).cpu().pin_memory() for n in names}
+    outs = [step.topk] + ([step.slots, step.indptr] if isinstance(case, PagedCase) else [])
+    host_out = [o.cpu().pin_memory() for o in outs]
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    stream = torch.cuda.current_stream()
+    steps = max(3, args.steps)
+
+    def one():
+        for n, t in host.items():
+            getattr(step, n).copy_(t, non_blocking=True)
+        step.run()
+        for h, o in zip(host_out, outs):
+            h.copy_(o, non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        one()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    return {"value": round(case.keys_scored / (ms * 1e-3) / 1e9, 4), "unit": UNIT,
+            "ms_per_step": round(ms, 5), "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h)}
+
+
+def _oracle_sample(case, nseq):
+    """The oracle's step (logits, mask, top-k, slots) over the first nseq
+    sequences (paged) or rows (contiguous) of the workload; returns keys."""
+    import oracle
+    from sparse_attention_indexer_mxfp4_gb300.synth import PagedCase
+    if isinstance(case, PagedCase):
+        rows = np.arange(nseq * case.next_n)
+        ctx = case.context_lens[rows] if case.ctx_per_row else case.context_lens[:nseq]
+        out, _ = oracle.paged_mqa_logits(case.fmt, case.q[rows],
+                                         None if case.q_scale is None else case.q_scale[rows],
+                                         case.weights[rows], case.pages, case.page_stride,
+                                         case.num_pages, case.block_table[:nseq], ctx,
+                                         case.ctx_per_row, None, nseq, case.next_n, case.H,
+                                         case.D, case.page_size, case.width)
+        ke = np.clip(case.row_ends()[rows], 0, case.width).astype(np.int32)
+        if case.cand is not None:
+            oracle.apply_candidate_mask(out, None, ke, case.cand[rows], case.cand_block)
+        out = np.where(np.isnan(out), -np.inf, out)
+        idx = oracle.topk(out, ke, case.topk)
+        oracle.topk_to_ragged_slots(idx, case.block_table[:nseq], case.page_size,
+                                    case.num_pages, next_n=case.next_n)
+        return int(ke.sum())
+    rows = np.arange(nseq)
+    out = oracle.mqa_logits(case.fmt, case.q[rows], None, case.weights[rows], case.k,
+                            case.k_scale, case.ks[rows], case.ke[rows], nseq, case.N, case.H,
+                            case.D)
+    oracle.topk(out, case.ke[rows], case.topk)
+    return int(np.maximum(case.ke[rows] - case.ks[rows], 0).sum())
+
+
+def _units(case):
+    from sparse_attention_indexer_mxfp4_gb300.synth import PagedCase
+    return case.B if isinstance(case, PagedCase) else case.M
+
+
+def cpu_baseline(case, args, target_s: float = 10.0):
+    """The oracle as it stands, on this host's cores, over a growing prefix
+    of the workload until about target_s seconds of work."""
+    import oracle
+    n = 1
+    total = _units(case)
+    while True:
+        t = time.time()
+        keys = _oracle_sample(case, n)
+        dt = time.time() - t
+        if dt >= target_s or n >= total:
+            break
+        n = min(total, max(n + 1, int(n * min(8.0, target_s / max(dt, 1e-3)))))
+    return {"value": round(keys / dt / 1e9, 6), "unit": UNIT, "cores": oracle.default_threads(),
+            "kind": "oracle",
+            "sample": f"first {n} of {total} {'sequences' if hasattr(case, 'B') else 'rows'} "
+                      f"({keys} keys): fp64 scalar logits + mask + top-k + slots, {dt:.1f} s"}
+
+
+def run_reference(args):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    import oracle
+    case = _case(args.config)
+    nseq = 1
+    for _ in range(args.warmup):
+        _oracle_sample(case, nseq)
+    t = time.time()
+    keys = 0
+    for _ in range(args.steps):
+        keys += _oracle_sample(case, nseq)
+    dt = time.time() - t
+    v = keys / dt / 1e9
+    total = _units(case)
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64 (scalar CPU oracle)",
+        "data": "synthetic", "config": {"workload": WORKLOAD_NAMES[args.config],
+                                        "config_id": args.config},
+        "cpu_baseline": {"value": round(v, 6), "unit": UNIT, "cores": oracle.default_threads(),
+                         "kind": "oracle",
+                         "sample": f"each step: the first 1 of {total} units of the workload"},
+        "e2e": {"value": round(v, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0}}))
+
+
+def main():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--config", type=int, default=4, choices=[1, 2, 3, 4, 5])
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    args = p.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

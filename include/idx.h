@@ -1,0 +1,204 @@
+/*
+ * idx.h -- C ABI of the GB300 (sm_103a) sparse-attention lightning indexer.
+ *
+ * For every query row r the indexer scores each cached key token t:
+ *
+ *     logits[r, t] = sum_h w[r, h] * relu(k_scale[t] * q_scale[r, h] * (q[r, h, :] . k[t, :]))
+ *
+ * (vLLM API page "vllm.v1.attention.ops.rocm_aiter_mla_sparse", section
+ * fp8_mqa_logits_torch), masks each row to [ks, ke) and optionally to
+ * candidate blocks (same page, _apply_candidate_mask_strided), selects the
+ * top-k token indices per row (page "vllm.v1.attention.ops.
+ * rocm_paged_mxfp4_indexer", section _topk) and maps them to ragged cache
+ * slots (page rocm_aiter_mla_sparse, build_prefill_topk_ragged_indices).
+ *
+ * Conventions shared by every entry point:
+ *   - Every data pointer is a DEVICE pointer owned by the caller; the library
+ *     never frees or keeps it.  Nothing on the compute path allocates device
+ *     memory.
+ *   - Every call is asynchronous on `stream` (0 = legacy default stream), never
+ *     synchronises the host, and derives its grid from the arguments alone, so
+ *     a call can be recorded into a CUDA graph.
+ *   - Host-side checks run before any launch and return IDX_ERR_INVALID_ARG
+ *     (null pointer, negative size, bad stride) or IDX_ERR_UNSUPPORTED (a
+ *     shape this build has no kernel for).  Nothing is launched then.
+ *   - Faults found on the device (a block-table entry or candidate id outside
+ *     its range) never trap: the affected keys are written -inf (logits) or
+ *     dropped (slots) and a sticky bit is set in the device status word, read
+ *     and cleared by idx_get_device_status().
+ *   - Integers are int32 unless stated; row-major layouts; strides in elements
+ *     unless the name ends in _bytes.
+ */
+#ifndef IDX_H_
+#define IDX_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *idx_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    IDX_OK = 0,
+    IDX_ERR_INVALID_ARG = 1,
+    IDX_ERR_UNSUPPORTED = 2,
+    IDX_ERR_WORKSPACE = 3,
+    IDX_ERR_CUDA = 4
+} idx_status;
+
+typedef enum {
+    /* OCP e4m3 values, one fp32 scale per key. */
+    IDX_KV_FP8_E4M3 = 0,
+    /* OCP MX: packed e2m1 (element 2i = low nibble of byte i) with one e8m0
+     * scale byte per 32 elements. */
+    IDX_KV_MXFP4 = 1
+} idx_kv_format;
+
+/* Bits of the device status word. */
+#define IDX_DEV_BAD_PAGE 1u      /* block-table entry outside [0, num_pages) */
+#define IDX_DEV_BAD_CANDIDATE 2u /* reserved: candidate ids are range-checked and ignored */
+#define IDX_DEV_TIMEOUT 4u       /* a bounded pipeline wait ran out; outputs undefined */
+
+/* ------------------------------------------------------------------------
+ * idx_mqa_logits -- non-paged logits for one key sequence.
+ * Passage: rocm_aiter_mla_sparse, fp8_mqa_logits_torch (shapes, [ks, ke)
+ * semantics) and rocm_fp8_mqa_logits.
+ *
+ *   q        FP8: e4m3 [M, H, D].  MXFP4: packed [M, H, D/2].
+ *   q_scale  FP8: NULL or fp32 [M, H], applied inside the relu.
+ *            MXFP4: e8m0 bytes [M, H, D/32] (one int32 per head at D = 128,
+ *            byte i scaling elements [32i, 32i+32)).  Required.
+ *   weights  fp32 [M, H].
+ *   k        FP8: e4m3 [N, D].  MXFP4: packed [N, D/2].  16-byte aligned.
+ *   k_scale  FP8: fp32 [N].  MXFP4: e8m0 bytes [N, D/32].
+ *   row_ks, row_ke  [M]: key range [ks, ke) of each row; 0 <= ks, ke <= N.
+ *   logits   fp32 [M, ld_logits], ld_logits >= N.  Columns [0, N) of every
+ *            row are written: the score inside [ks, ke), -inf outside.
+ *   ws, ws_bytes  unused (may be NULL / 0); kept for ABI stability.
+ * Supported: D = 128, H in {32, 64, 128}.  Keys are scored in tiles of 128
+ * on tcgen05 tensor cores with fp32 accumulation.
+ * ---------------------------------------------------------------------- */
+idx_status idx_mqa_logits(const void *q, const void *q_scale, const float *weights,
+                          const void *k, const void *k_scale, const int32_t *row_ks,
+                          const int32_t *row_ke, int M, int N, int H, int D,
+                          idx_kv_format fmt, float *logits, int64_t ld_logits, void *ws,
+                          size_t ws_bytes, idx_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * idx_paged_mqa_logits -- logits over a paged K cache for decode / MTP rows.
+ * Passage: rocm_aiter_mla_sparse, rocm_fp8_paged_mqa_logits and
+ * rocm_fp8_paged_mqa_logits_triton; MXFP4 inputs as in
+ * rocm_paged_mxfp4_indexer, rocm_mxfp4_sparse_attn_indexer.
+ *
+ *   q         [B, next_n, H, D] e4m3 or [B, next_n, H, D/2] packed e2m1.
+ *   q_scale   as for idx_mqa_logits, with M = B * next_n rows.
+ *   weights   fp32 [B * next_n, H].
+ *   kv_pages  the page pool, page p at kv_pages + p * page_stride_bytes
+ *             (16-byte aligned, stride a multiple of 16).  Block-flat pages:
+ *             FP8:   page_size * D e4m3 bytes (token-major), then page_size
+ *                    fp32 scales;
+ *             MXFP4: page_size * D/2 packed bytes, then page_size * D/32 e8m0
+ *                    bytes (token-major).
+ *   block_table [B, bt_stride] (>= ceil(max_model_len / page_size) columns
+ *             used): logical page j of sequence b is physical page
+ *             block_table[b * bt_stride + j].
+ *   context_lens [B] (ctx_per_row = 0) or [B * next_n] (ctx_per_row = 1).
+ *             Row j of sequence b ends at ke = context_lens[b] - next_n + j + 1
+ *             in the first case, at context_lens[b * next_n + j] in the second.
+ *   row_ks    NULL (all 0) or [B * next_n] row starts; keys below ks are -inf.
+ *   candidate_blocks NULL, or [B * next_n, cand_stride] int32 block ids of
+ *             cand_block keys counted from the row's ks: a fused candidate mask
+ *             (see idx_apply_candidate_mask); num_cand ids per row are read,
+ *             negative or out-of-range ids are ignored.
+ *   logits    fp32 [B * next_n, ld_logits], ld_logits >= max_model_len.  Only
+ *             columns [0, ke) of each row are written; [ke, max_model_len) is
+ *             left untouched (consumers read each row up to its length).
+ *   num_ctas  0 = one persistent CTA per SM; otherwise the grid size.
+ * Supported: D = 128, page_size a multiple of 64, next_n * H <= 256.
+ * ---------------------------------------------------------------------- */
+idx_status idx_paged_mqa_logits(const void *q, const void *q_scale, const float *weights,
+                                const uint8_t *kv_pages, int64_t page_stride_bytes,
+                                int num_pages, const int32_t *block_table, int64_t bt_stride,
+                                const int32_t *context_lens, int ctx_per_row,
+                                const int32_t *row_ks, int B, int next_n, int H, int D,
+                                int page_size, idx_kv_format fmt,
+                                const int32_t *candidate_blocks, int64_t cand_stride,
+                                int num_cand, int cand_block, float *logits,
+                                int64_t ld_logits, int max_model_len, int num_ctas, void *ws,
+                                size_t ws_bytes, idx_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * idx_apply_candidate_mask -- in-place candidate mask on existing logits.
+ * Passage: rocm_aiter_mla_sparse, _apply_candidate_mask_strided.
+ *
+ * Row r keeps column t iff ks_r <= t < ke_r and the block (t - ks_r) /
+ * block_size is one of the num_cand ids in candidate row r / row_repeat;
+ * every other column of [0, ke_r) is set to -inf.  Columns [ke_r, width) are
+ * not touched.  Only -inf is written; logits are never read.
+ *   logits [rows, ld], width <= ld; row_ks NULL (0) or [rows]; row_ke [rows]
+ *   (0 <= ke <= width); candidate_blocks [ceil(rows / row_repeat), cand_stride].
+ * ---------------------------------------------------------------------- */
+idx_status idx_apply_candidate_mask(float *logits, int64_t ld, int rows, int width,
+                                    const int32_t *row_ks, const int32_t *row_ke,
+                                    const int32_t *candidate_blocks, int64_t cand_stride,
+                                    int num_cand, int block_size, int row_repeat,
+                                    idx_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * idx_topk -- per-row top-k token indices.
+ * Passage: rocm_paged_mxfp4_indexer, _topk ("top-k over each row's
+ * [0, lengths[row]); -1 pads rows shorter than k").
+ *
+ *   logits  fp32 [rows, ld]; lengths [rows] with 0 <= lengths[r] <= ld.
+ *   out_idx int32 [rows, ld_out], ld_out >= k.  Row r receives the indices of
+ *           its min(k, #finite) largest finite values in [0, lengths[r]), in
+ *           ASCENDING index order, then -1 padding.  -inf and NaN are never
+ *           selected.  Among equal values at the k-th place the lower indices
+ *           win, so the selected set is unique.
+ *   1 <= k <= 16384.  Rows are processed by thread-block clusters that keep
+ *   the row in distributed shared memory.
+ *   ws, ws_bytes  unused (may be NULL / 0).
+ * ---------------------------------------------------------------------- */
+idx_status idx_topk(const float *logits, int64_t ld, int rows, const int32_t *lengths, int k,
+                    int32_t *out_idx, int64_t ld_out, void *ws, size_t ws_bytes,
+                    idx_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * idx_topk_to_ragged_slots -- top-k positions to a ragged list of cache slots.
+ * Passage: rocm_aiter_mla_sparse, build_prefill_topk_ragged_indices; the
+ * slot of position p is block_table[b, p / page_size] * page_size +
+ * p % page_size (page rocm_aiter_mla, _expand_page_indices_kernel).
+ *
+ *   topk [rows, ld] int32 positions (-1 = none).  Row r belongs to sequence
+ *   row_to_seq[r] (row_to_seq NULL: r / next_n).  Entries are kept in order;
+ *   -1 entries are dropped, and so is an entry whose logical page is
+ *   >= max_blocks or whose page id is outside [0, num_pages) (status bit
+ *   IDX_DEV_BAD_PAGE is then set).
+ *   slots  [rows * k] capacity; indptr [rows + 1] (exclusive prefix sum of
+ *   lens, indptr[0] = 0); lens [rows].
+ * ---------------------------------------------------------------------- */
+idx_status idx_topk_to_ragged_slots(const int32_t *topk, int64_t ld, int rows, int k,
+                                    const int32_t *row_to_seq, int next_n,
+                                    const int32_t *block_table, int64_t bt_stride,
+                                    int max_blocks, int page_size, int num_pages,
+                                    int32_t *slots, int32_t *indptr, int32_t *lens,
+                                    idx_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * idx_get_device_status -- read and clear the sticky device status word of
+ * the current device (IDX_DEV_* bits).  Synchronises `stream`; it is the
+ * only call that does.  *out receives the bits.
+ * ---------------------------------------------------------------------- */
+idx_status idx_get_device_status(idx_stream_t stream, uint32_t *out);
+
+/* Library version string, e.g. "idx 0.1 sm_103a". */
+const char *idx_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* IDX_H_ */

@@ -1,0 +1,195 @@
+"""Thin ctypes binding of libidx.so (include/idx.h).
+
+Argument marshalling only: every function takes torch CUDA tensors, checks
+dtype / shape / device, and passes raw device pointers, sizes and the current
+CUDA stream to the C entry point of the same name.  All computation happens in
+the library's CUDA kernels; there is no fallback path.  A missing or unloadable
+library raises at import of this module's first call.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+FMT_FP8 = 0
+FMT_MXFP4 = 1
+
+IDX_OK = 0
+_ERRORS = {1: "IDX_ERR_INVALID_ARG", 2: "IDX_ERR_UNSUPPORTED", 3: "IDX_ERR_WORKSPACE",
+           4: "IDX_ERR_CUDA"}
+DEV_BAD_PAGE = 1
+DEV_TIMEOUT = 4
+
+_lib = None
+_lock = threading.Lock()
+
+_P, _I, _L, _S = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+
+_SIGNATURES = {
+    "idx_mqa_logits": [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _L, _P, _S, _P],
+    "idx_paged_mqa_logits": [_P, _P, _P, _P, _L, _I, _P, _L, _P, _I, _P, _I, _I, _I, _I, _I, _I,
+                             _P, _L, _I, _I, _P, _L, _I, _I, _P, _S, _P],
+    "idx_apply_candidate_mask": [_P, _L, _I, _I, _P, _P, _P, _L, _I, _I, _I, _P],
+    "idx_topk": [_P, _L, _I, _P, _I, _P, _L, _P, _S, _P],
+    "idx_topk_to_ragged_slots": [_P, _L, _I, _I, _P, _I, _P, _L, _I, _I, _I, _P, _P, _P, _P],
+    "idx_get_device_status": [_P, ctypes.POINTER(ctypes.c_uint32)],
+}
+
+
+class IndexerError(RuntimeError):
+    pass
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib() -> ctypes.CDLL:
+    """Load libidx.so (building it first if the sources are newer)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build() if not os.environ.get("IDX_NO_BUILD") else _build.LIB
+            if not os.path.exists(path):
+                raise IndexerError(f"indexer library missing: {path}")
+            L = ctypes.CDLL(path)
+            for name, args in _SIGNATURES.items():
+                fn = getattr(L, name)
+                fn.argtypes = args
+                fn.restype = ctypes.c_int
+            L.idx_version.restype = ctypes.c_char_p
+            _lib = L
+    return _lib
+
+
+def _check(rc: int, name: str):
+    if rc != IDX_OK:
+        raise IndexerError(f"{name} returned {_ERRORS.get(rc, rc)}")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("indexer tensors must live on a CUDA device")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _u8(t):
+    return t.view(torch.uint8) if t.dtype != torch.uint8 else t
+
+
+def _need(t, dtype, name):
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def version() -> str:
+    return lib().idx_version().decode()
+
+
+def idx_mqa_logits(q, q_scale, weights, k, k_scale, row_ks, row_ke, fmt, logits,
+                   stream=None):
+    """Non-paged logits.  q [M,H,D] (fp8) or [M,H,D/2] (mxfp4) bytes; k [N,D] or
+    [N,D/2]; logits fp32 [M, >= N] (row stride used as ld)."""
+    q, k = _u8(q), _u8(k)
+    M, H = q.shape[0], q.shape[1]
+    D = q.shape[2] if fmt == FMT_FP8 else 2 * q.shape[2]
+    N = k.shape[0]
+    _need(weights, torch.float32, "weights")
+    _need(row_ks, torch.int32, "row_ks")
+    _need(row_ke, torch.int32, "row_ke")
+    if logits.dtype != torch.float32 or logits.stride(1) != 1:
+        raise ValueError("logits must be float32 with unit column stride")
+    rc = lib().idx_mqa_logits(_ptr(q), _ptr(q_scale), _ptr(weights), _ptr(k), _ptr(k_scale),
+                              _ptr(row_ks), _ptr(row_ke), M, N, H, D, fmt, _ptr(logits),
+                              logits.stride(0), None, 0, _stream(stream))
+    _check(rc, "idx_mqa_logits")
+
+
+def idx_paged_mqa_logits(q, q_scale, weights, kv_pages, block_table, context_lens, next_n,
+                         page_size, fmt, logits, max_model_len, row_ks=None, ctx_per_row=False,
+                         candidate_blocks=None, cand_block=0, num_ctas=0, stream=None):
+    """Paged logits.  q [B*next_n,H,D|D/2] bytes; kv_pages uint8 [num_pages, page_stride];
+    block_table int32 [B, >= ceil(max_model_len/page_size)]; logits fp32
+    [B*next_n, >= max_model_len]."""
+    q = _u8(q)
+    rows, H = q.shape[0], q.shape[1]
+    D = q.shape[2] if fmt == FMT_FP8 else 2 * q.shape[2]
+    B = rows // next_n
+    _need(weights, torch.float32, "weights")
+    _need(block_table, torch.int32, "block_table")
+    _need(context_lens, torch.int32, "context_lens")
+    if kv_pages.dtype != torch.uint8 or kv_pages.dim() != 2 or kv_pages.stride(1) != 1:
+        raise ValueError("kv_pages must be uint8 [num_pages, page_stride] with unit byte stride")
+    cand_stride, num_cand = 0, 0
+    if candidate_blocks is not None:
+        _need(candidate_blocks, torch.int32, "candidate_blocks")
+        cand_stride, num_cand = candidate_blocks.stride(0), candidate_blocks.shape[1]
+    rc = lib().idx_paged_mqa_logits(
+        _ptr(q), _ptr(q_scale), _ptr(weights), _ptr(kv_pages), kv_pages.stride(0),
+        kv_pages.shape[0], _ptr(block_table), block_table.stride(0), _ptr(context_lens),
+        int(ctx_per_row), _ptr(row_ks), B, next_n, H, D, page_size, fmt,
+        _ptr(candidate_blocks), cand_stride, num_cand, cand_block, _ptr(logits),
+        logits.stride(0), max_model_len, num_ctas, None, 0, _stream(stream))
+    _check(rc, "idx_paged_mqa_logits")
+
+
+def idx_apply_candidate_mask(logits, row_ks, row_ke, candidate_blocks, block_size,
+                             row_repeat=1, width=None, stream=None):
+    rows = logits.shape[0]
+    width = logits.shape[1] if width is None else width
+    _need(row_ke, torch.int32, "row_ke")
+    _need(candidate_blocks, torch.int32, "candidate_blocks")
+    rc = lib().idx_apply_candidate_mask(_ptr(logits), logits.stride(0), rows, width,
+                                        _ptr(row_ks), _ptr(row_ke), _ptr(candidate_blocks),
+                                        candidate_blocks.stride(0), candidate_blocks.shape[1],
+                                        block_size, row_repeat, _stream(stream))
+    _check(rc, "idx_apply_candidate_mask")
+
+
+def idx_topk(logits, lengths, k, out, stream=None):
+    """out int32 [rows, >= k]: ascending indices of the k largest finite logits
+    of each row within [0, lengths[r]), -1 padded."""
+    if logits.dtype != torch.float32 or logits.stride(1) != 1:
+        raise ValueError("logits must be float32 with unit column stride")
+    _need(lengths, torch.int32, "lengths")
+    if out.dtype != torch.int32 or out.stride(1) != 1:
+        raise ValueError("out must be int32 with unit column stride")
+    rc = lib().idx_topk(_ptr(logits), logits.stride(0), logits.shape[0], _ptr(lengths), k,
+                        _ptr(out), out.stride(0), None, 0, _stream(stream))
+    _check(rc, "idx_topk")
+
+
+def idx_topk_to_ragged_slots(topk, block_table, page_size, num_pages, slots, indptr, lens,
+                             next_n=1, row_to_seq=None, max_blocks=None, stream=None):
+    if topk.dtype != torch.int32 or topk.stride(1) != 1:
+        raise ValueError("topk must be int32 with unit column stride")
+    _need(block_table, torch.int32, "block_table")
+    rows, k = topk.shape
+    mb = block_table.shape[1] if max_blocks is None else max_blocks
+    rc = lib().idx_topk_to_ragged_slots(_ptr(topk), topk.stride(0), rows, k, _ptr(row_to_seq),
+                                        next_n, _ptr(block_table), block_table.stride(0), mb,
+                                        page_size, num_pages, _ptr(slots), _ptr(indptr),
+                                        _ptr(lens), _stream(stream))
+    _check(rc, "idx_topk_to_ragged_slots")
+
+
+def idx_get_device_status(stream=None) -> int:
+    v = ctypes.c_uint32(0)
+    rc = lib().idx_get_device_status(_stream(stream), ctypes.byref(v))
+    _check(rc, "idx_get_device_status")
+    return int(v.value)

@@ -1,0 +1,369 @@
+// idx_api.cu -- C ABI entry points of the logits kernels, argument checks,
+// TMA descriptor encoding and the device status word.
+#include <cstdio>
+#include <cudaTypedefs.h>
+#include <mutex>
+
+#include "idx_internal.h"
+#include "idx_logits_kernel.cuh"
+
+namespace idx {
+
+__device__ unsigned int g_idx_status;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+int current_device()
+{
+    int dev = 0;
+    cudaGetDevice(&dev);
+    return dev;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tma_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+} // namespace
+
+unsigned int *device_status_ptr()
+{
+    static unsigned int *ptrs[kMaxDevices] = {};
+    static std::mutex mu;
+    int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices)
+        return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ptrs[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_idx_status) != cudaSuccess)
+            return nullptr;
+        ptrs[dev] = static_cast<unsigned int *>(p);
+    }
+    return ptrs[dev];
+}
+
+int sm_count()
+{
+    static int counts[kMaxDevices] = {};
+    int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices)
+        return 1;
+    if (counts[dev] == 0) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        counts[dev] = n > 0 ? n : 1;
+    }
+    return counts[dev];
+}
+
+bool encode_tma_u8(CUtensorMap *map, int rank, const void *base, const uint64_t *dims,
+                   const uint64_t *strides_bytes, const uint32_t *box, CUtensorMapSwizzle swz)
+{
+    auto fn = tma_encoder();
+    if (!fn)
+        return false;
+    cuuint64_t gdim[5], gstr[4];
+    cuuint32_t bdim[5], estr[5];
+    for (int i = 0; i < rank; ++i) {
+        gdim[i] = dims[i];
+        bdim[i] = box[i];
+        estr[i] = 1;
+        if (i + 1 < rank)
+            gstr[i] = strides_bytes[i];
+    }
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, (cuuint32_t)rank, const_cast<void *>(base),
+                    gdim, gstr, bdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+namespace {
+
+template <int FMT, int H, int G, int S, int NA>
+cudaError_t launch_logits_t(const LogitsArgs &a, const CUtensorMap &tmK, const CUtensorMap &tmQ,
+                            int nctas, cudaStream_t stream)
+{
+    using C = LogitsCfg<FMT, H, G, S, NA>;
+    const size_t smem = (size_t)C::fixed_bytes() + (size_t)2 * G * a.cand_words * 4;
+    auto kern = logits_kernel<FMT, H, G, S, NA>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess)
+        return e;
+    kern<<<nctas, kLogitsThreads, smem, stream>>>(a, tmK, tmQ);
+    return cudaGetLastError();
+}
+
+// Shared memory the launch needs; 0 if the combination has no kernel.
+template <int FMT, int H, int G, int S, int NA>
+size_t logits_smem_t(int cand_words)
+{
+    return (size_t)LogitsCfg<FMT, H, G, S, NA>::fixed_bytes() + (size_t)2 * G * cand_words * 4;
+}
+
+constexpr size_t kMaxSmem = 227 * 1024;
+
+// Dispatch on (format, heads, rows per group) to the compiled instantiations.
+cudaError_t launch_logits(int fmt, int H, int G, const LogitsArgs &a, const CUtensorMap &tmK,
+                          const CUtensorMap &tmQ, int nctas, cudaStream_t s, bool *supported)
+{
+    *supported = true;
+    if (H == 64 && fmt == kFmtFp8) {
+        switch (G) {
+        case 1: return launch_logits_t<kFmtFp8, 64, 1, 8, 2>(a, tmK, tmQ, nctas, s);
+        case 2: return launch_logits_t<kFmtFp8, 64, 2, 8, 2>(a, tmK, tmQ, nctas, s);
+        case 4: return launch_logits_t<kFmtFp8, 64, 4, 6, 2>(a, tmK, tmQ, nctas, s);
+        }
+    } else if (H == 64 && fmt == kFmtMxfp4) {
+        switch (G) {
+        case 1: return launch_logits_t<kFmtMxfp4, 64, 1, 12, 2>(a, tmK, tmQ, nctas, s);
+        case 2: return launch_logits_t<kFmtMxfp4, 64, 2, 12, 2>(a, tmK, tmQ, nctas, s);
+        }
+    }
+    *supported = false;
+    return cudaSuccess;
+}
+
+size_t logits_smem(int fmt, int H, int G, int cand_words)
+{
+    if (H == 64 && fmt == kFmtFp8) {
+        switch (G) {
+        case 1: return logits_smem_t<kFmtFp8, 64, 1, 8, 2>(cand_words);
+        case 2: return logits_smem_t<kFmtFp8, 64, 2, 8, 2>(cand_words);
+        case 4: return logits_smem_t<kFmtFp8, 64, 4, 6, 2>(cand_words);
+        }
+    } else if (H == 64 && fmt == kFmtMxfp4) {
+        switch (G) {
+        case 1: return logits_smem_t<kFmtMxfp4, 64, 1, 12, 2>(cand_words);
+        case 2: return logits_smem_t<kFmtMxfp4, 64, 2, 12, 2>(cand_words);
+        }
+    }
+    return 0;
+}
+
+bool valid_fmt(idx_kv_format f)
+{
+    return f == IDX_KV_FP8_E4M3 || f == IDX_KV_MXFP4;
+}
+
+} // namespace
+} // namespace idx
+
+using namespace idx;
+
+extern "C" idx_status idx_mqa_logits(const void *q, const void *q_scale, const float *weights,
+                                     const void *k, const void *k_scale,
+                                     const int32_t *row_ks, const int32_t *row_ke, int M,
+                                     int N, int H, int D, idx_kv_format fmt, float *logits,
+                                     int64_t ld_logits, void *ws, size_t ws_bytes,
+                                     idx_stream_t stream)
+{
+    (void)ws;
+    (void)ws_bytes;
+    if (M < 0 || N < 0 || H <= 0 || D <= 0 || !valid_fmt(fmt))
+        return IDX_ERR_INVALID_ARG;
+    if (M == 0 || N == 0)
+        return IDX_OK;
+    if (!q || !weights || !k || !k_scale || !row_ks || !row_ke || !logits || ld_logits < N)
+        return IDX_ERR_INVALID_ARG;
+    const int f = fmt == IDX_KV_FP8_E4M3 ? kFmtFp8 : kFmtMxfp4;
+    if (f == kFmtMxfp4 && !q_scale)
+        return IDX_ERR_INVALID_ARG;
+    if (D != 128 || H != 64)
+        return IDX_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(weights) ||
+        (q_scale && !aligned16(q_scale)) || (f == kFmtMxfp4 && !aligned16(k_scale)))
+        return IDX_ERR_UNSUPPORTED;
+    if (f == kFmtMxfp4 && N % 4 != 0)
+        return IDX_ERR_UNSUPPORTED;
+    const int nsm = sm_count();
+    const int T = (N + kTileKeys - 1) / kTileKeys;
+    int G = 1;
+    const int gmax = f == kFmtFp8 ? 4 : 2;
+    for (int g = gmax; g > 1; g >>= 1)
+        if (g <= M && (long long)((M + g - 1) / g) * T >= 2LL * nsm) {
+            G = g;
+            break;
+        }
+    const int rowb = f == kFmtFp8 ? D : D / 2;
+    const CUtensorMapSwizzle swz =
+        f == kFmtFp8 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    CUtensorMap tmK, tmQ;
+    {
+        uint64_t dims[3] = {(uint64_t)rowb, (uint64_t)N, 1};
+        uint64_t str[2] = {(uint64_t)rowb, (uint64_t)rowb * (uint64_t)N};
+        uint32_t box[3] = {(uint32_t)rowb, (uint32_t)kHalfKeys, 1};
+        if (!encode_tma_u8(&tmK, 3, k, dims, str, box, swz))
+            return IDX_ERR_UNSUPPORTED;
+    }
+    {
+        uint64_t dims[2] = {(uint64_t)rowb, (uint64_t)M * H};
+        uint64_t str[1] = {(uint64_t)rowb};
+        uint32_t box[2] = {(uint32_t)rowb, (uint32_t)(G * H)};
+        if (!encode_tma_u8(&tmQ, 2, q, dims, str, box, swz))
+            return IDX_ERR_UNSUPPORTED;
+    }
+    LogitsArgs a = {};
+    a.paged = 0;
+    a.G = G;
+    a.total_rows = M;
+    a.num_groups = (M + G - 1) / G;
+    a.H = H;
+    a.q_scale = f == kFmtFp8 ? static_cast<const float *>(q_scale) : nullptr;
+    a.q_sf = f == kFmtMxfp4 ? static_cast<const uint8_t *>(q_scale) : nullptr;
+    a.weights = weights;
+    a.kv = static_cast<const uint8_t *>(k);
+    a.k_scale = f == kFmtFp8 ? static_cast<const float *>(k_scale) : nullptr;
+    a.k_sf = f == kFmtMxfp4 ? static_cast<const uint8_t *>(k_scale) : nullptr;
+    a.row_ks = row_ks;
+    a.row_ke = row_ke;
+    a.N = N;
+    a.logits = logits;
+    a.ld = ld_logits;
+    a.width = N;
+    a.status = device_status_ptr();
+    if (!a.status)
+        return IDX_ERR_CUDA;
+    const long long units = (long long)a.num_groups * T;
+    const int nctas = (int)(units < nsm ? units : nsm);
+    bool supported = false;
+    cudaError_t e = launch_logits(f, H, G, a, tmK, tmQ, nctas, (cudaStream_t)stream, &supported);
+    if (!supported)
+        return IDX_ERR_UNSUPPORTED;
+    return launch_status(e);
+}
+
+extern "C" idx_status idx_paged_mqa_logits(
+    const void *q, const void *q_scale, const float *weights, const uint8_t *kv_pages,
+    int64_t page_stride_bytes, int num_pages, const int32_t *block_table, int64_t bt_stride,
+    const int32_t *context_lens, int ctx_per_row, const int32_t *row_ks, int B, int next_n,
+    int H, int D, int page_size, idx_kv_format fmt, const int32_t *candidate_blocks,
+    int64_t cand_stride, int num_cand, int cand_block, float *logits, int64_t ld_logits,
+    int max_model_len, int num_ctas, void *ws, size_t ws_bytes, idx_stream_t stream)
+{
+    (void)ws;
+    (void)ws_bytes;
+    if (B < 0 || next_n <= 0 || H <= 0 || D <= 0 || page_size <= 0 || num_pages < 0 ||
+        max_model_len < 0 || num_ctas < 0 || !valid_fmt(fmt))
+        return IDX_ERR_INVALID_ARG;
+    if (B == 0 || max_model_len == 0)
+        return IDX_OK;
+    const int f = fmt == IDX_KV_FP8_E4M3 ? kFmtFp8 : kFmtMxfp4;
+    const int max_blocks = (max_model_len + page_size - 1) / page_size;
+    if (!q || !weights || !kv_pages || !block_table || !context_lens || !logits ||
+        ld_logits < max_model_len || bt_stride < max_blocks || num_pages <= 0)
+        return IDX_ERR_INVALID_ARG;
+    if (f == kFmtMxfp4 && !q_scale)
+        return IDX_ERR_INVALID_ARG;
+    if (candidate_blocks && (num_cand < 0 || cand_block <= 0 || cand_stride < num_cand))
+        return IDX_ERR_INVALID_ARG;
+    const int64_t page_bytes =
+        (int64_t)page_size * (f == kFmtFp8 ? (D + 4) : (D / 2 + D / 32));
+    if (page_stride_bytes < page_bytes)
+        return IDX_ERR_INVALID_ARG;
+    if (D != 128 || H != 64 || page_size % kHalfKeys != 0 || page_stride_bytes % 16 != 0)
+        return IDX_ERR_UNSUPPORTED;
+    const int G = next_n;
+    if (!aligned16(q) || !aligned16(kv_pages) || !aligned16(weights) ||
+        (q_scale && !aligned16(q_scale)))
+        return IDX_ERR_UNSUPPORTED;
+    const int rowb = f == kFmtFp8 ? D : D / 2;
+    const CUtensorMapSwizzle swz =
+        f == kFmtFp8 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    int cand_words = 0;
+    if (candidate_blocks && num_cand > 0) {
+        const int nblk = (max_model_len + cand_block - 1) / cand_block;
+        cand_words = (nblk + 31) / 32;
+    }
+    const size_t smem = logits_smem(f, H, G, cand_words);
+    if (smem == 0 || smem > kMaxSmem)
+        return IDX_ERR_UNSUPPORTED;
+    CUtensorMap tmK, tmQ;
+    {
+        uint64_t dims[3] = {(uint64_t)rowb, (uint64_t)page_size, (uint64_t)num_pages};
+        uint64_t str[2] = {(uint64_t)rowb, (uint64_t)page_stride_bytes};
+        uint32_t box[3] = {(uint32_t)rowb, (uint32_t)kHalfKeys, 1};
+        if (!encode_tma_u8(&tmK, 3, kv_pages, dims, str, box, swz))
+            return IDX_ERR_UNSUPPORTED;
+    }
+    {
+        uint64_t dims[2] = {(uint64_t)rowb, (uint64_t)B * next_n * H};
+        uint64_t str[1] = {(uint64_t)rowb};
+        uint32_t box[2] = {(uint32_t)rowb, (uint32_t)(G * H)};
+        if (!encode_tma_u8(&tmQ, 2, q, dims, str, box, swz))
+            return IDX_ERR_UNSUPPORTED;
+    }
+    LogitsArgs a = {};
+    a.paged = 1;
+    a.G = G;
+    a.total_rows = B * next_n;
+    a.num_groups = B;
+    a.H = H;
+    a.q_scale = f == kFmtFp8 ? static_cast<const float *>(q_scale) : nullptr;
+    a.q_sf = f == kFmtMxfp4 ? static_cast<const uint8_t *>(q_scale) : nullptr;
+    a.weights = weights;
+    a.kv = kv_pages;
+    a.page_stride = page_stride_bytes;
+    a.num_pages = num_pages;
+    a.page_size = page_size;
+    a.scale_off = (int64_t)page_size * rowb;
+    a.bt = block_table;
+    a.bt_stride = bt_stride;
+    a.max_blocks = max_blocks;
+    a.ctx = context_lens;
+    a.ctx_per_row = ctx_per_row ? 1 : 0;
+    a.row_ks = row_ks;
+    a.cand = cand_words ? candidate_blocks : nullptr;
+    a.cand_stride = cand_stride;
+    a.num_cand = num_cand;
+    a.cand_block = cand_block;
+    a.cand_words = cand_words;
+    a.logits = logits;
+    a.ld = ld_logits;
+    a.width = max_model_len;
+    a.status = device_status_ptr();
+    if (!a.status)
+        return IDX_ERR_CUDA;
+    const int nctas = num_ctas > 0 ? num_ctas : sm_count();
+    bool supported = false;
+    cudaError_t e = launch_logits(f, H, G, a, tmK, tmQ, nctas, (cudaStream_t)stream, &supported);
+    if (!supported)
+        return IDX_ERR_UNSUPPORTED;
+    return launch_status(e);
+}
+
+extern "C" idx_status idx_get_device_status(idx_stream_t stream, uint32_t *out)
+{
+    if (!out)
+        return IDX_ERR_INVALID_ARG;
+    unsigned int *p = device_status_ptr();
+    if (!p)
+        return IDX_ERR_CUDA;
+    unsigned int v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, p, sizeof(v), cudaMemcpyDeviceToHost, (cudaStream_t)stream);
+    if (e == cudaSuccess)
+        e = cudaMemsetAsync(p, 0, sizeof(unsigned int), (cudaStream_t)stream);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize((cudaStream_t)stream);
+    *out = v;
+    return launch_status(e);
+}
+
+extern "C" const char *idx_version(void)
+{
+    return "idx 0.1 sm_103a";
+}

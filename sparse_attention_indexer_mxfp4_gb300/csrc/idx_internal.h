@@ -1,0 +1,35 @@
+// idx_internal.h -- host-side helpers shared by the library's translation
+// units (not part of the public ABI).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/idx.h"
+
+namespace idx {
+
+// Device address of the sticky status word of the current device.
+unsigned int *device_status_ptr();
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+// 16-byte alignment check of a device pointer.
+inline bool aligned16(const void *p)
+{
+    return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+// Encode a tiled TMA descriptor of uint8 elements (rank 2 or 3).  Returns
+// false if the driver rejects the arguments.
+bool encode_tma_u8(CUtensorMap *map, int rank, const void *base, const uint64_t *dims,
+                   const uint64_t *strides_bytes, const uint32_t *box, CUtensorMapSwizzle swz);
+
+inline idx_status launch_status(cudaError_t e)
+{
+    return e == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
+}
+
+} // namespace idx

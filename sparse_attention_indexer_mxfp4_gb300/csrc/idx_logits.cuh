@@ -1,0 +1,262 @@
+// idx_logits.cuh -- argument block and work schedule of the logits kernel.
+//
+// Work is cut into units of (row group, 128-key tile).  A row group is the
+// set of query rows that share one key sequence and one MMA: the next_n rows
+// of a sequence for paged decode / MTP, or G consecutive rows of a contiguous
+// prefill chunk.  Each unit is either a "compute" tile (it overlaps the
+// group's live key range: K is loaded and scored on the tensor cores) or a
+// "fill" tile (it lies entirely below the group's first live key or, for the
+// contiguous layout, past its last one, and is only written -inf).
+//
+// The grid is persistent: CTA i takes the contiguous unit range
+// [i*U/G, (i+1)*U/G) of the global unit list (U units, G CTAs).  Ranges may
+// cross group boundaries; logits columns of different units never overlap,
+// so no reduction between CTAs is needed.  This is the flash-decode style
+// context split of the vLLM page rocm_aiter_mla_sparse (_decode_num_splits,
+// rocm_fp8_paged_mqa_logits_triton's N_SPLITS) done as an even split of
+// key tiles over a machine-sized grid.
+#pragma once
+
+#include <cstdint>
+
+namespace idx {
+
+constexpr int kTileKeys = 128;  // keys per tile = MMA M
+constexpr int kHalfKeys = 64;   // keys per TMA box (one page of 64 or part of a larger page)
+
+struct LogitsArgs {
+    int paged;         // 1: K through a block table; 0: one contiguous K sequence
+    int num_groups;    // paged: B; contiguous: ceil(M / G)
+    int G;             // rows per group (paged: next_n)
+    int total_rows;    // M (contiguous) or B * next_n (paged)
+    int H;
+    // query side
+    const float *q_scale;  // FP8: nullable fp32 [rows, H]
+    const uint8_t *q_sf;   // MXFP4: e8m0 [rows, H, D/32]
+    const float *weights;  // [rows, H]
+    // key side
+    const uint8_t *kv;       // paged: page pool; contiguous: k
+    int64_t page_stride;     // bytes between pages (paged)
+    int num_pages;           // pages in the pool (paged)
+    int page_size;           // tokens per page (paged)
+    int64_t scale_off;       // byte offset of the scale block inside a page
+    const float *k_scale;    // contiguous FP8: fp32 [N]
+    const uint8_t *k_sf;     // contiguous MXFP4: e8m0 [N, D/32]
+    const int32_t *bt;       // [B, bt_stride]
+    int64_t bt_stride;
+    int max_blocks;          // logical pages per sequence (columns of bt in use)
+    // row ranges
+    const int32_t *ctx;      // paged: context lengths
+    int ctx_per_row;
+    const int32_t *row_ks;   // nullable for paged
+    const int32_t *row_ke;   // contiguous only
+    int N;                   // contiguous: number of keys
+    // fused candidate mask (paged; nullable)
+    const int32_t *cand;
+    int64_t cand_stride;
+    int num_cand;
+    int cand_block;
+    int cand_words;          // 32-bit words of one row's candidate bitmap
+    // output
+    float *logits;
+    int64_t ld;
+    int width;               // paged: max_model_len; contiguous: N
+    unsigned int *status;    // device status word (IDX_DEV_* bits)
+};
+
+// Key range [ks, ke) of row r, clamped as the oracle clamps it.
+__device__ __forceinline__ void row_range(const LogitsArgs &a, int r, int &ks, int &ke)
+{
+    if (a.paged) {
+        int e;
+        if (a.ctx_per_row) {
+            e = a.ctx[r];
+        } else {
+            int b = r / a.G, j = r - (r / a.G) * a.G;
+            e = a.ctx[b] - a.G + j + 1;
+        }
+        ke = min(max(e, 0), a.width);
+        ks = a.row_ks ? min(max(a.row_ks[r], 0), ke) : 0;
+    } else {
+        ke = min(max(a.row_ke[r], 0), a.N);
+        ks = min(max(a.row_ks[r], 0), ke);
+    }
+}
+
+struct GroupInfo {
+    int row0, nrows;  // rows [row0, row0 + nrows)
+    int lo, hi;       // union of the rows' live ranges: [min ks, max ke)
+    int tiles;        // units of this group
+};
+
+__device__ __forceinline__ GroupInfo group_info(const LogitsArgs &a, int g)
+{
+    GroupInfo gi;
+    gi.row0 = g * a.G;
+    gi.nrows = min(a.G, a.total_rows - gi.row0);
+    int lo = 0x7fffffff, hi = 0;
+    for (int i = 0; i < gi.nrows; ++i) {
+        int ks, ke;
+        row_range(a, gi.row0 + i, ks, ke);
+        if (ke > ks) {
+            lo = min(lo, ks);
+            hi = max(hi, ke);
+        }
+    }
+    if (hi <= 0)
+        lo = 0;
+    gi.lo = lo;
+    gi.hi = hi;
+    if (a.paged)
+        gi.tiles = (hi + kTileKeys - 1) / kTileKeys;  // columns [0, max ke) are written
+    else
+        gi.tiles = (a.N + kTileKeys - 1) / kTileKeys;  // every column of [0, N) is written
+    return gi;
+}
+
+__device__ __forceinline__ bool tile_is_compute(const GroupInfo &gi, int j)
+{
+    int t0 = j * kTileKeys;
+    return gi.hi > gi.lo && t0 < gi.hi && t0 + kTileKeys > gi.lo;
+}
+
+// Walks this CTA's unit range in order.  Every role of the CTA runs its own
+// copy and sees the same sequence.
+struct UnitWalk {
+    int g, j;          // current group and tile
+    long long left;    // units still to visit (including the current one)
+    GroupInfo gi;
+    bool first_in_group;  // current unit is the first of its group in this range
+};
+
+} // namespace idx
+
+namespace idx {
+
+// Block-wide helpers for the schedule prologue (blockDim.x a multiple of 32).
+__device__ __forceinline__ long long block_sum_ll(long long v, long long *scratch)
+{
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xffffffffu, v, o);
+    int w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0)
+        scratch[w] = v;
+    __syncthreads();
+    long long t = 0;
+    for (int i = 0; i < nw; ++i)
+        t += scratch[i];
+    __syncthreads();
+    return t;
+}
+
+// Inclusive block scan of v; *total gets the block total.
+__device__ __forceinline__ long long block_incl_scan_ll(long long v, long long *scratch,
+                                                        long long *total)
+{
+    int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    for (int o = 1; o < 32; o <<= 1) {
+        long long n = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o)
+            v += n;
+    }
+    __syncthreads();
+    if (lane == 31)
+        scratch[w] = v;
+    __syncthreads();
+    long long off = 0, t = 0;
+    for (int i = 0; i < nw; ++i) {
+        if (i < w)
+            off += scratch[i];
+        t += scratch[i];
+    }
+    __syncthreads();
+    *total = t;
+    return v + off;
+}
+
+// Find this CTA's first unit: returns (g0, j0) and the number of units.
+// scratch: >= blockDim.x/32 + 2 long longs of shared memory.
+__device__ __forceinline__ void locate_units(const LogitsArgs &a, long long *scratch, int &g0,
+                                             int &j0, long long &count)
+{
+    long long total;
+    int T = 0;
+    if (!a.paged) {
+        T = (a.N + kTileKeys - 1) / kTileKeys;
+        total = (long long)a.num_groups * T;
+    } else {
+        long long loc = 0;
+        for (int g = threadIdx.x; g < a.num_groups; g += blockDim.x)
+            loc += group_info(a, g).tiles;
+        total = block_sum_ll(loc, scratch);
+    }
+    long long u0 = total * blockIdx.x / gridDim.x;
+    long long u1 = total * (blockIdx.x + 1) / gridDim.x;
+    count = u1 - u0;
+    if (count <= 0) {
+        g0 = a.num_groups;
+        j0 = 0;
+        count = 0;
+        return;
+    }
+    if (!a.paged) {
+        g0 = (int)(u0 / T);
+        j0 = (int)(u0 - (long long)g0 * T);
+        return;
+    }
+    volatile long long *found = scratch + 32;  // [0] = g0, [1] = j0
+    if (threadIdx.x == 0)
+        found[0] = -1;
+    __syncthreads();
+    long long running = 0;
+    for (int base = 0; base < a.num_groups; base += blockDim.x) {
+        int g = base + threadIdx.x;
+        long long v = g < a.num_groups ? group_info(a, g).tiles : 0;
+        long long chunk;
+        long long incl = block_incl_scan_ll(v, scratch, &chunk);
+        long long start = running + incl - v;
+        if (v > 0 && u0 >= start && u0 < start + v) {
+            found[0] = g;
+            found[1] = u0 - start;
+        }
+        running += chunk;
+        __syncthreads();
+        if (found[0] >= 0)
+            break;
+    }
+    g0 = (int)found[0];
+    j0 = (int)found[1];
+    __syncthreads();
+}
+
+__device__ __forceinline__ void walk_begin(const LogitsArgs &a, UnitWalk &w, int g0, int j0,
+                                           long long count)
+{
+    w.g = g0;
+    w.j = j0;
+    w.left = count;
+    w.first_in_group = true;
+    if (count > 0)
+        w.gi = group_info(a, g0);
+}
+
+__device__ __forceinline__ bool walk_last_in_group(const UnitWalk &w)
+{
+    return w.left == 1 || w.j + 1 >= w.gi.tiles;
+}
+
+__device__ __forceinline__ void walk_next(const LogitsArgs &a, UnitWalk &w)
+{
+    ++w.j;
+    --w.left;
+    w.first_in_group = false;
+    while (w.left > 0 && w.j >= w.gi.tiles) {
+        ++w.g;
+        w.j = 0;
+        w.first_in_group = true;
+        w.gi = group_info(a, w.g);
+    }
+}
+
+} // namespace idx

@@ -1,0 +1,476 @@
+// idx_logits_kernel.cuh -- the warp-specialised tcgen05 logits kernel.
+//
+// One persistent CTA per SM, 6 warps:
+//   warp 0    producer: TMA loads of K tiles (page by page through the block
+//             table) into a ring of shared-memory stages, and of each row
+//             group's Q tile, weights and scales into one of two group slots;
+//   warp 1    MMA issuer: owns the TMEM allocation and issues the tcgen05 MMAs
+//             S[t, (r,h)] = k[t,:] . q[r,h,:] with keys on M (128 lanes) and
+//             the group's (row, head) pairs on N;
+//   warps 2-5 epilogue: thread i of the four warps owns TMEM lane i, i.e. one
+//             key, and reduces  sum_h w[r,h] * relu(scale * S[t,(r,h)])  over the
+//             heads in registers, applies the [ks, ke) and candidate masks and
+//             stores the fp32 logit.  Per-head scores never leave TMEM and
+//             registers.
+// Stages, group slots and accumulators are handed over with mbarriers whose
+// waits are all bounded (mbar_wait), so a broken pipeline ends the kernel
+// with IDX_DEV_TIMEOUT instead of hanging.
+#pragma once
+
+#include "idx_common.cuh"
+#include "idx_logits.cuh"
+
+namespace idx {
+
+constexpr int kFmtFp8 = 0;
+constexpr int kFmtMxfp4 = 1;
+constexpr int kLogitsThreads = 192;
+constexpr int kEpiWarps = 4;
+
+template <int FMT, int H, int G, int S, int NA>
+struct LogitsCfg {
+    static constexpr int NCOLS = G * H;                    // MMA N
+    static constexpr int ROWB = FMT == kFmtFp8 ? 128 : 64;  // value bytes per key / query row
+    static constexpr int A_BYTES = kTileKeys * ROWB;
+    static constexpr int SF_STAGE = FMT == kFmtFp8 ? 0 : 512;  // K scales as loaded
+    static constexpr int SF_ATOM = FMT == kFmtFp8 ? 0 : 512;   // K scales in MMA order
+    static constexpr int STAGE_BYTES = ((A_BYTES + SF_STAGE + SF_ATOM) + 1023) / 1024 * 1024;
+    static constexpr int Q_BYTES = (NCOLS * ROWB + 1023) / 1024 * 1024;
+    static constexpr int W_BYTES = G * H * 4;
+    static constexpr int QS_BYTES = G * H * 4;  // FP8 q_scale or MXFP4 q scale words
+    static constexpr int QATOMS = (NCOLS + 127) / 128;
+    static constexpr int QATOM_BYTES = FMT == kFmtFp8 ? 0 : QATOMS * 512;
+    // shared memory offsets
+    static constexpr int OFF_STAGE = 0;
+    static constexpr int OFF_Q = OFF_STAGE + S * STAGE_BYTES;
+    static constexpr int OFF_W = OFF_Q + 2 * Q_BYTES;
+    static constexpr int OFF_QS = OFF_W + 2 * W_BYTES;
+    static constexpr int OFF_QATOM = OFF_QS + 2 * QS_BYTES;
+    static constexpr int OFF_BAR = (OFF_QATOM + 2 * QATOM_BYTES + 7) / 8 * 8;
+    // full[S], empty[S], acc_full[NA], acc_empty[NA], q_full[2], q_empty[2]
+    static constexpr int NUM_BARS = 2 * S + 2 * NA + 4;
+    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;  // tmem base, abort flag
+    static constexpr int OFF_SCRATCH = (OFF_MISC + 16 + 7) / 8 * 8;  // 40 long longs
+    static constexpr int OFF_BITMAP = OFF_SCRATCH + 40 * 8;
+    static constexpr int fixed_bytes() { return OFF_BITMAP + 1024; }  // + alignment slack
+    // TMEM columns: accumulators, then (MXFP4) scale factors of A per
+    // accumulator and of B per group slot.
+    static constexpr int TM_SFA = NA * NCOLS;
+    static constexpr int TM_SFB = TM_SFA + (FMT == kFmtFp8 ? 0 : NA * 4);
+    static constexpr int TM_USED = TM_SFB + (FMT == kFmtFp8 ? 0 : 2 * QATOMS * 4);
+    static constexpr int TM_COLS = TM_USED <= 32 ? 32 : TM_USED <= 64 ? 64 : TM_USED <= 128 ? 128
+                                 : TM_USED <= 256 ? 256 : 512;
+    static_assert(TM_USED <= 512, "accumulators do not fit in tensor memory");
+    static_assert(NCOLS % 16 == 0 && NCOLS >= 16 && NCOLS <= 256, "MMA N out of range");
+    static_assert(H % 32 == 0, "heads are read from TMEM 32 columns at a time");
+    // instruction descriptor: fp32 accumulate, K-major A and B, M = 128, N = NCOLS
+    __host__ __device__ static constexpr uint32_t idesc_f8()
+    {
+        return (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(NCOLS >> 3) << 17) |
+               ((uint32_t)(kTileKeys >> 4) << 24);
+    }
+    // block-scaled e2m1 x e2m1 with ue8m0 scales; the scale-factor ids select
+    // the byte of each 32-bit scale word the MMA starts from.
+    __host__ __device__ static constexpr uint32_t idesc_mxf4(int sf_id)
+    {
+        return ((uint32_t)sf_id << 4) | (1u << 7) | (1u << 10) |
+               ((uint32_t)(NCOLS >> 3) << 17) | (1u << 23) |
+               ((uint32_t)(kTileKeys >> 4) << 24) | ((uint32_t)sf_id << 29);
+    }
+};
+
+template <int FMT, int H, int G, int S, int NA>
+__global__ void __launch_bounds__(kLogitsThreads, 1)
+    logits_kernel(const __grid_constant__ LogitsArgs a, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmQ)
+{
+    using C = LogitsCfg<FMT, H, G, S, NA>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // swizzled TMA tiles and MMA descriptors assume 1024-byte aligned tiles
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
+    uint64_t *full = bars, *empty = bars + S;
+    uint64_t *acc_full = bars + 2 * S, *acc_empty = acc_full + NA;
+    uint64_t *q_full = acc_empty + NA, *q_empty = q_full + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
+    long long *scratch = reinterpret_cast<long long *>(smem + C::OFF_SCRATCH);
+    uint32_t *bitmap = reinterpret_cast<uint32_t *>(smem + C::OFF_BITMAP);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int i = 0; i < NA; ++i) {
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_empty[i], kEpiWarps);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&q_full[i], 1);
+            mbar_init(&q_empty[i], 1 + kEpiWarps);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmQ);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, C::TM_COLS);
+        tmem_relinquish();
+    }
+    int g0, j0;
+    long long count;
+    locate_units(a, scratch, g0, j0, count);  // contains __syncthreads
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    UnitWalk w;
+    walk_begin(a, w, g0, j0, count);
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        int gq = 0;        // groups started by this CTA
+        long long c = 0;   // compute tiles issued
+        for (; w.left > 0; walk_next(a, w)) {
+            if (w.first_in_group) {
+                const int slot = gq & 1;
+                if (!mbar_wait(&q_empty[slot], ((gq >> 1) & 1) ^ 1, abort_flag, a.status))
+                    break;
+                const int nrows = w.gi.nrows;
+                if (a.cand) {  // candidate bitmap of each row of the group
+                    uint32_t *bm = bitmap + (size_t)slot * G * a.cand_words;
+                    for (int i = lane; i < G * a.cand_words; i += 32)
+                        bm[i] = 0u;
+                    __syncwarp();
+                    const int nbits = a.cand_words * 32;
+                    for (int i = 0; i < nrows; ++i) {
+                        const int32_t *cr = a.cand + (size_t)(w.gi.row0 + i) * a.cand_stride;
+                        for (int e = lane; e < a.num_cand; e += 32) {
+                            int id = cr[e];
+                            if (id >= 0 && id < nbits)
+                                atomicOr(&bm[i * a.cand_words + (id >> 5)], 1u << (id & 31));
+                        }
+                    }
+                    __syncwarp();
+                }
+                if (lane == 0) {
+                    uint32_t bytes = (uint32_t)(C::NCOLS * C::ROWB) + nrows * H * 4;
+                    const bool qs = FMT == kFmtFp8 ? a.q_scale != nullptr : true;
+                    if (qs)
+                        bytes += nrows * H * 4;
+                    mbar_arrive_expect_tx(&q_full[slot], bytes);
+                    tma_load_2d(smem + C::OFF_Q + slot * C::Q_BYTES, &tmQ, &q_full[slot], 0,
+                                w.gi.row0 * H);
+                    bulk_load(smem + C::OFF_W + slot * C::W_BYTES,
+                              a.weights + (size_t)w.gi.row0 * H, nrows * H * 4, &q_full[slot]);
+                    if (qs) {
+                        const void *src = FMT == kFmtFp8
+                                              ? (const void *)(a.q_scale + (size_t)w.gi.row0 * H)
+                                              : (const void *)(a.q_sf + (size_t)w.gi.row0 * H * 4);
+                        bulk_load(smem + C::OFF_QS + slot * C::QS_BYTES, src, nrows * H * 4,
+                                  &q_full[slot]);
+                    }
+                }
+                __syncwarp();
+                ++gq;
+            }
+            if (!tile_is_compute(w.gi, w.j))
+                continue;
+            const int s = (int)(c % S);
+            if (!mbar_wait(&empty[s], (uint32_t)((c / S) & 1) ^ 1, abort_flag, a.status))
+                break;
+            if (lane == 0) {
+                int page[2], row[2];
+                uint32_t bytes = 0;
+                for (int k = 0; k < 2; ++k) {
+                    const int tok = w.j * kTileKeys + k * kHalfKeys;
+                    page[k] = -1;
+                    if (tok >= w.gi.hi || tok + kHalfKeys <= w.gi.lo)
+                        continue;  // no live key of the group in this half
+                    if (a.paged) {
+                        const int lp = tok / a.page_size;
+                        const int pg = a.bt[(size_t)w.g * a.bt_stride + lp];
+                        if (pg < 0 || pg >= a.num_pages) {
+                            atomicOr(a.status, kDevBadPage);
+                            continue;
+                        }
+                        page[k] = pg;
+                        row[k] = tok - lp * a.page_size;
+                    } else {
+                        page[k] = 0;
+                        row[k] = tok;
+                    }
+                    bytes += kHalfKeys * C::ROWB;
+                    if (FMT == kFmtMxfp4)
+                        bytes += a.paged ? 256u : (uint32_t)min(kHalfKeys, a.N - tok) * 4u;
+                }
+                mbar_arrive_expect_tx(&full[s], bytes);
+                uint8_t *st = smem + C::OFF_STAGE + s * C::STAGE_BYTES;
+                for (int k = 0; k < 2; ++k) {
+                    if (page[k] < 0)
+                        continue;
+                    tma_load_3d(st + k * kHalfKeys * C::ROWB, &tmK, &full[s], 0, row[k], page[k]);
+                    if constexpr (FMT == kFmtMxfp4) {
+                        uint8_t *sf = st + C::A_BYTES + k * 256;
+                        if (a.paged) {
+                            const uint8_t *src = a.kv + (size_t)page[k] * a.page_stride +
+                                                 a.scale_off + (size_t)row[k] * 4;
+                            bulk_load(sf, src, 256u, &full[s]);
+                        } else {
+                            const int tok = w.j * kTileKeys + k * kHalfKeys;
+                            bulk_load(sf, a.k_sf + (size_t)tok * 4,
+                                      (uint32_t)min(kHalfKeys, a.N - tok) * 4u, &full[s]);
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            ++c;
+        }
+        // Tail: wait until the MMA has released every stage and the epilogue
+        // every group slot this CTA filled, so no copy or commit is still in
+        // flight when the CTA exits.
+        if (!*abort_flag) {
+            for (long long i = c > S ? c - S : 0; i < c; ++i)
+                if (!mbar_wait(&empty[i % S], (uint32_t)((i / S) & 1), abort_flag, a.status))
+                    break;
+            for (int i = gq > 2 ? gq - 2 : 0; i < gq; ++i)
+                if (!mbar_wait(&q_empty[i & 1], (i >> 1) & 1, abort_flag, a.status))
+                    break;
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        int gq = 0;
+        long long c = 0;
+        int slot = 0;
+        for (; w.left > 0; walk_next(a, w)) {
+            if (w.first_in_group) {
+                slot = gq & 1;
+                if (!mbar_wait(&q_full[slot], (gq >> 1) & 1, abort_flag, a.status))
+                    break;
+                if constexpr (FMT == kFmtMxfp4) {
+                    // q scale words -> 32x16B atoms in MMA order, then into TMEM
+                    const uint32_t *qsw =
+                        reinterpret_cast<const uint32_t *>(smem + C::OFF_QS + slot * C::QS_BYTES);
+                    uint8_t *atom = smem + C::OFF_QATOM + slot * C::QATOM_BYTES;
+                    const int nvalid = w.gi.nrows * H;
+                    for (int at = 0; at < C::QATOMS; ++at) {
+                        uint4 v;
+                        int n0 = at * 128 + lane;
+                        v.x = n0 < nvalid ? qsw[n0] : 0u;
+                        v.y = n0 + 32 < nvalid ? qsw[n0 + 32] : 0u;
+                        v.z = n0 + 64 < nvalid ? qsw[n0 + 64] : 0u;
+                        v.w = n0 + 96 < nvalid ? qsw[n0 + 96] : 0u;
+                        *reinterpret_cast<uint4 *>(atom + at * 512 + lane * 16) = v;
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tc_fence_after();
+                        for (int at = 0; at < C::QATOMS; ++at) {
+                            uint64_t d = make_smem_desc(smem_u32(atom + at * 512), 128, 128,
+                                                        kLayoutNone);
+                            tmem_cp_32x128b_warpx4(tmem_base + C::TM_SFB + (slot * C::QATOMS + at) * 4, d);
+                        }
+                    }
+                    __syncwarp();
+                }
+                ++gq;
+            }
+            if (tile_is_compute(w.gi, w.j)) {
+                const int acc = (int)(c % NA);
+                const int s = (int)(c % S);
+                if (!mbar_wait(&acc_empty[acc], (uint32_t)((c / NA) & 1) ^ 1, abort_flag, a.status))
+                    break;
+                if (!mbar_wait(&full[s], (uint32_t)((c / S) & 1), abort_flag, a.status))
+                    break;
+                uint8_t *st = smem + C::OFF_STAGE + s * C::STAGE_BYTES;
+                if constexpr (FMT == kFmtMxfp4) {
+                    // K scale words (key-major as loaded) -> MMA order atom
+                    const uint32_t *sw = reinterpret_cast<const uint32_t *>(st + C::A_BYTES);
+                    uint4 v;
+                    v.x = sw[lane];
+                    v.y = sw[lane + 32];
+                    v.z = sw[lane + 64];
+                    v.w = sw[lane + 96];
+                    *reinterpret_cast<uint4 *>(st + C::A_BYTES + C::SF_STAGE + lane * 16) = v;
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                if (lane == 0) {
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + acc * C::NCOLS;
+                    const uint32_t a_addr = smem_u32(st);
+                    const uint32_t b_addr = smem_u32(smem + C::OFF_Q + slot * C::Q_BYTES);
+                    if constexpr (FMT == kFmtFp8) {
+                        #pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            uint64_t ad = make_smem_desc(a_addr + kk * 32, 16, 1024, kLayoutSw128);
+                            uint64_t bd = make_smem_desc(b_addr + kk * 32, 16, 1024, kLayoutSw128);
+                            mma_f8f6f4(d_tmem, ad, bd, C::idesc_f8(), kk > 0 ? 1u : 0u);
+                        }
+                    } else {
+                        const uint32_t sfa = tmem_base + C::TM_SFA + acc * 4;
+                        const uint32_t sfb = tmem_base + C::TM_SFB + slot * C::QATOMS * 4;
+                        uint64_t cd = make_smem_desc(smem_u32(st + C::A_BYTES + C::SF_STAGE), 128,
+                                                     128, kLayoutNone);
+                        tmem_cp_32x128b_warpx4(sfa, cd);
+                        #pragma unroll
+                        for (int kk = 0; kk < 2; ++kk) {
+                            uint64_t ad = make_smem_desc(a_addr + kk * 32, 16, 512, kLayoutSw64);
+                            uint64_t bd = make_smem_desc(b_addr + kk * 32, 16, 512, kLayoutSw64);
+                            mma_mxf4(d_tmem, ad, bd, C::idesc_mxf4(2 * kk), sfa, sfb,
+                                     kk > 0 ? 1u : 0u);
+                        }
+                    }
+                    mma_commit(&empty[s]);
+                    mma_commit(&acc_full[acc]);
+                }
+                __syncwarp();
+                ++c;
+            }
+            if (walk_last_in_group(w)) {
+                if (lane == 0)
+                    mma_commit(&q_empty[slot]);
+                __syncwarp();
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int quad = warp & 3;            // TMEM lane quadrant of this warp
+        const int key_in_tile = quad * 32 + lane;
+        int gq = 0;
+        long long c = 0;
+        int slot = 0;
+        int rks[G], rke[G];
+        for (; w.left > 0; walk_next(a, w)) {
+            if (w.first_in_group) {
+                slot = gq & 1;
+                for (int i = 0; i < G; ++i) {
+                    rks[i] = 0;
+                    rke[i] = 0;
+                    if (i < w.gi.nrows)
+                        row_range(a, w.gi.row0 + i, rks[i], rke[i]);
+                }
+                if (!mbar_wait(&q_full[slot], (gq >> 1) & 1, abort_flag, a.status))
+                    break;
+                ++gq;
+            }
+            const int t = w.j * kTileKeys + key_in_tile;
+            const int wend = a.paged ? w.gi.hi : a.N;  // columns this group writes
+            float val[G];
+            #pragma unroll
+            for (int i = 0; i < G; ++i)
+                val[i] = -INFINITY;
+            if (tile_is_compute(w.gi, w.j)) {
+                // key scale (FP8) and page check, issued before the accumulator wait
+                float ksc = 1.0f;
+                bool live = t < w.gi.hi && t >= w.gi.lo;
+                if (live && a.paged) {
+                    const int lp = t / a.page_size;
+                    const int pg = a.bt[(size_t)w.g * a.bt_stride + lp];
+                    if (pg < 0 || pg >= a.num_pages) {
+                        live = false;
+                    } else if (FMT == kFmtFp8) {
+                        ksc = __ldg(reinterpret_cast<const float *>(
+                            a.kv + (size_t)pg * a.page_stride + a.scale_off +
+                            (size_t)(t - lp * a.page_size) * 4));
+                    }
+                } else if (live && FMT == kFmtFp8) {
+                    ksc = __ldg(a.k_scale + t);
+                }
+                const int acc = (int)(c % NA);
+                if (!mbar_wait(&acc_full[acc], (uint32_t)((c / NA) & 1), abort_flag, a.status))
+                    break;
+                tc_fence_after();
+                const float *wsm = reinterpret_cast<const float *>(smem + C::OFF_W + slot * C::W_BYTES);
+                const float *qsm = reinterpret_cast<const float *>(smem + C::OFF_QS + slot * C::QS_BYTES);
+                const bool use_qs = FMT == kFmtFp8 && a.q_scale != nullptr;
+                // relu(ksc * x) = |ksc| * relu(sgn * x); the common all-positive
+                // case skips the sign multiply.  Branches stay warp-uniform so
+                // the warp is converged at every tcgen05.ld.
+                const bool all_pos = __all_sync(0xffffffffu, ksc >= 0.0f);
+                const float sgn = ksc >= 0.0f ? 1.0f : -1.0f;
+                const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * C::NCOLS;
+                #pragma unroll
+                for (int i = 0; i < G; ++i) {
+                    if (i >= w.gi.nrows)
+                        break;
+                    float sum = 0.0f;
+                    #pragma unroll
+                    for (int hc = 0; hc < H / 32; ++hc) {
+                        uint32_t r[32];
+                        tmem_ld_32x32b_x32(tbase + i * H + hc * 32, r);
+                        tmem_ld_wait();
+                        const float *wr = wsm + i * H + hc * 32;
+                        if (use_qs) {
+                            const float *qr = qsm + i * H + hc * 32;
+                            #pragma unroll
+                            for (int h = 0; h < 32; ++h)
+                                sum = fmaf(wr[h], fmaxf(ksc * qr[h] * __uint_as_float(r[h]), 0.0f), sum);
+                        } else if (all_pos) {
+                            #pragma unroll
+                            for (int h = 0; h < 32; ++h)
+                                sum = fmaf(wr[h], fmaxf(__uint_as_float(r[h]), 0.0f), sum);
+                        } else {
+                            #pragma unroll
+                            for (int h = 0; h < 32; ++h)
+                                sum = fmaf(wr[h], fmaxf(sgn * __uint_as_float(r[h]), 0.0f), sum);
+                        }
+                    }
+                    val[i] = use_qs ? sum : fabsf(ksc) * sum;
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&acc_empty[acc]);
+                ++c;
+                // masks
+                #pragma unroll
+                for (int i = 0; i < G; ++i) {
+                    bool keep = live && t >= rks[i] && t < rke[i];
+                    if (keep && a.cand) {
+                        const uint32_t *bm = bitmap + ((size_t)slot * G + i) * a.cand_words;
+                        const int blk = (t - rks[i]) / a.cand_block;
+                        keep = blk < a.cand_words * 32 && ((bm[blk >> 5] >> (blk & 31)) & 1u);
+                    }
+                    if (!keep)
+                        val[i] = -INFINITY;
+                }
+            }
+            if (t < wend) {
+                #pragma unroll
+                for (int i = 0; i < G; ++i) {
+                    if (i >= w.gi.nrows)
+                        break;
+                    const int end = a.paged ? rke[i] : a.N;
+                    if (t < end)
+                        a.logits[(size_t)(w.gi.row0 + i) * a.ld + t] = val[i];
+                }
+            }
+            if (walk_last_in_group(w)) {
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&q_empty[slot]);
+            }
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::TM_COLS);
+    }
+}
+
+} // namespace idx

@@ -1,0 +1,102 @@
+"""One indexer step over resident device buffers: logits (with the range and,
+when given, the candidate mask fused in), per-row top-k, and for paged
+caches the top-k -> ragged slot map.  Every stage is a libidx.so call."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import _binding as B
+from .synth import ContiguousCase, PagedCase
+
+
+def _dev(a, device, dtype=None):
+    if a is None:
+        return None
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dtype is not None:
+        t = t.to(dtype)
+    return t.to(device)
+
+
+class IndexerStep:
+    """Device-resident inputs and outputs of one workload and the calls of one
+    step.  ``fused_mask=False`` applies the candidate mask with the standalone
+    kernel after the logits instead of inside them."""
+
+    def __init__(self, case, device="cuda", fused_mask: bool = True, num_ctas: int = 0):
+        self.case = case
+        self.device = torch.device(device)
+        self.fused_mask = fused_mask
+        self.num_ctas = num_ctas
+        d = self.device
+        self.paged = isinstance(case, PagedCase)
+        self.q = _dev(case.q, d)
+        self.weights = _dev(case.weights, d)
+        self.q_scale = _dev(case.q_scale, d)
+        if self.paged:
+            self.pages = _dev(case.pages, d)
+            self.block_table = _dev(case.block_table, d)
+            self.context_lens = _dev(case.context_lens, d)
+            self.row_ks = _dev(case.row_ks, d)
+            self.cand = _dev(case.cand, d)
+            ke = np.clip(case.row_ends(), 0, case.width).astype(np.int32)
+            self.lengths = _dev(ke, d)
+            self.rows, self.width = case.rows, case.width
+            self.max_blocks = case.max_blocks
+        else:
+            self.k = _dev(case.k, d)
+            self.k_scale = _dev(case.k_scale, d)
+            self.ks = _dev(case.ks, d)
+            self.ke = _dev(case.ke, d)
+            self.lengths = self.ke
+            self.rows, self.width = case.M, case.N
+        self.k_top = case.topk
+        self.logits = torch.empty((self.rows, self.width), dtype=torch.float32, device=d)
+        self.topk = torch.empty((self.rows, self.k_top), dtype=torch.int32, device=d)
+        if self.paged:
+            self.slots = torch.empty(max(1, self.rows * self.k_top), dtype=torch.int32, device=d)
+            self.indptr = torch.empty(self.rows + 1, dtype=torch.int32, device=d)
+            self.lens = torch.empty(self.rows, dtype=torch.int32, device=d)
+
+    # -------------------------------------------------------------- stages
+    def logits_stage(self, stream=None):
+        c = self.case
+        if self.paged:
+            cand = self.cand if (self.cand is not None and self.fused_mask) else None
+            B.idx_paged_mqa_logits(self.q, self.q_scale, self.weights, self.pages,
+                                   self.block_table, self.context_lens, c.next_n, c.page_size,
+                                   c.fmt, self.logits, c.width, row_ks=self.row_ks,
+                                   ctx_per_row=c.ctx_per_row, candidate_blocks=cand,
+                                   cand_block=c.cand_block, num_ctas=self.num_ctas,
+                                   stream=stream)
+            if self.cand is not None and not self.fused_mask:
+                B.idx_apply_candidate_mask(self.logits, self.row_ks, self.lengths, self.cand,
+                                           c.cand_block, stream=stream)
+        else:
+            B.idx_mqa_logits(self.q, self.q_scale, self.weights, self.k, self.k_scale, self.ks,
+                             self.ke, c.fmt, self.logits, stream=stream)
+
+    def topk_stage(self, stream=None):
+        B.idx_topk(self.logits, self.lengths, self.k_top, self.topk, stream=stream)
+
+    def slots_stage(self, stream=None):
+        if self.paged:
+            B.idx_topk_to_ragged_slots(self.topk, self.block_table, self.case.page_size,
+                                       self.case.num_pages, self.slots, self.indptr, self.lens,
+                                       next_n=self.case.next_n, max_blocks=self.max_blocks,
+                                       stream=stream)
+
+    def run(self, stream=None):
+        self.logits_stage(stream)
+        self.topk_stage(stream)
+        self.slots_stage(stream)
+
+    @property
+    def launches_per_step(self) -> int:
+        n = 1 + 1  # logits, top-k
+        if self.paged:
+            n += 3  # slot count, indptr scan, slot write
+            if self.case.cand is not None and not self.fused_mask:
+                n += 1
+        return n

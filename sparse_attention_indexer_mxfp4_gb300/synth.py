@@ -48,25 +48,24 @@ def e4m3_bytes(x: np.ndarray) -> np.ndarray:
 def mx_quantize(x: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
     """MXFP4-quantise the last axis of ``x`` (a multiple of 32).
 
-    Returns (packed e2m1 bytes [..., D/2], e8m0 scale bytes [..., D/32])."""
-    x = np.asarray(x, dtype=np.float32)
-    D = x.shape[-1]
+    Returns (packed e2m1 bytes [..., D/2], e8m0 scale bytes [..., D/32]).
+    Runs on torch CPU ops (multi-threaded); fp64 where a rounding could bite."""
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    D = t.shape[-1]
     assert D % 32 == 0
-    blocks = x.reshape(x.shape[:-1] + (D // 32, 32))
-    amax = np.max(np.abs(blocks), axis=-1)
-    amax = np.maximum(amax, np.float32(2.0 ** -126))
-    e = np.ceil(np.log2(amax.astype(np.float64) / 6.0)) + 127.0
-    e = np.clip(e, 0, 254).astype(np.int32)
-    scaled = blocks.astype(np.float64) * np.exp2(127.0 - e)[..., None]
-    a = np.abs(scaled).astype(np.float32)
-    code = np.searchsorted(_E2M1_MID, a, side="left").astype(np.int32)
-    code = np.minimum(code, 7)
-    mid_hit = (code < 7) & (a == _E2M1_MID[np.minimum(code, 6)]) & (code % 2 == 1)
-    code = code + mid_hit.astype(np.int32)
-    nib = (code | ((scaled < 0) & (code > 0)).astype(np.int32) << 3).astype(np.uint8)
-    nib = nib.reshape(x.shape)
-    packed = (nib[..., 0::2] | (nib[..., 1::2] << 4)).astype(np.uint8)
-    return packed, e.astype(np.uint8)
+    blocks = t.reshape(*t.shape[:-1], D // 32, 32)
+    amax = blocks.abs().amax(dim=-1).clamp_min(2.0 ** -126).double()
+    e = (torch.ceil(torch.log2(amax / 6.0)) + 127.0).clamp(0, 254)
+    scaled = blocks.double() * torch.exp2(127.0 - e).unsqueeze(-1)
+    a = scaled.abs()
+    mids = torch.from_numpy(_E2M1_MID.astype(np.float64))
+    code = torch.bucketize(a, mids, right=False).clamp_max(7)
+    hit = (code < 7) & (a == mids[code.clamp_max(6)]) & (code % 2 == 1)
+    code = code + hit.to(code.dtype)
+    neg = (scaled < 0) & (code > 0)
+    nib = (code | (neg.to(code.dtype) << 3)).to(torch.uint8).reshape(t.shape)
+    packed = nib[..., 0::2] | (nib[..., 1::2] << 4)
+    return packed.contiguous().numpy(), e.to(torch.uint8).numpy()
 
 
 def _normal(rng: np.random.Generator, shape) -> np.ndarray:

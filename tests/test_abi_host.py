@@ -1,0 +1,96 @@
+"""CPU-side checks of the C ABI: the library builds, loads and exports every
+entry point include/idx.h declares, and host-side argument checks reject bad
+calls before anything reaches a GPU (only arguments that fail those checks
+are passed here, so no device memory is touched)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from sparse_attention_indexer_mxfp4_gb300 import _binding as B
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "idx.h")
+INVALID, UNSUPPORTED = 1, 2
+FAKE = 0x10000  # never dereferenced: every call below fails its host checks first
+
+
+def _declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:idx_status|const char \*)\s*(idx_\w+)\(", text, re.M)))
+
+
+def test_header_declares_the_five_operations():
+    names = _declared()
+    for n in ["idx_mqa_logits", "idx_paged_mqa_logits", "idx_apply_candidate_mask", "idx_topk",
+              "idx_topk_to_ragged_slots", "idx_get_device_status", "idx_version"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    L = B.lib()
+    for name in _declared():
+        assert hasattr(L, name), name
+    assert B.version().startswith("idx")
+
+
+def test_mqa_logits_argument_checks():
+    L = B.lib()
+    f = L.idx_mqa_logits
+    ok = dict(q=FAKE, qs=None, w=FAKE, k=FAKE, ks=FAKE, rks=FAKE, rke=FAKE, M=4, N=8, H=64,
+              D=128, fmt=0, lg=FAKE, ld=8)
+
+    def call(**kw):
+        a = {**ok, **kw}
+        return f(a["q"], a["qs"], a["w"], a["k"], a["ks"], a["rks"], a["rke"], a["M"], a["N"],
+                 a["H"], a["D"], a["fmt"], a["lg"], a["ld"], None, 0, None)
+    assert call(M=-1) == INVALID
+    assert call(fmt=7) == INVALID
+    assert call(q=None) == INVALID
+    assert call(ld=7) == INVALID
+    assert call(fmt=1) == INVALID          # MXFP4 needs q_scale
+    assert call(D=96) == UNSUPPORTED
+    assert call(H=48) == UNSUPPORTED
+    assert call(k=FAKE + 4) == UNSUPPORTED  # TMA base must be 16-byte aligned
+    assert call(M=0) == 0 and call(N=0) == 0
+
+
+def test_paged_argument_checks():
+    f = B.lib().idx_paged_mqa_logits
+    base = [FAKE, None, FAKE, FAKE, 8448, 10, FAKE, 1024, FAKE, 0, None, 2, 1, 64, 128, 64, 0,
+            None, 0, 0, 0, FAKE, 65536, 65536, 0, None, 0, None]
+
+    def call(**kw):
+        a = list(base)
+        idx = dict(stride=4, npages=5, bt_stride=7, B=11, next_n=12, H=13, D=14, P=15, fmt=16,
+                   cand=17, cand_stride=18, num_cand=19, cand_block=20, ld=22, mml=23)
+        for k, v in kw.items():
+            a[idx[k]] = v
+        return f(*a)
+    assert call(next_n=0) == INVALID
+    assert call(bt_stride=10) == INVALID        # fewer columns than max_model_len / P
+    assert call(stride=8000) == INVALID         # page smaller than P * (D + 4)
+    assert call(ld=100) == INVALID
+    assert call(cand=FAKE, num_cand=4, cand_stride=4, cand_block=0) == INVALID
+    assert call(P=96, bt_stride=700, stride=96 * 132) == UNSUPPORTED
+    assert call(next_n=5) == UNSUPPORTED        # next_n * H > 256
+    assert call(stride=8456) == UNSUPPORTED     # page stride not a multiple of 16
+    assert call(B=0) == 0
+
+
+def test_select_argument_checks():
+    L = B.lib()
+    assert L.idx_topk(FAKE, 100, 2, FAKE, 10, FAKE, 5, None, 0, None) == INVALID  # ld_out < k
+    assert L.idx_topk(FAKE, 100, -1, FAKE, 10, FAKE, 10, None, 0, None) == INVALID
+    assert L.idx_topk(None, 100, 2, FAKE, 10, FAKE, 10, None, 0, None) == INVALID
+    assert L.idx_topk(FAKE, 100, 0, FAKE, 10, FAKE, 10, None, 0, None) == 0
+    f = L.idx_apply_candidate_mask
+    assert f(FAKE, 10, 2, 20, None, FAKE, FAKE, 4, 4, 8, 1, None) == INVALID  # ld < width
+    assert f(FAKE, 20, 2, 20, None, FAKE, FAKE, 4, 4, 0, 1, None) == INVALID
+    assert f(FAKE, 20, 2, 20, None, FAKE, FAKE, 4, 4, 8, 0, None) == INVALID
+    g = L.idx_topk_to_ragged_slots
+    assert g(FAKE, 4, 2, 8, None, 1, FAKE, 10, 10, 64, 100, FAKE, FAKE, FAKE, None) == INVALID
+    assert g(FAKE, 8, 2, 8, None, 0, FAKE, 10, 10, 64, 100, FAKE, FAKE, FAKE, None) == INVALID
+    assert g(FAKE, 8, 2, 8, None, 1, FAKE, 10, 10, 0, 100, FAKE, FAKE, FAKE, None) == INVALID
+    assert L.idx_get_device_status(None, None) == INVALID

@@ -1,0 +1,98 @@
+"""The five benchmark workloads at full size, in the launch configuration the
+benchmark times (IndexerStep).  The oracle checks sampled rows one by one;
+top-k is checked end to end with the near-tie rule and bit-exactly on the
+oracle's own logits."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sparse_attention_indexer_mxfp4_gb300 import _binding as B
+from sparse_attention_indexer_mxfp4_gb300 import synth
+from sparse_attention_indexer_mxfp4_gb300.pipeline import IndexerStep
+from parity import assert_logits_close, assert_topk_exact, assert_topk_near_tie
+
+pytestmark = pytest.mark.gpu
+
+
+def _sub_paged(c: synth.PagedCase, seqs):
+    """The same problem restricted to some sequences (rows are independent)."""
+    seqs = np.asarray(seqs)
+    rows = (seqs[:, None] * c.next_n + np.arange(c.next_n)[None, :]).reshape(-1)
+    ctx = c.context_lens[rows] if c.ctx_per_row else c.context_lens[seqs]
+    sub = synth.PagedCase(c.fmt, len(seqs), c.next_n, c.H, c.D, c.page_size, c.num_pages,
+                          c.page_stride, c.width, c.q[rows],
+                          None if c.q_scale is None else c.q_scale[rows], c.weights[rows],
+                          c.pages, c.block_table[seqs], ctx, c.ctx_per_row, c.topk,
+                          None if c.row_ks is None else c.row_ks[rows],
+                          None if c.cand is None else c.cand[rows], c.cand_block)
+    return sub, rows
+
+
+def _oracle_paged_rows(sub):
+    out, bad = oracle.paged_mqa_logits(sub.fmt, sub.q, sub.q_scale, sub.weights, sub.pages,
+                                       sub.page_stride, sub.num_pages, sub.block_table,
+                                       sub.context_lens, sub.ctx_per_row, sub.row_ks, sub.B,
+                                       sub.next_n, sub.H, sub.D, sub.page_size, sub.width)
+    ke = np.clip(sub.row_ends(), 0, sub.width).astype(np.int32)
+    if sub.cand is not None:
+        oracle.apply_candidate_mask(out, sub.row_ks, ke, sub.cand, sub.cand_block)
+    return out, ke, bad
+
+
+@pytest.fixture(scope="module", params=[3, 4, 5])
+def paged_cfg(request):
+    return request.param, synth.CONFIGS[request.param]()
+
+
+def test_paged_config(paged_cfg):
+    cfg, c = paged_cfg
+    st = IndexerStep(c)
+    st.run()
+    torch.cuda.synchronize()
+    assert B.idx_get_device_status() == 0
+    seqs = [0, c.B // 2, c.B - 1]
+    sub, rows = _sub_paged(c, seqs)
+    ref, ke, bad = _oracle_paged_rows(sub)
+    assert bad == 0
+    gl = st.logits[torch.from_numpy(rows).cuda()].cpu().numpy()
+    for i in range(len(rows)):
+        assert_logits_close(gl[i, :ke[i]], ref[i, :ke[i]], f"config {cfg} row {rows[i]}")
+    # top-k: end to end (near-tie rule), then exact on the oracle's logits
+    ora_idx = oracle.topk(np.where(np.isnan(ref), -np.inf, ref), ke, c.topk)
+    gpu_idx = st.topk[torch.from_numpy(rows).cuda()].cpu().numpy()
+    assert_topk_near_tie(gpu_idx, ora_idx, ref, ke, c.topk, f"config {cfg}")
+    ref_dev = torch.from_numpy(np.where(np.isnan(ref), -np.inf, ref).astype(np.float32)).cuda()
+    out = torch.empty((len(rows), c.topk), dtype=torch.int32, device="cuda")
+    B.idx_topk(ref_dev, torch.from_numpy(ke).cuda(), c.topk, out)
+    assert_topk_exact(out.cpu().numpy(), ora_idx, f"config {cfg} top-k on oracle logits")
+    # slots: the ragged rows of the sampled rows are the oracle's slot map of
+    # the same top-k sets
+    indptr = st.indptr.cpu().numpy()
+    slots = st.slots.cpu().numpy()
+    s, ip, ln, _ = oracle.topk_to_ragged_slots(ora_idx, sub.block_table, c.page_size,
+                                               c.num_pages, next_n=c.next_n)
+    for i, r in enumerate(rows):
+        g = np.sort(slots[indptr[r]:indptr[r + 1]])
+        o = np.sort(s[ip[i]:ip[i + 1]])
+        if len(np.setxor1d(gpu_idx[i][gpu_idx[i] >= 0], ora_idx[i][ora_idx[i] >= 0])) == 0:
+            np.testing.assert_array_equal(g, o)
+    assert indptr[0] == 0 and (np.diff(indptr) == st.lens.cpu().numpy()).all()
+
+
+@pytest.mark.parametrize("cfg", [1, 2])
+def test_contiguous_config(cfg):
+    c = synth.CONFIGS[cfg]()
+    st = IndexerStep(c)
+    st.run()
+    torch.cuda.synchronize()
+    rows = np.unique(np.r_[0:3, c.M // 2, c.M - 3:c.M])
+    sub = synth.ContiguousCase(c.fmt, len(rows), c.N, c.H, c.D, c.q[rows], None, c.weights[rows],
+                               c.k, c.k_scale, c.ks[rows], c.ke[rows], c.topk)
+    ref = oracle.mqa_logits(sub.fmt, sub.q, None, sub.weights, sub.k, sub.k_scale, sub.ks,
+                            sub.ke, sub.M, sub.N, sub.H, sub.D)
+    gl = st.logits[torch.from_numpy(rows).cuda()].cpu().numpy()
+    assert_logits_close(gl, ref, f"config {cfg}")
+    ora_idx = oracle.topk(ref, sub.ke, c.topk)
+    gpu_idx = st.topk[torch.from_numpy(rows).cuda()].cpu().numpy()
+    assert_topk_near_tie(gpu_idx, ora_idx, ref, sub.ke, c.topk, f"config {cfg}")

@@ -1,0 +1,160 @@
+"""GPU parity of top-k, the standalone candidate mask and the slot map
+against the oracle, bit-exact, on identical inputs."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sparse_attention_indexer_mxfp4_gb300 import _binding as B
+from parity import assert_topk_exact
+
+pytestmark = pytest.mark.gpu
+
+
+def _t(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def gpu_topk(logits, lengths, k, ld_out=None):
+    rows = logits.shape[0]
+    out = torch.full((rows, ld_out or k), -7, dtype=torch.int32, device="cuda")
+    B.idx_topk(_t(logits), _t(lengths.astype(np.int32)), k, out)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()[:, :k]
+
+
+def _random_logits(rng, rows, width, tie_levels=None, neg_inf_frac=0.1):
+    if tie_levels:
+        x = rng.integers(0, tie_levels, size=(rows, width)).astype(np.float32) - tie_levels / 2
+    else:
+        x = rng.standard_normal((rows, width)).astype(np.float32)
+    x[rng.random((rows, width)) < neg_inf_frac] = -np.inf
+    return x
+
+
+@pytest.mark.parametrize("rows,width,k", [
+    (1, 1, 1), (3, 100, 7), (16, 1024, 256), (5, 1000, 2048), (64, 8192, 2048),
+    (7, 65536, 2048), (2, 131072, 2048), (300, 4096, 256), (33, 20000, 1)])
+def test_topk_random(rows, width, k):
+    rng = np.random.default_rng(rows * 7 + width + k)
+    x = _random_logits(rng, rows, width)
+    lengths = rng.integers(0, width + 1, size=rows)
+    lengths[0] = width
+    got = gpu_topk(x, lengths, k)
+    assert_topk_exact(got, oracle.topk(x, lengths, k))
+
+
+@pytest.mark.parametrize("levels", [1, 2, 5, 300])
+def test_topk_ties_lowest_index_wins(levels):
+    rng = np.random.default_rng(levels)
+    rows, width, k = 6, 50000, 2048
+    x = _random_logits(rng, rows, width, tie_levels=levels, neg_inf_frac=0.05)
+    lengths = np.full(rows, width)
+    lengths[3] = 1000
+    got = gpu_topk(x, lengths, k)
+    assert_topk_exact(got, oracle.topk(x, lengths, k))
+
+
+def test_topk_nonfinite_never_selected():
+    rows, width, k = 4, 3000, 2048
+    x = np.full((rows, width), -np.inf, np.float32)
+    x[0, ::2] = 1.0
+    x[1, 5] = np.nan
+    x[1, 7] = np.inf
+    x[1, 9] = 0.25
+    x[2, :] = np.nan
+    x[3, :] = -0.0
+    x[3, 10] = 0.0
+    lengths = np.full(rows, width)
+    got = gpu_topk(x, lengths, k)
+    assert_topk_exact(got, oracle.topk(x, lengths, k))
+    assert list(got[1, :2]) == [9, -1]
+
+
+def test_topk_extreme_values():
+    rng = np.random.default_rng(5)
+    rows, width, k = 3, 5000, 100
+    x = rng.standard_normal((rows, width)).astype(np.float32) * 1e-38
+    x[1] = np.float32(3.4e38) * np.sign(rng.standard_normal(width)).astype(np.float32)
+    x[2, :] = np.float32(1e-45)
+    lengths = np.full(rows, width)
+    got = gpu_topk(x, lengths, k)
+    assert_topk_exact(got, oracle.topk(x, lengths, k))
+
+
+def test_topk_wide_out_stride():
+    rng = np.random.default_rng(9)
+    x = _random_logits(rng, 5, 777)
+    lengths = np.array([777, 0, 5, 600, 700])
+    got = gpu_topk(x, lengths, 64, ld_out=100)
+    assert_topk_exact(got, oracle.topk(x, lengths, 64))
+
+
+# ------------------------------------------------------------ candidate mask
+
+
+@pytest.mark.parametrize("width,blk,C,repeat", [(1, 1, 1, 1), (1000, 16, 9, 1), (131072, 128, 64, 2),
+                                                (5000, 1, 300, 3), (70000, 64, 40, 1)])
+def test_candidate_mask(width, blk, C, repeat):
+    rng = np.random.default_rng(width + blk)
+    rows = 7
+    crow = -(-rows // repeat)
+    nblk = -(-width // blk)
+    cand = rng.integers(-3, nblk + 4, size=(crow, C)).astype(np.int32)
+    ke = rng.integers(0, width + 1, size=rows).astype(np.int32)
+    ks = np.minimum(rng.integers(0, width + 1, size=rows), ke).astype(np.int32)
+    x = rng.standard_normal((rows, width)).astype(np.float32)
+    ref = oracle.apply_candidate_mask(x.copy(), ks, ke, cand, blk, repeat)
+    g = _t(x)
+    B.idx_apply_candidate_mask(g, _t(ks), _t(ke), _t(cand), blk, row_repeat=repeat)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(g.cpu().numpy(), ref)
+    g = _t(x)
+    B.idx_apply_candidate_mask(g, None, _t(ke), _t(cand), blk, row_repeat=repeat)
+    ref0 = oracle.apply_candidate_mask(x.copy(), None, ke, cand, blk, repeat)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(g.cpu().numpy(), ref0)
+
+
+# ------------------------------------------------------------------ slot map
+
+
+@pytest.mark.parametrize("rows,k,P,next_n", [(1, 1, 64, 1), (6, 50, 16, 2), (256, 2048, 64, 2),
+                                             (1500, 300, 128, 1)])
+def test_slots(rows, k, P, next_n):
+    rng = np.random.default_rng(rows + k)
+    nseq = -(-rows // next_n)
+    num_pages, max_blocks = 5000, 40
+    bt = np.stack([rng.permutation(num_pages)[:max_blocks] for _ in range(nseq)]).astype(np.int32)
+    topk = rng.integers(-1, max_blocks * P, size=(rows, k)).astype(np.int32)
+    topk[rng.random((rows, k)) < 0.3] = -1
+    slots = torch.empty(rows * k, dtype=torch.int32, device="cuda")
+    indptr = torch.empty(rows + 1, dtype=torch.int32, device="cuda")
+    lens = torch.empty(rows, dtype=torch.int32, device="cuda")
+    B.idx_get_device_status()
+    B.idx_topk_to_ragged_slots(_t(topk), _t(bt), P, num_pages, slots, indptr, lens,
+                               next_n=next_n)
+    torch.cuda.synchronize()
+    s, ip, ln, bad = oracle.topk_to_ragged_slots(topk, bt, P, num_pages, next_n=next_n)
+    assert bad == 0 and B.idx_get_device_status() == 0
+    np.testing.assert_array_equal(indptr.cpu().numpy(), ip)
+    np.testing.assert_array_equal(lens.cpu().numpy(), ln)
+    np.testing.assert_array_equal(slots.cpu().numpy()[:ip[-1]], s)
+
+
+def test_slots_row_to_seq_and_invalid_pages():
+    P, num_pages = 4, 4
+    bt = np.array([[3, 1, -1], [0, 2, 9]], np.int32)
+    topk = np.array([[0, 5, 9, -1], [11, 4, -1, 8]], np.int32)
+    r2s = np.array([1, 0], np.int32)
+    slots = torch.empty(8, dtype=torch.int32, device="cuda")
+    indptr = torch.empty(3, dtype=torch.int32, device="cuda")
+    lens = torch.empty(2, dtype=torch.int32, device="cuda")
+    B.idx_get_device_status()
+    B.idx_topk_to_ragged_slots(_t(topk), _t(bt), P, num_pages, slots, indptr, lens,
+                               row_to_seq=_t(r2s))
+    torch.cuda.synchronize()
+    s, ip, ln, bad = oracle.topk_to_ragged_slots(topk, bt, P, num_pages, row_to_seq=r2s)
+    assert bad == 3 and B.idx_get_device_status() & B.DEV_BAD_PAGE
+    np.testing.assert_array_equal(indptr.cpu().numpy(), ip)
+    np.testing.assert_array_equal(slots.cpu().numpy()[:ip[-1]], s)
