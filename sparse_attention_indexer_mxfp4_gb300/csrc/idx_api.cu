@@ -219,6 +219,8 @@ extern "C" idx_status idx_mqa_logits(const void *q, const void *q_scale, const f
     }
     LogitsArgs a = {};
     a.paged = 0;
+    a.page_shift = -1;
+    a.page_size = 1;
     a.G = G;
     a.total_rows = M;
     a.num_groups = (M + G - 1) / G;
@@ -320,6 +322,11 @@ extern "C" idx_status idx_paged_mqa_logits(
     a.page_stride = page_stride_bytes;
     a.num_pages = num_pages;
     a.page_size = page_size;
+    a.page_shift = -1;
+    if ((page_size & (page_size - 1)) == 0)
+        for (int b = 0; b < 31; ++b)
+            if ((1 << b) == page_size)
+                a.page_shift = b;
     a.scale_off = (int64_t)page_size * rowb;
     a.bt = block_table;
     a.bt_stride = bt_stride;

@@ -69,11 +69,10 @@ IDX_DEVFN bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 // nanoseconds or as soon as *abort is set by another role.  On give-up sets
 // *abort and the timeout bit of the device status word *status and returns false.  Every pipeline wait
 // goes through here, so no wait can spin forever.
-IDX_DEVFN bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
-                         unsigned int *status, uint64_t limit_ns = 2000000000ull)
+// Slow path of mbar_wait, kept out of line so every call site stays small.
+__device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                            unsigned int *status, uint64_t limit_ns)
 {
-    if (mbar_try_wait(bar, parity))
-        return true;
     uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity))
@@ -88,6 +87,14 @@ IDX_DEVFN bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
             }
         }
     }
+}
+
+IDX_DEVFN bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
+                         unsigned int *status, uint64_t limit_ns = 2000000000ull)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    return mbar_wait_slow(bar, parity, abort, status, limit_ns);
 }
 
 // -------------------------------------------------------------------- TMA

@@ -39,6 +39,7 @@ struct LogitsArgs {
     int64_t page_stride;     // bytes between pages (paged)
     int num_pages;           // pages in the pool (paged)
     int page_size;           // tokens per page (paged)
+    int page_shift;          // log2(page_size) if a power of two, else -1
     int64_t scale_off;       // byte offset of the scale block inside a page
     const float *k_scale;    // contiguous FP8: fp32 [N]
     const uint8_t *k_sf;     // contiguous MXFP4: e8m0 [N, D/32]
@@ -89,7 +90,10 @@ struct GroupInfo {
     int tiles;        // units of this group
 };
 
-__device__ __forceinline__ GroupInfo group_info(const LogitsArgs &a, int g)
+// Out of line on purpose: it runs once per group and inlining it into every
+// role multiplies the kernel's code size several times over, which starves
+// the instruction cache of the hot loops.
+__device__ __noinline__ GroupInfo group_info(const LogitsArgs &a, int g)
 {
     GroupInfo gi;
     gi.row0 = g * a.G;

@@ -3,7 +3,10 @@
 // One persistent CTA per SM, 6 warps:
 //   warp 0    producer: TMA loads of K tiles (page by page through the block
 //             table) into a ring of shared-memory stages, and of each row
-//             group's Q tile, weights and scales into one of two group slots;
+//             group's Q tile, weights and scales into one of two group slots.
+//             The warp's 32 lanes resolve the pages of 16 tiles at a time
+//             (one half-tile each), one window ahead, so a tile costs only a
+//             barrier wait and two TMA issues;
 //   warp 1    MMA issuer: owns the TMEM allocation and issues the tcgen05 MMAs
 //             S[t, (r,h)] = k[t,:] . q[r,h,:] with keys on M (128 lanes) and
 //             the group's (row, head) pairs on N;
@@ -11,7 +14,8 @@
 //             key, and reduces  sum_h w[r,h] * relu(scale * S[t,(r,h)])  over the
 //             heads in registers, applies the [ks, ke) and candidate masks and
 //             stores the fp32 logit.  Per-head scores never leave TMEM and
-//             registers.
+//             registers.  Each thread fetches its key's scale itself, two
+//             tiles ahead, so the load latency hides behind the work.
 // Stages, group slots and accumulators are handed over with mbarriers whose
 // waits are all bounded (mbar_wait), so a broken pipeline ends the kernel
 // with IDX_DEV_TIMEOUT instead of hanging.
@@ -26,14 +30,16 @@ constexpr int kFmtFp8 = 0;
 constexpr int kFmtMxfp4 = 1;
 constexpr int kLogitsThreads = 192;
 constexpr int kEpiWarps = 4;
+constexpr int kWinTiles = 16;  // tiles whose pages the producer resolves at once (32 halves)
 
 template <int FMT, int H, int G, int S, int NA>
 struct LogitsCfg {
     static constexpr int NCOLS = G * H;                    // MMA N
     static constexpr int ROWB = FMT == kFmtFp8 ? 128 : 64;  // value bytes per key / query row
     static constexpr int A_BYTES = kTileKeys * ROWB;
-    static constexpr int SF_STAGE = FMT == kFmtFp8 ? 0 : 512;  // K scales as loaded
-    static constexpr int SF_ATOM = FMT == kFmtFp8 ? 0 : 512;   // K scales in MMA order
+    // stage: K values | (MXFP4) key scale words as loaded | the same in MMA order
+    static constexpr int SF_STAGE = FMT == kFmtFp8 ? 0 : 512;
+    static constexpr int SF_ATOM = FMT == kFmtFp8 ? 0 : 512;
     static constexpr int STAGE_BYTES = ((A_BYTES + SF_STAGE + SF_ATOM) + 1023) / 1024 * 1024;
     static constexpr int Q_BYTES = (NCOLS * ROWB + 1023) / 1024 * 1024;
     static constexpr int W_BYTES = G * H * 4;
@@ -78,6 +84,80 @@ struct LogitsCfg {
                ((uint32_t)(kTileKeys >> 4) << 24) | ((uint32_t)sf_id << 29);
     }
 };
+
+// Logical page of key position t (shift when the page size is a power of two).
+__device__ __forceinline__ int page_of(const LogitsArgs &a, int t)
+{
+    return a.page_shift >= 0 ? (t >> a.page_shift) : t / a.page_size;
+}
+
+// One lane's half-tile (64 keys) of a producer window: does the group need
+// it, which page and row it starts at.  The block-table load is issued here
+// and only consumed when the window becomes current.
+struct HalfInfo {
+    int page, row;
+    bool need;
+};
+
+__device__ __forceinline__ HalfInfo half_info(const LogitsArgs &a, const GroupInfo &gi, int g,
+                                              int tile0, int lane)
+{
+    HalfInfo h;
+    const int tok = (tile0 * 2 + lane) * kHalfKeys;
+    h.need = tok < gi.hi && tok + kHalfKeys > gi.lo;
+    h.page = 0;
+    h.row = tok;
+    if (a.paged) {
+        const int lp = page_of(a, tok);
+        h.row = tok - lp * a.page_size;
+        h.page = h.need && lp < a.max_blocks ? __ldg(a.bt + (size_t)g * a.bt_stride + lp) : -1;
+    }
+    return h;
+}
+
+// Scale and liveness of one key, fetched ahead of use by the epilogue.
+struct KeyPrefetch {
+    float ksc;
+    bool live;
+};
+
+template <int FMT>
+__device__ __forceinline__ KeyPrefetch key_prefetch(const LogitsArgs &a, const UnitWalk &la,
+                                                    int key_in_tile)
+{
+    KeyPrefetch p;
+    p.ksc = 1.0f;
+    p.live = false;
+    if (la.left <= 0)
+        return p;
+    const int t = la.j * kTileKeys + key_in_tile;
+    if (t >= la.gi.hi || t < la.gi.lo)
+        return p;
+    if (a.paged) {
+        const int lp = page_of(a, t);
+        const int pg = __ldg(a.bt + (size_t)la.g * a.bt_stride + lp);
+        if (pg < 0 || pg >= a.num_pages)
+            return p;
+        if (FMT == kFmtFp8)
+            p.ksc = __ldg(reinterpret_cast<const float *>(a.kv + (size_t)pg * a.page_stride +
+                                                          a.scale_off) +
+                          (t - lp * a.page_size));
+    } else if (FMT == kFmtFp8) {
+        p.ksc = __ldg(a.k_scale + t);
+    }
+    p.live = true;
+    return p;
+}
+
+__device__ __forceinline__ void skip_fill_units(const LogitsArgs &a, UnitWalk &w)
+{
+    while (w.left > 0 && !tile_is_compute(w.gi, w.j))
+        walk_next(a, w);
+}
+
+} // namespace idx
+
+namespace idx {
 
 template <int FMT, int H, int G, int S, int NA>
 __global__ void __launch_bounds__(kLogitsThreads, 1)
@@ -139,6 +219,9 @@ __global__ void __launch_bounds__(kLogitsThreads, 1)
         // ------------------------------------------------------------ producer
         int gq = 0;        // groups started by this CTA
         long long c = 0;   // compute tiles issued
+        int win0 = 0;      // first tile of the current page window
+        HalfInfo cur = {}, nxt = {};
+        bool cur_ok = false;
         for (; w.left > 0; walk_next(a, w)) {
             if (w.first_in_group) {
                 const int slot = gq & 1;
@@ -181,54 +264,64 @@ __global__ void __launch_bounds__(kLogitsThreads, 1)
                 }
                 __syncwarp();
                 ++gq;
+                // page window of this group: current and next, loads in flight
+                win0 = w.j;
+                cur = half_info(a, w.gi, w.g, win0, lane);
+                nxt = half_info(a, w.gi, w.g, win0 + kWinTiles, lane);
+                cur_ok = false;
             }
             if (!tile_is_compute(w.gi, w.j))
                 continue;
+            if (w.j >= win0 + kWinTiles) {  // slide the window (warp-uniform)
+                const int step = (w.j - win0) / kWinTiles;
+                if (step == 1) {
+                    cur = nxt;
+                } else {
+                    cur = half_info(a, w.gi, w.g, win0 + step * kWinTiles, lane);
+                }
+                win0 += step * kWinTiles;
+                nxt = half_info(a, w.gi, w.g, win0 + kWinTiles, lane);
+                cur_ok = false;
+            }
+            if (!cur_ok) {  // first use of this window: resolve validity
+                if (a.paged && cur.need && (cur.page < 0 || cur.page >= a.num_pages)) {
+                    atomicOr(a.status, kDevBadPage);
+                    cur.need = false;
+                }
+                cur_ok = true;
+            }
             const int s = (int)(c % S);
             if (!mbar_wait(&empty[s], (uint32_t)((c / S) & 1) ^ 1, abort_flag, a.status))
                 break;
+            const int h0 = 2 * (w.j - win0);  // lanes h0, h0 + 1 own this tile's halves
+            const uint32_t ball = __ballot_sync(0xffffffffu, cur.need);
+            const uint32_t mine = (ball >> h0) & 3u;
+            uint8_t *st = smem + C::OFF_STAGE + s * C::STAGE_BYTES;
             if (lane == 0) {
-                int page[2], row[2];
-                uint32_t bytes = 0;
-                for (int k = 0; k < 2; ++k) {
-                    const int tok = w.j * kTileKeys + k * kHalfKeys;
-                    page[k] = -1;
-                    if (tok >= w.gi.hi || tok + kHalfKeys <= w.gi.lo)
-                        continue;  // no live key of the group in this half
-                    if (a.paged) {
-                        const int lp = tok / a.page_size;
-                        const int pg = a.bt[(size_t)w.g * a.bt_stride + lp];
-                        if (pg < 0 || pg >= a.num_pages) {
-                            atomicOr(a.status, kDevBadPage);
-                            continue;
+                uint32_t bytes = (uint32_t)__popc(mine) * (kHalfKeys * C::ROWB);
+                if (FMT == kFmtMxfp4) {
+                    for (int k = 0; k < 2; ++k)
+                        if ((mine >> k) & 1u) {
+                            const int tok = w.j * kTileKeys + k * kHalfKeys;
+                            bytes += a.paged ? 256u : (uint32_t)min(kHalfKeys, a.N - tok) * 4u;
                         }
-                        page[k] = pg;
-                        row[k] = tok - lp * a.page_size;
-                    } else {
-                        page[k] = 0;
-                        row[k] = tok;
-                    }
-                    bytes += kHalfKeys * C::ROWB;
-                    if (FMT == kFmtMxfp4)
-                        bytes += a.paged ? 256u : (uint32_t)min(kHalfKeys, a.N - tok) * 4u;
                 }
                 mbar_arrive_expect_tx(&full[s], bytes);
-                uint8_t *st = smem + C::OFF_STAGE + s * C::STAGE_BYTES;
-                for (int k = 0; k < 2; ++k) {
-                    if (page[k] < 0)
-                        continue;
-                    tma_load_3d(st + k * kHalfKeys * C::ROWB, &tmK, &full[s], 0, row[k], page[k]);
-                    if constexpr (FMT == kFmtMxfp4) {
-                        uint8_t *sf = st + C::A_BYTES + k * 256;
-                        if (a.paged) {
-                            const uint8_t *src = a.kv + (size_t)page[k] * a.page_stride +
-                                                 a.scale_off + (size_t)row[k] * 4;
-                            bulk_load(sf, src, 256u, &full[s]);
-                        } else {
-                            const int tok = w.j * kTileKeys + k * kHalfKeys;
-                            bulk_load(sf, a.k_sf + (size_t)tok * 4,
-                                      (uint32_t)min(kHalfKeys, a.N - tok) * 4u, &full[s]);
-                        }
+            }
+            __syncwarp();
+            if ((lane == h0 || lane == h0 + 1) && cur.need) {
+                const int k = lane - h0;
+                tma_load_3d(st + k * kHalfKeys * C::ROWB, &tmK, &full[s], 0, cur.row, cur.page);
+                if (FMT == kFmtMxfp4) {
+                    uint8_t *dst = st + C::A_BYTES + k * 256;
+                    if (a.paged) {
+                        bulk_load(dst, a.kv + (size_t)cur.page * a.page_stride + a.scale_off +
+                                           (size_t)cur.row * 4,
+                                  256u, &full[s]);
+                    } else {
+                        const int tok = cur.row;
+                        bulk_load(dst, a.k_sf + (size_t)tok * 4,
+                                  (uint32_t)min(kHalfKeys, a.N - tok) * 4u, &full[s]);
                     }
                 }
             }
@@ -351,6 +444,19 @@ __global__ void __launch_bounds__(kLogitsThreads, 1)
         long long c = 0;
         int slot = 0;
         int rks[G], rke[G];
+        // key scales and page validity, two compute tiles ahead of use
+        UnitWalk la = w;
+        skip_fill_units(a, la);
+        KeyPrefetch pf0 = key_prefetch<FMT>(a, la, key_in_tile);
+        if (la.left > 0) {
+            walk_next(a, la);
+            skip_fill_units(a, la);
+        }
+        KeyPrefetch pf1 = key_prefetch<FMT>(a, la, key_in_tile);
+        if (la.left > 0) {
+            walk_next(a, la);
+            skip_fill_units(a, la);
+        }
         for (; w.left > 0; walk_next(a, w)) {
             if (w.first_in_group) {
                 slot = gq & 1;
@@ -371,21 +477,13 @@ __global__ void __launch_bounds__(kLogitsThreads, 1)
             for (int i = 0; i < G; ++i)
                 val[i] = -INFINITY;
             if (tile_is_compute(w.gi, w.j)) {
-                // key scale (FP8) and page check, issued before the accumulator wait
-                float ksc = 1.0f;
-                bool live = t < w.gi.hi && t >= w.gi.lo;
-                if (live && a.paged) {
-                    const int lp = t / a.page_size;
-                    const int pg = a.bt[(size_t)w.g * a.bt_stride + lp];
-                    if (pg < 0 || pg >= a.num_pages) {
-                        live = false;
-                    } else if (FMT == kFmtFp8) {
-                        ksc = __ldg(reinterpret_cast<const float *>(
-                            a.kv + (size_t)pg * a.page_stride + a.scale_off +
-                            (size_t)(t - lp * a.page_size) * 4));
-                    }
-                } else if (live && FMT == kFmtFp8) {
-                    ksc = __ldg(a.k_scale + t);
+                const float ksc = pf0.ksc;
+                const bool live = pf0.live;
+                pf0 = pf1;
+                pf1 = key_prefetch<FMT>(a, la, key_in_tile);
+                if (la.left > 0) {
+                    walk_next(a, la);
+                    skip_fill_units(a, la);
                 }
                 const int acc = (int)(c % NA);
                 if (!mbar_wait(&acc_full[acc], (uint32_t)((c / NA) & 1), abort_flag, a.status))

@@ -5,234 +5,12 @@
 #include <cstdint>
 
 #include "idx_internal.h"
+#include "idx_topk.cuh"
 
 namespace cg = cooperative_groups;
 
 namespace idx {
 namespace {
-
-// ------------------------------------------------------------------ top-k
-//
-// Passage: vLLM page rocm_paged_mxfp4_indexer, _topk -- top-k over each
-// row's [0, lengths[row]), -1 padding.  The design is our own: each row is
-// handled by one thread-block cluster of C CTAs.  CTA c of the cluster copies
-// its slice of the row into shared memory once, as order-preserving 32-bit
-// keys (non-finite values become key 0 and are never selected), and the
-// cluster then runs a three-digit (11/11/10 bit) radix select: each CTA
-// histograms its slice for the current digit, the C histograms are summed
-// through distributed shared memory, and every CTA finds the same digit of
-// the k-th largest key.  Finally every CTA writes its selected indices in
-// ascending index order at offsets given by a cluster prefix sum.  Elements
-// equal to the k-th largest key are taken lowest index first, so the
-// selected set is unique.  All waits are hardware cluster barriers that every
-// CTA reaches on the same, data-independent path.
-
-constexpr int kTopkThreads = 512;
-constexpr int kMaxCluster = 8;  // portable cluster size
-constexpr int kTopkWarps = kTopkThreads / 32;
-
-__device__ __forceinline__ uint32_t float_key(float v)
-{
-    uint32_t b = __float_as_uint(v);
-    if (!isfinite(v))
-        return 0u;
-    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-
-// Block-wide exclusive scan of one uint32 per thread; returns the exclusive
-// prefix, *total gets the sum.  Uses wsum[kTopkWarps + 1].
-__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *wsum, uint32_t *total)
-{
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    uint32_t x = v;
-    for (int o = 1; o < 32; o <<= 1) {
-        uint32_t n = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o)
-            x += n;
-    }
-    if (lane == 31)
-        wsum[w] = x;
-    __syncthreads();
-    if (w == 0) {
-        uint32_t s = lane < kTopkWarps ? wsum[lane] : 0u;
-        uint32_t incl = s;
-        for (int o = 1; o < 32; o <<= 1) {
-            uint32_t n = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o)
-                incl += n;
-        }
-        if (lane < kTopkWarps)
-            wsum[lane] = incl - s;
-        if (lane == 31)
-            wsum[kTopkWarps] = incl;
-    }
-    __syncthreads();
-    uint32_t r = wsum[w] + x - v;
-    *total = wsum[kTopkWarps];
-    __syncthreads();
-    return r;
-}
-
-struct TopkShared {
-    uint32_t hist[2][2048];
-    uint32_t wsum[kTopkWarps + 1];
-    uint32_t counts[4];  // valid, greater, equal (this CTA)
-    uint32_t sel[4];     // digit found, remaining k, ...
-};
-
-__global__ void __launch_bounds__(kTopkThreads)
-    topk_cluster_kernel(const float *__restrict__ logits, int64_t ld, int rows,
-                        const int32_t *__restrict__ lengths, int k, int32_t *__restrict__ out,
-                        int64_t ld_out, int slice_cap)
-{
-    cg::cluster_group cluster = cg::this_cluster();
-    const int C = (int)cluster.num_blocks();
-    const int crank = (int)cluster.block_rank();
-    const int row = blockIdx.x / C;
-    extern __shared__ __align__(16) uint8_t dsm[];
-    TopkShared &sh = *reinterpret_cast<TopkShared *>(dsm);
-    uint32_t *keys = reinterpret_cast<uint32_t *>(dsm + sizeof(TopkShared));
-    const int tid = threadIdx.x;
-
-    const bool row_ok = row < rows;  // every CTA of a cluster shares the row
-    int len = row_ok ? lengths[row] : 0;
-    len = max(0, min(len, (int)ld));
-    const int per = (len + C - 1) / C;
-    const int lo = min(len, crank * per);
-    const int hi = min(len, lo + per);
-    const int n = hi - lo;  // <= slice_cap by construction of the launch
-    (void)slice_cap;
-
-    // load the slice as keys, count valid keys, digit-1 histogram
-    for (int i = tid; i < 2 * 2048; i += kTopkThreads)
-        (&sh.hist[0][0])[i] = 0u;
-    __syncthreads();
-    uint32_t nvalid = 0;
-    const float *src = logits + (size_t)(row_ok ? row : 0) * ld + lo;
-    for (int i = tid; i < n; i += kTopkThreads) {
-        uint32_t key = float_key(__ldg(src + i));
-        keys[i] = key;
-        if (key) {
-            ++nvalid;
-            atomicAdd(&sh.hist[0][key >> 21], 1u);
-        }
-    }
-    uint32_t tot;
-    (void)block_excl_scan(nvalid, sh.wsum, &tot);
-    if (tid == 0)
-        sh.counts[0] = tot;
-    cluster.sync();
-    uint32_t total_valid = 0;
-    for (int r = 0; r < C; ++r)
-        total_valid += cluster.map_shared_rank(&sh, r)->counts[0];
-
-    // radix select of the threshold key T and the number of ties to take
-    uint32_t prefix = 0, prefix_mask = 0;
-    uint32_t krem = (uint32_t)k;
-    bool take_all = total_valid <= (uint32_t)k;
-    const int shifts[3] = {21, 10, 0};
-    const int nbins[3] = {2048, 2048, 1024};
-    for (int pass = 0; pass < 3 && !take_all; ++pass) {
-        uint32_t *h = sh.hist[pass & 1];
-        if (pass > 0) {
-            for (int i = tid; i < 2048; i += kTopkThreads)
-                h[i] = 0u;
-            __syncthreads();
-            const uint32_t dmask = (uint32_t)nbins[pass] - 1u;
-            for (int i = tid; i < n; i += kTopkThreads) {
-                uint32_t key = keys[i];
-                if (key && (key & prefix_mask) == prefix)
-                    atomicAdd(&h[(key >> shifts[pass]) & dmask], 1u);
-            }
-            cluster.sync();
-        }
-        // summed histogram; thread t owns 4 bins in descending order
-        const int nb = nbins[pass];
-        uint32_t loc[4];
-        uint32_t lsum = 0;
-        for (int j = 0; j < 4; ++j) {
-            int b = nb - 1 - (tid * 4 + j);
-            uint32_t s = 0;
-            if (b >= 0)
-                for (int r = 0; r < C; ++r)
-                    s += cluster.map_shared_rank(h, r)[b];
-            loc[j] = s;
-            lsum += s;
-        }
-        uint32_t before = block_excl_scan(lsum, sh.wsum, &tot);
-        for (int j = 0; j < 4; ++j) {
-            int b = nb - 1 - (tid * 4 + j);
-            if (b >= 0 && before < krem && before + loc[j] >= krem) {
-                sh.sel[0] = (uint32_t)b;
-                sh.sel[1] = krem - before;
-            }
-            before += loc[j];
-        }
-        __syncthreads();
-        const uint32_t digit = sh.sel[0];
-        krem = sh.sel[1];
-        prefix |= digit << shifts[pass];
-        prefix_mask |= ((uint32_t)nb - 1u) << shifts[pass];
-        __syncthreads();
-    }
-    // T = prefix (full key); select key > T, plus the first krem keys == T.
-    const uint32_t T = take_all ? 0u : prefix;
-    const uint32_t ties = take_all ? 0u : krem;
-
-    // per-CTA counts of greater and equal keys, cluster prefix sums
-    uint32_t ngt = 0, neq = 0;
-    for (int i = tid; i < n; i += kTopkThreads) {
-        uint32_t key = keys[i];
-        ngt += key > T;
-        neq += (key == T) && key;
-    }
-    uint32_t cgt, ceq;
-    (void)block_excl_scan(ngt, sh.wsum, &cgt);
-    (void)block_excl_scan(neq, sh.wsum, &ceq);
-    if (tid == 0) {
-        sh.counts[1] = cgt;
-        sh.counts[2] = ceq;
-    }
-    cluster.sync();
-    uint32_t gt_before = 0, eq_before = 0, total_sel = 0;
-    for (int r = 0; r < C; ++r) {
-        const TopkShared *o = cluster.map_shared_rank(&sh, r);
-        const uint32_t g = o->counts[1], e = o->counts[2];
-        if (r < crank) {
-            gt_before += g;
-            eq_before += e;
-        }
-        total_sel += g;
-    }
-    // ties: the first `ties` equal keys in index order across the cluster
-    const uint32_t my_quota = eq_before >= ties ? 0u : min(ceq, ties - eq_before);
-    uint32_t ties_before = min(eq_before, ties);
-    total_sel += ties;
-    const uint32_t base = gt_before + ties_before;
-
-    // ordered compaction of this CTA's selection
-    uint32_t written = 0, eq_seen = 0;
-    int32_t *orow = out + (size_t)(row_ok ? row : 0) * ld_out;
-    for (int start = 0; start < n; start += kTopkThreads) {
-        int i = start + tid;
-        uint32_t key = i < n ? keys[i] : 0u;
-        uint32_t is_eq = (key == T && key) ? 1u : 0u;
-        uint32_t tot_eq;
-        uint32_t eq_rank = eq_seen + block_excl_scan(is_eq, sh.wsum, &tot_eq);
-        uint32_t take = (key > T) || (is_eq && eq_rank < my_quota) ? 1u : 0u;
-        uint32_t tot_take;
-        uint32_t pos = written + block_excl_scan(take, sh.wsum, &tot_take);
-        if (take && row_ok)
-            orow[base + pos] = lo + i;
-        written += tot_take;
-        eq_seen += tot_eq;
-    }
-    // -1 padding of [total_sel, k), spread over the cluster
-    if (row_ok)
-        for (int j = (int)total_sel + crank * kTopkThreads + tid; j < k; j += C * kTopkThreads)
-            orow[j] = -1;
-    cluster.sync();  // no CTA leaves while another may still read its shared memory
-}
 
 // ---------------------------------------------------------- candidate mask
 //
@@ -426,36 +204,28 @@ extern "C" idx_status idx_topk(const float *logits, int64_t ld, int rows, const 
 {
     (void)ws;
     (void)ws_bytes;
-    if (rows < 0 || k < 0 || ld < 0 || ld_out < k)
+    namespace T = idx::topk_detail;
+    if (rows < 0 || k < 0 || ld < 0 || ld_out < k || ld > INT32_MAX)
         return IDX_ERR_INVALID_ARG;
     if (rows == 0 || k == 0)
         return IDX_OK;
     if (!logits || !lengths || !out_idx || ld <= 0)
         return IDX_ERR_INVALID_ARG;
     const int nsm = sm_count();
-    // cluster size: slice of the widest possible row within ~96 KB, and enough
-    // CTAs to cover the machine twice
+    // cluster size: enough CTAs to cover the machine, without cutting rows
+    // into slices shorter than a few thousand keys
     int C = 1;
-    const long long width = ld;
-    while (C < kMaxCluster && (width + C - 1) / C * 4 > 96 * 1024)
+    while (C < T::kMaxCluster && (long long)rows * C < nsm && ld / (2 * C) >= 4096)
         C <<= 1;
-    while (C < kMaxCluster && (long long)rows * C < 2LL * nsm &&
-           (width + 2 * C - 1) / (2 * C) >= 256)
-        C <<= 1;
-    const long long slice = (width + C - 1) / C;
-    const size_t smem = sizeof(TopkShared) + (size_t)slice * 4;
-    if (smem > 227 * 1024)
-        return IDX_ERR_UNSUPPORTED;
-    cudaError_t e = cudaFuncSetAttribute(topk_cluster_kernel,
+    const size_t smem = sizeof(T::Shared);
+    cudaError_t e = cudaFuncSetAttribute(T::topk_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess && C > 8)
-        e = cudaFuncSetAttribute(topk_cluster_kernel,
-                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess)
         return IDX_ERR_CUDA;
+    const int vec_ok = (ld % 4 == 0) && aligned16(logits);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(rows * C));
-    cfg.blockDim = dim3(kTopkThreads);
+    cfg.blockDim = dim3(T::kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = (cudaStream_t)stream;
     cudaLaunchAttribute attr[1];
@@ -465,8 +235,8 @@ extern "C" idx_status idx_topk(const float *logits, int64_t ld, int rows, const 
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, topk_cluster_kernel, logits, ld, rows, lengths, k, out_idx,
-                           ld_out, (int)slice);
+    e = cudaLaunchKernelEx(&cfg, T::topk_kernel, logits, ld, rows, lengths, k, out_idx, ld_out,
+                           vec_ok);
     return launch_status(e);
 }
 
