@@ -101,10 +101,23 @@ def version() -> str:
     return lib().idx_version().decode()
 
 
-def idx_mqa_logits(q, q_scale, weights, k, k_scale, row_ks, row_ke, fmt, logits,
-                   stream=None):
-    """Non-paged logits.  q [M,H,D] (fp8) or [M,H,D/2] (mxfp4) bytes; k [N,D] or
-    [N,D/2]; logits fp32 [M, >= N] (row stride used as ld)."""
+class Prepared:
+    """One validated library call with its arguments already marshalled;
+    calling it launches on the given (or current) stream."""
+
+    __slots__ = ("fn", "args", "name", "keep")
+
+    def __init__(self, name, args, keep):
+        self.fn = getattr(lib(), name)
+        self.name = name
+        self.args = tuple(args)
+        self.keep = keep  # tensors that must outlive the call
+
+    def __call__(self, stream=None):
+        _check(self.fn(*self.args, _stream(stream)), self.name)
+
+
+def prepare_mqa_logits(q, q_scale, weights, k, k_scale, row_ks, row_ke, fmt, logits):
     q, k = _u8(q), _u8(k)
     M, H = q.shape[0], q.shape[1]
     D = q.shape[2] if fmt == FMT_FP8 else 2 * q.shape[2]
@@ -114,18 +127,23 @@ def idx_mqa_logits(q, q_scale, weights, k, k_scale, row_ks, row_ke, fmt, logits,
     _need(row_ke, torch.int32, "row_ke")
     if logits.dtype != torch.float32 or logits.stride(1) != 1:
         raise ValueError("logits must be float32 with unit column stride")
-    rc = lib().idx_mqa_logits(_ptr(q), _ptr(q_scale), _ptr(weights), _ptr(k), _ptr(k_scale),
-                              _ptr(row_ks), _ptr(row_ke), M, N, H, D, fmt, _ptr(logits),
-                              logits.stride(0), None, 0, _stream(stream))
-    _check(rc, "idx_mqa_logits")
+    args = (_ptr(q), _ptr(q_scale), _ptr(weights), _ptr(k), _ptr(k_scale), _ptr(row_ks),
+            _ptr(row_ke), M, N, H, D, fmt, _ptr(logits), logits.stride(0), None, 0)
+    return Prepared("idx_mqa_logits", args, (q, q_scale, weights, k, k_scale, row_ks, row_ke,
+                                             logits))
 
 
-def idx_paged_mqa_logits(q, q_scale, weights, kv_pages, block_table, context_lens, next_n,
-                         page_size, fmt, logits, max_model_len, row_ks=None, ctx_per_row=False,
-                         candidate_blocks=None, cand_block=0, num_ctas=0, stream=None):
-    """Paged logits.  q [B*next_n,H,D|D/2] bytes; kv_pages uint8 [num_pages, page_stride];
-    block_table int32 [B, >= ceil(max_model_len/page_size)]; logits fp32
-    [B*next_n, >= max_model_len]."""
+def idx_mqa_logits(q, q_scale, weights, k, k_scale, row_ks, row_ke, fmt, logits,
+                   stream=None):
+    """Non-paged logits.  q [M,H,D] (fp8) or [M,H,D/2] (mxfp4) bytes; k [N,D] or
+    [N,D/2]; logits fp32 [M, >= N] (row stride used as ld)."""
+    prepare_mqa_logits(q, q_scale, weights, k, k_scale, row_ks, row_ke, fmt, logits)(stream)
+
+
+def prepare_paged_mqa_logits(q, q_scale, weights, kv_pages, block_table, context_lens, next_n,
+                             page_size, fmt, logits, max_model_len, row_ks=None,
+                             ctx_per_row=False, candidate_blocks=None, cand_block=0,
+                             num_ctas=0):
     q = _u8(q)
     rows, H = q.shape[0], q.shape[1]
     D = q.shape[2] if fmt == FMT_FP8 else 2 * q.shape[2]
@@ -139,53 +157,80 @@ def idx_paged_mqa_logits(q, q_scale, weights, kv_pages, block_table, context_len
     if candidate_blocks is not None:
         _need(candidate_blocks, torch.int32, "candidate_blocks")
         cand_stride, num_cand = candidate_blocks.stride(0), candidate_blocks.shape[1]
-    rc = lib().idx_paged_mqa_logits(
-        _ptr(q), _ptr(q_scale), _ptr(weights), _ptr(kv_pages), kv_pages.stride(0),
-        kv_pages.shape[0], _ptr(block_table), block_table.stride(0), _ptr(context_lens),
-        int(ctx_per_row), _ptr(row_ks), B, next_n, H, D, page_size, fmt,
-        _ptr(candidate_blocks), cand_stride, num_cand, cand_block, _ptr(logits),
-        logits.stride(0), max_model_len, num_ctas, None, 0, _stream(stream))
-    _check(rc, "idx_paged_mqa_logits")
+    args = (_ptr(q), _ptr(q_scale), _ptr(weights), _ptr(kv_pages), kv_pages.stride(0),
+            kv_pages.shape[0], _ptr(block_table), block_table.stride(0), _ptr(context_lens),
+            int(ctx_per_row), _ptr(row_ks), B, next_n, H, D, page_size, fmt,
+            _ptr(candidate_blocks), cand_stride, num_cand, cand_block, _ptr(logits),
+            logits.stride(0), max_model_len, num_ctas, None, 0)
+    return Prepared("idx_paged_mqa_logits", args, (q, q_scale, weights, kv_pages, block_table,
+                                                   context_lens, row_ks, candidate_blocks,
+                                                   logits))
 
 
-def idx_apply_candidate_mask(logits, row_ks, row_ke, candidate_blocks, block_size,
-                             row_repeat=1, width=None, stream=None):
+def idx_paged_mqa_logits(q, q_scale, weights, kv_pages, block_table, context_lens, next_n,
+                         page_size, fmt, logits, max_model_len, row_ks=None, ctx_per_row=False,
+                         candidate_blocks=None, cand_block=0, num_ctas=0, stream=None):
+    """Paged logits.  q [B*next_n,H,D|D/2] bytes; kv_pages uint8 [num_pages, page_stride];
+    block_table int32 [B, >= ceil(max_model_len/page_size)]; logits fp32
+    [B*next_n, >= max_model_len]."""
+    prepare_paged_mqa_logits(q, q_scale, weights, kv_pages, block_table, context_lens, next_n,
+                             page_size, fmt, logits, max_model_len, row_ks, ctx_per_row,
+                             candidate_blocks, cand_block, num_ctas)(stream)
+
+
+def prepare_apply_candidate_mask(logits, row_ks, row_ke, candidate_blocks, block_size,
+                                 row_repeat=1, width=None):
     rows = logits.shape[0]
     width = logits.shape[1] if width is None else width
     _need(row_ke, torch.int32, "row_ke")
     _need(candidate_blocks, torch.int32, "candidate_blocks")
-    rc = lib().idx_apply_candidate_mask(_ptr(logits), logits.stride(0), rows, width,
-                                        _ptr(row_ks), _ptr(row_ke), _ptr(candidate_blocks),
-                                        candidate_blocks.stride(0), candidate_blocks.shape[1],
-                                        block_size, row_repeat, _stream(stream))
-    _check(rc, "idx_apply_candidate_mask")
+    args = (_ptr(logits), logits.stride(0), rows, width, _ptr(row_ks), _ptr(row_ke),
+            _ptr(candidate_blocks), candidate_blocks.stride(0), candidate_blocks.shape[1],
+            block_size, row_repeat)
+    return Prepared("idx_apply_candidate_mask", args, (logits, row_ks, row_ke, candidate_blocks))
 
 
-def idx_topk(logits, lengths, k, out, stream=None):
-    """out int32 [rows, >= k]: ascending indices of the k largest finite logits
-    of each row within [0, lengths[r]), -1 padded."""
+def idx_apply_candidate_mask(logits, row_ks, row_ke, candidate_blocks, block_size,
+                             row_repeat=1, width=None, stream=None):
+    prepare_apply_candidate_mask(logits, row_ks, row_ke, candidate_blocks, block_size,
+                                 row_repeat, width)(stream)
+
+
+def prepare_topk(logits, lengths, k, out):
     if logits.dtype != torch.float32 or logits.stride(1) != 1:
         raise ValueError("logits must be float32 with unit column stride")
     _need(lengths, torch.int32, "lengths")
     if out.dtype != torch.int32 or out.stride(1) != 1:
         raise ValueError("out must be int32 with unit column stride")
-    rc = lib().idx_topk(_ptr(logits), logits.stride(0), logits.shape[0], _ptr(lengths), k,
-                        _ptr(out), out.stride(0), None, 0, _stream(stream))
-    _check(rc, "idx_topk")
+    args = (_ptr(logits), logits.stride(0), logits.shape[0], _ptr(lengths), k, _ptr(out),
+            out.stride(0), None, 0)
+    return Prepared("idx_topk", args, (logits, lengths, out))
 
 
-def idx_topk_to_ragged_slots(topk, block_table, page_size, num_pages, slots, indptr, lens,
-                             next_n=1, row_to_seq=None, max_blocks=None, stream=None):
+def idx_topk(logits, lengths, k, out, stream=None):
+    """out int32 [rows, >= k]: ascending indices of the k largest finite logits
+    of each row within [0, lengths[r]), -1 padded."""
+    prepare_topk(logits, lengths, k, out)(stream)
+
+
+def prepare_topk_to_ragged_slots(topk, block_table, page_size, num_pages, slots, indptr, lens,
+                                 next_n=1, row_to_seq=None, max_blocks=None):
     if topk.dtype != torch.int32 or topk.stride(1) != 1:
         raise ValueError("topk must be int32 with unit column stride")
     _need(block_table, torch.int32, "block_table")
     rows, k = topk.shape
     mb = block_table.shape[1] if max_blocks is None else max_blocks
-    rc = lib().idx_topk_to_ragged_slots(_ptr(topk), topk.stride(0), rows, k, _ptr(row_to_seq),
-                                        next_n, _ptr(block_table), block_table.stride(0), mb,
-                                        page_size, num_pages, _ptr(slots), _ptr(indptr),
-                                        _ptr(lens), _stream(stream))
-    _check(rc, "idx_topk_to_ragged_slots")
+    args = (_ptr(topk), topk.stride(0), rows, k, _ptr(row_to_seq), next_n, _ptr(block_table),
+            block_table.stride(0), mb, page_size, num_pages, _ptr(slots), _ptr(indptr),
+            _ptr(lens))
+    return Prepared("idx_topk_to_ragged_slots", args,
+                    (topk, block_table, slots, indptr, lens, row_to_seq))
+
+
+def idx_topk_to_ragged_slots(topk, block_table, page_size, num_pages, slots, indptr, lens,
+                             next_n=1, row_to_seq=None, max_blocks=None, stream=None):
+    prepare_topk_to_ragged_slots(topk, block_table, page_size, num_pages, slots, indptr, lens,
+                                 next_n, row_to_seq, max_blocks)(stream)
 
 
 def idx_get_device_status(stream=None) -> int:

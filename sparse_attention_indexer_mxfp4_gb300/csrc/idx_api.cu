@@ -93,18 +93,29 @@ bool encode_tma_u8(CUtensorMap *map, int rank, const void *base, const uint64_t 
 
 namespace {
 
+constexpr size_t kMaxSmem = 227 * 1024;
+constexpr int kMaxSmemBytes = 227 * 1024;
+
 template <int FMT, int H, int G, int S, int NA>
 cudaError_t launch_logits_t(const LogitsArgs &a, const CUtensorMap &tmK, const CUtensorMap &tmQ,
-                            int nctas, cudaStream_t stream)
+                            const CUtensorMap &tmS, int nctas, cudaStream_t stream)
 {
     using C = LogitsCfg<FMT, H, G, S, NA>;
     const size_t smem = (size_t)C::fixed_bytes() + (size_t)2 * G * a.cand_words * 4;
     auto kern = logits_kernel<FMT, H, G, S, NA>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess)
-        return e;
-    kern<<<nctas, kLogitsThreads, smem, stream>>>(a, tmK, tmQ);
+    // raise the dynamic shared memory limit once per device to the maximum
+    static int configured[kMaxDevices] = {};
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    if (!configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kMaxSmemBytes);
+        if (e != cudaSuccess)
+            return e;
+        configured[dev] = 1;
+    }
+    kern<<<nctas, kLogitsThreads, smem, stream>>>(a, tmK, tmQ, tmS);
     return cudaGetLastError();
 }
 
@@ -115,23 +126,23 @@ size_t logits_smem_t(int cand_words)
     return (size_t)LogitsCfg<FMT, H, G, S, NA>::fixed_bytes() + (size_t)2 * G * cand_words * 4;
 }
 
-constexpr size_t kMaxSmem = 227 * 1024;
 
 // Dispatch on (format, heads, rows per group) to the compiled instantiations.
 cudaError_t launch_logits(int fmt, int H, int G, const LogitsArgs &a, const CUtensorMap &tmK,
-                          const CUtensorMap &tmQ, int nctas, cudaStream_t s, bool *supported)
+                          const CUtensorMap &tmQ, const CUtensorMap &tmS, int nctas,
+                          cudaStream_t s, bool *supported)
 {
     *supported = true;
     if (H == 64 && fmt == kFmtFp8) {
         switch (G) {
-        case 1: return launch_logits_t<kFmtFp8, 64, 1, 8, 2>(a, tmK, tmQ, nctas, s);
-        case 2: return launch_logits_t<kFmtFp8, 64, 2, 8, 2>(a, tmK, tmQ, nctas, s);
-        case 4: return launch_logits_t<kFmtFp8, 64, 4, 6, 2>(a, tmK, tmQ, nctas, s);
+        case 1: return launch_logits_t<kFmtFp8, 64, 1, 8, 2>(a, tmK, tmQ, tmS, nctas, s);
+        case 2: return launch_logits_t<kFmtFp8, 64, 2, 8, 2>(a, tmK, tmQ, tmS, nctas, s);
+        case 4: return launch_logits_t<kFmtFp8, 64, 4, 6, 2>(a, tmK, tmQ, tmS, nctas, s);
         }
     } else if (H == 64 && fmt == kFmtMxfp4) {
         switch (G) {
-        case 1: return launch_logits_t<kFmtMxfp4, 64, 1, 12, 2>(a, tmK, tmQ, nctas, s);
-        case 2: return launch_logits_t<kFmtMxfp4, 64, 2, 12, 2>(a, tmK, tmQ, nctas, s);
+        case 1: return launch_logits_t<kFmtMxfp4, 64, 1, 12, 2>(a, tmK, tmQ, tmS, nctas, s);
+        case 2: return launch_logits_t<kFmtMxfp4, 64, 2, 12, 2>(a, tmK, tmQ, tmS, nctas, s);
         }
     }
     *supported = false;
@@ -186,7 +197,7 @@ extern "C" idx_status idx_mqa_logits(const void *q, const void *q_scale, const f
     if (D != 128 || H != 64)
         return IDX_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(k) || !aligned16(weights) ||
-        (q_scale && !aligned16(q_scale)) || (f == kFmtMxfp4 && !aligned16(k_scale)))
+        (q_scale && !aligned16(q_scale)) || !aligned16(k_scale))
         return IDX_ERR_UNSUPPORTED;
     if (f == kFmtMxfp4 && N % 4 != 0)
         return IDX_ERR_UNSUPPORTED;
@@ -202,7 +213,14 @@ extern "C" idx_status idx_mqa_logits(const void *q, const void *q_scale, const f
     const int rowb = f == kFmtFp8 ? D : D / 2;
     const CUtensorMapSwizzle swz =
         f == kFmtFp8 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-    CUtensorMap tmK, tmQ;
+    CUtensorMap tmK, tmQ, tmS;
+    {
+        // the key scales, 4 bytes per key (fp32 or four e8m0), 64 keys per box
+        uint64_t dims[1] = {(uint64_t)N * 4};
+        uint32_t box[1] = {(uint32_t)kHalfKeys * 4};
+        if (!encode_tma_u8(&tmS, 1, k_scale, dims, nullptr, box, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return IDX_ERR_UNSUPPORTED;
+    }
     {
         uint64_t dims[3] = {(uint64_t)rowb, (uint64_t)N, 1};
         uint64_t str[2] = {(uint64_t)rowb, (uint64_t)rowb * (uint64_t)N};
@@ -243,7 +261,8 @@ extern "C" idx_status idx_mqa_logits(const void *q, const void *q_scale, const f
     const long long units = (long long)a.num_groups * T;
     const int nctas = (int)(units < nsm ? units : nsm);
     bool supported = false;
-    cudaError_t e = launch_logits(f, H, G, a, tmK, tmQ, nctas, (cudaStream_t)stream, &supported);
+    cudaError_t e =
+        launch_logits(f, H, G, a, tmK, tmQ, tmS, nctas, (cudaStream_t)stream, &supported);
     if (!supported)
         return IDX_ERR_UNSUPPORTED;
     return launch_status(e);
@@ -294,7 +313,16 @@ extern "C" idx_status idx_paged_mqa_logits(
     const size_t smem = logits_smem(f, H, G, cand_words);
     if (smem == 0 || smem > kMaxSmem)
         return IDX_ERR_UNSUPPORTED;
-    CUtensorMap tmK, tmQ;
+    CUtensorMap tmK, tmQ, tmS;
+    {
+        // each page's scale block: page_size x 4 bytes after the values
+        uint64_t dims[2] = {(uint64_t)page_size * 4, (uint64_t)num_pages};
+        uint64_t str[1] = {(uint64_t)page_stride_bytes};
+        uint32_t box[2] = {(uint32_t)kHalfKeys * 4, 1};
+        if (!encode_tma_u8(&tmS, 2, kv_pages + (size_t)page_size * rowb, dims, str, box,
+                           CU_TENSOR_MAP_SWIZZLE_NONE))
+            return IDX_ERR_UNSUPPORTED;
+    }
     {
         uint64_t dims[3] = {(uint64_t)rowb, (uint64_t)page_size, (uint64_t)num_pages};
         uint64_t str[2] = {(uint64_t)rowb, (uint64_t)page_stride_bytes};
@@ -347,7 +375,8 @@ extern "C" idx_status idx_paged_mqa_logits(
         return IDX_ERR_CUDA;
     const int nctas = num_ctas > 0 ? num_ctas : sm_count();
     bool supported = false;
-    cudaError_t e = launch_logits(f, H, G, a, tmK, tmQ, nctas, (cudaStream_t)stream, &supported);
+    cudaError_t e =
+        launch_logits(f, H, G, a, tmK, tmQ, tmS, nctas, (cudaStream_t)stream, &supported);
     if (!supported)
         return IDX_ERR_UNSUPPORTED;
     return launch_status(e);

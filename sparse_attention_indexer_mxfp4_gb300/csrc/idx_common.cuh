@@ -65,26 +65,35 @@ IDX_DEVFN bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
-// Wait for phase `parity` of `bar` to complete, giving up after ~`limit_ns`
-// nanoseconds or as soon as *abort is set by another role.  On give-up sets
-// *abort and the timeout bit of the device status word *status and returns false.  Every pipeline wait
-// goes through here, so no wait can spin forever.
+// Like mbar_try_wait, but the thread may sleep in hardware for up to
+// `hint_ns` nanoseconds waiting for the phase instead of returning at once,
+// so a waiting warp takes no issue slots from the warps that work.
+IDX_DEVFN bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+                 : "memory");
+    return ok != 0;
+}
+
 // Slow path of mbar_wait, kept out of line so every call site stays small.
 __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, volatile int *abort,
                                             unsigned int *status, uint64_t limit_ns)
 {
     uint64_t t0 = globaltimer_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity))
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, 20000u))
             return true;
-        if ((it & 63) == 0) {
-            if (*abort)
-                return false;
-            if (globaltimer_ns() - t0 > limit_ns) {
-                *abort = 1;
-                atomicOr(status, kDevTimeout);
-                return false;
-            }
+        if (*abort)
+            return false;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            *abort = 1;
+            atomicOr(status, kDevTimeout);
+            return false;
         }
     }
 }
@@ -102,6 +111,14 @@ IDX_DEVFN bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
 IDX_DEVFN void tma_prefetch_desc(const void *desc)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(desc)) : "memory");
+}
+
+IDX_DEVFN void tma_load_1d(void *dst, const void *desc, uint64_t *bar, int x)
+{
+    asm volatile("cp.async.bulk.tensor.1d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%3}], [%2];" ::"r"(smem_u32(dst)),
+                 "l"(reinterpret_cast<uint64_t>(desc)), "r"(smem_u32(bar)), "r"(x)
+                 : "memory");
 }
 
 IDX_DEVFN void tma_load_2d(void *dst, const void *desc, uint64_t *bar, int x, int y)

@@ -10,7 +10,8 @@
 //   warp 1    MMA issuer: owns the TMEM allocation and issues the tcgen05 MMAs
 //             S[t, (r,h)] = k[t,:] . q[r,h,:] with keys on M (128 lanes) and
 //             the group's (row, head) pairs on N;
-//   warps 2-5 epilogue: thread i of the four warps owns TMEM lane i, i.e. one
+//   warps 2-9 epilogue, two warpgroups taking alternate tiles (one TMEM
+//             accumulator each): thread i of a warpgroup owns TMEM lane i, i.e. one
 //             key, and reduces  sum_h w[r,h] * relu(scale * S[t,(r,h)])  over the
 //             heads in registers, applies the [ks, ke) and candidate masks and
 //             stores the fp32 logit.  Per-head scores never leave TMEM and
@@ -28,8 +29,8 @@ namespace idx {
 
 constexpr int kFmtFp8 = 0;
 constexpr int kFmtMxfp4 = 1;
-constexpr int kLogitsThreads = 192;
-constexpr int kEpiWarps = 4;
+constexpr int kEpiWarps = 8;  // two warpgroups, one per TMEM accumulator
+constexpr int kLogitsThreads = 64 + 32 * kEpiWarps;
 constexpr int kWinTiles = 16;  // tiles whose pages the producer resolves at once (32 halves)
 
 template <int FMT, int H, int G, int S, int NA>
@@ -37,10 +38,12 @@ struct LogitsCfg {
     static constexpr int NCOLS = G * H;                    // MMA N
     static constexpr int ROWB = FMT == kFmtFp8 ? 128 : 64;  // value bytes per key / query row
     static constexpr int A_BYTES = kTileKeys * ROWB;
-    // stage: K values | (MXFP4) key scale words as loaded | the same in MMA order
-    static constexpr int SF_STAGE = FMT == kFmtFp8 ? 0 : 512;
+    // stage: K values | key scales as loaded (FP8 fp32, MXFP4 e8m0 words) |
+    // (MXFP4) the scale words in MMA order | flags: which halves hold data
+    static constexpr int SF_STAGE = 512;
     static constexpr int SF_ATOM = FMT == kFmtFp8 ? 0 : 512;
-    static constexpr int STAGE_BYTES = ((A_BYTES + SF_STAGE + SF_ATOM) + 1023) / 1024 * 1024;
+    static constexpr int OFF_FLAGS = A_BYTES + SF_STAGE + SF_ATOM;
+    static constexpr int STAGE_BYTES = ((OFF_FLAGS + 16) + 1023) / 1024 * 1024;
     static constexpr int Q_BYTES = (NCOLS * ROWB + 1023) / 1024 * 1024;
     static constexpr int W_BYTES = G * H * 4;
     static constexpr int QS_BYTES = G * H * 4;  // FP8 q_scale or MXFP4 q scale words
@@ -69,6 +72,7 @@ struct LogitsCfg {
     static_assert(TM_USED <= 512, "accumulators do not fit in tensor memory");
     static_assert(NCOLS % 16 == 0 && NCOLS >= 16 && NCOLS <= 256, "MMA N out of range");
     static_assert(H % 32 == 0, "heads are read from TMEM 32 columns at a time");
+    static_assert(NA == 2, "one TMEM accumulator per epilogue warpgroup");
     // instruction descriptor: fp32 accumulate, K-major A and B, M = 128, N = NCOLS
     __host__ __device__ static constexpr uint32_t idesc_f8()
     {
@@ -115,46 +119,6 @@ __device__ __forceinline__ HalfInfo half_info(const LogitsArgs &a, const GroupIn
     return h;
 }
 
-// Scale and liveness of one key, fetched ahead of use by the epilogue.
-struct KeyPrefetch {
-    float ksc;
-    bool live;
-};
-
-template <int FMT>
-__device__ __forceinline__ KeyPrefetch key_prefetch(const LogitsArgs &a, const UnitWalk &la,
-                                                    int key_in_tile)
-{
-    KeyPrefetch p;
-    p.ksc = 1.0f;
-    p.live = false;
-    if (la.left <= 0)
-        return p;
-    const int t = la.j * kTileKeys + key_in_tile;
-    if (t >= la.gi.hi || t < la.gi.lo)
-        return p;
-    if (a.paged) {
-        const int lp = page_of(a, t);
-        const int pg = __ldg(a.bt + (size_t)la.g * a.bt_stride + lp);
-        if (pg < 0 || pg >= a.num_pages)
-            return p;
-        if (FMT == kFmtFp8)
-            p.ksc = __ldg(reinterpret_cast<const float *>(a.kv + (size_t)pg * a.page_stride +
-                                                          a.scale_off) +
-                          (t - lp * a.page_size));
-    } else if (FMT == kFmtFp8) {
-        p.ksc = __ldg(a.k_scale + t);
-    }
-    p.live = true;
-    return p;
-}
-
-__device__ __forceinline__ void skip_fill_units(const LogitsArgs &a, UnitWalk &w)
-{
-    while (w.left > 0 && !tile_is_compute(w.gi, w.j))
-        walk_next(a, w);
-}
-
 } // namespace idx
 
 namespace idx {
@@ -162,7 +126,7 @@ namespace idx {
 template <int FMT, int H, int G, int S, int NA>
 __global__ void __launch_bounds__(kLogitsThreads, 1)
     logits_kernel(const __grid_constant__ LogitsArgs a, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmQ)
+                  const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmS)
 {
     using C = LogitsCfg<FMT, H, G, S, NA>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -183,11 +147,11 @@ __global__ void __launch_bounds__(kLogitsThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], 1 + 4);  // MMA commit + the owning epilogue warpgroup
         }
         for (int i = 0; i < NA; ++i) {
             mbar_init(&acc_full[i], 1);
-            mbar_init(&acc_empty[i], kEpiWarps);
+            mbar_init(&acc_empty[i], 4);  // the owning warpgroup's warps
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&q_full[i], 1);
@@ -199,6 +163,7 @@ __global__ void __launch_bounds__(kLogitsThreads, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmS);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, C::TM_COLS);
@@ -298,32 +263,19 @@ __global__ void __launch_bounds__(kLogitsThreads, 1)
             const uint32_t mine = (ball >> h0) & 3u;
             uint8_t *st = smem + C::OFF_STAGE + s * C::STAGE_BYTES;
             if (lane == 0) {
-                uint32_t bytes = (uint32_t)__popc(mine) * (kHalfKeys * C::ROWB);
-                if (FMT == kFmtMxfp4) {
-                    for (int k = 0; k < 2; ++k)
-                        if ((mine >> k) & 1u) {
-                            const int tok = w.j * kTileKeys + k * kHalfKeys;
-                            bytes += a.paged ? 256u : (uint32_t)min(kHalfKeys, a.N - tok) * 4u;
-                        }
-                }
-                mbar_arrive_expect_tx(&full[s], bytes);
+                *reinterpret_cast<uint32_t *>(st + C::OFF_FLAGS) = mine;
+                mbar_arrive_expect_tx(&full[s], (uint32_t)__popc(mine) *
+                                                    (kHalfKeys * C::ROWB + kHalfKeys * 4));
             }
             __syncwarp();
             if ((lane == h0 || lane == h0 + 1) && cur.need) {
                 const int k = lane - h0;
                 tma_load_3d(st + k * kHalfKeys * C::ROWB, &tmK, &full[s], 0, cur.row, cur.page);
-                if (FMT == kFmtMxfp4) {
-                    uint8_t *dst = st + C::A_BYTES + k * 256;
-                    if (a.paged) {
-                        bulk_load(dst, a.kv + (size_t)cur.page * a.page_stride + a.scale_off +
-                                           (size_t)cur.row * 4,
-                                  256u, &full[s]);
-                    } else {
-                        const int tok = cur.row;
-                        bulk_load(dst, a.k_sf + (size_t)tok * 4,
-                                  (uint32_t)min(kHalfKeys, a.N - tok) * 4u, &full[s]);
-                    }
-                }
+                // the half's 64 key scales (FP8 fp32 / MXFP4 4 x e8m0), 256 bytes
+                if (a.paged)
+                    tma_load_2d(st + C::A_BYTES + k * 256, &tmS, &full[s], cur.row * 4, cur.page);
+                else
+                    tma_load_1d(st + C::A_BYTES + k * 256, &tmS, &full[s], cur.row * 4);
             }
             __syncwarp();
             ++c;
@@ -438,26 +390,19 @@ __global__ void __launch_bounds__(kLogitsThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ epilogue
+        // Two warpgroups; warpgroup wg owns accumulator wg, i.e. the compute
+        // tiles with c % 2 == wg, and every other fill tile.
+        const int ew = warp - 2;
+        const int wg = ew >> 2;
         const int quad = warp & 3;            // TMEM lane quadrant of this warp
         const int key_in_tile = quad * 32 + lane;
         int gq = 0;
-        long long c = 0;
+        long long c = 0;    // compute tiles seen (both warpgroups')
+        long long u = 0;    // units seen
         int slot = 0;
         int rks[G], rke[G];
-        // key scales and page validity, two compute tiles ahead of use
-        UnitWalk la = w;
-        skip_fill_units(a, la);
-        KeyPrefetch pf0 = key_prefetch<FMT>(a, la, key_in_tile);
-        if (la.left > 0) {
-            walk_next(a, la);
-            skip_fill_units(a, la);
-        }
-        KeyPrefetch pf1 = key_prefetch<FMT>(a, la, key_in_tile);
-        if (la.left > 0) {
-            walk_next(a, la);
-            skip_fill_units(a, la);
-        }
-        for (; w.left > 0; walk_next(a, w)) {
+        constexpr int RB = H >= 64 ? 1 : 64 / H;  // rows per batch of TMEM loads (<= 64 values)
+        for (; w.left > 0; walk_next(a, w), ++u) {
             if (w.first_in_group) {
                 slot = gq & 1;
                 for (int i = 0; i < G; ++i) {
@@ -472,21 +417,36 @@ __global__ void __launch_bounds__(kLogitsThreads, 1)
             }
             const int t = w.j * kTileKeys + key_in_tile;
             const int wend = a.paged ? w.gi.hi : a.N;  // columns this group writes
+            const bool compute = tile_is_compute(w.gi, w.j);
+            bool mine;
             float val[G];
             #pragma unroll
             for (int i = 0; i < G; ++i)
                 val[i] = -INFINITY;
-            if (tile_is_compute(w.gi, w.j)) {
-                const float ksc = pf0.ksc;
-                const bool live = pf0.live;
-                pf0 = pf1;
-                pf1 = key_prefetch<FMT>(a, la, key_in_tile);
-                if (la.left > 0) {
-                    walk_next(a, la);
-                    skip_fill_units(a, la);
-                }
-                const int acc = (int)(c % NA);
-                if (!mbar_wait(&acc_full[acc], (uint32_t)((c / NA) & 1), abort_flag, a.status))
+            if (compute) {
+                mine = (c & 1) == wg;
+                ++c;
+            } else {
+                mine = (u & 1) == wg;
+            }
+            if (compute && mine) {
+                // key scale and page validity from the stage, which is then
+                // released (the MMA's commit is the stage's other arrival)
+                const int s = (int)((c - 1) % S);
+                if (!mbar_wait(&full[s], (uint32_t)(((c - 1) / S) & 1), abort_flag, a.status))
+                    break;
+                const uint8_t *st = smem + C::OFF_STAGE + s * C::STAGE_BYTES;
+                const uint32_t halves = *reinterpret_cast<const uint32_t *>(st + C::OFF_FLAGS);
+                const bool live = t < w.gi.hi && t >= w.gi.lo && ((halves >> (key_in_tile >> 6)) & 1u);
+                float ksc = 1.0f;
+                if (FMT == kFmtFp8)
+                    ksc = reinterpret_cast<const float *>(st + C::A_BYTES)[key_in_tile];
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&empty[s]);
+                const int acc = wg;
+                const long long use = (c - 1) >> 1;  // uses of this accumulator so far
+                if (!mbar_wait(&acc_full[acc], (uint32_t)(use & 1), abort_flag, a.status))
                     break;
                 tc_fence_after();
                 const float *wsm = reinterpret_cast<const float *>(smem + C::OFF_W + slot * C::W_BYTES);
@@ -499,38 +459,54 @@ __global__ void __launch_bounds__(kLogitsThreads, 1)
                 const float sgn = ksc >= 0.0f ? 1.0f : -1.0f;
                 const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * C::NCOLS;
                 #pragma unroll
-                for (int i = 0; i < G; ++i) {
-                    if (i >= w.gi.nrows)
+                for (int i0 = 0; i0 < G; i0 += RB) {
+                    if (i0 >= w.gi.nrows)
                         break;
-                    float sum = 0.0f;
+                    // all TMEM loads of RB rows first, then one wait
+                    uint32_t r[RB * H];
                     #pragma unroll
-                    for (int hc = 0; hc < H / 32; ++hc) {
-                        uint32_t r[32];
-                        tmem_ld_32x32b_x32(tbase + i * H + hc * 32, r);
-                        tmem_ld_wait();
-                        const float *wr = wsm + i * H + hc * 32;
+                    for (int ii = 0; ii < RB; ++ii)
+                        #pragma unroll
+                        for (int hc = 0; hc < H / 32; ++hc)
+                            tmem_ld_32x32b_x32(tbase + (i0 + ii) * H + hc * 32,
+                                               *reinterpret_cast<uint32_t(*)[32]>(&r[ii * H + hc * 32]));
+                    tmem_ld_wait();
+                    #pragma unroll
+                    for (int ii = 0; ii < RB; ++ii) {
+                        const int i = i0 + ii;
+                        const float4 *w4 = reinterpret_cast<const float4 *>(wsm + i * H);
+                        float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // independent partial sums
                         if (use_qs) {
-                            const float *qr = qsm + i * H + hc * 32;
+                            const float4 *q4 = reinterpret_cast<const float4 *>(qsm + i * H);
                             #pragma unroll
-                            for (int h = 0; h < 32; ++h)
-                                sum = fmaf(wr[h], fmaxf(ksc * qr[h] * __uint_as_float(r[h]), 0.0f), sum);
-                        } else if (all_pos) {
-                            #pragma unroll
-                            for (int h = 0; h < 32; ++h)
-                                sum = fmaf(wr[h], fmaxf(__uint_as_float(r[h]), 0.0f), sum);
+                            for (int h4 = 0; h4 < H / 4; ++h4) {
+                                const float4 wv = w4[h4], qv = q4[h4];
+                                const float *x = reinterpret_cast<const float *>(&r[ii * H + 4 * h4]);
+                                s4[0] = fmaf(wv.x, fmaxf(ksc * qv.x * x[0], 0.0f), s4[0]);
+                                s4[1] = fmaf(wv.y, fmaxf(ksc * qv.y * x[1], 0.0f), s4[1]);
+                                s4[2] = fmaf(wv.z, fmaxf(ksc * qv.z * x[2], 0.0f), s4[2]);
+                                s4[3] = fmaf(wv.w, fmaxf(ksc * qv.w * x[3], 0.0f), s4[3]);
+                            }
                         } else {
+                            const float sg = all_pos ? 1.0f : sgn;
                             #pragma unroll
-                            for (int h = 0; h < 32; ++h)
-                                sum = fmaf(wr[h], fmaxf(sgn * __uint_as_float(r[h]), 0.0f), sum);
+                            for (int h4 = 0; h4 < H / 4; ++h4) {
+                                const float4 wv = w4[h4];
+                                const float *x = reinterpret_cast<const float *>(&r[ii * H + 4 * h4]);
+                                s4[0] = fmaf(wv.x, fmaxf(sg * x[0], 0.0f), s4[0]);
+                                s4[1] = fmaf(wv.y, fmaxf(sg * x[1], 0.0f), s4[1]);
+                                s4[2] = fmaf(wv.z, fmaxf(sg * x[2], 0.0f), s4[2]);
+                                s4[3] = fmaf(wv.w, fmaxf(sg * x[3], 0.0f), s4[3]);
+                            }
                         }
+                        const float sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+                        val[i] = use_qs ? sum : fabsf(ksc) * sum;
                     }
-                    val[i] = use_qs ? sum : fabsf(ksc) * sum;
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(&acc_empty[acc]);
-                ++c;
                 // masks
                 #pragma unroll
                 for (int i = 0; i < G; ++i) {
@@ -544,7 +520,7 @@ __global__ void __launch_bounds__(kLogitsThreads, 1)
                         val[i] = -INFINITY;
                 }
             }
-            if (t < wend) {
+            if (mine && t < wend) {
                 #pragma unroll
                 for (int i = 0; i < G; ++i) {
                     if (i >= w.gi.nrows)

@@ -218,10 +218,19 @@ extern "C" idx_status idx_topk(const float *logits, int64_t ld, int rows, const 
     while (C < T::kMaxCluster && (long long)rows * C < nsm && ld / (2 * C) >= 4096)
         C <<= 1;
     const size_t smem = sizeof(T::Shared);
-    cudaError_t e = cudaFuncSetAttribute(T::topk_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess)
+    static int configured[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64)
         return IDX_ERR_CUDA;
+    cudaError_t e = cudaSuccess;
+    if (!configured[dev]) {
+        e = cudaFuncSetAttribute(T::topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+        if (e != cudaSuccess)
+            return IDX_ERR_CUDA;
+        configured[dev] = 1;
+    }
     const int vec_ok = (ld % 4 == 0) && aligned16(logits);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(rows * C));

@@ -59,33 +59,43 @@ class IndexerStep:
             self.indptr = torch.empty(self.rows + 1, dtype=torch.int32, device=d)
             self.lens = torch.empty(self.rows, dtype=torch.int32, device=d)
 
-    # -------------------------------------------------------------- stages
-    def logits_stage(self, stream=None):
+        self._prepare()
+
+    def _prepare(self):
+        """Marshal every call of the step once; run() only launches."""
         c = self.case
+        self._logits_calls = []
         if self.paged:
             cand = self.cand if (self.cand is not None and self.fused_mask) else None
-            B.idx_paged_mqa_logits(self.q, self.q_scale, self.weights, self.pages,
-                                   self.block_table, self.context_lens, c.next_n, c.page_size,
-                                   c.fmt, self.logits, c.width, row_ks=self.row_ks,
-                                   ctx_per_row=c.ctx_per_row, candidate_blocks=cand,
-                                   cand_block=c.cand_block, num_ctas=self.num_ctas,
-                                   stream=stream)
+            self._logits_calls.append(B.prepare_paged_mqa_logits(
+                self.q, self.q_scale, self.weights, self.pages, self.block_table,
+                self.context_lens, c.next_n, c.page_size, c.fmt, self.logits, c.width,
+                row_ks=self.row_ks, ctx_per_row=c.ctx_per_row, candidate_blocks=cand,
+                cand_block=c.cand_block, num_ctas=self.num_ctas))
             if self.cand is not None and not self.fused_mask:
-                B.idx_apply_candidate_mask(self.logits, self.row_ks, self.lengths, self.cand,
-                                           c.cand_block, stream=stream)
+                self._logits_calls.append(B.prepare_apply_candidate_mask(
+                    self.logits, self.row_ks, self.lengths, self.cand, c.cand_block))
+            self._slots_call = B.prepare_topk_to_ragged_slots(
+                self.topk, self.block_table, c.page_size, c.num_pages, self.slots, self.indptr,
+                self.lens, next_n=c.next_n, max_blocks=self.max_blocks)
         else:
-            B.idx_mqa_logits(self.q, self.q_scale, self.weights, self.k, self.k_scale, self.ks,
-                             self.ke, c.fmt, self.logits, stream=stream)
+            self._logits_calls.append(B.prepare_mqa_logits(
+                self.q, self.q_scale, self.weights, self.k, self.k_scale, self.ks, self.ke,
+                c.fmt, self.logits))
+            self._slots_call = None
+        self._topk_call = B.prepare_topk(self.logits, self.lengths, self.k_top, self.topk)
+
+    # -------------------------------------------------------------- stages
+    def logits_stage(self, stream=None):
+        for call in self._logits_calls:
+            call(stream)
 
     def topk_stage(self, stream=None):
-        B.idx_topk(self.logits, self.lengths, self.k_top, self.topk, stream=stream)
+        self._topk_call(stream)
 
     def slots_stage(self, stream=None):
-        if self.paged:
-            B.idx_topk_to_ragged_slots(self.topk, self.block_table, self.case.page_size,
-                                       self.case.num_pages, self.slots, self.indptr, self.lens,
-                                       next_n=self.case.next_n, max_blocks=self.max_blocks,
-                                       stream=stream)
+        if self._slots_call is not None:
+            self._slots_call(stream)
 
     def run(self, stream=None):
         self.logits_stage(stream)
