@@ -137,12 +137,12 @@ cudaError_t launch_logits(int fmt, int H, int G, const LogitsArgs &a, const CUte
         switch (G) {
         case 1: return launch_logits_t<kFmtFp8, 64, 1, 8, 2>(a, tmK, tmQ, tmS, nctas, s);
         case 2: return launch_logits_t<kFmtFp8, 64, 2, 8, 2>(a, tmK, tmQ, tmS, nctas, s);
-        case 4: return launch_logits_t<kFmtFp8, 64, 4, 6, 2>(a, tmK, tmQ, tmS, nctas, s);
+        case 4: return launch_logits_t<kFmtFp8, 64, 4, 8, 2>(a, tmK, tmQ, tmS, nctas, s);
         }
     } else if (H == 64 && fmt == kFmtMxfp4) {
         switch (G) {
-        case 1: return launch_logits_t<kFmtMxfp4, 64, 1, 12, 2>(a, tmK, tmQ, tmS, nctas, s);
-        case 2: return launch_logits_t<kFmtMxfp4, 64, 2, 12, 2>(a, tmK, tmQ, tmS, nctas, s);
+        case 1: return launch_logits_t<kFmtMxfp4, 64, 1, 16, 2>(a, tmK, tmQ, tmS, nctas, s);
+        case 2: return launch_logits_t<kFmtMxfp4, 64, 2, 16, 2>(a, tmK, tmQ, tmS, nctas, s);
         }
     }
     *supported = false;
@@ -155,12 +155,12 @@ size_t logits_smem(int fmt, int H, int G, int cand_words)
         switch (G) {
         case 1: return logits_smem_t<kFmtFp8, 64, 1, 8, 2>(cand_words);
         case 2: return logits_smem_t<kFmtFp8, 64, 2, 8, 2>(cand_words);
-        case 4: return logits_smem_t<kFmtFp8, 64, 4, 6, 2>(cand_words);
+        case 4: return logits_smem_t<kFmtFp8, 64, 4, 8, 2>(cand_words);
         }
     } else if (H == 64 && fmt == kFmtMxfp4) {
         switch (G) {
-        case 1: return logits_smem_t<kFmtMxfp4, 64, 1, 12, 2>(cand_words);
-        case 2: return logits_smem_t<kFmtMxfp4, 64, 2, 12, 2>(cand_words);
+        case 1: return logits_smem_t<kFmtMxfp4, 64, 1, 16, 2>(cand_words);
+        case 2: return logits_smem_t<kFmtMxfp4, 64, 2, 16, 2>(cand_words);
         }
     }
     return 0;

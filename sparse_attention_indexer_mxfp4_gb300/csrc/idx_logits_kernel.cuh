@@ -29,8 +29,15 @@ namespace idx {
 
 constexpr int kFmtFp8 = 0;
 constexpr int kFmtMxfp4 = 1;
-constexpr int kEpiWarps = 8;  // two warpgroups, one per TMEM accumulator
-constexpr int kLogitsThreads = 64 + 32 * kEpiWarps;
+// Warp roles: 0-1 producers (even / odd tiles), 2-3 MMA issuers (even / odd
+// tiles, i.e. TMEM accumulator 0 / 1), 4-11 epilogue (two warpgroups, one
+// per accumulator).  Every SMSP (warp % 4) runs one control warp and two
+// epilogue warps, and the per-tile issue cost of each control role is
+// split over two warps.
+constexpr int kEpiWarps = 8;
+constexpr int kFirstEpiWarp = 4;
+constexpr int kMmaWarp = 2;
+constexpr int kLogitsThreads = 32 * (kFirstEpiWarp + kEpiWarps);
 constexpr int kWinTiles = 16;  // tiles whose pages the producer resolves at once (32 halves)
 
 template <int FMT, int H, int G, int S, int NA>
@@ -48,14 +55,14 @@ struct LogitsCfg {
     static constexpr int W_BYTES = G * H * 4;
     static constexpr int QS_BYTES = G * H * 4;  // FP8 q_scale or MXFP4 q scale words
     static constexpr int QATOMS = (NCOLS + 127) / 128;
-    static constexpr int QATOM_BYTES = FMT == kFmtFp8 ? 0 : QATOMS * 512;
+    static constexpr int QATOM_BYTES = FMT == kFmtFp8 ? 0 : QATOMS * 512;  // per MMA warp
     // shared memory offsets
     static constexpr int OFF_STAGE = 0;
     static constexpr int OFF_Q = OFF_STAGE + S * STAGE_BYTES;
     static constexpr int OFF_W = OFF_Q + 2 * Q_BYTES;
     static constexpr int OFF_QS = OFF_W + 2 * W_BYTES;
     static constexpr int OFF_QATOM = OFF_QS + 2 * QS_BYTES;
-    static constexpr int OFF_BAR = (OFF_QATOM + 2 * QATOM_BYTES + 7) / 8 * 8;
+    static constexpr int OFF_BAR = (OFF_QATOM + 4 * QATOM_BYTES + 7) / 8 * 8;
     // full[S], empty[S], acc_full[NA], acc_empty[NA], q_full[2], q_empty[2]
     static constexpr int NUM_BARS = 2 * S + 2 * NA + 4;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;  // tmem base, abort flag
@@ -66,13 +73,15 @@ struct LogitsCfg {
     // accumulator and of B per group slot.
     static constexpr int TM_SFA = NA * NCOLS;
     static constexpr int TM_SFB = TM_SFA + (FMT == kFmtFp8 ? 0 : NA * 4);
-    static constexpr int TM_USED = TM_SFB + (FMT == kFmtFp8 ? 0 : 2 * QATOMS * 4);
+    static constexpr int TM_USED = TM_SFB + (FMT == kFmtFp8 ? 0 : 4 * QATOMS * 4);  // 2 slots x 2 MMA warps
     static constexpr int TM_COLS = TM_USED <= 32 ? 32 : TM_USED <= 64 ? 64 : TM_USED <= 128 ? 128
                                  : TM_USED <= 256 ? 256 : 512;
     static_assert(TM_USED <= 512, "accumulators do not fit in tensor memory");
     static_assert(NCOLS % 16 == 0 && NCOLS >= 16 && NCOLS <= 256, "MMA N out of range");
     static_assert(H % 32 == 0, "heads are read from TMEM 32 columns at a time");
     static_assert(NA == 2, "one TMEM accumulator per epilogue warpgroup");
+    static_assert((S & (S - 1)) == 0 && S >= 2, "stage count must be a power of two");
+    static constexpr int LOG2S = S == 2 ? 1 : S == 4 ? 2 : S == 8 ? 3 : S == 16 ? 4 : 5;
     // instruction descriptor: fp32 accumulate, K-major A and B, M = 128, N = NCOLS
     __host__ __device__ static constexpr uint32_t idesc_f8()
     {
@@ -155,17 +164,17 @@ __global__ void __launch_bounds__(kLogitsThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&q_full[i], 1);
-            mbar_init(&q_empty[i], 1 + kEpiWarps);
+            mbar_init(&q_empty[i], 2 + kEpiWarps);  // both MMA warps' commits + epilogue
         }
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 0 && lane == 0) {
+    if (warp == kMmaWarp && lane == 0) {
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmS);
     }
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tmem_alloc(tmem_slot, C::TM_COLS);
         tmem_relinquish();
     }
@@ -180,15 +189,18 @@ __global__ void __launch_bounds__(kLogitsThreads, 1)
     UnitWalk w;
     walk_begin(a, w, g0, j0, count);
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
+    if (warp < 2) {
+        // ------------------------------------------------------------ producers
+        // Producer pw issues the compute tiles with c % 2 == pw (stage parity
+        // pw); producer 0 also loads each group's Q tile, weights and scales.
+        const int pw = warp;
         int gq = 0;        // groups started by this CTA
-        long long c = 0;   // compute tiles issued
+        int c = 0;         // compute tiles of this CTA seen so far
         int win0 = 0;      // first tile of the current page window
         HalfInfo cur = {}, nxt = {};
         bool cur_ok = false;
         for (; w.left > 0; walk_next(a, w)) {
-            if (w.first_in_group) {
+            if (w.first_in_group && pw == 0) {
                 const int slot = gq & 1;
                 if (!mbar_wait(&q_empty[slot], ((gq >> 1) & 1) ^ 1, abort_flag, a.status))
                     break;
@@ -229,6 +241,8 @@ __global__ void __launch_bounds__(kLogitsThreads, 1)
                 }
                 __syncwarp();
                 ++gq;
+            }
+            if (w.first_in_group) {
                 // page window of this group: current and next, loads in flight
                 win0 = w.j;
                 cur = half_info(a, w.gi, w.g, win0, lane);
@@ -237,6 +251,10 @@ __global__ void __launch_bounds__(kLogitsThreads, 1)
             }
             if (!tile_is_compute(w.gi, w.j))
                 continue;
+            if ((c & 1) != pw) {  // the other producer's tile
+                ++c;
+                continue;
+            }
             if (w.j >= win0 + kWinTiles) {  // slide the window (warp-uniform)
                 const int step = (w.j - win0) / kWinTiles;
                 if (step == 1) {
@@ -255,8 +273,8 @@ __global__ void __launch_bounds__(kLogitsThreads, 1)
                 }
                 cur_ok = true;
             }
-            const int s = (int)(c % S);
-            if (!mbar_wait(&empty[s], (uint32_t)((c / S) & 1) ^ 1, abort_flag, a.status))
+            const int s = c & (S - 1);
+            if (!mbar_wait(&empty[s], (uint32_t)((c >> C::LOG2S) & 1) ^ 1, abort_flag, a.status))
                 break;
             const int h0 = 2 * (w.j - win0);  // lanes h0, h0 + 1 own this tile's halves
             const uint32_t ball = __ballot_sync(0xffffffffu, cur.need);
@@ -284,17 +302,20 @@ __global__ void __launch_bounds__(kLogitsThreads, 1)
         // every group slot this CTA filled, so no copy or commit is still in
         // flight when the CTA exits.
         if (!*abort_flag) {
-            for (long long i = c > S ? c - S : 0; i < c; ++i)
-                if (!mbar_wait(&empty[i % S], (uint32_t)((i / S) & 1), abort_flag, a.status))
+            for (int i = c > S ? c - S : 0; i < c; ++i)
+                if ((i & 1) == pw &&
+                    !mbar_wait(&empty[i & (S - 1)], (uint32_t)((i >> C::LOG2S) & 1), abort_flag,
+                               a.status))
                     break;
             for (int i = gq > 2 ? gq - 2 : 0; i < gq; ++i)
                 if (!mbar_wait(&q_empty[i & 1], (i >> 1) & 1, abort_flag, a.status))
                     break;
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+        // ------------------------------------------------------------ MMA issuers
+        const int mw = warp - kMmaWarp;  // issues tiles c % 2 == mw into accumulator mw
         int gq = 0;
-        long long c = 0;
+        int c = 0;
         int slot = 0;
         for (; w.left > 0; walk_next(a, w)) {
             if (w.first_in_group) {
@@ -305,7 +326,7 @@ __global__ void __launch_bounds__(kLogitsThreads, 1)
                     // q scale words -> 32x16B atoms in MMA order, then into TMEM
                     const uint32_t *qsw =
                         reinterpret_cast<const uint32_t *>(smem + C::OFF_QS + slot * C::QS_BYTES);
-                    uint8_t *atom = smem + C::OFF_QATOM + slot * C::QATOM_BYTES;
+                    uint8_t *atom = smem + C::OFF_QATOM + (mw * 2 + slot) * C::QATOM_BYTES;
                     const int nvalid = w.gi.nrows * H;
                     for (int at = 0; at < C::QATOMS; ++at) {
                         uint4 v;
@@ -323,19 +344,22 @@ __global__ void __launch_bounds__(kLogitsThreads, 1)
                         for (int at = 0; at < C::QATOMS; ++at) {
                             uint64_t d = make_smem_desc(smem_u32(atom + at * 512), 128, 128,
                                                         kLayoutNone);
-                            tmem_cp_32x128b_warpx4(tmem_base + C::TM_SFB + (slot * C::QATOMS + at) * 4, d);
+                            tmem_cp_32x128b_warpx4(
+                                tmem_base + C::TM_SFB + ((mw * 2 + slot) * C::QATOMS + at) * 4, d);
                         }
                     }
                     __syncwarp();
                 }
                 ++gq;
             }
-            if (tile_is_compute(w.gi, w.j)) {
-                const int acc = (int)(c % NA);
-                const int s = (int)(c % S);
-                if (!mbar_wait(&acc_empty[acc], (uint32_t)((c / NA) & 1) ^ 1, abort_flag, a.status))
+            if (tile_is_compute(w.gi, w.j) && (c & 1) != mw) {
+                ++c;  // the other MMA warp's tile
+            } else if (tile_is_compute(w.gi, w.j)) {
+                const int acc = mw;
+                const int s = c & (S - 1);
+                if (!mbar_wait(&acc_empty[acc], (uint32_t)((c >> 1) & 1) ^ 1, abort_flag, a.status))
                     break;
-                if (!mbar_wait(&full[s], (uint32_t)((c / S) & 1), abort_flag, a.status))
+                if (!mbar_wait(&full[s], (uint32_t)((c >> C::LOG2S) & 1), abort_flag, a.status))
                     break;
                 uint8_t *st = smem + C::OFF_STAGE + s * C::STAGE_BYTES;
                 if constexpr (FMT == kFmtMxfp4) {
@@ -364,7 +388,7 @@ __global__ void __launch_bounds__(kLogitsThreads, 1)
                         }
                     } else {
                         const uint32_t sfa = tmem_base + C::TM_SFA + acc * 4;
-                        const uint32_t sfb = tmem_base + C::TM_SFB + slot * C::QATOMS * 4;
+                        const uint32_t sfb = tmem_base + C::TM_SFB + (mw * 2 + slot) * C::QATOMS * 4;
                         uint64_t cd = make_smem_desc(smem_u32(st + C::A_BYTES + C::SF_STAGE), 128,
                                                      128, kLayoutNone);
                         tmem_cp_32x128b_warpx4(sfa, cd);
@@ -388,16 +412,16 @@ __global__ void __launch_bounds__(kLogitsThreads, 1)
                 __syncwarp();
             }
         }
-    } else {
+    } else if (warp >= kFirstEpiWarp) {
         // ------------------------------------------------------------ epilogue
         // Two warpgroups; warpgroup wg owns accumulator wg, i.e. the compute
         // tiles with c % 2 == wg, and every other fill tile.
-        const int ew = warp - 2;
+        const int ew = warp - kFirstEpiWarp;
         const int wg = ew >> 2;
         const int quad = warp & 3;            // TMEM lane quadrant of this warp
         const int key_in_tile = quad * 32 + lane;
         int gq = 0;
-        long long c = 0;    // compute tiles seen (both warpgroups')
+        int c = 0;          // compute tiles seen (both warpgroups')
         long long u = 0;    // units seen
         int slot = 0;
         int rks[G], rke[G];
@@ -432,8 +456,8 @@ __global__ void __launch_bounds__(kLogitsThreads, 1)
             if (compute && mine) {
                 // key scale and page validity from the stage, which is then
                 // released (the MMA's commit is the stage's other arrival)
-                const int s = (int)((c - 1) % S);
-                if (!mbar_wait(&full[s], (uint32_t)(((c - 1) / S) & 1), abort_flag, a.status))
+                const int s = (c - 1) & (S - 1);
+                if (!mbar_wait(&full[s], (uint32_t)(((c - 1) >> C::LOG2S) & 1), abort_flag, a.status))
                     break;
                 const uint8_t *st = smem + C::OFF_STAGE + s * C::STAGE_BYTES;
                 const uint32_t halves = *reinterpret_cast<const uint32_t *>(st + C::OFF_FLAGS);
@@ -445,7 +469,7 @@ __global__ void __launch_bounds__(kLogitsThreads, 1)
                 if (lane == 0)
                     mbar_arrive(&empty[s]);
                 const int acc = wg;
-                const long long use = (c - 1) >> 1;  // uses of this accumulator so far
+                const int use = (c - 1) >> 1;  // uses of this accumulator so far
                 if (!mbar_wait(&acc_full[acc], (uint32_t)(use & 1), abort_flag, a.status))
                     break;
                 tc_fence_after();
@@ -541,7 +565,7 @@ __global__ void __launch_bounds__(kLogitsThreads, 1)
     // ---------------------------------------------------------------- teardown
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem_base, C::TM_COLS);
     }
