@@ -149,8 +149,8 @@ idx_status idx_apply_candidate_mask(float *logits, int64_t ld, int rows, int wid
 
 /* ------------------------------------------------------------------------
  * idx_topk -- per-row top-k token indices.
- * Passage: rocm_paged_mxfp4_indexer, _topk ("top-k over each row's
- * [0, lengths[row]); -1 pads rows shorter than k").
+ * Passage: rocm_paged_mxfp4_indexer, _topk: the k largest logits of each
+ * row over [0, lengths[row]), -1 where a row has fewer than k.
  *
  *   logits  fp32 [rows, ld]; lengths [rows] with 0 <= lengths[r] <= ld.
  *   out_idx int32 [rows, ld_out], ld_out >= k.  Row r receives the indices of
@@ -158,13 +158,28 @@ idx_status idx_apply_candidate_mask(float *logits, int64_t ld, int rows, int wid
  *           ASCENDING index order, then -1 padding.  -inf and NaN are never
  *           selected.  Among equal values at the k-th place the lower indices
  *           win, so the selected set is unique.
- *   1 <= k <= 16384.  Rows are processed by thread-block clusters that keep
- *   the row in distributed shared memory.
- *   ws, ws_bytes  unused (may be NULL / 0).
+ *   k >= 0 (k == 0 writes nothing).  ld <= INT32_MAX.
+ *   ws, ws_bytes  optional caller-owned device scratch, 16-byte aligned.
+ *           With ws_bytes >= idx_topk_workspace_size(rows, ld, k) and
+ *           ld > 8192, each row is cut into chunks of 8192 keys and the
+ *           selection runs as five launches spread over the whole GPU (the
+ *           first clears part of ws with cudaMemsetAsync on `stream`).
+ *           Otherwise (ws NULL or too small) one CTA selects each row.  Both
+ *           give the same indices.  Calls that share one ws must not overlap
+ *           in time (same stream, or ordered by events); ws holds nothing
+ *           the caller needs after the call.
+ * Errors: IDX_ERR_INVALID_ARG for negative sizes, ld_out < k or NULL
+ *   pointers; IDX_ERR_CUDA when a launch fails.
  * ---------------------------------------------------------------------- */
 idx_status idx_topk(const float *logits, int64_t ld, int rows, const int32_t *lengths, int k,
                     int32_t *out_idx, int64_t ld_out, void *ws, size_t ws_bytes,
                     idx_stream_t stream);
+
+/* Bytes of ws that idx_topk needs for its chunked path with these sizes;
+ * 0 when the chunked path does not apply (rows <= 0, ld <= 0, ld above
+ * 8192 * 1024, or rows * chunks above INT32_MAX).  Pure host arithmetic:
+ * no CUDA call, no device touched. */
+size_t idx_topk_workspace_size(int rows, int64_t ld, int k);
 
 /* ------------------------------------------------------------------------
  * idx_topk_to_ragged_slots -- top-k positions to a ragged list of cache slots.

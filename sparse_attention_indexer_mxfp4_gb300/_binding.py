@@ -63,6 +63,8 @@ def lib() -> ctypes.CDLL:
                 fn.argtypes = args
                 fn.restype = ctypes.c_int
             L.idx_version.restype = ctypes.c_char_p
+            L.idx_topk_workspace_size.argtypes = [_I, _L, _I]
+            L.idx_topk_workspace_size.restype = _S
             _lib = L
     return _lib
 
@@ -105,13 +107,14 @@ class Prepared:
     """One validated library call with its arguments already marshalled;
     calling it launches on the given (or current) stream."""
 
-    __slots__ = ("fn", "args", "name", "keep")
+    __slots__ = ("fn", "args", "name", "keep", "kernels")
 
-    def __init__(self, name, args, keep):
+    def __init__(self, name, args, keep, kernels=1):
         self.fn = getattr(lib(), name)
         self.name = name
         self.args = tuple(args)
         self.keep = keep  # tensors that must outlive the call
+        self.kernels = kernels  # kernel launches per call
 
     def __call__(self, stream=None):
         _check(self.fn(*self.args, _stream(stream)), self.name)
@@ -196,21 +199,40 @@ def idx_apply_candidate_mask(logits, row_ks, row_ke, candidate_blocks, block_siz
                                  row_repeat, width)(stream)
 
 
-def prepare_topk(logits, lengths, k, out):
+def topk_workspace_size(rows, ld, k) -> int:
+    """Bytes of device scratch idx_topk's chunked path needs (0: not used)."""
+    return int(lib().idx_topk_workspace_size(rows, ld, k))
+
+
+def prepare_topk(logits, lengths, k, out, workspace=True):
+    """workspace: True allocates the scratch for the chunked path once here
+    (held by the returned call), a uint8 CUDA tensor supplies it, False or
+    None runs the one-CTA-per-row path."""
     if logits.dtype != torch.float32 or logits.stride(1) != 1:
         raise ValueError("logits must be float32 with unit column stride")
     _need(lengths, torch.int32, "lengths")
     if out.dtype != torch.int32 or out.stride(1) != 1:
         raise ValueError("out must be int32 with unit column stride")
-    args = (_ptr(logits), logits.stride(0), logits.shape[0], _ptr(lengths), k, _ptr(out),
-            out.stride(0), None, 0)
-    return Prepared("idx_topk", args, (logits, lengths, out))
+    rows, ld = logits.shape[0], logits.stride(0)
+    ws = None
+    if workspace is True:
+        nbytes = topk_workspace_size(rows, ld, k)
+        if nbytes:
+            ws = torch.empty(nbytes, dtype=torch.uint8, device=logits.device)
+    elif workspace is not None and workspace is not False:
+        ws = workspace
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    args = (_ptr(logits), ld, rows, _ptr(lengths), k, _ptr(out), out.stride(0), _ptr(ws), nbytes)
+    # the library takes the chunked path (five kernels) under these conditions
+    need = topk_workspace_size(rows, ld, k)
+    chunked = ws is not None and need > 0 and nbytes >= need and ld > 8192
+    return Prepared("idx_topk", args, (logits, lengths, out, ws), 5 if chunked else 1)
 
 
-def idx_topk(logits, lengths, k, out, stream=None):
+def idx_topk(logits, lengths, k, out, stream=None, workspace=True):
     """out int32 [rows, >= k]: ascending indices of the k largest finite logits
     of each row within [0, lengths[r]), -1 padded."""
-    prepare_topk(logits, lengths, k, out)(stream)
+    prepare_topk(logits, lengths, k, out, workspace)(stream)
 
 
 def prepare_topk_to_ragged_slots(topk, block_table, page_size, num_pages, slots, indptr, lens,
@@ -224,7 +246,7 @@ def prepare_topk_to_ragged_slots(topk, block_table, page_size, num_pages, slots,
             block_table.stride(0), mb, page_size, num_pages, _ptr(slots), _ptr(indptr),
             _ptr(lens))
     return Prepared("idx_topk_to_ragged_slots", args,
-                    (topk, block_table, slots, indptr, lens, row_to_seq))
+                    (topk, block_table, slots, indptr, lens, row_to_seq), 3)
 
 
 def idx_topk_to_ragged_slots(topk, block_table, page_size, num_pages, slots, indptr, lens,

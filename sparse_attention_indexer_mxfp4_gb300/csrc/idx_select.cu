@@ -1,13 +1,12 @@
-// idx_select.cu -- per-row top-k (cluster radix select), candidate mask and
+// idx_select.cu -- per-row top-k (radix select; chunked over the GPU for long
+// rows), candidate mask and
 // top-k -> ragged slot map, with their C ABI entry points.
-#include <cooperative_groups.h>
 #include <algorithm>
 #include <cstdint>
 
 #include "idx_internal.h"
 #include "idx_topk.cuh"
-
-namespace cg = cooperative_groups;
+#include "idx_topk_chunked.cuh"
 
 namespace idx {
 namespace {
@@ -193,60 +192,94 @@ __global__ void __launch_bounds__(kSlotThreads)
     }
 }
 
+// ------------------------------------------------------------------ top-k
+
+idx_status topk_launch_per_row(const float *logits, int64_t ld, int rows,
+                               const int32_t *lengths, int k, int32_t *out, int64_t ld_out,
+                               int vec_ok, cudaStream_t s)
+{
+    namespace T = topk_detail;
+    const size_t smem = sizeof(T::Shared);
+    static int configured[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return IDX_ERR_CUDA;
+    if (!configured[dev]) {
+        if (cudaFuncSetAttribute(T::topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem) != cudaSuccess)
+            return IDX_ERR_CUDA;
+        configured[dev] = 1;
+    }
+    T::topk_kernel<<<rows, T::kThreads, smem, s>>>(logits, ld, rows, lengths, k, out, ld_out,
+                                                   vec_ok);
+    return launch_status(cudaGetLastError());
+}
+
+// Five launches over the caller's workspace; see idx_topk_chunked.cuh.
+idx_status topk_launch_chunked(const float *logits, int64_t ld, int rows,
+                               const int32_t *lengths, int k, int32_t *out, int64_t ld_out,
+                               void *ws, int vec_ok, cudaStream_t s)
+{
+    namespace C = topk_chunked;
+    const int P = (int)((ld + C::kCh - 1) / C::kCh);
+    const C::Ws w = C::ws_carve(ws, rows, P);
+    const size_t rsmem = sizeof(C::ResolveShared);
+    static int configured[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return IDX_ERR_CUDA;
+    if (!configured[dev]) {
+        if (cudaFuncSetAttribute(C::resolve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)rsmem) != cudaSuccess)
+            return IDX_ERR_CUDA;
+        configured[dev] = 1;
+    }
+    if (cudaMemsetAsync(ws, 0, C::ws_zeroed_bytes(rows), s) != cudaSuccess)
+        return IDX_ERR_CUDA;
+    const unsigned cgrid = (unsigned)rows * (unsigned)P;
+    C::hist_kernel<<<cgrid, C::kThreads, 0, s>>>(logits, ld, lengths, P, w, vec_ok);
+    C::pick_kernel<<<rows, C::kRowThreads, 0, s>>>(k, w);
+    C::filter_kernel<<<cgrid, C::kThreads, 0, s>>>(logits, ld, lengths, P, w, vec_ok);
+    C::resolve_kernel<<<rows, C::kRowThreads, rsmem, s>>>(logits, ld, lengths, k, P, w, out,
+                                                          ld_out, vec_ok);
+    C::write_kernel<<<cgrid, C::kThreads, 0, s>>>(logits, ld, lengths, P, w, out, ld_out,
+                                                  vec_ok);
+    return launch_status(cudaGetLastError());
+}
+
 } // namespace
 } // namespace idx
 
 using namespace idx;
 
+extern "C" size_t idx_topk_workspace_size(int rows, int64_t ld, int k)
+{
+    (void)k;
+    namespace C = idx::topk_chunked;
+    if (rows <= 0 || ld <= 0 || ld > INT32_MAX)
+        return 0;
+    const int64_t P = (ld + C::kCh - 1) / C::kCh;
+    if (P > C::kMaxChunks || (int64_t)rows * P > INT32_MAX)
+        return 0;
+    return C::ws_bytes(rows, (int)P);
+}
+
 extern "C" idx_status idx_topk(const float *logits, int64_t ld, int rows, const int32_t *lengths,
                                int k, int32_t *out_idx, int64_t ld_out, void *ws, size_t ws_bytes,
                                idx_stream_t stream)
 {
-    (void)ws;
-    (void)ws_bytes;
-    namespace T = idx::topk_detail;
     if (rows < 0 || k < 0 || ld < 0 || ld_out < k || ld > INT32_MAX)
         return IDX_ERR_INVALID_ARG;
     if (rows == 0 || k == 0)
         return IDX_OK;
     if (!logits || !lengths || !out_idx || ld <= 0)
         return IDX_ERR_INVALID_ARG;
-    const int nsm = sm_count();
-    // cluster size: enough CTAs to cover the machine, without cutting rows
-    // into slices shorter than a few thousand keys
-    int C = 1;
-    while (C < T::kMaxCluster && (long long)rows * C < nsm && ld / (2 * C) >= 4096)
-        C <<= 1;
-    const size_t smem = sizeof(T::Shared);
-    static int configured[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64)
-        return IDX_ERR_CUDA;
-    cudaError_t e = cudaSuccess;
-    if (!configured[dev]) {
-        e = cudaFuncSetAttribute(T::topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
-        if (e != cudaSuccess)
-            return IDX_ERR_CUDA;
-        configured[dev] = 1;
-    }
     const int vec_ok = (ld % 4 == 0) && aligned16(logits);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(rows * C));
-    cfg.blockDim = dim3(T::kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = (cudaStream_t)stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)C;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, T::topk_kernel, logits, ld, rows, lengths, k, out_idx, ld_out,
-                           vec_ok);
-    return launch_status(e);
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t need = idx_topk_workspace_size(rows, ld, k);
+    if (ws && need > 0 && ws_bytes >= need && aligned16(ws) && ld > topk_chunked::kCh)
+        return topk_launch_chunked(logits, ld, rows, lengths, k, out_idx, ld_out, ws, vec_ok, s);
+    return topk_launch_per_row(logits, ld, rows, lengths, k, out_idx, ld_out, vec_ok, s);
 }
 
 extern "C" idx_status idx_apply_candidate_mask(float *logits, int64_t ld, int rows, int width,

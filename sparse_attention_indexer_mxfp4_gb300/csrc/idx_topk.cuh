@@ -1,49 +1,43 @@
-// idx_topk.cuh -- per-row top-k by cluster radix select.
+// idx_topk.cuh -- per-row top-k by radix select, one CTA per row.
 //
 // Passage: vLLM page rocm_paged_mxfp4_indexer, _topk -- top-k over each
 // row's [0, lengths[row]), -1 padding.  The design is our own.
 //
-// One thread-block cluster of C CTAs handles one row; CTA c takes a
-// contiguous slice of [0, len) and each of its warps a contiguous sub-slice,
-// so (CTA, warp, position) is index order.  Values become order-preserving
-// 32-bit keys; non-finite values become key 0 and are never selected.
-//   pass 1 (stream): histogram of the top 11 key bits; the C histograms are
-//          summed through distributed shared memory and every CTA finds the
-//          same bin b1 holding the k-th largest key.
+// Each warp of the CTA takes a contiguous sub-slice of [0, len), so
+// (warp, position) is index order.  Values become order-preserving 32-bit
+// keys; non-finite values become key 0 and are never selected.  Every
+// streaming pass keeps four float4 loads per thread in flight.
+//   pass 1 (stream): histogram of the top 11 key bits and the valid count;
+//          the bin b1 holding the k-th largest key follows from a block scan.
 //   pass 2 (stream): keys in bin b1 are appended, with their index, to a
 //          shared-memory candidate list; keys above b1 are counted per warp.
 //   digits 2 and 3 (11 and 10 bits) are then resolved on the candidates
-//          (or, if the list overflowed, by streaming the slice again), which
+//          (or, if the list overflowed, by streaming the row again), which
 //          gives the k-th largest key T and how many keys equal to T to take.
 //   pass 3 (stream): every warp writes its selected indices in index order
-//          at offsets from block and cluster prefix sums.  Keys equal to T
-//          are taken lowest index first, so the selected set is unique.
-// All cross-CTA waits are hardware cluster barriers on a path every CTA of
-// the cluster takes the same number of times.
+//          at offsets from a block prefix sum.  Keys equal to T are taken
+//          lowest index first, so the selected set is unique.
 #pragma once
 
-#include <cooperative_groups.h>
 #include <cstdint>
 
 namespace idx {
 namespace topk_detail {
 
-namespace cg = cooperative_groups;
-
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kCandCap = 6144;  // candidate keys kept in shared memory per CTA
-constexpr int kMaxCluster = 8;
+constexpr int kUnroll = 4;             // float4 loads in flight per thread
+constexpr int kChunk = 128 * kUnroll;  // elements a warp handles per step
+constexpr int kCandCap = 6144;         // candidate keys kept in shared memory
 
 struct Shared {
     uint32_t hist[2][2048];
     uint32_t cand_key[kCandCap];
     int32_t cand_idx[kCandCap];
     uint32_t wsum[kWarps + 1];
-    uint32_t wgt[kWarps];     // per warp: keys > T
-    uint32_t weq[kWarps];     // per warp: keys == T
-    uint32_t cta[4];          // exported to the cluster: valid, selected, equal
-    uint32_t sel[2];          // digit found, remaining rank
+    uint32_t wgt[kWarps];  // per warp: keys > T
+    uint32_t weq[kWarps];  // per warp: keys == T
+    uint32_t sel[2];       // digit found, remaining rank
     uint32_t ncand;
 };
 
@@ -71,64 +65,61 @@ __device__ __forceinline__ void load4(const float *row, int i0, int end, bool ve
     }
 }
 
-// Exclusive scan over the kWarps per-warp values v[w] (one thread per warp
-// slot, executed by warp 0); returns nothing, rewrites v in place and puts
-// the total in *tot.  Caller syncs.
-__device__ __forceinline__ void warp0_excl_scan(uint32_t *v, uint32_t *tot)
+// One warp step: the keys of elements cb + 128u + 4*lane + e (u < kUnroll,
+// e < 4), all loads issued before any is used.  Element order within the
+// step is (u, lane, e).
+__device__ __forceinline__ void load_step(const float *row, int cb, int end, bool vec, int lane,
+                                          uint32_t (&k)[kUnroll][4])
 {
-    const int lane = threadIdx.x & 31;
-    uint32_t x = lane < kWarps ? v[lane] : 0u;
-    uint32_t incl = x;
-    for (int o = 1; o < 32; o <<= 1) {
-        uint32_t n = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o)
-            incl += n;
-    }
-    if (lane < kWarps)
-        v[lane] = incl - x;
-    if (lane == 31)
-        *tot = incl;
+    #pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+        load4(row, cb + 128 * u + 4 * lane, end, vec, k[u]);
 }
 
-// Sum the C histograms of `h` (nb bins) through distributed shared memory,
-// find the bin where the descending cumulative count reaches krem; returns
-// (bin, krem - count above the bin) via sh.sel.  Every CTA computes the same.
-__device__ __forceinline__ void find_bin(cg::cluster_group &cluster, Shared &sh, uint32_t *h,
-                                         int nb, uint32_t krem)
+// Sum of a value over the warp.
+__device__ __forceinline__ uint32_t warp_sum(uint32_t v)
 {
-    const int C = (int)cluster.num_blocks();
-    const int tid = threadIdx.x;
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Exclusive prefix of v over the lanes; *tot gets the warp total.
+__device__ __forceinline__ uint32_t warp_excl(uint32_t v, int lane, uint32_t *tot)
+{
+    uint32_t x = v;
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t n = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o)
+            x += n;
+    }
+    *tot = __shfl_sync(0xffffffffu, x, 31);
+    return x - v;
+}
+
+// Find the bin (of nb, scanned from the top) where the descending
+// cumulative count reaches krem; writes (bin, krem - count above it) to
+// sh.sel.  All threads call it; it starts and ends with a barrier.
+__device__ __forceinline__ void find_bin(Shared &sh, const uint32_t *h, int nb, uint32_t krem)
+{
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     uint32_t loc[4];
     uint32_t lsum = 0;
     #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const int b = nb - 1 - (tid * 4 + j);  // descending bins
-        uint32_t v = 0;
-        if (b >= 0) {
-            if (C == 1)
-                v = h[b];
-            else
-                for (int r = 0; r < C; ++r)
-                    v += cluster.map_shared_rank(h, r)[b];
-        }
-        loc[j] = v;
-        lsum += v;
+        loc[j] = b >= 0 ? h[b] : 0u;
+        lsum += loc[j];
     }
-    // block exclusive scan of lsum
-    const int lane = tid & 31, w = tid >> 5;
-    uint32_t x = lsum;
-    for (int o = 1; o < 32; o <<= 1) {
-        uint32_t n = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o)
-            x += n;
-    }
-    if (lane == 31)
-        sh.wsum[w] = x;
+    uint32_t wt;
+    const uint32_t ex = warp_excl(lsum, lane, &wt);
+    __syncthreads();  // earlier readers of wsum are done
+    if (lane == 0)
+        sh.wsum[w] = wt;
     __syncthreads();
-    if (w == 0)
-        warp0_excl_scan(sh.wsum, &sh.wsum[kWarps]);
-    __syncthreads();
-    uint32_t before = sh.wsum[w] + x - lsum;
+    uint32_t before = ex;
+    for (int i = 0; i < w; ++i)
+        before += sh.wsum[i];
     #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const int b = nb - 1 - (tid * 4 + j);
@@ -146,25 +137,18 @@ __global__ void __launch_bounds__(kThreads)
                 const int32_t *__restrict__ lengths, int k, int32_t *__restrict__ out,
                 int64_t ld_out, int vec_ok)
 {
-    cg::cluster_group cluster = cg::this_cluster();
-    const int C = (int)cluster.num_blocks();
-    const int crank = (int)cluster.block_rank();
-    const int row = blockIdx.x / C;
+    const int row = blockIdx.x;
     extern __shared__ __align__(16) uint8_t dsm[];
     Shared &sh = *reinterpret_cast<Shared *>(dsm);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-
-    const bool row_ok = row < rows;
-    int len = row_ok ? lengths[row] : 0;
-    len = max(0, min(len, (int)ld));
-    // CTA slice and warp sub-slices, starts aligned to 4 elements
-    const int per = ((len + C - 1) / C + 3) & ~3;
-    const int lo = min(len, crank * per);
-    const int hi = min(len, lo + per);
-    const int wper = ((hi - lo + kWarps - 1) / kWarps + 3) & ~3;
-    const int ws = min(hi, lo + warp * wper);
-    const int we = min(hi, ws + wper);
-    const float *rowp = logits + (size_t)(row_ok ? row : 0) * ld;
+    if (row >= rows)
+        return;
+    const int len = max(0, min(lengths[row], (int)ld));
+    // warp sub-slices, starts aligned to 4 elements
+    const int wper = ((len + kWarps - 1) / kWarps + 3) & ~3;
+    const int ws = min(len, warp * wper);
+    const int we = min(len, ws + wper);
+    const float *rowp = logits + (size_t)row * ld;
     const bool vec = vec_ok != 0;
 
     for (int i = tid; i < 2 * 2048; i += kThreads)
@@ -175,62 +159,58 @@ __global__ void __launch_bounds__(kThreads)
 
     // ---- pass 1: histogram of digit 1, count of valid keys
     uint32_t nvalid = 0;
-    for (int cb = ws; cb < we; cb += 128) {
-        uint32_t key[4];
-        load4(rowp, cb + 4 * lane, we, vec, key);
+    for (int cb = ws; cb < we; cb += kChunk) {
+        uint32_t key[kUnroll][4];
+        load_step(rowp, cb, we, vec, lane, key);
         #pragma unroll
-        for (int e = 0; e < 4; ++e)
-            if (key[e]) {
-                ++nvalid;
-                atomicAdd(&sh.hist[0][key[e] >> 21], 1u);
-            }
+        for (int u = 0; u < kUnroll; ++u)
+            #pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (key[u][e]) {
+                    ++nvalid;
+                    atomicAdd(&sh.hist[0][key[u][e] >> 21], 1u);
+                }
     }
-    for (int o = 16; o > 0; o >>= 1)
-        nvalid += __shfl_xor_sync(0xffffffffu, nvalid, o);
+    nvalid = warp_sum(nvalid);
     if (lane == 0)
         sh.wsum[warp] = nvalid;
     __syncthreads();
-    if (tid == 0) {
-        uint32_t t = 0;
-        for (int i = 0; i < kWarps; ++i)
-            t += sh.wsum[i];
-        sh.cta[0] = t;
-    }
-    cluster.sync();
     uint32_t total_valid = 0;
-    for (int r = 0; r < C; ++r)
-        total_valid += C == 1 ? sh.cta[0] : cluster.map_shared_rank(&sh, r)->cta[0];
+    for (int i = 0; i < kWarps; ++i)
+        total_valid += sh.wsum[i];
     const bool take_all = total_valid <= (uint32_t)k;
 
     uint32_t T = 0, ties = 0;
-    uint32_t my_gt = 0;  // this lane's share of its warp's keys above bin b1
+    uint32_t my_gt = 0;  // this lane's keys above bin b1
     bool overflow = false;
     if (!take_all) {
-        find_bin(cluster, sh, sh.hist[0], 2048, (uint32_t)k);
+        find_bin(sh, sh.hist[0], 2048, (uint32_t)k);
         const uint32_t b1 = sh.sel[0];
         uint32_t krem = sh.sel[1];
         // ---- pass 2: candidates of bin b1, count keys above it
-        for (int cb = ws; cb < we; cb += 128) {
-            uint32_t key[4];
-            load4(rowp, cb + 4 * lane, we, vec, key);
+        for (int cb = ws; cb < we; cb += kChunk) {
+            uint32_t key[kUnroll][4];
+            load_step(rowp, cb, we, vec, lane, key);
             #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const uint32_t d = key[e] >> 21;
-                my_gt += key[e] && d > b1;
-                const bool is_c = key[e] && d == b1;
-                const uint32_t ball = __ballot_sync(0xffffffffu, is_c);
-                if (ball) {
-                    uint32_t base = 0;
-                    if (lane == 0)
-                        base = atomicAdd(&sh.ncand, (uint32_t)__popc(ball));
-                    base = __shfl_sync(0xffffffffu, base, 0);
-                    const uint32_t pos = base + __popc(ball & ((1u << lane) - 1u));
-                    if (is_c && pos < (uint32_t)kCandCap) {
-                        sh.cand_key[pos] = key[e];
-                        sh.cand_idx[pos] = cb + 4 * lane + e;
+            for (int u = 0; u < kUnroll; ++u)
+                #pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const uint32_t d = key[u][e] >> 21;
+                    my_gt += key[u][e] && d > b1;
+                    const bool is_c = key[u][e] && d == b1;
+                    const uint32_t ball = __ballot_sync(0xffffffffu, is_c);
+                    if (ball) {
+                        uint32_t base = 0;
+                        if (lane == 0)
+                            base = atomicAdd(&sh.ncand, (uint32_t)__popc(ball));
+                        base = __shfl_sync(0xffffffffu, base, 0);
+                        const uint32_t pos = base + __popc(ball & ((1u << lane) - 1u));
+                        if (is_c && pos < (uint32_t)kCandCap) {
+                            sh.cand_key[pos] = key[u][e];
+                            sh.cand_idx[pos] = cb + 128 * u + 4 * lane + e;
+                        }
                     }
                 }
-            }
         }
         __syncthreads();
         const uint32_t ncand = sh.ncand;
@@ -251,17 +231,19 @@ __global__ void __launch_bounds__(kThreads)
                         atomicAdd(&h[(kk >> shift) & (uint32_t)(nb - 1)], 1u);
                 }
             } else {
-                for (int cb = ws; cb < we; cb += 128) {
-                    uint32_t key[4];
-                    load4(rowp, cb + 4 * lane, we, vec, key);
+                for (int cb = ws; cb < we; cb += kChunk) {
+                    uint32_t key[kUnroll][4];
+                    load_step(rowp, cb, we, vec, lane, key);
                     #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        if (key[e] && (key[e] & pmask) == prefix)
-                            atomicAdd(&h[(key[e] >> shift) & (uint32_t)(nb - 1)], 1u);
+                    for (int u = 0; u < kUnroll; ++u)
+                        #pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            if (key[u][e] && (key[u][e] & pmask) == prefix)
+                                atomicAdd(&h[(key[u][e] >> shift) & (uint32_t)(nb - 1)], 1u);
                 }
             }
-            cluster.sync();
-            find_bin(cluster, sh, h, nb, krem);
+            __syncthreads();
+            find_bin(sh, h, nb, krem);
             prefix |= sh.sel[0] << shift;
             pmask |= (uint32_t)(nb - 1) << shift;
             krem = sh.sel[1];
@@ -271,29 +253,28 @@ __global__ void __launch_bounds__(kThreads)
     }
 
     // ---- per-warp counts of keys > T and == T (T = 0 when every valid key fits)
-    uint32_t gt = 0, eq = 0;
     if (take_all || overflow) {
-        for (int cb = ws; cb < we; cb += 128) {
-            uint32_t key[4];
-            load4(rowp, cb + 4 * lane, we, vec, key);
+        uint32_t gt = 0, eq = 0;
+        for (int cb = ws; cb < we; cb += kChunk) {
+            uint32_t key[kUnroll][4];
+            load_step(rowp, cb, we, vec, lane, key);
             #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                gt += key[e] > T;
-                eq += key[e] == T && key[e];
-            }
+            for (int u = 0; u < kUnroll; ++u)
+                #pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    gt += key[u][e] > T;
+                    eq += key[u][e] == T && key[u][e];
+                }
         }
-        for (int o = 16; o > 0; o >>= 1) {
-            gt += __shfl_xor_sync(0xffffffffu, gt, o);
-            eq += __shfl_xor_sync(0xffffffffu, eq, o);
-        }
+        gt = warp_sum(gt);
+        eq = warp_sum(eq);
         if (lane == 0) {
             sh.wgt[warp] = gt;
             sh.weq[warp] = eq;
         }
         __syncthreads();
     } else {
-        for (int o = 16; o > 0; o >>= 1)
-            my_gt += __shfl_xor_sync(0xffffffffu, my_gt, o);
+        my_gt = warp_sum(my_gt);
         if (lane == 0) {
             sh.wgt[warp] = my_gt;
             sh.weq[warp] = 0;
@@ -302,7 +283,7 @@ __global__ void __launch_bounds__(kThreads)
         const uint32_t ncand = sh.ncand;
         for (uint32_t i = tid; i < ncand; i += kThreads) {
             const uint32_t kk = sh.cand_key[i];
-            const int wi = wper > 0 ? (sh.cand_idx[i] - lo) / wper : 0;
+            const int wi = sh.cand_idx[i] / wper;
             if (kk > T)
                 atomicAdd(&sh.wgt[wi], 1u);
             else if (kk == T)
@@ -310,89 +291,56 @@ __global__ void __launch_bounds__(kThreads)
         }
         __syncthreads();
     }
-    // block prefix over warps (index order), then cluster prefix over CTAs
-    if (tid == 0) {
-        uint32_t g = 0, e = 0;
-        for (int i = 0; i < kWarps; ++i) {
-            g += sh.wgt[i];
-            e += sh.weq[i];
-        }
-        sh.cta[1] = g;
-        sh.cta[2] = e;
-    }
-    cluster.sync();
-    uint32_t eq_before_cta = 0, sel_before_cta = 0, total_sel = 0, eq_run = 0;
-    for (int r = 0; r < C; ++r) {
-        const Shared *o = C == 1 ? &sh : cluster.map_shared_rank(&sh, r);
-        const uint32_t g = o->cta[1], e = o->cta[2];
+    // this warp's tie quota and output base (warps in index order)
+    uint32_t eq_run = 0, base = 0, total_sel = 0, quota = 0;
+    for (int i = 0; i < kWarps; ++i) {
+        const uint32_t e = sh.weq[i];
         const uint32_t take = eq_run >= ties ? 0u : min(e, ties - eq_run);
-        if (r < crank) {
-            sel_before_cta += g + take;
-            eq_before_cta += e;
-        }
-        total_sel += g + take;
+        if (i < warp)
+            base += sh.wgt[i] + take;
+        if (i == warp)
+            quota = take;
+        total_sel += sh.wgt[i] + take;
         eq_run += e;
     }
-    // this warp's tie quota and output base
-    uint32_t eq_before = eq_before_cta, base = sel_before_cta;
-    for (int i = 0; i < warp; ++i) {
-        const uint32_t e = sh.weq[i];
-        const uint32_t take = eq_before >= ties ? 0u : min(e, ties - eq_before);
-        base += sh.wgt[i] + take;
-        eq_before += e;
-    }
-    const uint32_t quota = eq_before >= ties ? 0u : min(sh.weq[warp], ties - eq_before);
 
     // ---- pass 3: ordered write of the selection
-    if (row_ok) {
-        int32_t *orow = out + (size_t)row * ld_out;
-        uint32_t written = 0, eq_seen = 0;
-        for (int cb = ws; cb < we; cb += 128) {
-            uint32_t key[4];
-            load4(rowp, cb + 4 * lane, we, vec, key);
+    int32_t *orow = out + (size_t)row * ld_out;
+    uint32_t written = 0, eq_seen = 0;
+    for (int cb = ws; cb < we; cb += kChunk) {
+        uint32_t key[kUnroll][4];
+        load_step(rowp, cb, we, vec, lane, key);
+        #pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
             uint32_t neq = 0;
             #pragma unroll
             for (int e = 0; e < 4; ++e)
-                neq += key[e] == T && key[e];
-            uint32_t eq_pre = neq;  // exclusive prefix of ties over lanes
-            for (int o = 1; o < 32; o <<= 1) {
-                uint32_t n = __shfl_up_sync(0xffffffffu, eq_pre, o);
-                if (lane >= o)
-                    eq_pre += n;
-            }
-            const uint32_t eq_tot = __shfl_sync(0xffffffffu, eq_pre, 31);
-            eq_pre -= neq;
-            uint32_t take[4], nt = 0, er = eq_seen + eq_pre;
+                neq += key[u][e] == T && key[u][e];
+            uint32_t eq_tot;
+            uint32_t er = eq_seen + warp_excl(neq, lane, &eq_tot);
+            uint32_t take[4], nt = 0;
             #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                bool t = key[e] > T;
-                if (key[e] == T && key[e]) {
+                bool t = key[u][e] > T;
+                if (key[u][e] == T && key[u][e]) {
                     t = er < quota;
                     ++er;
                 }
                 take[e] = t;
                 nt += t;
             }
-            uint32_t pre = nt;
-            for (int o = 1; o < 32; o <<= 1) {
-                uint32_t n = __shfl_up_sync(0xffffffffu, pre, o);
-                if (lane >= o)
-                    pre += n;
-            }
-            const uint32_t tot = __shfl_sync(0xffffffffu, pre, 31);
-            pre -= nt;
-            uint32_t pos = base + written + pre;
+            uint32_t tot;
+            uint32_t pos = base + written + warp_excl(nt, lane, &tot);
             #pragma unroll
             for (int e = 0; e < 4; ++e)
                 if (take[e])
-                    orow[pos++] = cb + 4 * lane + e;
+                    orow[pos++] = cb + 128 * u + 4 * lane + e;
             written += tot;
             eq_seen += eq_tot;
         }
-        for (int j = (int)total_sel + crank * kThreads + tid; j < k; j += C * kThreads)
-            orow[j] = -1;
     }
-    cluster.sync();  // no CTA leaves while another may still read its shared memory
+    for (int j = (int)total_sel + tid; j < k; j += kThreads)
+        orow[j] = -1;
 }
 
 } // namespace topk_detail

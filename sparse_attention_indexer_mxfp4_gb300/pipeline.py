@@ -104,9 +104,7 @@ class IndexerStep:
 
     @property
     def launches_per_step(self) -> int:
-        n = 1 + 1  # logits, top-k
-        if self.paged:
-            n += 3  # slot count, indptr scan, slot write
-            if self.case.cand is not None and not self.fused_mask:
-                n += 1
-        return n
+        calls = self._logits_calls + [self._topk_call]
+        if self._slots_call is not None:
+            calls.append(self._slots_call)
+        return sum(c.kernels for c in calls)

@@ -18,13 +18,14 @@ FAKE = 0x10000  # never dereferenced: every call below fails its host checks fir
 
 def _declared():
     text = open(HEADER).read()
-    return sorted(set(re.findall(r"^\s*(?:idx_status|const char \*)\s*(idx_\w+)\(", text, re.M)))
+    return sorted(set(re.findall(r"^\s*(?:idx_status|const char \*|size_t)\s*(idx_\w+)\(", text, re.M)))
 
 
 def test_header_declares_the_five_operations():
     names = _declared()
     for n in ["idx_mqa_logits", "idx_paged_mqa_logits", "idx_apply_candidate_mask", "idx_topk",
-              "idx_topk_to_ragged_slots", "idx_get_device_status", "idx_version"]:
+              "idx_topk_to_ragged_slots", "idx_get_device_status", "idx_version",
+              "idx_topk_workspace_size"]:
         assert n in names
 
 
@@ -94,3 +95,12 @@ def test_select_argument_checks():
     assert g(FAKE, 8, 2, 8, None, 0, FAKE, 10, 10, 64, 100, FAKE, FAKE, FAKE, None) == INVALID
     assert g(FAKE, 8, 2, 8, None, 1, FAKE, 10, 10, 0, 100, FAKE, FAKE, FAKE, None) == INVALID
     assert L.idx_get_device_status(None, None) == INVALID
+
+
+def test_topk_workspace_size_query():
+    f = B.topk_workspace_size
+    assert f(0, 1000, 10) == 0 and f(4, 0, 10) == 0
+    assert f(2, 8192 * 1024 + 1, 10) == 0          # more chunks than the path supports
+    one, two = f(3, 8192, 64), f(3, 8193, 64)       # 1 vs 2 chunks per row
+    assert 0 < one < two and two - one == 3 * 4 * 4  # four per-chunk words per row
+    assert f(6, 100000, 64) > f(3, 100000, 64)

@@ -15,10 +15,10 @@ def _t(a):
     return torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
 
-def gpu_topk(logits, lengths, k, ld_out=None):
+def gpu_topk(logits, lengths, k, ld_out=None, workspace=True):
     rows = logits.shape[0]
     out = torch.full((rows, ld_out or k), -7, dtype=torch.int32, device="cuda")
-    B.idx_topk(_t(logits), _t(lengths.astype(np.int32)), k, out)
+    B.idx_topk(_t(logits), _t(lengths.astype(np.int32)), k, out, workspace=workspace)
     torch.cuda.synchronize()
     return out.cpu().numpy()[:, :k]
 
@@ -34,24 +34,38 @@ def _random_logits(rng, rows, width, tie_levels=None, neg_inf_frac=0.1):
 
 @pytest.mark.parametrize("rows,width,k", [
     (1, 1, 1), (3, 100, 7), (16, 1024, 256), (5, 1000, 2048), (64, 8192, 2048),
-    (7, 65536, 2048), (2, 131072, 2048), (300, 4096, 256), (33, 20000, 1)])
-def test_topk_random(rows, width, k):
+    (7, 65536, 2048), (2, 131072, 2048), (300, 4096, 256), (33, 20000, 1), (4, 24577, 300)])
+@pytest.mark.parametrize("workspace", [True, False])
+def test_topk_random(rows, width, k, workspace):
     rng = np.random.default_rng(rows * 7 + width + k)
     x = _random_logits(rng, rows, width)
     lengths = rng.integers(0, width + 1, size=rows)
     lengths[0] = width
-    got = gpu_topk(x, lengths, k)
+    got = gpu_topk(x, lengths, k, workspace=workspace)
     assert_topk_exact(got, oracle.topk(x, lengths, k))
 
 
 @pytest.mark.parametrize("levels", [1, 2, 5, 300])
-def test_topk_ties_lowest_index_wins(levels):
+@pytest.mark.parametrize("workspace", [True, False])
+def test_topk_ties_lowest_index_wins(levels, workspace):
     rng = np.random.default_rng(levels)
     rows, width, k = 6, 50000, 2048
     x = _random_logits(rng, rows, width, tie_levels=levels, neg_inf_frac=0.05)
     lengths = np.full(rows, width)
     lengths[3] = 1000
-    got = gpu_topk(x, lengths, k)
+    got = gpu_topk(x, lengths, k, workspace=workspace)
+    assert_topk_exact(got, oracle.topk(x, lengths, k))
+
+
+@pytest.mark.parametrize("workspace", [True, False])
+def test_topk_candidate_overflow(workspace):
+    """Values packed into a narrow range put far more keys in the threshold
+    bin than either candidate list holds, forcing the streaming fallback."""
+    rng = np.random.default_rng(77)
+    rows, width, k = 3, 100000, 2048
+    x = (1.0 + rng.random((rows, width)) * 1e-3).astype(np.float32)
+    lengths = np.array([100000, 70000, 30000])
+    got = gpu_topk(x, lengths, k, workspace=workspace)
     assert_topk_exact(got, oracle.topk(x, lengths, k))
 
 
