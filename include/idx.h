@@ -182,6 +182,35 @@ idx_status idx_topk(const float *logits, int64_t ld, int rows, const int32_t *le
 size_t idx_topk_workspace_size(int rows, int64_t ld, int k);
 
 /* ------------------------------------------------------------------------
+ * idx_topk_noalloc -- idx_topk without caller scratch.
+ * The pages have no counterpart of this call: it is a library convenience.
+ * It exists for callers that cannot hand over device scratch or allocate it
+ * at call time: a serving engine that reserves nearly all free device
+ * memory for its KV cache at start-up and allows no allocation afterwards,
+ * a latency-critical loop where cudaMalloc / cudaFree may synchronise the
+ * device, or a plain C caller with no device allocator of its own.
+ *
+ *   Same arguments and results as idx_topk, always on the chunked path.
+ *   Its scratch is one fixed array of IDX_TOPK_NOALLOC_MAX_BYTES per device,
+ *   part of the library's device image: the call allocates nothing.  The
+ *   first call on a device looks up that array's address (with the device
+ *   current); make that first call before any stream capture on the device.
+ *   Every call clears the part of the array that must start at zero
+ *   (cudaMemsetAsync on `stream`) before its kernels run.
+ *   Calls on one device share the array: two calls that overlap in time
+ *   (different streams, not ordered by events) race and give wrong indices.
+ * Errors: as idx_topk; IDX_ERR_WORKSPACE when
+ *   idx_topk_workspace_size(rows, ld, k) > IDX_TOPK_NOALLOC_MAX_BYTES (about
+ *   450 rows of 131072 keys), IDX_ERR_UNSUPPORTED when it is 0 for rows > 0
+ *   (ld above 8192 * 1024); IDX_ERR_CUDA when the address lookup or a launch
+ *   fails.
+ * ---------------------------------------------------------------------- */
+#define IDX_TOPK_NOALLOC_MAX_BYTES (32u << 20)
+
+idx_status idx_topk_noalloc(const float *logits, int64_t ld, int rows, const int32_t *lengths,
+                            int k, int32_t *out_idx, int64_t ld_out, idx_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * idx_topk_to_ragged_slots -- top-k positions to a ragged list of cache slots.
  * Passage: rocm_aiter_mla_sparse, build_prefill_topk_ragged_indices; the
  * slot of position p is block_table[b, p / page_size] * page_size +

@@ -36,6 +36,7 @@ _SIGNATURES = {
                              _P, _L, _I, _I, _P, _L, _I, _I, _P, _S, _P],
     "idx_apply_candidate_mask": [_P, _L, _I, _I, _P, _P, _P, _L, _I, _I, _I, _P],
     "idx_topk": [_P, _L, _I, _P, _I, _P, _L, _P, _S, _P],
+    "idx_topk_noalloc": [_P, _L, _I, _P, _I, _P, _L, _P],
     "idx_topk_to_ragged_slots": [_P, _L, _I, _I, _P, _I, _P, _L, _I, _I, _I, _P, _P, _P, _P],
     "idx_get_device_status": [_P, ctypes.POINTER(ctypes.c_uint32)],
 }
@@ -233,6 +234,19 @@ def idx_topk(logits, lengths, k, out, stream=None, workspace=True):
     """out int32 [rows, >= k]: ascending indices of the k largest finite logits
     of each row within [0, lengths[r]), -1 padded."""
     prepare_topk(logits, lengths, k, out, workspace)(stream)
+
+
+def idx_topk_noalloc(logits, lengths, k, out, stream=None):
+    """idx_topk over the library's fixed per-device scratch array: no
+    allocation, no workspace argument; calls on one device must not overlap."""
+    if logits.dtype != torch.float32 or logits.stride(1) != 1:
+        raise ValueError("logits must be float32 with unit column stride")
+    _need(lengths, torch.int32, "lengths")
+    if out.dtype != torch.int32 or out.stride(1) != 1:
+        raise ValueError("out must be int32 with unit column stride")
+    rc = lib().idx_topk_noalloc(_ptr(logits), logits.stride(0), logits.shape[0], _ptr(lengths),
+                                k, _ptr(out), out.stride(0), _stream(stream))
+    _check(rc, "idx_topk_noalloc")
 
 
 def prepare_topk_to_ragged_slots(topk, block_table, page_size, num_pages, slots, indptr, lens,

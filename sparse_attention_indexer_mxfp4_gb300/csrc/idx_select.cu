@@ -3,6 +3,7 @@
 // top-k -> ragged slot map, with their C ABI entry points.
 #include <algorithm>
 #include <cstdint>
+#include <mutex>
 
 #include "idx_internal.h"
 #include "idx_topk.cuh"
@@ -340,4 +341,61 @@ extern "C" idx_status idx_topk_to_ragged_slots(const int32_t *topk, int64_t ld, 
                                                     block_table, bt_stride, max_blocks,
                                                     page_size, num_pages, indptr, slots);
     return launch_status(cudaGetLastError());
+}
+
+// ------------------------------------------------ top-k without allocation
+//
+// idx_topk_noalloc runs the chunked top-k over one fixed array per device
+// instead of caller scratch, for callers that can neither pass scratch nor
+// allocate it when they call.  The array is part of this library's device
+// image; its address is looked up once per device, with that device
+// current, and cached.
+
+static __device__ __align__(256) unsigned char g_topk_scratch[IDX_TOPK_NOALLOC_MAX_BYTES];
+
+namespace {
+
+std::mutex g_scratch_mu;
+void *g_scratch_ptr[64];
+
+idx_status topk_scratch(void **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return IDX_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_topk_scratch) != cudaSuccess || !p)
+            return IDX_ERR_CUDA;
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return IDX_OK;
+}
+
+} // namespace
+
+extern "C" idx_status idx_topk_noalloc(const float *logits, int64_t ld, int rows,
+                                       const int32_t *lengths, int k, int32_t *out_idx,
+                                       int64_t ld_out, idx_stream_t stream)
+{
+    if (rows < 0 || k < 0 || ld < 0 || ld_out < k || ld > INT32_MAX)
+        return IDX_ERR_INVALID_ARG;
+    if (rows == 0 || k == 0)
+        return IDX_OK;
+    if (!logits || !lengths || !out_idx || ld <= 0)
+        return IDX_ERR_INVALID_ARG;
+    const size_t need = idx_topk_workspace_size(rows, ld, k);
+    if (need == 0)
+        return IDX_ERR_UNSUPPORTED;
+    if (need > (size_t)IDX_TOPK_NOALLOC_MAX_BYTES)
+        return IDX_ERR_WORKSPACE;
+    void *ws = nullptr;
+    const idx_status st = topk_scratch(&ws);
+    if (st != IDX_OK)
+        return st;
+    const int vec_ok = (ld % 4 == 0) && aligned16(logits);
+    return topk_launch_chunked(logits, ld, rows, lengths, k, out_idx, ld_out, ws, vec_ok,
+                               (cudaStream_t)stream);
 }
