@@ -162,8 +162,11 @@ idx_status idx_apply_candidate_mask(float *logits, int64_t ld, int rows, int wid
  *   ws, ws_bytes  optional caller-owned device scratch, 16-byte aligned.
  *           With ws_bytes >= idx_topk_workspace_size(rows, ld, k) and
  *           ld > 8192, each row is cut into chunks of 8192 keys and the
- *           selection runs as five launches spread over the whole GPU (the
- *           first clears part of ws with cudaMemsetAsync on `stream`).
+ *           selection runs over the whole GPU as two launches: a plan
+ *           kernel that clears the part of ws that must start at zero, then
+ *           one cooperative launch whose phases meet at grid barriers (each
+ *           wait is bounded; a timeout sets IDX_DEV_TIMEOUT in the device
+ *           status and leaves the output undefined).
  *           Otherwise (ws NULL or too small) one CTA selects each row.  Both
  *           give the same indices.  Calls that share one ws must not overlap
  *           in time (same stream, or ordered by events); ws holds nothing
@@ -195,8 +198,8 @@ size_t idx_topk_workspace_size(int rows, int64_t ld, int k);
  *   part of the library's device image: the call allocates nothing.  The
  *   first call on a device looks up that array's address (with the device
  *   current); make that first call before any stream capture on the device.
- *   Every call clears the part of the array that must start at zero
- *   (cudaMemsetAsync on `stream`) before its kernels run.
+ *   Every call clears the part of the array that must start at zero (its
+ *   first kernel, on `stream`) before the others run.
  *   Calls on one device share the array: two calls that overlap in time
  *   (different streams, not ordered by events) race and give wrong indices.
  * Errors: as idx_topk; IDX_ERR_WORKSPACE when

@@ -224,10 +224,10 @@ def prepare_topk(logits, lengths, k, out, workspace=True):
         ws = workspace
     nbytes = 0 if ws is None else ws.numel() * ws.element_size()
     args = (_ptr(logits), ld, rows, _ptr(lengths), k, _ptr(out), out.stride(0), _ptr(ws), nbytes)
-    # the library takes the chunked path (five kernels) under these conditions
+    # the library takes the chunked path (two kernels) under these conditions
     need = topk_workspace_size(rows, ld, k)
     chunked = ws is not None and need > 0 and nbytes >= need and ld > 8192
-    return Prepared("idx_topk", args, (logits, lengths, out, ws), 5 if chunked else 1)
+    return Prepared("idx_topk", args, (logits, lengths, out, ws), 2 if chunked else 1)
 
 
 def idx_topk(logits, lengths, k, out, stream=None, workspace=True):

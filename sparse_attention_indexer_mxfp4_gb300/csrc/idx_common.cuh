@@ -81,7 +81,7 @@ IDX_DEVFN bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint
 }
 
 // Slow path of mbar_wait, kept out of line so every call site stays small.
-__device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, volatile int *abort,
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, volatile int *abort,
                                             unsigned int *status, uint64_t limit_ns)
 {
     uint64_t t0 = globaltimer_ns();
@@ -285,6 +285,22 @@ IDX_DEVFN uint64_t make_smem_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t s
 }
 
 // ------------------------------------------------------------- misc helpers
+
+// Two fp32 fused multiply-adds in one packed instruction: (a * b + c) per
+// lane, each rounded to nearest like fmaf.
+IDX_DEVFN float2 fma2(float2 a, float2 b, float2 c)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "mov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
 
 IDX_DEVFN void named_bar_sync(int id, int nthreads)
 {

@@ -511,16 +511,32 @@ __global__ void __launch_bounds__(kLogitsThreads, 1)
                                 s4[2] = fmaf(wv.z, fmaxf(ksc * qv.z * x[2], 0.0f), s4[2]);
                                 s4[3] = fmaf(wv.w, fmaxf(ksc * qv.w * x[3], 0.0f), s4[3]);
                             }
-                        } else {
-                            const float sg = all_pos ? 1.0f : sgn;
+                        } else if (all_pos) {
+                            // the same four partial sums as below, two per
+                            // packed FMA: bit-identical results
+                            float2 s01 = make_float2(0.0f, 0.0f), s23 = s01;
                             #pragma unroll
                             for (int h4 = 0; h4 < H / 4; ++h4) {
                                 const float4 wv = w4[h4];
                                 const float *x = reinterpret_cast<const float *>(&r[ii * H + 4 * h4]);
-                                s4[0] = fmaf(wv.x, fmaxf(sg * x[0], 0.0f), s4[0]);
-                                s4[1] = fmaf(wv.y, fmaxf(sg * x[1], 0.0f), s4[1]);
-                                s4[2] = fmaf(wv.z, fmaxf(sg * x[2], 0.0f), s4[2]);
-                                s4[3] = fmaf(wv.w, fmaxf(sg * x[3], 0.0f), s4[3]);
+                                s01 = fma2(make_float2(wv.x, wv.y),
+                                           make_float2(fmaxf(x[0], 0.0f), fmaxf(x[1], 0.0f)), s01);
+                                s23 = fma2(make_float2(wv.z, wv.w),
+                                           make_float2(fmaxf(x[2], 0.0f), fmaxf(x[3], 0.0f)), s23);
+                            }
+                            s4[0] = s01.x;
+                            s4[1] = s01.y;
+                            s4[2] = s23.x;
+                            s4[3] = s23.y;
+                        } else {
+                            #pragma unroll
+                            for (int h4 = 0; h4 < H / 4; ++h4) {
+                                const float4 wv = w4[h4];
+                                const float *x = reinterpret_cast<const float *>(&r[ii * H + 4 * h4]);
+                                s4[0] = fmaf(wv.x, fmaxf(sgn * x[0], 0.0f), s4[0]);
+                                s4[1] = fmaf(wv.y, fmaxf(sgn * x[1], 0.0f), s4[1]);
+                                s4[2] = fmaf(wv.z, fmaxf(sgn * x[2], 0.0f), s4[2]);
+                                s4[3] = fmaf(wv.w, fmaxf(sgn * x[3], 0.0f), s4[3]);
                             }
                         }
                         const float sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);

@@ -216,36 +216,69 @@ idx_status topk_launch_per_row(const float *logits, int64_t ld, int rows,
     return launch_status(cudaGetLastError());
 }
 
-// Five launches over the caller's workspace; see idx_topk_chunked.cuh.
+// Chunked top-k over the caller's workspace: the plan kernel, then one
+// cooperative launch of the phases (see idx_topk_chunked.cuh).  Returns
+// IDX_ERR_UNSUPPORTED when the device has no cooperative launch.
 idx_status topk_launch_chunked(const float *logits, int64_t ld, int rows,
                                const int32_t *lengths, int k, int32_t *out, int64_t ld_out,
                                void *ws, int vec_ok, cudaStream_t s)
 {
     namespace C = topk_chunked;
-    const int P = (int)((ld + C::kCh - 1) / C::kCh);
-    const C::Ws w = C::ws_carve(ws, rows, P);
-    const size_t rsmem = sizeof(C::ResolveShared);
-    static int configured[64] = {};
+    static int grid_per_sm[64] = {};  // resident phase CTAs per SM, 0 = not known yet
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return IDX_ERR_CUDA;
-    if (!configured[dev]) {
-        if (cudaFuncSetAttribute(C::resolve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)rsmem) != cudaSuccess)
+    if (!grid_per_sm[dev]) {
+        int coop = 0, n = 0;
+        if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess)
             return IDX_ERR_CUDA;
-        configured[dev] = 1;
+        if (!coop)
+            return IDX_ERR_UNSUPPORTED;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, C::phases_kernel, C::kThreads, 0) !=
+                cudaSuccess ||
+            n < 1)
+            return IDX_ERR_CUDA;
+        grid_per_sm[dev] = n;
     }
-    if (cudaMemsetAsync(ws, 0, C::ws_zeroed_bytes(rows), s) != cudaSuccess)
+    unsigned int *status = device_status_ptr();
+    if (!status)
         return IDX_ERR_CUDA;
-    const unsigned cgrid = (unsigned)rows * (unsigned)P;
-    C::hist_kernel<<<cgrid, C::kThreads, 0, s>>>(logits, ld, lengths, P, w, vec_ok);
-    C::pick_kernel<<<rows, C::kRowThreads, 0, s>>>(k, w);
-    C::filter_kernel<<<cgrid, C::kThreads, 0, s>>>(logits, ld, lengths, P, w, vec_ok);
-    C::resolve_kernel<<<rows, C::kRowThreads, rsmem, s>>>(logits, ld, lengths, k, P, w, out,
-                                                          ld_out, vec_ok);
-    C::write_kernel<<<cgrid, C::kThreads, 0, s>>>(logits, ld, lengths, P, w, out, ld_out,
-                                                  vec_ok);
-    return launch_status(cudaGetLastError());
+    const int P = (int)((ld + C::kCh - 1) / C::kCh);
+    C::PhaseArgs a;
+    a.logits = logits;
+    a.ld = ld;
+    a.lengths = lengths;
+    a.R = rows;
+    a.P = P;
+    a.k = k;
+    a.out = out;
+    a.ld_out = ld_out;
+    a.vec_ok = vec_ok;
+    a.status = status;
+    C::ws_layout(ws, rows, P, &a.ws);
+    const long long zero_vec4 = ((long long)rows * (2048 + 2) + 3) / 4;
+    const int g_plan = (int)std::max<long long>(
+        1, std::min<long long>(sm_count(), (zero_vec4 + C::kPlanThreads - 1) / C::kPlanThreads));
+    C::plan_kernel<<<g_plan, C::kPlanThreads, 0, s>>>(lengths, ld, rows, a.ws);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return IDX_ERR_CUDA;
+    // every CTA resident (the phases wait on one another), no more CTAs
+    // than there can be items or rows
+    const long long cap = (long long)grid_per_sm[dev] * sm_count();
+    const long long want = std::max<long long>((long long)rows * P, rows);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)std::max<long long>(1, std::min(cap, want)));
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, C::phases_kernel, a);
+    return launch_status(e);
 }
 
 } // namespace
@@ -278,8 +311,12 @@ extern "C" idx_status idx_topk(const float *logits, int64_t ld, int rows, const 
     const int vec_ok = (ld % 4 == 0) && aligned16(logits);
     cudaStream_t s = (cudaStream_t)stream;
     const size_t need = idx_topk_workspace_size(rows, ld, k);
-    if (ws && need > 0 && ws_bytes >= need && aligned16(ws) && ld > topk_chunked::kCh)
-        return topk_launch_chunked(logits, ld, rows, lengths, k, out_idx, ld_out, ws, vec_ok, s);
+    if (ws && need > 0 && ws_bytes >= need && aligned16(ws) && ld > topk_chunked::kCh) {
+        const idx_status st =
+            topk_launch_chunked(logits, ld, rows, lengths, k, out_idx, ld_out, ws, vec_ok, s);
+        if (st != IDX_ERR_UNSUPPORTED)
+            return st;
+    }
     return topk_launch_per_row(logits, ld, rows, lengths, k, out_idx, ld_out, vec_ok, s);
 }
 

@@ -65,15 +65,52 @@ __device__ __forceinline__ void load4(const float *row, int i0, int end, bool ve
     }
 }
 
+// Keys of U runs of four elements, run u starting at base + u * stride (0
+// past `end`).  Every load is issued before any key is formed, so the U
+// memory round trips overlap: float4 loads where the whole run is in range
+// and the row allows them, scalar loads for the rest.
+template <int U>
+__device__ __forceinline__ void load_keys(const float *row, int base, int stride, int end, bool vec,
+                                          uint32_t (&k)[U][4])
+{
+    float4 v[U];
+    #pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int i0 = base + u * stride;
+        v[u] = make_float4(NAN, NAN, NAN, NAN);
+        if (vec && i0 + 3 < end)
+            v[u] = __ldg(reinterpret_cast<const float4 *>(row + i0));
+    }
+    #pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int i0 = base + u * stride;
+        if (!(vec && i0 + 3 < end)) {
+            if (i0 < end)
+                v[u].x = __ldg(row + i0);
+            if (i0 + 1 < end)
+                v[u].y = __ldg(row + i0 + 1);
+            if (i0 + 2 < end)
+                v[u].z = __ldg(row + i0 + 2);
+            if (i0 + 3 < end)
+                v[u].w = __ldg(row + i0 + 3);
+        }
+    }
+    #pragma unroll
+    for (int u = 0; u < U; ++u) {
+        k[u][0] = float_key(v[u].x);
+        k[u][1] = float_key(v[u].y);
+        k[u][2] = float_key(v[u].z);
+        k[u][3] = float_key(v[u].w);
+    }
+}
+
 // One warp step: the keys of elements cb + 128u + 4*lane + e (u < kUnroll,
 // e < 4), all loads issued before any is used.  Element order within the
 // step is (u, lane, e).
 __device__ __forceinline__ void load_step(const float *row, int cb, int end, bool vec, int lane,
                                           uint32_t (&k)[kUnroll][4])
 {
-    #pragma unroll
-    for (int u = 0; u < kUnroll; ++u)
-        load4(row, cb + 128 * u + 4 * lane, end, vec, k[u]);
+    load_keys<kUnroll>(row, cb + 4 * lane, 128, end, vec, k);
 }
 
 // Sum of a value over the warp.
@@ -132,7 +169,7 @@ __device__ __forceinline__ void find_bin(Shared &sh, const uint32_t *h, int nb, 
     __syncthreads();
 }
 
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 2)
     topk_kernel(const float *__restrict__ logits, int64_t ld, int rows,
                 const int32_t *__restrict__ lengths, int k, int32_t *__restrict__ out,
                 int64_t ld_out, int vec_ok)

@@ -102,5 +102,5 @@ def test_topk_workspace_size_query():
     assert f(0, 1000, 10) == 0 and f(4, 0, 10) == 0
     assert f(2, 8192 * 1024 + 1, 10) == 0          # more chunks than the path supports
     one, two = f(3, 8192, 64), f(3, 8193, 64)       # 1 vs 2 chunks per row
-    assert 0 < one < two and two - one == 3 * 4 * 4  # four per-chunk words per row
+    assert 0 < one < two and two - one == 3 * 8 * 4  # eight per-chunk words per row
     assert f(6, 100000, 64) > f(3, 100000, 64)
