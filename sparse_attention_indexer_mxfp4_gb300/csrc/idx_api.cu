@@ -115,7 +115,7 @@ cudaError_t launch_logits_t(const LogitsArgs &a, const CUtensorMap &tmK, const C
             return e;
         configured[dev] = 1;
     }
-    kern<<<nctas, kLogitsThreads, smem, stream>>>(a, tmK, tmQ, tmS);
+    kern<<<nctas, C::THREADS, smem, stream>>>(a, tmK, tmQ, tmS);
     return cudaGetLastError();
 }
 
@@ -136,13 +136,13 @@ cudaError_t launch_logits(int fmt, int H, int G, const LogitsArgs &a, const CUte
     if (H == 64 && fmt == kFmtFp8) {
         switch (G) {
         case 1: return launch_logits_t<kFmtFp8, 64, 1, 8, 2>(a, tmK, tmQ, tmS, nctas, s);
-        case 2: return launch_logits_t<kFmtFp8, 64, 2, 8, 2>(a, tmK, tmQ, tmS, nctas, s);
+        case 2: return launch_logits_t<kFmtFp8, 64, 2, 6, 3>(a, tmK, tmQ, tmS, nctas, s);
         case 4: return launch_logits_t<kFmtFp8, 64, 4, 8, 2>(a, tmK, tmQ, tmS, nctas, s);
         }
     } else if (H == 64 && fmt == kFmtMxfp4) {
         switch (G) {
         case 1: return launch_logits_t<kFmtMxfp4, 64, 1, 16, 2>(a, tmK, tmQ, tmS, nctas, s);
-        case 2: return launch_logits_t<kFmtMxfp4, 64, 2, 16, 2>(a, tmK, tmQ, tmS, nctas, s);
+        case 2: return launch_logits_t<kFmtMxfp4, 64, 2, 12, 3>(a, tmK, tmQ, tmS, nctas, s);
         }
     }
     *supported = false;
@@ -154,13 +154,13 @@ size_t logits_smem(int fmt, int H, int G, int cand_words)
     if (H == 64 && fmt == kFmtFp8) {
         switch (G) {
         case 1: return logits_smem_t<kFmtFp8, 64, 1, 8, 2>(cand_words);
-        case 2: return logits_smem_t<kFmtFp8, 64, 2, 8, 2>(cand_words);
+        case 2: return logits_smem_t<kFmtFp8, 64, 2, 6, 3>(cand_words);
         case 4: return logits_smem_t<kFmtFp8, 64, 4, 8, 2>(cand_words);
         }
     } else if (H == 64 && fmt == kFmtMxfp4) {
         switch (G) {
         case 1: return logits_smem_t<kFmtMxfp4, 64, 1, 16, 2>(cand_words);
-        case 2: return logits_smem_t<kFmtMxfp4, 64, 2, 16, 2>(cand_words);
+        case 2: return logits_smem_t<kFmtMxfp4, 64, 2, 12, 3>(cand_words);
         }
     }
     return 0;
@@ -366,6 +366,10 @@ extern "C" idx_status idx_paged_mqa_logits(
     a.cand_stride = cand_stride;
     a.num_cand = num_cand;
     a.cand_block = cand_block;
+    a.cand_shift = -1;
+    for (int b = 0; b < 31; ++b)
+        if ((1 << b) == cand_block)
+            a.cand_shift = b;
     a.cand_words = cand_words;
     a.logits = logits;
     a.ld = ld_logits;

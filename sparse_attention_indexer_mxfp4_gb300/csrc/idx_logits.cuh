@@ -57,6 +57,7 @@ struct LogitsArgs {
     int64_t cand_stride;
     int num_cand;
     int cand_block;
+    int cand_shift;          // log2(cand_block) if a power of two, else -1
     int cand_words;          // 32-bit words of one row's candidate bitmap
     // output
     float *logits;

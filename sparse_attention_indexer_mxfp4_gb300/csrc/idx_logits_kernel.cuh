@@ -1,22 +1,23 @@
 // idx_logits_kernel.cuh -- the warp-specialised tcgen05 logits kernel.
 //
-// One persistent CTA per SM, 6 warps:
-//   warp 0    producer: TMA loads of K tiles (page by page through the block
-//             table) into a ring of shared-memory stages, and of each row
-//             group's Q tile, weights and scales into one of two group slots.
-//             The warp's 32 lanes resolve the pages of 16 tiles at a time
-//             (one half-tile each), one window ahead, so a tile costs only a
-//             barrier wait and two TMA issues;
-//   warp 1    MMA issuer: owns the TMEM allocation and issues the tcgen05 MMAs
-//             S[t, (r,h)] = k[t,:] . q[r,h,:] with keys on M (128 lanes) and
-//             the group's (row, head) pairs on N;
-//   warps 2-9 epilogue, two warpgroups taking alternate tiles (one TMEM
-//             accumulator each): thread i of a warpgroup owns TMEM lane i, i.e. one
-//             key, and reduces  sum_h w[r,h] * relu(scale * S[t,(r,h)])  over the
-//             heads in registers, applies the [ks, ke) and candidate masks and
-//             stores the fp32 logit.  Per-head scores never leave TMEM and
-//             registers.  Each thread fetches its key's scale itself, two
-//             tiles ahead, so the load latency hides behind the work.
+// One persistent CTA per SM, warp-specialised:
+//   producers (warps 0-1, even / odd tiles): TMA loads of each 128-key tile
+//             (values and key scales, page by page through the block table)
+//             into a ring of shared-memory stages; warp 0 also loads each row
+//             group's Q tile, weights and scales into one of two group slots
+//             and builds the group's candidate bitmap.  The 32 lanes resolve
+//             the pages of 16 tiles at a time (one half-tile each), one window
+//             ahead, so a tile costs a barrier wait and a few TMA issues;
+//   MMA issuers (warps 2-3): one elected lane issues the tcgen05 MMAs
+//             S[t, (r,h)] = k[t,:] . q[r,h,:] with keys on M (128 TMEM lanes)
+//             and the group's (row, head) pairs on N, into one of NA TMEM
+//             accumulators; warp 2 owns the TMEM allocation;
+//   epilogue  NA warpgroups, one per accumulator: thread i of a warpgroup
+//             owns TMEM lane i, i.e. one key, and reduces
+//             sum_h w[r,h] * relu(scale * S[t,(r,h)]) over the heads in
+//             registers, applies the [ks, ke) and candidate masks and stores
+//             the fp32 logit.  Per-head scores never leave TMEM and registers;
+//             the key's scale comes from the stage.
 // Stages, group slots and accumulators are handed over with mbarriers whose
 // waits are all bounded (mbar_wait), so a broken pipeline ends the kernel
 // with IDX_DEV_TIMEOUT instead of hanging.
@@ -29,15 +30,14 @@ namespace idx {
 
 constexpr int kFmtFp8 = 0;
 constexpr int kFmtMxfp4 = 1;
-// Warp roles: 0-1 producers (even / odd tiles), 2-3 MMA issuers (even / odd
-// tiles, i.e. TMEM accumulator 0 / 1), 4-11 epilogue (two warpgroups, one
-// per accumulator).  Every SMSP (warp % 4) runs one control warp and two
-// epilogue warps, and the per-tile issue cost of each control role is
-// split over two warps.
-constexpr int kEpiWarps = 8;
+// Warp roles: 0-1 producers (even / odd tiles), 2-3 MMA issuers, 4..
+// epilogue (NA warpgroups).  Tile c goes to TMEM accumulator c % NA, which
+// MMA warp (c % NA) & 1 fills and epilogue warpgroup c % NA drains, so every
+// accumulator has one filler and one drainer.  Every SMSP (warp % 4) runs one
+// control warp and NA epilogue warps, and the per-tile issue cost of each
+// control role is split over two warps.
 constexpr int kFirstEpiWarp = 4;
 constexpr int kMmaWarp = 2;
-constexpr int kLogitsThreads = 32 * (kFirstEpiWarp + kEpiWarps);
 constexpr int kWinTiles = 16;  // tiles whose pages the producer resolves at once (32 halves)
 
 template <int FMT, int H, int G, int S, int NA>
@@ -79,9 +79,17 @@ struct LogitsCfg {
     static_assert(TM_USED <= 512, "accumulators do not fit in tensor memory");
     static_assert(NCOLS % 16 == 0 && NCOLS >= 16 && NCOLS <= 256, "MMA N out of range");
     static_assert(H % 32 == 0, "heads are read from TMEM 32 columns at a time");
-    static_assert(NA == 2, "one TMEM accumulator per epilogue warpgroup");
-    static_assert((S & (S - 1)) == 0 && S >= 2, "stage count must be a power of two");
-    static constexpr int LOG2S = S == 2 ? 1 : S == 4 ? 2 : S == 8 ? 3 : S == 16 ? 4 : 5;
+    static_assert(NA == 2 || NA == 3, "two or three epilogue warpgroups");
+    static constexpr int EPI_WARPS = 4 * NA;
+    static constexpr int THREADS = 32 * (kFirstEpiWarp + EPI_WARPS);
+    // Tile c uses stage c % S.  S a multiple of 2 and of NA keeps every stage
+    // (and every accumulator) with one producer, one MMA warp and one
+    // epilogue warpgroup, each of which waits on every phase of it in turn:
+    // a role that could skip a phase might wait one phase early, and an
+    // mbarrier parity wait cannot tell phase n from phase n + 2.
+    static_assert(S >= 2 && S % 2 == 0 && S % NA == 0, "stages must divide among the roles");
+    __host__ __device__ static constexpr int stage(int c) { return c % S; }
+    __host__ __device__ static constexpr uint32_t phase(int c) { return (uint32_t)(c / S) & 1u; }
     // instruction descriptor: fp32 accumulate, K-major A and B, M = 128, N = NCOLS
     __host__ __device__ static constexpr uint32_t idesc_f8()
     {
@@ -133,7 +141,7 @@ __device__ __forceinline__ HalfInfo half_info(const LogitsArgs &a, const GroupIn
 namespace idx {
 
 template <int FMT, int H, int G, int S, int NA>
-__global__ void __launch_bounds__(kLogitsThreads, 1)
+__global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA>::THREADS, 1)
     logits_kernel(const __grid_constant__ LogitsArgs a, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmS)
 {
@@ -164,7 +172,7 @@ __global__ void __launch_bounds__(kLogitsThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&q_full[i], 1);
-            mbar_init(&q_empty[i], 2 + kEpiWarps);  // both MMA warps' commits + epilogue
+            mbar_init(&q_empty[i], 2 + C::EPI_WARPS);  // both MMA warps' commits + epilogue
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -273,8 +281,8 @@ __global__ void __launch_bounds__(kLogitsThreads, 1)
                 }
                 cur_ok = true;
             }
-            const int s = c & (S - 1);
-            if (!mbar_wait(&empty[s], (uint32_t)((c >> C::LOG2S) & 1) ^ 1, abort_flag, a.status))
+            const int s = C::stage(c);
+            if (!mbar_wait(&empty[s], C::phase(c) ^ 1, abort_flag, a.status))
                 break;
             const int h0 = 2 * (w.j - win0);  // lanes h0, h0 + 1 own this tile's halves
             const uint32_t ball = __ballot_sync(0xffffffffu, cur.need);
@@ -304,7 +312,7 @@ __global__ void __launch_bounds__(kLogitsThreads, 1)
         if (!*abort_flag) {
             for (int i = c > S ? c - S : 0; i < c; ++i)
                 if ((i & 1) == pw &&
-                    !mbar_wait(&empty[i & (S - 1)], (uint32_t)((i >> C::LOG2S) & 1), abort_flag,
+                    !mbar_wait(&empty[C::stage(i)], C::phase(i), abort_flag,
                                a.status))
                     break;
             for (int i = gq > 2 ? gq - 2 : 0; i < gq; ++i)
@@ -313,7 +321,7 @@ __global__ void __launch_bounds__(kLogitsThreads, 1)
         }
     } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
         // ------------------------------------------------------------ MMA issuers
-        const int mw = warp - kMmaWarp;  // issues tiles c % 2 == mw into accumulator mw
+        const int mw = warp - kMmaWarp;  // issues the tiles with (c % NA) & 1 == mw
         int gq = 0;
         int c = 0;
         int slot = 0;
@@ -352,14 +360,14 @@ __global__ void __launch_bounds__(kLogitsThreads, 1)
                 }
                 ++gq;
             }
-            if (tile_is_compute(w.gi, w.j) && (c & 1) != mw) {
+            if (tile_is_compute(w.gi, w.j) && ((c % NA) & 1) != mw) {
                 ++c;  // the other MMA warp's tile
             } else if (tile_is_compute(w.gi, w.j)) {
-                const int acc = mw;
-                const int s = c & (S - 1);
-                if (!mbar_wait(&acc_empty[acc], (uint32_t)((c >> 1) & 1) ^ 1, abort_flag, a.status))
+                const int acc = c % NA;
+                const int s = C::stage(c);
+                if (!mbar_wait(&acc_empty[acc], (uint32_t)((c / NA) & 1) ^ 1, abort_flag, a.status))
                     break;
-                if (!mbar_wait(&full[s], (uint32_t)((c >> C::LOG2S) & 1), abort_flag, a.status))
+                if (!mbar_wait(&full[s], C::phase(c), abort_flag, a.status))
                     break;
                 uint8_t *st = smem + C::OFF_STAGE + s * C::STAGE_BYTES;
                 if constexpr (FMT == kFmtMxfp4) {
@@ -414,8 +422,8 @@ __global__ void __launch_bounds__(kLogitsThreads, 1)
         }
     } else if (warp >= kFirstEpiWarp) {
         // ------------------------------------------------------------ epilogue
-        // Two warpgroups; warpgroup wg owns accumulator wg, i.e. the compute
-        // tiles with c % 2 == wg, and every other fill tile.
+        // NA warpgroups; warpgroup wg owns accumulator wg, i.e. the compute
+        // tiles with c % NA == wg, and the fill tiles with u % NA == wg.
         const int ew = warp - kFirstEpiWarp;
         const int wg = ew >> 2;
         const int quad = warp & 3;            // TMEM lane quadrant of this warp
@@ -448,16 +456,16 @@ __global__ void __launch_bounds__(kLogitsThreads, 1)
             for (int i = 0; i < G; ++i)
                 val[i] = -INFINITY;
             if (compute) {
-                mine = (c & 1) == wg;
+                mine = c % NA == wg;
                 ++c;
             } else {
-                mine = (u & 1) == wg;
+                mine = (int)(u % NA) == wg;
             }
             if (compute && mine) {
                 // key scale and page validity from the stage, which is then
                 // released (the MMA's commit is the stage's other arrival)
-                const int s = (c - 1) & (S - 1);
-                if (!mbar_wait(&full[s], (uint32_t)(((c - 1) >> C::LOG2S) & 1), abort_flag, a.status))
+                const int s = C::stage(c - 1);
+                if (!mbar_wait(&full[s], C::phase(c - 1), abort_flag, a.status))
                     break;
                 const uint8_t *st = smem + C::OFF_STAGE + s * C::STAGE_BYTES;
                 const uint32_t halves = *reinterpret_cast<const uint32_t *>(st + C::OFF_FLAGS);
@@ -469,7 +477,7 @@ __global__ void __launch_bounds__(kLogitsThreads, 1)
                 if (lane == 0)
                     mbar_arrive(&empty[s]);
                 const int acc = wg;
-                const int use = (c - 1) >> 1;  // uses of this accumulator so far
+                const int use = (c - 1) / NA;  // uses of this accumulator so far
                 if (!mbar_wait(&acc_full[acc], (uint32_t)(use & 1), abort_flag, a.status))
                     break;
                 tc_fence_after();
@@ -512,22 +520,27 @@ __global__ void __launch_bounds__(kLogitsThreads, 1)
                                 s4[3] = fmaf(wv.w, fmaxf(ksc * qv.w * x[3], 0.0f), s4[3]);
                             }
                         } else if (all_pos) {
-                            // the same four partial sums as below, two per
-                            // packed FMA: bit-identical results
-                            float2 s01 = make_float2(0.0f, 0.0f), s23 = s01;
+                            // eight partial sums in four packed-FMA chains,
+                            // so consecutive FMAs do not wait on each other
+                            float2 c[4];
+                            #pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                c[j] = make_float2(0.0f, 0.0f);
                             #pragma unroll
                             for (int h4 = 0; h4 < H / 4; ++h4) {
                                 const float4 wv = w4[h4];
                                 const float *x = reinterpret_cast<const float *>(&r[ii * H + 4 * h4]);
-                                s01 = fma2(make_float2(wv.x, wv.y),
-                                           make_float2(fmaxf(x[0], 0.0f), fmaxf(x[1], 0.0f)), s01);
-                                s23 = fma2(make_float2(wv.z, wv.w),
-                                           make_float2(fmaxf(x[2], 0.0f), fmaxf(x[3], 0.0f)), s23);
+                                const int j = (h4 & 1) * 2;
+                                c[j] = fma2(make_float2(wv.x, wv.y),
+                                            make_float2(fmaxf(x[0], 0.0f), fmaxf(x[1], 0.0f)), c[j]);
+                                c[j + 1] = fma2(make_float2(wv.z, wv.w),
+                                                make_float2(fmaxf(x[2], 0.0f), fmaxf(x[3], 0.0f)),
+                                                c[j + 1]);
                             }
-                            s4[0] = s01.x;
-                            s4[1] = s01.y;
-                            s4[2] = s23.x;
-                            s4[3] = s23.y;
+                            s4[0] = c[0].x + c[2].x;
+                            s4[1] = c[0].y + c[2].y;
+                            s4[2] = c[1].x + c[3].x;
+                            s4[3] = c[1].y + c[3].y;
                         } else {
                             #pragma unroll
                             for (int h4 = 0; h4 < H / 4; ++h4) {
@@ -553,7 +566,8 @@ __global__ void __launch_bounds__(kLogitsThreads, 1)
                     bool keep = live && t >= rks[i] && t < rke[i];
                     if (keep && a.cand) {
                         const uint32_t *bm = bitmap + ((size_t)slot * G + i) * a.cand_words;
-                        const int blk = (t - rks[i]) / a.cand_block;
+                        const int blk = a.cand_shift >= 0 ? (t - rks[i]) >> a.cand_shift
+                                                          : (t - rks[i]) / a.cand_block;
                         keep = blk < a.cand_words * 32 && ((bm[blk >> 5] >> (blk & 31)) & 1u);
                     }
                     if (!keep)

@@ -682,7 +682,7 @@ union PhaseShared {
 
 static_assert(kRowThreads == kThreads, "the resolve phase runs in the chunk CTAs");
 
-__global__ void __launch_bounds__(kThreads, 4) phases_kernel(const __grid_constant__ PhaseArgs a)
+__global__ void __launch_bounds__(kThreads, 3) phases_kernel(const __grid_constant__ PhaseArgs a)
 {
     __shared__ PhaseShared sh;
     __shared__ uint32_t abort_flag;
