@@ -42,6 +42,34 @@ WORKLOAD_NAMES = {
 }
 
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one logits
+# launch from an ncu capture, per workload, with a digest of the kernel's
+# sources at capture time.  A different digest means the kernel changed
+# since and the traffic is reported as null.
+LOGITS_SOURCES = ["idx_logits_kernel.cuh", "idx_logits.cuh", "idx_common.cuh", "idx_api.cu"]
+NCU_TRAFFIC = {
+    4: {"bytes": 435548416, "digest": "7eced4b2285bd1ee",
+        "profile": "profiles/logits_kernel_paged_fp8_decode_b128_mtp2.md"},
+}
+
+
+def logits_digest() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sparse_attention_indexer_mxfp4_gb300", "csrc")
+    for name in LOGITS_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def logits_traffic(config: int):
+    rec = NCU_TRAFFIC.get(config)
+    if rec is None or rec["digest"] != logits_digest():
+        return None
+    return rec["bytes"]
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -206,7 +234,7 @@ def run_ours(args):
                 "traffic": None, "peak_source": f"{src} bf16 x 2 (fp8 dense)"}
     else:
         roof = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(achieved_gbs / hbm, 4), "traffic": None,
+                "frac": round(achieved_gbs / hbm, 4), "traffic": logits_traffic(args.config),
                 "peak_source": f"{src} hbm_gbs", "kernel": "logits_kernel",
                 "algorithmic_bytes_per_launch": lb, "avg_launch_ms": round(logit_avg, 5)}
     out = {
