@@ -251,26 +251,33 @@ def paged_case(seed: int, context_lens, next_n: int, H: int, D: int, page_size: 
 # --------------------------------------------------------------------------
 
 
-def config1() -> ContiguousCase:
+def shard_seed(base: int, shard: int) -> int:
+    """Data seed of one shard of a workload: shard 0 is the workload itself,
+    every other shard (one per data-parallel rank) draws its own values with
+    the same shapes and lengths."""
+    return base + 7919 * shard
+
+
+def config1(shard: int = 0) -> ContiguousCase:
     """Non-paged FP8: 16 rows x 1024 keys, H=64, D=128, ke_i = 1009 + i, top-256."""
     M = 16
-    return contiguous_case(0, M, 1024, 64, 128, ke=1009 + np.arange(M), topk=256,
-                           name="contig_fp8_M16_N1024")
+    return contiguous_case(shard_seed(0, shard), M, 1024, 64, 128, ke=1009 + np.arange(M),
+                           topk=256, name="contig_fp8_M16_N1024")
 
 
-def config2() -> ContiguousCase:
+def config2(shard: int = 0) -> ContiguousCase:
     """Prefill chunk: rows 6144..8191 of an 8192-token sequence, causal, top-2048."""
     pos = np.arange(6144, 8192)
-    return contiguous_case(1, pos.size, 8192, 64, 128, ke=pos + 1, topk=2048,
-                           name="prefill_fp8_2048x8192")
+    return contiguous_case(shard_seed(1, shard), pos.size, 8192, 64, 128, ke=pos + 1,
+                           topk=2048, name="prefill_fp8_2048x8192")
 
 
-def config3() -> PagedCase:
+def config3(shard: int = 0) -> PagedCase:
     """Paged FP8 decode: B=64, next_n=1, ctx ~ U[4096, 32768], 40,000-page pool."""
     rng = np.random.default_rng(1003)
     ctx = rng.integers(4096, 32768, size=64, endpoint=True).astype(np.int32)
-    return paged_case(3, ctx, 1, 64, 128, 64, 65536, pool_pages=40000, topk=2048,
-                      name="paged_fp8_decode_B64")
+    return paged_case(shard_seed(3, shard), ctx, 1, 64, 128, 64, 65536, pool_pages=40000,
+                      topk=2048, name="paged_fp8_decode_B64")
 
 
 def config4_context_lens() -> np.ndarray:
@@ -279,18 +286,19 @@ def config4_context_lens() -> np.ndarray:
     return np.clip(ctx, 2, 131072).astype(np.int32)
 
 
-def config4() -> PagedCase:
+def config4(shard: int = 0) -> PagedCase:
     """Paged FP8 MTP decode: B=128, next_n=2, lognormal ctx (median 16384),
     64 candidate blocks of 128 per row, top-2048 mapped to ragged slots."""
-    return paged_case(4, config4_context_lens(), 2, 64, 128, 64, 131072, pool_factor=1.1,
-                      topk=2048, cand_num=64, cand_block=128, name="paged_fp8_mtp_cand_B128")
+    return paged_case(shard_seed(4, shard), config4_context_lens(), 2, 64, 128, 64, 131072,
+                      pool_factor=1.1, topk=2048, cand_num=64, cand_block=128,
+                      name="paged_fp8_mtp_cand_B128")
 
 
-def config5() -> PagedCase:
+def config5(shard: int = 0) -> PagedCase:
     """Paged MXFP4: B=32, ctx 131072 each, 65,536-page pool, top-2048."""
     ctx = np.full(32, 131072, dtype=np.int32)
-    return paged_case(5, ctx, 1, 64, 128, 64, 131072, fmt=FMT_MXFP4, pool_pages=65536,
-                      topk=2048, name="paged_mxfp4_decode_B32")
+    return paged_case(shard_seed(5, shard), ctx, 1, 64, 128, 64, 131072, fmt=FMT_MXFP4,
+                      pool_pages=65536, topk=2048, name="paged_mxfp4_decode_B32")
 
 
 CONFIGS = {1: config1, 2: config2, 3: config3, 4: config4, 5: config5}
