@@ -96,13 +96,15 @@ namespace {
 constexpr size_t kMaxSmem = 227 * 1024;
 constexpr int kMaxSmemBytes = 227 * 1024;
 
-template <int FMT, int H, int G, int S, int NA>
-cudaError_t launch_logits_t(const LogitsArgs &a, const CUtensorMap &tmK, const CUtensorMap &tmQ,
+template <int FMT, int H, int G, int S, int NA, int TK>
+cudaError_t launch_logits_t(const LogitsArgs &a0, const CUtensorMap &tmK, const CUtensorMap &tmQ,
                             const CUtensorMap &tmS, int nctas, cudaStream_t stream)
 {
-    using C = LogitsCfg<FMT, H, G, S, NA>;
+    using C = LogitsCfg<FMT, H, G, S, NA, TK>;
+    LogitsArgs a = a0;
+    a.tile_shift = TK == 256 ? 8 : 7;
     const size_t smem = (size_t)C::fixed_bytes() + (size_t)2 * G * a.cand_words * 4;
-    auto kern = logits_kernel<FMT, H, G, S, NA>;
+    auto kern = logits_kernel<FMT, H, G, S, NA, TK>;
     // raise the dynamic shared memory limit once per device to the maximum
     static int configured[kMaxDevices] = {};
     const int dev = current_device();
@@ -120,10 +122,10 @@ cudaError_t launch_logits_t(const LogitsArgs &a, const CUtensorMap &tmK, const C
 }
 
 // Shared memory the launch needs; 0 if the combination has no kernel.
-template <int FMT, int H, int G, int S, int NA>
+template <int FMT, int H, int G, int S, int NA, int TK>
 size_t logits_smem_t(int cand_words)
 {
-    return (size_t)LogitsCfg<FMT, H, G, S, NA>::fixed_bytes() + (size_t)2 * G * cand_words * 4;
+    return (size_t)LogitsCfg<FMT, H, G, S, NA, TK>::fixed_bytes() + (size_t)2 * G * cand_words * 4;
 }
 
 
@@ -135,14 +137,14 @@ cudaError_t launch_logits(int fmt, int H, int G, const LogitsArgs &a, const CUte
     *supported = true;
     if (H == 64 && fmt == kFmtFp8) {
         switch (G) {
-        case 1: return launch_logits_t<kFmtFp8, 64, 1, 8, 2>(a, tmK, tmQ, tmS, nctas, s);
-        case 2: return launch_logits_t<kFmtFp8, 64, 2, 6, 3>(a, tmK, tmQ, tmS, nctas, s);
-        case 4: return launch_logits_t<kFmtFp8, 64, 4, 8, 2>(a, tmK, tmQ, tmS, nctas, s);
+        case 1: return launch_logits_t<kFmtFp8, 64, 1, 4, 2, 256>(a, tmK, tmQ, tmS, nctas, s);
+        case 2: return launch_logits_t<kFmtFp8, 64, 2, 4, 2, 256>(a, tmK, tmQ, tmS, nctas, s);
+        case 4: return launch_logits_t<kFmtFp8, 64, 4, 8, 2, 128>(a, tmK, tmQ, tmS, nctas, s);
         }
     } else if (H == 64 && fmt == kFmtMxfp4) {
         switch (G) {
-        case 1: return launch_logits_t<kFmtMxfp4, 64, 1, 16, 2>(a, tmK, tmQ, tmS, nctas, s);
-        case 2: return launch_logits_t<kFmtMxfp4, 64, 2, 12, 3>(a, tmK, tmQ, tmS, nctas, s);
+        case 1: return launch_logits_t<kFmtMxfp4, 64, 1, 8, 2, 256>(a, tmK, tmQ, tmS, nctas, s);
+        case 2: return launch_logits_t<kFmtMxfp4, 64, 2, 12, 3, 128>(a, tmK, tmQ, tmS, nctas, s);
         }
     }
     *supported = false;
@@ -153,14 +155,14 @@ size_t logits_smem(int fmt, int H, int G, int cand_words)
 {
     if (H == 64 && fmt == kFmtFp8) {
         switch (G) {
-        case 1: return logits_smem_t<kFmtFp8, 64, 1, 8, 2>(cand_words);
-        case 2: return logits_smem_t<kFmtFp8, 64, 2, 6, 3>(cand_words);
-        case 4: return logits_smem_t<kFmtFp8, 64, 4, 8, 2>(cand_words);
+        case 1: return logits_smem_t<kFmtFp8, 64, 1, 4, 2, 256>(cand_words);
+        case 2: return logits_smem_t<kFmtFp8, 64, 2, 4, 2, 256>(cand_words);
+        case 4: return logits_smem_t<kFmtFp8, 64, 4, 8, 2, 128>(cand_words);
         }
     } else if (H == 64 && fmt == kFmtMxfp4) {
         switch (G) {
-        case 1: return logits_smem_t<kFmtMxfp4, 64, 1, 16, 2>(cand_words);
-        case 2: return logits_smem_t<kFmtMxfp4, 64, 2, 12, 3>(cand_words);
+        case 1: return logits_smem_t<kFmtMxfp4, 64, 1, 8, 2, 256>(cand_words);
+        case 2: return logits_smem_t<kFmtMxfp4, 64, 2, 12, 3, 128>(cand_words);
         }
     }
     return 0;
@@ -202,7 +204,7 @@ extern "C" idx_status idx_mqa_logits(const void *q, const void *q_scale, const f
     if (f == kFmtMxfp4 && N % 4 != 0)
         return IDX_ERR_UNSUPPORTED;
     const int nsm = sm_count();
-    const int T = (N + kTileKeys - 1) / kTileKeys;
+    const int T = (N + kMmaM - 1) / kMmaM;  // 128-key tiles, for sizing only
     int G = 1;
     const int gmax = f == kFmtFp8 ? 4 : 2;
     for (int g = gmax; g > 1; g >>= 1)

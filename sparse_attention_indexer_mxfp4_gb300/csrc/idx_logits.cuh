@@ -1,6 +1,7 @@
 // idx_logits.cuh -- argument block and work schedule of the logits kernel.
 //
-// Work is cut into units of (row group, 128-key tile).  A row group is the
+// Work is cut into units of (row group, key tile), a tile being 128 or 256
+// keys (LogitsArgs::tile_shift; the kernel instantiation fixes it).  A row group is the
 // set of query rows that share one key sequence and one MMA: the next_n rows
 // of a sequence for paged decode / MTP, or G consecutive rows of a contiguous
 // prefill chunk.  Each unit is either a "compute" tile (it overlaps the
@@ -21,8 +22,8 @@
 
 namespace idx {
 
-constexpr int kTileKeys = 128;  // keys per tile = MMA M
-constexpr int kHalfKeys = 64;   // keys per TMA box (one page of 64 or part of a larger page)
+constexpr int kMmaM = 128;     // keys per MMA = TMEM lanes
+constexpr int kHalfKeys = 64;  // keys per TMA box (one page of 64 or part of a larger page)
 
 struct LogitsArgs {
     int paged;         // 1: K through a block table; 0: one contiguous K sequence
@@ -64,6 +65,7 @@ struct LogitsArgs {
     int64_t ld;
     int width;               // paged: max_model_len; contiguous: N
     unsigned int *status;    // device status word (IDX_DEV_* bits)
+    int tile_shift;          // log2 of the keys per tile (7 or 8)
 };
 
 // Key range [ks, ke) of row r, clamped as the oracle clamps it.
@@ -112,17 +114,18 @@ __device__ __noinline__ GroupInfo group_info(const LogitsArgs &a, int g)
         lo = 0;
     gi.lo = lo;
     gi.hi = hi;
+    const int tk = 1 << a.tile_shift;
     if (a.paged)
-        gi.tiles = (hi + kTileKeys - 1) / kTileKeys;  // columns [0, max ke) are written
+        gi.tiles = (hi + tk - 1) >> a.tile_shift;  // columns [0, max ke) are written
     else
-        gi.tiles = (a.N + kTileKeys - 1) / kTileKeys;  // every column of [0, N) is written
+        gi.tiles = (a.N + tk - 1) >> a.tile_shift;  // every column of [0, N) is written
     return gi;
 }
 
-__device__ __forceinline__ bool tile_is_compute(const GroupInfo &gi, int j)
+__device__ __forceinline__ bool tile_is_compute(const GroupInfo &gi, int j, int shift)
 {
-    int t0 = j * kTileKeys;
-    return gi.hi > gi.lo && t0 < gi.hi && t0 + kTileKeys > gi.lo;
+    const int t0 = j << shift;
+    return gi.hi > gi.lo && t0 < gi.hi && t0 + (1 << shift) > gi.lo;
 }
 
 // Walks this CTA's unit range in order.  Every role of the CTA runs its own
@@ -188,7 +191,7 @@ __device__ __forceinline__ void locate_units(const LogitsArgs &a, long long *scr
     long long total;
     int T = 0;
     if (!a.paged) {
-        T = (a.N + kTileKeys - 1) / kTileKeys;
+        T = (a.N + (1 << a.tile_shift) - 1) >> a.tile_shift;
         total = (long long)a.num_groups * T;
     } else {
         long long loc = 0;

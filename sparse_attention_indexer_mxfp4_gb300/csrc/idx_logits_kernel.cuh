@@ -38,17 +38,22 @@ constexpr int kFmtMxfp4 = 1;
 // control role is split over two warps.
 constexpr int kFirstEpiWarp = 4;
 constexpr int kMmaWarp = 2;
-constexpr int kWinTiles = 16;  // tiles whose pages the producer resolves at once (32 halves)
 
-template <int FMT, int H, int G, int S, int NA>
+template <int FMT, int H, int G, int S, int NA, int TK>
 struct LogitsCfg {
+    static_assert(TK == 128 || TK == 256, "a tile is one or two MMAs of 128 keys");
+    static constexpr int NSUB = TK / kMmaM;               // MMAs (of 128 keys) per tile
+    static constexpr int NH = TK / kHalfKeys;             // 64-key TMA boxes per tile
+    static constexpr int WIN_TILES = 32 / NH;             // tiles of one producer page window
     static constexpr int NCOLS = G * H;                    // MMA N
+    static constexpr int ACC_COLS = NSUB * NCOLS;          // TMEM columns of one tile
     static constexpr int ROWB = FMT == kFmtFp8 ? 128 : 64;  // value bytes per key / query row
-    static constexpr int A_BYTES = kTileKeys * ROWB;
+    static constexpr int A_BYTES = TK * ROWB;
+    static constexpr int SUB_BYTES = kMmaM * ROWB;         // one MMA's A operand
     // stage: K values | key scales as loaded (FP8 fp32, MXFP4 e8m0 words) |
     // (MXFP4) the scale words in MMA order | flags: which halves hold data
-    static constexpr int SF_STAGE = 512;
-    static constexpr int SF_ATOM = FMT == kFmtFp8 ? 0 : 512;
+    static constexpr int SF_STAGE = TK * 4;
+    static constexpr int SF_ATOM = FMT == kFmtFp8 ? 0 : NSUB * 512;
     static constexpr int OFF_FLAGS = A_BYTES + SF_STAGE + SF_ATOM;
     static constexpr int STAGE_BYTES = ((OFF_FLAGS + 16) + 1023) / 1024 * 1024;
     static constexpr int Q_BYTES = (NCOLS * ROWB + 1023) / 1024 * 1024;
@@ -71,8 +76,8 @@ struct LogitsCfg {
     static constexpr int fixed_bytes() { return OFF_BITMAP + 1024; }  // + alignment slack
     // TMEM columns: accumulators, then (MXFP4) scale factors of A per
     // accumulator and of B per group slot.
-    static constexpr int TM_SFA = NA * NCOLS;
-    static constexpr int TM_SFB = TM_SFA + (FMT == kFmtFp8 ? 0 : NA * 4);
+    static constexpr int TM_SFA = NA * ACC_COLS;
+    static constexpr int TM_SFB = TM_SFA + (FMT == kFmtFp8 ? 0 : NA * NSUB * 4);
     static constexpr int TM_USED = TM_SFB + (FMT == kFmtFp8 ? 0 : 4 * QATOMS * 4);  // 2 slots x 2 MMA warps
     static constexpr int TM_COLS = TM_USED <= 32 ? 32 : TM_USED <= 64 ? 64 : TM_USED <= 128 ? 128
                                  : TM_USED <= 256 ? 256 : 512;
@@ -94,7 +99,7 @@ struct LogitsCfg {
     __host__ __device__ static constexpr uint32_t idesc_f8()
     {
         return (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(NCOLS >> 3) << 17) |
-               ((uint32_t)(kTileKeys >> 4) << 24);
+               ((uint32_t)(kMmaM >> 4) << 24);
     }
     // block-scaled e2m1 x e2m1 with ue8m0 scales; the scale-factor ids select
     // the byte of each 32-bit scale word the MMA starts from.
@@ -102,7 +107,7 @@ struct LogitsCfg {
     {
         return ((uint32_t)sf_id << 4) | (1u << 7) | (1u << 10) |
                ((uint32_t)(NCOLS >> 3) << 17) | (1u << 23) |
-               ((uint32_t)(kTileKeys >> 4) << 24) | ((uint32_t)sf_id << 29);
+               ((uint32_t)(kMmaM >> 4) << 24) | ((uint32_t)sf_id << 29);
     }
 };
 
@@ -112,19 +117,21 @@ __device__ __forceinline__ int page_of(const LogitsArgs &a, int t)
     return a.page_shift >= 0 ? (t >> a.page_shift) : t / a.page_size;
 }
 
-// One lane's half-tile (64 keys) of a producer window: does the group need
-// it, which page and row it starts at.  The block-table load is issued here
-// and only consumed when the window becomes current.
+// One lane's 64-key box of a producer window (NH boxes per tile, 32 per
+// window): does the group need it, which page and row it starts at.  The
+// block-table load is issued here and only consumed when the window becomes
+// current.
 struct HalfInfo {
     int page, row;
     bool need;
 };
 
+template <int NH>
 __device__ __forceinline__ HalfInfo half_info(const LogitsArgs &a, const GroupInfo &gi, int g,
                                               int tile0, int lane)
 {
     HalfInfo h;
-    const int tok = (tile0 * 2 + lane) * kHalfKeys;
+    const int tok = (tile0 * NH + lane) * kHalfKeys;
     h.need = tok < gi.hi && tok + kHalfKeys > gi.lo;
     h.page = 0;
     h.row = tok;
@@ -140,12 +147,13 @@ __device__ __forceinline__ HalfInfo half_info(const LogitsArgs &a, const GroupIn
 
 namespace idx {
 
-template <int FMT, int H, int G, int S, int NA>
-__global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA>::THREADS, 1)
+template <int FMT, int H, int G, int S, int NA, int TK>
+__global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
     logits_kernel(const __grid_constant__ LogitsArgs a, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmS)
 {
-    using C = LogitsCfg<FMT, H, G, S, NA>;
+    using C = LogitsCfg<FMT, H, G, S, NA, TK>;
+    constexpr int TSH = TK == 256 ? 8 : 7;  // equals a.tile_shift
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // swizzled TMA tiles and MMA descriptors assume 1024-byte aligned tiles
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -253,25 +261,25 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA>::THREADS, 1)
             if (w.first_in_group) {
                 // page window of this group: current and next, loads in flight
                 win0 = w.j;
-                cur = half_info(a, w.gi, w.g, win0, lane);
-                nxt = half_info(a, w.gi, w.g, win0 + kWinTiles, lane);
+                cur = half_info<C::NH>(a, w.gi, w.g, win0, lane);
+                nxt = half_info<C::NH>(a, w.gi, w.g, win0 + C::WIN_TILES, lane);
                 cur_ok = false;
             }
-            if (!tile_is_compute(w.gi, w.j))
+            if (!tile_is_compute(w.gi, w.j, TSH))
                 continue;
             if ((c & 1) != pw) {  // the other producer's tile
                 ++c;
                 continue;
             }
-            if (w.j >= win0 + kWinTiles) {  // slide the window (warp-uniform)
-                const int step = (w.j - win0) / kWinTiles;
+            if (w.j >= win0 + C::WIN_TILES) {  // slide the window (warp-uniform)
+                const int step = (w.j - win0) / C::WIN_TILES;
                 if (step == 1) {
                     cur = nxt;
                 } else {
-                    cur = half_info(a, w.gi, w.g, win0 + step * kWinTiles, lane);
+                    cur = half_info<C::NH>(a, w.gi, w.g, win0 + step * C::WIN_TILES, lane);
                 }
-                win0 += step * kWinTiles;
-                nxt = half_info(a, w.gi, w.g, win0 + kWinTiles, lane);
+                win0 += step * C::WIN_TILES;
+                nxt = half_info<C::NH>(a, w.gi, w.g, win0 + C::WIN_TILES, lane);
                 cur_ok = false;
             }
             if (!cur_ok) {  // first use of this window: resolve validity
@@ -284,9 +292,9 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA>::THREADS, 1)
             const int s = C::stage(c);
             if (!mbar_wait(&empty[s], C::phase(c) ^ 1, abort_flag, a.status))
                 break;
-            const int h0 = 2 * (w.j - win0);  // lanes h0, h0 + 1 own this tile's halves
+            const int h0 = C::NH * (w.j - win0);  // lanes h0 .. h0 + NH - 1 own this tile's boxes
             const uint32_t ball = __ballot_sync(0xffffffffu, cur.need);
-            const uint32_t mine = (ball >> h0) & 3u;
+            const uint32_t mine = (ball >> h0) & ((1u << C::NH) - 1u);
             uint8_t *st = smem + C::OFF_STAGE + s * C::STAGE_BYTES;
             if (lane == 0) {
                 *reinterpret_cast<uint32_t *>(st + C::OFF_FLAGS) = mine;
@@ -294,7 +302,7 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA>::THREADS, 1)
                                                     (kHalfKeys * C::ROWB + kHalfKeys * 4));
             }
             __syncwarp();
-            if ((lane == h0 || lane == h0 + 1) && cur.need) {
+            if (lane >= h0 && lane < h0 + C::NH && cur.need) {
                 const int k = lane - h0;
                 tma_load_3d(st + k * kHalfKeys * C::ROWB, &tmK, &full[s], 0, cur.row, cur.page);
                 // the half's 64 key scales (FP8 fp32 / MXFP4 4 x e8m0), 256 bytes
@@ -360,9 +368,9 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA>::THREADS, 1)
                 }
                 ++gq;
             }
-            if (tile_is_compute(w.gi, w.j) && ((c % NA) & 1) != mw) {
+            if (tile_is_compute(w.gi, w.j, TSH) && ((c % NA) & 1) != mw) {
                 ++c;  // the other MMA warp's tile
-            } else if (tile_is_compute(w.gi, w.j)) {
+            } else if (tile_is_compute(w.gi, w.j, TSH)) {
                 const int acc = c % NA;
                 const int s = C::stage(c);
                 if (!mbar_wait(&acc_empty[acc], (uint32_t)((c / NA) & 1) ^ 1, abort_flag, a.status))
@@ -371,41 +379,53 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA>::THREADS, 1)
                     break;
                 uint8_t *st = smem + C::OFF_STAGE + s * C::STAGE_BYTES;
                 if constexpr (FMT == kFmtMxfp4) {
-                    // K scale words (key-major as loaded) -> MMA order atom
+                    // K scale words (key-major as loaded) -> one MMA-order atom
+                    // per 128 keys
                     const uint32_t *sw = reinterpret_cast<const uint32_t *>(st + C::A_BYTES);
-                    uint4 v;
-                    v.x = sw[lane];
-                    v.y = sw[lane + 32];
-                    v.z = sw[lane + 64];
-                    v.w = sw[lane + 96];
-                    *reinterpret_cast<uint4 *>(st + C::A_BYTES + C::SF_STAGE + lane * 16) = v;
+                    #pragma unroll
+                    for (int sub = 0; sub < C::NSUB; ++sub) {
+                        uint4 v;
+                        v.x = sw[sub * kMmaM + lane];
+                        v.y = sw[sub * kMmaM + lane + 32];
+                        v.z = sw[sub * kMmaM + lane + 64];
+                        v.w = sw[sub * kMmaM + lane + 96];
+                        *reinterpret_cast<uint4 *>(st + C::A_BYTES + C::SF_STAGE + sub * 512 +
+                                                   lane * 16) = v;
+                    }
                     fence_proxy_async_smem();
                     __syncwarp();
                 }
                 if (lane == 0) {
                     tc_fence_after();
-                    const uint32_t d_tmem = tmem_base + acc * C::NCOLS;
-                    const uint32_t a_addr = smem_u32(st);
                     const uint32_t b_addr = smem_u32(smem + C::OFF_Q + slot * C::Q_BYTES);
-                    if constexpr (FMT == kFmtFp8) {
-                        #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            uint64_t ad = make_smem_desc(a_addr + kk * 32, 16, 1024, kLayoutSw128);
-                            uint64_t bd = make_smem_desc(b_addr + kk * 32, 16, 1024, kLayoutSw128);
-                            mma_f8f6f4(d_tmem, ad, bd, C::idesc_f8(), kk > 0 ? 1u : 0u);
-                        }
-                    } else {
-                        const uint32_t sfa = tmem_base + C::TM_SFA + acc * 4;
-                        const uint32_t sfb = tmem_base + C::TM_SFB + (mw * 2 + slot) * C::QATOMS * 4;
-                        uint64_t cd = make_smem_desc(smem_u32(st + C::A_BYTES + C::SF_STAGE), 128,
-                                                     128, kLayoutNone);
-                        tmem_cp_32x128b_warpx4(sfa, cd);
-                        #pragma unroll
-                        for (int kk = 0; kk < 2; ++kk) {
-                            uint64_t ad = make_smem_desc(a_addr + kk * 32, 16, 512, kLayoutSw64);
-                            uint64_t bd = make_smem_desc(b_addr + kk * 32, 16, 512, kLayoutSw64);
-                            mma_mxf4(d_tmem, ad, bd, C::idesc_mxf4(2 * kk), sfa, sfb,
-                                     kk > 0 ? 1u : 0u);
+                    #pragma unroll
+                    for (int sub = 0; sub < C::NSUB; ++sub) {
+                        // keys 128 sub .. 128 sub + 127 of the tile -> columns
+                        // [sub NCOLS, (sub + 1) NCOLS) of the accumulator
+                        const uint32_t d_tmem = tmem_base + acc * C::ACC_COLS + sub * C::NCOLS;
+                        const uint32_t a_addr = smem_u32(st + sub * C::SUB_BYTES);
+                        if constexpr (FMT == kFmtFp8) {
+                            #pragma unroll
+                            for (int kk = 0; kk < 4; ++kk) {
+                                uint64_t ad = make_smem_desc(a_addr + kk * 32, 16, 1024, kLayoutSw128);
+                                uint64_t bd = make_smem_desc(b_addr + kk * 32, 16, 1024, kLayoutSw128);
+                                mma_f8f6f4(d_tmem, ad, bd, C::idesc_f8(), kk > 0 ? 1u : 0u);
+                            }
+                        } else {
+                            const uint32_t sfa = tmem_base + C::TM_SFA + (acc * C::NSUB + sub) * 4;
+                            const uint32_t sfb =
+                                tmem_base + C::TM_SFB + (mw * 2 + slot) * C::QATOMS * 4;
+                            uint64_t cd = make_smem_desc(
+                                smem_u32(st + C::A_BYTES + C::SF_STAGE + sub * 512), 128, 128,
+                                kLayoutNone);
+                            tmem_cp_32x128b_warpx4(sfa, cd);
+                            #pragma unroll
+                            for (int kk = 0; kk < 2; ++kk) {
+                                uint64_t ad = make_smem_desc(a_addr + kk * 32, 16, 512, kLayoutSw64);
+                                uint64_t bd = make_smem_desc(b_addr + kk * 32, 16, 512, kLayoutSw64);
+                                mma_mxf4(d_tmem, ad, bd, C::idesc_mxf4(2 * kk), sfa, sfb,
+                                         kk > 0 ? 1u : 0u);
+                            }
                         }
                     }
                     mma_commit(&empty[s]);
@@ -427,13 +447,13 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA>::THREADS, 1)
         const int ew = warp - kFirstEpiWarp;
         const int wg = ew >> 2;
         const int quad = warp & 3;            // TMEM lane quadrant of this warp
-        const int key_in_tile = quad * 32 + lane;
+        const int kq = quad * 32 + lane;      // key of each 128-key MMA block this thread owns
         int gq = 0;
-        int c = 0;          // compute tiles seen (both warpgroups')
+        int c = 0;          // compute tiles seen (all warpgroups')
         long long u = 0;    // units seen
         int slot = 0;
         int rks[G], rke[G];
-        constexpr int RB = H >= 64 ? 1 : 64 / H;  // rows per batch of TMEM loads (<= 64 values)
+        constexpr int NSUB = C::NSUB;
         for (; w.left > 0; walk_next(a, w), ++u) {
             if (w.first_in_group) {
                 slot = gq & 1;
@@ -447,14 +467,16 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA>::THREADS, 1)
                     break;
                 ++gq;
             }
-            const int t = w.j * kTileKeys + key_in_tile;
+            const int t0 = (w.j << TSH) + kq;  // this thread's key in sub-tile 0
             const int wend = a.paged ? w.gi.hi : a.N;  // columns this group writes
-            const bool compute = tile_is_compute(w.gi, w.j);
+            const bool compute = tile_is_compute(w.gi, w.j, TSH);
             bool mine;
-            float val[G];
+            float val[NSUB][G];
             #pragma unroll
-            for (int i = 0; i < G; ++i)
-                val[i] = -INFINITY;
+            for (int sub = 0; sub < NSUB; ++sub)
+                #pragma unroll
+                for (int i = 0; i < G; ++i)
+                    val[sub][i] = -INFINITY;
             if (compute) {
                 mine = c % NA == wg;
                 ++c;
@@ -462,17 +484,25 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA>::THREADS, 1)
                 mine = (int)(u % NA) == wg;
             }
             if (compute && mine) {
-                // key scale and page validity from the stage, which is then
+                // key scales and page validity from the stage, which is then
                 // released (the MMA's commit is the stage's other arrival)
                 const int s = C::stage(c - 1);
                 if (!mbar_wait(&full[s], C::phase(c - 1), abort_flag, a.status))
                     break;
                 const uint8_t *st = smem + C::OFF_STAGE + s * C::STAGE_BYTES;
                 const uint32_t halves = *reinterpret_cast<const uint32_t *>(st + C::OFF_FLAGS);
-                const bool live = t < w.gi.hi && t >= w.gi.lo && ((halves >> (key_in_tile >> 6)) & 1u);
-                float ksc = 1.0f;
-                if (FMT == kFmtFp8)
-                    ksc = reinterpret_cast<const float *>(st + C::A_BYTES)[key_in_tile];
+                bool live[NSUB];
+                float ksc[NSUB];
+                bool pos = true;
+                #pragma unroll
+                for (int sub = 0; sub < NSUB; ++sub) {
+                    const int key = sub * kMmaM + kq, t = t0 + sub * kMmaM;
+                    live[sub] = t < w.gi.hi && t >= w.gi.lo && ((halves >> (key >> 6)) & 1u);
+                    ksc[sub] = 1.0f;
+                    if (FMT == kFmtFp8)
+                        ksc[sub] = reinterpret_cast<const float *>(st + C::A_BYTES)[key];
+                    pos = pos && ksc[sub] >= 0.0f;
+                }
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(&empty[s]);
@@ -487,25 +517,22 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA>::THREADS, 1)
                 // relu(ksc * x) = |ksc| * relu(sgn * x); the common all-positive
                 // case skips the sign multiply.  Branches stay warp-uniform so
                 // the warp is converged at every tcgen05.ld.
-                const bool all_pos = __all_sync(0xffffffffu, ksc >= 0.0f);
-                const float sgn = ksc >= 0.0f ? 1.0f : -1.0f;
-                const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * C::NCOLS;
+                const bool all_pos = __all_sync(0xffffffffu, pos);
+                const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * C::ACC_COLS;
                 #pragma unroll
-                for (int i0 = 0; i0 < G; i0 += RB) {
-                    if (i0 >= w.gi.nrows)
-                        break;
-                    // all TMEM loads of RB rows first, then one wait
-                    uint32_t r[RB * H];
+                for (int sub = 0; sub < NSUB; ++sub) {
+                    const float sgn = ksc[sub] >= 0.0f ? 1.0f : -1.0f;
                     #pragma unroll
-                    for (int ii = 0; ii < RB; ++ii)
+                    for (int i = 0; i < G; ++i) {
+                        if (i >= w.gi.nrows)
+                            break;
+                        // the row's H scores of this key: two TMEM loads, one wait
+                        uint32_t r[H];
                         #pragma unroll
                         for (int hc = 0; hc < H / 32; ++hc)
-                            tmem_ld_32x32b_x32(tbase + (i0 + ii) * H + hc * 32,
-                                               *reinterpret_cast<uint32_t(*)[32]>(&r[ii * H + hc * 32]));
-                    tmem_ld_wait();
-                    #pragma unroll
-                    for (int ii = 0; ii < RB; ++ii) {
-                        const int i = i0 + ii;
+                            tmem_ld_32x32b_x32(tbase + sub * C::NCOLS + i * H + hc * 32,
+                                               *reinterpret_cast<uint32_t(*)[32]>(&r[hc * 32]));
+                        tmem_ld_wait();
                         const float4 *w4 = reinterpret_cast<const float4 *>(wsm + i * H);
                         float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // independent partial sums
                         if (use_qs) {
@@ -513,39 +540,40 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA>::THREADS, 1)
                             #pragma unroll
                             for (int h4 = 0; h4 < H / 4; ++h4) {
                                 const float4 wv = w4[h4], qv = q4[h4];
-                                const float *x = reinterpret_cast<const float *>(&r[ii * H + 4 * h4]);
-                                s4[0] = fmaf(wv.x, fmaxf(ksc * qv.x * x[0], 0.0f), s4[0]);
-                                s4[1] = fmaf(wv.y, fmaxf(ksc * qv.y * x[1], 0.0f), s4[1]);
-                                s4[2] = fmaf(wv.z, fmaxf(ksc * qv.z * x[2], 0.0f), s4[2]);
-                                s4[3] = fmaf(wv.w, fmaxf(ksc * qv.w * x[3], 0.0f), s4[3]);
+                                const float *x = reinterpret_cast<const float *>(&r[4 * h4]);
+                                const float k = ksc[sub];
+                                s4[0] = fmaf(wv.x, fmaxf(k * qv.x * x[0], 0.0f), s4[0]);
+                                s4[1] = fmaf(wv.y, fmaxf(k * qv.y * x[1], 0.0f), s4[1]);
+                                s4[2] = fmaf(wv.z, fmaxf(k * qv.z * x[2], 0.0f), s4[2]);
+                                s4[3] = fmaf(wv.w, fmaxf(k * qv.w * x[3], 0.0f), s4[3]);
                             }
                         } else if (all_pos) {
                             // eight partial sums in four packed-FMA chains,
                             // so consecutive FMAs do not wait on each other
-                            float2 c[4];
+                            float2 cc[4];
                             #pragma unroll
                             for (int j = 0; j < 4; ++j)
-                                c[j] = make_float2(0.0f, 0.0f);
+                                cc[j] = make_float2(0.0f, 0.0f);
                             #pragma unroll
                             for (int h4 = 0; h4 < H / 4; ++h4) {
                                 const float4 wv = w4[h4];
-                                const float *x = reinterpret_cast<const float *>(&r[ii * H + 4 * h4]);
+                                const float *x = reinterpret_cast<const float *>(&r[4 * h4]);
                                 const int j = (h4 & 1) * 2;
-                                c[j] = fma2(make_float2(wv.x, wv.y),
-                                            make_float2(fmaxf(x[0], 0.0f), fmaxf(x[1], 0.0f)), c[j]);
-                                c[j + 1] = fma2(make_float2(wv.z, wv.w),
-                                                make_float2(fmaxf(x[2], 0.0f), fmaxf(x[3], 0.0f)),
-                                                c[j + 1]);
+                                cc[j] = fma2(make_float2(wv.x, wv.y),
+                                             make_float2(fmaxf(x[0], 0.0f), fmaxf(x[1], 0.0f)), cc[j]);
+                                cc[j + 1] = fma2(make_float2(wv.z, wv.w),
+                                                 make_float2(fmaxf(x[2], 0.0f), fmaxf(x[3], 0.0f)),
+                                                 cc[j + 1]);
                             }
-                            s4[0] = c[0].x + c[2].x;
-                            s4[1] = c[0].y + c[2].y;
-                            s4[2] = c[1].x + c[3].x;
-                            s4[3] = c[1].y + c[3].y;
+                            s4[0] = cc[0].x + cc[2].x;
+                            s4[1] = cc[0].y + cc[2].y;
+                            s4[2] = cc[1].x + cc[3].x;
+                            s4[3] = cc[1].y + cc[3].y;
                         } else {
                             #pragma unroll
                             for (int h4 = 0; h4 < H / 4; ++h4) {
                                 const float4 wv = w4[h4];
-                                const float *x = reinterpret_cast<const float *>(&r[ii * H + 4 * h4]);
+                                const float *x = reinterpret_cast<const float *>(&r[4 * h4]);
                                 s4[0] = fmaf(wv.x, fmaxf(sgn * x[0], 0.0f), s4[0]);
                                 s4[1] = fmaf(wv.y, fmaxf(sgn * x[1], 0.0f), s4[1]);
                                 s4[2] = fmaf(wv.z, fmaxf(sgn * x[2], 0.0f), s4[2]);
@@ -553,7 +581,7 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA>::THREADS, 1)
                             }
                         }
                         const float sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
-                        val[i] = use_qs ? sum : fabsf(ksc) * sum;
+                        val[sub][i] = use_qs ? sum : fabsf(ksc[sub]) * sum;
                     }
                 }
                 tc_fence_before();
@@ -562,26 +590,35 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA>::THREADS, 1)
                     mbar_arrive(&acc_empty[acc]);
                 // masks
                 #pragma unroll
-                for (int i = 0; i < G; ++i) {
-                    bool keep = live && t >= rks[i] && t < rke[i];
-                    if (keep && a.cand) {
-                        const uint32_t *bm = bitmap + ((size_t)slot * G + i) * a.cand_words;
-                        const int blk = a.cand_shift >= 0 ? (t - rks[i]) >> a.cand_shift
-                                                          : (t - rks[i]) / a.cand_block;
-                        keep = blk < a.cand_words * 32 && ((bm[blk >> 5] >> (blk & 31)) & 1u);
+                for (int sub = 0; sub < NSUB; ++sub) {
+                    const int t = t0 + sub * kMmaM;
+                    #pragma unroll
+                    for (int i = 0; i < G; ++i) {
+                        bool keep = live[sub] && t >= rks[i] && t < rke[i];
+                        if (keep && a.cand) {
+                            const uint32_t *bm = bitmap + ((size_t)slot * G + i) * a.cand_words;
+                            const int blk = a.cand_shift >= 0 ? (t - rks[i]) >> a.cand_shift
+                                                              : (t - rks[i]) / a.cand_block;
+                            keep = blk < a.cand_words * 32 && ((bm[blk >> 5] >> (blk & 31)) & 1u);
+                        }
+                        if (!keep)
+                            val[sub][i] = -INFINITY;
                     }
-                    if (!keep)
-                        val[i] = -INFINITY;
                 }
             }
-            if (mine && t < wend) {
+            if (mine) {
                 #pragma unroll
                 for (int i = 0; i < G; ++i) {
                     if (i >= w.gi.nrows)
                         break;
-                    const int end = a.paged ? rke[i] : a.N;
-                    if (t < end)
-                        a.logits[(size_t)(w.gi.row0 + i) * a.ld + t] = val[i];
+                    const int end = min(wend, a.paged ? rke[i] : a.N);
+                    float *orow = a.logits + (size_t)(w.gi.row0 + i) * a.ld;
+                    #pragma unroll
+                    for (int sub = 0; sub < NSUB; ++sub) {
+                        const int t = t0 + sub * kMmaM;
+                        if (t < end)
+                            orow[t] = val[sub][i];
+                    }
                 }
             }
             if (walk_last_in_group(w)) {
