@@ -245,6 +245,14 @@ IDX_DEVFN void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32])
                  : "r"(taddr));
 }
 
+// Four consecutive 32-bit columns of the warp's 32 TMEM lanes.
+IDX_DEVFN void tmem_ld_32x32b_x4(uint32_t taddr, uint32_t (&r)[4])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr));
+}
+
 IDX_DEVFN void tmem_st_32x32b_x4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
 {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),

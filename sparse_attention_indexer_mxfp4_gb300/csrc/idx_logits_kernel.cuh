@@ -526,28 +526,36 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
                     for (int i = 0; i < G; ++i) {
                         if (i >= w.gi.nrows)
                             break;
-                        // the row's H scores of this key: two TMEM loads, one wait
-                        uint32_t r[H];
-                        #pragma unroll
-                        for (int hc = 0; hc < H / 32; ++hc)
-                            tmem_ld_32x32b_x32(tbase + sub * C::NCOLS + i * H + hc * 32,
-                                               *reinterpret_cast<uint32_t(*)[32]>(&r[hc * 32]));
-                        tmem_ld_wait();
+                        const uint32_t trow = tbase + sub * C::NCOLS + i * H;
                         const float4 *w4 = reinterpret_cast<const float4 *>(wsm + i * H);
                         float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // independent partial sums
-                        if (use_qs) {
-                            const float4 *q4 = reinterpret_cast<const float4 *>(qsm + i * H);
-                            #pragma unroll
-                            for (int h4 = 0; h4 < H / 4; ++h4) {
-                                const float4 wv = w4[h4], qv = q4[h4];
-                                const float *x = reinterpret_cast<const float *>(&r[4 * h4]);
-                                const float k = ksc[sub];
-                                s4[0] = fmaf(wv.x, fmaxf(k * qv.x * x[0], 0.0f), s4[0]);
-                                s4[1] = fmaf(wv.y, fmaxf(k * qv.y * x[1], 0.0f), s4[1]);
-                                s4[2] = fmaf(wv.z, fmaxf(k * qv.z * x[2], 0.0f), s4[2]);
-                                s4[3] = fmaf(wv.w, fmaxf(k * qv.w * x[3], 0.0f), s4[3]);
+                        if (use_qs || !all_pos) {
+                            // rare (per-head q scales, or a negative key scale):
+                            // a rolled loop over four heads at a time keeps the
+                            // code small; the common path below is unrolled
+                            const float *qrow = qsm + i * H;
+                            #pragma unroll 1
+                            for (int h = 0; h < H; h += 4) {
+                                uint32_t x4[4];
+                                tmem_ld_32x32b_x4(trow + h, x4);
+                                tmem_ld_wait();
+                                const float4 wv = w4[h >> 2];
+                                const float wj[4] = {wv.x, wv.y, wv.z, wv.w};
+                                #pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const float x = __uint_as_float(x4[e]);
+                                    const float y = use_qs ? ksc[sub] * qrow[h + e] * x : sgn * x;
+                                    s4[e] = fmaf(wj[e], fmaxf(y, 0.0f), s4[e]);
+                                }
                             }
-                        } else if (all_pos) {
+                        } else {
+                            // the row's H scores of this key: two TMEM loads, one wait
+                            uint32_t r[H];
+                            #pragma unroll
+                            for (int hc = 0; hc < H / 32; ++hc)
+                                tmem_ld_32x32b_x32(trow + hc * 32,
+                                                   *reinterpret_cast<uint32_t(*)[32]>(&r[hc * 32]));
+                            tmem_ld_wait();
                             // eight partial sums in four packed-FMA chains,
                             // so consecutive FMAs do not wait on each other
                             float2 cc[4];
@@ -569,16 +577,6 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
                             s4[1] = cc[0].y + cc[2].y;
                             s4[2] = cc[1].x + cc[3].x;
                             s4[3] = cc[1].y + cc[3].y;
-                        } else {
-                            #pragma unroll
-                            for (int h4 = 0; h4 < H / 4; ++h4) {
-                                const float4 wv = w4[h4];
-                                const float *x = reinterpret_cast<const float *>(&r[4 * h4]);
-                                s4[0] = fmaf(wv.x, fmaxf(sgn * x[0], 0.0f), s4[0]);
-                                s4[1] = fmaf(wv.y, fmaxf(sgn * x[1], 0.0f), s4[1]);
-                                s4[2] = fmaf(wv.z, fmaxf(sgn * x[2], 0.0f), s4[2]);
-                                s4[3] = fmaf(wv.w, fmaxf(sgn * x[3], 0.0f), s4[3]);
-                            }
                         }
                         const float sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
                         val[sub][i] = use_qs ? sum : fabsf(ksc[sub]) * sum;
