@@ -62,36 +62,66 @@ __global__ void candidate_mask_kernel(float *__restrict__ logits, int64_t ld, in
 // and page rocm_aiter_mla, _expand_page_indices_kernel: position p of
 // sequence b lives at slot block_table[b, p / P] * P + p % P.
 
-__device__ __forceinline__ int slot_of(int p, int b, const int32_t *bt, int64_t bt_stride,
-                                       int max_blocks, int P, int num_pages)
-{
-    if (p < 0)
-        return -1;
-    const int lp = p / P;
-    if (lp >= max_blocks)
-        return -2;
-    const int pg = bt[(size_t)b * bt_stride + lp];
-    if (pg < 0 || pg >= num_pages)
-        return -2;
-    return pg * P + (p - lp * P);
-}
+// Page geometry of the slot map: P tokens per page, shift = log2(P) when P
+// is a power of two, else -1.
+struct SlotGeom {
+    const int32_t *bt;
+    int64_t bt_stride;
+    int max_blocks, P, shift, num_pages;
+};
 
 constexpr int kSlotThreads = 256;
+constexpr int kSlotSteps = 8;  // entries per thread loaded before any is used
+
+// Slots of entries j = base + i * kSlotThreads + tid (i < kSlotSteps) of one
+// top-k row of sequence b: >= 0 a slot, -1 no entry (-1 or past k), -2 an
+// invalid position (logical page beyond max_blocks or page id outside the
+// pool).  The index loads are all issued first, then the block-table loads.
+__device__ __forceinline__ void row_slots(const int32_t *trow, int k, int base, int b,
+                                          const SlotGeom &g, int (&s)[kSlotSteps])
+{
+    int p[kSlotSteps];
+    #pragma unroll
+    for (int i = 0; i < kSlotSteps; ++i) {
+        const int j = base + i * kSlotThreads + (int)threadIdx.x;
+        p[i] = j < k ? __ldg(trow + j) : -1;
+    }
+    int lp[kSlotSteps], pg[kSlotSteps];
+    #pragma unroll
+    for (int i = 0; i < kSlotSteps; ++i) {
+        lp[i] = p[i] < 0 ? -1 : (g.shift >= 0 ? p[i] >> g.shift : p[i] / g.P);
+        pg[i] = lp[i] >= 0 && lp[i] < g.max_blocks
+                    ? __ldg(g.bt + (size_t)b * g.bt_stride + lp[i]) : -1;
+    }
+    #pragma unroll
+    for (int i = 0; i < kSlotSteps; ++i) {
+        if (p[i] < 0)
+            s[i] = -1;
+        else if (lp[i] >= g.max_blocks || pg[i] < 0 || pg[i] >= g.num_pages)
+            s[i] = -2;
+        else
+            s[i] = pg[i] * g.P + (p[i] - lp[i] * g.P);
+    }
+}
 
 __global__ void __launch_bounds__(kSlotThreads)
     slot_count_kernel(const int32_t *__restrict__ topk, int64_t ld, int rows, int k,
-                      const int32_t *__restrict__ row_to_seq, int next_n,
-                      const int32_t *__restrict__ bt, int64_t bt_stride, int max_blocks, int P,
-                      int num_pages, int32_t *__restrict__ lens, unsigned int *status)
+                      const int32_t *__restrict__ row_to_seq, int next_n, SlotGeom g,
+                      int32_t *__restrict__ lens, unsigned int *status)
 {
     __shared__ uint32_t wsum[kSlotThreads / 32];
     const int r = blockIdx.x;
     const int b = row_to_seq ? row_to_seq[r] : r / next_n;
+    const int32_t *trow = topk + (size_t)r * ld;
     uint32_t cnt = 0, bad = 0;
-    for (int j = threadIdx.x; j < k; j += kSlotThreads) {
-        int s = slot_of(topk[(size_t)r * ld + j], b, bt, bt_stride, max_blocks, P, num_pages);
-        cnt += s >= 0;
-        bad += s == -2;
+    for (int base = 0; base < k; base += kSlotSteps * kSlotThreads) {
+        int sl[kSlotSteps];
+        row_slots(trow, k, base, b, g, sl);
+        #pragma unroll
+        for (int i = 0; i < kSlotSteps; ++i) {
+            cnt += sl[i] >= 0;
+            bad += sl[i] == -2;
+        }
     }
     for (int o = 16; o > 0; o >>= 1)
         cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
@@ -152,43 +182,55 @@ __global__ void __launch_bounds__(1024) indptr_scan_kernel(const int32_t *__rest
     }
 }
 
+// Ordered write of one row's valid slots.  Entry order is (step i, warp,
+// lane); a ballot gives each lane its rank inside the warp and step, and
+// warp 0 scans the (step, warp) counts once per batch of kSlotSteps steps.
 __global__ void __launch_bounds__(kSlotThreads)
     slot_write_kernel(const int32_t *__restrict__ topk, int64_t ld, int rows, int k,
-                      const int32_t *__restrict__ row_to_seq, int next_n,
-                      const int32_t *__restrict__ bt, int64_t bt_stride, int max_blocks, int P,
-                      int num_pages, const int32_t *__restrict__ indptr,
-                      int32_t *__restrict__ slots)
+                      const int32_t *__restrict__ row_to_seq, int next_n, SlotGeom g,
+                      const int32_t *__restrict__ indptr, int32_t *__restrict__ slots)
 {
-    __shared__ uint32_t wsum[kSlotThreads / 32 + 1];
+    constexpr int NW = kSlotThreads / 32;
+    static_assert(kSlotSteps * NW == 64, "warp 0 scans 64 (step, warp) counts");
+    __shared__ uint32_t tab[kSlotSteps * NW + 1];
     const int r = blockIdx.x;
     const int b = row_to_seq ? row_to_seq[r] : r / next_n;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const uint32_t lt = (1u << lane) - 1u;
+    const int32_t *trow = topk + (size_t)r * ld;
     int32_t *dst = slots + indptr[r];
     uint32_t written = 0;
-    for (int start = 0; start < k; start += kSlotThreads) {
-        int j = start + threadIdx.x;
-        int s = j < k ? slot_of(topk[(size_t)r * ld + j], b, bt, bt_stride, max_blocks, P,
-                                num_pages)
-                      : -1;
-        uint32_t keep = s >= 0;
-        uint32_t ball = __ballot_sync(0xffffffffu, keep);
-        uint32_t in_warp = __popc(ball & ((1u << lane) - 1u));
-        if (lane == 0)
-            wsum[w] = __popc(ball);
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            uint32_t acc = 0;
-            for (int i = 0; i < kSlotThreads / 32; ++i) {
-                uint32_t t = wsum[i];
-                wsum[i] = acc;
-                acc += t;
-            }
-            wsum[kSlotThreads / 32] = acc;
+    for (int base = 0; base < k; base += kSlotSteps * kSlotThreads) {
+        int sl[kSlotSteps];
+        row_slots(trow, k, base, b, g, sl);
+        uint32_t ball[kSlotSteps];
+        #pragma unroll
+        for (int i = 0; i < kSlotSteps; ++i) {
+            ball[i] = __ballot_sync(0xffffffffu, sl[i] >= 0);
+            if (lane == i)
+                tab[i * NW + w] = __popc(ball[i]);
         }
         __syncthreads();
-        if (keep)
-            dst[written + wsum[w] + in_warp] = s;
-        written += wsum[kSlotThreads / 32];
+        if (w == 0) {
+            const uint32_t a0 = tab[2 * lane], a1 = tab[2 * lane + 1];
+            uint32_t x = a0 + a1;
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t n = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o)
+                    x += n;
+            }
+            const uint32_t ex = x - (a0 + a1);
+            tab[2 * lane] = ex;
+            tab[2 * lane + 1] = ex + a0;
+            if (lane == 31)
+                tab[kSlotSteps * NW] = x;
+        }
+        __syncthreads();
+        #pragma unroll
+        for (int i = 0; i < kSlotSteps; ++i)
+            if (sl[i] >= 0)
+                dst[written + tab[i * NW + w] + __popc(ball[i] & lt)] = sl[i];
+        written += tab[kSlotSteps * NW];
         __syncthreads();
     }
 }
@@ -370,13 +412,21 @@ extern "C" idx_status idx_topk_to_ragged_slots(const int32_t *topk, int64_t ld, 
     unsigned int *status = device_status_ptr();
     if (!status)
         return IDX_ERR_CUDA;
-    slot_count_kernel<<<rows, kSlotThreads, 0, s>>>(topk, ld, rows, k, row_to_seq, next_n,
-                                                    block_table, bt_stride, max_blocks,
-                                                    page_size, num_pages, lens, status);
+    SlotGeom g;
+    g.bt = block_table;
+    g.bt_stride = bt_stride;
+    g.max_blocks = max_blocks;
+    g.P = page_size;
+    g.shift = -1;
+    for (int i = 0; i < 31; ++i)
+        if ((1 << i) == page_size)
+            g.shift = i;
+    g.num_pages = num_pages;
+    slot_count_kernel<<<rows, kSlotThreads, 0, s>>>(topk, ld, rows, k, row_to_seq, next_n, g,
+                                                    lens, status);
     indptr_scan_kernel<<<1, 1024, 0, s>>>(lens, rows, indptr);
-    slot_write_kernel<<<rows, kSlotThreads, 0, s>>>(topk, ld, rows, k, row_to_seq, next_n,
-                                                    block_table, bt_stride, max_blocks,
-                                                    page_size, num_pages, indptr, slots);
+    slot_write_kernel<<<rows, kSlotThreads, 0, s>>>(topk, ld, rows, k, row_to_seq, next_n, g,
+                                                    indptr, slots);
     return launch_status(cudaGetLastError());
 }
 
