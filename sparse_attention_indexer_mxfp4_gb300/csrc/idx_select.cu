@@ -276,8 +276,11 @@ idx_status topk_launch_chunked(const float *logits, int64_t ld, int rows,
             return IDX_ERR_CUDA;
         if (!coop)
             return IDX_ERR_UNSUPPORTED;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, C::phases_kernel, C::kThreads, 0) !=
-                cudaSuccess ||
+        if (cudaFuncSetAttribute(C::phases_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 C::kPhaseDynSmem) != cudaSuccess)
+            return IDX_ERR_CUDA;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, C::phases_kernel, C::kThreads,
+                                                          C::kPhaseDynSmem) != cudaSuccess ||
             n < 1)
             return IDX_ERR_CUDA;
         grid_per_sm[dev] = n;
@@ -312,7 +315,7 @@ idx_status topk_launch_chunked(const float *logits, int64_t ld, int rows,
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)std::max<long long>(1, std::min(cap, want)));
     cfg.blockDim = dim3(C::kThreads);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = C::kPhaseDynSmem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeCooperative;

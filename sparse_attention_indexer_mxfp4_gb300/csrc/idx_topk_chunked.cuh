@@ -42,12 +42,10 @@ constexpr int kMaxChunks = 1024;          // chunks per row (ld <= 8M elements)
 constexpr int kChunksPerThread = kMaxChunks / kRowThreads;
 constexpr int kPlanThreads = 1024;
 constexpr int kCandBatch = 8;             // candidate loads in flight per thread
-// Control words: [0] live chunks, [1] barrier generation, [2] top-level
-// arrivals, then kBarGroups group arrival counters kBarStride words apart
-// (one 128-byte line each, so their atomics do not share a line).
-constexpr int kBarGroups = 16;
-constexpr int kBarStride = 32;
-constexpr int kCtrlWords = kBarStride * (kBarGroups + 1);
+constexpr int kResident = 3;              // chunks a phase CTA keeps in shared memory
+constexpr int kSlotBytes = kCh * 4;       // one resident chunk
+// Control words: [0] live chunks, [1] grid barrier arrivals of the call.
+constexpr int kCtrlWords = 32;
 
 // Workspace (rows R, chunks per row P).  hist, valid and ncand are
 // contiguous and cleared by the plan kernel; everything else is written
@@ -110,6 +108,28 @@ __device__ __forceinline__ void load_chunk(const float *rowp, int c0, int c1, bo
                                            uint32_t (&k)[kVec][4])
 {
     topk_detail::load_keys<kVec>(rowp, c0 + 4 * (int)threadIdx.x, 4 * kThreads, c1, vec, k);
+}
+
+// Keys of a chunk from its shared-memory copy (slot != nullptr; elements
+// past the chunk's n keys read as key 0) or else from global memory, in the
+// same thread / step layout as load_chunk.
+__device__ __forceinline__ void chunk_keys(const float *slot, const float *logits, int64_t ld,
+                                           int4 item, bool vec, uint32_t (&k)[kVec][4])
+{
+    if (slot) {
+        const int n = item.w - item.z;
+        #pragma unroll
+        for (int u = 0; u < kVec; ++u) {
+            const int i0 = 4 * (u * kThreads + (int)threadIdx.x);
+            const float4 v = reinterpret_cast<const float4 *>(slot)[u * kThreads + threadIdx.x];
+            k[u][0] = i0 < n ? topk_detail::float_key(v.x) : 0u;
+            k[u][1] = i0 + 1 < n ? topk_detail::float_key(v.y) : 0u;
+            k[u][2] = i0 + 2 < n ? topk_detail::float_key(v.z) : 0u;
+            k[u][3] = i0 + 3 < n ? topk_detail::float_key(v.w) : 0u;
+        }
+    } else {
+        load_chunk(logits + (size_t)item.x * ld, item.z, item.w, vec, k);
+    }
 }
 
 // Exclusive prefix of v over the CTA in thread order; *tot gets the total.
@@ -181,10 +201,10 @@ __global__ void __launch_bounds__(kPlanThreads)
         }
         carry += tot;
     }
-    if (tid == 0)
+    if (tid == 0) {
         ws.nitems[0] = carry;
-    if (tid <= kBarGroups)  // arrival counters; the generation may hold anything
-        ws.nitems[tid == 0 ? 2 : kBarStride * tid] = 0u;
+        ws.nitems[1] = 0u;  // grid barrier arrivals of this call
+    }
 }
 
 // ------------------------------------------------------------- phase hist
@@ -194,10 +214,10 @@ struct HistShared {
 };
 
 __device__ __forceinline__ void hist_item(const float *logits, int64_t ld, int P, const Ws &ws,
-                                          bool vec, int4 item, HistShared &sh)
+                                          bool vec, int4 item, const float *slot, HistShared &sh)
 {
     uint32_t k[kVec][4];
-    load_chunk(logits + (size_t)item.x * ld, item.z, item.w, vec, k);
+    chunk_keys(slot, logits, ld, item, vec, k);
     for (int i = threadIdx.x; i < 2048; i += kThreads)
         sh.h[i] = 0u;
     if (threadIdx.x == 0)
@@ -235,14 +255,15 @@ struct FilterShared {
 };
 
 __device__ __forceinline__ void filter_item(const float *logits, int64_t ld, int k, int P,
-                                            const Ws &ws, bool vec, int4 item, FilterShared &sh)
+                                            const Ws &ws, bool vec, int4 item, const float *slot,
+                                            FilterShared &sh)
 {
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int row = item.x;
     if (ld_cg(ws.valid + row) <= (uint32_t)k)
         return;  // the row takes all its valid keys (CTA-uniform)
     uint32_t key[kVec][4];
-    load_chunk(logits + (size_t)row * ld, item.z, item.w, vec, key);
+    chunk_keys(slot, logits, ld, item, vec, key);
 
     // threshold bin b1 of the row: thread t holds bins 2047 - 8t down to
     // 2040 - 8t; the count from the top reaches k in exactly one
@@ -564,12 +585,12 @@ __device__ __forceinline__ void chunk_ranks(const uint32_t (&f)[kVec], uint32_t 
 }
 
 __device__ __forceinline__ void write_item(const float *logits, int64_t ld, int k, int P,
-                                           const Ws &ws, bool vec, int4 item, uint32_t *tab,
-                                           int32_t *out, int64_t ld_out)
+                                           const Ws &ws, bool vec, int4 item, const float *slot,
+                                           uint32_t *tab, int32_t *out, int64_t ld_out)
 {
     const int row = item.x;
     uint32_t key[kVec][4];
-    load_chunk(logits + (size_t)row * ld, item.z, item.w, vec, key);
+    chunk_keys(slot, logits, ld, item, vec, key);
     const bool take_all = ld_cg(ws.valid + row) <= (uint32_t)k;
     const uint32_t tk = ld_cg(ws.tkey + (size_t)row * 2);
     const uint32_t quota = ld_cg(ws.cquota + (size_t)row * P + item.y);
@@ -614,40 +635,39 @@ __device__ __forceinline__ void write_item(const float *logits, int64_t ld, int 
 
 // ------------------------------------------------------------ the phases
 //
-// Grid barrier for a cooperative launch (every CTA resident), two levels
-// so no counter takes more than a few dozen atomics: CTA b arrives on group
-// counter b % kBarGroups; the group's last arrival clears that counter and
-// arrives on the top counter; the last top arrival clears it and advances
-// the generation ctrl[1].  The others wait for the generation to move, at
-// most two seconds, after which the status gets the timeout bit and the CTA
-// stops.
+// Grid barrier for a cooperative launch (every CTA resident).  ctrl[1]
+// counts arrivals over the whole call (the plan kernel clears it): the n-th
+// barrier is passed once the count reaches n * gridDim.x.  Thread 0 arrives
+// with a release add, so the CTA's earlier writes (ordered before it by the
+// CTA barrier) are visible to every CTA that then reads the count with an
+// acquire load.  The wait is bounded (two seconds), after which the status
+// gets the timeout bit and the CTA stops.
+__device__ __forceinline__ uint32_t atom_add_release_gpu(uint32_t *p, uint32_t v)
+{
+    uint32_t old;
+    asm volatile("atom.add.release.gpu.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ bool grid_sync(uint32_t *ctrl, unsigned *status,
                                           volatile uint32_t *abort_sh)
 {
     __syncthreads();
     if (threadIdx.x == 0) {
-        volatile uint32_t *vgen = ctrl + 1;
-        const uint32_t g = *vgen;
-        const uint32_t grp = blockIdx.x % kBarGroups;
-        const uint32_t ngroups = min((uint32_t)kBarGroups, gridDim.x);
-        const uint32_t in_grp = (gridDim.x - grp + kBarGroups - 1) / kBarGroups;
-        uint32_t *gc = ctrl + kBarStride * (grp + 1);
-        __threadfence();
-        bool last = false;
-        if (atomicAdd(gc, 1u) == in_grp - 1) {
-            *reinterpret_cast<volatile uint32_t *>(gc) = 0u;
-            __threadfence();
-            if (atomicAdd(ctrl + 2, 1u) == ngroups - 1) {
-                *reinterpret_cast<volatile uint32_t *>(ctrl + 2) = 0u;
-                __threadfence();
-                atomicAdd(ctrl + 1, 1u);
-                last = true;
-            }
-        }
-        if (!last) {
+        uint32_t *count = ctrl + 1;
+        const uint32_t old = atom_add_release_gpu(count, 1u);
+        const uint32_t target = (old / gridDim.x + 1u) * gridDim.x;
+        if (ld_acquire_gpu(count) < target) {
             const uint64_t t0 = globaltimer_ns();
-            while (*vgen == g) {
-                __nanosleep(32);
+            while (ld_acquire_gpu(count) < target) {
+                __nanosleep(20);
                 if (globaltimer_ns() - t0 > 2000000000ull) {
                     atomicOr(status, kDevTimeout);
                     *abort_sh = 1u;
@@ -655,7 +675,6 @@ __device__ __forceinline__ bool grid_sync(uint32_t *ctrl, unsigned *status,
                 }
             }
         }
-        __threadfence();
     }
     __syncthreads();
     return *abort_sh == 0u;
@@ -682,22 +701,59 @@ union PhaseShared {
 
 static_assert(kRowThreads == kThreads, "the resolve phase runs in the chunk CTAs");
 
-__global__ void __launch_bounds__(kThreads, 3) phases_kernel(const __grid_constant__ PhaseArgs a)
+// Dynamic shared memory of the phases kernel: kResident chunk slots.
+constexpr int kPhaseDynSmem = kResident * kSlotBytes;
+
+__global__ void __launch_bounds__(kThreads, 2) phases_kernel(const __grid_constant__ PhaseArgs a)
 {
     __shared__ PhaseShared sh;
     __shared__ uint32_t abort_flag;
-    if (threadIdx.x == 0)
-        abort_flag = 0u;
+    __shared__ int wait_abort;
+    __shared__ __align__(8) uint64_t slot_full[kResident];
+    extern __shared__ __align__(128) uint8_t dyn[];
     const bool vec = a.vec_ok != 0;
     const uint32_t nitems = a.ws.nitems[0];
     uint32_t *ctrl = a.ws.nitems;
+    // The CTA's j-th item is blockIdx.x + j * gridDim.x; the first kResident
+    // of them are copied into shared memory once (one bulk copy each, needs
+    // 16-byte aligned rows) and every phase reads them from there.
+    const bool resident = vec;
+    if (threadIdx.x == 0) {
+        abort_flag = 0u;
+        wait_abort = 0;
+        for (int j = 0; j < kResident; ++j)
+            mbar_init(&slot_full[j], 1);
+        fence_mbar_init();
+        if (resident)
+            for (int j = 0; j < kResident; ++j) {
+                const uint32_t it = blockIdx.x + (uint32_t)j * gridDim.x;
+                if (it >= nitems)
+                    break;
+                const int4 item = a.ws.items[it];
+                // whole 16-byte groups: the row holds ld (a multiple of 4) floats
+                const uint32_t bytes = (uint32_t)(((item.w - item.z) * 4 + 15) & ~15);
+                mbar_arrive_expect_tx(&slot_full[j], bytes);
+                bulk_load(dyn + j * kSlotBytes, a.logits + (size_t)item.x * a.ld + item.z, bytes,
+                          &slot_full[j]);
+            }
+    }
     __syncthreads();
-    for (uint32_t it = blockIdx.x; it < nitems; it += gridDim.x)
-        hist_item(a.logits, a.ld, a.P, a.ws, vec, a.ws.items[it], sh.hist);
+    auto slot_of = [&](int j) -> const float * {
+        return resident && j < kResident ? reinterpret_cast<const float *>(dyn + j * kSlotBytes)
+                                         : nullptr;
+    };
+    int j = 0;
+    for (uint32_t it = blockIdx.x; it < nitems; it += gridDim.x, ++j) {
+        if (resident && j < kResident &&
+            !mbar_wait(&slot_full[j], 0u, &wait_abort, a.status))
+            abort_flag = 1u;  // a copy did not land in time: stop at the next barrier
+        hist_item(a.logits, a.ld, a.P, a.ws, vec, a.ws.items[it], slot_of(j), sh.hist);
+    }
     if (!grid_sync(ctrl, a.status, &abort_flag))
         return;
-    for (uint32_t it = blockIdx.x; it < nitems; it += gridDim.x)
-        filter_item(a.logits, a.ld, a.k, a.P, a.ws, vec, a.ws.items[it], sh.filter);
+    j = 0;
+    for (uint32_t it = blockIdx.x; it < nitems; it += gridDim.x, ++j)
+        filter_item(a.logits, a.ld, a.k, a.P, a.ws, vec, a.ws.items[it], slot_of(j), sh.filter);
     if (!grid_sync(ctrl, a.status, &abort_flag))
         return;
     for (int row = blockIdx.x; row < a.R; row += gridDim.x)
@@ -705,8 +761,10 @@ __global__ void __launch_bounds__(kThreads, 3) phases_kernel(const __grid_consta
                     a.ld_out);
     if (!grid_sync(ctrl, a.status, &abort_flag))
         return;
-    for (uint32_t it = blockIdx.x; it < nitems; it += gridDim.x)
-        write_item(a.logits, a.ld, a.k, a.P, a.ws, vec, a.ws.items[it], sh.tab, a.out, a.ld_out);
+    j = 0;
+    for (uint32_t it = blockIdx.x; it < nitems; it += gridDim.x, ++j)
+        write_item(a.logits, a.ld, a.k, a.P, a.ws, vec, a.ws.items[it], slot_of(j), sh.tab,
+                   a.out, a.ld_out);
 }
 
 } // namespace topk_chunked
