@@ -519,67 +519,87 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
                 // the warp is converged at every tcgen05.ld.
                 const bool all_pos = __all_sync(0xffffffffu, pos);
                 const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * C::ACC_COLS;
-                #pragma unroll
-                for (int sub = 0; sub < NSUB; ++sub) {
-                    const float sgn = ksc[sub] >= 0.0f ? 1.0f : -1.0f;
+                if (!use_qs && all_pos) {
+                    // Common path.  The (sub-tile, row, half) blocks of 32 heads
+                    // are loaded from TMEM into two register buffers in turn: the
+                    // load of the next block is in flight while this one is
+                    // summed (tcgen05.wait::ld then waits for it).  Each row sums
+                    // its heads in eight partial sums, four packed-FMA chains.
+                    // Rows past the group's last are computed and discarded.
+                    constexpr int NU = NSUB * G * 2;
+                    uint32_t rb[2][32];
+                    float2 cc[4];
+                    tmem_ld_32x32b_x32(tbase, rb[0]);
+                    tmem_ld_wait();
                     #pragma unroll
-                    for (int i = 0; i < G; ++i) {
-                        if (i >= w.gi.nrows)
-                            break;
-                        const uint32_t trow = tbase + sub * C::NCOLS + i * H;
-                        const float4 *w4 = reinterpret_cast<const float4 *>(wsm + i * H);
-                        float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // independent partial sums
-                        if (use_qs || !all_pos) {
-                            // rare (per-head q scales, or a negative key scale):
-                            // a rolled loop over four heads at a time keeps the
-                            // code small; the common path below is unrolled
-                            const float *qrow = qsm + i * H;
-                            #pragma unroll 1
-                            for (int h = 0; h < H; h += 4) {
-                                uint32_t x4[4];
-                                tmem_ld_32x32b_x4(trow + h, x4);
-                                tmem_ld_wait();
-                                const float4 wv = w4[h >> 2];
-                                const float wj[4] = {wv.x, wv.y, wv.z, wv.w};
-                                #pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    const float x = __uint_as_float(x4[e]);
-                                    const float y = use_qs ? ksc[sub] * qrow[h + e] * x : sgn * x;
-                                    s4[e] = fmaf(wj[e], fmaxf(y, 0.0f), s4[e]);
+                    for (int u = 0; u < NU; ++u) {
+                        const int sub = u / (2 * G), i = (u / 2) % G, half = u & 1;
+                        if (u + 1 < NU) {
+                            const int s1 = (u + 1) / (2 * G), i1 = ((u + 1) / 2) % G,
+                                      h1 = (u + 1) & 1;
+                            tmem_ld_32x32b_x32(tbase + s1 * C::NCOLS + i1 * H + h1 * 32,
+                                               rb[(u + 1) & 1]);
+                        }
+                        if (half == 0) {
+                            #pragma unroll
+                            for (int jj = 0; jj < 4; ++jj)
+                                cc[jj] = make_float2(0.0f, 0.0f);
+                        }
+                        const float4 *w4 = reinterpret_cast<const float4 *>(wsm + i * H + half * 32);
+                        #pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const int h4 = half * 8 + q;
+                            const float4 wv = w4[q];
+                            const float *x = reinterpret_cast<const float *>(&rb[u & 1][4 * q]);
+                            const int jj = (h4 & 1) * 2;
+                            cc[jj] = fma2(make_float2(wv.x, wv.y),
+                                          make_float2(fmaxf(x[0], 0.0f), fmaxf(x[1], 0.0f)), cc[jj]);
+                            cc[jj + 1] = fma2(make_float2(wv.z, wv.w),
+                                              make_float2(fmaxf(x[2], 0.0f), fmaxf(x[3], 0.0f)),
+                                              cc[jj + 1]);
+                        }
+                        if (half == 1) {
+                            const float sum = ((cc[0].x + cc[2].x) + (cc[0].y + cc[2].y)) +
+                                              ((cc[1].x + cc[3].x) + (cc[1].y + cc[3].y));
+                            val[sub][i] = fabsf(ksc[sub]) * sum;
+                        }
+                        if (u + 1 < NU)
+                            tmem_ld_wait();
+                    }
+                } else {
+                    #pragma unroll
+                    for (int sub = 0; sub < NSUB; ++sub) {
+                        const float sgn = ksc[sub] >= 0.0f ? 1.0f : -1.0f;
+                        #pragma unroll
+                        for (int i = 0; i < G; ++i) {
+                            if (i >= w.gi.nrows)
+                                break;
+                            const uint32_t trow = tbase + sub * C::NCOLS + i * H;
+                            const float4 *w4 = reinterpret_cast<const float4 *>(wsm + i * H);
+                            float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // independent partial sums
+                            {
+                                // rare (per-head q scales, or a negative key scale):
+                                // a rolled loop over four heads at a time keeps the
+                                // code small
+                                const float *qrow = qsm + i * H;
+                                #pragma unroll 1
+                                for (int h = 0; h < H; h += 4) {
+                                    uint32_t x4[4];
+                                    tmem_ld_32x32b_x4(trow + h, x4);
+                                    tmem_ld_wait();
+                                    const float4 wv = w4[h >> 2];
+                                    const float wj[4] = {wv.x, wv.y, wv.z, wv.w};
+                                    #pragma unroll
+                                    for (int e = 0; e < 4; ++e) {
+                                        const float x = __uint_as_float(x4[e]);
+                                        const float y = use_qs ? ksc[sub] * qrow[h + e] * x : sgn * x;
+                                        s4[e] = fmaf(wj[e], fmaxf(y, 0.0f), s4[e]);
+                                    }
                                 }
                             }
-                        } else {
-                            // the row's H scores of this key: two TMEM loads, one wait
-                            uint32_t r[H];
-                            #pragma unroll
-                            for (int hc = 0; hc < H / 32; ++hc)
-                                tmem_ld_32x32b_x32(trow + hc * 32,
-                                                   *reinterpret_cast<uint32_t(*)[32]>(&r[hc * 32]));
-                            tmem_ld_wait();
-                            // eight partial sums in four packed-FMA chains,
-                            // so consecutive FMAs do not wait on each other
-                            float2 cc[4];
-                            #pragma unroll
-                            for (int j = 0; j < 4; ++j)
-                                cc[j] = make_float2(0.0f, 0.0f);
-                            #pragma unroll
-                            for (int h4 = 0; h4 < H / 4; ++h4) {
-                                const float4 wv = w4[h4];
-                                const float *x = reinterpret_cast<const float *>(&r[4 * h4]);
-                                const int j = (h4 & 1) * 2;
-                                cc[j] = fma2(make_float2(wv.x, wv.y),
-                                             make_float2(fmaxf(x[0], 0.0f), fmaxf(x[1], 0.0f)), cc[j]);
-                                cc[j + 1] = fma2(make_float2(wv.z, wv.w),
-                                                 make_float2(fmaxf(x[2], 0.0f), fmaxf(x[3], 0.0f)),
-                                                 cc[j + 1]);
-                            }
-                            s4[0] = cc[0].x + cc[2].x;
-                            s4[1] = cc[0].y + cc[2].y;
-                            s4[2] = cc[1].x + cc[3].x;
-                            s4[3] = cc[1].y + cc[3].y;
+                            const float sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+                            val[sub][i] = use_qs ? sum : fabsf(ksc[sub]) * sum;
                         }
-                        const float sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
-                        val[sub][i] = use_qs ? sum : fabsf(ksc[sub]) * sum;
                     }
                 }
                 tc_fence_before();
