@@ -117,8 +117,7 @@ cudaError_t launch_logits_t(const LogitsArgs &a0, const CUtensorMap &tmK, const 
             return e;
         configured[dev] = 1;
     }
-    kern<<<nctas, C::THREADS, smem, stream>>>(a, tmK, tmQ, tmS);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(nctas), dim3(C::THREADS), smem, stream, a, tmK, tmQ, tmS);
 }
 
 // Shared memory the launch needs; 0 if the combination has no kernel.

@@ -294,6 +294,22 @@ IDX_DEVFN uint64_t make_smem_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t s
 
 // ------------------------------------------------------------- misc helpers
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start before the previous kernel on its stream has
+// finished; pdl_wait() blocks until that kernel has completed and its memory
+// operations are visible, so everything a kernel reads or writes that an
+// earlier kernel may touch comes after it.  pdl_launch_dependents() lets the
+// next such kernel start launching.  Both are no-ops without the attribute.
+IDX_DEVFN void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+IDX_DEVFN void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Two fp32 fused multiply-adds in one packed instruction: (a * b + c) per
 // lane, each rounded to nearest like fmaf.
 IDX_DEVFN float2 fma2(float2 a, float2 b, float2 c)

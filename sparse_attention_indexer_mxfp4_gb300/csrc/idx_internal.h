@@ -32,4 +32,24 @@ inline idx_status launch_status(cudaError_t e)
     return e == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
 }
 
+// Launch with programmatic stream serialization: the kernel may begin while
+// the previous kernel on the stream finishes; it must call pdl_wait() before
+// touching memory an earlier kernel may use.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 } // namespace idx

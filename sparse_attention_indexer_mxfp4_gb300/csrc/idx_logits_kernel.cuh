@@ -194,6 +194,10 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
         tmem_alloc(tmem_slot, C::TM_COLS);
         tmem_relinquish();
     }
+    // everything above touches only this CTA's own resources; inputs and the
+    // logits buffer may still be in use by the previous kernel on the stream
+    pdl_wait();
+    pdl_launch_dependents();
     int g0, j0;
     long long count;
     locate_units(a, scratch, g0, j0, count);  // contains __syncthreads

@@ -110,6 +110,8 @@ __global__ void __launch_bounds__(kSlotThreads)
                       int32_t *__restrict__ lens, unsigned int *status)
 {
     __shared__ uint32_t wsum[kSlotThreads / 32];
+    pdl_wait();
+    pdl_launch_dependents();
     const int r = blockIdx.x;
     const int b = row_to_seq ? row_to_seq[r] : r / next_n;
     const int32_t *trow = topk + (size_t)r * ld;
@@ -143,6 +145,8 @@ __global__ void __launch_bounds__(1024) indptr_scan_kernel(const int32_t *__rest
 {
     __shared__ int32_t wsum[32];
     __shared__ int32_t carry;
+    pdl_wait();
+    pdl_launch_dependents();
     if (threadIdx.x == 0) {
         carry = 0;
         indptr[0] = 0;
@@ -193,6 +197,8 @@ __global__ void __launch_bounds__(kSlotThreads)
     constexpr int NW = kSlotThreads / 32;
     static_assert(kSlotSteps * NW == 64, "warp 0 scans 64 (step, warp) counts");
     __shared__ uint32_t tab[kSlotSteps * NW + 1];
+    pdl_wait();
+    pdl_launch_dependents();
     const int r = blockIdx.x;
     const int b = row_to_seq ? row_to_seq[r] : r / next_n;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -304,8 +310,8 @@ idx_status topk_launch_chunked(const float *logits, int64_t ld, int rows,
     const long long zero_vec4 = ((long long)rows * (2048 + 2) + 3) / 4;
     const int g_plan = (int)std::max<long long>(
         1, std::min<long long>(sm_count(), (zero_vec4 + C::kPlanThreads - 1) / C::kPlanThreads));
-    C::plan_kernel<<<g_plan, C::kPlanThreads, 0, s>>>(lengths, ld, rows, a.ws);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(C::plan_kernel, dim3(g_plan), dim3(C::kPlanThreads), 0, s, lengths,
+                               ld, rows, a.ws);
     if (e != cudaSuccess)
         return IDX_ERR_CUDA;
     // every CTA resident (the phases wait on one another), no more CTAs
@@ -425,12 +431,14 @@ extern "C" idx_status idx_topk_to_ragged_slots(const int32_t *topk, int64_t ld, 
         if ((1 << i) == page_size)
             g.shift = i;
     g.num_pages = num_pages;
-    slot_count_kernel<<<rows, kSlotThreads, 0, s>>>(topk, ld, rows, k, row_to_seq, next_n, g,
-                                                    lens, status);
-    indptr_scan_kernel<<<1, 1024, 0, s>>>(lens, rows, indptr);
-    slot_write_kernel<<<rows, kSlotThreads, 0, s>>>(topk, ld, rows, k, row_to_seq, next_n, g,
-                                                    indptr, slots);
-    return launch_status(cudaGetLastError());
+    cudaError_t e = launch_pdl(slot_count_kernel, dim3(rows), dim3(kSlotThreads), 0, s, topk, ld,
+                               rows, k, row_to_seq, next_n, g, lens, status);
+    if (e == cudaSuccess)
+        e = launch_pdl(indptr_scan_kernel, dim3(1), dim3(1024), 0, s, lens, rows, indptr);
+    if (e == cudaSuccess)
+        e = launch_pdl(slot_write_kernel, dim3(rows), dim3(kSlotThreads), 0, s, topk, ld, rows, k,
+                       row_to_seq, next_n, g, indptr, slots);
+    return launch_status(e);
 }
 
 // ------------------------------------------------ top-k without allocation

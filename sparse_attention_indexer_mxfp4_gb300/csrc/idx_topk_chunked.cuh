@@ -178,6 +178,7 @@ __global__ void __launch_bounds__(kPlanThreads)
     plan_kernel(const int32_t *__restrict__ lengths, int64_t ld, int R, Ws ws)
 {
     __shared__ uint32_t red[kPlanThreads / 32];
+    pdl_wait();  // the workspace and lengths may belong to the previous kernel until here
     const int tid = threadIdx.x;
     const size_t nz = (size_t)R * (2048 + 2);  // hist, valid, ncand are contiguous
     const size_t stride = (size_t)gridDim.x * kPlanThreads;
