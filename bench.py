@@ -160,9 +160,33 @@ def job_value(world: int, keys_per_rank: int, ms_per_step: float) -> float:
     return world * keys_per_rank / (ms_per_step * 1e-3) / 1e9
 
 
+def candidate_box_keys(case) -> int:
+    """Keys in the 64-key boxes that hold a candidate key of some row of their
+    sequence (candidate blocks clipped to each row's [ks, ke))."""
+    ke = np.clip(case.row_ends(), 0, case.width).reshape(case.B, case.next_n)
+    ks = (np.zeros_like(ke) if case.row_ks is None else
+          np.minimum(case.row_ks.reshape(case.B, case.next_n), ke))
+    total = 0
+    for b in range(case.B):
+        hi = int(ke[b].max())
+        boxes = np.zeros(-(-hi // 64) + 1, dtype=bool)
+        for j in range(case.next_n):
+            r = b * case.next_n + j
+            ids = case.cand[r]
+            ids = ids[ids >= 0].astype(np.int64)
+            lo = int(ks[b, j]) + ids * case.cand_block
+            hi_r = np.minimum(lo + case.cand_block, int(ke[b, j]))
+            for t0, t1 in zip(lo[lo < hi_r], hi_r[lo < hi_r]):
+                boxes[t0 // 64:(t1 - 1) // 64 + 1] = True
+        idx = np.nonzero(boxes)[0]
+        total += int(np.minimum(64, hi - idx * 64).clip(min=0).sum())
+    return total
+
+
 def logits_bytes(case) -> float:
-    """Algorithmic bytes of one logits launch: every live key's values and
-    scale read once per sequence, the group's queries, weights and candidate
+    """Algorithmic bytes of one logits stage: every live key's values and
+    scale read once per sequence (with a candidate mask, only the keys of
+    boxes that hold a candidate), the group's queries, weights and candidate
     ids read once, one fp32 logit written per scored (row, key), block-table
     entries read once per page."""
     from sparse_attention_indexer_mxfp4_gb300.synth import FMT_FP8, PagedCase
@@ -172,7 +196,12 @@ def logits_bytes(case) -> float:
     if isinstance(case, PagedCase):
         ke = np.clip(case.row_ends(), 0, case.width)
         seq_keys = ke.reshape(case.B, case.next_n).max(axis=1)
-        b = float(seq_keys.sum()) * per_key
+        if case.cand is not None:
+            # gather path: only 64-key boxes holding a candidate key of any
+            # row of the sequence are read
+            b = float(candidate_box_keys(case)) * per_key
+        else:
+            b = float(seq_keys.sum()) * per_key
         b += case.rows * per_q
         b += float(ke.sum()) * 4
         b += float(np.ceil(seq_keys / case.page_size).sum()) * 4
@@ -251,7 +280,10 @@ def run_ours(args):
     else:
         roof = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(achieved_gbs / hbm, 4), "traffic": logits_traffic(args.config),
-                "peak_source": f"{src} hbm_gbs", "kernel": "logits_kernel",
+                "peak_source": f"{src} hbm_gbs",
+                "kernel": ("logits stage: cand_plan_kernel (candidate plan, -inf fill) + "
+                           "logits_kernel" if getattr(case, "cand", None) is not None
+                           else "logits_kernel"),
                 "algorithmic_bytes_per_launch": lb, "avg_launch_ms": round(logit_avg, 5)}
     out = {
         "metric": METRIC, "value": round(job_value(world, keys, ms_per_step), 4),

@@ -117,6 +117,15 @@ idx_status idx_mqa_logits(const void *q, const void *q_scale, const float *weigh
  *             columns [0, ke) of each row are written; [ke, max_model_len) is
  *             left untouched (consumers read each row up to its length).
  *   num_ctas  0 = one persistent CTA per SM; otherwise the grid size.
+ *   ws, ws_bytes  optional device scratch, 16-byte aligned.  With a fused
+ *             candidate mask and ws_bytes >= idx_paged_mqa_logits_workspace_size
+ *             (B, next_n, max_model_len, num_cand), a first kernel writes a
+ *             plan of the tiles and 64-key boxes that hold a candidate key of
+ *             any row of a sequence, and the logits kernel loads and scores
+ *             only those (every other key of [0, ke) is written -inf, as the
+ *             mask requires): the same logits, fewer K bytes read.  Block-table
+ *             entries of pages that are never loaded are then not checked.
+ *             Calls sharing one ws must not overlap in time.
  * Supported: D = 128, page_size a multiple of 64, next_n * H <= 256.
  * ---------------------------------------------------------------------- */
 idx_status idx_paged_mqa_logits(const void *q, const void *q_scale, const float *weights,
@@ -129,6 +138,10 @@ idx_status idx_paged_mqa_logits(const void *q, const void *q_scale, const float 
                                 int num_cand, int cand_block, float *logits,
                                 int64_t ld_logits, int max_model_len, int num_ctas, void *ws,
                                 size_t ws_bytes, idx_stream_t stream);
+
+/* Bytes of ws the gather path of idx_paged_mqa_logits needs (0 without a
+ * candidate mask: num_cand <= 0).  Pure host arithmetic. */
+size_t idx_paged_mqa_logits_workspace_size(int B, int next_n, int max_model_len, int num_cand);
 
 /* ------------------------------------------------------------------------
  * idx_apply_candidate_mask -- in-place candidate mask on existing logits.

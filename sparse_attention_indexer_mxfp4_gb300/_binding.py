@@ -66,6 +66,8 @@ def lib() -> ctypes.CDLL:
             L.idx_version.restype = ctypes.c_char_p
             L.idx_topk_workspace_size.argtypes = [_I, _L, _I]
             L.idx_topk_workspace_size.restype = _S
+            L.idx_paged_mqa_logits_workspace_size.argtypes = [_I, _I, _I, _I]
+            L.idx_paged_mqa_logits_workspace_size.restype = _S
             _lib = L
     return _lib
 
@@ -147,7 +149,10 @@ def idx_mqa_logits(q, q_scale, weights, k, k_scale, row_ks, row_ke, fmt, logits,
 def prepare_paged_mqa_logits(q, q_scale, weights, kv_pages, block_table, context_lens, next_n,
                              page_size, fmt, logits, max_model_len, row_ks=None,
                              ctx_per_row=False, candidate_blocks=None, cand_block=0,
-                             num_ctas=0):
+                             num_ctas=0, workspace=True):
+    """workspace (used with candidate_blocks): True allocates the gather plan
+    scratch here (held by the returned call), a uint8 CUDA tensor supplies it,
+    False or None scores every key of the context."""
     q = _u8(q)
     rows, H = q.shape[0], q.shape[1]
     D = q.shape[2] if fmt == FMT_FP8 else 2 * q.shape[2]
@@ -161,25 +166,40 @@ def prepare_paged_mqa_logits(q, q_scale, weights, kv_pages, block_table, context
     if candidate_blocks is not None:
         _need(candidate_blocks, torch.int32, "candidate_blocks")
         cand_stride, num_cand = candidate_blocks.stride(0), candidate_blocks.shape[1]
+    ws = None
+    need = paged_workspace_size(B, next_n, max_model_len, num_cand)
+    if need and workspace is True:
+        ws = torch.empty(need, dtype=torch.uint8, device=logits.device)
+    elif need and workspace is not None and workspace is not False:
+        ws = workspace
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
     args = (_ptr(q), _ptr(q_scale), _ptr(weights), _ptr(kv_pages), kv_pages.stride(0),
             kv_pages.shape[0], _ptr(block_table), block_table.stride(0), _ptr(context_lens),
             int(ctx_per_row), _ptr(row_ks), B, next_n, H, D, page_size, fmt,
             _ptr(candidate_blocks), cand_stride, num_cand, cand_block, _ptr(logits),
-            logits.stride(0), max_model_len, num_ctas, None, 0)
+            logits.stride(0), max_model_len, num_ctas, _ptr(ws), nbytes)
+    # with a plan the library launches the plan kernel before the logits kernel
+    planned = ws is not None and need > 0 and nbytes >= need
     return Prepared("idx_paged_mqa_logits", args, (q, q_scale, weights, kv_pages, block_table,
                                                    context_lens, row_ks, candidate_blocks,
-                                                   logits))
+                                                   logits, ws), 2 if planned else 1)
+
+
+def paged_workspace_size(B, next_n, max_model_len, num_cand) -> int:
+    """Bytes of the gather-plan scratch of idx_paged_mqa_logits (0: not used)."""
+    return int(lib().idx_paged_mqa_logits_workspace_size(B, next_n, max_model_len, num_cand))
 
 
 def idx_paged_mqa_logits(q, q_scale, weights, kv_pages, block_table, context_lens, next_n,
                          page_size, fmt, logits, max_model_len, row_ks=None, ctx_per_row=False,
-                         candidate_blocks=None, cand_block=0, num_ctas=0, stream=None):
+                         candidate_blocks=None, cand_block=0, num_ctas=0, stream=None,
+                         workspace=True):
     """Paged logits.  q [B*next_n,H,D|D/2] bytes; kv_pages uint8 [num_pages, page_stride];
     block_table int32 [B, >= ceil(max_model_len/page_size)]; logits fp32
     [B*next_n, >= max_model_len]."""
     prepare_paged_mqa_logits(q, q_scale, weights, kv_pages, block_table, context_lens, next_n,
                              page_size, fmt, logits, max_model_len, row_ks, ctx_per_row,
-                             candidate_blocks, cand_block, num_ctas)(stream)
+                             candidate_blocks, cand_block, num_ctas, workspace)(stream)
 
 
 def prepare_apply_candidate_mask(logits, row_ks, row_ke, candidate_blocks, block_size,

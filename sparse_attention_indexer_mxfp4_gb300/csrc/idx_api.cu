@@ -104,18 +104,20 @@ cudaError_t launch_logits_t(const LogitsArgs &a0, const CUtensorMap &tmK, const 
     LogitsArgs a = a0;
     a.tile_shift = TK == 256 ? 8 : 7;
     const size_t smem = (size_t)C::fixed_bytes() + (size_t)2 * G * a.cand_words * 4;
-    auto kern = logits_kernel<FMT, H, G, S, NA, TK>;
-    // raise the dynamic shared memory limit once per device to the maximum
-    static int configured[kMaxDevices] = {};
+    const int plan = a.plan ? 1 : 0;
+    auto kern = plan ? logits_kernel<FMT, H, G, S, NA, TK, true>
+                     : logits_kernel<FMT, H, G, S, NA, TK, false>;
+    // raise each kernel's dynamic shared memory limit once per device
+    static int configured[2][kMaxDevices] = {};
     const int dev = current_device();
     if (dev < 0 || dev >= kMaxDevices)
         return cudaErrorInvalidDevice;
-    if (!configured[dev]) {
+    if (!configured[plan][dev]) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)kMaxSmemBytes);
         if (e != cudaSuccess)
             return e;
-        configured[dev] = 1;
+        configured[plan][dev] = 1;
     }
     return launch_pdl(kern, dim3(nctas), dim3(C::THREADS), smem, stream, a, tmK, tmQ, tmS);
 }
@@ -137,7 +139,12 @@ cudaError_t launch_logits(int fmt, int H, int G, const LogitsArgs &a, const CUte
     if (H == 64 && fmt == kFmtFp8) {
         switch (G) {
         case 1: return launch_logits_t<kFmtFp8, 64, 1, 4, 2, 256>(a, tmK, tmQ, tmS, nctas, s);
-        case 2: return launch_logits_t<kFmtFp8, 64, 2, 4, 2, 256>(a, tmK, tmQ, tmS, nctas, s);
+        case 2:
+            // under a gather plan, 128-key tiles: candidate blocks of 128 keys
+            // then fill whole tiles and stages
+            if (a.plan)
+                return launch_logits_t<kFmtFp8, 64, 2, 6, 3, 128>(a, tmK, tmQ, tmS, nctas, s);
+            return launch_logits_t<kFmtFp8, 64, 2, 4, 2, 256>(a, tmK, tmQ, tmS, nctas, s);
         case 4: return launch_logits_t<kFmtFp8, 64, 4, 8, 2, 128>(a, tmK, tmQ, tmS, nctas, s);
         }
     } else if (H == 64 && fmt == kFmtMxfp4) {
@@ -150,12 +157,43 @@ cudaError_t launch_logits(int fmt, int H, int G, const LogitsArgs &a, const CUte
     return cudaSuccess;
 }
 
+// log2 of the keys per tile of the instantiation launch_logits picks.
+int logits_tile_shift(int fmt, int G, bool plan)
+{
+    if (fmt == kFmtFp8)
+        return G == 4 || (G == 2 && plan) ? 7 : 8;
+    return G == 2 ? 7 : 8;
+}
+
+// Gather-plan geometry for a row width: box bits for 64-key boxes and a
+// tile list long enough for 128-key tiles (the most tiles any instantiation
+// has); the plan kernel's shared memory also holds the tile bits.
+void plan_geom(int width, int *box_words, int *plan_words, int *tile_words)
+{
+    const int tiles = (width + kMmaM - 1) / kMmaM;
+    const int boxes = (width + kHalfKeys - 1) / kHalfKeys;
+    *box_words = (boxes + 31) / 32;
+    *tile_words = (tiles + 31) / 32;
+    *plan_words = (1 + *box_words + tiles + 3) / 4 * 4;
+}
+
+cudaError_t launch_plan(const LogitsArgs &a, int groups, int tile_words, cudaStream_t s)
+{
+    const size_t smem = (size_t)(a.box_words + tile_words) * 4;
+    const dim3 grid(groups, kPlanSlices);
+    if (a.tile_shift == 8)
+        return launch_pdl(cand_plan_kernel<8>, grid, dim3(kPlanThreads), smem, s, a);
+    return launch_pdl(cand_plan_kernel<7>, grid, dim3(kPlanThreads), smem, s, a);
+}
+
 size_t logits_smem(int fmt, int H, int G, int cand_words)
 {
     if (H == 64 && fmt == kFmtFp8) {
         switch (G) {
         case 1: return logits_smem_t<kFmtFp8, 64, 1, 4, 2, 256>(cand_words);
-        case 2: return logits_smem_t<kFmtFp8, 64, 2, 4, 2, 256>(cand_words);
+        case 2:
+            return std::max(logits_smem_t<kFmtFp8, 64, 2, 4, 2, 256>(cand_words),
+                            logits_smem_t<kFmtFp8, 64, 2, 6, 3, 128>(cand_words));
         case 4: return logits_smem_t<kFmtFp8, 64, 4, 8, 2, 128>(cand_words);
         }
     } else if (H == 64 && fmt == kFmtMxfp4) {
@@ -379,12 +417,35 @@ extern "C" idx_status idx_paged_mqa_logits(
     if (!a.status)
         return IDX_ERR_CUDA;
     const int nctas = num_ctas > 0 ? num_ctas : sm_count();
+    // gather path: with a fused candidate mask and scratch for the plan, only
+    // tiles and 64-key boxes that hold a candidate key are loaded and scored
+    const size_t plan_need =
+        idx_paged_mqa_logits_workspace_size(B, next_n, max_model_len, a.cand ? num_cand : 0);
+    if (plan_need > 0 && ws && ws_bytes >= plan_need && aligned16(ws)) {
+        int tile_words = 0;
+        a.plan = static_cast<uint32_t *>(ws);
+        plan_geom(max_model_len, &a.box_words, &a.plan_words, &tile_words);
+        a.tile_shift = logits_tile_shift(f, G, true);
+        if (launch_plan(a, B, tile_words, (cudaStream_t)stream) != cudaSuccess)
+            return IDX_ERR_CUDA;
+    }
     bool supported = false;
     cudaError_t e =
         launch_logits(f, H, G, a, tmK, tmQ, tmS, nctas, (cudaStream_t)stream, &supported);
     if (!supported)
         return IDX_ERR_UNSUPPORTED;
     return launch_status(e);
+}
+
+extern "C" size_t idx_paged_mqa_logits_workspace_size(int B, int next_n, int max_model_len,
+                                                      int num_cand)
+{
+    (void)next_n;
+    if (B <= 0 || max_model_len <= 0 || num_cand <= 0)
+        return 0;
+    int bw, pw, tw;
+    plan_geom(max_model_len, &bw, &pw, &tw);
+    return (size_t)B * pw * 4;
 }
 
 extern "C" idx_status idx_get_device_status(idx_stream_t stream, uint32_t *out)

@@ -66,7 +66,22 @@ struct LogitsArgs {
     int width;               // paged: max_model_len; contiguous: N
     unsigned int *status;    // device status word (IDX_DEV_* bits)
     int tile_shift;          // log2 of the keys per tile (7 or 8)
+    // Candidate gather plan (nullable), written by cand_plan_kernel: per row
+    // group plan_words words: [0] the number n of compute tiles (tiles that
+    // hold a candidate key of any of the group's rows), then box_words words
+    // of per-64-key-box bits (boxes holding a candidate key), then the n
+    // compute tile indices in ascending order.  Only those tiles are scored
+    // and only those boxes loaded; every other key is -inf anyway.
+    uint32_t *plan;
+    int plan_words, box_words;
 };
+
+// Plan bit of 64-key box b of group g (true without a plan).
+__device__ __forceinline__ bool plan_box(const LogitsArgs &a, int g, int b)
+{
+    return !a.plan ||
+           ((__ldg(a.plan + (size_t)g * a.plan_words + 1 + (b >> 5)) >> (b & 31)) & 1u);
+}
 
 // Key range [ks, ke) of row r, clamped as the oracle clamps it.
 __device__ __forceinline__ void row_range(const LogitsArgs &a, int r, int &ks, int &ke)
@@ -132,6 +147,7 @@ __device__ __forceinline__ bool tile_is_compute(const GroupInfo &gi, int j, int 
 // copy and sees the same sequence.
 struct UnitWalk {
     int g, j;          // current group and tile
+    int k, n;          // unit index within the group, the group's units
     long long left;    // units still to visit (including the current one)
     GroupInfo gi;
     bool first_in_group;  // current unit is the first of its group in this range
@@ -183,8 +199,32 @@ __device__ __forceinline__ long long block_incl_scan_ll(long long v, long long *
     return v + off;
 }
 
-// Find this CTA's first unit: returns (g0, j0) and the number of units.
+// Units of group g: all its tiles, or under a gather plan only its compute
+// tiles (the plan kernel writes -inf over the others).
+template <bool PLAN>
+__device__ __forceinline__ long long group_units(const LogitsArgs &a, int g)
+{
+    if constexpr (PLAN)
+        return (long long)__ldg(a.plan + (size_t)g * a.plan_words);
+    else
+        return group_info(a, g).tiles;
+}
+
+// Tile of unit k of group g: k itself, or under a gather plan the group's
+// k-th compute tile.
+template <bool PLAN>
+__device__ __forceinline__ int unit_tile(const LogitsArgs &a, int g, int k)
+{
+    if constexpr (PLAN)
+        return (int)__ldg(a.plan + (size_t)g * a.plan_words + 1 + a.box_words + k);
+    else
+        return k;
+}
+
+// Find this CTA's first unit: returns (g0, k0) -- the group and the unit's
+// index within it -- and the number of units.
 // scratch: >= blockDim.x/32 + 2 long longs of shared memory.
+template <bool PLAN>
 __device__ __forceinline__ void locate_units(const LogitsArgs &a, long long *scratch, int &g0,
                                              int &j0, long long &count)
 {
@@ -196,7 +236,7 @@ __device__ __forceinline__ void locate_units(const LogitsArgs &a, long long *scr
     } else {
         long long loc = 0;
         for (int g = threadIdx.x; g < a.num_groups; g += blockDim.x)
-            loc += group_info(a, g).tiles;
+            loc += group_units<PLAN>(a, g);
         total = block_sum_ll(loc, scratch);
     }
     long long u0 = total * blockIdx.x / gridDim.x;
@@ -213,14 +253,14 @@ __device__ __forceinline__ void locate_units(const LogitsArgs &a, long long *scr
         j0 = (int)(u0 - (long long)g0 * T);
         return;
     }
-    volatile long long *found = scratch + 32;  // [0] = g0, [1] = j0
+    volatile long long *found = scratch + 32;  // [0] = g0, [1] = unit within the group
     if (threadIdx.x == 0)
         found[0] = -1;
     __syncthreads();
     long long running = 0;
     for (int base = 0; base < a.num_groups; base += blockDim.x) {
         int g = base + threadIdx.x;
-        long long v = g < a.num_groups ? group_info(a, g).tiles : 0;
+        long long v = g < a.num_groups ? group_units<PLAN>(a, g) : 0;
         long long chunk;
         long long incl = block_incl_scan_ll(v, scratch, &chunk);
         long long start = running + incl - v;
@@ -234,36 +274,50 @@ __device__ __forceinline__ void locate_units(const LogitsArgs &a, long long *scr
             break;
     }
     g0 = (int)found[0];
-    j0 = (int)found[1];
+    j0 = (int)found[1];  // unit index within the group
     __syncthreads();
 }
 
-__device__ __forceinline__ void walk_begin(const LogitsArgs &a, UnitWalk &w, int g0, int j0,
+template <bool PLAN>
+__device__ __forceinline__ void walk_begin(const LogitsArgs &a, UnitWalk &w, int g0, int k0,
                                            long long count)
 {
     w.g = g0;
-    w.j = j0;
+    w.k = k0;
     w.left = count;
     w.first_in_group = true;
-    if (count > 0)
+    if (count > 0) {
         w.gi = group_info(a, g0);
+        w.n = PLAN ? (int)group_units<PLAN>(a, g0) : w.gi.tiles;
+        w.j = unit_tile<PLAN>(a, g0, k0);
+    }
 }
 
 __device__ __forceinline__ bool walk_last_in_group(const UnitWalk &w)
 {
-    return w.left == 1 || w.j + 1 >= w.gi.tiles;
+    return w.left == 1 || w.k + 1 >= w.n;
 }
 
+// Next unit: the group's next one, else the first of the next group that
+// has units.
+template <bool PLAN>
 __device__ __forceinline__ void walk_next(const LogitsArgs &a, UnitWalk &w)
 {
-    ++w.j;
+    ++w.k;
     --w.left;
     w.first_in_group = false;
-    while (w.left > 0 && w.j >= w.gi.tiles) {
+    while (w.left > 0 && w.k >= w.n) {
         ++w.g;
-        w.j = 0;
+        w.k = 0;
         w.first_in_group = true;
         w.gi = group_info(a, w.g);
+        w.n = PLAN ? (int)group_units<PLAN>(a, w.g) : w.gi.tiles;
+    }
+    if constexpr (PLAN) {
+        if (w.left > 0)
+            w.j = unit_tile<PLAN>(a, w.g, w.k);
+    } else {
+        w.j = w.k;
     }
 }
 

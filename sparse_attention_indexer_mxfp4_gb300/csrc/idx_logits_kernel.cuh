@@ -111,28 +111,45 @@ struct LogitsCfg {
     }
 };
 
+// Whether the walk's current unit is scored (K loaded, MMA issued) rather
+// than only written -inf: it overlaps the group's live keys and, under a
+// gather plan, holds a candidate key.
+template <bool PLAN>
+__device__ __forceinline__ bool unit_compute(const UnitWalk &w, int shift)
+{
+    return PLAN || tile_is_compute(w.gi, w.j, shift);  // a plan lists compute tiles only
+}
+
 // Logical page of key position t (shift when the page size is a power of two).
 __device__ __forceinline__ int page_of(const LogitsArgs &a, int t)
 {
     return a.page_shift >= 0 ? (t >> a.page_shift) : t / a.page_size;
 }
 
-// One lane's 64-key box of a producer window (NH boxes per tile, 32 per
-// window): does the group need it, which page and row it starts at.  The
-// block-table load is issued here and only consumed when the window becomes
-// current.
+// One lane's 64-key box of a producer window of 32 / NH units starting at
+// unit k0 of the walk's group (lane l: box l % NH of unit k0 + l / NH): does
+// the group need it, which page and row it starts at.  The block-table load
+// is issued here and only consumed when the window becomes current.
 struct HalfInfo {
     int page, row;
     bool need;
 };
 
-template <int NH>
-__device__ __forceinline__ HalfInfo half_info(const LogitsArgs &a, const GroupInfo &gi, int g,
-                                              int tile0, int lane)
+template <int NH, bool PLAN>
+__device__ __forceinline__ HalfInfo half_info(const LogitsArgs &a, const UnitWalk &w, int k0,
+                                              int lane)
 {
     HalfInfo h;
-    const int tok = (tile0 * NH + lane) * kHalfKeys;
-    h.need = tok < gi.hi && tok + kHalfKeys > gi.lo;
+    const GroupInfo &gi = w.gi;
+    const int g = w.g;
+    int tok;
+    if constexpr (PLAN) {
+        const int kk = k0 + lane / NH;
+        tok = kk < w.n ? (unit_tile<PLAN>(a, g, kk) * NH + lane % NH) * kHalfKeys : gi.hi;
+    } else {
+        tok = (k0 * NH + lane) * kHalfKeys;  // units are consecutive tiles
+    }
+    h.need = tok < gi.hi && tok + kHalfKeys > gi.lo && (!PLAN || plan_box(a, g, tok / kHalfKeys));
     h.page = 0;
     h.row = tok;
     if (a.paged) {
@@ -147,7 +164,7 @@ __device__ __forceinline__ HalfInfo half_info(const LogitsArgs &a, const GroupIn
 
 namespace idx {
 
-template <int FMT, int H, int G, int S, int NA, int TK>
+template <int FMT, int H, int G, int S, int NA, int TK, bool PLAN>
 __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
     logits_kernel(const __grid_constant__ LogitsArgs a, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmS)
@@ -200,14 +217,14 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
     pdl_launch_dependents();
     int g0, j0;
     long long count;
-    locate_units(a, scratch, g0, j0, count);  // contains __syncthreads
+    locate_units<PLAN>(a, scratch, g0, j0, count);  // contains __syncthreads
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
     UnitWalk w;
-    walk_begin(a, w, g0, j0, count);
+    walk_begin<PLAN>(a, w, g0, j0, count);
 
     if (warp < 2) {
         // ------------------------------------------------------------ producers
@@ -219,7 +236,7 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
         int win0 = 0;      // first tile of the current page window
         HalfInfo cur = {}, nxt = {};
         bool cur_ok = false;
-        for (; w.left > 0; walk_next(a, w)) {
+        for (; w.left > 0; walk_next<PLAN>(a, w)) {
             if (w.first_in_group && pw == 0) {
                 const int slot = gq & 1;
                 if (!mbar_wait(&q_empty[slot], ((gq >> 1) & 1) ^ 1, abort_flag, a.status))
@@ -264,26 +281,26 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
             }
             if (w.first_in_group) {
                 // page window of this group: current and next, loads in flight
-                win0 = w.j;
-                cur = half_info<C::NH>(a, w.gi, w.g, win0, lane);
-                nxt = half_info<C::NH>(a, w.gi, w.g, win0 + C::WIN_TILES, lane);
+                win0 = w.k;
+                cur = half_info<C::NH, PLAN>(a, w, win0, lane);
+                nxt = half_info<C::NH, PLAN>(a, w, win0 + C::WIN_TILES, lane);
                 cur_ok = false;
             }
-            if (!tile_is_compute(w.gi, w.j, TSH))
+            if (!unit_compute<PLAN>(w, TSH))
                 continue;
             if ((c & 1) != pw) {  // the other producer's tile
                 ++c;
                 continue;
             }
-            if (w.j >= win0 + C::WIN_TILES) {  // slide the window (warp-uniform)
-                const int step = (w.j - win0) / C::WIN_TILES;
+            if (w.k >= win0 + C::WIN_TILES) {  // slide the window (warp-uniform)
+                const int step = (w.k - win0) / C::WIN_TILES;
                 if (step == 1) {
                     cur = nxt;
                 } else {
-                    cur = half_info<C::NH>(a, w.gi, w.g, win0 + step * C::WIN_TILES, lane);
+                    cur = half_info<C::NH, PLAN>(a, w, win0 + step * C::WIN_TILES, lane);
                 }
                 win0 += step * C::WIN_TILES;
-                nxt = half_info<C::NH>(a, w.gi, w.g, win0 + C::WIN_TILES, lane);
+                nxt = half_info<C::NH, PLAN>(a, w, win0 + C::WIN_TILES, lane);
                 cur_ok = false;
             }
             if (!cur_ok) {  // first use of this window: resolve validity
@@ -296,7 +313,7 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
             const int s = C::stage(c);
             if (!mbar_wait(&empty[s], C::phase(c) ^ 1, abort_flag, a.status))
                 break;
-            const int h0 = C::NH * (w.j - win0);  // lanes h0 .. h0 + NH - 1 own this tile's boxes
+            const int h0 = C::NH * (w.k - win0);  // lanes h0 .. h0 + NH - 1 own this tile's boxes
             const uint32_t ball = __ballot_sync(0xffffffffu, cur.need);
             const uint32_t mine = (ball >> h0) & ((1u << C::NH) - 1u);
             uint8_t *st = smem + C::OFF_STAGE + s * C::STAGE_BYTES;
@@ -337,7 +354,7 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
         int gq = 0;
         int c = 0;
         int slot = 0;
-        for (; w.left > 0; walk_next(a, w)) {
+        for (; w.left > 0; walk_next<PLAN>(a, w)) {
             if (w.first_in_group) {
                 slot = gq & 1;
                 if (!mbar_wait(&q_full[slot], (gq >> 1) & 1, abort_flag, a.status))
@@ -372,9 +389,9 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
                 }
                 ++gq;
             }
-            if (tile_is_compute(w.gi, w.j, TSH) && ((c % NA) & 1) != mw) {
+            if (unit_compute<PLAN>(w, TSH) && ((c % NA) & 1) != mw) {
                 ++c;  // the other MMA warp's tile
-            } else if (tile_is_compute(w.gi, w.j, TSH)) {
+            } else if (unit_compute<PLAN>(w, TSH)) {
                 const int acc = c % NA;
                 const int s = C::stage(c);
                 if (!mbar_wait(&acc_empty[acc], (uint32_t)((c / NA) & 1) ^ 1, abort_flag, a.status))
@@ -458,7 +475,7 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
         int slot = 0;
         int rks[G], rke[G];
         constexpr int NSUB = C::NSUB;
-        for (; w.left > 0; walk_next(a, w), ++u) {
+        for (; w.left > 0; walk_next<PLAN>(a, w), ++u) {
             if (w.first_in_group) {
                 slot = gq & 1;
                 for (int i = 0; i < G; ++i) {
@@ -473,7 +490,7 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
             }
             const int t0 = (w.j << TSH) + kq;  // this thread's key in sub-tile 0
             const int wend = a.paged ? w.gi.hi : a.N;  // columns this group writes
-            const bool compute = tile_is_compute(w.gi, w.j, TSH);
+            const bool compute = unit_compute<PLAN>(w, TSH);
             bool mine;
             float val[NSUB][G];
             #pragma unroll
@@ -657,6 +674,125 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
     if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem_base, C::TM_COLS);
+    }
+}
+
+
+// ----------------------------------------------------------------- gather plan
+//
+// Grid (row groups, kPlanSlices).  Each CTA finds, for its row group, the
+// 64-key boxes that hold a candidate key of any of the group's rows
+// (candidate blocks clipped to each row's [ks, ke)) and the tiles of 2^TSH
+// keys that hold such a box (and overlap the group's live keys).  Slice 0
+// writes the plan the logits kernel walks: the number of such tiles, the box
+// bits and the tile list.  Every CTA writes -inf over the other tiles of its
+// slice of the group, for each row up to the row's end: the logits the
+// logits kernel will not write.  Dynamic shared memory: box_words +
+// ceil(width / 128 / 32) words.
+constexpr int kPlanSlices = 8;
+constexpr int kPlanThreads = 256;
+
+template <int TSH>
+__global__ void __launch_bounds__(kPlanThreads) cand_plan_kernel(const __grid_constant__ LogitsArgs a)
+{
+    extern __shared__ uint32_t pbits[];
+    uint32_t *box = pbits, *tb = pbits + a.box_words;
+    __shared__ uint32_t red[kPlanThreads / 32];
+    __shared__ int rks[8], rke[8];
+    pdl_wait();
+    pdl_launch_dependents();
+    const int g = blockIdx.x, slice = blockIdx.y, tid = threadIdx.x;
+    const int tw = ((a.width + kMmaM - 1) / kMmaM + 31) / 32;
+    const GroupInfo gi = group_info(a, g);
+    for (int i = tid; i < a.box_words + tw; i += kPlanThreads)
+        pbits[i] = 0u;
+    if (tid < gi.nrows)
+        row_range(a, gi.row0 + tid, rks[tid], rke[tid]);
+    __syncthreads();
+    for (int i = 0; i < gi.nrows; ++i) {
+        const int ks = rks[i], ke = rke[i];
+        const int32_t *cr = a.cand + (size_t)(gi.row0 + i) * a.cand_stride;
+        for (int e = tid; e < a.num_cand; e += kPlanThreads) {
+            const int id = cr[e];
+            if (id < 0)
+                continue;
+            const long long lo = (long long)ks + (long long)id * a.cand_block;
+            if (lo >= ke)
+                continue;
+            const int t_lo = (int)lo;
+            const int t_hi = (int)min((long long)ke, lo + a.cand_block);
+            for (int b = t_lo / kHalfKeys; b <= (t_hi - 1) / kHalfKeys; ++b)
+                atomicOr(&box[b >> 5], 1u << (b & 31));
+        }
+    }
+    __syncthreads();
+    // tile bits; thread t owns the contiguous tiles [t * per, (t + 1) * per)
+    constexpr int BPT = (1 << TSH) / kHalfKeys;  // boxes per tile
+    const int per = (gi.tiles + kPlanThreads - 1) / kPlanThreads;
+    uint32_t mine = 0;
+    for (int j = tid * per; j < min(gi.tiles, (tid + 1) * per); ++j) {
+        bool any = false;
+        #pragma unroll
+        for (int q = 0; q < BPT; ++q) {
+            const int b = j * BPT + q;
+            any = any || ((box[b >> 5] >> (b & 31)) & 1u);
+        }
+        if (any && tile_is_compute(gi, j, TSH)) {
+            atomicOr(&tb[j >> 5], 1u << (j & 31));
+            ++mine;
+        }
+    }
+    __syncthreads();
+    if (slice == 0) {
+        // the tile list: exclusive prefix of the per-thread counts
+        const int lane = tid & 31, wi = tid >> 5;
+        uint32_t x = mine;
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t n = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o)
+                x += n;
+        }
+        if (lane == 31)
+            red[wi] = x;
+        __syncthreads();
+        uint32_t before = x - mine, total = 0;
+        for (int i = 0; i < kPlanThreads / 32; ++i) {
+            if (i < wi)
+                before += red[i];
+            total += red[i];
+        }
+        uint32_t *dst = a.plan + (size_t)g * a.plan_words;
+        uint32_t *list = dst + 1 + a.box_words;
+        for (int j = tid * per; j < min(gi.tiles, (tid + 1) * per); ++j)
+            if ((tb[j >> 5] >> (j & 31)) & 1u)
+                list[before++] = (uint32_t)j;
+        if (tid == 0)
+            dst[0] = total;
+        for (int i = tid; i < a.box_words; i += kPlanThreads)
+            dst[1 + i] = box[i];
+    }
+    // -inf over the slice's tiles that are not scored, four keys per store
+    // where the row allows it
+    const int j0 = (int)((long long)gi.tiles * slice / kPlanSlices);
+    const int j1 = (int)((long long)gi.tiles * (slice + 1) / kPlanSlices);
+    constexpr int V = (1 << TSH) / 4;  // float4 per tile
+    const bool vec = (a.ld & 3) == 0 && ((uintptr_t)a.logits & 15) == 0;
+    for (int i = 0; i < gi.nrows; ++i) {
+        float *orow = a.logits + (size_t)(gi.row0 + i) * a.ld;
+        const int end = rke[i];
+        for (int v = tid; v < (j1 - j0) * V; v += kPlanThreads) {
+            const int j = j0 + v / V;
+            if ((tb[j >> 5] >> (j & 31)) & 1u)
+                continue;
+            const int t = (j << TSH) + 4 * (v % V);
+            if (t + 4 <= end && vec) {
+                *reinterpret_cast<float4 *>(orow + t) =
+                    make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            } else {
+                for (int e = 0; e < 4 && t + e < end; ++e)
+                    orow[t + e] = -INFINITY;
+            }
+        }
     }
 }
 

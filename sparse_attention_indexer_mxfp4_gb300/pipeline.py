@@ -22,12 +22,15 @@ def _dev(a, device, dtype=None):
 class IndexerStep:
     """Device-resident inputs and outputs of one workload and the calls of one
     step.  ``fused_mask=False`` applies the candidate mask with the standalone
-    kernel after the logits instead of inside them."""
+    kernel after the logits instead of inside them; ``gather=False`` keeps the
+    fused mask but scores every key (no candidate gather plan)."""
 
-    def __init__(self, case, device="cuda", fused_mask: bool = True, num_ctas: int = 0):
+    def __init__(self, case, device="cuda", fused_mask: bool = True, num_ctas: int = 0,
+                 gather: bool = True):
         self.case = case
         self.device = torch.device(device)
         self.fused_mask = fused_mask
+        self.gather = gather
         self.num_ctas = num_ctas
         d = self.device
         self.paged = isinstance(case, PagedCase)
@@ -71,7 +74,7 @@ class IndexerStep:
                 self.q, self.q_scale, self.weights, self.pages, self.block_table,
                 self.context_lens, c.next_n, c.page_size, c.fmt, self.logits, c.width,
                 row_ks=self.row_ks, ctx_per_row=c.ctx_per_row, candidate_blocks=cand,
-                cand_block=c.cand_block, num_ctas=self.num_ctas))
+                cand_block=c.cand_block, num_ctas=self.num_ctas, workspace=self.gather))
             if self.cand is not None and not self.fused_mask:
                 self._logits_calls.append(B.prepare_apply_candidate_mask(
                     self.logits, self.row_ks, self.lengths, self.cand, c.cand_block))

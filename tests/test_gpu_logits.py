@@ -1,5 +1,7 @@
 """GPU parity of the logits kernels (through the C ABI) against the oracle,
 element by element, on sizes that span several tiles and a ragged tail."""
+import functools
+
 import numpy as np
 import pytest
 import torch
@@ -31,8 +33,8 @@ def ora_contig(c: synth.ContiguousCase):
                              c.M, c.N, c.H, c.D)
 
 
-def gpu_paged(c: synth.PagedCase, fused=True, num_ctas=0):
-    st = IndexerStep(c, fused_mask=fused, num_ctas=num_ctas)
+def gpu_paged(c: synth.PagedCase, fused=True, num_ctas=0, gather=True):
+    st = IndexerStep(c, fused_mask=fused, num_ctas=num_ctas, gather=gather)
     st.logits.fill_(float("nan"))
     st.logits_stage()
     torch.cuda.synchronize()
@@ -148,7 +150,27 @@ def test_paged_fused_candidate_mask(next_n):
     c.cand[1, 2] = -7
     ref, _ = ora_paged(c)
     compare_paged(c, gpu_paged(c, fused=True), ref)
+    compare_paged(c, gpu_paged(c, fused=True, gather=False), ref)
     compare_paged(c, gpu_paged(c, fused=False), ref)
+
+
+@functools.lru_cache(maxsize=None)
+def _sparse_candidate_case(fmt):
+    ctx = [40000, 3, 700, 16385, 9000, 257]
+    c = synth.paged_case(90 + fmt, ctx, 2, 64, 128, 64, 40960, fmt=fmt, pool_factor=1.2,
+                         cand_num=6, cand_block=128)
+    c.cand[2, 0] = 10**6  # far out of range
+    c.cand[3, :] = -1     # a row without candidates
+    return c, ora_paged(c)[0]
+
+
+@pytest.mark.parametrize("fmt", [synth.FMT_FP8, synth.FMT_MXFP4])
+@pytest.mark.parametrize("num_ctas", [0, 1, 5, 1000])
+def test_paged_candidate_gather_plan(fmt, num_ctas):
+    """Sparse candidates over long rows: most tiles hold no candidate and are
+    only written -inf, and the work split follows the candidate tiles."""
+    c, ref = _sparse_candidate_case(fmt)
+    compare_paged(c, gpu_paged(c, num_ctas=num_ctas), ref)
 
 
 @pytest.mark.parametrize("next_n", [1, 2])
