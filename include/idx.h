@@ -139,6 +139,28 @@ idx_status idx_paged_mqa_logits(const void *q, const void *q_scale, const float 
                                 int64_t ld_logits, int max_model_len, int num_ctas, void *ws,
                                 size_t ws_bytes, idx_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * idx_paged_mqa_logits_candidates -- idx_paged_mqa_logits for a consumer
+ * that reads only the candidate blocks (idx_topk_candidates).
+ * Passage: as idx_paged_mqa_logits; the candidate mask of rocm_aiter_mla_sparse,
+ * _apply_candidate_mask_strided, applied by reading only candidate keys.
+ *
+ *   Arguments as idx_paged_mqa_logits; candidate_blocks (num_cand > 0) and
+ *   ws_bytes >= idx_paged_mqa_logits_workspace_size(...) are required.
+ *   Writes the logits of every key of the tiles that hold a candidate key
+ *   (keys of those tiles outside every candidate block get -inf) and leaves
+ *   every other column untouched.
+ * Errors: IDX_ERR_INVALID_ARG without candidates, IDX_ERR_WORKSPACE when ws
+ *   is missing or too small; otherwise as idx_paged_mqa_logits.
+ * ---------------------------------------------------------------------- */
+idx_status idx_paged_mqa_logits_candidates(
+    const void *q, const void *q_scale, const float *weights, const uint8_t *kv_pages,
+    int64_t page_stride_bytes, int num_pages, const int32_t *block_table, int64_t bt_stride,
+    const int32_t *context_lens, int ctx_per_row, const int32_t *row_ks, int B, int next_n, int H,
+    int D, int page_size, idx_kv_format fmt, const int32_t *candidate_blocks, int64_t cand_stride,
+    int num_cand, int cand_block, float *logits, int64_t ld_logits, int max_model_len,
+    int num_ctas, void *ws, size_t ws_bytes, idx_stream_t stream);
+
 /* Bytes of ws the gather path of idx_paged_mqa_logits needs (0 without a
  * candidate mask: num_cand <= 0).  Pure host arithmetic. */
 size_t idx_paged_mqa_logits_workspace_size(int B, int next_n, int max_model_len, int num_cand);
@@ -225,6 +247,29 @@ size_t idx_topk_workspace_size(int rows, int64_t ld, int k);
 
 idx_status idx_topk_noalloc(const float *logits, int64_t ld, int rows, const int32_t *lengths,
                             int k, int32_t *out_idx, int64_t ld_out, idx_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * idx_topk_candidates -- per-row top-k over a row's candidate blocks only.
+ * Passage: rocm_paged_mxfp4_indexer, _topk, after the candidate mask of
+ * rocm_aiter_mla_sparse, _apply_candidate_mask_strided.
+ *
+ *   Same result as idx_apply_candidate_mask (with row_ke = lengths) followed
+ *   by idx_topk, reading only the candidate keys: row r selects among the
+ *   keys t of [ks_r, lengths[r]) whose block (t - ks_r) / block_size is one
+ *   of the num_cand ids of candidate row r / row_repeat (negative, repeated
+ *   and out-of-range ids are ignored).  Output as idx_topk: ascending token
+ *   indices, -1 padding, ties at the k-th value to the lowest index.
+ *   logits [rows, ld] (columns outside the candidate blocks are never read);
+ *   row_ks NULL (0) or [rows]; candidate_blocks [ceil(rows / row_repeat),
+ *   cand_stride].
+ * Supported: num_cand <= 512 and num_cand * block_size <= 16384.
+ * Errors: IDX_ERR_INVALID_ARG for bad sizes or NULL pointers,
+ *   IDX_ERR_UNSUPPORTED beyond the supported sizes, IDX_ERR_CUDA on launch.
+ * ---------------------------------------------------------------------- */
+idx_status idx_topk_candidates(const float *logits, int64_t ld, int rows, const int32_t *lengths,
+                               const int32_t *row_ks, const int32_t *candidate_blocks,
+                               int64_t cand_stride, int num_cand, int block_size, int row_repeat,
+                               int k, int32_t *out_idx, int64_t ld_out, idx_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * idx_topk_to_ragged_slots -- top-k positions to a ragged list of cache slots.

@@ -36,7 +36,9 @@ _SIGNATURES = {
                              _P, _L, _I, _I, _P, _L, _I, _I, _P, _S, _P],
     "idx_apply_candidate_mask": [_P, _L, _I, _I, _P, _P, _P, _L, _I, _I, _I, _P],
     "idx_topk": [_P, _L, _I, _P, _I, _P, _L, _P, _S, _P],
+    "idx_paged_mqa_logits_candidates": None,  # same as idx_paged_mqa_logits
     "idx_topk_noalloc": [_P, _L, _I, _P, _I, _P, _L, _P],
+    "idx_topk_candidates": [_P, _L, _I, _P, _P, _P, _L, _I, _I, _I, _I, _P, _L, _P],
     "idx_topk_to_ragged_slots": [_P, _L, _I, _I, _P, _I, _P, _L, _I, _I, _I, _P, _P, _P, _P],
     "idx_get_device_status": [_P, ctypes.POINTER(ctypes.c_uint32)],
 }
@@ -61,6 +63,8 @@ def lib() -> ctypes.CDLL:
             L = ctypes.CDLL(path)
             for name, args in _SIGNATURES.items():
                 fn = getattr(L, name)
+                if args is None:
+                    args = _SIGNATURES["idx_paged_mqa_logits"]
                 fn.argtypes = args
                 fn.restype = ctypes.c_int
             L.idx_version.restype = ctypes.c_char_p
@@ -149,10 +153,12 @@ def idx_mqa_logits(q, q_scale, weights, k, k_scale, row_ks, row_ke, fmt, logits,
 def prepare_paged_mqa_logits(q, q_scale, weights, kv_pages, block_table, context_lens, next_n,
                              page_size, fmt, logits, max_model_len, row_ks=None,
                              ctx_per_row=False, candidate_blocks=None, cand_block=0,
-                             num_ctas=0, workspace=True):
+                             num_ctas=0, workspace=True, candidates_only=False):
     """workspace (used with candidate_blocks): True allocates the gather plan
     scratch here (held by the returned call), a uint8 CUDA tensor supplies it,
-    False or None scores every key of the context."""
+    False or None scores every key of the context.  candidates_only calls
+    idx_paged_mqa_logits_candidates: only tiles holding a candidate key are
+    written (for idx_topk_candidates)."""
     q = _u8(q)
     rows, H = q.shape[0], q.shape[1]
     D = q.shape[2] if fmt == FMT_FP8 else 2 * q.shape[2]
@@ -180,7 +186,8 @@ def prepare_paged_mqa_logits(q, q_scale, weights, kv_pages, block_table, context
             logits.stride(0), max_model_len, num_ctas, _ptr(ws), nbytes)
     # with a plan the library launches the plan kernel before the logits kernel
     planned = ws is not None and need > 0 and nbytes >= need
-    return Prepared("idx_paged_mqa_logits", args, (q, q_scale, weights, kv_pages, block_table,
+    name = "idx_paged_mqa_logits_candidates" if candidates_only else "idx_paged_mqa_logits"
+    return Prepared(name, args, (q, q_scale, weights, kv_pages, block_table,
                                                    context_lens, row_ks, candidate_blocks,
                                                    logits, ws), 2 if planned else 1)
 
@@ -267,6 +274,29 @@ def idx_topk_noalloc(logits, lengths, k, out, stream=None):
     rc = lib().idx_topk_noalloc(_ptr(logits), logits.stride(0), logits.shape[0], _ptr(lengths),
                                 k, _ptr(out), out.stride(0), _stream(stream))
     _check(rc, "idx_topk_noalloc")
+
+
+def prepare_topk_candidates(logits, lengths, k, out, candidate_blocks, block_size, row_ks=None,
+                            row_repeat=1):
+    """out int32 [rows, >= k]: ascending indices of the k largest finite logits
+    of each row among the keys of its candidate blocks within [ks, lengths)."""
+    if logits.dtype != torch.float32 or logits.stride(1) != 1:
+        raise ValueError("logits must be float32 with unit column stride")
+    _need(lengths, torch.int32, "lengths")
+    _need(candidate_blocks, torch.int32, "candidate_blocks")
+    if out.dtype != torch.int32 or out.stride(1) != 1:
+        raise ValueError("out must be int32 with unit column stride")
+    args = (_ptr(logits), logits.stride(0), logits.shape[0], _ptr(lengths), _ptr(row_ks),
+            _ptr(candidate_blocks), candidate_blocks.stride(0), candidate_blocks.shape[1],
+            block_size, row_repeat, k, _ptr(out), out.stride(0))
+    return Prepared("idx_topk_candidates", args,
+                    (logits, lengths, out, candidate_blocks, row_ks))
+
+
+def idx_topk_candidates(logits, lengths, k, out, candidate_blocks, block_size, row_ks=None,
+                        row_repeat=1, stream=None):
+    prepare_topk_candidates(logits, lengths, k, out, candidate_blocks, block_size, row_ks,
+                            row_repeat)(stream)
 
 
 def prepare_topk_to_ragged_slots(topk, block_table, page_size, num_pages, slots, indptr, lens,

@@ -307,7 +307,7 @@ extern "C" idx_status idx_mqa_logits(const void *q, const void *q_scale, const f
     return launch_status(e);
 }
 
-extern "C" idx_status idx_paged_mqa_logits(
+static idx_status paged_logits(bool cand_only,
     const void *q, const void *q_scale, const float *weights, const uint8_t *kv_pages,
     int64_t page_stride_bytes, int num_pages, const int32_t *block_table, int64_t bt_stride,
     const int32_t *context_lens, int ctx_per_row, const int32_t *row_ks, int B, int next_n,
@@ -315,8 +315,6 @@ extern "C" idx_status idx_paged_mqa_logits(
     int64_t cand_stride, int num_cand, int cand_block, float *logits, int64_t ld_logits,
     int max_model_len, int num_ctas, void *ws, size_t ws_bytes, idx_stream_t stream)
 {
-    (void)ws;
-    (void)ws_bytes;
     if (B < 0 || next_n <= 0 || H <= 0 || D <= 0 || page_size <= 0 || num_pages < 0 ||
         max_model_len < 0 || num_ctas < 0 || !valid_fmt(fmt))
         return IDX_ERR_INVALID_ARG;
@@ -421,9 +419,13 @@ extern "C" idx_status idx_paged_mqa_logits(
     // tiles and 64-key boxes that hold a candidate key are loaded and scored
     const size_t plan_need =
         idx_paged_mqa_logits_workspace_size(B, next_n, max_model_len, a.cand ? num_cand : 0);
-    if (plan_need > 0 && ws && ws_bytes >= plan_need && aligned16(ws)) {
+    const bool planned = plan_need > 0 && ws && ws_bytes >= plan_need && aligned16(ws);
+    if (cand_only && !planned)
+        return plan_need == 0 ? IDX_ERR_INVALID_ARG : IDX_ERR_WORKSPACE;
+    if (planned) {
         int tile_words = 0;
         a.plan = static_cast<uint32_t *>(ws);
+        a.plan_fill = cand_only ? 0 : 1;
         plan_geom(max_model_len, &a.box_words, &a.plan_words, &tile_words);
         a.tile_shift = logits_tile_shift(f, G, true);
         if (launch_plan(a, B, tile_words, (cudaStream_t)stream) != cudaSuccess)
@@ -435,6 +437,36 @@ extern "C" idx_status idx_paged_mqa_logits(
     if (!supported)
         return IDX_ERR_UNSUPPORTED;
     return launch_status(e);
+}
+
+extern "C" idx_status idx_paged_mqa_logits(
+    const void *q, const void *q_scale, const float *weights, const uint8_t *kv_pages,
+    int64_t page_stride_bytes, int num_pages, const int32_t *block_table, int64_t bt_stride,
+    const int32_t *context_lens, int ctx_per_row, const int32_t *row_ks, int B, int next_n, int H,
+    int D, int page_size, idx_kv_format fmt, const int32_t *candidate_blocks, int64_t cand_stride,
+    int num_cand, int cand_block, float *logits, int64_t ld_logits, int max_model_len,
+    int num_ctas, void *ws, size_t ws_bytes, idx_stream_t stream)
+{
+    return paged_logits(false, q, q_scale, weights, kv_pages, page_stride_bytes, num_pages,
+                        block_table, bt_stride, context_lens, ctx_per_row, row_ks, B, next_n, H, D,
+                        page_size, fmt, candidate_blocks, cand_stride, num_cand, cand_block, logits,
+                        ld_logits, max_model_len, num_ctas, ws, ws_bytes, stream);
+}
+
+extern "C" idx_status idx_paged_mqa_logits_candidates(
+    const void *q, const void *q_scale, const float *weights, const uint8_t *kv_pages,
+    int64_t page_stride_bytes, int num_pages, const int32_t *block_table, int64_t bt_stride,
+    const int32_t *context_lens, int ctx_per_row, const int32_t *row_ks, int B, int next_n, int H,
+    int D, int page_size, idx_kv_format fmt, const int32_t *candidate_blocks, int64_t cand_stride,
+    int num_cand, int cand_block, float *logits, int64_t ld_logits, int max_model_len,
+    int num_ctas, void *ws, size_t ws_bytes, idx_stream_t stream)
+{
+    if (!candidate_blocks || num_cand <= 0)
+        return IDX_ERR_INVALID_ARG;
+    return paged_logits(true, q, q_scale, weights, kv_pages, page_stride_bytes, num_pages,
+                        block_table, bt_stride, context_lens, ctx_per_row, row_ks, B, next_n, H, D,
+                        page_size, fmt, candidate_blocks, cand_stride, num_cand, cand_block, logits,
+                        ld_logits, max_model_len, num_ctas, ws, ws_bytes, stream);
 }
 
 extern "C" size_t idx_paged_mqa_logits_workspace_size(int B, int next_n, int max_model_len,

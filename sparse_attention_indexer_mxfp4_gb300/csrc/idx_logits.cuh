@@ -74,6 +74,7 @@ struct LogitsArgs {
     // and only those boxes loaded; every other key is -inf anyway.
     uint32_t *plan;
     int plan_words, box_words;
+    int plan_fill;  // the plan kernel writes -inf over the tiles it does not list
 };
 
 // Plan bit of 64-key box b of group g (true without a plan).

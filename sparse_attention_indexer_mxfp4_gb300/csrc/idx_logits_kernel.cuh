@@ -771,6 +771,8 @@ __global__ void __launch_bounds__(kPlanThreads) cand_plan_kernel(const __grid_co
         for (int i = tid; i < a.box_words; i += kPlanThreads)
             dst[1 + i] = box[i];
     }
+    if (!a.plan_fill)
+        return;
     // -inf over the slice's tiles that are not scored, four keys per store
     // where the row allows it
     const int j0 = (int)((long long)gi.tiles * slice / kPlanSlices);

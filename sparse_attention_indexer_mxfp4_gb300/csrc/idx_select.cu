@@ -8,6 +8,7 @@
 #include "idx_internal.h"
 #include "idx_topk.cuh"
 #include "idx_topk_chunked.cuh"
+#include "idx_topk_cand.cuh"
 
 namespace idx {
 namespace {
@@ -369,6 +370,40 @@ extern "C" idx_status idx_topk(const float *logits, int64_t ld, int rows, const 
             return st;
     }
     return topk_launch_per_row(logits, ld, rows, lengths, k, out_idx, ld_out, vec_ok, s);
+}
+
+extern "C" idx_status idx_topk_candidates(const float *logits, int64_t ld, int rows,
+                                          const int32_t *lengths, const int32_t *row_ks,
+                                          const int32_t *candidate_blocks, int64_t cand_stride,
+                                          int num_cand, int block_size, int row_repeat, int k,
+                                          int32_t *out_idx, int64_t ld_out, idx_stream_t stream)
+{
+    namespace T = idx::topk_cand;
+    if (rows < 0 || k < 0 || ld < 0 || ld_out < k || ld > INT32_MAX || num_cand < 0 ||
+        block_size <= 0 || row_repeat <= 0 || cand_stride < num_cand)
+        return IDX_ERR_INVALID_ARG;
+    if (rows == 0 || k == 0)
+        return IDX_OK;
+    if (!logits || !lengths || !out_idx || (num_cand > 0 && !candidate_blocks))
+        return IDX_ERR_INVALID_ARG;
+    if (num_cand > T::kMaxIds || (long long)num_cand * block_size > T::kMaxKeys)
+        return IDX_ERR_UNSUPPORTED;
+    const size_t smem = sizeof(T::Shared);
+    static int configured[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return IDX_ERR_CUDA;
+    if (!configured[dev]) {
+        if (cudaFuncSetAttribute(T::topk_cand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem) != cudaSuccess)
+            return IDX_ERR_CUDA;
+        configured[dev] = 1;
+    }
+    const int vec4 = ld % 4 == 0 && block_size % 4 == 0 && aligned16(logits);
+    return launch_status(launch_pdl(T::topk_cand_kernel, dim3(rows), dim3(T::kThreads), smem,
+                                    (cudaStream_t)stream, logits, ld, rows, lengths, row_ks,
+                                    candidate_blocks, cand_stride, num_cand, block_size,
+                                    row_repeat, k, out_idx, ld_out, vec4));
 }
 
 extern "C" idx_status idx_apply_candidate_mask(float *logits, int64_t ld, int rows, int width,

@@ -23,14 +23,19 @@ class IndexerStep:
     """Device-resident inputs and outputs of one workload and the calls of one
     step.  ``fused_mask=False`` applies the candidate mask with the standalone
     kernel after the logits instead of inside them; ``gather=False`` keeps the
-    fused mask but scores every key (no candidate gather plan)."""
+    fused mask but scores every key (no candidate gather plan).
+    ``cand_topk`` (with a fused mask and the gather plan) writes only the
+    tiles holding candidate keys and selects with idx_topk_candidates, which
+    reads only the candidate blocks; the top-k and slots are the same, the
+    logits outside those tiles are left unwritten."""
 
     def __init__(self, case, device="cuda", fused_mask: bool = True, num_ctas: int = 0,
-                 gather: bool = True):
+                 gather: bool = True, cand_topk: bool = True):
         self.case = case
         self.device = torch.device(device)
         self.fused_mask = fused_mask
         self.gather = gather
+        self.cand_topk = bool(cand_topk and gather and fused_mask)
         self.num_ctas = num_ctas
         d = self.device
         self.paged = isinstance(case, PagedCase)
@@ -74,7 +79,8 @@ class IndexerStep:
                 self.q, self.q_scale, self.weights, self.pages, self.block_table,
                 self.context_lens, c.next_n, c.page_size, c.fmt, self.logits, c.width,
                 row_ks=self.row_ks, ctx_per_row=c.ctx_per_row, candidate_blocks=cand,
-                cand_block=c.cand_block, num_ctas=self.num_ctas, workspace=self.gather))
+                cand_block=c.cand_block, num_ctas=self.num_ctas, workspace=self.gather,
+                candidates_only=self.cand_topk and cand is not None))
             if self.cand is not None and not self.fused_mask:
                 self._logits_calls.append(B.prepare_apply_candidate_mask(
                     self.logits, self.row_ks, self.lengths, self.cand, c.cand_block))
@@ -86,7 +92,12 @@ class IndexerStep:
                 self.q, self.q_scale, self.weights, self.k, self.k_scale, self.ks, self.ke,
                 c.fmt, self.logits))
             self._slots_call = None
-        self._topk_call = B.prepare_topk(self.logits, self.lengths, self.k_top, self.topk)
+        if self.paged and self.cand is not None and self.cand_topk:
+            self._topk_call = B.prepare_topk_candidates(
+                self.logits, self.lengths, self.k_top, self.topk, self.cand, c.cand_block,
+                row_ks=self.row_ks)
+        else:
+            self._topk_call = B.prepare_topk(self.logits, self.lengths, self.k_top, self.topk)
 
     # -------------------------------------------------------------- stages
     def logits_stage(self, stream=None):

@@ -33,8 +33,8 @@ def ora_contig(c: synth.ContiguousCase):
                              c.M, c.N, c.H, c.D)
 
 
-def gpu_paged(c: synth.PagedCase, fused=True, num_ctas=0, gather=True):
-    st = IndexerStep(c, fused_mask=fused, num_ctas=num_ctas, gather=gather)
+def gpu_paged(c: synth.PagedCase, fused=True, num_ctas=0, gather=True, cand_topk=False):
+    st = IndexerStep(c, fused_mask=fused, num_ctas=num_ctas, gather=gather, cand_topk=cand_topk)
     st.logits.fill_(float("nan"))
     st.logits_stage()
     torch.cuda.synchronize()
@@ -171,6 +171,23 @@ def test_paged_candidate_gather_plan(fmt, num_ctas):
     only written -inf, and the work split follows the candidate tiles."""
     c, ref = _sparse_candidate_case(fmt)
     compare_paged(c, gpu_paged(c, num_ctas=num_ctas), ref)
+
+
+@pytest.mark.parametrize("fmt", [synth.FMT_FP8, synth.FMT_MXFP4])
+def test_paged_candidates_only_writes_candidate_tiles(fmt):
+    """idx_paged_mqa_logits_candidates: every candidate key is written and
+    matches; columns outside the plan's tiles stay untouched (NaN here)."""
+    c, ref = _sparse_candidate_case(fmt)
+    gpu = gpu_paged(c, cand_topk=True)
+    ke = np.clip(c.row_ends(), 0, c.width)
+    for r in range(c.rows):
+        live = np.isfinite(ref[r, :ke[r]])
+        assert_logits_close(gpu[r, :ke[r]][live], ref[r, :ke[r]][live], f"row {r}")
+        wrote = ~np.isnan(gpu[r, :ke[r]])
+        assert wrote[live].all()
+        # whatever was written is either a candidate logit or -inf
+        assert np.isneginf(gpu[r, :ke[r]][wrote & ~live]).all()
+        assert np.isnan(gpu[r, ke[r]:]).all()
 
 
 @pytest.mark.parametrize("next_n", [1, 2])

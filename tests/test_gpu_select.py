@@ -172,3 +172,34 @@ def test_slots_row_to_seq_and_invalid_pages():
     assert bad == 3 and B.idx_get_device_status() & B.DEV_BAD_PAGE
     np.testing.assert_array_equal(indptr.cpu().numpy(), ip)
     np.testing.assert_array_equal(slots.cpu().numpy()[:ip[-1]], s)
+
+
+def _cand_case(rng, rows, width, num_cand, blk, row_repeat=1, ties=None):
+    if ties:
+        x = rng.integers(0, ties, size=(rows, width)).astype(np.float32)
+    else:
+        x = rng.standard_normal((rows, width)).astype(np.float32)
+    x[rng.random((rows, width)) < 0.05] = -np.inf
+    ke = rng.integers(0, width + 1, size=rows).astype(np.int32)
+    ke[0] = width
+    ks = np.minimum(rng.integers(0, 300, size=rows), ke).astype(np.int32)
+    crow = -(-rows // row_repeat)
+    nblk = width // blk + 2
+    cand = rng.integers(-2, nblk + 3, size=(crow, num_cand)).astype(np.int32)
+    cand[:, 1] = cand[:, 0]          # a repeated id per row
+    return x, ks, ke, cand
+
+
+@pytest.mark.parametrize("rows,width,num_cand,blk,k,rr,ties", [
+    (3, 1000, 4, 64, 50, 1, None), (17, 20000, 64, 128, 2048, 1, None),
+    (8, 9000, 64, 128, 300, 2, None), (5, 40000, 128, 128, 2048, 1, 3),
+    (4, 5000, 16, 100, 4000, 1, None), (6, 70000, 64, 256, 2048, 1, 7)])
+def test_topk_candidates_equals_mask_then_topk(rows, width, num_cand, blk, k, rr, ties):
+    rng = np.random.default_rng(rows * 31 + num_cand + blk)
+    x, ks, ke, cand = _cand_case(rng, rows, width, num_cand, blk, rr, ties)
+    masked = oracle.apply_candidate_mask(x.copy(), ks, ke, cand, blk, rr)
+    ref = oracle.topk(masked, ke, k)
+    out = torch.full((rows, k), -7, dtype=torch.int32, device="cuda")
+    B.idx_topk_candidates(_t(x), _t(ke), k, out, _t(cand), blk, row_ks=_t(ks), row_repeat=rr)
+    torch.cuda.synchronize()
+    assert_topk_exact(out.cpu().numpy(), ref)
