@@ -180,7 +180,7 @@ void plan_geom(int width, int *box_words, int *plan_words, int *tile_words)
 cudaError_t launch_plan(const LogitsArgs &a, int groups, int tile_words, cudaStream_t s)
 {
     const size_t smem = (size_t)(a.box_words + tile_words) * 4;
-    const dim3 grid(groups, kPlanSlices);
+    const dim3 grid(groups, a.plan_fill ? kPlanSlices : 1);  // slices only split the fill
     if (a.tile_shift == 8)
         return launch_pdl(cand_plan_kernel<8>, grid, dim3(kPlanThreads), smem, s, a);
     return launch_pdl(cand_plan_kernel<7>, grid, dim3(kPlanThreads), smem, s, a);

@@ -10,8 +10,7 @@
 // shared memory, the keys of the candidate blocks are gathered into shared
 // memory in ascending id order (so that order is ascending token order), and
 // the 11/11/10-bit radix select of idx_topk.cuh runs there: a histogram per
-// digit over the shared keys, then one ordered write in which thread t owns
-// a contiguous run of keys.  Keys outside [ks, ke), non-finite values and
+// digit over the shared keys, then an ordered write ranked by warp ballots.  Keys outside [ks, ke), non-finite values and
 // duplicate ids read as key 0 and are never selected; ties at the k-th value
 // go to the lowest token index.
 #pragma once
@@ -26,7 +25,8 @@ namespace topk_cand {
 constexpr int kThreads = 512;
 constexpr int kMaxIds = 512;        // candidate ids per row
 constexpr int kMaxKeys = 16384;     // num_cand * block_size
-constexpr int kPer = kMaxKeys / kThreads;  // keys a thread owns in the ordered write
+constexpr int kWarps = kThreads / 32;
+constexpr int kSteps = kMaxKeys / kThreads;
 
 struct Shared {
     uint32_t keys[kMaxKeys];
@@ -34,6 +34,8 @@ struct Shared {
     uint32_t hist[2048];
     uint32_t wsum[kThreads / 32];
     uint32_t sel[2];
+    uint32_t tab[(kMaxKeys / kThreads) * (kThreads / 32)];    // (step, warp) taken counts
+    uint32_t eqtab[(kMaxKeys / kThreads) * (kThreads / 32)];  // (step, warp) counts of T
 };
 
 // Descending-bin search over hist[nb] (nb <= 2048, kThreads threads, 4 bins
@@ -91,7 +93,41 @@ __device__ __forceinline__ uint32_t block_excl(Shared &sh, uint32_t v, uint32_t 
     return off;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+// Exclusive scan, in place, of the first nsteps * kWarps entries of a
+// (step, warp) table by warp 0; returns the total.  Barriers on both sides.
+__device__ __forceinline__ uint32_t scan_table(Shared &sh, uint32_t *tab, int nsteps)
+{
+    constexpr int E = kSteps * kWarps / 32;  // entries per lane
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x < 32) {
+        const int n = nsteps * kWarps;
+        uint32_t v[E], sum = 0;
+        #pragma unroll
+        for (int e = 0; e < E; ++e) {
+            const int idx = lane * E + e;
+            v[e] = idx < n ? tab[idx] : 0u;
+            sum += v[e];
+        }
+        uint32_t tot;
+        uint32_t run = topk_detail::warp_excl(sum, lane, &tot);
+        #pragma unroll
+        for (int e = 0; e < E; ++e) {
+            const int idx = lane * E + e;
+            if (idx < n)
+                tab[idx] = run;
+            run += v[e];
+        }
+        if (lane == 0)
+            sh.sel[0] = tot;
+    }
+    __syncthreads();
+    const uint32_t t = sh.sel[0];
+    __syncthreads();
+    return t;
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
     topk_cand_kernel(const float *__restrict__ logits, int64_t ld, int rows,
                      const int32_t *__restrict__ lengths, const int32_t *__restrict__ row_ks,
                      const int32_t *__restrict__ cand, int64_t cand_stride, int num_cand,
@@ -108,6 +144,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int32_t *crow = cand + (size_t)(r / row_repeat) * cand_stride;
     const int n = num_cand;
     const int nkeys = n * blk;
+    // block of compact position q: a shift for power-of-two blocks
+    const int bsh = (blk & (blk - 1)) == 0 ? __ffs(blk) - 1 : -1;
+    auto blk_of = [&](int q) -> int { return bsh >= 0 ? q >> bsh : q / blk; };
 
     // sort the ids (rank = ids before it in (id, position) order); a
     // repeated id keeps its first copy, invalid ids (negative, or a block
@@ -116,16 +155,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = tid; i < n; i += kThreads)
         raw[i] = crow[i];
     __syncthreads();
+    const int id_end = (ke - ks + blk - 1) / blk;  // ids [0, id_end) start below ke
     for (int i = tid; i < n; i += kThreads) {
-        int id = raw[i];
-        const bool valid = id >= 0 && (long long)ks + (long long)id * blk < ke;
-        const long long key_i = valid ? (long long)id : (1LL << 40);
+        const int id = raw[i];
+        const bool valid = id >= 0 && id < id_end;
+        const unsigned key_i = valid ? (unsigned)id : 0xFFFFFFFFu;
         int rank = 0;
         bool dup = false;
         for (int j = 0; j < n; ++j) {
             const int idj = raw[j];
-            const bool vj = idj >= 0 && (long long)ks + (long long)idj * blk < ke;
-            const long long key_j = vj ? (long long)idj : (1LL << 40);
+            const unsigned key_j = idj >= 0 && idj < id_end ? (unsigned)idj : 0xFFFFFFFFu;
             rank += key_j < key_i || (key_j == key_i && j < i);
             dup = dup || (key_j == key_i && j < i);
         }
@@ -145,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int q = 4 * (tid + i * kThreads);
             v[i] = make_float4(NAN, NAN, NAN, NAN);
             if (q < nkeys) {
-                const int e = q / blk, o = q - e * blk;
+                const int e = blk_of(q), o = q - e * blk;
                 const int id = sh.ids[e];
                 const long long t = (long long)ks + (long long)id * blk + o;
                 if (id >= 0 && t + 3 < ke)
@@ -156,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < NV; ++i) {
             const int q = 4 * (tid + i * kThreads);
             if (q < nkeys) {
-                const int e = q / blk, o = q - e * blk;
+                const int e = blk_of(q), o = q - e * blk;
                 const int id = sh.ids[e];
                 const long long t = (long long)ks + (long long)id * blk + o;
                 float x[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
@@ -176,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int q = tid + i * kThreads;
             x[i] = NAN;
             if (q < nkeys) {
-                const int e = q / blk, o = q - e * blk;
+                const int e = blk_of(q), o = q - e * blk;
                 const int id = sh.ids[e];
                 const long long t = (long long)ks + (long long)id * blk + o;
                 if (id >= 0 && t < ke)
@@ -206,6 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t total;
     block_excl(sh, nvalid, &total);  // its barriers also publish hist
     uint32_t T = 0u, ties = 0u;      // T = 0: every finite key is taken
+    bool all_ties = true;
     if (total > (uint32_t)k) {
         find_bin(sh, 2048, (uint32_t)k);
         uint32_t prefix = sh.sel[0] << 21, pmask = 0xFFE00000u, krem = sh.sel[1];
@@ -228,50 +268,59 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         T = prefix;
         ties = krem;
+        all_ties = ties == sh.hist[T & 1023u];  // every key equal to T is taken
     }
 
-    // ordered write: thread t owns keys [t * per, (t + 1) * per)
-    const int per = (nkeys + kThreads - 1) / kThreads;
-    const int q0 = min(nkeys, tid * per), q1 = min(nkeys, q0 + per);
-    uint32_t neq = 0;
-    for (int q = q0; q < q1; ++q)
-        neq += T != 0u && sh.keys[q] == T;
-    uint32_t eq_tot;
-    uint32_t eq_rank = block_excl(sh, neq, &eq_tot);
-    uint32_t nsel = 0;
-    for (int q = q0; q < q1; ++q) {
-        const uint32_t key = sh.keys[q];
-        if (T == 0u) {
-            nsel += key != 0u;
-        } else if (key > T) {
-            ++nsel;
-        } else if (key == T) {
-            nsel += eq_rank < ties;
-            ++eq_rank;
+    // Ordered write.  Step i covers keys [i * kThreads, (i + 1) * kThreads),
+    // thread t key i * kThreads + t, so order is (step, warp, lane): a ballot
+    // ranks a key inside its warp and step, and warp 0 scans the (step,
+    // warp) counts.  Three light passes over the shared keys, ballots
+    // recomputed rather than kept: count the keys equal to T, then the taken
+    // keys (ties in index order up to the quota), then write.
+    const int lane = tid & 31, w = tid >> 5;
+    const uint32_t lt = (1u << lane) - 1u;
+    const int nsteps = (nkeys + kThreads - 1) / kThreads;
+    auto key_at = [&](int i) -> uint32_t {
+        const int q = i * kThreads + tid;
+        return q < nkeys ? sh.keys[q] : 0u;
+    };
+    // pass 0 (only when some key equal to T is left out): keys equal to T
+    if (!all_ties) {
+        for (int i = 0; i < nsteps; ++i) {
+            const uint32_t b = __ballot_sync(0xffffffffu, key_at(i) == T);
+            if (lane == 0)
+                sh.eqtab[i * kWarps + w] = __popc(b);
+        }
+        scan_table(sh, sh.eqtab, nsteps);
+    }
+    // every lane reaches the ballot: all_ties and T are the same CTA-wide
+    const uint32_t tmin = T == 0u ? 1u : T;  // T = 0: every finite (nonzero) key
+    auto taken = [&](int i, uint32_t key) -> bool {
+        if (all_ties)
+            return key >= tmin;
+        const uint32_t eb = __ballot_sync(0xffffffffu, key == T);
+        return key > T || (key == T && sh.eqtab[i * kWarps + w] + __popc(eb & lt) < ties);
+    };
+    // pass 1: taken keys
+    for (int i = 0; i < nsteps; ++i) {
+        const uint32_t b = __ballot_sync(0xffffffffu, taken(i, key_at(i)));
+        if (lane == 0)
+            sh.tab[i * kWarps + w] = __popc(b);
+    }
+    const uint32_t sel_tot = scan_table(sh, sh.tab, nsteps);
+    // pass 2: write
+    for (int i = 0; i < nsteps; ++i) {
+        const uint32_t key = key_at(i);
+        const bool t = taken(i, key);
+        const uint32_t b = __ballot_sync(0xffffffffu, t);
+        if (t) {
+            const int q = i * kThreads + tid;
+            const int e = blk_of(q), o = q - e * blk;
+            out[(size_t)r * ld_out + sh.tab[i * kWarps + w] + __popc(b & lt)] =
+                ks + sh.ids[e] * blk + o;
         }
     }
-    uint32_t sel_tot;
-    uint32_t pos = block_excl(sh, nsel, &sel_tot);
-    eq_rank -= neq;  // back to this thread's first tie rank
     int32_t *orow = out + (size_t)r * ld_out;
-    for (int q = q0; q < q1; ++q) {
-        const uint32_t key = sh.keys[q];
-        bool take;
-        if (T == 0u) {
-            take = key != 0u;
-        } else if (key > T) {
-            take = true;
-        } else if (key == T) {
-            take = eq_rank < ties;
-            ++eq_rank;
-        } else {
-            take = false;
-        }
-        if (take) {
-            const int e = q / blk, o = q - e * blk;
-            orow[pos++] = ks + sh.ids[e] * blk + o;
-        }
-    }
     for (int j = (int)sel_tot + tid; j < k; j += kThreads)
         orow[j] = -1;
 }
