@@ -43,12 +43,13 @@ WORKLOAD_NAMES = {
 
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one logits
-# launch from an ncu capture, per workload, with a digest of the kernel's
-# sources at capture time.  A different digest means the kernel changed
+# stage (the plan kernel and the logits kernel under a candidate plan) from an
+# ncu capture, per workload, with a digest of the kernels' sources at capture
+# time.  A different digest means the kernel changed
 # since and the traffic is reported as null.
 LOGITS_SOURCES = ["idx_logits_kernel.cuh", "idx_logits.cuh", "idx_common.cuh", "idx_api.cu"]
 NCU_TRAFFIC = {
-    4: {"bytes": 435548416, "digest": "7eced4b2285bd1ee",
+    4: {"bytes": 87808 + 189607424 + 8508416, "digest": "e3e3d6a2eea472b5",
         "profile": "profiles/logits_kernel_paged_fp8_decode_b128_mtp2.md"},
 }
 
@@ -160,6 +161,30 @@ def job_value(world: int, keys_per_rank: int, ms_per_step: float) -> float:
     return world * keys_per_rank / (ms_per_step * 1e-3) / 1e9
 
 
+def candidate_tile_logits(case, tile=128) -> int:
+    """(row, key) logits the candidates-only logits call writes: every key of
+    each row below its end inside the tiles (of `tile` keys) that hold a
+    candidate key of some row of the sequence."""
+    ke = np.clip(case.row_ends(), 0, case.width).reshape(case.B, case.next_n)
+    ks = (np.zeros_like(ke) if case.row_ks is None else
+          np.minimum(case.row_ks.reshape(case.B, case.next_n), ke))
+    total = 0
+    for b in range(case.B):
+        hi = int(ke[b].max())
+        tiles = np.zeros(-(-hi // tile) + 1, dtype=bool)
+        for j in range(case.next_n):
+            ids = case.cand[b * case.next_n + j]
+            ids = ids[ids >= 0].astype(np.int64)
+            lo = int(ks[b, j]) + ids * case.cand_block
+            hi_r = np.minimum(lo + case.cand_block, int(ke[b, j]))
+            for t0, t1 in zip(lo[lo < hi_r], hi_r[lo < hi_r]):
+                tiles[t0 // tile:(t1 - 1) // tile + 1] = True
+        idx = np.nonzero(tiles)[0]
+        for j in range(case.next_n):
+            total += int(np.clip(int(ke[b, j]) - idx * tile, 0, tile).sum())
+    return total
+
+
 def candidate_box_keys(case) -> int:
     """Keys in the 64-key boxes that hold a candidate key of some row of their
     sequence (candidate blocks clipped to each row's [ks, ke))."""
@@ -183,7 +208,7 @@ def candidate_box_keys(case) -> int:
     return total
 
 
-def logits_bytes(case) -> float:
+def logits_bytes(case, cand_only: bool = True) -> float:
     """Algorithmic bytes of one logits stage: every live key's values and
     scale read once per sequence (with a candidate mask, only the keys of
     boxes that hold a candidate), the group's queries, weights and candidate
@@ -203,7 +228,10 @@ def logits_bytes(case) -> float:
         else:
             b = float(seq_keys.sum()) * per_key
         b += case.rows * per_q
-        b += float(ke.sum()) * 4
+        if case.cand is not None and cand_only:
+            b += float(candidate_tile_logits(case)) * 4  # only candidate tiles are written
+        else:
+            b += float(ke.sum()) * 4
         b += float(np.ceil(seq_keys / case.page_size).sum()) * 4
         if case.cand is not None:
             b += case.cand.size * 4
@@ -269,7 +297,7 @@ def run_ours(args):
     e2e = run_e2e(step, case, args, dev) if rank == 0 else None
 
     hbm, bf16, src = _peaks()
-    lb = logits_bytes(case)
+    lb = logits_bytes(case, cand_only=getattr(step, "cand_topk", False))
     achieved_gbs = lb / (logit_avg * 1e-3) / 1e9
     if args.config == 2:
         fp8_peak = 2.0 * bf16  # dense fp8 rate = 2x bf16 on this part
