@@ -24,6 +24,7 @@ _ERRORS = {1: "IDX_ERR_INVALID_ARG", 2: "IDX_ERR_UNSUPPORTED", 3: "IDX_ERR_WORKS
            4: "IDX_ERR_CUDA"}
 DEV_BAD_PAGE = 1
 DEV_TIMEOUT = 4
+SLOT_DIRECT_ROWS = 4096  # above it the slot map runs a third (scan) kernel
 
 _lib = None
 _lock = threading.Lock()
@@ -310,7 +311,8 @@ def prepare_topk_to_ragged_slots(topk, block_table, page_size, num_pages, slots,
             block_table.stride(0), mb, page_size, num_pages, _ptr(slots), _ptr(indptr),
             _ptr(lens))
     return Prepared("idx_topk_to_ragged_slots", args,
-                    (topk, block_table, slots, indptr, lens, row_to_seq), 3)
+                    (topk, block_table, slots, indptr, lens, row_to_seq),
+                    2 + (rows > SLOT_DIRECT_ROWS))
 
 
 def idx_topk_to_ragged_slots(topk, block_table, page_size, num_pages, slots, indptr, lens,

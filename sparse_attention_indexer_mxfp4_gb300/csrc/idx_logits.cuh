@@ -109,10 +109,7 @@ struct GroupInfo {
     int tiles;        // units of this group
 };
 
-// Out of line on purpose: it runs once per group and inlining it into every
-// role multiplies the kernel's code size several times over, which starves
-// the instruction cache of the hot loops.
-__device__ __noinline__ GroupInfo group_info(const LogitsArgs &a, int g)
+__device__ __forceinline__ GroupInfo group_info_inline(const LogitsArgs &a, int g)
 {
     GroupInfo gi;
     gi.row0 = g * a.G;
@@ -136,6 +133,14 @@ __device__ __noinline__ GroupInfo group_info(const LogitsArgs &a, int g)
     else
         gi.tiles = (a.N + tk - 1) >> a.tile_shift;  // every column of [0, N) is written
     return gi;
+}
+
+// Out of line on purpose: it runs once per group and inlining it into every
+// role multiplies the kernel's code size several times over, which starves
+// the instruction cache of the hot loops.
+__device__ __noinline__ GroupInfo group_info(const LogitsArgs &a, int g)
+{
+    return group_info_inline(a, g);
 }
 
 __device__ __forceinline__ bool tile_is_compute(const GroupInfo &gi, int j, int shift)
@@ -222,75 +227,84 @@ __device__ __forceinline__ int unit_tile(const LogitsArgs &a, int g, int k)
         return k;
 }
 
-// Find this CTA's first unit: returns (g0, k0) -- the group and the unit's
-// index within it -- and the number of units.
-// scratch: >= blockDim.x/32 + 2 long longs of shared memory.
+// Find this CTA's first unit: returns (g0, k0, n0) -- the group, the unit's
+// index within it and the group's number of units -- and the CTA's number of
+// units.  The CTAs split the units evenly.  Paged: thread t owns a contiguous
+// range of groups, so one block scan of the per-thread unit counts places
+// every range, and the one thread whose range holds the CTA's first unit
+// walks it again (from L1) to find the group.
+// scratch: >= blockDim.x/32 + 3 long longs of shared memory (at most 1024
+// threads).
 template <bool PLAN>
 __device__ __forceinline__ void locate_units(const LogitsArgs &a, long long *scratch, int &g0,
-                                             int &j0, long long &count)
+                                             int &k0, int &n0, long long &count)
 {
-    long long total;
-    int T = 0;
     if (!a.paged) {
-        T = (a.N + (1 << a.tile_shift) - 1) >> a.tile_shift;
-        total = (long long)a.num_groups * T;
-    } else {
-        long long loc = 0;
-        for (int g = threadIdx.x; g < a.num_groups; g += blockDim.x)
-            loc += group_units<PLAN>(a, g);
-        total = block_sum_ll(loc, scratch);
+        const int T = (a.N + (1 << a.tile_shift) - 1) >> a.tile_shift;
+        const long long total = (long long)a.num_groups * T;
+        const long long u0 = total * blockIdx.x / gridDim.x;
+        count = total * (blockIdx.x + 1) / gridDim.x - u0;
+        g0 = (int)(u0 / (T > 0 ? T : 1));
+        k0 = (int)(u0 - (long long)g0 * T);
+        n0 = T;
+        if (count <= 0) {
+            g0 = a.num_groups;
+            k0 = 0;
+            count = 0;
+        }
+        return;
     }
-    long long u0 = total * blockIdx.x / gridDim.x;
-    long long u1 = total * (blockIdx.x + 1) / gridDim.x;
-    count = u1 - u0;
-    if (count <= 0) {
+    const int m = (a.num_groups + (int)blockDim.x - 1) / (int)blockDim.x;
+    const int gb = min((int)threadIdx.x * m, a.num_groups), ge = min(gb + m, a.num_groups);
+    long long loc = 0;
+    for (int g = gb; g < ge; ++g)
+        loc += group_units<PLAN>(a, g);
+    long long total;
+    const long long start = block_incl_scan_ll(loc, scratch, &total) - loc;
+    const long long u0 = total * blockIdx.x / gridDim.x;
+    count = total * (blockIdx.x + 1) / gridDim.x - u0;
+    if (count <= 0) {  // the same in every thread
         g0 = a.num_groups;
-        j0 = 0;
+        k0 = 0;
+        n0 = 0;
         count = 0;
         return;
     }
-    if (!a.paged) {
-        g0 = (int)(u0 / T);
-        j0 = (int)(u0 - (long long)g0 * T);
-        return;
-    }
-    volatile long long *found = scratch + 32;  // [0] = g0, [1] = unit within the group
-    if (threadIdx.x == 0)
-        found[0] = -1;
-    __syncthreads();
-    long long running = 0;
-    for (int base = 0; base < a.num_groups; base += blockDim.x) {
-        int g = base + threadIdx.x;
-        long long v = g < a.num_groups ? group_units<PLAN>(a, g) : 0;
-        long long chunk;
-        long long incl = block_incl_scan_ll(v, scratch, &chunk);
-        long long start = running + incl - v;
-        if (v > 0 && u0 >= start && u0 < start + v) {
-            found[0] = g;
-            found[1] = u0 - start;
+    volatile long long *found = scratch + 32;  // [0] = g0, [1] = unit within it, [2] = its units
+    if (loc > 0 && u0 >= start && u0 < start + loc) {
+        long long run = start;
+        for (int g = gb; g < ge; ++g) {
+            const long long v = group_units<PLAN>(a, g);
+            if (u0 < run + v) {
+                found[0] = g;
+                found[1] = u0 - run;
+                found[2] = v;
+                break;
+            }
+            run += v;
         }
-        running += chunk;
-        __syncthreads();
-        if (found[0] >= 0)
-            break;
     }
+    __syncthreads();
     g0 = (int)found[0];
-    j0 = (int)found[1];  // unit index within the group
+    k0 = (int)found[1];
+    n0 = (int)found[2];
     __syncthreads();
 }
 
+// The first unit's tile load and the group's row ranges are issued together
+// (group_info inlined here: walk_begin runs once, before the roles split).
 template <bool PLAN>
 __device__ __forceinline__ void walk_begin(const LogitsArgs &a, UnitWalk &w, int g0, int k0,
-                                           long long count)
+                                           int n0, long long count)
 {
     w.g = g0;
     w.k = k0;
+    w.n = n0;
     w.left = count;
     w.first_in_group = true;
     if (count > 0) {
-        w.gi = group_info(a, g0);
-        w.n = PLAN ? (int)group_units<PLAN>(a, g0) : w.gi.tiles;
         w.j = unit_tile<PLAN>(a, g0, k0);
+        w.gi = group_info_inline(a, g0);
     }
 }
 

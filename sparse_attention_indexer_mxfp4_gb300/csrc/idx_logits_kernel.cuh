@@ -1,23 +1,25 @@
 // idx_logits_kernel.cuh -- the warp-specialised tcgen05 logits kernel.
 //
 // One persistent CTA per SM, warp-specialised:
-//   producers (warps 0-1, even / odd tiles): TMA loads of each 128-key tile
-//             (values and key scales, page by page through the block table)
-//             into a ring of shared-memory stages; warp 0 also loads each row
-//             group's Q tile, weights and scales into one of two group slots
-//             and builds the group's candidate bitmap.  The 32 lanes resolve
-//             the pages of 16 tiles at a time (one half-tile each), one window
+//   producers (warps 0-1, even / odd tiles): TMA loads of each tile
+//             (values and key scales, 64-key boxes page by page through the
+//             block table) into a ring of shared-memory stages; warp 0 also
+//             loads each row group's Q tile, weights and scales into one of
+//             two group slots and builds the group's candidate bitmap.  The
+//             32 lanes resolve the pages of 32 boxes at a time, one window
 //             ahead, so a tile costs a barrier wait and a few TMA issues;
 //   MMA issuers (warps 2-3): one elected lane issues the tcgen05 MMAs
 //             S[t, (r,h)] = k[t,:] . q[r,h,:] with keys on M (128 TMEM lanes)
 //             and the group's (row, head) pairs on N, into one of NA TMEM
-//             accumulators; warp 2 owns the TMEM allocation;
+//             accumulators, after the warp has copied the tile's key scales
+//             out of the stage, which the MMA's commit then frees; warp 2 owns
+//             the TMEM allocation;
 //   epilogue  NA warpgroups, one per accumulator: thread i of a warpgroup
 //             owns TMEM lane i, i.e. one key, and reduces
 //             sum_h w[r,h] * relu(scale * S[t,(r,h)]) over the heads in
 //             registers, applies the [ks, ke) and candidate masks and stores
 //             the fp32 logit.  Per-head scores never leave TMEM and registers;
-//             the key's scale comes from the stage.
+//             the key's scale comes from the accumulator's side copy.
 // Stages, group slots and accumulators are handed over with mbarriers whose
 // waits are all bounded (mbar_wait), so a broken pipeline ends the kernel
 // with IDX_DEV_TIMEOUT instead of hanging.
@@ -67,7 +69,12 @@ struct LogitsCfg {
     static constexpr int OFF_W = OFF_Q + 2 * Q_BYTES;
     static constexpr int OFF_QS = OFF_W + 2 * W_BYTES;
     static constexpr int OFF_QATOM = OFF_QS + 2 * QS_BYTES;
-    static constexpr int OFF_BAR = (OFF_QATOM + 4 * QATOM_BYTES + 7) / 8 * 8;
+    // per accumulator: the tile's key scales (FP8) and flags, copied out of
+    // the stage by the MMA warp so that the stage is free once the MMA is done
+    static constexpr int SIDE_FLAGS = FMT == kFmtFp8 ? TK * 4 : 0;
+    static constexpr int SIDE_BYTES = SIDE_FLAGS + 16;
+    static constexpr int OFF_SIDE = OFF_QATOM + 4 * QATOM_BYTES;
+    static constexpr int OFF_BAR = (OFF_SIDE + NA * SIDE_BYTES + 7) / 8 * 8;
     // full[S], empty[S], acc_full[NA], acc_empty[NA], q_full[2], q_empty[2]
     static constexpr int NUM_BARS = 2 * S + 2 * NA + 4;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;  // tmem base, abort flag
@@ -88,10 +95,10 @@ struct LogitsCfg {
     static constexpr int EPI_WARPS = 4 * NA;
     static constexpr int THREADS = 32 * (kFirstEpiWarp + EPI_WARPS);
     // Tile c uses stage c % S.  S a multiple of 2 and of NA keeps every stage
-    // (and every accumulator) with one producer, one MMA warp and one
-    // epilogue warpgroup, each of which waits on every phase of it in turn:
-    // a role that could skip a phase might wait one phase early, and an
-    // mbarrier parity wait cannot tell phase n from phase n + 2.
+    // with one producer and one MMA warp (and every accumulator with one MMA
+    // warp and one epilogue warpgroup), each of which waits on every phase of
+    // it in turn: a role that could skip a phase might wait one phase early,
+    // and an mbarrier parity wait cannot tell phase n from phase n + 2.
     static_assert(S >= 2 && S % 2 == 0 && S % NA == 0, "stages must divide among the roles");
     __host__ __device__ static constexpr int stage(int c) { return c % S; }
     __host__ __device__ static constexpr uint32_t phase(int c) { return (uint32_t)(c / S) & 1u; }
@@ -189,10 +196,10 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1 + 4);  // MMA commit + the owning epilogue warpgroup
+            mbar_init(&empty[s], 1);  // the MMA's commit
         }
         for (int i = 0; i < NA; ++i) {
-            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_full[i], 2);  // the MMA's commit + the MMA warp's side copy
             mbar_init(&acc_empty[i], 4);  // the owning warpgroup's warps
         }
         for (int i = 0; i < 2; ++i) {
@@ -215,16 +222,16 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
     // logits buffer may still be in use by the previous kernel on the stream
     pdl_wait();
     pdl_launch_dependents();
-    int g0, j0;
+    int g0, k0, n0;
     long long count;
-    locate_units<PLAN>(a, scratch, g0, j0, count);  // contains __syncthreads
+    locate_units<PLAN>(a, scratch, g0, k0, n0, count);  // contains __syncthreads
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
     UnitWalk w;
-    walk_begin<PLAN>(a, w, g0, j0, count);
+    walk_begin<PLAN>(a, w, g0, k0, n0, count);
 
     if (warp < 2) {
         // ------------------------------------------------------------ producers
@@ -399,6 +406,20 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
                 if (!mbar_wait(&full[s], C::phase(c), abort_flag, a.status))
                     break;
                 uint8_t *st = smem + C::OFF_STAGE + s * C::STAGE_BYTES;
+                {
+                    // the epilogue's key scales and flags, out of the stage
+                    uint8_t *sd = smem + C::OFF_SIDE + acc * C::SIDE_BYTES;
+                    if constexpr (FMT == kFmtFp8) {
+                        const float4 *src = reinterpret_cast<const float4 *>(st + C::A_BYTES);
+                        #pragma unroll
+                        for (int i = lane; i < TK / 4; i += 32)
+                            reinterpret_cast<float4 *>(sd)[i] = src[i];
+                    }
+                    if (lane == 0)
+                        *reinterpret_cast<uint32_t *>(sd + C::SIDE_FLAGS) =
+                            *reinterpret_cast<const uint32_t *>(st + C::OFF_FLAGS);
+                    __syncwarp();
+                }
                 if constexpr (FMT == kFmtMxfp4) {
                     // K scale words (key-major as loaded) -> one MMA-order atom
                     // per 128 keys
@@ -451,6 +472,7 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
                     }
                     mma_commit(&empty[s]);
                     mma_commit(&acc_full[acc]);
+                    mbar_arrive(&acc_full[acc]);  // releases the side copy
                 }
                 __syncwarp();
                 ++c;
@@ -505,13 +527,14 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
                 mine = (int)(u % NA) == wg;
             }
             if (compute && mine) {
-                // key scales and page validity from the stage, which is then
-                // released (the MMA's commit is the stage's other arrival)
-                const int s = C::stage(c - 1);
-                if (!mbar_wait(&full[s], C::phase(c - 1), abort_flag, a.status))
+                const int acc = wg;
+                const int use = (c - 1) / NA;  // uses of this accumulator so far
+                if (!mbar_wait(&acc_full[acc], (uint32_t)(use & 1), abort_flag, a.status))
                     break;
-                const uint8_t *st = smem + C::OFF_STAGE + s * C::STAGE_BYTES;
-                const uint32_t halves = *reinterpret_cast<const uint32_t *>(st + C::OFF_FLAGS);
+                tc_fence_after();
+                // key scales and box flags from the accumulator's side copy
+                const uint8_t *sd = smem + C::OFF_SIDE + acc * C::SIDE_BYTES;
+                const uint32_t halves = *reinterpret_cast<const uint32_t *>(sd + C::SIDE_FLAGS);
                 bool live[NSUB];
                 float ksc[NSUB];
                 bool pos = true;
@@ -521,17 +544,9 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
                     live[sub] = t < w.gi.hi && t >= w.gi.lo && ((halves >> (key >> 6)) & 1u);
                     ksc[sub] = 1.0f;
                     if (FMT == kFmtFp8)
-                        ksc[sub] = reinterpret_cast<const float *>(st + C::A_BYTES)[key];
+                        ksc[sub] = reinterpret_cast<const float *>(sd)[key];
                     pos = pos && ksc[sub] >= 0.0f;
                 }
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&empty[s]);
-                const int acc = wg;
-                const int use = (c - 1) / NA;  // uses of this accumulator so far
-                if (!mbar_wait(&acc_full[acc], (uint32_t)(use & 1), abort_flag, a.status))
-                    break;
-                tc_fence_after();
                 const float *wsm = reinterpret_cast<const float *>(smem + C::OFF_W + slot * C::W_BYTES);
                 const float *qsm = reinterpret_cast<const float *>(smem + C::OFF_QS + slot * C::QS_BYTES);
                 const bool use_qs = FMT == kFmtFp8 && a.q_scale != nullptr;

@@ -141,6 +141,11 @@ __global__ void __launch_bounds__(kSlotThreads)
     }
 }
 
+// Up to this many rows each write CTA adds up the earlier rows' counts
+// itself (at most rows / kSlotThreads loads a thread, from L2); above it a
+// scan kernel writes indptr first, since the direct sums grow as rows^2.
+constexpr int kSlotDirectRows = 4096;
+
 __global__ void __launch_bounds__(1024) indptr_scan_kernel(const int32_t *__restrict__ lens, int rows,
                                                            int32_t *__restrict__ indptr)
 {
@@ -187,17 +192,23 @@ __global__ void __launch_bounds__(1024) indptr_scan_kernel(const int32_t *__rest
     }
 }
 
-// Ordered write of one row's valid slots.  Entry order is (step i, warp,
-// lane); a ballot gives each lane its rank inside the warp and step, and
-// warp 0 scans the (step, warp) counts once per batch of kSlotSteps steps.
+// Ordered write of one row's valid slots.  The row's offset is indptr[r]
+// when the scan kernel ran (scanned != 0); otherwise it is the sum of the
+// earlier rows' counts, which the CTA adds up itself and publishes as
+// indptr[r + 1] (CTA 0 also writes indptr[0] = 0).  Entry order is (step i,
+// warp, lane); a ballot gives each lane its rank inside the warp and step,
+// and warp 0 scans the (step, warp) counts once per batch of kSlotSteps
+// steps.
 __global__ void __launch_bounds__(kSlotThreads)
     slot_write_kernel(const int32_t *__restrict__ topk, int64_t ld, int rows, int k,
                       const int32_t *__restrict__ row_to_seq, int next_n, SlotGeom g,
-                      const int32_t *__restrict__ indptr, int32_t *__restrict__ slots)
+                      const int32_t *__restrict__ lens, int32_t *__restrict__ indptr,
+                      int scanned, int32_t *__restrict__ slots)
 {
     constexpr int NW = kSlotThreads / 32;
     static_assert(kSlotSteps * NW == 64, "warp 0 scans 64 (step, warp) counts");
     __shared__ uint32_t tab[kSlotSteps * NW + 1];
+    __shared__ uint32_t red[NW];
     pdl_wait();
     pdl_launch_dependents();
     const int r = blockIdx.x;
@@ -205,11 +216,34 @@ __global__ void __launch_bounds__(kSlotThreads)
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const uint32_t lt = (1u << lane) - 1u;
     const int32_t *trow = topk + (size_t)r * ld;
-    int32_t *dst = slots + indptr[r];
+    // the first batch's loads go out before the offset is summed
+    int sl[kSlotSteps];
+    row_slots(trow, k, 0, b, g, sl);
+    uint32_t off = 0;
+    if (scanned) {
+        off = (uint32_t)indptr[r];
+    } else {
+        uint32_t part = 0;
+        for (int i = threadIdx.x; i < r; i += kSlotThreads)
+            part += (uint32_t)lens[i];
+        for (int o = 16; o > 0; o >>= 1)
+            part += __shfl_xor_sync(0xffffffffu, part, o);
+        if (lane == 0)
+            red[w] = part;
+        __syncthreads();
+        for (int i = 0; i < NW; ++i)
+            off += red[i];
+        if (threadIdx.x == 0) {
+            indptr[r + 1] = (int32_t)(off + (uint32_t)lens[r]);
+            if (r == 0)
+                indptr[0] = 0;
+        }
+    }
+    int32_t *dst = slots + off;
     uint32_t written = 0;
     for (int base = 0; base < k; base += kSlotSteps * kSlotThreads) {
-        int sl[kSlotSteps];
-        row_slots(trow, k, base, b, g, sl);
+        if (base > 0)
+            row_slots(trow, k, base, b, g, sl);
         uint32_t ball[kSlotSteps];
         #pragma unroll
         for (int i = 0; i < kSlotSteps; ++i) {
@@ -468,11 +502,13 @@ extern "C" idx_status idx_topk_to_ragged_slots(const int32_t *topk, int64_t ld, 
     g.num_pages = num_pages;
     cudaError_t e = launch_pdl(slot_count_kernel, dim3(rows), dim3(kSlotThreads), 0, s, topk, ld,
                                rows, k, row_to_seq, next_n, g, lens, status);
-    if (e == cudaSuccess)
-        e = launch_pdl(indptr_scan_kernel, dim3(1), dim3(1024), 0, s, lens, rows, indptr);
+    const int scanned = rows > kSlotDirectRows;
+    if (e == cudaSuccess && scanned)
+        e = launch_pdl(indptr_scan_kernel, dim3(1), dim3(1024), 0, s, (const int32_t *)lens, rows,
+                       indptr);
     if (e == cudaSuccess)
         e = launch_pdl(slot_write_kernel, dim3(rows), dim3(kSlotThreads), 0, s, topk, ld, rows, k,
-                       row_to_seq, next_n, g, indptr, slots);
+                       row_to_seq, next_n, g, (const int32_t *)lens, indptr, scanned, slots);
     return launch_status(e);
 }
 

@@ -133,8 +133,11 @@ def test_candidate_mask(width, blk, C, repeat):
 # ------------------------------------------------------------------ slot map
 
 
+# 4096 rows is the largest batch whose write kernel sums its own offsets;
+# 4097 and up run the scan kernel first
 @pytest.mark.parametrize("rows,k,P,next_n", [(1, 1, 64, 1), (6, 50, 16, 2), (256, 2048, 64, 2),
-                                             (1500, 300, 128, 1)])
+                                             (1500, 300, 128, 1), (4096, 40, 16, 2),
+                                             (4097, 40, 16, 1), (9000, 17, 64, 3)])
 def test_slots(rows, k, P, next_n):
     rng = np.random.default_rng(rows + k)
     nseq = -(-rows // next_n)
