@@ -94,6 +94,10 @@ bool encode_tma_u8(CUtensorMap *map, int rank, const void *base, const uint64_t 
 namespace {
 
 constexpr size_t kMaxSmem = 227 * 1024;
+// Units a CTA is charged for starting a row group of a paged call (see
+// locate_units), for 128-key tiles: about the latency of a group start over
+// the time of a tile.  256-key tiles measured best with no charge.
+constexpr int kGroupCost128 = 5;
 constexpr int kMaxSmemBytes = 227 * 1024;
 
 template <int FMT, int H, int G, int S, int NA, int TK>
@@ -103,6 +107,7 @@ cudaError_t launch_logits_t(const LogitsArgs &a0, const CUtensorMap &tmK, const 
     using C = LogitsCfg<FMT, H, G, S, NA, TK>;
     LogitsArgs a = a0;
     a.tile_shift = TK == 256 ? 8 : 7;
+    a.group_cost = a.paged && TK == 128 ? kGroupCost128 : 0;
     const size_t smem = (size_t)C::fixed_bytes() + (size_t)2 * G * a.cand_words * 4;
     const int plan = a.plan ? 1 : 0;
     auto kern = plan ? logits_kernel<FMT, H, G, S, NA, TK, true>

@@ -66,6 +66,7 @@ struct LogitsArgs {
     int width;               // paged: max_model_len; contiguous: N
     unsigned int *status;    // device status word (IDX_DEV_* bits)
     int tile_shift;          // log2 of the keys per tile (7 or 8)
+    int group_cost;          // paged: units a CTA is charged for starting a row group
     // Candidate gather plan (nullable), written by cand_plan_kernel: per row
     // group plan_words words: [0] the number n of compute tiles (tiles that
     // hold a candidate key of any of the group's rows), then box_words words
@@ -229,10 +230,14 @@ __device__ __forceinline__ int unit_tile(const LogitsArgs &a, int g, int k)
 
 // Find this CTA's first unit: returns (g0, k0, n0) -- the group, the unit's
 // index within it and the group's number of units -- and the CTA's number of
-// units.  The CTAs split the units evenly.  Paged: thread t owns a contiguous
-// range of groups, so one block scan of the per-thread unit counts places
-// every range, and the one thread whose range holds the CTA's first unit
-// walks it again (from L1) to find the group.
+// units.  The CTAs split the units evenly.  Paged: every group with units
+// also counts a.group_cost leading units that are never scored, so that a
+// CTA whose range starts a group (new Q tile, row ranges and page window:
+// a few microseconds of latency) gets that many fewer tiles; k0 and count
+// include them and the walk skips them.  Thread t owns a contiguous range
+// of groups, so one block scan of the per-thread unit counts places every
+// range, and the one thread whose range holds the CTA's first unit walks it
+// again (from L1) to find the group.
 // scratch: >= blockDim.x/32 + 3 long longs of shared memory (at most 1024
 // threads).
 template <bool PLAN>
@@ -257,8 +262,10 @@ __device__ __forceinline__ void locate_units(const LogitsArgs &a, long long *scr
     const int m = (a.num_groups + (int)blockDim.x - 1) / (int)blockDim.x;
     const int gb = min((int)threadIdx.x * m, a.num_groups), ge = min(gb + m, a.num_groups);
     long long loc = 0;
-    for (int g = gb; g < ge; ++g)
-        loc += group_units<PLAN>(a, g);
+    for (int g = gb; g < ge; ++g) {
+        const long long v = group_units<PLAN>(a, g);
+        loc += v > 0 ? v + a.group_cost : 0;
+    }
     long long total;
     const long long start = block_incl_scan_ll(loc, scratch, &total) - loc;
     const long long u0 = total * blockIdx.x / gridDim.x;
@@ -275,13 +282,14 @@ __device__ __forceinline__ void locate_units(const LogitsArgs &a, long long *scr
         long long run = start;
         for (int g = gb; g < ge; ++g) {
             const long long v = group_units<PLAN>(a, g);
-            if (u0 < run + v) {
+            const long long e = v > 0 ? v + a.group_cost : 0;
+            if (u0 < run + e) {
                 found[0] = g;
                 found[1] = u0 - run;
                 found[2] = v;
                 break;
             }
-            run += v;
+            run += e;
         }
     }
     __syncthreads();
@@ -293,17 +301,19 @@ __device__ __forceinline__ void locate_units(const LogitsArgs &a, long long *scr
 
 // The first unit's tile load and the group's row ranges are issued together
 // (group_info inlined here: walk_begin runs once, before the roles split).
+// k0 and count include the group's charged units (paged), which are skipped.
 template <bool PLAN>
 __device__ __forceinline__ void walk_begin(const LogitsArgs &a, UnitWalk &w, int g0, int k0,
                                            int n0, long long count)
 {
+    const int skip = a.paged ? max(a.group_cost - k0, 0) : 0;
     w.g = g0;
-    w.k = k0;
+    w.k = a.paged ? max(k0 - a.group_cost, 0) : k0;
     w.n = n0;
-    w.left = count;
+    w.left = count - skip;
     w.first_in_group = true;
-    if (count > 0) {
-        w.j = unit_tile<PLAN>(a, g0, k0);
+    if (w.left > 0) {
+        w.j = unit_tile<PLAN>(a, g0, w.k);
         w.gi = group_info_inline(a, g0);
     }
 }
@@ -314,7 +324,7 @@ __device__ __forceinline__ bool walk_last_in_group(const UnitWalk &w)
 }
 
 // Next unit: the group's next one, else the first of the next group that
-// has units.
+// has units (after its charged units, paged).
 template <bool PLAN>
 __device__ __forceinline__ void walk_next(const LogitsArgs &a, UnitWalk &w)
 {
@@ -327,6 +337,8 @@ __device__ __forceinline__ void walk_next(const LogitsArgs &a, UnitWalk &w)
         w.first_in_group = true;
         w.gi = group_info(a, w.g);
         w.n = PLAN ? (int)group_units<PLAN>(a, w.g) : w.gi.tiles;
+        if (w.n > 0 && a.paged)
+            w.left -= a.group_cost;
     }
     if constexpr (PLAN) {
         if (w.left > 0)
