@@ -718,27 +718,48 @@ __global__ void __launch_bounds__(kPlanThreads) cand_plan_kernel(const __grid_co
     pdl_launch_dependents();
     const int g = blockIdx.x, slice = blockIdx.y, tid = threadIdx.x;
     const int tw = ((a.width + kMmaM - 1) / kMmaM + 31) / 32;
+    // the group's candidate ids (row-major over its rows) are loaded before
+    // the row ranges, so the two loads overlap; ids past the register batch
+    // are read in the loop below
+    const int row0 = g * a.G, nrows = min(a.G, a.total_rows - row0);
+    const int nid = nrows * a.num_cand;
+    constexpr int kIds = 4;
+    int idv[kIds];
+    #pragma unroll
+    for (int q = 0; q < kIds; ++q) {
+        const int e = tid + q * kPlanThreads;
+        idv[q] = -1;
+        if (e < nid)
+            idv[q] = a.cand[(size_t)(row0 + e / a.num_cand) * a.cand_stride + e % a.num_cand];
+    }
     const GroupInfo gi = group_info(a, g);
     for (int i = tid; i < a.box_words + tw; i += kPlanThreads)
         pbits[i] = 0u;
     if (tid < gi.nrows)
         row_range(a, gi.row0 + tid, rks[tid], rke[tid]);
     __syncthreads();
-    for (int i = 0; i < gi.nrows; ++i) {
+    for (int q = 0; q * kPlanThreads < nid; ++q) {
+        const int e = tid + q * kPlanThreads;
+        if (e >= nid)
+            break;
+        int id = -1;
+        #pragma unroll
+        for (int qq = 0; qq < kIds; ++qq)
+            if (qq == q)
+                id = idv[qq];
+        if (q >= kIds)
+            id = a.cand[(size_t)(row0 + e / a.num_cand) * a.cand_stride + e % a.num_cand];
+        if (id < 0)
+            continue;
+        const int i = e / a.num_cand;
         const int ks = rks[i], ke = rke[i];
-        const int32_t *cr = a.cand + (size_t)(gi.row0 + i) * a.cand_stride;
-        for (int e = tid; e < a.num_cand; e += kPlanThreads) {
-            const int id = cr[e];
-            if (id < 0)
-                continue;
-            const long long lo = (long long)ks + (long long)id * a.cand_block;
-            if (lo >= ke)
-                continue;
-            const int t_lo = (int)lo;
-            const int t_hi = (int)min((long long)ke, lo + a.cand_block);
-            for (int b = t_lo / kHalfKeys; b <= (t_hi - 1) / kHalfKeys; ++b)
-                atomicOr(&box[b >> 5], 1u << (b & 31));
-        }
+        const long long lo = (long long)ks + (long long)id * a.cand_block;
+        if (lo >= ke)
+            continue;
+        const int t_lo = (int)lo;
+        const int t_hi = (int)min((long long)ke, lo + a.cand_block);
+        for (int b = t_lo / kHalfKeys; b <= (t_hi - 1) / kHalfKeys; ++b)
+            atomicOr(&box[b >> 5], 1u << (b & 31));
     }
     __syncthreads();
     // tile bits; thread t owns the contiguous tiles [t * per, (t + 1) * per)

@@ -428,8 +428,12 @@ extern "C" idx_status idx_topk_candidates(const float *logits, int64_t ld, int r
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return IDX_ERR_CUDA;
     if (!configured[dev]) {
+        // two CTAs per SM need the largest shared-memory carveout
         if (cudaFuncSetAttribute(T::topk_cand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem) != cudaSuccess)
+                                 (int)smem) != cudaSuccess ||
+            cudaFuncSetAttribute(T::topk_cand_kernel,
+                                 cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared) != cudaSuccess)
             return IDX_ERR_CUDA;
         configured[dev] = 1;
     }

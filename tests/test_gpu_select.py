@@ -178,7 +178,10 @@ def test_slots_row_to_seq_and_invalid_pages():
 
 
 def _cand_case(rng, rows, width, num_cand, blk, row_repeat=1, ties=None):
-    if ties:
+    if ties == "narrow":
+        # distinct values inside one bin of the first radix digit
+        x = rng.uniform(1.0, 1.2, size=(rows, width)).astype(np.float32)
+    elif ties:
         x = rng.integers(0, ties, size=(rows, width)).astype(np.float32)
     else:
         x = rng.standard_normal((rows, width)).astype(np.float32)
@@ -193,10 +196,14 @@ def _cand_case(rng, rows, width, num_cand, blk, row_repeat=1, ties=None):
     return x, ks, ke, cand
 
 
+# The last three: candidate ids over a wide range (blocks of one key), and a
+# threshold bin holding most keys, with ties left out and with distinct values.
 @pytest.mark.parametrize("rows,width,num_cand,blk,k,rr,ties", [
     (3, 1000, 4, 64, 50, 1, None), (17, 20000, 64, 128, 2048, 1, None),
     (8, 9000, 64, 128, 300, 2, None), (5, 40000, 128, 128, 2048, 1, 3),
-    (4, 5000, 16, 100, 4000, 1, None), (6, 70000, 64, 256, 2048, 1, 7)])
+    (4, 5000, 16, 100, 4000, 1, None), (6, 70000, 64, 256, 2048, 1, 7),
+    (4, 80000, 256, 1, 100, 1, None), (3, 20000, 128, 128, 2048, 1, 2),
+    (3, 20000, 128, 128, 2048, 1, "narrow")])
 def test_topk_candidates_equals_mask_then_topk(rows, width, num_cand, blk, k, rr, ties):
     rng = np.random.default_rng(rows * 31 + num_cand + blk)
     x, ks, ke, cand = _cand_case(rng, rows, width, num_cand, blk, rr, ties)
