@@ -49,7 +49,7 @@ WORKLOAD_NAMES = {
 # since and the traffic is reported as null.
 LOGITS_SOURCES = ["idx_logits_kernel.cuh", "idx_logits.cuh", "idx_common.cuh", "idx_api.cu"]
 NCU_TRAFFIC = {
-    4: {"bytes": 87808 + 189607424 + 8508416, "digest": "e3e3d6a2eea472b5",
+    4: {"bytes": 91136 + 189571328 + 8772608, "digest": "1d3a6cfb962b53b2",
         "profile": "profiles/logits_kernel_paged_fp8_decode_b128_mtp2.md"},
 }
 
