@@ -27,10 +27,12 @@ class IndexerStep:
     ``cand_topk`` (with a fused mask and the gather plan) writes only the
     tiles holding candidate keys and selects with idx_topk_candidates, which
     reads only the candidate blocks; the top-k and slots are the same, the
-    logits outside those tiles are left unwritten."""
+    logits outside those tiles are left unwritten.  ``kv_from`` (another
+    IndexerStep of the same case) shares its device K cache instead of
+    uploading a second copy."""
 
     def __init__(self, case, device="cuda", fused_mask: bool = True, num_ctas: int = 0,
-                 gather: bool = True, cand_topk: bool = True):
+                 gather: bool = True, cand_topk: bool = True, kv_from=None):
         self.case = case
         self.device = torch.device(device)
         self.fused_mask = fused_mask
@@ -43,7 +45,7 @@ class IndexerStep:
         self.weights = _dev(case.weights, d)
         self.q_scale = _dev(case.q_scale, d)
         if self.paged:
-            self.pages = _dev(case.pages, d)
+            self.pages = kv_from.pages if kv_from is not None else _dev(case.pages, d)
             self.block_table = _dev(case.block_table, d)
             self.context_lens = _dev(case.context_lens, d)
             self.row_ks = _dev(case.row_ks, d)
@@ -53,8 +55,8 @@ class IndexerStep:
             self.rows, self.width = case.rows, case.width
             self.max_blocks = case.max_blocks
         else:
-            self.k = _dev(case.k, d)
-            self.k_scale = _dev(case.k_scale, d)
+            self.k = kv_from.k if kv_from is not None else _dev(case.k, d)
+            self.k_scale = kv_from.k_scale if kv_from is not None else _dev(case.k_scale, d)
             self.ks = _dev(case.ks, d)
             self.ke = _dev(case.ke, d)
             self.lengths = self.ke
