@@ -140,6 +140,40 @@ idx_status idx_paged_mqa_logits(const void *q, const void *q_scale, const float 
                                 size_t ws_bytes, idx_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * idx_paged_mqa_logits_block_max -- the candidate source: idx_paged_mqa_logits
+ * without a candidate mask, which also writes the block maxima of its logits
+ * from the same walk.
+ * Passage: vllm.v1.attention.ops.rocm_paged_mxfp4_indexer, module description
+ * (the candidate source "takes its block maxima from the same walk that writes
+ * its logits"), reserve_rocm_mxfp4_indexer_workspace (block scores
+ * [rows, cdiv(logits_width, candidate_block_size)] fp32) and
+ * rocm_mxfp4_sparse_attn_indexer (candidate_write: the source's scores are
+ * not masked to a pool).
+ *
+ *   Arguments as idx_paged_mqa_logits with no candidates and no scratch, plus
+ *   block_max   fp32 [B * next_n, ld_block_max], ld_block_max >=
+ *               nb = ceil(max_model_len / block_size), caller-owned.  Block j
+ *               of row r covers the keys [ks + j * block_size,
+ *               ks + (j + 1) * block_size) clipped to [ks, ke) (numbered
+ *               from the row start, like candidate ids); block_max[r, j] is
+ *               the largest logit there, -inf for an empty block.  Columns
+ *               [0, nb) of every row are written (a first kernel fills them
+ *               with -inf, the logits kernel raises them with atomics).
+ *   block_size  keys per block, >= 32.
+ *   Selecting a row's candidate blocks is then idx_topk over block_max with
+ *   lengths ceil((ke - ks) / block_size).
+ * Errors: IDX_ERR_INVALID_ARG for a null block_max, block_size <= 0 or
+ *   ld_block_max < nb; IDX_ERR_UNSUPPORTED for block_size < 32 or next_n > 2;
+ *   otherwise as idx_paged_mqa_logits.
+ * ---------------------------------------------------------------------- */
+idx_status idx_paged_mqa_logits_block_max(
+    const void *q, const void *q_scale, const float *weights, const uint8_t *kv_pages,
+    int64_t page_stride_bytes, int num_pages, const int32_t *block_table, int64_t bt_stride,
+    const int32_t *context_lens, int ctx_per_row, const int32_t *row_ks, int B, int next_n, int H,
+    int D, int page_size, idx_kv_format fmt, float *logits, int64_t ld_logits, int max_model_len,
+    float *block_max, int64_t ld_block_max, int block_size, int num_ctas, idx_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * idx_paged_mqa_logits_candidates -- idx_paged_mqa_logits for a consumer
  * that reads only the candidate blocks (idx_topk_candidates).
  * Passage: as idx_paged_mqa_logits; the candidate mask of rocm_aiter_mla_sparse,

@@ -71,6 +71,8 @@ def _declare(L):
     L.orc_paged_mqa_logits.restype = _I
     L.orc_apply_candidate_mask.argtypes = [_P, _L, _I, _I, _P, _P, _P, _L, _I, _I, _I, _I]
     L.orc_apply_candidate_mask.restype = _I
+    L.orc_block_max.argtypes = [_P, _L, _I, _I, _P, _P, _I, _P, _L, _I, _I]
+    L.orc_block_max.restype = _I
     L.orc_topk.argtypes = [_P, _L, _I, _I, _P, _I, _P, _L, _I]
     L.orc_topk.restype = _I
     L.orc_topk_to_ragged_slots.argtypes = [_P, _L, _I, _I, _P, _I, _P, _L, _I, _I, _I,
@@ -165,6 +167,22 @@ def apply_candidate_mask(logits, row_ks, row_ke, cand, block_size, row_repeat=1,
     if rc != 0:
         raise ValueError("oracle apply_candidate_mask rejected its arguments")
     return logits
+
+
+def block_max(logits, row_ks, row_ke, block_size, nthreads=0) -> np.ndarray:
+    """Block maxima [rows, cdiv(width, block_size)] float32 of the candidate
+    source: block j of row r is [ks + j*bs, ks + (j+1)*bs) clipped to
+    [ks, ke); -inf when empty."""
+    lg = _c(logits, np.float32)
+    rows, width = lg.shape
+    nb = -(-width // block_size)
+    out = np.empty((rows, max(nb, 1)), dtype=np.float32)
+    rks, rke = _c(row_ks, np.int32), _c(row_ke, np.int32)
+    rc = lib().orc_block_max(_ptr(lg), width, rows, width, _ptr(rks), _ptr(rke), block_size,
+                             _ptr(out), out.shape[1], nb, nthreads)
+    if rc != 0:
+        raise ValueError("oracle block_max rejected its arguments")
+    return out[:, :nb]
 
 
 def topk(logits, lengths, k, nthreads=0) -> np.ndarray:

@@ -429,6 +429,57 @@ int orc_apply_candidate_mask(float *logits, int64_t ld, int rows, int width,
 }
 
 /* ------------------------------------------------------------------------ */
+/* Block maxima of the candidate source: rocm_paged_mxfp4_indexer, module   */
+/* description (the candidate source "takes its block maxima from the same  */
+/* walk that writes its logits") and reserve_rocm_mxfp4_indexer_workspace   */
+/* (block scores [rows, cdiv(logits_width, candidate_block_size)] fp32).    */
+/* Block j of row r holds the keys [ks + j*bs, ks + (j+1)*bs) clipped to    */
+/* [ks, ke), numbered from the row start like the candidate ids of          */
+/* _apply_candidate_mask_strided; its score is the largest logit there,     */
+/* -inf for an empty block.  NaN logits never win (fmax semantics).        */
+/* ------------------------------------------------------------------------ */
+
+struct bmax_ctx {
+    const float *logits;
+    int64_t ld;
+    int width;
+    const int32_t *row_ks, *row_ke;
+    int block_size;
+    float *out;
+    int64_t ld_out;
+    int nblocks;
+};
+
+static void bmax_row(void *vc, int r)
+{
+    struct bmax_ctx *c = (struct bmax_ctx *)vc;
+    const int ke = clampi(c->row_ke[r], 0, c->width);
+    const int ks = c->row_ks ? clampi(c->row_ks[r], 0, ke) : 0;
+    const float *row = c->logits + (size_t)r * c->ld;
+    float *o = c->out + (size_t)r * c->ld_out;
+    for (int j = 0; j < c->nblocks; ++j) {
+        float m = -INFINITY;
+        const long long lo = (long long)ks + (long long)j * c->block_size;
+        for (long long t = lo; t < lo + c->block_size && t < ke; ++t)
+            if (row[t] > m)
+                m = row[t];
+        o[j] = m;
+    }
+}
+
+/* out[r, 0:nblocks) = the block maxima of row r (see above). */
+int orc_block_max(const float *logits, int64_t ld, int rows, int width,
+                  const int32_t *row_ks, const int32_t *row_ke, int block_size,
+                  float *out, int64_t ld_out, int nblocks, int nthreads)
+{
+    if (block_size <= 0 || nblocks < 0 || ld_out < nblocks)
+        return 1;
+    struct bmax_ctx c = {logits, ld, width, row_ks, row_ke, block_size, out, ld_out, nblocks};
+    parallel_rows(bmax_row, &c, rows, nthreads);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Per-row top-k: rocm_paged_mxfp4_indexer _topk semantics.                 */
 /* ------------------------------------------------------------------------ */
 

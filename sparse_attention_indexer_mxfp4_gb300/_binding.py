@@ -38,6 +38,8 @@ _SIGNATURES = {
     "idx_apply_candidate_mask": [_P, _L, _I, _I, _P, _P, _P, _L, _I, _I, _I, _P],
     "idx_topk": [_P, _L, _I, _P, _I, _P, _L, _P, _S, _P],
     "idx_paged_mqa_logits_candidates": None,  # same as idx_paged_mqa_logits
+    "idx_paged_mqa_logits_block_max": [_P, _P, _P, _P, _L, _I, _P, _L, _P, _I, _P, _I, _I, _I,
+                                       _I, _I, _I, _P, _L, _I, _P, _L, _I, _I, _P],
     "idx_topk_noalloc": [_P, _L, _I, _P, _I, _P, _L, _P],
     "idx_topk_candidates": [_P, _L, _I, _P, _P, _P, _L, _I, _I, _I, _I, _P, _L, _P],
     "idx_topk_to_ragged_slots": [_P, _L, _I, _I, _P, _I, _P, _L, _I, _I, _I, _P, _P, _P, _P],
@@ -191,6 +193,43 @@ def prepare_paged_mqa_logits(q, q_scale, weights, kv_pages, block_table, context
     return Prepared(name, args, (q, q_scale, weights, kv_pages, block_table,
                                                    context_lens, row_ks, candidate_blocks,
                                                    logits, ws), 2 if planned else 1)
+
+
+def prepare_paged_mqa_logits_block_max(q, q_scale, weights, kv_pages, block_table,
+                                       context_lens, next_n, page_size, fmt, logits,
+                                       max_model_len, block_max, block_size, row_ks=None,
+                                       ctx_per_row=False, num_ctas=0):
+    """The candidate source: dense paged logits plus block maxima
+    block_max fp32 [B*next_n, >= ceil(max_model_len / block_size)]."""
+    q = _u8(q)
+    rows, H = q.shape[0], q.shape[1]
+    D = q.shape[2] if fmt == FMT_FP8 else 2 * q.shape[2]
+    B = rows // next_n
+    _need(weights, torch.float32, "weights")
+    _need(block_table, torch.int32, "block_table")
+    _need(context_lens, torch.int32, "context_lens")
+    _need(block_max, torch.float32, "block_max")
+    if kv_pages.dtype != torch.uint8 or kv_pages.dim() != 2 or kv_pages.stride(1) != 1:
+        raise ValueError("kv_pages must be uint8 [num_pages, page_stride] with unit byte stride")
+    args = (_ptr(q), _ptr(q_scale), _ptr(weights), _ptr(kv_pages), kv_pages.stride(0),
+            kv_pages.shape[0], _ptr(block_table), block_table.stride(0), _ptr(context_lens),
+            int(ctx_per_row), _ptr(row_ks), B, next_n, H, D, page_size, fmt, _ptr(logits),
+            logits.stride(0), max_model_len, _ptr(block_max), block_max.stride(0), block_size,
+            num_ctas)
+    # the -inf fill of the block maxima, then the logits kernel
+    return Prepared("idx_paged_mqa_logits_block_max", args,
+                    (q, q_scale, weights, kv_pages, block_table, context_lens, row_ks, logits,
+                     block_max), 2)
+
+
+def idx_paged_mqa_logits_block_max(q, q_scale, weights, kv_pages, block_table, context_lens,
+                                   next_n, page_size, fmt, logits, max_model_len, block_max,
+                                   block_size, row_ks=None, ctx_per_row=False, num_ctas=0,
+                                   stream=None):
+    prepare_paged_mqa_logits_block_max(q, q_scale, weights, kv_pages, block_table,
+                                       context_lens, next_n, page_size, fmt, logits,
+                                       max_model_len, block_max, block_size, row_ks,
+                                       ctx_per_row, num_ctas)(stream)
 
 
 def paged_workspace_size(B, next_n, max_model_len, num_cand) -> int:

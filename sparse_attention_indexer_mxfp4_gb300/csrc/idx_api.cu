@@ -100,7 +100,9 @@ constexpr size_t kMaxSmem = 227 * 1024;
 constexpr int kGroupCost128 = 5;
 constexpr int kMaxSmemBytes = 227 * 1024;
 
-template <int FMT, int H, int G, int S, int NA, int TK>
+// BM: whether this instantiation also has the block-maxima variant (dense
+// walks of one- and two-row groups, the candidate source's shapes).
+template <int FMT, int H, int G, int S, int NA, int TK, bool BM>
 cudaError_t launch_logits_t(const LogitsArgs &a0, const CUtensorMap &tmK, const CUtensorMap &tmQ,
                             const CUtensorMap &tmS, int nctas, cudaStream_t stream)
 {
@@ -109,20 +111,28 @@ cudaError_t launch_logits_t(const LogitsArgs &a0, const CUtensorMap &tmK, const 
     a.tile_shift = TK == 256 ? 8 : 7;
     a.group_cost = a.paged && TK == 128 ? kGroupCost128 : 0;
     const size_t smem = (size_t)C::fixed_bytes() + (size_t)2 * G * a.cand_words * 4;
-    const int plan = a.plan ? 1 : 0;
-    auto kern = plan ? logits_kernel<FMT, H, G, S, NA, TK, true>
-                     : logits_kernel<FMT, H, G, S, NA, TK, false>;
+    // variant: 0 dense, 1 gather plan, 2 dense with block maxima
+    const int variant = a.plan ? 1 : a.bmax ? 2 : 0;
+    decltype(&logits_kernel<FMT, H, G, S, NA, TK, false>) kern = nullptr;
+    if (variant == 1)
+        kern = logits_kernel<FMT, H, G, S, NA, TK, true>;
+    else if (variant == 0)
+        kern = logits_kernel<FMT, H, G, S, NA, TK, false>;
+    else if constexpr (BM)
+        kern = logits_kernel<FMT, H, G, S, NA, TK, false, true>;
+    if (!kern)
+        return cudaErrorNotSupported;
     // raise each kernel's dynamic shared memory limit once per device
-    static int configured[2][kMaxDevices] = {};
+    static int configured[3][kMaxDevices] = {};
     const int dev = current_device();
     if (dev < 0 || dev >= kMaxDevices)
         return cudaErrorInvalidDevice;
-    if (!configured[plan][dev]) {
+    if (!configured[variant][dev]) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)kMaxSmemBytes);
         if (e != cudaSuccess)
             return e;
-        configured[plan][dev] = 1;
+        configured[variant][dev] = 1;
     }
     return launch_pdl(kern, dim3(nctas), dim3(C::THREADS), smem, stream, a, tmK, tmQ, tmS);
 }
@@ -143,19 +153,22 @@ cudaError_t launch_logits(int fmt, int H, int G, const LogitsArgs &a, const CUte
     *supported = true;
     if (H == 64 && fmt == kFmtFp8) {
         switch (G) {
-        case 1: return launch_logits_t<kFmtFp8, 64, 1, 4, 2, 256>(a, tmK, tmQ, tmS, nctas, s);
+        case 1: return launch_logits_t<kFmtFp8, 64, 1, 4, 2, 256, true>(a, tmK, tmQ, tmS, nctas, s);
         case 2:
             // under a gather plan, 128-key tiles: candidate blocks of 128 keys
             // then fill whole tiles and stages
             if (a.plan)
-                return launch_logits_t<kFmtFp8, 64, 2, 6, 3, 128>(a, tmK, tmQ, tmS, nctas, s);
-            return launch_logits_t<kFmtFp8, 64, 2, 4, 2, 256>(a, tmK, tmQ, tmS, nctas, s);
-        case 4: return launch_logits_t<kFmtFp8, 64, 4, 8, 2, 128>(a, tmK, tmQ, tmS, nctas, s);
+                return launch_logits_t<kFmtFp8, 64, 2, 6, 3, 128, false>(a, tmK, tmQ, tmS, nctas, s);
+            return launch_logits_t<kFmtFp8, 64, 2, 4, 2, 256, true>(a, tmK, tmQ, tmS, nctas, s);
+        case 4:
+            if (a.bmax)
+                break;  // no block-maxima variant for four-row groups
+            return launch_logits_t<kFmtFp8, 64, 4, 8, 2, 128, false>(a, tmK, tmQ, tmS, nctas, s);
         }
     } else if (H == 64 && fmt == kFmtMxfp4) {
         switch (G) {
-        case 1: return launch_logits_t<kFmtMxfp4, 64, 1, 8, 2, 256>(a, tmK, tmQ, tmS, nctas, s);
-        case 2: return launch_logits_t<kFmtMxfp4, 64, 2, 12, 3, 128>(a, tmK, tmQ, tmS, nctas, s);
+        case 1: return launch_logits_t<kFmtMxfp4, 64, 1, 8, 2, 256, true>(a, tmK, tmQ, tmS, nctas, s);
+        case 2: return launch_logits_t<kFmtMxfp4, 64, 2, 12, 3, 128, true>(a, tmK, tmQ, tmS, nctas, s);
         }
     }
     *supported = false;
@@ -312,13 +325,32 @@ extern "C" idx_status idx_mqa_logits(const void *q, const void *q_scale, const f
     return launch_status(e);
 }
 
+// -inf over rows x [0, nb) of the block maxima, before the logits kernel
+// raises them.
+__global__ void __launch_bounds__(256) bmax_fill_kernel(float *bmax, int64_t ld, int rows, int nb)
+{
+    pdl_wait();
+    pdl_launch_dependents();
+    const long long n = (long long)rows * nb;
+    for (long long i = blockIdx.x * 256ll + threadIdx.x; i < n; i += (long long)gridDim.x * 256)
+        bmax[(i / nb) * ld + i % nb] = -INFINITY;
+}
+
+// Block maxima requested with the logits (nullable).
+struct BlockMaxOut {
+    float *out = nullptr;
+    int64_t ld = 0;
+    int block = 0;
+};
+
 static idx_status paged_logits(bool cand_only,
     const void *q, const void *q_scale, const float *weights, const uint8_t *kv_pages,
     int64_t page_stride_bytes, int num_pages, const int32_t *block_table, int64_t bt_stride,
     const int32_t *context_lens, int ctx_per_row, const int32_t *row_ks, int B, int next_n,
     int H, int D, int page_size, idx_kv_format fmt, const int32_t *candidate_blocks,
     int64_t cand_stride, int num_cand, int cand_block, float *logits, int64_t ld_logits,
-    int max_model_len, int num_ctas, void *ws, size_t ws_bytes, idx_stream_t stream)
+    int max_model_len, int num_ctas, void *ws, size_t ws_bytes, idx_stream_t stream,
+    BlockMaxOut bm = BlockMaxOut())
 {
     if (B < 0 || next_n <= 0 || H <= 0 || D <= 0 || page_size <= 0 || num_pages < 0 ||
         max_model_len < 0 || num_ctas < 0 || !valid_fmt(fmt))
@@ -334,6 +366,17 @@ static idx_status paged_logits(bool cand_only,
         return IDX_ERR_INVALID_ARG;
     if (candidate_blocks && (num_cand < 0 || cand_block <= 0 || cand_stride < num_cand))
         return IDX_ERR_INVALID_ARG;
+    int bm_blocks = 0;
+    if (bm.out) {
+        if (bm.block <= 0)
+            return IDX_ERR_INVALID_ARG;
+        bm_blocks = (int)(((long long)max_model_len + bm.block - 1) / bm.block);
+        if (bm.ld < bm_blocks)
+            return IDX_ERR_INVALID_ARG;
+        if (bm.block < 32 || next_n > 2)
+            return IDX_ERR_UNSUPPORTED;  // a warp's 32 keys span at most two blocks;
+                                         // one- and two-row groups only
+    }
     const int64_t page_bytes =
         (int64_t)page_size * (f == kFmtFp8 ? (D + 4) : (D / 2 + D / 32));
     if (page_stride_bytes < page_bytes)
@@ -427,6 +470,16 @@ static idx_status paged_logits(bool cand_only,
     const bool planned = plan_need > 0 && ws && ws_bytes >= plan_need && aligned16(ws);
     if (cand_only && !planned)
         return plan_need == 0 ? IDX_ERR_INVALID_ARG : IDX_ERR_WORKSPACE;
+    if (bm.out) {
+        a.bmax = bm.out;
+        a.ld_bmax = bm.ld;
+        a.bmax_block = bm.block;
+        const long long n = (long long)B * next_n * bm_blocks;
+        const int grid = (int)std::min<long long>((n + 255) / 256, (long long)sm_count() * 8);
+        if (launch_pdl(bmax_fill_kernel, dim3(grid), dim3(256), 0, (cudaStream_t)stream,
+                       bm.out, bm.ld, B * next_n, bm_blocks) != cudaSuccess)
+            return IDX_ERR_CUDA;
+    }
     if (planned) {
         int tile_words = 0;
         a.plan = static_cast<uint32_t *>(ws);
@@ -472,6 +525,25 @@ extern "C" idx_status idx_paged_mqa_logits_candidates(
                         block_table, bt_stride, context_lens, ctx_per_row, row_ks, B, next_n, H, D,
                         page_size, fmt, candidate_blocks, cand_stride, num_cand, cand_block, logits,
                         ld_logits, max_model_len, num_ctas, ws, ws_bytes, stream);
+}
+
+extern "C" idx_status idx_paged_mqa_logits_block_max(
+    const void *q, const void *q_scale, const float *weights, const uint8_t *kv_pages,
+    int64_t page_stride_bytes, int num_pages, const int32_t *block_table, int64_t bt_stride,
+    const int32_t *context_lens, int ctx_per_row, const int32_t *row_ks, int B, int next_n, int H,
+    int D, int page_size, idx_kv_format fmt, float *logits, int64_t ld_logits, int max_model_len,
+    float *block_max, int64_t ld_block_max, int block_size, int num_ctas, idx_stream_t stream)
+{
+    if (!block_max)
+        return IDX_ERR_INVALID_ARG;
+    BlockMaxOut bm;
+    bm.out = block_max;
+    bm.ld = ld_block_max;
+    bm.block = block_size;
+    return paged_logits(false, q, q_scale, weights, kv_pages, page_stride_bytes, num_pages,
+                        block_table, bt_stride, context_lens, ctx_per_row, row_ks, B, next_n, H, D,
+                        page_size, fmt, nullptr, 0, 0, 0, logits, ld_logits, max_model_len,
+                        num_ctas, nullptr, 0, stream, bm);
 }
 
 extern "C" size_t idx_paged_mqa_logits_workspace_size(int B, int next_n, int max_model_len,

@@ -106,6 +106,19 @@ IDX_DEVFN bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
     return mbar_wait_slow(bar, parity, abort, status, limit_ns);
 }
 
+// Float max into memory holding a float (prefilled, e.g. with -inf): values
+// with the sign bit clear order like their bits as signed integers and win by
+// atomicMax; values with it set order inversely to their bits as unsigned
+// integers and win by atomicMin, which never replaces a value whose sign bit
+// is clear (those are smaller as unsigned integers).
+IDX_DEVFN void atomic_max_float(float *addr, float v)
+{
+    if (__float_as_int(v) >= 0)
+        atomicMax(reinterpret_cast<int *>(addr), __float_as_int(v));
+    else
+        atomicMin(reinterpret_cast<unsigned int *>(addr), __float_as_uint(v));
+}
+
 // -------------------------------------------------------------------- TMA
 
 IDX_DEVFN void tma_prefetch_desc(const void *desc)

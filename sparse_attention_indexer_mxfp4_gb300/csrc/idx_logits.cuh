@@ -67,6 +67,12 @@ struct LogitsArgs {
     unsigned int *status;    // device status word (IDX_DEV_* bits)
     int tile_shift;          // log2 of the keys per tile (7 or 8)
     int group_cost;          // paged: units a CTA is charged for starting a row group
+    // Block maxima of the candidate source (nullable): bmax[r, j] = max of the
+    // row's logits over [ks + j * bmax_block, ks + (j + 1) * bmax_block),
+    // prefilled with -inf and raised by atomics (bmax_block >= 32).
+    float *bmax;
+    int64_t ld_bmax;
+    int bmax_block;
     // Candidate gather plan (nullable), written by cand_plan_kernel: per row
     // group plan_words words: [0] the number n of compute tiles (tiles that
     // hold a candidate key of any of the group's rows), then box_words words

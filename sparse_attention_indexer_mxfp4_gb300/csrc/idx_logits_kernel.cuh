@@ -171,7 +171,7 @@ __device__ __forceinline__ HalfInfo half_info(const LogitsArgs &a, const UnitWal
 
 namespace idx {
 
-template <int FMT, int H, int G, int S, int NA, int TK, bool PLAN>
+template <int FMT, int H, int G, int S, int NA, int TK, bool PLAN, bool BMAX = false>
 __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
     logits_kernel(const __grid_constant__ LogitsArgs a, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmS)
@@ -672,6 +672,36 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
                         const int t = t0 + sub * kMmaM;
                         if (t < end)
                             orow[t] = val[sub][i];
+                    }
+                }
+                if (BMAX && compute) {
+                    // block maxima: a warp's 32 consecutive keys span at most
+                    // two blocks (block >= 32 keys); each part's maximum goes
+                    // to memory with one atomic
+                    #pragma unroll
+                    for (int i = 0; i < G; ++i) {
+                        if (i >= w.gi.nrows)
+                            break;
+                        float *brow = a.bmax + (size_t)(w.gi.row0 + i) * a.ld_bmax;
+                        #pragma unroll
+                        for (int sub = 0; sub < NSUB; ++sub) {
+                            const int t = t0 + sub * kMmaM;
+                            const int b = t >= rks[i] ? (t - rks[i]) / a.bmax_block : -1;
+                            const int b0 = __shfl_sync(0xffffffffu, b, 0);
+                            const bool first = b == b0;
+                            float m0 = first ? val[sub][i] : -INFINITY;
+                            float m1 = first ? -INFINITY : val[sub][i];
+                            #pragma unroll
+                            for (int o = 16; o > 0; o >>= 1) {
+                                m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+                                m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+                            }
+                            const uint32_t second = __ballot_sync(0xffffffffu, !first);
+                            if (lane == 0 && b0 >= 0 && m0 > -INFINITY)
+                                atomic_max_float(brow + b0, m0);
+                            if (second && lane == __ffs(second) - 1 && b >= 0 && m1 > -INFINITY)
+                                atomic_max_float(brow + b, m1);
+                        }
                     }
                 }
             }

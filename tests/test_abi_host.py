@@ -80,6 +80,27 @@ def test_paged_argument_checks():
     assert call(B=0) == 0
 
 
+def test_block_max_argument_checks():
+    f = B.lib().idx_paged_mqa_logits_block_max
+    # q, q_scale, w, pages, stride, npages, bt, bt_stride, ctx, ctx_per_row, row_ks, B,
+    # next_n, H, D, P, fmt, logits, ld, mml, block_max, ld_bmax, block, num_ctas, stream
+    base = [FAKE, None, FAKE, FAKE, 8448, 10, FAKE, 1024, FAKE, 0, None, 2, 1, 64, 128, 64, 0,
+            FAKE, 65536, 65536, FAKE, 512, 128, 0, None]
+
+    def call(**kw):
+        a = list(base)
+        idx = dict(B=11, next_n=12, bmax=20, ld_bmax=21, block=22)
+        for k, v in kw.items():
+            a[idx[k]] = v
+        return f(*a)
+    assert call(bmax=None) == INVALID
+    assert call(block=0) == INVALID
+    assert call(ld_bmax=511) == INVALID          # fewer columns than 65536 / 128
+    assert call(block=16, ld_bmax=4096) == UNSUPPORTED
+    assert call(next_n=4) == UNSUPPORTED
+    assert call(B=0) == 0
+
+
 def test_select_argument_checks():
     L = B.lib()
     assert L.idx_topk(FAKE, 100, 2, FAKE, 10, FAKE, 5, None, 0, None) == INVALID  # ld_out < k
