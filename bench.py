@@ -10,7 +10,7 @@ Metric: indexer keys scored per second (sum over rows of ke - ks, per step
 time), whole job over all ranks.  Every rank runs its own independent batch
 (weak scaling; the path has no exchange step).
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..5]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..6]
                   [--impl ours|reference]
 """
 from __future__ import annotations
@@ -39,6 +39,9 @@ WORKLOAD_NAMES = {
     4: "paged FP8 MTP decode, B=128 next_n=2 lognormal ctx (median 16384), 64 candidate blocks "
        "of 128 per row, top-2048 + ragged slots",
     5: "paged MXFP4 decode, B=32 ctx 131072, page 64, top-2048 + slots",
+    6: "candidate source at the config-4 shapes: paged FP8 MTP decode, B=128 next_n=2, every "
+       "live key scored with block maxima of 128 keys, top-2048 + ragged slots, the 64 best "
+       "blocks per row as the candidate pool",
 }
 
 
@@ -232,6 +235,9 @@ def logits_bytes(case, cand_only: bool = True) -> float:
             b += float(candidate_tile_logits(case)) * 4  # only candidate tiles are written
         else:
             b += float(ke.sum()) * 4
+        if getattr(case, "source_block", 0):
+            # block maxima: the -inf fill and the atomic raises, one word each
+            b += 2.0 * case.rows * -(-case.width // case.source_block) * 4
         b += float(np.ceil(seq_keys / case.page_size).sum()) * 4
         if case.cand is not None:
             b += case.cand.size * 4
@@ -311,7 +317,8 @@ def run_ours(args):
                 "peak_source": f"{src} hbm_gbs",
                 "kernel": ("logits stage: cand_plan_kernel (candidate plan, -inf fill) + "
                            "logits_kernel" if getattr(case, "cand", None) is not None
-                           else "logits_kernel"),
+                           else "logits stage: bmax_fill_kernel + logits_kernel with block "
+                           "maxima" if getattr(case, "source_block", 0) else "logits_kernel"),
                 "algorithmic_bytes_per_launch": lb, "avg_launch_ms": round(logit_avg, 5)}
     out = {
         "metric": METRIC, "value": round(job_value(world, keys, ms_per_step), 4),
@@ -538,6 +545,10 @@ def _oracle_sample(case, nseq):
         idx = oracle.topk(out, ke, case.topk)
         oracle.topk_to_ragged_slots(idx, case.block_table[:nseq], case.page_size,
                                     case.num_pages, next_n=case.next_n)
+        if getattr(case, "source_block", 0):
+            bs = case.source_block
+            bm = oracle.block_max(out, None, ke, bs)
+            oracle.topk(bm, ((ke + bs - 1) // bs).astype(np.int32), case.source_cands)
         return int(ke.sum())
     rows = np.arange(nseq)
     out = oracle.mqa_logits(case.fmt, case.q[rows], None, case.weights[rows], case.k,
@@ -606,7 +617,7 @@ def main():
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=20)
     p.add_argument("--warmup", type=int, default=5)
-    p.add_argument("--config", type=int, default=4, choices=[1, 2, 3, 4, 5])
+    p.add_argument("--config", type=int, default=4, choices=[1, 2, 3, 4, 5, 6])
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     args = p.parse_args()

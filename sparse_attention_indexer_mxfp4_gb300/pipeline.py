@@ -68,6 +68,16 @@ class IndexerStep:
             self.slots = torch.empty(max(1, self.rows * self.k_top), dtype=torch.int32, device=d)
             self.indptr = torch.empty(self.rows + 1, dtype=torch.int32, device=d)
             self.lens = torch.empty(self.rows, dtype=torch.int32, device=d)
+        self.source = self.paged and getattr(case, "source_block", 0) > 0
+        if self.source:
+            # candidate source: block maxima, and the best blocks of each row
+            bs = case.source_block
+            self.nblocks = -(-case.width // bs)
+            self.block_max = torch.empty((self.rows, self.nblocks), dtype=torch.float32, device=d)
+            ks = np.zeros(self.rows, np.int64) if case.row_ks is None else case.row_ks
+            span = np.maximum(ke - np.minimum(ks, ke), 0)
+            self.block_lens = _dev(((span + bs - 1) // bs).astype(np.int32), d)
+            self.pool = torch.empty((self.rows, case.source_cands), dtype=torch.int32, device=d)
 
         self._prepare()
 
@@ -75,7 +85,16 @@ class IndexerStep:
         """Marshal every call of the step once; run() only launches."""
         c = self.case
         self._logits_calls = []
-        if self.paged:
+        if self.source:
+            self._logits_calls.append(B.prepare_paged_mqa_logits_block_max(
+                self.q, self.q_scale, self.weights, self.pages, self.block_table,
+                self.context_lens, c.next_n, c.page_size, c.fmt, self.logits, c.width,
+                self.block_max, c.source_block, row_ks=self.row_ks, ctx_per_row=c.ctx_per_row,
+                num_ctas=self.num_ctas))
+            self._slots_call = B.prepare_topk_to_ragged_slots(
+                self.topk, self.block_table, c.page_size, c.num_pages, self.slots, self.indptr,
+                self.lens, next_n=c.next_n, max_blocks=self.max_blocks)
+        elif self.paged:
             cand = self.cand if (self.cand is not None and self.fused_mask) else None
             self._logits_calls.append(B.prepare_paged_mqa_logits(
                 self.q, self.q_scale, self.weights, self.pages, self.block_table,
@@ -100,6 +119,9 @@ class IndexerStep:
                 row_ks=self.row_ks)
         else:
             self._topk_call = B.prepare_topk(self.logits, self.lengths, self.k_top, self.topk)
+        # the candidate pool: the best blocks of each row, from the block maxima
+        self._pool_call = (B.prepare_topk(self.block_max, self.block_lens, c.source_cands,
+                                          self.pool) if self.source else None)
 
     # -------------------------------------------------------------- stages
     def logits_stage(self, stream=None):
@@ -108,6 +130,8 @@ class IndexerStep:
 
     def topk_stage(self, stream=None):
         self._topk_call(stream)
+        if self._pool_call is not None:
+            self._pool_call(stream)
 
     def slots_stage(self, stream=None):
         if self._slots_call is not None:
@@ -121,6 +145,8 @@ class IndexerStep:
     @property
     def launches_per_step(self) -> int:
         calls = self._logits_calls + [self._topk_call]
+        if self._pool_call is not None:
+            calls.append(self._pool_call)
         if self._slots_call is not None:
             calls.append(self._slots_call)
         return sum(c.kernels for c in calls)

@@ -127,6 +127,10 @@ class PagedCase:
     cand_block: int = 0
     name: str = ""
     extra: dict = field(default_factory=dict)
+    # candidate source: block maxima of source_block keys and the
+    # source_cands best blocks of each row (0: not a source)
+    source_block: int = 0
+    source_cands: int = 0
 
     @property
     def rows(self) -> int:
@@ -301,4 +305,15 @@ def config5(shard: int = 0) -> PagedCase:
                       pool_pages=65536, topk=2048, name="paged_mxfp4_decode_B32")
 
 
-CONFIGS = {1: config1, 2: config2, 3: config3, 4: config4, 5: config5}
+def config6(shard: int = 0) -> PagedCase:
+    """Candidate source at the config-4 shapes: paged FP8 MTP decode, B=128,
+    next_n=2, lognormal ctx (median 16384), every live key scored, block
+    maxima of 128 keys, the 64 best blocks per row as the candidate pool, the
+    row's top-2048 mapped to ragged slots."""
+    c = paged_case(shard_seed(6, shard), config4_context_lens(), 2, 64, 128, 64, 131072,
+                   pool_factor=1.1, topk=2048, name="paged_fp8_mtp_source_B128")
+    c.source_block, c.source_cands = 128, 64
+    return c
+
+
+CONFIGS = {1: config1, 2: config2, 3: config3, 4: config4, 5: config5, 6: config6}

@@ -1,4 +1,4 @@
-"""The five benchmark workloads at full size, in the launch configuration the
+"""The benchmark workloads at full size, in the launch configuration the
 benchmark times (IndexerStep).  The oracle checks sampled rows one by one;
 top-k is checked end to end with the near-tie rule and bit-exactly on the
 oracle's own logits."""
@@ -40,7 +40,7 @@ def _oracle_paged_rows(sub):
     return out, ke, bad
 
 
-@pytest.fixture(scope="module", params=[3, 4, 5])
+@pytest.fixture(scope="module", params=[3, 4, 5, 6])
 def paged_cfg(request):
     return request.param, synth.CONFIGS[request.param]()
 
@@ -84,6 +84,23 @@ def test_paged_config(paged_cfg, cand_topk):
         if len(np.setxor1d(gpu_idx[i][gpu_idx[i] >= 0], ora_idx[i][ora_idx[i] >= 0])) == 0:
             np.testing.assert_array_equal(g, o)
     assert indptr[0] == 0 and (np.diff(indptr) == st.lens.cpu().numpy()).all()
+    if st.source:
+        # candidate source: block maxima bit-exact on the GPU's own logits and
+        # within tolerance of the oracle's; the pool (best blocks) with the
+        # near-tie rule, and exactly on the GPU's own block maxima
+        bs = c.source_block
+        gb = st.block_max[torch.from_numpy(rows).cuda()].cpu().numpy()
+        bl = ((ke + bs - 1) // bs).astype(np.int32)
+        own = oracle.block_max(np.where(np.isnan(gl), -np.inf, gl), None, ke, bs)
+        np.testing.assert_array_equal(gb, own)
+        ref_bm = oracle.block_max(np.where(np.isnan(ref), -np.inf, ref), None, ke, bs)
+        assert_logits_close(gb, ref_bm, f"config {cfg} block maxima")
+        gpu_pool = st.pool[torch.from_numpy(rows).cuda()].cpu().numpy()
+        ora_pool = oracle.topk(ref_bm, bl, c.source_cands)
+        assert_topk_near_tie(gpu_pool, ora_pool, ref_bm, bl, c.source_cands,
+                             f"config {cfg} candidate pool")
+        assert_topk_exact(gpu_pool, oracle.topk(own, bl, c.source_cands),
+                          f"config {cfg} pool on the GPU block maxima")
 
 
 @pytest.mark.parametrize("cfg", [1, 2])
