@@ -46,14 +46,17 @@ WORKLOAD_NAMES = {
 
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one logits
-# stage (the plan kernel and the logits kernel under a candidate plan) from an
+# stage (the plan kernel and the logits kernel under a candidate plan; the
+# block-maxima fill and the logits kernel for the candidate source) from an
 # ncu capture, per workload, with a digest of the kernels' sources at capture
 # time.  A different digest means the kernel changed
 # since and the traffic is reported as null.
 LOGITS_SOURCES = ["idx_logits_kernel.cuh", "idx_logits.cuh", "idx_common.cuh", "idx_api.cu"]
 NCU_TRAFFIC = {
-    4: {"bytes": 91136 + 189571328 + 8772608, "digest": "1d3a6cfb962b53b2",
+    4: {"bytes": 91136 + 189568000 + 8561408, "digest": "bf7c7ffb2c11e59f",
         "profile": "profiles/logits_kernel_paged_fp8_decode_b128_mtp2.md"},
+    6: {"bytes": 3840 + 413296896 + 21575936, "digest": "bf7c7ffb2c11e59f",
+        "profile": "profiles/logits_kernel_candidate_source_b128_mtp2.md"},
 }
 
 

@@ -326,14 +326,16 @@ extern "C" idx_status idx_mqa_logits(const void *q, const void *q_scale, const f
 }
 
 // -inf over rows x [0, nb) of the block maxima, before the logits kernel
-// raises them.
+// raises them: grid (column blocks of 256, rows), both strided.
 __global__ void __launch_bounds__(256) bmax_fill_kernel(float *bmax, int64_t ld, int rows, int nb)
 {
     pdl_wait();
     pdl_launch_dependents();
-    const long long n = (long long)rows * nb;
-    for (long long i = blockIdx.x * 256ll + threadIdx.x; i < n; i += (long long)gridDim.x * 256)
-        bmax[(i / nb) * ld + i % nb] = -INFINITY;
+    for (int r = blockIdx.y; r < rows; r += gridDim.y) {
+        float *row = bmax + (size_t)r * ld;
+        for (int j = blockIdx.x * 256 + threadIdx.x; j < nb; j += gridDim.x * 256)
+            row[j] = -INFINITY;
+    }
 }
 
 // Block maxima requested with the logits (nullable).
@@ -474,10 +476,9 @@ static idx_status paged_logits(bool cand_only,
         a.bmax = bm.out;
         a.ld_bmax = bm.ld;
         a.bmax_block = bm.block;
-        const long long n = (long long)B * next_n * bm_blocks;
-        const int grid = (int)std::min<long long>((n + 255) / 256, (long long)sm_count() * 8);
-        if (launch_pdl(bmax_fill_kernel, dim3(grid), dim3(256), 0, (cudaStream_t)stream,
-                       bm.out, bm.ld, B * next_n, bm_blocks) != cudaSuccess)
+        const dim3 grid(std::min((bm_blocks + 255) / 256, 64), std::min(B * next_n, 65535));
+        if (launch_pdl(bmax_fill_kernel, grid, dim3(256), 0, (cudaStream_t)stream, bm.out, bm.ld,
+                       B * next_n, bm_blocks) != cudaSuccess)
             return IDX_ERR_CUDA;
     }
     if (planned) {
