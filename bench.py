@@ -10,7 +10,7 @@ Metric: indexer keys scored per second (sum over rows of ke - ks, per step
 time), whole job over all ranks.  Every rank runs its own independent batch
 (weak scaling; the path has no exchange step).
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..6]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..7]
                   [--impl ours|reference]
 """
 from __future__ import annotations
@@ -42,7 +42,40 @@ WORKLOAD_NAMES = {
     6: "candidate source at the config-4 shapes: paged FP8 MTP decode, B=128 next_n=2, every "
        "live key scored with block maxima of 128 keys, top-2048 + ragged slots, the 64 best "
        "blocks per row as the candidate pool",
+    7: "K/Q producers of a prefill chunk: 8192 tokens, H=64 D=128 rope_dim=64, MXFP4 keys "
+       "(RMS norm, RoPE, quantise) stored into 64-token pages, MXFP4 query heads + weights",
 }
+PROD_METRIC = "producer Mtokens/s (K norm+RoPE+quantise+store, Q RoPE+quantise); % of HBM roofline"
+PROD_UNIT = "Mtok/s"
+
+
+def _is_producer(case) -> bool:
+    from sparse_attention_indexer_mxfp4_gb300.synth import ProducerCase
+    return isinstance(case, ProducerCase)
+
+
+def _metric_unit_div(case):
+    """(metric, unit, divisor of work per second) of a workload."""
+    if _is_producer(case):
+        return PROD_METRIC, PROD_UNIT, 1e6
+    return METRIC, UNIT, 1e9
+
+
+def _work(case) -> int:
+    """Units of work of one step: keys scored, or tokens produced."""
+    return case.T if _is_producer(case) else case.keys_scored
+
+
+def producer_bytes(case) -> float:
+    """Algorithmic bytes of one producer step: each key read once (bf16) and
+    written once (codes + scales), its slot, position and rotary row read
+    once; each query head read once (bf16) and written once (codes + scales),
+    its weight read and written once; the norm weight once."""
+    D, H, T = case.D, case.H, case.T
+    out = (D + 4) if case.fmt == 0 else (D // 2 + D // 32)
+    per_token = 2 * D + out + 8 + 4 + case.rope_dim * 4
+    per_head = 2 * D + (D if case.fmt == 0 else D // 2 + 4) + 8
+    return float(T * per_token + T * H * per_head + 4 * D)
 
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one logits
@@ -161,10 +194,10 @@ def max_over_ranks(values, device, world: int):
     return t.tolist()
 
 
-def job_value(world: int, keys_per_rank: int, ms_per_step: float) -> float:
-    """Whole-job keys scored per second (Gkeys/s): every rank scores
-    keys_per_rank keys per step and the step takes the slowest rank's time."""
-    return world * keys_per_rank / (ms_per_step * 1e-3) / 1e9
+def job_value(world: int, keys_per_rank: int, ms_per_step: float, div: float = 1e9) -> float:
+    """Whole-job work per second (Gkeys/s by default): every rank does
+    keys_per_rank units per step and the step takes the slowest rank's time."""
+    return world * keys_per_rank / (ms_per_step * 1e-3) / div
 
 
 def candidate_tile_logits(case, tile=128) -> int:
@@ -258,7 +291,8 @@ def logits_flops(case) -> float:
 def run_ours(args):
     import torch
     import torch.distributed as dist
-    from sparse_attention_indexer_mxfp4_gb300 import IndexerStep, idx_get_device_status
+    from sparse_attention_indexer_mxfp4_gb300 import (IndexerStep, ProducerStep,
+                                                      idx_get_device_status)
     from sparse_attention_indexer_mxfp4_gb300.synth import PagedCase
 
     world, rank, local = _dist()
@@ -267,7 +301,9 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     case = _case(args.config, shard=rank)
-    step = IndexerStep(case, device=dev)
+    prod = _is_producer(case)
+    step = ProducerStep(case, device=dev) if prod else IndexerStep(case, device=dev)
+    metric, unit, div = _metric_unit_div(case)
     stream = torch.cuda.current_stream()
 
     # warm-up (also builds and loads the library)
@@ -280,7 +316,7 @@ def run_ours(args):
     # workloads; for the contiguous ones a 256 MB buffer is rewritten
     # between steps.
     flush = None
-    if not isinstance(case, PagedCase):
+    if not isinstance(case, PagedCase):  # contiguous workloads and the producers
         flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
 
     clocks = Clocks(local)
@@ -301,14 +337,24 @@ def run_ours(args):
     ms_per_step, logit_avg, topk_avg = max_over_ranks(
         [ms_per_step, sum(logit_ms) / len(logit_ms), sum(topk_ms) / len(topk_ms)], dev, world)
 
-    keys = case.keys_scored
-    rows = case.rows if isinstance(case, PagedCase) else case.M
+    keys = _work(case)
+    rows = case.rows if isinstance(case, PagedCase) or prod else case.M
     e2e = run_e2e(step, case, args, dev) if rank == 0 else None
 
     hbm, bf16, src = _peaks()
-    lb = logits_bytes(case, cand_only=getattr(step, "cand_topk", False))
-    achieved_gbs = lb / (logit_avg * 1e-3) / 1e9
-    if args.config == 2:
+    if prod:  # the producers' stage times are the K call and the Q call
+        lb = producer_bytes(case)
+        achieved_gbs = lb / (ms_per_step * 1e-3) / 1e9
+    else:
+        lb = logits_bytes(case, cand_only=getattr(step, "cand_topk", False))
+        achieved_gbs = lb / (logit_avg * 1e-3) / 1e9
+    if prod:
+        roof = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved_gbs / hbm, 4), "traffic": None,
+                "peak_source": f"{src} hbm_gbs",
+                "kernel": "producer step: k_store_kernel + q_quant_kernel",
+                "algorithmic_bytes_per_launch": lb, "avg_launch_ms": round(ms_per_step, 5)}
+    elif args.config == 2:
         fp8_peak = 2.0 * bf16  # dense fp8 rate = 2x bf16 on this part
         ach = logits_flops(case) / (logit_avg * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": fp8_peak,
@@ -324,18 +370,20 @@ def run_ours(args):
                            "maxima" if getattr(case, "source_block", 0) else "logits_kernel"),
                 "algorithmic_bytes_per_launch": lb, "avg_launch_ms": round(logit_avg, 5)}
     out = {
-        "metric": METRIC, "value": round(job_value(world, keys, ms_per_step), 4),
-        "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "metric": metric, "value": round(job_value(world, keys, ms_per_step, div), 4),
+        "unit": unit, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32" if case.fmt == 0 else
-        "e2m1 x e2m1 (e8m0 block scales) -> f32",
+        "vs_baseline": None, "dtype": ("bf16 -> e2m1 (e8m0 block scales)" if prod else
+                                       "e4m3 x e4m3 -> f32" if case.fmt == 0 else
+                                       "e2m1 x e2m1 (e8m0 block scales) -> f32"),
         "data": "synthetic (seeded; shapes and distributions of the workload description)",
         "config": {"workload": WORKLOAD_NAMES[args.config], "config_id": args.config,
                    "rows": rows, "keys_scored_per_step": keys,
                    "l2": "flushed between steps" if flush is not None else
                    "K pages read per step exceed L2", "timing": mode},
-        "topk_rows_per_s": round(world * rows / (topk_avg * 1e-3), 1),
-        "logits_ms": round(logit_avg, 5), "topk_ms": round(topk_avg, 5),
+        "topk_rows_per_s": None if prod else round(world * rows / (topk_avg * 1e-3), 1),
+        "logits_ms" if not prod else "k_store_ms": round(logit_avg, 5),
+        "topk_ms" if not prod else "q_quant_ms": round(topk_avg, 5),
         "roofline": roof, "clocks": clk,
         "gpu_launches": step.launches_per_step * args.steps,
         "e2e": e2e,
@@ -436,10 +484,12 @@ def time_steps_eager(step, K, flush):
 
 def run_e2e(step, case, args, dev):
     """Same metric through the public API with host buffers: each step copies
-    the step's inputs (queries, weights, lengths, block table, candidates)
-    from pinned host memory and reads the top-k indices and ragged slots
-    back.  The K cache itself is resident device state (it is written by the
-    cache producer, not per step).  Steps run as a serving loop runs them:
+    the step's inputs (step.input_names(): queries, weights, lengths, block
+    table, candidates; for the producers the new keys, queries, weights,
+    positions and slots) from pinned host memory and reads its results back
+    (step.results(): top-k indices and ragged slots; the quantised queries,
+    their scales and weights).  The K cache and the model constants are
+    resident device state, not per-step inputs.  Steps run as a serving loop runs them:
     two sets of device buffers (sharing the K cache); step i's inputs are
     copied in on one stream while step i-1 computes (its calls replayed from a
     CUDA graph) on a second and step i-2's results are copied out on a
@@ -447,23 +497,10 @@ def run_e2e(step, case, args, dev):
     next copy-in.  The timed region spans the first copy-in to the last
     copy-out."""
     import torch
-    from sparse_attention_indexer_mxfp4_gb300 import IndexerStep
-    from sparse_attention_indexer_mxfp4_gb300.synth import PagedCase
 
-    sets = [step, IndexerStep(case, device=dev, fused_mask=step.fused_mask,
-                              num_ctas=step.num_ctas, gather=step.gather,
-                              cand_topk=step.cand_topk, kv_from=step)]
-    names = ["q", "weights", "lengths"]
-    if isinstance(case, PagedCase):
-        names += ["block_table", "context_lens"] + (["cand"] if case.cand is not None else [])
-    else:
-        names += ["ks", "ke"]
-    host = {n: getattr(step, n).cpu().pin_memory() for n in names}
-
-    def outs_of(st):
-        return [st.topk] + ([st.slots, st.indptr] if isinstance(case, PagedCase) else [])
-
-    outs = [outs_of(st) for st in sets]
+    sets = [step, step.twin()]
+    host = {n: getattr(step, n).cpu().pin_memory() for n in step.input_names()}
+    outs = [st.results() for st in sets]
     host_out = [[o.cpu().pin_memory() for o in os_] for os_ in outs]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = sum(t.numel() * t.element_size() for t in host_out[0])
@@ -520,7 +557,8 @@ def run_e2e(step, case, args, dev):
     ms = a.elapsed_time(b) / steps
     for h0, h1 in zip(host_out[0], host_out[1]):  # both sets computed the same step
         assert torch.equal(h0, h1), "the two buffer sets returned different results"
-    return {"value": round(case.keys_scored / (ms * 1e-3) / 1e9, 4), "unit": UNIT,
+    _, unit, div = _metric_unit_div(case)
+    return {"value": round(_work(case) / (ms * 1e-3) / div, 4), "unit": unit,
             "ms_per_step": round(ms, 5), "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h),
             "pipeline": "two buffer sets; copy-in, compute (CUDA graph) and copy-out on "
@@ -529,9 +567,24 @@ def run_e2e(step, case, args, dev):
 
 def _oracle_sample(case, nseq):
     """The oracle's step (logits, mask, top-k, slots) over the first nseq
-    sequences (paged) or rows (contiguous) of the workload; returns keys."""
+    sequences (paged) or rows (contiguous) of the workload, or its producers
+    over the first nseq tokens; returns the units of work (keys, tokens)."""
     import oracle
     from sparse_attention_indexer_mxfp4_gb300.synth import PagedCase
+    if _is_producer(case):
+        import torch
+        n = nseq
+
+        def bits(x):
+            return torch.from_numpy(np.ascontiguousarray(x)).to(torch.bfloat16).view(
+                torch.int16).numpy().view(np.uint16)
+        pages = np.zeros((case.num_pages, case.page_stride), np.uint8)
+        oracle.k_norm_rope_store(case.fmt, bits(case.k_pre[:n]), case.positions[:n], case.cos_sin,
+                                 case.rope_dim, case.norm_weight, case.eps, pages,
+                                 case.page_size, case.slots[:n])
+        oracle.q_rope_quant(case.fmt, bits(case.q[:n]), case.positions[:n], case.cos_sin,
+                            case.rope_dim, case.weights[:n], case.weight_scale)
+        return n
     if isinstance(case, PagedCase):
         rows = np.arange(nseq * case.next_n)
         ctx = case.context_lens[rows] if case.ctx_per_row else case.context_lens[:nseq]
@@ -563,6 +616,8 @@ def _oracle_sample(case, nseq):
 
 def _units(case):
     from sparse_attention_indexer_mxfp4_gb300.synth import PagedCase
+    if _is_producer(case):
+        return case.T
     return case.B if isinstance(case, PagedCase) else case.M
 
 
@@ -579,10 +634,15 @@ def cpu_baseline(case, args, target_s: float = 10.0):
         if dt >= target_s or n >= total:
             break
         n = min(total, max(n + 1, int(n * min(8.0, target_s / max(dt, 1e-3)))))
-    return {"value": round(keys / dt / 1e9, 6), "unit": UNIT, "cores": oracle.default_threads(),
-            "kind": "oracle",
-            "sample": f"first {n} of {total} {'sequences' if hasattr(case, 'B') else 'rows'} "
-                      f"({keys} keys): fp64 scalar logits + mask + top-k + slots, {dt:.1f} s"}
+    _, unit, div = _metric_unit_div(case)
+    if _is_producer(case):
+        what = (f"first {n} of {total} tokens: fp64 scalar norm + RoPE + quantise of the key "
+                f"and of the {case.H} query heads, {dt:.1f} s")
+    else:
+        what = (f"first {n} of {total} {'sequences' if hasattr(case, 'B') else 'rows'} "
+                f"({keys} keys): fp64 scalar logits + mask + top-k + slots, {dt:.1f} s")
+    return {"value": round(keys / dt / div, 6), "unit": unit, "cores": oracle.default_threads(),
+            "kind": "oracle", "sample": what}
 
 
 def run_reference(args):
@@ -599,19 +659,20 @@ def run_reference(args):
     for _ in range(args.steps):
         keys += _oracle_sample(case, nseq)
     dt = time.time() - t
-    v = keys / dt / 1e9
+    metric, unit, div = _metric_unit_div(case)
+    v = keys / dt / div
     total = _units(case)
     print(json.dumps({
-        "impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": UNIT,
+        "impl": "reference", "metric": metric, "value": round(v, 6), "unit": unit,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64 (scalar CPU oracle)",
         "data": "synthetic", "config": {"workload": WORKLOAD_NAMES[args.config],
                                         "config_id": args.config},
-        "cpu_baseline": {"value": round(v, 6), "unit": UNIT, "cores": oracle.default_threads(),
+        "cpu_baseline": {"value": round(v, 6), "unit": unit, "cores": oracle.default_threads(),
                          "kind": "oracle",
                          "sample": f"each step: the first 1 of {total} units of the workload"},
-        "e2e": {"value": round(v, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+        "e2e": {"value": round(v, 6), "unit": unit, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0}}))
 
 
@@ -620,7 +681,7 @@ def main():
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=20)
     p.add_argument("--warmup", type=int, default=5)
-    p.add_argument("--config", type=int, default=4, choices=[1, 2, 3, 4, 5, 6])
+    p.add_argument("--config", type=int, default=4, choices=[1, 2, 3, 4, 5, 6, 7])
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     args = p.parse_args()

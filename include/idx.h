@@ -61,6 +61,7 @@ typedef enum {
 #define IDX_DEV_BAD_PAGE 1u      /* block-table entry outside [0, num_pages) */
 #define IDX_DEV_BAD_CANDIDATE 2u /* reserved: candidate ids are range-checked and ignored */
 #define IDX_DEV_TIMEOUT 4u       /* a bounded pipeline wait ran out; outputs undefined */
+#define IDX_DEV_BAD_POSITION 8u  /* a producer's position outside its cos/sin table */
 
 /* ------------------------------------------------------------------------
  * idx_mqa_logits -- non-paged logits for one key sequence.
@@ -325,6 +326,71 @@ idx_status idx_topk_to_ragged_slots(const int32_t *topk, int64_t ld, int rows, i
                                     int max_blocks, int page_size, int num_pages,
                                     int32_t *slots, int32_t *indptr, int32_t *lens,
                                     idx_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * idx_k_norm_rope_store -- the K producer: normalise, rotate, quantise and
+ * write each new key into its cache slot.
+ * Passage: vllm/models/deepseek_v41/amd/rocm.py, rocm_mxfp4_indexer_k_store
+ * (RMS norm with weight and eps, RoPE at the token's position, quantised
+ * store into kv_slot_mapping[t]); RoPE as the forward of
+ * rocm_aiter_mla_sparse _inverse_rope_gptj_kernel (GPT-J pairs on the
+ * trailing rope_dim, cos/sin row = cos | sin); quantiser as
+ * rocm_aiter_mla_sparse _mxfp8_scale_bits (E8M0 exponent putting the block's
+ * amax at 448 for e4m3 / 6 for e2m1; values times 2^(127 - bits) rounded to
+ * the nearest code, ties to even).
+ *
+ *   k_pre       bf16 bits [T, ld_k], ld_k >= D (multiple of 4), 8-byte
+ *               aligned: the keys before the norm.
+ *   positions   [T] int32, each in [0, num_positions).
+ *   cos_sin     fp32 [num_positions, ld_cos_sin]: row p = cos(p * f_i) for
+ *               i < rope_dim / 2, then sin(p * f_i); nullable when rope_dim = 0.
+ *   rope_dim    even, 0 <= rope_dim <= D: the trailing rope_dim elements of
+ *               the key are rotated in pairs (2i, 2i + 1).
+ *   norm_weight fp32 [D] (16-byte aligned); eps >= 0:
+ *               y = x / sqrt(mean(x^2) + eps) * norm_weight.
+ *   kv_pages, page_stride_bytes, num_pages, page_size  the cache of
+ *               idx_paged_mqa_logits (same block-flat layout).  FP8: codes
+ *               of y * 2^(127 - bits) with one exponent per token, its scale
+ *               2^(bits - 127) stored as the token's fp32 scale; MXFP4: one
+ *               e8m0 exponent per 32 elements.
+ *   slot_mapping [T] int64: cache slot page * page_size + offset; -1 skips
+ *               the token.
+ * Supported: D = 128.  A slot outside the pool sets IDX_DEV_BAD_PAGE, a
+ * position outside the table IDX_DEV_BAD_POSITION; those tokens are skipped.
+ * ---------------------------------------------------------------------- */
+idx_status idx_k_norm_rope_store(const uint16_t *k_pre, int64_t ld_k, const int32_t *positions,
+                                 const float *cos_sin, int64_t ld_cos_sin, int num_positions,
+                                 int rope_dim, const float *norm_weight, float eps, int T, int D,
+                                 idx_kv_format fmt, uint8_t *kv_pages, int64_t page_stride_bytes,
+                                 int num_pages, int page_size, const int64_t *slot_mapping,
+                                 idx_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * idx_q_rope_quant -- the Q producer: rotate and quantise the query heads
+ * and scale their weights, in the formats idx_paged_mqa_logits reads.
+ * Passage: vllm/models/deepseek_v41/amd/rocm.py, rocm_mxfp4_indexer_q_quant
+ * (packed [T, H, D/2] + one int32 of four e8m0 bytes per head, fp32 weights
+ * times index_weights_softmax_scale * index_weights_head_scale); RoPE and
+ * quantiser as idx_k_norm_rope_store.
+ *
+ *   q           bf16 bits [T, H, D] contiguous, 8-byte aligned.
+ *   positions, cos_sin, ld_cos_sin, num_positions, rope_dim  as above.
+ *   weights     fp32 [T, H]; weight_scale the product of the softmax and
+ *               head scales.
+ *   q_out       FP8: e4m3 [T, H, D]; MXFP4: packed e2m1 [T, H, D/2].
+ *   q_scale_out MXFP4: [T, H] int32 (byte j = e8m0 exponent of elements
+ *               [32 j, 32 j + 32)); unused (nullable) for FP8.
+ *   weights_out fp32 [T, H]: weights * weight_scale, and for FP8 also times
+ *               the head's power-of-two scale 2^(bits - 127) (relu(s x) =
+ *               s relu(x) for s > 0, so the logits need no q_scale).
+ * Supported: D = 128.  Tokens with a position outside the table set
+ * IDX_DEV_BAD_POSITION and are left unwritten.
+ * ---------------------------------------------------------------------- */
+idx_status idx_q_rope_quant(const uint16_t *q, const int32_t *positions, const float *cos_sin,
+                            int64_t ld_cos_sin, int num_positions, int rope_dim,
+                            const float *weights, float weight_scale, int T, int H, int D,
+                            idx_kv_format fmt, uint8_t *q_out, void *q_scale_out,
+                            float *weights_out, idx_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * idx_get_device_status -- read and clear the sticky device status word of

@@ -73,6 +73,19 @@ def _declare(L):
     L.orc_apply_candidate_mask.restype = _I
     L.orc_block_max.argtypes = [_P, _L, _I, _I, _P, _P, _I, _P, _L, _I, _I]
     L.orc_block_max.restype = _I
+    _D = ctypes.c_double
+    L.orc_e4m3_encode.argtypes = [_D]
+    L.orc_e4m3_encode.restype = ctypes.c_uint8
+    L.orc_e2m1_encode.argtypes = [_D]
+    L.orc_e2m1_encode.restype = ctypes.c_uint8
+    L.orc_scale_bits.argtypes = [_D, _D]
+    L.orc_scale_bits.restype = _I
+    L.orc_k_norm_rope_store.argtypes = [_P, _L, _P, _P, _L, _I, _I, _P, _D, _P, _L, _I, _I, _P,
+                                        _I, _I, _I, _P, _P]
+    L.orc_k_norm_rope_store.restype = _I
+    L.orc_q_rope_quant.argtypes = [_P, _P, _P, _L, _I, _I, _P, _D, _I, _I, _I, _I, _P, _P, _P,
+                                   _P, _P]
+    L.orc_q_rope_quant.restype = _I
     L.orc_topk.argtypes = [_P, _L, _I, _I, _P, _I, _P, _L, _I]
     L.orc_topk.restype = _I
     L.orc_topk_to_ragged_slots.argtypes = [_P, _L, _I, _I, _P, _I, _P, _L, _I, _I, _I,
@@ -183,6 +196,61 @@ def block_max(logits, row_ks, row_ke, block_size, nthreads=0) -> np.ndarray:
     if rc != 0:
         raise ValueError("oracle block_max rejected its arguments")
     return out[:, :nb]
+
+
+def e4m3_encode(y: float) -> int:
+    """Nearest e4m3 code (ties to the even code) of |y| <= 448."""
+    return int(lib().orc_e4m3_encode(float(y)))
+
+
+def e2m1_encode(y: float) -> int:
+    """Nearest e2m1 code (ties to the even code) of |y| <= 6."""
+    return int(lib().orc_e2m1_encode(float(y)))
+
+
+def scale_bits(amax: float, top: float) -> int:
+    """Biased E8M0 exponent putting amax at the top of the element range."""
+    return int(lib().orc_scale_bits(float(amax), float(top)))
+
+
+def k_norm_rope_store(fmt, k_pre_bits, positions, cos_sin, rope_dim, norm_w, eps, pages,
+                      page_size, slots):
+    """K producer into ``pages`` (uint8 [num_pages, stride], in place).
+    k_pre_bits: uint16 bf16 bits [T, D].  Returns (bad, pre [T, D] float64,
+    bits [T, D/32] int32)."""
+    k = _c(k_pre_bits, np.uint16)
+    T, D = k.shape
+    pos, cs = _c(positions, np.int32), _c(cos_sin, np.float32)
+    w, sl = _c(norm_w, np.float32), _c(slots, np.int64)
+    assert pages.dtype == np.uint8 and pages.flags["C_CONTIGUOUS"]
+    pre = np.zeros((T, D), np.float64)
+    bits = np.zeros((T, max(D // 32, 1)), np.int32)
+    ldcs, ncs = (0, 2 ** 31 - 1) if cs is None else (cs.shape[1], cs.shape[0])
+    bad = lib().orc_k_norm_rope_store(_ptr(k), D, _ptr(pos), _ptr(cs), ldcs, ncs,
+                                      rope_dim, _ptr(w), float(eps), _ptr(pages), pages.shape[1],
+                                      pages.shape[0], page_size, _ptr(sl), T, D, fmt, _ptr(pre),
+                                      _ptr(bits))
+    return bad, pre, bits
+
+
+def q_rope_quant(fmt, q_bits, positions, cos_sin, rope_dim, w_in, w_scale):
+    """Q producer.  q_bits: uint16 bf16 bits [T, H, D].  Returns (bad, q_out
+    uint8 [T, H, D or D/2], q_sf uint8 [T, H, D/32] (MXFP4), w_out float32
+    [T, H], pre [T*H, D] float64, bits [T*H, D/32] int32)."""
+    q = _c(q_bits, np.uint16)
+    T, H, D = q.shape
+    pos, cs, w = _c(positions, np.int32), _c(cos_sin, np.float32), _c(w_in, np.float32)
+    rowb = D if fmt == 0 else D // 2
+    q_out = np.zeros((T, H, rowb), np.uint8)
+    q_sf = np.zeros((T, H, max(D // 32, 1)), np.uint8)
+    w_out = np.zeros((T, H), np.float32)
+    pre = np.zeros((T * H, D), np.float64)
+    bits = np.zeros((T * H, max(D // 32, 1)), np.int32)
+    ldcs, ncs = (0, 2 ** 31 - 1) if cs is None else (cs.shape[1], cs.shape[0])
+    bad = lib().orc_q_rope_quant(_ptr(q), _ptr(pos), _ptr(cs), ldcs, ncs,
+                                 rope_dim, _ptr(w), float(w_scale), T, H, D, fmt, _ptr(q_out),
+                                 _ptr(q_sf), _ptr(w_out), _ptr(pre), _ptr(bits))
+    return bad, q_out, q_sf, w_out, pre, bits
 
 
 def topk(logits, lengths, k, nthreads=0) -> np.ndarray:

@@ -582,3 +582,228 @@ int orc_topk_to_ragged_slots(const int32_t *topk, int64_t ld, int rows, int k,
     }
     return bad;
 }
+
+/* ------------------------------------------------------------------------ */
+/* K and Q producers.                                                       */
+/*   - deepseek_v41 rocm.py, rocm_mxfp4_indexer_k_store: the key is RMS-     */
+/*     normalised (weight, eps), rotated by RoPE at its position and         */
+/*     written quantised into the cache slot kv_slot_mapping[t];             */
+/*   - same page, rocm_mxfp4_indexer_q_quant: the query heads are rotated    */
+/*     and quantised, and the weights are multiplied by the softmax scale    */
+/*     times the head scale;                                                 */
+/*   - RoPE: GPT-J pairs on the trailing rope_dim of a head with the cache   */
+/*     row laid out cos | sin, the forward rotation of the inverse one of    */
+/*     rocm_aiter_mla_sparse _inverse_rope_gptj_kernel;                      */
+/*   - quantiser: rocm_aiter_mla_sparse _mxfp8_scale_bits (biased E8M0       */
+/*     exponent that puts amax at the top of the element range) with top    */
+/*     448 (e4m3) or 6 (e2m1), values multiplied by 2^(127 - bits) and      */
+/*     rounded to the nearest element code, ties to the even code.          */
+/* ------------------------------------------------------------------------ */
+
+static double bf16_to_double(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Forward GPT-J rotation of the pairs (x[n + 2i], x[n + 2i + 1]),
+ * n = D - rope_dim: even' = a cos - b sin, odd' = b cos + a sin, with
+ * cos = cs[i], sin = cs[rope_dim / 2 + i]. */
+static void rope_gptj(double *x, int D, int rope_dim, const float *cs)
+{
+    const int n = D - rope_dim, half = rope_dim / 2;
+    for (int i = 0; i < half; ++i) {
+        const double a = x[n + 2 * i], b = x[n + 2 * i + 1];
+        const double c = cs[i], s = cs[half + i];
+        x[n + 2 * i] = a * c - b * s;
+        x[n + 2 * i + 1] = b * c + a * s;
+    }
+}
+
+/* Biased E8M0 exponent putting amax at the top `top` of the element range. */
+static int scale_bits(double amax, double top)
+{
+    const double floor_amax = ldexp(1.0, -126);
+    if (amax < floor_amax)
+        amax = floor_amax;
+    double bits = ceil(log2(amax / top)) + 127.0;
+    if (bits < 0.0)
+        bits = 0.0;
+    if (bits > 254.0)
+        bits = 254.0;
+    return (int)bits;
+}
+
+/* Nearest code among the non-negative codes 0..ncodes-1 of a decoder,
+ * ties to the even code; the sign bit `sign_bit` copies y's sign bit (so
+ * -0 and negatives that round to zero give negative zero, as a cast does). */
+static uint8_t encode_nearest(double y, double (*dec)(uint8_t), int ncodes, uint8_t sign_bit)
+{
+    const double a = fabs(y);
+    int best = 0;
+    double bestd = INFINITY;
+    for (int c = 0; c < ncodes; ++c) {
+        const double d = fabs(dec((uint8_t)c) - a);
+        if (d < bestd || (d == bestd && (c & 1) == 0 && (best & 1) == 1)) {
+            best = c;
+            bestd = d;
+        }
+    }
+    return (uint8_t)((signbit(y) ? sign_bit : 0) | best);
+}
+
+uint8_t orc_e4m3_encode(double y)
+{
+    return encode_nearest(y, orc_e4m3_to_double, 0x7F, 0x80); /* 0..0x7E finite */
+}
+
+uint8_t orc_e2m1_encode(double y)
+{
+    return encode_nearest(y, orc_e2m1_to_double, 8, 0x8);
+}
+
+int orc_scale_bits(double amax, double top)
+{
+    return scale_bits(amax, top);
+}
+
+/* Quantise one head vector y[D]: FP8 -> codes[D] and one exponent; MXFP4 ->
+ * packed[D/2] and D/32 exponents.  Returns nothing; bits[] receives the
+ * exponents. */
+static void quantise_vec(const double *y, int D, int fmt, uint8_t *codes, int *bits)
+{
+    if (fmt == ORC_FMT_FP8) {
+        double amax = 0.0;
+        for (int d = 0; d < D; ++d)
+            if (fabs(y[d]) > amax)
+                amax = fabs(y[d]);
+        bits[0] = scale_bits(amax, 448.0);
+        const double inv = ldexp(1.0, 127 - bits[0]);
+        for (int d = 0; d < D; ++d)
+            codes[d] = orc_e4m3_encode(y[d] * inv);
+        return;
+    }
+    for (int j = 0; j < D / 32; ++j) {
+        double amax = 0.0;
+        for (int d = 32 * j; d < 32 * j + 32; ++d)
+            if (fabs(y[d]) > amax)
+                amax = fabs(y[d]);
+        bits[j] = scale_bits(amax, 6.0);
+    }
+    memset(codes, 0, (size_t)D / 2);
+    for (int d = 0; d < D; ++d) {
+        const uint8_t nib = orc_e2m1_encode(y[d] * ldexp(1.0, 127 - bits[d / 32]));
+        codes[d / 2] |= (uint8_t)(d % 2 == 0 ? nib : nib << 4);
+    }
+}
+
+/* K producer: token t (slot_mapping[t] >= 0) -> RMSNorm -> RoPE at
+ * positions[t] -> quantise -> the block-flat page of cache slot
+ * slot_mapping[t] (FP8: P*D codes then P fp32 scales 2^(bits-127); MXFP4:
+ * P*D/2 packed bytes then P*D/32 e8m0 bytes).  pre (nullable, [T, D]) gets
+ * the rotated values before scaling, bits_out (nullable, [T, D/32]) the
+ * exponents (FP8: one, in column 0).  Returns the number of tokens skipped
+ * for a slot outside the pool or a position outside the cos/sin table. */
+int orc_k_norm_rope_store(const uint16_t *k_pre, int64_t ld_k, const int32_t *positions,
+                          const float *cos_sin, int64_t ld_cs, int num_pos, int rope_dim,
+                          const float *norm_w, double eps, uint8_t *pages, int64_t page_stride,
+                          int num_pages, int page_size, const int64_t *slots, int T, int D,
+                          int fmt, double *pre, int32_t *bits_out)
+{
+    int bad = 0;
+    double *y = (double *)malloc(sizeof(double) * D);
+    uint8_t *codes = (uint8_t *)malloc((size_t)D);
+    int *bits = (int *)malloc(sizeof(int) * (D / 32 > 0 ? D / 32 : 1));
+    const int rowb = fmt == ORC_FMT_FP8 ? D : D / 2;
+    for (int t = 0; t < T; ++t) {
+        const int64_t slot = slots[t];
+        if (slot < 0)
+            continue;
+        const int64_t page = slot / page_size, off = slot % page_size;
+        const int pos = positions[t];
+        if (page >= num_pages || pos < 0 || pos >= num_pos) {
+            ++bad;
+            continue;
+        }
+        double ss = 0.0;
+        for (int d = 0; d < D; ++d) {
+            y[d] = bf16_to_double(k_pre[(size_t)t * ld_k + d]);
+            ss += y[d] * y[d];
+        }
+        const double r = 1.0 / sqrt(ss / D + eps);
+        for (int d = 0; d < D; ++d)
+            y[d] = y[d] * r * (double)norm_w[d];
+        rope_gptj(y, D, rope_dim, cos_sin + (size_t)pos * ld_cs);
+        if (pre)
+            memcpy(pre + (size_t)t * D, y, sizeof(double) * D);
+        quantise_vec(y, D, fmt, codes, bits);
+        uint8_t *pg = pages + page * page_stride;
+        memcpy(pg + off * rowb, codes, (size_t)rowb);
+        if (fmt == ORC_FMT_FP8) {
+            const float sc = (float)ldexp(1.0, bits[0] - 127);
+            memcpy(pg + (int64_t)page_size * rowb + off * 4, &sc, 4);
+        } else {
+            for (int j = 0; j < D / 32; ++j)
+                pg[(int64_t)page_size * rowb + off * (D / 32) + j] = (uint8_t)bits[j];
+        }
+        if (bits_out)
+            for (int j = 0; j < (fmt == ORC_FMT_FP8 ? 1 : D / 32); ++j)
+                bits_out[(size_t)t * (D / 32) + j] = bits[j];
+    }
+    free(y);
+    free(codes);
+    free(bits);
+    return bad;
+}
+
+/* Q producer: head (t, h) of q [T, H, D] -> RoPE at positions[t] ->
+ * quantise.  FP8: codes [T, H, D], weights_out = w_in * w_scale *
+ * 2^(bits-127) (the power-of-two query scale folded into the weight);
+ * MXFP4: packed [T, H, D/2] and e8m0 bytes [T, H, D/32], weights_out =
+ * w_in * w_scale.  pre / bits_out as for the K producer ([T*H, D],
+ * [T*H, D/32]).  Returns the number of tokens with a position outside the
+ * table (their heads are left untouched). */
+int orc_q_rope_quant(const uint16_t *q, const int32_t *positions, const float *cos_sin,
+                     int64_t ld_cs, int num_pos, int rope_dim, const float *w_in, double w_scale,
+                     int T, int H, int D, int fmt, uint8_t *q_out, uint8_t *q_sf_out,
+                     float *w_out, double *pre, int32_t *bits_out)
+{
+    int bad = 0;
+    double *y = (double *)malloc(sizeof(double) * D);
+    uint8_t *codes = (uint8_t *)malloc((size_t)D);
+    int *bits = (int *)malloc(sizeof(int) * (D / 32 > 0 ? D / 32 : 1));
+    const int rowb = fmt == ORC_FMT_FP8 ? D : D / 2;
+    for (int t = 0; t < T; ++t) {
+        const int pos = positions[t];
+        if (pos < 0 || pos >= num_pos) {
+            ++bad;
+            continue;
+        }
+        for (int h = 0; h < H; ++h) {
+            const size_t th = (size_t)t * H + h;
+            for (int d = 0; d < D; ++d)
+                y[d] = bf16_to_double(q[th * D + d]);
+            rope_gptj(y, D, rope_dim, cos_sin + (size_t)pos * ld_cs);
+            if (pre)
+                memcpy(pre + th * D, y, sizeof(double) * D);
+            quantise_vec(y, D, fmt, codes, bits);
+            memcpy(q_out + th * rowb, codes, (size_t)rowb);
+            if (fmt == ORC_FMT_FP8) {
+                w_out[th] = (float)((double)w_in[th] * w_scale * ldexp(1.0, bits[0] - 127));
+            } else {
+                for (int j = 0; j < D / 32; ++j)
+                    q_sf_out[th * (D / 32) + j] = (uint8_t)bits[j];
+                w_out[th] = (float)((double)w_in[th] * w_scale);
+            }
+            if (bits_out)
+                for (int j = 0; j < (fmt == ORC_FMT_FP8 ? 1 : D / 32); ++j)
+                    bits_out[th * (D / 32) + j] = bits[j];
+        }
+    }
+    free(y);
+    free(codes);
+    free(bits);
+    return bad;
+}

@@ -20,4 +20,4 @@ from ._binding import (  # noqa: F401
     library_path,
     version,
 )
-from .pipeline import IndexerStep  # noqa: F401
+from .pipeline import IndexerStep, ProducerStep  # noqa: F401

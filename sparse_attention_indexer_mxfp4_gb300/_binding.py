@@ -24,6 +24,7 @@ _ERRORS = {1: "IDX_ERR_INVALID_ARG", 2: "IDX_ERR_UNSUPPORTED", 3: "IDX_ERR_WORKS
            4: "IDX_ERR_CUDA"}
 DEV_BAD_PAGE = 1
 DEV_TIMEOUT = 4
+DEV_BAD_POSITION = 8
 SLOT_DIRECT_ROWS = 4096  # above it the slot map runs a third (scan) kernel
 
 _lib = None
@@ -43,6 +44,10 @@ _SIGNATURES = {
     "idx_topk_noalloc": [_P, _L, _I, _P, _I, _P, _L, _P],
     "idx_topk_candidates": [_P, _L, _I, _P, _P, _P, _L, _I, _I, _I, _I, _P, _L, _P],
     "idx_topk_to_ragged_slots": [_P, _L, _I, _I, _P, _I, _P, _L, _I, _I, _I, _P, _P, _P, _P],
+    "idx_k_norm_rope_store": [_P, _L, _P, _P, _L, _I, _I, _P, ctypes.c_float, _I, _I, _I, _P,
+                              _L, _I, _I, _P, _P],
+    "idx_q_rope_quant": [_P, _P, _P, _L, _I, _I, _P, ctypes.c_float, _I, _I, _I, _I, _P, _P, _P,
+                         _P],
     "idx_get_device_status": [_P, ctypes.POINTER(ctypes.c_uint32)],
 }
 
@@ -358,6 +363,72 @@ def idx_topk_to_ragged_slots(topk, block_table, page_size, num_pages, slots, ind
                              next_n=1, row_to_seq=None, max_blocks=None, stream=None):
     prepare_topk_to_ragged_slots(topk, block_table, page_size, num_pages, slots, indptr, lens,
                                  next_n, row_to_seq, max_blocks)(stream)
+
+
+def _bf16_bits(t):
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16)
+    if t.dtype in (torch.int16, torch.uint16):
+        return t
+    raise ValueError("expected bfloat16 (or its 16-bit pattern)")
+
+
+def prepare_k_norm_rope_store(k_pre, positions, cos_sin, rope_dim, norm_weight, eps, kv_pages,
+                              page_size, slot_mapping, fmt):
+    """K producer into kv_pages (uint8 [num_pages, page_stride]).  k_pre
+    bf16 [T, >= D]; positions int32 [T]; cos_sin fp32 [P, >= rope_dim];
+    norm_weight fp32 [D]; slot_mapping int64 [T] (-1 skips)."""
+    k = _bf16_bits(k_pre)
+    T = k.shape[0]
+    _need(positions, torch.int32, "positions")
+    _need(norm_weight, torch.float32, "norm_weight")
+    _need(slot_mapping, torch.int64, "slot_mapping")
+    if cos_sin is not None:
+        _need(cos_sin, torch.float32, "cos_sin")
+    if kv_pages.dtype != torch.uint8 or kv_pages.dim() != 2 or kv_pages.stride(1) != 1:
+        raise ValueError("kv_pages must be uint8 [num_pages, page_stride] with unit byte stride")
+    # no table (rope_dim 0): positions are not bounded by one
+    ncs, ldcs = (2 ** 31 - 1, rope_dim) if cos_sin is None else (cos_sin.shape[0],
+                                                                cos_sin.stride(0))
+    args = (_ptr(k), k.stride(0), _ptr(positions), _ptr(cos_sin), ldcs, ncs, rope_dim,
+            _ptr(norm_weight), float(eps), T, norm_weight.shape[0], fmt, _ptr(kv_pages),
+            kv_pages.stride(0), kv_pages.shape[0], page_size, _ptr(slot_mapping))
+    return Prepared("idx_k_norm_rope_store", args,
+                    (k, positions, cos_sin, norm_weight, kv_pages, slot_mapping))
+
+
+def idx_k_norm_rope_store(k_pre, positions, cos_sin, rope_dim, norm_weight, eps, kv_pages,
+                          page_size, slot_mapping, fmt, stream=None):
+    prepare_k_norm_rope_store(k_pre, positions, cos_sin, rope_dim, norm_weight, eps, kv_pages,
+                              page_size, slot_mapping, fmt)(stream)
+
+
+def prepare_q_rope_quant(q, positions, cos_sin, rope_dim, weights, weight_scale, fmt, q_out,
+                         weights_out, q_scale_out=None):
+    """Q producer.  q bf16 [T, H, D]; weights fp32 [T, H]; q_out uint8
+    [T, H, D] (FP8) or [T, H, D/2] (MXFP4); q_scale_out int32 [T, H] (MXFP4);
+    weights_out fp32 [T, H]."""
+    qb = _bf16_bits(q)
+    if not qb.is_contiguous():
+        raise ValueError("q must be contiguous [T, H, D]")
+    T, H, D = qb.shape
+    _need(positions, torch.int32, "positions")
+    _need(weights, torch.float32, "weights")
+    _need(weights_out, torch.float32, "weights_out")
+    if cos_sin is not None:
+        _need(cos_sin, torch.float32, "cos_sin")
+    ncs, ldcs = (2 ** 31 - 1, rope_dim) if cos_sin is None else (cos_sin.shape[0],
+                                                                cos_sin.stride(0))
+    args = (_ptr(qb), _ptr(positions), _ptr(cos_sin), ldcs, ncs, rope_dim, _ptr(weights),
+            float(weight_scale), T, H, D, fmt, _ptr(q_out), _ptr(q_scale_out), _ptr(weights_out))
+    return Prepared("idx_q_rope_quant", args,
+                    (qb, positions, cos_sin, weights, q_out, q_scale_out, weights_out))
+
+
+def idx_q_rope_quant(q, positions, cos_sin, rope_dim, weights, weight_scale, fmt, q_out,
+                     weights_out, q_scale_out=None, stream=None):
+    prepare_q_rope_quant(q, positions, cos_sin, rope_dim, weights, weight_scale, fmt, q_out,
+                         weights_out, q_scale_out)(stream)
 
 
 def idx_get_device_status(stream=None) -> int:

@@ -142,6 +142,25 @@ class IndexerStep:
         self.topk_stage(stream)
         self.slots_stage(stream)
 
+    # ---------------------------------------------------- host round trip
+    def twin(self):
+        """A second buffer set for the same case, sharing the K cache."""
+        return IndexerStep(self.case, device=self.device, fused_mask=self.fused_mask,
+                           num_ctas=self.num_ctas, gather=self.gather,
+                           cand_topk=self.cand_topk, kv_from=self)
+
+    def input_names(self):
+        """The per-step inputs a caller copies in (the K cache is state)."""
+        names = ["q", "weights", "lengths"]
+        if self.paged:
+            return names + ["block_table", "context_lens"] + (
+                ["cand"] if self.cand is not None else [])
+        return names + ["ks", "ke"]
+
+    def results(self):
+        """The per-step outputs a caller reads back."""
+        return [self.topk] + ([self.slots, self.indptr] if self.paged else [])
+
     @property
     def launches_per_step(self) -> int:
         calls = self._logits_calls + [self._topk_call]
@@ -150,3 +169,64 @@ class IndexerStep:
         if self._slots_call is not None:
             calls.append(self._slots_call)
         return sum(c.kernels for c in calls)
+
+
+class ProducerStep:
+    """Device-resident inputs and outputs of one K/Q producer step
+    (synth.ProducerCase) and its two calls: the K producer writes the new
+    keys into the cache pages, the Q producer quantises the query heads and
+    scales their weights.  ``logits_stage``/``topk_stage`` name the K and Q
+    calls so the benchmark's stage timing applies unchanged."""
+
+    def __init__(self, case, device="cuda", consts_from=None):
+        self.case = case
+        self.device = torch.device(device)
+        d = self.device
+        c = case
+        self.k_pre = torch.from_numpy(c.k_pre).to(d).to(torch.bfloat16)
+        self.q = torch.from_numpy(c.q).to(d).to(torch.bfloat16)
+        self.weights = _dev(c.weights, d)
+        self.positions = _dev(c.positions, d)
+        self.slots = _dev(c.slots, d)
+        if consts_from is not None:  # model constants: the rotary table and the norm weight
+            self.cos_sin, self.norm_weight = consts_from.cos_sin, consts_from.norm_weight
+        else:
+            self.cos_sin, self.norm_weight = _dev(c.cos_sin, d), _dev(c.norm_weight, d)
+        self.pages = torch.zeros((c.num_pages, c.page_stride), dtype=torch.uint8, device=d)
+        rowb = c.D if c.fmt == 0 else c.D // 2
+        self.q_out = torch.empty((c.T, c.H, rowb), dtype=torch.uint8, device=d)
+        self.q_sf = (torch.empty((c.T, c.H), dtype=torch.int32, device=d) if c.fmt == 1
+                     else None)
+        self.weights_out = torch.empty((c.T, c.H), dtype=torch.float32, device=d)
+        self._k_call = B.prepare_k_norm_rope_store(
+            self.k_pre, self.positions, self.cos_sin, c.rope_dim, self.norm_weight, c.eps,
+            self.pages, c.page_size, self.slots, c.fmt)
+        self._q_call = B.prepare_q_rope_quant(
+            self.q, self.positions, self.cos_sin, c.rope_dim, self.weights, c.weight_scale,
+            c.fmt, self.q_out, self.weights_out, self.q_sf)
+
+    def logits_stage(self, stream=None):
+        self._k_call(stream)
+
+    def topk_stage(self, stream=None):
+        self._q_call(stream)
+
+    def slots_stage(self, stream=None):
+        pass
+
+    def run(self, stream=None):
+        self._k_call(stream)
+        self._q_call(stream)
+
+    def twin(self):
+        return ProducerStep(self.case, device=self.device, consts_from=self)
+
+    def input_names(self):
+        return ["k_pre", "q", "weights", "positions", "slots"]
+
+    def results(self):
+        return [self.q_out] + ([self.q_sf] if self.q_sf is not None else []) + [self.weights_out]
+
+    @property
+    def launches_per_step(self) -> int:
+        return 2

@@ -316,4 +316,80 @@ def config6(shard: int = 0) -> PagedCase:
     return c
 
 
-CONFIGS = {1: config1, 2: config2, 3: config3, 4: config4, 5: config5, 6: config6}
+@dataclass
+class ProducerCase:
+    """Inputs of one K/Q producer step: T new tokens whose keys are
+    normalised, rotated, quantised and stored into cache slots, and whose
+    query heads are rotated and quantised with their weights scaled."""
+
+    fmt: int
+    T: int
+    H: int
+    D: int
+    rope_dim: int
+    page_size: int
+    num_pages: int
+    page_stride: int
+    k_pre: np.ndarray        # float32 [T, D] holding bf16-exact values
+    q: np.ndarray            # float32 [T, H, D] holding bf16-exact values
+    weights: np.ndarray      # float32 [T, H]
+    weight_scale: float
+    positions: np.ndarray    # int32 [T]
+    cos_sin: np.ndarray      # float32 [num_positions, rope_dim]: cos | sin
+    norm_weight: np.ndarray  # float32 [D]
+    eps: float
+    slots: np.ndarray        # int64 [T] cache slots
+    name: str = ""
+
+    @property
+    def rows(self) -> int:
+        return self.T
+
+
+def _bf16_exact(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to the nearest bf16 (ties to even) and return
+    them as float32."""
+    u = np.asarray(x, np.float32).view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    return u.astype(np.uint32).view(np.float32)
+
+
+def rope_table(num_positions: int, rope_dim: int, base: float = 10000.0) -> np.ndarray:
+    """Rotary table, row p = cos(p f_i) for i < rope_dim/2, then sin(p f_i),
+    f_i = base^(-i / (rope_dim/2))."""
+    half = rope_dim // 2
+    f = base ** (-np.arange(half, dtype=np.float64) / half)
+    ang = np.arange(num_positions, dtype=np.float64)[:, None] * f[None, :]
+    return np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32)
+
+
+def producer_case(seed: int, T: int, H: int, D: int, rope_dim: int, page_size: int,
+                  fmt: int = FMT_MXFP4, start_pos: int = 0, pool_factor: float = 1.0,
+                  name: str = "") -> ProducerCase:
+    rng = np.random.default_rng(seed)
+    npages = max(1, int(math.ceil(T / page_size * pool_factor)))
+    rowb = D if fmt == FMT_FP8 else D // 2
+    sbytes = 4 if fmt == FMT_FP8 else D // 32
+    stride = page_size * (rowb + sbytes)
+    stride = (stride + 15) // 16 * 16
+    scale = rng.uniform(0.1, 10.0, (T, 1))
+    k_pre = _bf16_exact((rng.standard_normal((T, D)) * scale).astype(np.float32))
+    q = _bf16_exact(rng.standard_normal((T, H, D)).astype(np.float32))
+    w = (rng.standard_normal((T, H)) / 8).astype(np.float32)
+    pos = (start_pos + np.arange(T)).astype(np.int32)
+    slots = rng.permutation(npages * page_size)[:T].astype(np.int64)
+    return ProducerCase(fmt, T, H, D, rope_dim, page_size, npages, stride, k_pre, q, w,
+                        float(np.float32(1.0 / math.sqrt(D) * H ** -0.5)), pos,
+                        rope_table(start_pos + T, rope_dim),
+                        rng.uniform(0.5, 1.5, D).astype(np.float32), 1e-6, slots, name)
+
+
+def config7(shard: int = 0) -> ProducerCase:
+    """K/Q producers of a prefill chunk: 8192 new tokens at positions
+    0..8191, H=64, D=128, rope_dim=64, MXFP4 keys into 64-token pages and
+    MXFP4 query heads."""
+    return producer_case(shard_seed(7, shard), 8192, 64, 128, 64, 64,
+                         name="producers_prefill_T8192_mxfp4")
+
+
+CONFIGS = {1: config1, 2: config2, 3: config3, 4: config4, 5: config5, 6: config6, 7: config7}

@@ -101,6 +101,46 @@ def test_block_max_argument_checks():
     assert call(B=0) == 0
 
 
+def test_producer_argument_checks():
+    L = B.lib()
+    k = L.idx_k_norm_rope_store
+    # k_pre, ld_k, pos, cos_sin, ld_cs, npos, rope_dim, norm_w, eps, T, D, fmt, pages, stride,
+    # npages, P, slots, stream
+    kb = [FAKE, 128, FAKE, FAKE, 64, 100, 64, FAKE, 1e-6, 8, 128, 0, FAKE, 8448, 4, 64, FAKE,
+          None]
+
+    def kc(**kw):
+        a = list(kb)
+        idx = dict(ld=1, rd=6, eps=8, T=9, D=10, fmt=11, stride=13, slots=16)
+        for n, v in kw.items():
+            a[idx[n]] = v
+        return k(*a)
+    assert kc(rd=63) == INVALID            # odd rope_dim
+    assert kc(rd=130) == INVALID           # rope_dim > D
+    assert kc(eps=-1.0) == INVALID
+    assert kc(stride=8000) == INVALID      # page smaller than P * (D + 4)
+    assert kc(slots=None) == INVALID
+    assert kc(fmt=5) == INVALID
+    assert kc(D=64, stride=64 * 68) == UNSUPPORTED
+    assert kc(ld=130) == UNSUPPORTED       # rows of k_pre not 8-byte aligned
+    assert kc(T=0) == 0
+    q = L.idx_q_rope_quant
+    # q, pos, cos_sin, ld_cs, npos, rope_dim, w, w_scale, T, H, D, fmt, q_out, q_sf, w_out, stream
+    qb = [FAKE, FAKE, FAKE, 64, 100, 64, FAKE, 0.5, 4, 64, 128, 1, FAKE, FAKE, FAKE, None]
+
+    def qc(**kw):
+        a = list(qb)
+        idx = dict(rd=5, T=8, H=9, D=10, fmt=11, qsf=13)
+        for n, v in kw.items():
+            a[idx[n]] = v
+        return q(*a)
+    assert qc(qsf=None) == INVALID          # MXFP4 needs the scale output
+    assert qc(H=0) == INVALID
+    assert qc(rd=3) == INVALID
+    assert qc(D=256) == UNSUPPORTED
+    assert qc(T=0) == 0
+
+
 def test_select_argument_checks():
     L = B.lib()
     assert L.idx_topk(FAKE, 100, 2, FAKE, 10, FAKE, 5, None, 0, None) == INVALID  # ld_out < k

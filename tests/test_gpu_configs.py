@@ -119,3 +119,53 @@ def test_contiguous_config(cfg):
     ora_idx = oracle.topk(ref, sub.ke, c.topk)
     gpu_idx = st.topk[torch.from_numpy(rows).cuda()].cpu().numpy()
     assert_topk_near_tie(gpu_idx, ora_idx, ref, sub.ke, c.topk, f"config {cfg}")
+
+
+def test_producer_config():
+    """Config 7 (K/Q producers of an 8192-token prefill chunk) through
+    ProducerStep: sampled tokens against the oracle, with the same rounding
+    rule as the producer tests."""
+    from sparse_attention_indexer_mxfp4_gb300.pipeline import ProducerStep
+    from test_gpu_producers import _bits_ok, _check_block, _decode
+    c = synth.CONFIGS[7]()
+    st = ProducerStep(c)
+    st.run()
+    torch.cuda.synchronize()
+    assert B.idx_get_device_status() == 0
+    toks = np.array([0, 1, c.T // 2, c.T - 1])
+    kbits = torch.from_numpy(c.k_pre[toks]).to(torch.bfloat16).view(torch.int16).numpy() \
+        .view(np.uint16)
+    pages = np.zeros((c.num_pages, c.page_stride), np.uint8)
+    bad, pre, obits = oracle.k_norm_rope_store(c.fmt, kbits, c.positions[toks], c.cos_sin,
+                                               c.rope_dim, c.norm_weight, c.eps, pages,
+                                               c.page_size, c.slots[toks])
+    assert bad == 0
+    g = st.pages.cpu().numpy()
+    rowb, sbytes, span = c.D // 2, c.D // 32, 32
+    for i, t in enumerate(toks):
+        pg, off = divmod(int(c.slots[t]), c.page_size)
+        dec = _decode(c.fmt, g[pg, off * rowb:(off + 1) * rowb])
+        sb = g[pg, c.page_size * rowb + off * sbytes:c.page_size * rowb + (off + 1) * sbytes]
+        for j in range(c.D // span):
+            seg = pre[i, j * span:(j + 1) * span]
+            assert _bits_ok(c.fmt, np.abs(seg).max(), int(sb[j]), int(obits[i, j]))
+            if int(sb[j]) == int(obits[i, j]):
+                _check_block(c.fmt, seg * 2.0 ** (127 - int(obits[i, j])),
+                             dec[j * span:(j + 1) * span])
+    qbits = torch.from_numpy(c.q[toks]).to(torch.bfloat16).view(torch.int16).numpy() \
+        .view(np.uint16)
+    bad, o_q, o_sf, o_w, qpre, qob = oracle.q_rope_quant(c.fmt, qbits, c.positions[toks],
+                                                         c.cos_sin, c.rope_dim, c.weights[toks],
+                                                         c.weight_scale)
+    assert bad == 0
+    gq = st.q_out.cpu().numpy()[toks].reshape(len(toks) * c.H, rowb)
+    gsf = st.q_sf.cpu().numpy()[toks].reshape(-1).view(np.uint8).reshape(-1, 4)
+    np.testing.assert_array_equal(st.weights_out.cpu().numpy()[toks], o_w)
+    for th in range(len(toks) * c.H):
+        dec = _decode(c.fmt, gq[th])
+        for j in range(c.D // span):
+            seg = qpre[th, j * span:(j + 1) * span]
+            assert _bits_ok(c.fmt, np.abs(seg).max(), int(gsf[th, j]), int(qob[th, j]))
+            if int(gsf[th, j]) == int(qob[th, j]):
+                _check_block(c.fmt, seg * 2.0 ** (127 - int(qob[th, j])),
+                             dec[j * span:(j + 1) * span])
