@@ -61,17 +61,22 @@ __device__ __forceinline__ float scale_of(int bits)
     return bits > 0 ? __uint_as_float((uint32_t)bits << 23) : __uint_as_float(0x400000u);
 }
 
-// Nearest e2m1 code of y (|y| <= 6 after scaling), ties to the even code;
-// the sign bit copies y's (negative zero for -0 and for negatives that round
-// to zero, as a cast does).  Codes 0..7 are 0, 0.5, 1, 1.5, 2, 3, 4, 6: each
-// threshold is the midpoint between two neighbours, inclusive on the side of
-// the even one.
-__device__ __forceinline__ uint32_t e2m1_code(float y)
+// Four values (|y| <= 6 after scaling) to four e2m1 codes in the low 16
+// bits, element 2j in the low nibble of byte j: the hardware conversion of
+// a pair of f32 to a packed e2m1 pair, round to nearest even (its second
+// source lands in the low nibble).
+__device__ __forceinline__ uint32_t e2m1_pack4(float y0, float y1, float y2, float y3)
 {
-    const float a = fabsf(y);
-    const uint32_t c = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) +
-                       (a >= 3.5f) + (a > 5.0f);
-    return ((__float_as_uint(y) >> 31) << 3) | c;
+    uint32_t out;
+    asm("{\n"
+        ".reg .b8 lo, hi;\n"
+        "cvt.rn.satfinite.e2m1x2.f32 lo, %2, %1;\n"
+        "cvt.rn.satfinite.e2m1x2.f32 hi, %4, %3;\n"
+        "mov.b32 %0, {lo, hi, 0, 0};\n"
+        "}"
+        : "=r"(out)
+        : "f"(y0), "f"(y1), "f"(y2), "f"(y3));
+    return out;
 }
 
 // GPT-J rotation of the lane's pairs (y[0], y[1]) and (y[2], y[3]) that lie
@@ -125,12 +130,8 @@ __device__ __forceinline__ uint32_t quantise_lane(const float y[4], int fmt, int
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     const int bits = scale_bits(amax, 0x400000u, 2);  // 6 = 1.5 * 2^2
     const float inv = inv_scale(bits);
-    uint32_t half = 0;
-    #pragma unroll
-    for (int i = 0; i < 4; ++i)
-        half |= e2m1_code(y[i] * inv) << (4 * i);  // element 2j in the low nibble of byte j
     *bits_out = bits;
-    return half;
+    return e2m1_pack4(y[0] * inv, y[1] * inv, y[2] * inv, y[3] * inv);
 }
 
 __global__ void __launch_bounds__(kProdThreads)
@@ -186,11 +187,11 @@ __global__ void __launch_bounds__(kProdThreads)
     }
 }
 
-// Each warp takes kQHeads heads at a time and issues all their loads (the
-// positions, then the heads and their cos/sin rows) before it computes any:
-// a head is only 256 bytes, so one head per warp leaves too little in flight
-// to cover the memory latency.
-constexpr int kQHeads = 4;
+// Each warp takes kQHeads heads of one token at a time: the token's
+// position and cos/sin row are loaded once for them, and all the heads'
+// loads are issued before any is computed (a head is only 256 bytes, so one
+// head per warp leaves too little in flight to cover the memory latency).
+constexpr int kQHeads = 8;
 
 __global__ void __launch_bounds__(kProdThreads)
     q_quant_kernel(const uint16_t *__restrict__ q, const int32_t *__restrict__ positions,
@@ -202,56 +203,50 @@ __global__ void __launch_bounds__(kProdThreads)
     pdl_wait();
     pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
-    const long long heads = (long long)T * H;
+    const int groups = (H + kQHeads - 1) / kQHeads;  // head groups of a token
+    const long long items = (long long)T * groups;
     const long long warps = (long long)gridDim.x * (kProdThreads / 32);
     const int n = 128 - rope_dim, half = rope_dim / 2;
-    for (long long base = ((long long)blockIdx.x * (kProdThreads / 32) + (threadIdx.x >> 5)) *
-                          kQHeads;
-         base < heads; base += warps * kQHeads) {
-        int pos[kQHeads];
+    for (long long it = (long long)blockIdx.x * (kProdThreads / 32) + (threadIdx.x >> 5);
+         it < items; it += warps) {
+        const int t = (int)(it / groups);
+        const int h0 = (int)(it - (long long)t * groups) * kQHeads;
+        const int pos = positions[t];
         uint2 raw[kQHeads];
-        float cs[kQHeads][4];  // cos, sin of the lane's two pairs
         #pragma unroll
         for (int u = 0; u < kQHeads; ++u) {
-            const long long th = base + u;
-            pos[u] = th < heads ? positions[th / H] : -1;
-            raw[u] = th < heads ? *reinterpret_cast<const uint2 *>(q + th * 128 + 4 * lane)
+            const long long th = (long long)t * H + h0 + u;
+            raw[u] = h0 + u < H ? *reinterpret_cast<const uint2 *>(q + th * 128 + 4 * lane)
                                 : make_uint2(0u, 0u);
         }
+        if (pos < 0 || pos >= num_pos) {
+            if (lane == 0)
+                atomicOr(status, kDevBadPosition);
+            continue;
+        }
+        float cs[4] = {1.0f, 0.0f, 1.0f, 0.0f};  // cos, sin of the lane's two pairs
         #pragma unroll
-        for (int u = 0; u < kQHeads; ++u) {
-            const bool ok = pos[u] >= 0 && pos[u] < num_pos;
-            #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const int e = 4 * lane + 2 * i;
-                cs[u][2 * i] = 1.0f;
-                cs[u][2 * i + 1] = 0.0f;
-                if (ok && e >= n) {
-                    const float *row = cos_sin + (size_t)pos[u] * ld_cs;
-                    cs[u][2 * i] = row[(e - n) >> 1];
-                    cs[u][2 * i + 1] = row[half + ((e - n) >> 1)];
-                }
+        for (int i = 0; i < 2; ++i) {
+            const int e = 4 * lane + 2 * i;
+            if (e >= n) {
+                const float *row = cos_sin + (size_t)pos * ld_cs;
+                cs[2 * i] = row[(e - n) >> 1];
+                cs[2 * i + 1] = row[half + ((e - n) >> 1)];
             }
         }
         #pragma unroll
         for (int u = 0; u < kQHeads; ++u) {
-            const long long th = base + u;
-            if (th >= heads)
+            if (h0 + u >= H)
                 break;
-            if (pos[u] < 0 || pos[u] >= num_pos) {
-                if (lane == 0)
-                    atomicOr(status, kDevBadPosition);
-                continue;
-            }
+            const long long th = (long long)t * H + h0 + u;
             float y[4] = {bf16_bits_to_float(raw[u].x & 0xffffu), bf16_bits_to_float(raw[u].x >> 16),
                           bf16_bits_to_float(raw[u].y & 0xffffu), bf16_bits_to_float(raw[u].y >> 16)};
             #pragma unroll
             for (int i = 0; i < 2; ++i) {
                 if (4 * lane + 2 * i >= n) {  // GPT-J pair of the trailing rope_dim
                     const float a = y[2 * i], b = y[2 * i + 1];
-                    const float c = cs[u][2 * i], sn = cs[u][2 * i + 1];
-                    y[2 * i] = a * c - b * sn;
-                    y[2 * i + 1] = b * c + a * sn;
+                    y[2 * i] = a * cs[2 * i] - b * cs[2 * i + 1];
+                    y[2 * i + 1] = b * cs[2 * i] + a * cs[2 * i + 1];
                 }
             }
             int bits;
@@ -347,7 +342,7 @@ extern "C" idx_status idx_q_rope_quant(const uint16_t *q, const int32_t *positio
     if (!status)
         return IDX_ERR_CUDA;
     return launch_status(launch_pdl(q_quant_kernel,
-                                    dim3(prod_grid(((long long)T * H + kQHeads - 1) / kQHeads)),
+                                    dim3(prod_grid((long long)T * ((H + kQHeads - 1) / kQHeads))),
                                     dim3(kProdThreads), 0, (cudaStream_t)stream, q, positions,
                                     cos_sin, ld_cos_sin, num_positions, rope_dim, weights,
                                     weight_scale, T, H, f,
