@@ -86,9 +86,9 @@ def producer_bytes(case) -> float:
 # since and the traffic is reported as null.
 LOGITS_SOURCES = ["idx_logits_kernel.cuh", "idx_logits.cuh", "idx_common.cuh", "idx_api.cu"]
 NCU_TRAFFIC = {
-    4: {"bytes": 91136 + 189568000 + 8561408, "digest": "bf7c7ffb2c11e59f",
+    4: {"bytes": 91136 + 189573632 + 8378112, "digest": "81d1e06d97682009",
         "profile": "profiles/logits_kernel_paged_fp8_decode_b128_mtp2.md"},
-    6: {"bytes": 3840 + 413296896 + 21575936, "digest": "bf7c7ffb2c11e59f",
+    6: {"bytes": 3840 + 413373184 + 21578496, "digest": "81d1e06d97682009",
         "profile": "profiles/logits_kernel_candidate_source_b128_mtp2.md"},
 }
 
@@ -302,7 +302,9 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     case = _case(args.config, shard=rank)
     prod = _is_producer(case)
-    step = ProducerStep(case, device=dev) if prod else IndexerStep(case, device=dev)
+    step = (ProducerStep(case, device=dev) if prod else
+            IndexerStep(case, device=dev, fused_topk=args.fused_topk))
+    fused = getattr(step, "fused_topk", False)
     metric, unit, div = _metric_unit_div(case)
     stream = torch.cuda.current_stream()
 
@@ -347,6 +349,8 @@ def run_ours(args):
         achieved_gbs = lb / (ms_per_step * 1e-3) / 1e9
     else:
         lb = logits_bytes(case, cand_only=getattr(step, "cand_topk", False))
+        if fused:  # the stage also holds the top-k: one more read of the live logits
+            lb += 4.0 * float(np.clip(case.row_ends(), 0, case.width).sum())
         achieved_gbs = lb / (logit_avg * 1e-3) / 1e9
     if prod:
         roof = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": hbm, "unit": "GB/s",
@@ -362,9 +366,12 @@ def run_ours(args):
                 "traffic": None, "peak_source": f"{src} bf16 x 2 (fp8 dense)"}
     else:
         roof = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(achieved_gbs / hbm, 4), "traffic": logits_traffic(args.config),
+                "frac": round(achieved_gbs / hbm, 4),
+                "traffic": None if fused else logits_traffic(args.config),
                 "peak_source": f"{src} hbm_gbs",
-                "kernel": ("logits stage: cand_plan_kernel (candidate plan, -inf fill) + "
+                "kernel": ("fused logits + top-k stage: top-k plan_kernel, logits_kernel with "
+                           "digit-1 histograms, top-k phases_kernel from the filter" if fused
+                           else "logits stage: cand_plan_kernel (candidate plan, -inf fill) + "
                            "logits_kernel" if getattr(case, "cand", None) is not None
                            else "logits stage: bmax_fill_kernel + logits_kernel with block "
                            "maxima" if getattr(case, "source_block", 0) else "logits_kernel"),
@@ -386,6 +393,7 @@ def run_ours(args):
         "topk_ms" if not prod else "q_quant_ms": round(topk_avg, 5),
         "roofline": roof, "clocks": clk,
         "gpu_launches": step.launches_per_step * args.steps,
+        "fused_topk": fused,
         "e2e": e2e,
     }
     if rank == 0:
@@ -684,6 +692,9 @@ def main():
     p.add_argument("--config", type=int, default=4, choices=[1, 2, 3, 4, 5, 6, 7])
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    p.add_argument("--fused-topk", action="store_true",
+                   help="paged workloads without a candidate list: one call for the logits and "
+                        "the row top-k (idx_paged_mqa_logits_topk)")
     args = p.parse_args()
     if args.warmup < 3:
         args.warmup = 3

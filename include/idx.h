@@ -175,6 +175,39 @@ idx_status idx_paged_mqa_logits_block_max(
     float *block_max, int64_t ld_block_max, int block_size, int num_ctas, idx_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * idx_paged_mqa_logits_topk -- the paged logits (with block maxima when
+ * block_max is given) and the per-row top-k of them in one call, the logits
+ * kernel counting the top-k's first radix digit as it writes the logits.
+ * Passage: as idx_paged_mqa_logits_block_max and idx_topk; the fusion (a
+ * logits -> top-k prefilter) is a design of this library with no counterpart
+ * in the pages.
+ *
+ *   Arguments as idx_paged_mqa_logits_block_max (block_max NULL: none), plus
+ *   lengths   [B * next_n] int32: each row's ke as the logits define it (the
+ *             top-k's row lengths; other values break the fused counts).
+ *   k, out_idx, ld_out  as idx_topk.
+ *   ws, ws_bytes  the top-k's scratch (idx_topk_workspace_size(B * next_n,
+ *             ld_logits, k), 16-byte aligned).
+ *   With that scratch, ld_logits > 8192, next_n <= 2 and cooperative launch,
+ *   the top-k's plan kernel runs first, the logits kernel adds every written
+ *   logit's digit-1 bin to the top-k's row histogram (shared-memory
+ *   histograms per warpgroup, flushed per row group) and its valid counts,
+ *   and the top-k starts at its filter phase: the same logits and indices as
+ *   the two calls, one pass over the logits fewer.  Otherwise it is
+ *   idx_paged_mqa_logits_block_max (or idx_paged_mqa_logits) followed by
+ *   idx_topk.
+ * Errors: as those calls; nothing is launched when a host check fails.
+ * ---------------------------------------------------------------------- */
+idx_status idx_paged_mqa_logits_topk(
+    const void *q, const void *q_scale, const float *weights, const uint8_t *kv_pages,
+    int64_t page_stride_bytes, int num_pages, const int32_t *block_table, int64_t bt_stride,
+    const int32_t *context_lens, int ctx_per_row, const int32_t *row_ks, int B, int next_n, int H,
+    int D, int page_size, idx_kv_format fmt, float *logits, int64_t ld_logits, int max_model_len,
+    float *block_max, int64_t ld_block_max, int block_size, const int32_t *lengths, int k,
+    int32_t *out_idx, int64_t ld_out, int num_ctas, void *ws, size_t ws_bytes,
+    idx_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * idx_paged_mqa_logits_candidates -- idx_paged_mqa_logits for a consumer
  * that reads only the candidate blocks (idx_topk_candidates).
  * Passage: as idx_paged_mqa_logits; the candidate mask of rocm_aiter_mla_sparse,

@@ -44,6 +44,9 @@ _SIGNATURES = {
     "idx_topk_noalloc": [_P, _L, _I, _P, _I, _P, _L, _P],
     "idx_topk_candidates": [_P, _L, _I, _P, _P, _P, _L, _I, _I, _I, _I, _P, _L, _P],
     "idx_topk_to_ragged_slots": [_P, _L, _I, _I, _P, _I, _P, _L, _I, _I, _I, _P, _P, _P, _P],
+    "idx_paged_mqa_logits_topk": [_P, _P, _P, _P, _L, _I, _P, _L, _P, _I, _P, _I, _I, _I, _I,
+                                  _I, _I, _P, _L, _I, _P, _L, _I, _P, _I, _P, _L, _I, _P, _S,
+                                  _P],
     "idx_k_norm_rope_store": [_P, _L, _P, _P, _L, _I, _I, _P, ctypes.c_float, _I, _I, _I, _P,
                               _L, _I, _I, _P, _P],
     "idx_q_rope_quant": [_P, _P, _P, _L, _I, _I, _P, ctypes.c_float, _I, _I, _I, _I, _P, _P, _P,
@@ -235,6 +238,50 @@ def idx_paged_mqa_logits_block_max(q, q_scale, weights, kv_pages, block_table, c
                                        context_lens, next_n, page_size, fmt, logits,
                                        max_model_len, block_max, block_size, row_ks,
                                        ctx_per_row, num_ctas)(stream)
+
+
+def prepare_paged_mqa_logits_topk(q, q_scale, weights, kv_pages, block_table, context_lens,
+                                  next_n, page_size, fmt, logits, max_model_len, lengths, k, out,
+                                  block_max=None, block_size=0, row_ks=None, ctx_per_row=False,
+                                  num_ctas=0, workspace=True):
+    """Paged logits (+ block maxima) and their top-k in one call; with the
+    top-k scratch (workspace=True allocates it) the logits kernel counts the
+    top-k's first digit and the top-k skips a pass.  lengths: each row's ke."""
+    q = _u8(q)
+    rows, H = q.shape[0], q.shape[1]
+    D = q.shape[2] if fmt == FMT_FP8 else 2 * q.shape[2]
+    B = rows // next_n
+    _need(weights, torch.float32, "weights")
+    _need(block_table, torch.int32, "block_table")
+    _need(context_lens, torch.int32, "context_lens")
+    _need(lengths, torch.int32, "lengths")
+    if out.dtype != torch.int32 or out.stride(1) != 1:
+        raise ValueError("out must be int32 with unit column stride")
+    if block_max is not None:
+        _need(block_max, torch.float32, "block_max")
+    if kv_pages.dtype != torch.uint8 or kv_pages.dim() != 2 or kv_pages.stride(1) != 1:
+        raise ValueError("kv_pages must be uint8 [num_pages, page_stride] with unit byte stride")
+    ld = logits.stride(0)
+    ws = None
+    if workspace is True:
+        nbytes = topk_workspace_size(rows, ld, k)
+        if nbytes:
+            ws = torch.empty(nbytes, dtype=torch.uint8, device=logits.device)
+    elif workspace is not None and workspace is not False:
+        ws = workspace
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    args = (_ptr(q), _ptr(q_scale), _ptr(weights), _ptr(kv_pages), kv_pages.stride(0),
+            kv_pages.shape[0], _ptr(block_table), block_table.stride(0), _ptr(context_lens),
+            int(ctx_per_row), _ptr(row_ks), B, next_n, H, D, page_size, fmt, _ptr(logits), ld,
+            max_model_len, _ptr(block_max), 0 if block_max is None else block_max.stride(0),
+            block_size, _ptr(lengths), k, _ptr(out), out.stride(0), num_ctas, _ptr(ws), nbytes)
+    need = topk_workspace_size(rows, ld, k)
+    chunked = ws is not None and need > 0 and nbytes >= need and ld > 8192
+    # launches: top-k plan, (block-maxima fill), logits, top-k phases
+    kernels = (1 if block_max is not None else 0) + (3 if chunked else 2)
+    return Prepared("idx_paged_mqa_logits_topk", args,
+                    (q, q_scale, weights, kv_pages, block_table, context_lens, row_ks, logits,
+                     block_max, lengths, out, ws), kernels)
 
 
 def paged_workspace_size(B, next_n, max_model_len, num_cand) -> int:

@@ -110,20 +110,31 @@ cudaError_t launch_logits_t(const LogitsArgs &a0, const CUtensorMap &tmK, const 
     LogitsArgs a = a0;
     a.tile_shift = TK == 256 ? 8 : 7;
     a.group_cost = a.paged && TK == 128 ? kGroupCost128 : 0;
-    const size_t smem = (size_t)C::fixed_bytes() + (size_t)2 * G * a.cand_words * 4;
-    // variant: 0 dense, 1 gather plan, 2 dense with block maxima
-    const int variant = a.plan ? 1 : a.bmax ? 2 : 0;
+    size_t smem = (size_t)C::fixed_bytes() + (size_t)2 * G * a.cand_words * 4;
+    // variant: 0 dense, 1 gather plan, 2 dense with block maxima, 3 dense
+    // with digit-1 histograms, 4 both
+    const int variant = a.plan ? 1 : (a.bmax ? 2 : 0) + (a.hist ? (a.bmax ? 2 : 3) : 0);
     decltype(&logits_kernel<FMT, H, G, S, NA, TK, false>) kern = nullptr;
     if (variant == 1)
         kern = logits_kernel<FMT, H, G, S, NA, TK, true>;
     else if (variant == 0)
         kern = logits_kernel<FMT, H, G, S, NA, TK, false>;
-    else if constexpr (BM)
-        kern = logits_kernel<FMT, H, G, S, NA, TK, false, true>;
+    else if constexpr (BM) {
+        if (variant == 2)
+            kern = logits_kernel<FMT, H, G, S, NA, TK, false, true>;
+        else if (variant == 3)
+            kern = logits_kernel<FMT, H, G, S, NA, TK, false, false, true>;
+        else
+            kern = logits_kernel<FMT, H, G, S, NA, TK, false, true, true>;
+    }
     if (!kern)
         return cudaErrorNotSupported;
+    if (a.hist)
+        smem += 16 + hist_smem_bytes<G, NA>();
+    if (smem > kMaxSmem)
+        return cudaErrorNotSupported;
     // raise each kernel's dynamic shared memory limit once per device
-    static int configured[3][kMaxDevices] = {};
+    static int configured[5][kMaxDevices] = {};
     const int dev = current_device();
     if (dev < 0 || dev >= kMaxDevices)
         return cudaErrorInvalidDevice;
@@ -338,11 +349,14 @@ __global__ void __launch_bounds__(256) bmax_fill_kernel(float *bmax, int64_t ld,
     }
 }
 
-// Block maxima requested with the logits (nullable).
+// Extra epilogue outputs requested with the logits: block maxima (nullable
+// out) and the digit-1 histograms of a chunked top-k (nullable hist).
 struct BlockMaxOut {
     float *out = nullptr;
     int64_t ld = 0;
     int block = 0;
+    uint32_t *hist = nullptr, *hvalid = nullptr, *cvalid = nullptr;
+    int hist_P = 0;
 };
 
 static idx_status paged_logits(bool cand_only,
@@ -352,7 +366,7 @@ static idx_status paged_logits(bool cand_only,
     int H, int D, int page_size, idx_kv_format fmt, const int32_t *candidate_blocks,
     int64_t cand_stride, int num_cand, int cand_block, float *logits, int64_t ld_logits,
     int max_model_len, int num_ctas, void *ws, size_t ws_bytes, idx_stream_t stream,
-    BlockMaxOut bm = BlockMaxOut())
+    BlockMaxOut bm = BlockMaxOut(), bool check_only = false)
 {
     if (B < 0 || next_n <= 0 || H <= 0 || D <= 0 || page_size <= 0 || num_pages < 0 ||
         max_model_len < 0 || num_ctas < 0 || !valid_fmt(fmt))
@@ -464,6 +478,8 @@ static idx_status paged_logits(bool cand_only,
     a.status = device_status_ptr();
     if (!a.status)
         return IDX_ERR_CUDA;
+    if (check_only)  // every host check passed; nothing is launched
+        return IDX_OK;
     const int nctas = num_ctas > 0 ? num_ctas : sm_count();
     // gather path: with a fused candidate mask and scratch for the plan, only
     // tiles and 64-key boxes that hold a candidate key are loaded and scored
@@ -472,6 +488,10 @@ static idx_status paged_logits(bool cand_only,
     const bool planned = plan_need > 0 && ws && ws_bytes >= plan_need && aligned16(ws);
     if (cand_only && !planned)
         return plan_need == 0 ? IDX_ERR_INVALID_ARG : IDX_ERR_WORKSPACE;
+    a.hist = bm.hist;
+    a.hvalid = bm.hvalid;
+    a.cvalid = bm.cvalid;
+    a.hist_P = bm.hist_P;
     if (bm.out) {
         a.bmax = bm.out;
         a.ld_bmax = bm.ld;
@@ -493,7 +513,7 @@ static idx_status paged_logits(bool cand_only,
     bool supported = false;
     cudaError_t e =
         launch_logits(f, H, G, a, tmK, tmQ, tmS, nctas, (cudaStream_t)stream, &supported);
-    if (!supported)
+    if (!supported || e == cudaErrorNotSupported)
         return IDX_ERR_UNSUPPORTED;
     return launch_status(e);
 }
@@ -545,6 +565,66 @@ extern "C" idx_status idx_paged_mqa_logits_block_max(
                         block_table, bt_stride, context_lens, ctx_per_row, row_ks, B, next_n, H, D,
                         page_size, fmt, nullptr, 0, 0, 0, logits, ld_logits, max_model_len,
                         num_ctas, nullptr, 0, stream, bm);
+}
+
+extern "C" idx_status idx_paged_mqa_logits_topk(
+    const void *q, const void *q_scale, const float *weights, const uint8_t *kv_pages,
+    int64_t page_stride_bytes, int num_pages, const int32_t *block_table, int64_t bt_stride,
+    const int32_t *context_lens, int ctx_per_row, const int32_t *row_ks, int B, int next_n, int H,
+    int D, int page_size, idx_kv_format fmt, float *logits, int64_t ld_logits, int max_model_len,
+    float *block_max, int64_t ld_block_max, int block_size, const int32_t *lengths, int k,
+    int32_t *out_idx, int64_t ld_out, int num_ctas, void *ws, size_t ws_bytes,
+    idx_stream_t stream)
+{
+    if (B < 0 || next_n <= 0 || k < 0 || ld_out < k || ld_logits <= 0 || ld_logits > INT32_MAX)
+        return IDX_ERR_INVALID_ARG;
+    if (B == 0 || max_model_len == 0)
+        return IDX_OK;
+    if (!lengths || (k > 0 && !out_idx))
+        return IDX_ERR_INVALID_ARG;
+    const int rows = B * next_n;
+    BlockMaxOut bm;
+    bm.out = block_max;
+    bm.ld = ld_block_max;
+    bm.block = block_size;
+    cudaStream_t s = (cudaStream_t)stream;
+    // the fused path: the logits kernel counts the top-k's digit-1 histograms
+    // (one- and two-row groups; the chunked top-k must apply)
+    const bool fused = k > 0 && next_n <= 2 &&
+                       topk_takes_chunked(logits, ld_logits, rows, k, ws, ws_bytes);
+    if (fused) {
+        // the logits call's own checks run before the top-k's plan is
+        // launched, so a rejected call launches nothing
+        const idx_status chk = paged_logits(false, q, q_scale, weights, kv_pages,
+                                            page_stride_bytes, num_pages, block_table, bt_stride,
+                                            context_lens, ctx_per_row, row_ks, B, next_n, H, D,
+                                            page_size, fmt, nullptr, 0, 0, 0, logits, ld_logits,
+                                            max_model_len, num_ctas, nullptr, 0, stream, bm,
+                                            /*check_only=*/true);
+        if (chk != IDX_OK)
+            return chk;
+        idx_status st = topk_chunked_plan(lengths, ld_logits, rows, ws, 1, s);
+        if (st != IDX_OK)
+            return st;
+        bm.hist_P = topk_chunked_counts(ws, rows, ld_logits, &bm.hist, &bm.hvalid, &bm.cvalid);
+        st = paged_logits(false, q, q_scale, weights, kv_pages, page_stride_bytes, num_pages,
+                          block_table, bt_stride, context_lens, ctx_per_row, row_ks, B, next_n,
+                          H, D, page_size, fmt, nullptr, 0, 0, 0, logits, ld_logits,
+                          max_model_len, num_ctas, nullptr, 0, stream, bm);
+        if (st != IDX_OK)
+            return st;
+        const int vec_ok = (ld_logits % 4 == 0) && aligned16(logits);
+        return topk_chunked_phases(logits, ld_logits, rows, lengths, k, out_idx, ld_out, ws,
+                                   vec_ok, 1, s);
+    }
+    const idx_status st = paged_logits(false, q, q_scale, weights, kv_pages, page_stride_bytes,
+                                       num_pages, block_table, bt_stride, context_lens,
+                                       ctx_per_row, row_ks, B, next_n, H, D, page_size, fmt,
+                                       nullptr, 0, 0, 0, logits, ld_logits, max_model_len,
+                                       num_ctas, nullptr, 0, stream, bm);
+    if (st != IDX_OK || k == 0)
+        return st;
+    return idx_topk(logits, ld_logits, rows, lengths, k, out_idx, ld_out, ws, ws_bytes, stream);
 }
 
 extern "C" size_t idx_paged_mqa_logits_workspace_size(int B, int next_n, int max_model_len,

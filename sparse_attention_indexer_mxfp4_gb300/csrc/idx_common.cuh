@@ -106,6 +106,18 @@ IDX_DEVFN bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
     return mbar_wait_slow(bar, parity, abort, status, limit_ns);
 }
 
+// Order-preserving 32-bit key of a float: a larger float gives a larger key;
+// non-finite values give 0, below the key of every finite value.  The
+// top-k's radix digits and the logits kernel's digit-1 histograms both use
+// it.
+IDX_DEVFN uint32_t order_key(float v)
+{
+    const uint32_t b = __float_as_uint(v);
+    if (!isfinite(v))
+        return 0u;
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
 // Float max into memory holding a float (prefilled, e.g. with -inf): values
 // with the sign bit clear order like their bits as signed integers and win by
 // atomicMax; values with it set order inversely to their bits as unsigned

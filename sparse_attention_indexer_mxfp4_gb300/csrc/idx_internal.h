@@ -27,6 +27,21 @@ inline bool aligned16(const void *p)
 bool encode_tma_u8(CUtensorMap *map, int rank, const void *base, const uint64_t *dims,
                    const uint64_t *strides_bytes, const uint32_t *box, CUtensorMapSwizzle swz);
 
+// Chunked top-k pieces (idx_select.cu) for a logits call that computes the
+// top-k's digit-1 histograms itself: the plan kernel (with zero_cvalid it
+// also clears the per-chunk valid counts), the phases (hist_done: start at
+// the filter), where the counts live in ws, and whether idx_topk would take
+// the chunked path for these arguments.
+idx_status topk_chunked_plan(const int32_t *lengths, int64_t ld, int rows, void *ws,
+                             int zero_cvalid, cudaStream_t s);
+idx_status topk_chunked_phases(const float *logits, int64_t ld, int rows, const int32_t *lengths,
+                               int k, int32_t *out, int64_t ld_out, void *ws, int vec_ok,
+                               int hist_done, cudaStream_t s);
+int topk_chunked_counts(void *ws, int rows, int64_t ld, uint32_t **hist, uint32_t **valid,
+                        uint32_t **cvalid);
+bool topk_takes_chunked(const float *logits, int64_t ld, int rows, int k, const void *ws,
+                        size_t ws_bytes);
+
 inline idx_status launch_status(cudaError_t e)
 {
     return e == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;

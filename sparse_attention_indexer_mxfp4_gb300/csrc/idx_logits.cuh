@@ -73,6 +73,14 @@ struct LogitsArgs {
     float *bmax;
     int64_t ld_bmax;
     int bmax_block;
+    // Digit-1 histograms for a chunked top-k that runs next (nullable):
+    // hist[r][2048] counts the written finite logits of row r by their
+    // order-preserving key's top 11 bits, hvalid[r] and cvalid[r][hist_P]
+    // (per 8192-key chunk) count them; all cleared beforehand.
+    uint32_t *hist;
+    uint32_t *hvalid;
+    uint32_t *cvalid;
+    int hist_P;
     // Candidate gather plan (nullable), written by cand_plan_kernel: per row
     // group plan_words words: [0] the number n of compute tiles (tiles that
     // hold a candidate key of any of the group's rows), then box_words words

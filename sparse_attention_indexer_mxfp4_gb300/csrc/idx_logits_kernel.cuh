@@ -76,7 +76,8 @@ struct LogitsCfg {
     static constexpr int OFF_SIDE = OFF_QATOM + 4 * QATOM_BYTES;
     static constexpr int OFF_BAR = (OFF_SIDE + NA * SIDE_BYTES + 7) / 8 * 8;
     // full[S], empty[S], acc_full[NA], acc_empty[NA], q_full[2], q_empty[2]
-    static constexpr int NUM_BARS = 2 * S + 2 * NA + 4;
+    // + hist[NA][2]: a warpgroup's histogram hand-over (histogram variant)
+    static constexpr int NUM_BARS = 2 * S + 2 * NA + 4 + 2 * NA;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;  // tmem base, abort flag
     static constexpr int OFF_SCRATCH = (OFF_MISC + 16 + 7) / 8 * 8;  // 40 long longs
     static constexpr int OFF_BITMAP = OFF_SCRATCH + 40 * 8;
@@ -171,7 +172,17 @@ __device__ __forceinline__ HalfInfo half_info(const LogitsArgs &a, const UnitWal
 
 namespace idx {
 
-template <int FMT, int H, int G, int S, int NA, int TK, bool PLAN, bool BMAX = false>
+// Shared-memory bytes of the digit-1 histograms of the histogram variant:
+// one 2048-bin histogram per row of the group for each epilogue warpgroup,
+// placed after the candidate bitmaps.
+template <int G, int NA>
+constexpr int hist_smem_bytes()
+{
+    return NA * G * 2048 * 4;
+}
+
+template <int FMT, int H, int G, int S, int NA, int TK, bool PLAN, bool BMAX = false,
+          bool HIST = false>
 __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
     logits_kernel(const __grid_constant__ LogitsArgs a, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmS)
@@ -185,6 +196,7 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
     uint64_t *full = bars, *empty = bars + S;
     uint64_t *acc_full = bars + 2 * S, *acc_empty = acc_full + NA;
     uint64_t *q_full = acc_empty + NA, *q_empty = q_full + 2;
+    uint64_t *hbar = q_empty + 2;  // [NA][2]: counts done, flush done
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
     long long *scratch = reinterpret_cast<long long *>(smem + C::OFF_SCRATCH);
@@ -206,6 +218,9 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
             mbar_init(&q_full[i], 1);
             mbar_init(&q_empty[i], 2 + C::EPI_WARPS);  // both MMA warps' commits + epilogue
         }
+        for (int i = 0; i < 2 * NA; ++i) {
+            mbar_init(&hbar[i], 4);  // the warpgroup's four warps
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -225,6 +240,15 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
     int g0, k0, n0;
     long long count;
     locate_units<PLAN>(a, scratch, g0, k0, n0, count);  // contains __syncthreads
+    // histogram variant: one 2048-bin histogram per (warpgroup, row of the
+    // group), after the candidate bitmaps, cleared before the barrier below
+    uint32_t *hist_sm = nullptr;
+    if constexpr (HIST) {
+        hist_sm = reinterpret_cast<uint32_t *>(
+            smem + ((C::OFF_BITMAP + 2 * G * a.cand_words * 4 + 15) & ~15));
+        for (int b = threadIdx.x; b < NA * G * 2048; b += C::THREADS)
+            hist_sm[b] = 0u;
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -497,6 +521,16 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
         int slot = 0;
         int rks[G], rke[G];
         constexpr int NSUB = C::NSUB;
+        // histogram variant: this warpgroup's G x 2048 bins; the warp's
+        // valid keys of each row in the 8192-key chunk it is in (flushed
+        // when the chunk or the group changes) and in the group
+        uint32_t *hs = HIST ? hist_sm + (size_t)wg * G * 2048 : nullptr;
+        uint32_t hphase = 0;  // phase of this warpgroup's hand-over barriers
+        uint32_t vchunk_n[G], vrow_n[G];
+        int vchunk = -1;
+        #pragma unroll
+        for (int i = 0; i < G; ++i)
+            vchunk_n[i] = vrow_n[i] = 0u;
         for (; w.left > 0; walk_next<PLAN>(a, w), ++u) {
             if (w.first_in_group) {
                 slot = gq & 1;
@@ -674,6 +708,41 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
                             orow[t] = val[sub][i];
                     }
                 }
+                if (HIST && compute) {
+                    // digit-1 counts of the written logits into the
+                    // warpgroup's shared histogram, one atomic per distinct
+                    // bin of the warp; valid keys counted per warp (its 32
+                    // keys lie in one 8192-key chunk)
+                    #pragma unroll
+                    for (int sub = 0; sub < NSUB; ++sub) {
+                        const int chunk = (t0 - lane + sub * kMmaM) >> 13;  // the warp's first key
+                        if (chunk != vchunk) {
+                            if (vchunk >= 0 && lane == 0)
+                                #pragma unroll
+                                for (int i = 0; i < G; ++i)
+                                    if (vchunk_n[i])
+                                        atomicAdd(a.cvalid + (size_t)(w.gi.row0 + i) * a.hist_P +
+                                                      vchunk, vchunk_n[i]);
+                            #pragma unroll
+                            for (int i = 0; i < G; ++i)
+                                vchunk_n[i] = 0u;
+                            vchunk = chunk;
+                        }
+                        #pragma unroll
+                        for (int i = 0; i < G; ++i) {
+                            if (i >= w.gi.nrows)
+                                break;
+                            const uint32_t key = order_key(val[sub][i]);
+                            const uint32_t bin = key ? key >> 21 : 0xffffffffu;
+                            const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+                            if (key && lane == __ffs(peers) - 1)
+                                atomicAdd(&hs[i * 2048 + bin], (uint32_t)__popc(peers));
+                            const uint32_t n = (uint32_t)__popc(__ballot_sync(0xffffffffu, key != 0u));
+                            vchunk_n[i] += n;
+                            vrow_n[i] += n;
+                        }
+                    }
+                }
                 if (BMAX && compute) {
                     // block maxima: a warp's 32 consecutive keys span at most
                     // two blocks (block >= 32 keys); each part's maximum goes
@@ -709,6 +778,44 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(&q_empty[slot]);
+                if constexpr (HIST) {
+                    // the warp's valid counts of the group go out; the
+                    // group's bins of this warpgroup go to the rows'
+                    // histograms once its four warps are done with the
+                    // group; the bins are cleared before any warp counts the
+                    // next group (bounded waits on two barriers)
+                    if (lane == 0)
+                        #pragma unroll
+                        for (int i = 0; i < G; ++i) {
+                            if (i < w.gi.nrows && vchunk_n[i])
+                                atomicAdd(a.cvalid + (size_t)(w.gi.row0 + i) * a.hist_P + vchunk,
+                                          vchunk_n[i]);
+                            if (i < w.gi.nrows && vrow_n[i])
+                                atomicAdd(a.hvalid + w.gi.row0 + i, vrow_n[i]);
+                        }
+                    #pragma unroll
+                    for (int i = 0; i < G; ++i)
+                        vchunk_n[i] = vrow_n[i] = 0u;
+                    vchunk = -1;
+                    if (lane == 0)
+                        mbar_arrive(&hbar[2 * wg]);
+                    if (!mbar_wait(&hbar[2 * wg], hphase, abort_flag, a.status))
+                        break;
+                    for (int b = quad * 32 + lane; b < G * 2048; b += 128) {
+                        const uint32_t v = hs[b];
+                        if (v) {
+                            atomicAdd(a.hist + (size_t)(w.gi.row0 + b / 2048) * 2048 + (b & 2047),
+                                      v);
+                            hs[b] = 0u;
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&hbar[2 * wg + 1]);
+                    if (!mbar_wait(&hbar[2 * wg + 1], hphase, abort_flag, a.status))
+                        break;
+                    hphase ^= 1u;
+                }
             }
         }
     }

@@ -299,33 +299,71 @@ idx_status topk_launch_per_row(const float *logits, int64_t ld, int rows,
     return launch_status(cudaGetLastError());
 }
 
-// Chunked top-k over the caller's workspace: the plan kernel, then one
-// cooperative launch of the phases (see idx_topk_chunked.cuh).  Returns
-// IDX_ERR_UNSUPPORTED when the device has no cooperative launch.
-idx_status topk_launch_chunked(const float *logits, int64_t ld, int rows,
-                               const int32_t *lengths, int k, int32_t *out, int64_t ld_out,
-                               void *ws, int vec_ok, cudaStream_t s)
+} // namespace
+
+// Resident phase CTAs per SM of the chunked top-k on the current device
+// (0 on error, -1 without cooperative launch).
+static int chunked_grid_per_sm()
 {
     namespace C = topk_chunked;
-    static int grid_per_sm[64] = {};  // resident phase CTAs per SM, 0 = not known yet
+    static int grid_per_sm[64] = {};  // 0 = not known yet
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
-        return IDX_ERR_CUDA;
+        return 0;
     if (!grid_per_sm[dev]) {
         int coop = 0, n = 0;
         if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess)
-            return IDX_ERR_CUDA;
+            return 0;
         if (!coop)
-            return IDX_ERR_UNSUPPORTED;
+            return -1;
         if (cudaFuncSetAttribute(C::phases_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::kPhaseDynSmem) != cudaSuccess)
-            return IDX_ERR_CUDA;
+            return 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, C::phases_kernel, C::kThreads,
                                                           C::kPhaseDynSmem) != cudaSuccess ||
             n < 1)
-            return IDX_ERR_CUDA;
+            return 0;
         grid_per_sm[dev] = n;
     }
+    return grid_per_sm[dev];
+}
+
+// The chunked top-k's plan kernel: clears the row histograms and counters
+// (and, with zero_cvalid, the per-chunk valid counts) and lists the live
+// chunks.  IDX_ERR_UNSUPPORTED without cooperative launch.
+idx_status topk_chunked_plan(const int32_t *lengths, int64_t ld, int rows, void *ws,
+                             int zero_cvalid, cudaStream_t s)
+{
+    namespace C = topk_chunked;
+    const int g = chunked_grid_per_sm();
+    if (g < 0)
+        return IDX_ERR_UNSUPPORTED;
+    if (g == 0)
+        return IDX_ERR_CUDA;
+    const int P = (int)((ld + C::kCh - 1) / C::kCh);
+    C::Ws w;
+    C::ws_layout(ws, rows, P, &w);
+    const long long zero_vec4 = ((long long)rows * (2048 + 2) + 3) / 4;
+    const int g_plan = (int)std::max<long long>(
+        1, std::min<long long>(sm_count(), (zero_vec4 + C::kPlanThreads - 1) / C::kPlanThreads));
+    return launch_status(launch_pdl(C::plan_kernel, dim3(g_plan), dim3(C::kPlanThreads), 0, s,
+                                    lengths, ld, rows, P, w, zero_cvalid));
+}
+
+// The chunked top-k's phases (one cooperative launch; every CTA resident).
+// hist_done: the row histograms and the valid counts were written by the
+// kernel before (the logits kernel's histogram variant), so the phases start
+// at the filter.
+idx_status topk_chunked_phases(const float *logits, int64_t ld, int rows, const int32_t *lengths,
+                               int k, int32_t *out, int64_t ld_out, void *ws, int vec_ok,
+                               int hist_done, cudaStream_t s)
+{
+    namespace C = topk_chunked;
+    const int g = chunked_grid_per_sm();
+    if (g < 0)
+        return IDX_ERR_UNSUPPORTED;
+    if (g == 0)
+        return IDX_ERR_CUDA;
     unsigned int *status = device_status_ptr();
     if (!status)
         return IDX_ERR_CUDA;
@@ -340,18 +378,12 @@ idx_status topk_launch_chunked(const float *logits, int64_t ld, int rows,
     a.out = out;
     a.ld_out = ld_out;
     a.vec_ok = vec_ok;
+    a.hist_done = hist_done;
     a.status = status;
     C::ws_layout(ws, rows, P, &a.ws);
-    const long long zero_vec4 = ((long long)rows * (2048 + 2) + 3) / 4;
-    const int g_plan = (int)std::max<long long>(
-        1, std::min<long long>(sm_count(), (zero_vec4 + C::kPlanThreads - 1) / C::kPlanThreads));
-    cudaError_t e = launch_pdl(C::plan_kernel, dim3(g_plan), dim3(C::kPlanThreads), 0, s, lengths,
-                               ld, rows, a.ws);
-    if (e != cudaSuccess)
-        return IDX_ERR_CUDA;
     // every CTA resident (the phases wait on one another), no more CTAs
     // than there can be items or rows
-    const long long cap = (long long)grid_per_sm[dev] * sm_count();
+    const long long cap = (long long)g * sm_count();
     const long long want = std::max<long long>((long long)rows * P, rows);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)std::max<long long>(1, std::min(cap, want)));
@@ -363,8 +395,47 @@ idx_status topk_launch_chunked(const float *logits, int64_t ld, int rows,
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, C::phases_kernel, a);
-    return launch_status(e);
+    return launch_status(cudaLaunchKernelEx(&cfg, C::phases_kernel, a));
+}
+
+// Where a chunked top-k over (rows, ld) keeps its row histograms, valid
+// counts and per-chunk valid counts inside ws; returns the chunks per row.
+int topk_chunked_counts(void *ws, int rows, int64_t ld, uint32_t **hist, uint32_t **valid,
+                        uint32_t **cvalid)
+{
+    namespace C = topk_chunked;
+    const int P = (int)((ld + C::kCh - 1) / C::kCh);
+    C::Ws w;
+    C::ws_layout(ws, rows, P, &w);
+    *hist = w.hist;
+    *valid = w.valid;
+    *cvalid = w.cvalid;
+    return P;
+}
+
+// Whether idx_topk takes the chunked path for these arguments.
+bool topk_takes_chunked(const float *logits, int64_t ld, int rows, int k, const void *ws,
+                        size_t ws_bytes)
+{
+    const size_t need = idx_topk_workspace_size(rows, ld, k);
+    (void)logits;
+    return ws && need > 0 && ws_bytes >= need && aligned16(ws) && ld > topk_chunked::kCh &&
+           chunked_grid_per_sm() > 0;
+}
+
+namespace {
+
+// Chunked top-k over the caller's workspace: the plan kernel, then one
+// cooperative launch of the phases (see idx_topk_chunked.cuh).  Returns
+// IDX_ERR_UNSUPPORTED when the device has no cooperative launch.
+idx_status topk_launch_chunked(const float *logits, int64_t ld, int rows,
+                               const int32_t *lengths, int k, int32_t *out, int64_t ld_out,
+                               void *ws, int vec_ok, cudaStream_t s)
+{
+    const idx_status st = topk_chunked_plan(lengths, ld, rows, ws, 0, s);
+    if (st != IDX_OK)
+        return st;
+    return topk_chunked_phases(logits, ld, rows, lengths, k, out, ld_out, ws, vec_ok, 0, s);
 }
 
 } // namespace

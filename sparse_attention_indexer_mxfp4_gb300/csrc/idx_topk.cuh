@@ -21,6 +21,8 @@
 
 #include <cstdint>
 
+#include "idx_common.cuh"
+
 namespace idx {
 namespace topk_detail {
 
@@ -43,10 +45,7 @@ struct Shared {
 
 __device__ __forceinline__ uint32_t float_key(float v)
 {
-    const uint32_t b = __float_as_uint(v);
-    if (!isfinite(v))
-        return 0u;
-    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    return order_key(v);
 }
 
 // Keys of elements i0..i0+3 of a row (0 past `end`).

@@ -175,7 +175,8 @@ __device__ __forceinline__ uint32_t ld_cg(const uint32_t *p)
 // live chunks in (row, chunk) order, stores their number and clears the
 // grid barrier's arrival count.
 __global__ void __launch_bounds__(kPlanThreads)
-    plan_kernel(const int32_t *__restrict__ lengths, int64_t ld, int R, Ws ws)
+    plan_kernel(const int32_t *__restrict__ lengths, int64_t ld, int R, int P, Ws ws,
+                int zero_cvalid)
 {
     __shared__ uint32_t red[kPlanThreads / 32];
     pdl_wait();  // the workspace and lengths may belong to the previous kernel until here
@@ -187,6 +188,9 @@ __global__ void __launch_bounds__(kPlanThreads)
         z4[i] = make_uint4(0u, 0u, 0u, 0u);
     if (blockIdx.x == 0 && tid < (int)(nz & 3))
         ws.hist[(nz & ~(size_t)3) + tid] = 0u;
+    if (zero_cvalid)  // a logits kernel will count the chunks' valid keys into it
+        for (size_t i = (size_t)blockIdx.x * kPlanThreads + tid; i < (size_t)R * P; i += stride)
+            ws.cvalid[i] = 0u;
     if (blockIdx.x != 0)
         return;
     uint32_t carry = 0;
@@ -689,6 +693,7 @@ struct PhaseArgs {
     int32_t *out;
     int64_t ld_out;
     int vec_ok;
+    int hist_done;  // the row histograms and valid counts are already in ws
     unsigned *status;
     Ws ws;
 };
@@ -743,18 +748,26 @@ __global__ void __launch_bounds__(kThreads, 2) phases_kernel(const __grid_consta
         return resident && j < kResident ? reinterpret_cast<const float *>(dyn + j * kSlotBytes)
                                          : nullptr;
     };
-    int j = 0;
-    for (uint32_t it = blockIdx.x; it < nitems; it += gridDim.x, ++j) {
-        if (resident && j < kResident &&
-            !mbar_wait(&slot_full[j], 0u, &wait_abort, a.status))
+    // the first phase that reads a resident chunk waits for its copy
+    auto slot_wait = [&](int j) {
+        if (resident && j < kResident && !mbar_wait(&slot_full[j], 0u, &wait_abort, a.status))
             abort_flag = 1u;  // a copy did not land in time: stop at the next barrier
-        hist_item(a.logits, a.ld, a.P, a.ws, vec, a.ws.items[it], slot_of(j), sh.hist);
+    };
+    int j = 0;
+    if (!a.hist_done) {
+        for (uint32_t it = blockIdx.x; it < nitems; it += gridDim.x, ++j) {
+            slot_wait(j);
+            hist_item(a.logits, a.ld, a.P, a.ws, vec, a.ws.items[it], slot_of(j), sh.hist);
+        }
+        if (!grid_sync(ctrl, a.status, &abort_flag))
+            return;
     }
-    if (!grid_sync(ctrl, a.status, &abort_flag))
-        return;
     j = 0;
-    for (uint32_t it = blockIdx.x; it < nitems; it += gridDim.x, ++j)
+    for (uint32_t it = blockIdx.x; it < nitems; it += gridDim.x, ++j) {
+        if (a.hist_done)
+            slot_wait(j);
         filter_item(a.logits, a.ld, a.k, a.P, a.ws, vec, a.ws.items[it], slot_of(j), sh.filter);
+    }
     if (!grid_sync(ctrl, a.status, &abort_flag))
         return;
     for (int row = blockIdx.x; row < a.R; row += gridDim.x)

@@ -29,15 +29,20 @@ class IndexerStep:
     reads only the candidate blocks; the top-k and slots are the same, the
     logits outside those tiles are left unwritten.  ``kv_from`` (another
     IndexerStep of the same case) shares its device K cache instead of
-    uploading a second copy."""
+    uploading a second copy.  ``fused_topk`` (paged, no candidate list) runs
+    the logits and the row top-k as one idx_paged_mqa_logits_topk call, the
+    logits kernel counting the top-k's first digit; its logits stage then
+    holds the top-k too."""
 
     def __init__(self, case, device="cuda", fused_mask: bool = True, num_ctas: int = 0,
-                 gather: bool = True, cand_topk: bool = True, kv_from=None):
+                 gather: bool = True, cand_topk: bool = True, kv_from=None,
+                 fused_topk: bool = False):
         self.case = case
         self.device = torch.device(device)
         self.fused_mask = fused_mask
         self.gather = gather
         self.cand_topk = bool(cand_topk and gather and fused_mask)
+        self.fused_topk = bool(fused_topk and isinstance(case, PagedCase) and case.cand is None)
         self.num_ctas = num_ctas
         d = self.device
         self.paged = isinstance(case, PagedCase)
@@ -85,7 +90,20 @@ class IndexerStep:
         """Marshal every call of the step once; run() only launches."""
         c = self.case
         self._logits_calls = []
-        if self.source:
+        fused = None
+        if self.fused_topk:
+            fused = B.prepare_paged_mqa_logits_topk(
+                self.q, self.q_scale, self.weights, self.pages, self.block_table,
+                self.context_lens, c.next_n, c.page_size, c.fmt, self.logits, c.width,
+                self.lengths, self.k_top, self.topk,
+                block_max=self.block_max if self.source else None,
+                block_size=c.source_block if self.source else 0, row_ks=self.row_ks,
+                ctx_per_row=c.ctx_per_row, num_ctas=self.num_ctas)
+            self._logits_calls.append(fused)
+            self._slots_call = B.prepare_topk_to_ragged_slots(
+                self.topk, self.block_table, c.page_size, c.num_pages, self.slots, self.indptr,
+                self.lens, next_n=c.next_n, max_blocks=self.max_blocks)
+        elif self.source:
             self._logits_calls.append(B.prepare_paged_mqa_logits_block_max(
                 self.q, self.q_scale, self.weights, self.pages, self.block_table,
                 self.context_lens, c.next_n, c.page_size, c.fmt, self.logits, c.width,
@@ -117,6 +135,8 @@ class IndexerStep:
             self._topk_call = B.prepare_topk_candidates(
                 self.logits, self.lengths, self.k_top, self.topk, self.cand, c.cand_block,
                 row_ks=self.row_ks)
+        elif fused is not None:
+            self._topk_call = None  # inside the fused logits call
         else:
             self._topk_call = B.prepare_topk(self.logits, self.lengths, self.k_top, self.topk)
         # the candidate pool: the best blocks of each row, from the block maxima
@@ -129,7 +149,8 @@ class IndexerStep:
             call(stream)
 
     def topk_stage(self, stream=None):
-        self._topk_call(stream)
+        if self._topk_call is not None:
+            self._topk_call(stream)
         if self._pool_call is not None:
             self._pool_call(stream)
 
@@ -147,7 +168,7 @@ class IndexerStep:
         """A second buffer set for the same case, sharing the K cache."""
         return IndexerStep(self.case, device=self.device, fused_mask=self.fused_mask,
                            num_ctas=self.num_ctas, gather=self.gather,
-                           cand_topk=self.cand_topk, kv_from=self)
+                           cand_topk=self.cand_topk, kv_from=self, fused_topk=self.fused_topk)
 
     def input_names(self):
         """The per-step inputs a caller copies in (the K cache is state)."""
@@ -163,7 +184,7 @@ class IndexerStep:
 
     @property
     def launches_per_step(self) -> int:
-        calls = self._logits_calls + [self._topk_call]
+        calls = self._logits_calls + ([self._topk_call] if self._topk_call is not None else [])
         if self._pool_call is not None:
             calls.append(self._pool_call)
         if self._slots_call is not None:

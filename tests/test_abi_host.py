@@ -101,6 +101,29 @@ def test_block_max_argument_checks():
     assert call(B=0) == 0
 
 
+def test_logits_topk_argument_checks():
+    f = B.lib().idx_paged_mqa_logits_topk
+    # q, q_scale, w, pages, stride, npages, bt, bt_stride, ctx, ctx_per_row, row_ks, B,
+    # next_n, H, D, P, fmt, logits, ld, mml, block_max, ld_bmax, block, lengths, k,
+    # out_idx, ld_out, num_ctas, ws, ws_bytes, stream
+    base = [FAKE, None, FAKE, FAKE, 8448, 10, FAKE, 1024, FAKE, 0, None, 2, 1, 64, 128, 64, 0,
+            FAKE, 65536, 65536, None, 0, 0, FAKE, 2048, FAKE, 2048, 0, FAKE, 1 << 20, None]
+
+    def call(**kw):
+        a = list(base)
+        idx = dict(B=11, next_n=12, ld=18, lengths=23, k=24, out=25, ld_out=26)
+        for k, v in kw.items():
+            a[idx[k]] = v
+        return f(*a)
+    assert call(k=-1) == INVALID
+    assert call(ld_out=2047) == INVALID          # fewer columns than k
+    assert call(lengths=None) == INVALID
+    assert call(out=None) == INVALID
+    assert call(next_n=0) == INVALID
+    assert call(ld=0) == INVALID
+    assert call(B=0) == 0
+
+
 def test_producer_argument_checks():
     L = B.lib()
     k = L.idx_k_norm_rope_store
