@@ -8,6 +8,7 @@
 #include "idx_internal.h"
 #include "idx_topk.cuh"
 #include "idx_topk_chunked.cuh"
+#include "idx_topk_short.cuh"
 #include "idx_topk_cand.cuh"
 
 namespace idx {
@@ -299,6 +300,16 @@ idx_status topk_launch_per_row(const float *logits, int64_t ld, int rows,
     return launch_status(cudaGetLastError());
 }
 
+// Rows of at most 8192 keys: one 256-thread CTA per row, keys in registers.
+idx_status topk_launch_short(const float *logits, int64_t ld, int rows, const int32_t *lengths,
+                             int k, int32_t *out, int64_t ld_out, int vec_ok, cudaStream_t s)
+{
+    namespace T = topk_short;
+    T::topk_short_kernel<<<rows, T::kThreads, 0, s>>>(logits, ld, rows, lengths, k, out, ld_out,
+                                                      vec_ok);
+    return launch_status(cudaGetLastError());
+}
+
 } // namespace
 
 // Resident phase CTAs per SM of the chunked top-k on the current device
@@ -467,6 +478,8 @@ extern "C" idx_status idx_topk(const float *logits, int64_t ld, int rows, const 
         return IDX_ERR_INVALID_ARG;
     const int vec_ok = (ld % 4 == 0) && aligned16(logits);
     cudaStream_t s = (cudaStream_t)stream;
+    if (ld <= topk_short::kMaxLen)
+        return topk_launch_short(logits, ld, rows, lengths, k, out_idx, ld_out, vec_ok, s);
     const size_t need = idx_topk_workspace_size(rows, ld, k);
     if (ws && need > 0 && ws_bytes >= need && aligned16(ws) && ld > topk_chunked::kCh) {
         const idx_status st =
@@ -630,6 +643,9 @@ extern "C" idx_status idx_topk_noalloc(const float *logits, int64_t ld, int rows
         return IDX_OK;
     if (!logits || !lengths || !out_idx || ld <= 0)
         return IDX_ERR_INVALID_ARG;
+    if (ld <= topk_short::kMaxLen)  // short rows need no scratch
+        return topk_launch_short(logits, ld, rows, lengths, k, out_idx, ld_out,
+                                 (ld % 4 == 0) && aligned16(logits), (cudaStream_t)stream);
     const size_t need = idx_topk_workspace_size(rows, ld, k);
     if (need == 0)
         return IDX_ERR_UNSUPPORTED;

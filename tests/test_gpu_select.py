@@ -69,6 +69,29 @@ def test_topk_candidate_overflow(workspace):
     assert_topk_exact(got, oracle.topk(x, lengths, k))
 
 
+@pytest.mark.parametrize("width", [8192, 8191, 4099, 130])
+@pytest.mark.parametrize("kind", ["ties1", "ties3", "narrow", "normal"])
+def test_topk_short_rows(width, kind):
+    """Rows of at most 8192 keys (held in registers by the short-row
+    kernel): exact ties, three tie levels, values packed into one digit-1
+    bin, k above the row's finite count, empty rows, lengths past the row."""
+    rng = np.random.default_rng(width + len(kind))
+    rows = 37
+    if kind == "ties1":
+        x = _random_logits(rng, rows, width, tie_levels=1, neg_inf_frac=0.02)
+    elif kind == "ties3":
+        x = _random_logits(rng, rows, width, tie_levels=3, neg_inf_frac=0.02)
+    elif kind == "narrow":
+        x = (1.0 + rng.random((rows, width)) * 1e-4).astype(np.float32)
+    else:
+        x = _random_logits(rng, rows, width)
+    lengths = rng.integers(0, width + 1, size=rows)
+    lengths[0], lengths[1], lengths[2], lengths[3] = width, 0, 5, width + 100
+    for k in (2048, 1, width):
+        got = gpu_topk(x, lengths, k)
+        assert_topk_exact(got, oracle.topk(x, np.minimum(lengths, width), k))
+
+
 def test_topk_nonfinite_never_selected():
     rows, width, k = 4, 3000, 2048
     x = np.full((rows, width), -np.inf, np.float32)
