@@ -506,26 +506,14 @@ extern "C" idx_status idx_topk_candidates(const float *logits, int64_t ld, int r
         return IDX_ERR_INVALID_ARG;
     if (num_cand > T::kMaxIds || (long long)num_cand * block_size > T::kMaxKeys)
         return IDX_ERR_UNSUPPORTED;
-    const size_t smem = sizeof(T::Shared);
-    static int configured[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
-        return IDX_ERR_CUDA;
-    if (!configured[dev]) {
-        // two CTAs per SM need the largest shared-memory carveout
-        if (cudaFuncSetAttribute(T::topk_cand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem) != cudaSuccess ||
-            cudaFuncSetAttribute(T::topk_cand_kernel,
-                                 cudaFuncAttributePreferredSharedMemoryCarveout,
-                                 cudaSharedmemCarveoutMaxShared) != cudaSuccess)
-            return IDX_ERR_CUDA;
-        configured[dev] = 1;
-    }
     const int vec4 = ld % 4 == 0 && block_size % 4 == 0 && aligned16(logits);
-    return launch_status(launch_pdl(T::topk_cand_kernel, dim3(rows), dim3(T::kThreads), smem,
-                                    (cudaStream_t)stream, logits, ld, rows, lengths, row_ks,
-                                    candidate_blocks, cand_stride, num_cand, block_size,
-                                    row_repeat, k, out_idx, ld_out, vec4));
+    // register runs per thread: four up to 8192 candidate keys, else eight
+    const bool small = (long long)num_cand * block_size <= 4LL * T::kThreads * T::kStepsSmall;
+    auto kern = small ? T::topk_cand_kernel<T::kStepsSmall> : T::topk_cand_kernel<T::kStepsLarge>;
+    return launch_status(launch_pdl(kern, dim3(rows), dim3(T::kThreads), 0, (cudaStream_t)stream,
+                                    logits, ld, rows, lengths, row_ks, candidate_blocks,
+                                    cand_stride, num_cand, block_size, row_repeat, k, out_idx,
+                                    ld_out, vec4));
 }
 
 extern "C" idx_status idx_apply_candidate_mask(float *logits, int64_t ld, int rows, int width,

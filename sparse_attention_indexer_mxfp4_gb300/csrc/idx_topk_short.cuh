@@ -1,20 +1,21 @@
-// idx_topk_short.cuh -- per-row top-k for rows of at most 8192 keys, the
-// row's keys held in registers.
+// idx_topk_short.cuh -- top-k over keys held in registers: the per-row
+// top-k for rows of at most 8192 keys, and the selection core that the
+// candidate top-k (idx_topk_cand.cuh) shares.
 //
 // Passage: vLLM page rocm_paged_mxfp4_indexer, _topk -- top-k over each
 // row's [0, lengths[row]), -1 padding.  The design is our own.
 //
-// One CTA of 256 threads per row.  Thread t holds the keys of elements
-// 1024 s + 4 t + e (s < 8, e < 4), loaded once, so (s, warp, lane, e) is
-// index order and no pass reads the row again.  Radix select over the
-// order-preserving keys with 11/11/10-bit digits: a shared histogram per
-// digit (digits 2 and 3 count only the keys matching the digits found so
-// far), each followed by a descending bin search.  One counting pass then
-// fills (step, warp) tables of the keys above the k-th largest key T and of
-// the keys equal to it; two warps scan them, and the ordered write ranks
-// each key inside its warp and step by ballots.  Keys equal to T are taken
-// lowest index first.  Every phase is separated by CTA barriers only; no
-// thread waits on another CTA.
+// One CTA per row.  Thread t of NT holds KS runs of four keys, run s at
+// order positions 4 NT s + 4 t + e (e < 4), so (s, warp, lane, e) is the
+// order in which ties are broken and indices are written.  Radix select
+// over the order-preserving keys with 11/11/10-bit digits: a shared
+// histogram per digit (digits 2 and 3 count only the keys matching the
+// digits found so far), each followed by a descending bin search.  One
+// counting pass then fills (step, warp) tables of the keys above the k-th
+// largest key T and of the keys equal to it; two warps scan them, and the
+// ordered write ranks each key inside its warp and step by ballots.  Keys
+// equal to T are taken first in order.  Phases are separated by CTA
+// barriers only.
 #pragma once
 
 #include <cstdint>
@@ -22,15 +23,12 @@
 #include "idx_topk.cuh"
 
 namespace idx {
-namespace topk_short {
+namespace regsel {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
-constexpr int kSteps = 8;                     // float4 runs per thread
-constexpr int kMaxLen = kSteps * kThreads * 4;  // 8192
-constexpr int kTab = kSteps * kWarps;         // (step, warp) entries
-
+template <int NT, int KS>
 struct Shared {
+    static constexpr int kWarps = NT / 32;
+    static constexpr int kTab = KS * kWarps;  // (step, warp) entries
     uint32_t hist[2][2048];
     uint32_t wvalid[kWarps];
     uint32_t wbin[3][kWarps];
@@ -41,15 +39,17 @@ struct Shared {
 
 // Descending-bin search over h[nb] (nb = 2048 or 1024): the bin where the
 // count from the top reaches krem, and the rank left inside it, go to
-// sel[0..1].  Reads h and writes wbin/sel only; two barriers.
+// sel[0..1].  Reads h, writes wbin and sel only; two barriers.
+template <int NT>
 __device__ __forceinline__ void find_bin(const uint32_t *h, int nb, uint32_t krem,
                                          uint32_t *wbin, uint32_t *sel)
 {
+    constexpr int MAXPER = 2048 / NT;
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-    const int per = nb / kThreads;  // 8 or 4 bins per thread
-    uint32_t loc[8], lsum = 0;
+    const int per = nb / NT;
+    uint32_t loc[MAXPER], lsum = 0;
     #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < MAXPER; ++j) {
         loc[j] = j < per ? h[nb - 1 - (tid * per + j)] : 0u;
         lsum += loc[j];
     }
@@ -61,7 +61,7 @@ __device__ __forceinline__ void find_bin(const uint32_t *h, int nb, uint32_t kre
     for (int i = 0; i < w; ++i)
         before += wbin[i];
     #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < MAXPER; ++j) {
         if (j < per && before < krem && before + loc[j] >= krem) {
             sel[0] = (uint32_t)(nb - 1 - (tid * per + j));
             sel[1] = krem - before;
@@ -71,40 +71,47 @@ __device__ __forceinline__ void find_bin(const uint32_t *h, int nb, uint32_t kre
     __syncthreads();
 }
 
-// In-place exclusive scan of a kTab-entry table by one warp (two entries
-// per lane).
+// In-place exclusive scan of an N-entry table (N a multiple of 32) by one
+// warp.
+template <int N>
 __device__ __forceinline__ void scan_tab(uint32_t *tab, int lane)
 {
-    const uint32_t a = tab[2 * lane], b = tab[2 * lane + 1];
+    constexpr int E = N / 32;
+    uint32_t v[E], sum = 0;
+    #pragma unroll
+    for (int e = 0; e < E; ++e) {
+        v[e] = tab[E * lane + e];
+        sum += v[e];
+    }
     uint32_t tot;
-    const uint32_t ex = topk_detail::warp_excl(a + b, lane, &tot);
-    tab[2 * lane] = ex;
-    tab[2 * lane + 1] = ex + a;
+    uint32_t run = topk_detail::warp_excl(sum, lane, &tot);
+    #pragma unroll
+    for (int e = 0; e < E; ++e) {
+        tab[E * lane + e] = run;
+        run += v[e];
+    }
 }
 
-__global__ void __launch_bounds__(kThreads, 3)
-    topk_short_kernel(const float *__restrict__ logits, int64_t ld, int rows,
-                      const int32_t *__restrict__ lengths, int k, int32_t *__restrict__ out,
-                      int64_t ld_out, int vec_ok)
+// Selects the k largest nonzero keys of the CTA (ties first in order) and
+// writes index_of(s, e) of each at its rank in order to orow[0, k), -1
+// after the last.  key[s][e] is the thread's key at order position
+// 4 NT s + 4 tid + e; 0 marks an empty or non-finite entry.  Uses every
+// thread of the CTA; begins by clearing the histograms.
+template <int NT, int KS, class IndexOf>
+__device__ __forceinline__ void select_write(Shared<NT, KS> &sh, const uint32_t (&key)[KS][4],
+                                             int k, int32_t *orow, IndexOf index_of)
 {
-    static_assert(kTab == 64, "scan_tab covers 64 entries");
-    __shared__ __align__(16) Shared sh;
-    const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-    if (row >= rows)
-        return;
-    const int len = max(0, min(lengths[row], (int)ld));
-    const float *rowp = logits + (size_t)row * ld;
-
-    uint32_t key[kSteps][4];
-    topk_detail::load_keys<kSteps>(rowp, 4 * tid, 4 * kThreads, len, vec_ok != 0, key);
-    for (int i = tid; i < 2 * 2048; i += kThreads)
+    using S = Shared<NT, KS>;
+    static_assert(S::kTab % 32 == 0, "tables are scanned 32 lanes wide");
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    for (int i = tid; i < 2 * 2048; i += NT)
         (&sh.hist[0][0])[i] = 0u;
     __syncthreads();
 
     // digit 1 (top 11 bits) and the number of finite keys
     uint32_t nvalid = 0;
     #pragma unroll
-    for (int s = 0; s < kSteps; ++s)
+    for (int s = 0; s < KS; ++s)
         #pragma unroll
         for (int e = 0; e < 4; ++e)
             if (key[s][e]) {
@@ -117,39 +124,39 @@ __global__ void __launch_bounds__(kThreads, 3)
     __syncthreads();
     uint32_t total = 0;
     #pragma unroll
-    for (int i = 0; i < kWarps; ++i)
+    for (int i = 0; i < S::kWarps; ++i)
         total += sh.wvalid[i];
 
     // T: the k-th largest key (0 when every finite key is taken); ties: how
     // many keys equal to T are taken
     uint32_t T = 0u, ties = 0u;
     if (total > (uint32_t)k) {
-        find_bin(sh.hist[0], 2048, (uint32_t)k, sh.wbin[0], sh.sel[0]);
+        find_bin<NT>(sh.hist[0], 2048, (uint32_t)k, sh.wbin[0], sh.sel[0]);
         const uint32_t b1 = sh.sel[0][0];
         uint32_t krem = sh.sel[0][1];
         // digit 2 (next 11 bits) of the keys in bin b1; digit 1's histogram
         // is cleared meanwhile for digit 3
-        for (int i = tid; i < 1024; i += kThreads)
+        for (int i = tid; i < 1024; i += NT)
             sh.hist[0][i] = 0u;
         #pragma unroll
-        for (int s = 0; s < kSteps; ++s)
+        for (int s = 0; s < KS; ++s)
             #pragma unroll
             for (int e = 0; e < 4; ++e)
                 if (key[s][e] >> 21 == b1)
                     atomicAdd(&sh.hist[1][(key[s][e] >> 10) & 2047u], 1u);
         __syncthreads();
-        find_bin(sh.hist[1], 2048, krem, sh.wbin[1], sh.sel[1]);
+        find_bin<NT>(sh.hist[1], 2048, krem, sh.wbin[1], sh.sel[1]);
         const uint32_t p2 = (b1 << 11) | sh.sel[1][0];  // the top 22 bits of T
         krem = sh.sel[1][1];
         // digit 3 (low 10 bits) of the keys matching the top 22 bits
         #pragma unroll
-        for (int s = 0; s < kSteps; ++s)
+        for (int s = 0; s < KS; ++s)
             #pragma unroll
             for (int e = 0; e < 4; ++e)
                 if (key[s][e] >> 10 == p2)
                     atomicAdd(&sh.hist[0][key[s][e] & 1023u], 1u);
         __syncthreads();
-        find_bin(sh.hist[0], 1024, krem, sh.wbin[2], sh.sel[2]);
+        find_bin<NT>(sh.hist[0], 1024, krem, sh.wbin[2], sh.sel[2]);
         T = (p2 << 10) | sh.sel[2][0];
         ties = sh.sel[2][1];
     }
@@ -157,7 +164,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     // counts of keys above and equal to T per (step, warp)
     const uint32_t lt = (1u << lane) - 1u;
     #pragma unroll
-    for (int s = 0; s < kSteps; ++s) {
+    for (int s = 0; s < KS; ++s) {
         uint32_t ngt = 0, neq = 0;
         #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -167,32 +174,28 @@ __global__ void __launch_bounds__(kThreads, 3)
         ngt = __reduce_add_sync(0xffffffffu, ngt);
         neq = __reduce_add_sync(0xffffffffu, neq);
         if (lane == 0) {
-            sh.gt[s * kWarps + w] = ngt;
-            sh.eq[s * kWarps + w] = neq;
+            sh.gt[s * S::kWarps + w] = ngt;
+            sh.eq[s * S::kWarps + w] = neq;
         }
     }
     __syncthreads();
     if (w == 0)
-        scan_tab(sh.gt, lane);
+        scan_tab<S::kTab>(sh.gt, lane);
     else if (w == 1)
-        scan_tab(sh.eq, lane);
+        scan_tab<S::kTab>(sh.eq, lane);
     __syncthreads();
 
-    // ordered write: the keys of (step, warp) start at the keys above T
-    // before it plus the keys equal to T taken before it
-    int32_t *orow = out + (size_t)row * ld_out;
+    // ordered write: the keys of (step, warp) start after the keys above T
+    // before it and the keys equal to T taken before it
     #pragma unroll
-    for (int s = 0; s < kSteps; ++s) {
-        const uint32_t eq0 = sh.eq[s * kWarps + w];
-        uint32_t beq[4], mine_eq = 0;
-        #pragma unroll
-        for (int e = 0; e < 4; ++e)
-            beq[e] = __ballot_sync(0xffffffffu, key[s][e] == T);
+    for (int s = 0; s < KS; ++s) {
+        const uint32_t eq0 = sh.eq[s * S::kWarps + w];
         uint32_t eq_below = 0;
         #pragma unroll
         for (int e = 0; e < 4; ++e)
-            eq_below += __popc(beq[e] & lt);
+            eq_below += __popc(__ballot_sync(0xffffffffu, key[s][e] == T) & lt);
         bool tk[4];
+        uint32_t mine_eq = 0;
         #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const bool is_eq = key[s][e] == T;
@@ -203,15 +206,42 @@ __global__ void __launch_bounds__(kThreads, 3)
         #pragma unroll
         for (int e = 0; e < 4; ++e)
             tk_below += __popc(__ballot_sync(0xffffffffu, tk[e]) & lt);
-        uint32_t pos = sh.gt[s * kWarps + w] + min(eq0, ties) + tk_below;
+        uint32_t pos = sh.gt[s * S::kWarps + w] + min(eq0, ties) + tk_below;
         #pragma unroll
         for (int e = 0; e < 4; ++e)
             if (tk[e])
-                orow[pos++] = s * 4 * kThreads + 4 * tid + e;
+                orow[pos++] = index_of(s, e);
     }
     const int nsel = (int)min(total, (uint32_t)k);
-    for (int j = nsel + tid; j < k; j += kThreads)
+    for (int j = nsel + tid; j < k; j += NT)
         orow[j] = -1;
+}
+
+} // namespace regsel
+
+namespace topk_short {
+
+constexpr int kThreads = 256;
+constexpr int kSteps = 8;                       // runs of four keys per thread
+constexpr int kMaxLen = kSteps * kThreads * 4;  // 8192
+
+// Rows of at most 8192 keys; thread t holds elements 1024 s + 4 t + e.
+__global__ void __launch_bounds__(kThreads, 3)
+    topk_short_kernel(const float *__restrict__ logits, int64_t ld, int rows,
+                      const int32_t *__restrict__ lengths, int k, int32_t *__restrict__ out,
+                      int64_t ld_out, int vec_ok)
+{
+    __shared__ __align__(16) regsel::Shared<kThreads, kSteps> sh;
+    const int row = blockIdx.x, tid = threadIdx.x;
+    if (row >= rows)
+        return;
+    const int len = max(0, min(lengths[row], (int)ld));
+    uint32_t key[kSteps][4];
+    topk_detail::load_keys<kSteps>(logits + (size_t)row * ld, 4 * tid, 4 * kThreads, len,
+                                   vec_ok != 0, key);
+    regsel::select_write<kThreads, kSteps>(
+        sh, key, k, out + (size_t)row * ld_out,
+        [&](int s, int e) -> int32_t { return s * 4 * kThreads + 4 * tid + e; });
 }
 
 } // namespace topk_short
