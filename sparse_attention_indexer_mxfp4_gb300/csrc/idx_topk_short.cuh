@@ -14,7 +14,8 @@
 // counting pass then fills (step, warp) tables of the keys above the k-th
 // largest key T and of the keys equal to it; two warps scan them, and the
 // ordered write ranks each key inside its warp and step by ballots.  Keys
-// equal to T are taken first in order.  Phases are separated by CTA
+// equal to T are taken first in order.  When every key equal to T is taken
+// (the usual case) one table of the keys at or above T serves instead.  Phases are separated by CTA
 // barriers only.
 #pragma once
 
@@ -104,8 +105,8 @@ __device__ __forceinline__ void select_write(Shared<NT, KS> &sh, const uint32_t 
     using S = Shared<NT, KS>;
     static_assert(S::kTab % 32 == 0, "tables are scanned 32 lanes wide");
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-    for (int i = tid; i < 2 * 2048; i += NT)
-        (&sh.hist[0][0])[i] = 0u;
+    for (int i = tid; i < 2 * 2048 / 4; i += NT)
+        reinterpret_cast<uint4 *>(&sh.hist[0][0])[i] = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
 
     // digit 1 (top 11 bits) and the number of finite keys
@@ -130,14 +131,15 @@ __device__ __forceinline__ void select_write(Shared<NT, KS> &sh, const uint32_t 
     // T: the k-th largest key (0 when every finite key is taken); ties: how
     // many keys equal to T are taken
     uint32_t T = 0u, ties = 0u;
+    bool all_ties = true;  // every key equal to T is taken
     if (total > (uint32_t)k) {
         find_bin<NT>(sh.hist[0], 2048, (uint32_t)k, sh.wbin[0], sh.sel[0]);
         const uint32_t b1 = sh.sel[0][0];
         uint32_t krem = sh.sel[0][1];
         // digit 2 (next 11 bits) of the keys in bin b1; digit 1's histogram
         // is cleared meanwhile for digit 3
-        for (int i = tid; i < 1024; i += NT)
-            sh.hist[0][i] = 0u;
+        for (int i = tid; i < 1024 / 4; i += NT)
+            reinterpret_cast<uint4 *>(sh.hist[0])[i] = make_uint4(0u, 0u, 0u, 0u);
         #pragma unroll
         for (int s = 0; s < KS; ++s)
             #pragma unroll
@@ -159,10 +161,50 @@ __device__ __forceinline__ void select_write(Shared<NT, KS> &sh, const uint32_t 
         find_bin<NT>(sh.hist[0], 1024, krem, sh.wbin[2], sh.sel[2]);
         T = (p2 << 10) | sh.sel[2][0];
         ties = sh.sel[2][1];
+        all_ties = ties == sh.hist[0][T & 1023u];  // the keys equal to T
+    }
+    const uint32_t lt = (1u << lane) - 1u;
+
+    if (all_ties) {
+        // every key at or above tmin is taken (tmin = 1 when every finite
+        // key is): one table of taken counts per (step, warp)
+        const uint32_t tmin = T == 0u ? 1u : T;
+        #pragma unroll
+        for (int s = 0; s < KS; ++s) {
+            uint32_t n = 0;
+            #pragma unroll
+            for (int e = 0; e < 4; ++e)
+                n += key[s][e] >= tmin;
+            n = __reduce_add_sync(0xffffffffu, n);
+            if (lane == 0)
+                sh.gt[s * S::kWarps + w] = n;
+        }
+        __syncthreads();
+        if (w == 0)
+            scan_tab<S::kTab>(sh.gt, lane);
+        __syncthreads();
+        #pragma unroll
+        for (int s = 0; s < KS; ++s) {
+            bool tk[4];
+            uint32_t tk_below = 0;
+            #pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                tk[e] = key[s][e] >= tmin;
+                tk_below += __popc(__ballot_sync(0xffffffffu, tk[e]) & lt);
+            }
+            uint32_t pos = sh.gt[s * S::kWarps + w] + tk_below;
+            #pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (tk[e])
+                    orow[pos++] = index_of(s, e);
+        }
+        const int nsel = (int)min(total, (uint32_t)k);
+        for (int j = nsel + tid; j < k; j += NT)
+            orow[j] = -1;
+        return;
     }
 
     // counts of keys above and equal to T per (step, warp)
-    const uint32_t lt = (1u << lane) - 1u;
     #pragma unroll
     for (int s = 0; s < KS; ++s) {
         uint32_t ngt = 0, neq = 0;
