@@ -262,18 +262,24 @@ idx_status idx_apply_candidate_mask(float *logits, int64_t ld, int rows, int wid
  *           selected.  Among equal values at the k-th place the lower indices
  *           win, so the selected set is unique.
  *   k >= 0 (k == 0 writes nothing).  ld <= INT32_MAX.
- *   ws, ws_bytes  optional caller-owned device scratch, 16-byte aligned.
- *           With ws_bytes >= idx_topk_workspace_size(rows, ld, k) and
- *           ld > 8192, each row is cut into chunks of 8192 keys and the
- *           selection runs over the whole GPU as two launches: a plan
- *           kernel that clears the part of ws that must start at zero, then
- *           one cooperative launch whose phases meet at grid barriers (each
- *           wait is bounded; a timeout sets IDX_DEV_TIMEOUT in the device
- *           status and leaves the output undefined).
- *           Otherwise (ws NULL or too small) one CTA selects each row.  Both
- *           give the same indices.  Calls that share one ws must not overlap
- *           in time (same stream, or ordered by events); ws holds nothing
- *           the caller needs after the call.
+ *   The launch depends on ld alone (one launch unless noted):
+ *           ld <= 8192: one CTA of 256 threads per row, the row's keys in
+ *           registers.  ld <= 262144: one thread-block cluster of
+ *           ceil(ld / 32768) CTAs per row, each CTA holding 32768 keys in
+ *           shared memory and reading the others' histograms through
+ *           distributed shared memory (when the device cannot hold such a
+ *           cluster, the rules for longer rows apply).  Longer rows: with
+ *           ws, chunks of 8192 keys over the whole GPU in two launches (a
+ *           plan kernel that clears the part of ws that must start at zero,
+ *           then one cooperative launch whose phases meet at grid barriers;
+ *           each wait is bounded, a timeout sets IDX_DEV_TIMEOUT in the
+ *           device status and leaves the output undefined); without ws one
+ *           CTA streams each row.  Every path gives the same indices.
+ *   ws, ws_bytes  optional caller-owned device scratch, 16-byte aligned,
+ *           used only by the chunked path (ws_bytes >=
+ *           idx_topk_workspace_size(rows, ld, k)).  Calls that share one ws
+ *           must not overlap in time (same stream, or ordered by events); ws
+ *           holds nothing the caller needs after the call.
  * Errors: IDX_ERR_INVALID_ARG for negative sizes, ld_out < k or NULL
  *   pointers; IDX_ERR_CUDA when a launch fails.
  * ---------------------------------------------------------------------- */
@@ -296,8 +302,9 @@ size_t idx_topk_workspace_size(int rows, int64_t ld, int k);
  * a latency-critical loop where cudaMalloc / cudaFree may synchronise the
  * device, or a plain C caller with no device allocator of its own.
  *
- *   Same arguments and results as idx_topk, always on the chunked path.
- *   Its scratch is one fixed array of IDX_TOPK_NOALLOC_MAX_BYTES per device,
+ *   Same arguments and results as idx_topk.  Rows of up to 262144 keys take
+ *   idx_topk's scratch-free paths; longer rows the chunked path, whose
+ *   scratch is one fixed array of IDX_TOPK_NOALLOC_MAX_BYTES per device,
  *   part of the library's device image: the call allocates nothing.  The
  *   first call on a device looks up that array's address (with the device
  *   current); make that first call before any stream capture on the device.
@@ -305,9 +312,9 @@ size_t idx_topk_workspace_size(int rows, int64_t ld, int k);
  *   first kernel, on `stream`) before the others run.
  *   Calls on one device share the array: two calls that overlap in time
  *   (different streams, not ordered by events) race and give wrong indices.
- * Errors: as idx_topk; IDX_ERR_WORKSPACE when
+ * Errors: as idx_topk; on the chunked path IDX_ERR_WORKSPACE when
  *   idx_topk_workspace_size(rows, ld, k) > IDX_TOPK_NOALLOC_MAX_BYTES (about
- *   450 rows of 131072 keys), IDX_ERR_UNSUPPORTED when it is 0 for rows > 0
+ *   450 rows), IDX_ERR_UNSUPPORTED when it is 0 for rows > 0
  *   (ld above 8192 * 1024); IDX_ERR_CUDA when the address lookup or a launch
  *   fails.
  * ---------------------------------------------------------------------- */

@@ -26,6 +26,7 @@ DEV_BAD_PAGE = 1
 DEV_TIMEOUT = 4
 DEV_BAD_POSITION = 8
 SLOT_DIRECT_ROWS = 4096  # above it the slot map runs a third (scan) kernel
+TOPK_CLUSTER_MAX_LEN = 262144  # rows the one-cluster-per-row top-k holds (8 x 32768 keys)
 
 _lib = None
 _lock = threading.Lock()
@@ -343,9 +344,10 @@ def prepare_topk(logits, lengths, k, out, workspace=True):
         ws = workspace
     nbytes = 0 if ws is None else ws.numel() * ws.element_size()
     args = (_ptr(logits), ld, rows, _ptr(lengths), k, _ptr(out), out.stride(0), _ptr(ws), nbytes)
-    # the library takes the chunked path (two kernels) under these conditions
+    # rows of up to TOPK_CLUSTER_MAX_LEN keys take one kernel (a CTA or a
+    # cluster per row); longer rows with scratch the chunked path (two kernels)
     need = topk_workspace_size(rows, ld, k)
-    chunked = ws is not None and need > 0 and nbytes >= need and ld > 8192
+    chunked = ws is not None and need > 0 and nbytes >= need and ld > TOPK_CLUSTER_MAX_LEN
     return Prepared("idx_topk", args, (logits, lengths, out, ws), 2 if chunked else 1)
 
 

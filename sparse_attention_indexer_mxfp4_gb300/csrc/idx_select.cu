@@ -8,6 +8,7 @@
 #include "idx_internal.h"
 #include "idx_topk.cuh"
 #include "idx_topk_chunked.cuh"
+#include "idx_topk_cluster.cuh"
 #include "idx_topk_short.cuh"
 #include "idx_topk_cand.cuh"
 
@@ -310,6 +311,53 @@ idx_status topk_launch_short(const float *logits, int64_t ld, int rows, const in
     return launch_status(cudaGetLastError());
 }
 
+// Rows of up to 262144 keys: one cluster of ceil(ld / 32768) CTAs per row.
+// IDX_ERR_UNSUPPORTED when no such cluster can be resident on the device.
+idx_status topk_launch_cluster(const float *logits, int64_t ld, int rows, const int32_t *lengths,
+                               int k, int32_t *out, int64_t ld_out, int vec_ok, cudaStream_t s)
+{
+    namespace T = topk_cluster;
+    const int C = (int)((ld + T::kChunk - 1) / T::kChunk);
+    if (C < 1 || C > T::kMaxCluster || (long long)rows * C > INT32_MAX)
+        return IDX_ERR_UNSUPPORTED;
+    const size_t smem = sizeof(T::Shared);
+    static int configured[64] = {};
+    static int resident[64][T::kMaxCluster + 1] = {};  // 0 unknown, 1 yes, -1 no
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return IDX_ERR_CUDA;
+    if (!configured[dev]) {
+        if (cudaFuncSetAttribute(T::topk_cluster_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem) != cudaSuccess)
+            return IDX_ERR_CUDA;
+        configured[dev] = 1;
+    }
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(rows * C));
+    cfg.blockDim = dim3(T::kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (!resident[dev][C]) {
+        int n = 0;
+        const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, T::topk_cluster_kernel, &cfg);
+        if (e != cudaSuccess)
+            (void)cudaGetLastError();
+        resident[dev][C] = e == cudaSuccess && n > 0 ? 1 : -1;
+    }
+    if (resident[dev][C] < 0)
+        return IDX_ERR_UNSUPPORTED;
+    return launch_status(cudaLaunchKernelEx(&cfg, T::topk_cluster_kernel, logits, ld, rows,
+                                            lengths, k, out, ld_out, vec_ok));
+}
+
 } // namespace
 
 // Resident phase CTAs per SM of the chunked top-k on the current device
@@ -480,6 +528,12 @@ extern "C" idx_status idx_topk(const float *logits, int64_t ld, int rows, const 
     cudaStream_t s = (cudaStream_t)stream;
     if (ld <= topk_short::kMaxLen)
         return topk_launch_short(logits, ld, rows, lengths, k, out_idx, ld_out, vec_ok, s);
+    if (ld <= topk_cluster::kMaxLen) {
+        const idx_status st =
+            topk_launch_cluster(logits, ld, rows, lengths, k, out_idx, ld_out, vec_ok, s);
+        if (st != IDX_ERR_UNSUPPORTED)
+            return st;
+    }
     const size_t need = idx_topk_workspace_size(rows, ld, k);
     if (ws && need > 0 && ws_bytes >= need && aligned16(ws) && ld > topk_chunked::kCh) {
         const idx_status st =
@@ -631,9 +685,16 @@ extern "C" idx_status idx_topk_noalloc(const float *logits, int64_t ld, int rows
         return IDX_OK;
     if (!logits || !lengths || !out_idx || ld <= 0)
         return IDX_ERR_INVALID_ARG;
-    if (ld <= topk_short::kMaxLen)  // short rows need no scratch
-        return topk_launch_short(logits, ld, rows, lengths, k, out_idx, ld_out,
-                                 (ld % 4 == 0) && aligned16(logits), (cudaStream_t)stream);
+    const int vec = (ld % 4 == 0) && aligned16(logits);
+    if (ld <= topk_short::kMaxLen)  // rows a CTA or a cluster holds need no scratch
+        return topk_launch_short(logits, ld, rows, lengths, k, out_idx, ld_out, vec,
+                                 (cudaStream_t)stream);
+    if (ld <= topk_cluster::kMaxLen) {
+        const idx_status st = topk_launch_cluster(logits, ld, rows, lengths, k, out_idx, ld_out,
+                                                  vec, (cudaStream_t)stream);
+        if (st != IDX_ERR_UNSUPPORTED)
+            return st;
+    }
     const size_t need = idx_topk_workspace_size(rows, ld, k);
     if (need == 0)
         return IDX_ERR_UNSUPPORTED;

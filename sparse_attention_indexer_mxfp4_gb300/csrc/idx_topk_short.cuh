@@ -73,9 +73,9 @@ __device__ __forceinline__ void find_bin(const uint32_t *h, int nb, uint32_t kre
 }
 
 // In-place exclusive scan of an N-entry table (N a multiple of 32) by one
-// warp.
+// warp; returns the table's total.
 template <int N>
-__device__ __forceinline__ void scan_tab(uint32_t *tab, int lane)
+__device__ __forceinline__ uint32_t scan_tab(uint32_t *tab, int lane)
 {
     constexpr int E = N / 32;
     uint32_t v[E], sum = 0;
@@ -91,6 +91,7 @@ __device__ __forceinline__ void scan_tab(uint32_t *tab, int lane)
         tab[E * lane + e] = run;
         run += v[e];
     }
+    return tot;
 }
 
 // Selects the k largest nonzero keys of the CTA (ties first in order) and

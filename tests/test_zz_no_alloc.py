@@ -15,7 +15,7 @@ FAKE = 0x10000  # never dereferenced: these calls fail their host checks first
 
 def test_noalloc_rejects_calls_beyond_the_array():
     f = B.lib().idx_topk_noalloc
-    ld, k = 131072, 2048
+    ld, k = B.TOPK_CLUSTER_MAX_LEN + 4, 2048  # rows past the cluster path use the array
     too_many = next(r for r in range(1, 4096) if B.topk_workspace_size(r, ld, k) > (32 << 20))
     assert B.topk_workspace_size(too_many - 1, ld, k) <= (32 << 20)
     assert f(FAKE, ld, too_many, FAKE, k, FAKE, k, None) == WORKSPACE
@@ -40,7 +40,8 @@ def test_noalloc_matches_idx_topk_on_two_calls_in_a_row():
     rng = np.random.default_rng(2024)
     # a long-row decode batch, then a smaller one with heavy ties: the second
     # call must not see anything the first left in the shared array
-    cases = [(_case(rng, 96, 131072), 2048), (_case(rng, 7, 20000, tie_levels=3), 300)]
+    cases = [(_case(rng, 96, 131072), 2048), (_case(rng, 7, 20000, tie_levels=3), 300),
+             (_case(rng, 5, 300000), 2048)]
     got = []
     for (x, lengths), k in cases:
         out = torch.full((x.shape[0], k), -7, dtype=torch.int32, device="cuda")
