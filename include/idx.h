@@ -264,11 +264,12 @@ idx_status idx_apply_candidate_mask(float *logits, int64_t ld, int rows, int wid
  *   k >= 0 (k == 0 writes nothing).  ld <= INT32_MAX.
  *   The launch depends on ld alone (one launch unless noted):
  *           ld <= 8192: one CTA of 256 threads per row, the row's keys in
- *           registers.  ld <= 262144: one thread-block cluster of
- *           ceil(ld / 32768) CTAs per row, each CTA holding 32768 keys in
- *           shared memory and reading the others' histograms through
- *           distributed shared memory (when the device cannot hold such a
- *           cluster, the rules for longer rows apply).  Longer rows: with
+ *           registers.  ld <= 262144 and rows * ceil(ld / 32768) at most
+ *           the number of SMs: one thread-block cluster of ceil(ld / 32768)
+ *           CTAs per row, each CTA holding 32768 keys in shared memory and
+ *           reading the others' histograms through distributed shared
+ *           memory (when the device cannot hold such a cluster, the rules
+ *           for longer rows apply).  Otherwise (more or longer rows): with
  *           ws, chunks of 8192 keys over the whole GPU in two launches (a
  *           plan kernel that clears the part of ws that must start at zero,
  *           then one cooperative launch whose phases meet at grid barriers;
@@ -302,9 +303,10 @@ size_t idx_topk_workspace_size(int rows, int64_t ld, int k);
  * a latency-critical loop where cudaMalloc / cudaFree may synchronise the
  * device, or a plain C caller with no device allocator of its own.
  *
- *   Same arguments and results as idx_topk.  Rows of up to 262144 keys take
- *   idx_topk's scratch-free paths; longer rows the chunked path, whose
- *   scratch is one fixed array of IDX_TOPK_NOALLOC_MAX_BYTES per device,
+ *   Same arguments and results as idx_topk.  Calls that idx_topk serves
+ *   with one CTA or one cluster per row take those scratch-free paths; the
+ *   others the chunked path, whose scratch is one fixed array of
+ *   IDX_TOPK_NOALLOC_MAX_BYTES per device,
  *   part of the library's device image: the call allocates nothing.  The
  *   first call on a device looks up that array's address (with the device
  *   current); make that first call before any stream capture on the device.

@@ -325,6 +325,10 @@ def topk_workspace_size(rows, ld, k) -> int:
     return int(lib().idx_topk_workspace_size(rows, ld, k))
 
 
+def _sm_count(device) -> int:
+    return torch.cuda.get_device_properties(device).multi_processor_count
+
+
 def prepare_topk(logits, lengths, k, out, workspace=True):
     """workspace: True allocates the scratch for the chunked path once here
     (held by the returned call), a uint8 CUDA tensor supplies it, False or
@@ -344,10 +348,13 @@ def prepare_topk(logits, lengths, k, out, workspace=True):
         ws = workspace
     nbytes = 0 if ws is None else ws.numel() * ws.element_size()
     args = (_ptr(logits), ld, rows, _ptr(lengths), k, _ptr(out), out.stride(0), _ptr(ws), nbytes)
-    # rows of up to TOPK_CLUSTER_MAX_LEN keys take one kernel (a CTA or a
-    # cluster per row); longer rows with scratch the chunked path (two kernels)
+    # one kernel for rows of up to 8192 keys (a CTA per row) and for rows of
+    # up to TOPK_CLUSTER_MAX_LEN keys whose clusters fit the GPU in one wave;
+    # otherwise, with scratch, the chunked path (two kernels)
     need = topk_workspace_size(rows, ld, k)
-    chunked = ws is not None and need > 0 and nbytes >= need and ld > TOPK_CLUSTER_MAX_LEN
+    clusters = -(-ld // 32768) if ld <= TOPK_CLUSTER_MAX_LEN else 0
+    one_wave = ld <= 8192 or (clusters and rows * clusters <= _sm_count(logits.device))
+    chunked = ws is not None and need > 0 and nbytes >= need and not one_wave
     return Prepared("idx_topk", args, (logits, lengths, out, ws), 2 if chunked else 1)
 
 

@@ -311,14 +311,18 @@ idx_status topk_launch_short(const float *logits, int64_t ld, int rows, const in
     return launch_status(cudaGetLastError());
 }
 
-// Rows of up to 262144 keys: one cluster of ceil(ld / 32768) CTAs per row.
-// IDX_ERR_UNSUPPORTED when no such cluster can be resident on the device.
+// Rows of up to 262144 keys: one cluster of ceil(ld / 32768) CTAs per row,
+// when those CTAs (one per SM) fit the GPU in one wave: the clusters run
+// side by side and every row ends after one cluster's time.  More rows than
+// that are spread better over the GPU by the chunked path.
+// IDX_ERR_UNSUPPORTED when the call is outside that range or no such
+// cluster can be resident on the device.
 idx_status topk_launch_cluster(const float *logits, int64_t ld, int rows, const int32_t *lengths,
                                int k, int32_t *out, int64_t ld_out, int vec_ok, cudaStream_t s)
 {
     namespace T = topk_cluster;
     const int C = (int)((ld + T::kChunk - 1) / T::kChunk);
-    if (C < 1 || C > T::kMaxCluster || (long long)rows * C > INT32_MAX)
+    if (C < 1 || C > T::kMaxCluster || (long long)rows * C > sm_count())
         return IDX_ERR_UNSUPPORTED;
     const size_t smem = sizeof(T::Shared);
     static int configured[64] = {};

@@ -35,7 +35,7 @@ def _random_logits(rng, rows, width, tie_levels=None, neg_inf_frac=0.1):
 @pytest.mark.parametrize("rows,width,k", [
     (1, 1, 1), (3, 100, 7), (16, 1024, 256), (5, 1000, 2048), (64, 8192, 2048),
     (7, 65536, 2048), (2, 131072, 2048), (300, 4096, 256), (33, 20000, 1), (4, 24577, 300),
-    (3, 262144, 2048), (2, 300001, 2048), (40, 32769, 2048)])
+    (3, 262144, 2048), (2, 300001, 2048), (40, 32769, 2048), (160, 40000, 512)])
 @pytest.mark.parametrize("workspace", [True, False])
 def test_topk_random(rows, width, k, workspace):
     rng = np.random.default_rng(rows * 7 + width + k)
