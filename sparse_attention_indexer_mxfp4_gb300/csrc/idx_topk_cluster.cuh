@@ -49,26 +49,25 @@ struct Shared {
     uint32_t mh[2048];  // the cluster's sum of the current digit's histograms
     uint32_t wbin[3][kWarps];
     uint32_t sel[3][2];
-    uint32_t wred[2][kWarps];
+    uint32_t wred[kWarps];
     uint32_t cta[3];    // this CTA's finite keys, keys above T, keys equal to T
     uint32_t gt[kTab];  // keys above T (or taken) per (step, warp), then offsets
     uint32_t eq[kTab];  // keys equal to T per (step, warp), then offsets
 };
 
 // Sum over the CTA of one value per thread (every thread gets it); one
-// barrier, slot picks one of two scratch rows so back-to-back calls do not
-// race.
-__device__ __forceinline__ uint32_t cta_sum(Shared &sh, uint32_t v, int slot)
+// barrier.  Called once per launch, so its scratch is never reused.
+__device__ __forceinline__ uint32_t cta_sum(Shared &sh, uint32_t v)
 {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     v = __reduce_add_sync(0xffffffffu, v);
     if (lane == 0)
-        sh.wred[slot][w] = v;
+        sh.wred[w] = v;
     __syncthreads();
     uint32_t t = 0;
     #pragma unroll 8
     for (int i = 0; i < kWarps; ++i)
-        t += sh.wred[slot][i];
+        t += sh.wred[i];
     return t;
 }
 
@@ -126,7 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // the thread's run s of keys, from shared memory (only this thread writes it)
     auto run = [&](int s) -> uint4 { return sh.keys[s * kThreads + tid]; };
-    nvalid = cta_sum(sh, nvalid, 0);
+    nvalid = cta_sum(sh, nvalid);
     if (tid == 0)
         sh.cta[0] = nvalid;
     cl.sync();  // histograms and counts of digit 1 complete in every CTA
