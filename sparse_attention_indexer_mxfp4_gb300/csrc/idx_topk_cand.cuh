@@ -64,19 +64,43 @@ __global__ void __launch_bounds__(kThreads, KS == kStepsSmall ? 2 : 1)
         sh.raw[i] = crow[i];
     __syncthreads();
     const int id_end = (ke - ks + blk - 1) / blk;  // ids [0, id_end) start below ke
-    for (int i = tid; i < n; i += kThreads) {
-        const int id = sh.raw[i];
-        const bool valid = id >= 0 && id < id_end;
-        const unsigned key_i = valid ? (unsigned)id : 0xFFFFFFFFu;
-        int rank = 0;
-        bool dup = false;
-        for (int j = 0; j < n; ++j) {
-            const int idj = sh.raw[j];
-            const unsigned key_j = idj >= 0 && idj < id_end ? (unsigned)idj : 0xFFFFFFFFu;
-            rank += key_j < key_i || (key_j == key_i && j < i);
-            dup = dup || (key_j == key_i && j < i);
+    auto sort_key = [&](int id) -> unsigned {
+        return id >= 0 && id < id_end ? (unsigned)id : 0xFFFFFFFFu;
+    };
+    if (n <= kThreads / 8) {
+        // eight lanes per id, each comparing it with every eighth id, their
+        // counts added across the eight lanes (which share a warp)
+        const int i = tid >> 3, sub = tid & 7;
+        int rank = 0, dup = 0, id = -1;
+        if (i < n) {
+            id = sh.raw[i];
+            const unsigned key_i = sort_key(id);
+            for (int j = sub; j < n; j += 8) {
+                const unsigned key_j = sort_key(sh.raw[j]);
+                rank += key_j < key_i || (key_j == key_i && j < i);
+                dup |= key_j == key_i && j < i;
+            }
         }
-        sh.ids[rank] = valid && !dup ? id : -1;
+        #pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+            rank += __shfl_xor_sync(0xffffffffu, rank, o);
+            dup |= __shfl_xor_sync(0xffffffffu, dup, o);
+        }
+        if (i < n && sub == 0)
+            sh.ids[rank] = sort_key(id) != 0xFFFFFFFFu && !dup ? id : -1;
+    } else {
+        for (int i = tid; i < n; i += kThreads) {
+            const int id = sh.raw[i];
+            const unsigned key_i = sort_key(id);
+            int rank = 0;
+            bool dup = false;
+            for (int j = 0; j < n; ++j) {
+                const unsigned key_j = sort_key(sh.raw[j]);
+                rank += key_j < key_i || (key_j == key_i && j < i);
+                dup = dup || (key_j == key_i && j < i);
+            }
+            sh.ids[rank] = key_i != 0xFFFFFFFFu && !dup ? id : -1;
+        }
     }
     __syncthreads();
 

@@ -59,8 +59,14 @@ __device__ __forceinline__ void find_bin(const uint32_t *h, int nb, uint32_t kre
     if (lane == 0)
         wbin[w] = wt;
     __syncthreads();
-    for (int i = 0; i < w; ++i)
-        before += wbin[i];
+    {
+        // the counts of the warps before this one: a scan of the per-warp
+        // totals across the lanes (NT / 32 <= 32 of them)
+        const uint32_t wv = lane < NT / 32 ? wbin[lane] : 0u;
+        uint32_t unused;
+        const uint32_t wex = topk_detail::warp_excl(wv, lane, &unused);
+        before += __shfl_sync(0xffffffffu, wex, w);
+    }
     #pragma unroll
     for (int j = 0; j < MAXPER; ++j) {
         if (j < per && before < krem && before + loc[j] >= krem) {
