@@ -332,7 +332,8 @@ def _sm_count(device) -> int:
 def prepare_topk(logits, lengths, k, out, workspace=True):
     """workspace: True allocates the scratch for the chunked path once here
     (held by the returned call), a uint8 CUDA tensor supplies it, False or
-    None runs the one-CTA-per-row path."""
+    None passes none (calls that would take the chunked path then stream
+    each row in one CTA; the register and cluster paths need no scratch)."""
     if logits.dtype != torch.float32 or logits.stride(1) != 1:
         raise ValueError("logits must be float32 with unit column stride")
     _need(lengths, torch.int32, "lengths")
