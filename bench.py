@@ -313,6 +313,13 @@ def run_ours(args):
         step.run()
     torch.cuda.synchronize()
     assert idx_get_device_status() == 0, "device status set during warm-up"
+    if args.profile_run:
+        if rank == 0:
+            print(json.dumps({"profile_run": True, "config": args.config,
+                              "launches": step.launches_per_step * args.warmup}))
+        if world > 1:
+            dist.destroy_process_group()
+        return
 
     # L2: the K pages read per step exceed the 129 MB L2 for the paged
     # workloads; for the contiguous ones a 256 MB buffer is rewritten
@@ -692,6 +699,8 @@ def main():
     p.add_argument("--config", type=int, default=4, choices=[1, 2, 3, 4, 5, 6, 7])
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    p.add_argument("--profile-run", action="store_true",
+                   help="run the warm-up steps only and exit (a short command for ncu captures)")
     p.add_argument("--fused-topk", action="store_true",
                    help="paged workloads without a candidate list: one call for the logits and "
                         "the row top-k (idx_paged_mqa_logits_topk)")

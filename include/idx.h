@@ -303,22 +303,23 @@ size_t idx_topk_workspace_size(int rows, int64_t ld, int k);
  * a latency-critical loop where cudaMalloc / cudaFree may synchronise the
  * device, or a plain C caller with no device allocator of its own.
  *
- *   Same arguments and results as idx_topk.  Calls that idx_topk serves
- *   with one CTA or one cluster per row take those scratch-free paths; the
- *   others the chunked path, whose scratch is one fixed array of
- *   IDX_TOPK_NOALLOC_MAX_BYTES per device,
- *   part of the library's device image: the call allocates nothing.  The
- *   first call on a device looks up that array's address (with the device
- *   current); make that first call before any stream capture on the device.
- *   Every call clears the part of the array that must start at zero (its
- *   first kernel, on `stream`) before the others run.
+ *   Same arguments and results as idx_topk, and it succeeds wherever
+ *   idx_topk succeeds.  Calls that idx_topk serves with one CTA or one
+ *   cluster per row take those scratch-free paths.  The others take the
+ *   chunked path when its scratch fits one fixed array of
+ *   IDX_TOPK_NOALLOC_MAX_BYTES per device (part of the library's device
+ *   image: the call allocates nothing; that is up to about 450 rows of
+ *   262144 keys), and otherwise the scratch-free kernel that streams each row
+ *   in one CTA (slower on many long rows, same indices).
+ *   The first chunked call on a device looks up the array's address with
+ *   the device current, and so does the first one after the device's primary
+ *   context was replaced (cudaDeviceReset); make that call before any stream
+ *   capture on the device.  Every chunked call clears the part of the array
+ *   that must start at zero (its first kernel, on `stream`) before the
+ *   others run, so nothing a previous call left there is read.
  *   Calls on one device share the array: two calls that overlap in time
  *   (different streams, not ordered by events) race and give wrong indices.
- * Errors: as idx_topk; on the chunked path IDX_ERR_WORKSPACE when
- *   idx_topk_workspace_size(rows, ld, k) > IDX_TOPK_NOALLOC_MAX_BYTES (about
- *   450 rows), IDX_ERR_UNSUPPORTED when it is 0 for rows > 0
- *   (ld above 8192 * 1024); IDX_ERR_CUDA when the address lookup or a launch
- *   fails.
+ * Errors: as idx_topk; IDX_ERR_CUDA also when the address lookup fails.
  * ---------------------------------------------------------------------- */
 #define IDX_TOPK_NOALLOC_MAX_BYTES (32u << 20)
 
@@ -440,6 +441,23 @@ idx_status idx_q_rope_quant(const uint16_t *q, const int32_t *positions, const f
  * only call that does.  *out receives the bits.
  * ---------------------------------------------------------------------- */
 idx_status idx_get_device_status(idx_stream_t stream, uint32_t *out);
+
+/* ------------------------------------------------------------------------
+ * idx_debug_wait_expiry -- diagnostic: make one of the library's bounded
+ * device waits run out.  The pages have no counterpart; it exists so that
+ * the timeout path can be tested without breaking a real kernel.
+ *
+ *   which     0: the mbarrier wait that every pipeline stage of the logits
+ *             kernel uses, on a barrier that no thread arrives on;
+ *             1: the grid barrier of the chunked top-k, in a launch of two
+ *             CTAs of which only the first arrives.
+ *   limit_ns  the wait's limit, 1 .. 10^10 ns (the kernels use 2 * 10^9).
+ * The kernel returns after about limit_ns with IDX_DEV_TIMEOUT set in the
+ * device status word (read it with idx_get_device_status); the context stays
+ * usable for the next call.  Errors: IDX_ERR_INVALID_ARG for other values,
+ * IDX_ERR_CUDA when the launch fails.
+ * ---------------------------------------------------------------------- */
+idx_status idx_debug_wait_expiry(int which, uint64_t limit_ns, idx_stream_t stream);
 
 /* Library version string, e.g. "idx 0.1 sm_103a". */
 const char *idx_version(void);

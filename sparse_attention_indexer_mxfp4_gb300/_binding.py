@@ -53,6 +53,7 @@ _SIGNATURES = {
     "idx_q_rope_quant": [_P, _P, _P, _L, _I, _I, _P, ctypes.c_float, _I, _I, _I, _I, _P, _P, _P,
                          _P],
     "idx_get_device_status": [_P, ctypes.POINTER(ctypes.c_uint32)],
+    "idx_debug_wait_expiry": [_I, ctypes.c_uint64, _P],
 }
 
 
@@ -486,6 +487,15 @@ def idx_q_rope_quant(q, positions, cos_sin, rope_dim, weights, weight_scale, fmt
                      weights_out, q_scale_out=None, stream=None):
     prepare_q_rope_quant(q, positions, cos_sin, rope_dim, weights, weight_scale, fmt, q_out,
                          weights_out, q_scale_out)(stream)
+
+
+def idx_debug_wait_expiry(which: int, limit_ns: int, stream=None):
+    """Diagnostic: one of the library's bounded device waits (0: the logits
+    pipeline's mbarrier wait, 1: the chunked top-k's grid barrier) on a
+    condition that never holds; it gives up after limit_ns and sets
+    DEV_TIMEOUT in the device status."""
+    _check(lib().idx_debug_wait_expiry(int(which), int(limit_ns), _stream(stream)),
+           "idx_debug_wait_expiry")
 
 
 def idx_get_device_status(stream=None) -> int:

@@ -98,6 +98,20 @@ static __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parit
     }
 }
 
+// Wait for a phase after an abort, regardless of the abort flag: the async
+// copies and MMAs a role has issued finish on their own, and the role waits
+// (at most limit_ns) for them before its CTA frees its shared and tensor
+// memory.
+static __device__ __noinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity,
+                                                    uint64_t limit_ns = 20000000ull)
+{
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait_sleep(bar, parity, 20000u))
+        if (globaltimer_ns() - t0 > limit_ns)
+            return false;
+    return true;
+}
+
 IDX_DEVFN bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
                          unsigned int *status, uint64_t limit_ns = 2000000000ull)
 {
@@ -336,19 +350,12 @@ IDX_DEVFN void pdl_launch_dependents()
 }
 
 // Two fp32 fused multiply-adds in one packed instruction: (a * b + c) per
-// lane, each rounded to nearest like fmaf.
+// lane, each rounded to nearest like fmaf.  The compiler builtin (rather
+// than inline assembly) leaves the choice of the register pairs to the
+// register allocator, which then needs no moves to build them.
 IDX_DEVFN float2 fma2(float2 a, float2 b, float2 c)
 {
-    float2 d;
-    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
-        "mov.b64 ra, {%2, %3};\n\t"
-        "mov.b64 rb, {%4, %5};\n\t"
-        "mov.b64 rc, {%6, %7};\n\t"
-        "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
-        "mov.b64 {%0, %1}, rd;\n\t}"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-    return d;
+    return __ffma2_rn(a, b, c);
 }
 
 IDX_DEVFN void named_bar_sync(int id, int nthreads)

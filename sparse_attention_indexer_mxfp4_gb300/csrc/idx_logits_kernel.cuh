@@ -77,7 +77,8 @@ struct LogitsCfg {
     static constexpr int OFF_BAR = (OFF_SIDE + NA * SIDE_BYTES + 7) / 8 * 8;
     // full[S], empty[S], acc_full[NA], acc_empty[NA], q_full[2], q_empty[2]
     // + hist[NA][2]: a warpgroup's histogram hand-over (histogram variant)
-    static constexpr int NUM_BARS = 2 * S + 2 * NA + 4 + 2 * NA;
+    // + drain[2]: each MMA warp's last commit after an abort
+    static constexpr int NUM_BARS = 2 * S + 2 * NA + 4 + 2 * NA + 2;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;  // tmem base, abort flag
     static constexpr int OFF_SCRATCH = (OFF_MISC + 16 + 7) / 8 * 8;  // 40 long longs
     static constexpr int OFF_BITMAP = OFF_SCRATCH + 40 * 8;
@@ -197,6 +198,7 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
     uint64_t *acc_full = bars + 2 * S, *acc_empty = acc_full + NA;
     uint64_t *q_full = acc_empty + NA, *q_empty = q_full + 2;
     uint64_t *hbar = q_empty + 2;  // [NA][2]: counts done, flush done
+    uint64_t *drain = hbar + 2 * NA;  // [2]: MMA warps' commits after an abort
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
     long long *scratch = reinterpret_cast<long long *>(smem + C::OFF_SCRATCH);
@@ -221,6 +223,8 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
         for (int i = 0; i < 2 * NA; ++i) {
             mbar_init(&hbar[i], 4);  // the warpgroup's four warps
         }
+        mbar_init(&drain[0], 1);
+        mbar_init(&drain[1], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -379,6 +383,15 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
                 if (!mbar_wait(&q_empty[i & 1], (i >> 1) & 1, abort_flag, a.status))
                     break;
         }
+        if (*abort_flag) {
+            // after an abort: the copies this warp issued (its last S tiles'
+            // stages, the last two group slots) land before the CTA exits
+            for (int i = c > S ? c - S : 0; i < c; ++i)
+                if ((i & 1) == pw)
+                    mbar_wait_drain(&full[C::stage(i)], C::phase(i));
+            for (int i = gq > 2 ? gq - 2 : 0; i < gq; ++i)
+                mbar_wait_drain(&q_full[i & 1], (i >> 1) & 1);
+        }
     } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
         // ------------------------------------------------------------ MMA issuers
         const int mw = warp - kMmaWarp;  // issues the tiles with (c % NA) & 1 == mw
@@ -506,6 +519,15 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
                     mma_commit(&q_empty[slot]);
                 __syncwarp();
             }
+        }
+        if (*abort_flag) {
+            // after an abort: this warp's MMAs and tensor-memory copies in
+            // flight complete before the tensor memory is freed
+            if (lane == 0) {
+                mma_commit(&drain[mw]);
+                mbar_wait_drain(&drain[mw], 0);
+            }
+            __syncwarp();
         }
     } else if (warp >= kFirstEpiWarp) {
         // ------------------------------------------------------------ epilogue

@@ -646,13 +646,73 @@ extern "C" idx_status idx_topk_to_ragged_slots(const int32_t *topk, int64_t ld, 
     return launch_status(e);
 }
 
+// ---------------------------------------------------- bounded-wait expiry
+//
+// A diagnostic that makes the library's bounded waits run out, so that a
+// test can check the path every pipeline takes when a wait never completes:
+// the wait returns after its limit, the device status gets IDX_DEV_TIMEOUT,
+// the kernel ends, and the context stays usable.  which = 0: the mbarrier
+// wait of the logits pipeline (mbar_wait) on a barrier no thread arrives
+// on; which = 1: the grid barrier of the chunked top-k (grid_sync) in a
+// launch of two CTAs of which only the first arrives.
+
+namespace idx {
+
+__device__ uint32_t g_expiry_ctrl[2];
+
+__global__ void wait_expiry_kernel(int which, uint64_t limit_ns, unsigned *status)
+{
+    if (which == 0) {
+        __shared__ __align__(8) uint64_t bar;
+        __shared__ int abort;
+        if (threadIdx.x == 0) {
+            mbar_init(&bar, 1);
+            abort = 0;
+            fence_mbar_init();
+        }
+        __syncthreads();
+        if (threadIdx.x == 0)
+            (void)mbar_wait(&bar, 0u, &abort, status, limit_ns);
+        __syncthreads();
+        return;
+    }
+    if (blockIdx.x != 0)  // the CTA that never arrives
+        return;
+    __shared__ uint32_t abort_sh;
+    if (threadIdx.x == 0)
+        abort_sh = 0u;
+    __syncthreads();
+    (void)topk_chunked::grid_sync(g_expiry_ctrl, status, &abort_sh, limit_ns);
+}
+
+} // namespace idx
+
+extern "C" idx_status idx_debug_wait_expiry(int which, uint64_t limit_ns, idx_stream_t stream)
+{
+    if ((which != 0 && which != 1) || limit_ns == 0 || limit_ns > 10000000000ull)
+        return IDX_ERR_INVALID_ARG;
+    unsigned int *status = device_status_ptr();
+    if (!status)
+        return IDX_ERR_CUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (which == 1) {  // the barrier's arrival count starts at zero
+        void *ctrl = nullptr;
+        if (cudaGetSymbolAddress(&ctrl, g_expiry_ctrl) != cudaSuccess ||
+            cudaMemsetAsync(ctrl, 0, sizeof(g_expiry_ctrl), s) != cudaSuccess)
+            return IDX_ERR_CUDA;
+    }
+    wait_expiry_kernel<<<which == 0 ? 1 : 2, 128, 0, s>>>(which, limit_ns, status);
+    return launch_status(cudaGetLastError());
+}
+
 // ------------------------------------------------ top-k without allocation
 //
 // idx_topk_noalloc runs the chunked top-k over one fixed array per device
 // instead of caller scratch, for callers that can neither pass scratch nor
 // allocate it when they call.  The array is part of this library's device
-// image; its address is looked up once per device, with that device
-// current, and cached.
+// image; its address is looked up with the device current and cached per
+// (device, context): a new primary context after a device reset gets a new
+// lookup.
 
 static __device__ __align__(256) unsigned char g_topk_scratch[IDX_TOPK_NOALLOC_MAX_BYTES];
 
@@ -660,18 +720,47 @@ namespace {
 
 std::mutex g_scratch_mu;
 void *g_scratch_ptr[64];
+CUcontext g_scratch_ctx[64];
+
+// The driver's cuCtxGetCurrent, through the runtime's entry-point query (the
+// library links no driver library).
+CUresult (*ctx_getter())(CUcontext *)
+{
+    static CUresult (*fn)(CUcontext *) = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CUresult (*)(CUcontext *)>(p);
+    });
+    return fn;
+}
 
 idx_status topk_scratch(void **out)
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return IDX_ERR_CUDA;
+    auto get_ctx = ctx_getter();
+    if (!get_ctx)
+        return IDX_ERR_CUDA;
+    // the context current on this thread (null before the runtime has bound
+    // one); the cached address is valid only in the context it was taken in
+    CUcontext ctx = nullptr;
+    if (get_ctx(&ctx) != CUDA_SUCCESS)
+        return IDX_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_ptr[dev]) {
-        void *p = nullptr;
+    if (!ctx || !g_scratch_ptr[dev] || g_scratch_ctx[dev] != ctx) {
+        void *p = nullptr;  // the lookup binds the device's primary context
         if (cudaGetSymbolAddress(&p, g_topk_scratch) != cudaSuccess || !p)
             return IDX_ERR_CUDA;
+        if (get_ctx(&ctx) != CUDA_SUCCESS || !ctx)
+            return IDX_ERR_CUDA;
         g_scratch_ptr[dev] = p;
+        g_scratch_ctx[dev] = ctx;
     }
     *out = g_scratch_ptr[dev];
     return IDX_OK;
@@ -689,26 +778,29 @@ extern "C" idx_status idx_topk_noalloc(const float *logits, int64_t ld, int rows
         return IDX_OK;
     if (!logits || !lengths || !out_idx || ld <= 0)
         return IDX_ERR_INVALID_ARG;
-    const int vec = (ld % 4 == 0) && aligned16(logits);
+    cudaStream_t s = (cudaStream_t)stream;
+    const int vec_ok = (ld % 4 == 0) && aligned16(logits);
     if (ld <= topk_short::kMaxLen)  // rows a CTA or a cluster holds need no scratch
-        return topk_launch_short(logits, ld, rows, lengths, k, out_idx, ld_out, vec,
-                                 (cudaStream_t)stream);
+        return topk_launch_short(logits, ld, rows, lengths, k, out_idx, ld_out, vec_ok, s);
     if (ld <= topk_cluster::kMaxLen) {
-        const idx_status st = topk_launch_cluster(logits, ld, rows, lengths, k, out_idx, ld_out,
-                                                  vec, (cudaStream_t)stream);
+        const idx_status st =
+            topk_launch_cluster(logits, ld, rows, lengths, k, out_idx, ld_out, vec_ok, s);
         if (st != IDX_ERR_UNSUPPORTED)
             return st;
     }
+    // the chunked path over the fixed array when the call fits it; otherwise
+    // (too many rows for the array, rows too long for the chunked path, no
+    // cooperative launch) the scratch-free kernel that streams each row
     const size_t need = idx_topk_workspace_size(rows, ld, k);
-    if (need == 0)
-        return IDX_ERR_UNSUPPORTED;
-    if (need > (size_t)IDX_TOPK_NOALLOC_MAX_BYTES)
-        return IDX_ERR_WORKSPACE;
-    void *ws = nullptr;
-    const idx_status st = topk_scratch(&ws);
-    if (st != IDX_OK)
-        return st;
-    const int vec_ok = (ld % 4 == 0) && aligned16(logits);
-    return topk_launch_chunked(logits, ld, rows, lengths, k, out_idx, ld_out, ws, vec_ok,
-                               (cudaStream_t)stream);
+    if (need > 0 && need <= (size_t)IDX_TOPK_NOALLOC_MAX_BYTES && ld > topk_chunked::kCh) {
+        void *ws = nullptr;
+        const idx_status st = topk_scratch(&ws);
+        if (st != IDX_OK)
+            return st;
+        const idx_status sc =
+            topk_launch_chunked(logits, ld, rows, lengths, k, out_idx, ld_out, ws, vec_ok, s);
+        if (sc != IDX_ERR_UNSUPPORTED)
+            return sc;
+    }
+    return topk_launch_per_row(logits, ld, rows, lengths, k, out_idx, ld_out, vec_ok, s);
 }

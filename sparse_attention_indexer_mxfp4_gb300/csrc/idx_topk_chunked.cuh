@@ -645,8 +645,8 @@ __device__ __forceinline__ void write_item(const float *logits, int64_t ld, int 
 // barrier is passed once the count reaches n * gridDim.x.  Thread 0 arrives
 // with a release add, so the CTA's earlier writes (ordered before it by the
 // CTA barrier) are visible to every CTA that then reads the count with an
-// acquire load.  The wait is bounded (two seconds), after which the status
-// gets the timeout bit and the CTA stops.
+// acquire load.  The wait is bounded (limit_ns, two seconds by default),
+// after which the status gets the timeout bit and the CTA stops.
 __device__ __forceinline__ uint32_t atom_add_release_gpu(uint32_t *p, uint32_t v)
 {
     uint32_t old;
@@ -662,7 +662,8 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p)
 }
 
 __device__ __forceinline__ bool grid_sync(uint32_t *ctrl, unsigned *status,
-                                          volatile uint32_t *abort_sh)
+                                          volatile uint32_t *abort_sh,
+                                          uint64_t limit_ns = 2000000000ull)
 {
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -673,7 +674,7 @@ __device__ __forceinline__ bool grid_sync(uint32_t *ctrl, unsigned *status,
             const uint64_t t0 = globaltimer_ns();
             while (ld_acquire_gpu(count) < target) {
                 __nanosleep(20);
-                if (globaltimer_ns() - t0 > 2000000000ull) {
+                if (globaltimer_ns() - t0 > limit_ns) {
                     atomicOr(status, kDevTimeout);
                     *abort_sh = 1u;
                     break;
@@ -753,14 +754,25 @@ __global__ void __launch_bounds__(kThreads, 2) phases_kernel(const __grid_consta
         if (resident && j < kResident && !mbar_wait(&slot_full[j], 0u, &wait_abort, a.status))
             abort_flag = 1u;  // a copy did not land in time: stop at the next barrier
     };
+    // leaving after an abort: the chunk copies this CTA issued land first
+    auto drain_slots = [&]() {
+        if (threadIdx.x == 0 && resident)
+            for (int jj = 0; jj < kResident; ++jj) {
+                if (blockIdx.x + (uint32_t)jj * gridDim.x >= nitems)
+                    break;
+                mbar_wait_drain(&slot_full[jj], 0u);
+            }
+    };
     int j = 0;
     if (!a.hist_done) {
         for (uint32_t it = blockIdx.x; it < nitems; it += gridDim.x, ++j) {
             slot_wait(j);
             hist_item(a.logits, a.ld, a.P, a.ws, vec, a.ws.items[it], slot_of(j), sh.hist);
         }
-        if (!grid_sync(ctrl, a.status, &abort_flag))
+        if (!grid_sync(ctrl, a.status, &abort_flag)) {
+            drain_slots();
             return;
+        }
     }
     j = 0;
     for (uint32_t it = blockIdx.x; it < nitems; it += gridDim.x, ++j) {
@@ -768,13 +780,17 @@ __global__ void __launch_bounds__(kThreads, 2) phases_kernel(const __grid_consta
             slot_wait(j);
         filter_item(a.logits, a.ld, a.k, a.P, a.ws, vec, a.ws.items[it], slot_of(j), sh.filter);
     }
-    if (!grid_sync(ctrl, a.status, &abort_flag))
+    if (!grid_sync(ctrl, a.status, &abort_flag)) {
+        drain_slots();
         return;
+    }
     for (int row = blockIdx.x; row < a.R; row += gridDim.x)
         resolve_row(a.logits, a.ld, a.lengths, a.k, a.P, a.ws, vec, row, sh.resolve, a.out,
                     a.ld_out);
-    if (!grid_sync(ctrl, a.status, &abort_flag))
+    if (!grid_sync(ctrl, a.status, &abort_flag)) {
+        drain_slots();
         return;
+    }
     j = 0;
     for (uint32_t it = blockIdx.x; it < nitems; it += gridDim.x, ++j)
         write_item(a.logits, a.ld, a.k, a.P, a.ws, vec, a.ws.items[it], slot_of(j), sh.tab,

@@ -1,7 +1,18 @@
 """The benchmark workloads at full size, in the launch configuration the
-benchmark times (IndexerStep).  The oracle checks sampled rows one by one;
-top-k is checked end to end with the near-tie rule and bit-exactly on the
-oracle's own logits."""
+benchmark times (IndexerStep).
+
+* Logits: the oracle computes 16 sampled sequences per paged workload (the
+  longest and the shortest among them, the rest evenly spaced) and sampled
+  rows of the contiguous ones; each is compared element by element.  With
+  152 persistent CTAs sharing 32 to 128 sequences, every sequence is split
+  between CTAs, so each sample also crosses the split's boundaries.
+* Top-k: every row of the workload is compared exactly with the oracle's
+  top-k of the GPU's own logits (the candidate mask applied for the
+  candidate pipeline); the sampled rows also end to end against the
+  oracle's logits with the near-tie rule, and exactly on the oracle's own
+  logits.
+* Slots: the ragged rows of the sampled rows are the oracle's slot map of
+  the same top-k sets."""
 import numpy as np
 import pytest
 import torch
@@ -29,6 +40,30 @@ def _sub_paged(c: synth.PagedCase, seqs):
     return sub, rows
 
 
+def _sample_seqs(c: synth.PagedCase, n: int = 16):
+    """n sequences: the longest, the shortest, the rest evenly spaced."""
+    lens = np.clip(c.row_ends(), 0, c.width).reshape(c.B, c.next_n).max(axis=1)
+    pick = set(np.linspace(0, c.B - 1, max(n - 2, 1)).round().astype(int).tolist())
+    pick |= {int(np.argmax(lens)), int(np.argmin(lens))}
+    return sorted(pick)
+
+
+def _assert_all_rows_topk_on_own_logits(st, c, what):
+    """Every row: the GPU's top-k equals the oracle's top-k of the GPU's own
+    logits over [0, ke) (candidate-masked when the step selects among
+    candidates, whose other columns the step leaves unwritten)."""
+    ke = (np.clip(c.row_ends(), 0, c.width) if st.paged else c.ke).astype(np.int32)
+    own = st.logits.cpu().numpy()
+    if st.paged and c.cand is not None:
+        ks = None if c.row_ks is None else c.row_ks.astype(np.int32)
+        oracle.apply_candidate_mask(own, ks, ke, c.cand, c.cand_block)
+    own = np.where(np.isnan(own), -np.inf, own)
+    for r in range(own.shape[0]):
+        own[r, ke[r]:] = -np.inf
+    assert_topk_exact(st.topk.cpu().numpy(), oracle.topk(own, ke, c.topk),
+                      f"{what}: top-k of every row on the GPU's logits")
+
+
 def _oracle_paged_rows(sub):
     out, bad = oracle.paged_mqa_logits(sub.fmt, sub.q, sub.q_scale, sub.weights, sub.pages,
                                        sub.page_stride, sub.num_pages, sub.block_table,
@@ -54,7 +89,8 @@ def test_paged_config(paged_cfg, cand_topk):
     st.run()
     torch.cuda.synchronize()
     assert B.idx_get_device_status() == 0
-    seqs = [0, c.B // 2, c.B - 1]
+    _assert_all_rows_topk_on_own_logits(st, c, f"config {cfg}")
+    seqs = _sample_seqs(c)
     sub, rows = _sub_paged(c, seqs)
     ref, ke, bad = _oracle_paged_rows(sub)
     assert bad == 0
@@ -109,7 +145,8 @@ def test_contiguous_config(cfg):
     st = IndexerStep(c)
     st.run()
     torch.cuda.synchronize()
-    rows = np.unique(np.r_[0:3, c.M // 2, c.M - 3:c.M])
+    _assert_all_rows_topk_on_own_logits(st, c, f"config {cfg}")
+    rows = np.unique(np.r_[0:3, np.linspace(0, c.M - 1, 13).round().astype(int), c.M - 3:c.M])
     sub = synth.ContiguousCase(c.fmt, len(rows), c.N, c.H, c.D, c.q[rows], None, c.weights[rows],
                                c.k, c.k_scale, c.ks[rows], c.ke[rows], c.topk)
     ref = oracle.mqa_logits(sub.fmt, sub.q, None, sub.weights, sub.k, sub.k_scale, sub.ks,
