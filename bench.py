@@ -1,17 +1,20 @@
 """Benchmark of one indexer step on synthetic data.
 
-Default workload: paged FP8 MTP decode with a candidate mask (B=128
-sequences, next_n=2, lognormal contexts with median 16384, 64 candidate
-blocks of 128 keys per row, top-2048 mapped to ragged cache slots).  A step
-is the whole hot path: paged logits with the candidate mask fused in, per-row
-top-k, and the top-k -> slot map.
+Headline workload: paged FP8 decode (B=64 sequences, next_n=1, context
+lengths U[4096, 32768], 64-token pages in a 40,000-page pool, top-2048
+mapped to ragged cache slots).  A step is the whole hot path: paged logits,
+per-row top-k, and the top-k -> slot map.
 
-Metric: indexer keys scored per second (sum over rows of ke - ks, per step
-time), whole job over all ranks.  Every rank runs its own independent batch
-(weak scaling; the path has no exchange step).
+Metric: indexer keys scored per second (the (row, key) pairs that receive a
+score per step, over the step time), whole job over all ranks.  Every rank
+runs its own independent batch (weak scaling; the path has no exchange
+step).  After the headline, the same process measures every other workload
+(``per_config``: the contiguous prefill and small cases, the MTP candidate
+pipeline, MXFP4 decode, the candidate source, the K/Q producers), each with
+its own clock record and rooflines.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..7]
-                  [--impl ours|reference]
+                  [--impl ours|reference] [--no-per-config] [--no-cpu]
 """
 from __future__ import annotations
 
@@ -288,32 +291,183 @@ def logits_flops(case) -> float:
     return 2.0 * case.H * case.D * case.keys_scored
 
 
-def run_ours(args):
+def candidate_keys(case) -> int:
+    """(row, key) pairs inside a row's candidate blocks (clipped to its
+    [ks, ke)): the keys a candidate pipeline gives a real score."""
+    ke = np.clip(case.row_ends(), 0, case.width).astype(np.int64)
+    ks = (np.zeros_like(ke) if case.row_ks is None else
+          np.minimum(case.row_ks.astype(np.int64), ke))
+    total = 0
+    for r in range(case.rows):
+        ids = np.unique(case.cand[r][case.cand[r] >= 0].astype(np.int64))
+        lo = ks[r] + ids * case.cand_block
+        hi = np.minimum(lo + case.cand_block, ke[r])
+        total += int(np.maximum(hi - lo, 0).sum())
+    return total
+
+
+def scored_keys(case) -> int:
+    """(row, key) pairs a step scores: every live key, or with a candidate
+    list only the candidate keys (the dense-equivalent count is
+    case.keys_scored)."""
+    from sparse_attention_indexer_mxfp4_gb300.synth import PagedCase
+    if isinstance(case, PagedCase) and case.cand is not None:
+        return candidate_keys(case)
+    return case.keys_scored
+
+
+def topk_bytes(case) -> float:
+    """Algorithmic bytes of one top-k stage: every logit the selection
+    ranks read once (the live keys of each row, or only its candidate keys)
+    and k int32 indices written per row; the candidate source also reads its
+    block maxima and writes its pool."""
+    from sparse_attention_indexer_mxfp4_gb300.synth import PagedCase
+    if isinstance(case, PagedCase):
+        b = 4.0 * scored_keys(case) + 4.0 * case.rows * case.topk
+        if case.cand is not None:
+            b += 4.0 * case.cand.size
+        if getattr(case, "source_block", 0):
+            nb = -(-case.width // case.source_block)
+            b += 4.0 * case.rows * (nb + case.source_cands)
+        return b
+    return 4.0 * float(np.maximum(case.ke - case.ks, 0).sum()) + 4.0 * case.M * case.topk
+
+
+def measure(cfg: int, args, dev, world: int, rank: int, headline: bool) -> dict:
+    """One workload: build it, warm up, time args.steps steps (a CUDA graph
+    replay), and return its figures.  Paged workloads rotate over three
+    device copies of the K pool, so the pages a step reads were last read two
+    steps earlier (the 129 MB L2 holds none of them); the contiguous ones and
+    the producers rewrite a 256 MB buffer between steps."""
     import torch
-    import torch.distributed as dist
     from sparse_attention_indexer_mxfp4_gb300 import (IndexerStep, ProducerStep,
                                                       idx_get_device_status)
     from sparse_attention_indexer_mxfp4_gb300.synth import PagedCase
+
+    case = _case(cfg, shard=rank)
+    prod = _is_producer(case)
+    step = (ProducerStep(case, device=dev) if prod else
+            IndexerStep(case, device=dev, fused_topk=args.fused_topk))
+    fused = getattr(step, "fused_topk", False)
+    paged = isinstance(case, PagedCase)
+    steps = [step] + ([step.twin(kv_copy=True), step.twin(kv_copy=True)] if paged else [])
+    metric, unit, div = _metric_unit_div(case)
+
+    for _ in range(args.warmup):  # (the first call also builds and loads the library)
+        for st in steps:
+            st.run()
+    torch.cuda.synchronize()
+    assert idx_get_device_status() == 0, f"device status set during warm-up (config {cfg})"
+    flush = None
+    if not paged:
+        flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    clocks = Clocks(dev.index if dev.index is not None else 0)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    timing = time_steps_graph(steps, args.steps, flush, clock_soak_s=0.4)
+    if timing is None:
+        timing = time_steps_eager(steps, args.steps, flush)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    ms_per_step, logit_ms, topk_ms, mode = timing
+    assert idx_get_device_status() == 0, f"device status set during the timed steps (config {cfg})"
+    ms_per_step, logit_avg, topk_avg = max_over_ranks(
+        [ms_per_step, sum(logit_ms) / len(logit_ms), sum(topk_ms) / len(topk_ms)], dev, world)
+
+    keys = _work(case) if prod else scored_keys(case)
+    rows = case.rows if paged or prod else case.M
+    hbm, bf16, src = _peaks()
+    if prod:  # the producers' stage times are the K call and the Q call
+        lb = producer_bytes(case)
+        ach = lb / (ms_per_step * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(ach / hbm, 4), "traffic": None, "peak_source": f"{src} hbm_gbs",
+                "kernel": "producer step: k_store_kernel + q_quant_kernel",
+                "algorithmic_bytes_per_launch": lb, "avg_launch_ms": round(ms_per_step, 5)}
+    elif not paged and cfg == 2:
+        fp8_peak = 2.0 * bf16  # dense fp8 rate = 2x bf16 on this part
+        ach = logits_flops(case) / (logit_avg * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": fp8_peak,
+                "unit": "TFLOP/s", "frac": round(ach / fp8_peak, 4), "traffic": None,
+                "peak_source": f"{src} bf16_tflops x 2 (fp8 dense)", "kernel": "logits_kernel",
+                "algorithmic_flops_per_launch": logits_flops(case),
+                "avg_launch_ms": round(logit_avg, 5)}
+    else:
+        lb = logits_bytes(case, cand_only=getattr(step, "cand_topk", False))
+        if fused:  # the stage also holds the top-k: one more read of the live logits
+            lb += 4.0 * float(np.clip(case.row_ends(), 0, case.width).sum())
+        ach = lb / (logit_avg * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(ach / hbm, 4),
+                "traffic": None if fused else logits_traffic(cfg),
+                "peak_source": f"{src} hbm_gbs",
+                "kernel": ("fused logits + top-k stage: top-k plan_kernel, logits_kernel with "
+                           "digit-1 histograms, top-k phases_kernel from the filter" if fused
+                           else "logits stage: cand_plan_kernel (candidate plan) + "
+                           "logits_kernel" if getattr(case, "cand", None) is not None
+                           else "logits stage: bmax_fill_kernel + logits_kernel with block "
+                           "maxima" if getattr(case, "source_block", 0) else "logits_kernel"),
+                "algorithmic_bytes_per_launch": lb, "avg_launch_ms": round(logit_avg, 5)}
+    out = {
+        "workload": WORKLOAD_NAMES[cfg], "config_id": cfg, "metric": metric,
+        "value": round(job_value(world, keys, ms_per_step, div), 4), "unit": unit,
+        "ms_per_step": round(ms_per_step, 5), "rows": rows,
+        "timing": mode, "clocks": clk, "roofline": roof,
+        "gpu_launches_per_step": step.launches_per_step,
+        "l2": ("K pool rotated over three device copies (each step reads pages last read two "
+               "steps earlier)" if paged else "256 MB buffer rewritten between steps"),
+    }
+    if prod:
+        out.update({"tokens_per_step": case.T, "k_store_ms": round(logit_avg, 5),
+                    "q_quant_ms": round(topk_avg, 5)})
+    else:
+        tb = topk_bytes(case)
+        tach = tb / (topk_avg * 1e-3) / 1e9
+        out.update({
+            "keys_scored_per_step": keys,
+            "keys_dense_equivalent_per_step": case.keys_scored,
+            "logits_ms": round(logit_avg, 5), "topk_ms": round(topk_avg, 5),
+            "topk_rows_per_s": round(world * rows / (topk_avg * 1e-3), 1),
+            "topk_roofline": {"bound": "hbm", "achieved": round(tach, 1), "peak": hbm,
+                              "unit": "GB/s", "frac": round(tach / hbm, 4),
+                              "algorithmic_bytes_per_launch": tb,
+                              "avg_launch_ms": round(topk_avg, 5),
+                              "peak_source": f"{src} hbm_gbs"},
+            "fused_topk": fused,
+        })
+    if headline:
+        out["_step"] = step
+        out["_case"] = case
+    return out
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
 
     world, rank, local = _dist()
     if world > 1:
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    case = _case(args.config, shard=rank)
-    prod = _is_producer(case)
-    step = (ProducerStep(case, device=dev) if prod else
-            IndexerStep(case, device=dev, fused_topk=args.fused_topk))
-    fused = getattr(step, "fused_topk", False)
-    metric, unit, div = _metric_unit_div(case)
-    stream = torch.cuda.current_stream()
 
-    # warm-up (also builds and loads the library)
-    for _ in range(args.warmup):
-        step.run()
-    torch.cuda.synchronize()
-    assert idx_get_device_status() == 0, "device status set during warm-up"
-    if args.profile_run:
+    if args.profile_run:  # warm-up steps only, for ncu captures
+        from sparse_attention_indexer_mxfp4_gb300 import (IndexerStep, ProducerStep,
+                                                          idx_get_device_status)
+        case = _case(args.config, shard=rank)
+        step = (ProducerStep(case, device=dev) if _is_producer(case) else
+                IndexerStep(case, device=dev, fused_topk=args.fused_topk))
+        for _ in range(args.warmup):
+            step.run()
+        torch.cuda.synchronize()
+        assert idx_get_device_status() == 0, "device status set during warm-up"
         if rank == 0:
             print(json.dumps({"profile_run": True, "config": args.config,
                               "launches": step.launches_per_step * args.warmup}))
@@ -321,87 +475,41 @@ def run_ours(args):
             dist.destroy_process_group()
         return
 
-    # L2: the K pages read per step exceed the 129 MB L2 for the paged
-    # workloads; for the contiguous ones a 256 MB buffer is rewritten
-    # between steps.
-    flush = None
-    if not isinstance(case, PagedCase):  # contiguous workloads and the producers
-        flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-
-    clocks = Clocks(local)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    clocks.start()
-    timing = time_steps_graph(step, args.steps, flush, clock_soak_s=0.4)
-    if timing is None:
-        timing = time_steps_eager(step, args.steps, flush)
-    torch.cuda.synchronize()
-    clk = clocks.stop()
-    if world > 1:
-        dist.barrier()
-    ms_per_step, logit_ms, topk_ms, mode = timing
-
-    assert idx_get_device_status() == 0, "device status set during the timed steps"
-    ms_per_step, logit_avg, topk_avg = max_over_ranks(
-        [ms_per_step, sum(logit_ms) / len(logit_ms), sum(topk_ms) / len(topk_ms)], dev, world)
-
-    keys = _work(case)
-    rows = case.rows if isinstance(case, PagedCase) or prod else case.M
+    head = measure(args.config, args, dev, world, rank, headline=True)
+    step, case = head.pop("_step"), head.pop("_case")
     e2e = run_e2e(step, case, args, dev) if rank == 0 else None
-
-    hbm, bf16, src = _peaks()
-    if prod:  # the producers' stage times are the K call and the Q call
-        lb = producer_bytes(case)
-        achieved_gbs = lb / (ms_per_step * 1e-3) / 1e9
-    else:
-        lb = logits_bytes(case, cand_only=getattr(step, "cand_topk", False))
-        if fused:  # the stage also holds the top-k: one more read of the live logits
-            lb += 4.0 * float(np.clip(case.row_ends(), 0, case.width).sum())
-        achieved_gbs = lb / (logit_avg * 1e-3) / 1e9
-    if prod:
-        roof = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(achieved_gbs / hbm, 4), "traffic": None,
-                "peak_source": f"{src} hbm_gbs",
-                "kernel": "producer step: k_store_kernel + q_quant_kernel",
-                "algorithmic_bytes_per_launch": lb, "avg_launch_ms": round(ms_per_step, 5)}
-    elif args.config == 2:
-        fp8_peak = 2.0 * bf16  # dense fp8 rate = 2x bf16 on this part
-        ach = logits_flops(case) / (logit_avg * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": fp8_peak,
-                "unit": "TFLOP/s", "frac": round(ach / fp8_peak, 4),
-                "traffic": None, "peak_source": f"{src} bf16 x 2 (fp8 dense)"}
-    else:
-        roof = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(achieved_gbs / hbm, 4),
-                "traffic": None if fused else logits_traffic(args.config),
-                "peak_source": f"{src} hbm_gbs",
-                "kernel": ("fused logits + top-k stage: top-k plan_kernel, logits_kernel with "
-                           "digit-1 histograms, top-k phases_kernel from the filter" if fused
-                           else "logits stage: cand_plan_kernel (candidate plan, -inf fill) + "
-                           "logits_kernel" if getattr(case, "cand", None) is not None
-                           else "logits stage: bmax_fill_kernel + logits_kernel with block "
-                           "maxima" if getattr(case, "source_block", 0) else "logits_kernel"),
-                "algorithmic_bytes_per_launch": lb, "avg_launch_ms": round(logit_avg, 5)}
+    per_config = {}
+    if not args.no_per_config:
+        for c in sorted(WORKLOAD_NAMES):
+            if c != args.config:
+                r = measure(c, args, dev, world, rank, headline=False)
+                per_config[str(c)] = r
+                del r
+                torch.cuda.empty_cache()
+    prod = _is_producer(case)
     out = {
-        "metric": metric, "value": round(job_value(world, keys, ms_per_step, div), 4),
-        "unit": unit, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": ("bf16 -> e2m1 (e8m0 block scales)" if prod else
-                                       "e4m3 x e4m3 -> f32" if case.fmt == 0 else
-                                       "e2m1 x e2m1 (e8m0 block scales) -> f32"),
+        "metric": head["metric"], "value": head["value"], "unit": head["unit"],
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": ("bf16 -> e2m1 (e8m0 block scales)" if prod else
+                  "e4m3 x e4m3 -> f32" if case.fmt == 0 else
+                  "e2m1 x e2m1 (e8m0 block scales) -> f32"),
         "data": "synthetic (seeded; shapes and distributions of the workload description)",
-        "config": {"workload": WORKLOAD_NAMES[args.config], "config_id": args.config,
-                   "rows": rows, "keys_scored_per_step": keys,
-                   "l2": "flushed between steps" if flush is not None else
-                   "K pages read per step exceed L2", "timing": mode},
-        "topk_rows_per_s": None if prod else round(world * rows / (topk_avg * 1e-3), 1),
-        "logits_ms" if not prod else "k_store_ms": round(logit_avg, 5),
-        "topk_ms" if not prod else "q_quant_ms": round(topk_avg, 5),
-        "roofline": roof, "clocks": clk,
-        "gpu_launches": step.launches_per_step * args.steps,
-        "fused_topk": fused,
+        "config": {"workload": head["workload"], "config_id": args.config, "rows": head["rows"],
+                   "keys_scored_per_step": head.get("keys_scored_per_step"),
+                   "keys_dense_equivalent_per_step": head.get("keys_dense_equivalent_per_step"),
+                   "l2": head["l2"], "timing": head["timing"]},
+        "logits_ms" if not prod else "k_store_ms": head.get("logits_ms", head.get("k_store_ms")),
+        "topk_ms" if not prod else "q_quant_ms": head.get("topk_ms", head.get("q_quant_ms")),
+        "topk_rows_per_s": head.get("topk_rows_per_s"),
+        "roofline": head["roofline"],
+        "topk_roofline": head.get("topk_roofline"),
+        "clocks": head["clocks"],
+        "gpu_launches": head["gpu_launches_per_step"] * args.steps,
+        "fused_topk": head.get("fused_topk", False),
         "e2e": e2e,
+        "per_config": per_config,
     }
     if rank == 0:
         out["cpu_baseline"] = cpu_baseline(case, args) if world == 1 and not args.no_cpu else None
@@ -410,8 +518,9 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def time_steps_graph(step, K, flush, clock_soak_s=0.4):
+def time_steps_graph(steps, K, flush, clock_soak_s=0.4):
     """K steps captured into one CUDA graph; the timed region is one replay.
+    Step i runs buffer set i % len(steps).
     The step time comes from a graph with timing events only at step
     boundaries (events between kernels would cut the programmatic overlap of
     one kernel's launch with the end of the one before); the per-stage times
@@ -436,6 +545,7 @@ def time_steps_graph(step, K, flush, clock_soak_s=0.4):
             for i in range(K):
                 if flush is not None:
                     flush.fill_(float(i))
+                step = steps[i % len(steps)]
                 if staged:
                     evs[i][0].record()
                     step.logits_stage()
@@ -476,11 +586,12 @@ def time_steps_graph(step, K, flush, clock_soak_s=0.4):
                                    "second replay with events between the stages)")
 
 
-def time_steps_eager(step, K, flush):
+def time_steps_eager(steps, K, flush):
     import torch
     stream = torch.cuda.current_stream()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     for i in range(K):
+        step = steps[i % len(steps)]
         if flush is not None:
             flush.fill_(float(i))
         ev[i][0].record(stream)
@@ -505,7 +616,7 @@ def run_e2e(step, case, args, dev):
     (step.results(): top-k indices and ragged slots; the quantised queries,
     their scales and weights).  The K cache and the model constants are
     resident device state, not per-step inputs.  Steps run as a serving loop runs them:
-    two sets of device buffers (sharing the K cache); step i's inputs are
+    two sets of device buffers; step i's inputs are
     copied in on one stream while step i-1 computes (its calls replayed from a
     CUDA graph) on a second and step i-2's results are copied out on a
     third, with events ordering each set's copy-in -> compute -> copy-out ->
@@ -513,7 +624,10 @@ def run_e2e(step, case, args, dev):
     copy-out."""
     import torch
 
-    sets = [step, step.twin()]
+    from sparse_attention_indexer_mxfp4_gb300.synth import PagedCase
+    # two buffer sets; paged sets hold their own copy of the K pool, so a
+    # step never reads pages the step before it left in L2
+    sets = [step, step.twin(kv_copy=isinstance(case, PagedCase))]
     host = {n: getattr(step, n).cpu().pin_memory() for n in step.input_names()}
     outs = [st.results() for st in sets]
     host_out = [[o.cpu().pin_memory() for o in os_] for os_ in outs]
@@ -580,7 +694,7 @@ def run_e2e(step, case, args, dev):
                         "three streams"}
 
 
-def _oracle_sample(case, nseq):
+def _oracle_sample(case, nseq, nthreads=0):
     """The oracle's step (logits, mask, top-k, slots) over the first nseq
     sequences (paged) or rows (contiguous) of the workload, or its producers
     over the first nseq tokens; returns the units of work (keys, tokens)."""
@@ -608,12 +722,13 @@ def _oracle_sample(case, nseq):
                                          case.weights[rows], case.pages, case.page_stride,
                                          case.num_pages, case.block_table[:nseq], ctx,
                                          case.ctx_per_row, None, nseq, case.next_n, case.H,
-                                         case.D, case.page_size, case.width)
+                                         case.D, case.page_size, case.width, nthreads=nthreads)
         ke = np.clip(case.row_ends()[rows], 0, case.width).astype(np.int32)
         if case.cand is not None:
-            oracle.apply_candidate_mask(out, None, ke, case.cand[rows], case.cand_block)
+            oracle.apply_candidate_mask(out, None, ke, case.cand[rows], case.cand_block,
+                                        nthreads=nthreads)
         out = np.where(np.isnan(out), -np.inf, out)
-        idx = oracle.topk(out, ke, case.topk)
+        idx = oracle.topk(out, ke, case.topk, nthreads=nthreads)
         oracle.topk_to_ragged_slots(idx, case.block_table[:nseq], case.page_size,
                                     case.num_pages, next_n=case.next_n)
         if getattr(case, "source_block", 0):
@@ -624,8 +739,8 @@ def _oracle_sample(case, nseq):
     rows = np.arange(nseq)
     out = oracle.mqa_logits(case.fmt, case.q[rows], None, case.weights[rows], case.k,
                             case.k_scale, case.ks[rows], case.ke[rows], nseq, case.N, case.H,
-                            case.D)
-    oracle.topk(out, case.ke[rows], case.topk)
+                            case.D, nthreads=nthreads)
+    oracle.topk(out, case.ke[rows], case.topk, nthreads=nthreads)
     return int(np.maximum(case.ke[rows] - case.ks[rows], 0).sum())
 
 
@@ -656,8 +771,16 @@ def cpu_baseline(case, args, target_s: float = 10.0):
     else:
         what = (f"first {n} of {total} {'sequences' if hasattr(case, 'B') else 'rows'} "
                 f"({keys} keys): fp64 scalar logits + mask + top-k + slots, {dt:.1f} s")
+    # the single-thread oracle on the whole small contiguous workload
+    c1 = _case(1)
+    t = time.time()
+    k1 = _oracle_sample(c1, c1.M, nthreads=1)
+    dt1 = time.time() - t
     return {"value": round(keys / dt / div, 6), "unit": unit, "cores": oracle.default_threads(),
-            "kind": "oracle", "sample": what}
+            "kind": "oracle", "sample": what,
+            "single_thread": {"workload": WORKLOAD_NAMES[1], "value": round(k1 / dt1 / 1e9, 6),
+                              "unit": "Gkeys/s", "seconds": round(dt1, 3), "cores": 1,
+                              "sample": f"all {c1.M} rows ({k1} keys): logits + top-k"}}
 
 
 def run_reference(args):
@@ -665,8 +788,12 @@ def run_reference(args):
     if rank != 0:
         return
     import oracle
+    from sparse_attention_indexer_mxfp4_gb300.synth import PagedCase
     case = _case(args.config)
-    nseq = 1
+    cores = oracle.default_threads()
+    # enough sequences (rows) that the oracle's row threads cover every core
+    per = case.next_n if isinstance(case, PagedCase) else 1
+    nseq = min(_units(case), max(1, -(-cores // per)))
     for _ in range(args.warmup):
         _oracle_sample(case, nseq)
     t = time.time()
@@ -684,9 +811,10 @@ def run_reference(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64 (scalar CPU oracle)",
         "data": "synthetic", "config": {"workload": WORKLOAD_NAMES[args.config],
                                         "config_id": args.config},
-        "cpu_baseline": {"value": round(v, 6), "unit": unit, "cores": oracle.default_threads(),
+        "cpu_baseline": {"value": round(v, 6), "unit": unit, "cores": cores,
                          "kind": "oracle",
-                         "sample": f"each step: the first 1 of {total} units of the workload"},
+                         "sample": f"each step: the first {nseq} of {total} units of the "
+                                   f"workload ({keys // max(args.steps, 1)} units of work)"},
         "e2e": {"value": round(v, 6), "unit": unit, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0}}))
 
@@ -696,9 +824,11 @@ def main():
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=20)
     p.add_argument("--warmup", type=int, default=5)
-    p.add_argument("--config", type=int, default=4, choices=[1, 2, 3, 4, 5, 6, 7])
+    p.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5, 6, 7])
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    p.add_argument("--no-per-config", action="store_true",
+                   help="measure the headline workload only")
     p.add_argument("--profile-run", action="store_true",
                    help="run the warm-up steps only and exit (a short command for ncu captures)")
     p.add_argument("--fused-topk", action="store_true",

@@ -29,14 +29,15 @@ class IndexerStep:
     reads only the candidate blocks; the top-k and slots are the same, the
     logits outside those tiles are left unwritten.  ``kv_from`` (another
     IndexerStep of the same case) shares its device K cache instead of
-    uploading a second copy.  ``fused_topk`` (paged, no candidate list) runs
+    uploading a second copy; with ``kv_copy`` it takes a device copy of it
+    instead (the same keys at other addresses).  ``fused_topk`` (paged, no candidate list) runs
     the logits and the row top-k as one idx_paged_mqa_logits_topk call, the
     logits kernel counting the top-k's first digit; its logits stage then
     holds the top-k too."""
 
     def __init__(self, case, device="cuda", fused_mask: bool = True, num_ctas: int = 0,
                  gather: bool = True, cand_topk: bool = True, kv_from=None,
-                 fused_topk: bool = False):
+                 fused_topk: bool = False, kv_copy: bool = False):
         self.case = case
         self.device = torch.device(device)
         self.fused_mask = fused_mask
@@ -50,7 +51,10 @@ class IndexerStep:
         self.weights = _dev(case.weights, d)
         self.q_scale = _dev(case.q_scale, d)
         if self.paged:
-            self.pages = kv_from.pages if kv_from is not None else _dev(case.pages, d)
+            if kv_from is not None:
+                self.pages = kv_from.pages.clone() if kv_copy else kv_from.pages
+            else:
+                self.pages = _dev(case.pages, d)
             self.block_table = _dev(case.block_table, d)
             self.context_lens = _dev(case.context_lens, d)
             self.row_ks = _dev(case.row_ks, d)
@@ -60,8 +64,11 @@ class IndexerStep:
             self.rows, self.width = case.rows, case.width
             self.max_blocks = case.max_blocks
         else:
-            self.k = kv_from.k if kv_from is not None else _dev(case.k, d)
-            self.k_scale = kv_from.k_scale if kv_from is not None else _dev(case.k_scale, d)
+            if kv_from is not None:
+                self.k = kv_from.k.clone() if kv_copy else kv_from.k
+                self.k_scale = kv_from.k_scale.clone() if kv_copy else kv_from.k_scale
+            else:
+                self.k, self.k_scale = _dev(case.k, d), _dev(case.k_scale, d)
             self.ks = _dev(case.ks, d)
             self.ke = _dev(case.ke, d)
             self.lengths = self.ke
@@ -164,11 +171,13 @@ class IndexerStep:
         self.slots_stage(stream)
 
     # ---------------------------------------------------- host round trip
-    def twin(self):
-        """A second buffer set for the same case, sharing the K cache."""
+    def twin(self, kv_copy: bool = False):
+        """A second buffer set for the same case, sharing the K cache (or,
+        with kv_copy, holding its own device copy of it)."""
         return IndexerStep(self.case, device=self.device, fused_mask=self.fused_mask,
                            num_ctas=self.num_ctas, gather=self.gather,
-                           cand_topk=self.cand_topk, kv_from=self, fused_topk=self.fused_topk)
+                           cand_topk=self.cand_topk, kv_from=self, fused_topk=self.fused_topk,
+                           kv_copy=kv_copy)
 
     def input_names(self):
         """The per-step inputs a caller copies in (the K cache is state)."""
@@ -239,7 +248,7 @@ class ProducerStep:
         self._k_call(stream)
         self._q_call(stream)
 
-    def twin(self):
+    def twin(self, kv_copy: bool = False):
         return ProducerStep(self.case, device=self.device, consts_from=self)
 
     def input_names(self):
