@@ -108,6 +108,21 @@ def test_contig_fp8_many_groups():
     assert_logits_close(g[rows], ora_contig(sub))
 
 
+@pytest.mark.parametrize("rare", [False, True], ids=["common", "q_scale+negative_k_scale"])
+def test_contig_fp8_four_row_groups_ragged(rare):
+    # four-row groups (each group's rows reduced by two epilogue warpgroups),
+    # a last group of three rows, and a ragged key tail; with per-head q
+    # scales and negative key scales the epilogue takes its other path
+    M, N = 1203, 777
+    pos = np.arange(M) % N
+    c = synth.contiguous_case(12 + rare, M, N, 64, 128, ke=pos + 1,
+                              ks=np.maximum(pos - 500, 0), with_q_scale=rare)
+    if rare:
+        c.k_scale[::7] *= -1.0
+        c.q_scale[:, ::5] *= -1.0
+    assert_logits_close(gpu_contig(c), ora_contig(c))
+
+
 @pytest.mark.parametrize("M", [1, 5])
 def test_contig_mxfp4(M):
     N = 332
