@@ -371,6 +371,43 @@ idx_status idx_topk_to_ragged_slots(const int32_t *topk, int64_t ld, int rows, i
                                     idx_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * idx_row_ends -- each paged row's end ke, derived on the device from the
+ * context lengths by the rule idx_paged_mqa_logits applies to its rows.
+ * Passage: rocm_aiter_mla_sparse, rocm_fp8_paged_mqa_logits_triton (one
+ * length per row with ctx_per_row); rocm_aiter_mla, the DCP verify path (row
+ * t of a qlen-token verify attends to [0, seq_len - qlen + t]).
+ *
+ *   context_lens [B] (ctx_per_row = 0) or [B * next_n] (ctx_per_row = 1).
+ *   row_ends     int32 [B * next_n] out: row j of sequence b gets
+ *                context_lens[b] - next_n + j + 1, or context_lens[b * next_n
+ *                + j], clamped to [0, max_model_len].  These are the lengths
+ *                idx_topk, idx_topk_candidates and idx_fill_logits_tail take
+ *                for paged logits.
+ * Errors: IDX_ERR_INVALID_ARG for negative sizes, next_n <= 0 or NULL
+ *   pointers with rows > 0; IDX_ERR_CUDA when the launch fails.
+ * ---------------------------------------------------------------------- */
+idx_status idx_row_ends(const int32_t *context_lens, int ctx_per_row, int B, int next_n,
+                        int max_model_len, int32_t *row_ends, idx_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * idx_fill_logits_tail -- -inf over [row_ends[r], width) of every row.
+ * Passage: rocm_aiter_mla_sparse, rocm_fp8_paged_mqa_logits: the stage-1
+ * path fills its whole logits workspace with -inf before scoring, so every
+ * column past a row's end reads -inf.  idx_paged_mqa_logits leaves those
+ * columns untouched (its consumers read each row up to its end); a caller
+ * that hands the full-width rows to code expecting the filled workspace calls
+ * this after it.
+ *
+ *   logits   fp32 [rows, ld], width <= ld; columns [row_ends[r], width) of
+ *            row r are written -inf (row_ends clamped to [0, width]).
+ *   row_ends int32 [rows] (e.g. from idx_row_ends).
+ * Errors: IDX_ERR_INVALID_ARG for negative sizes, ld < width or NULL
+ *   pointers with rows > 0; IDX_ERR_CUDA when the launch fails.
+ * ---------------------------------------------------------------------- */
+idx_status idx_fill_logits_tail(float *logits, int64_t ld, int rows, const int32_t *row_ends,
+                                int width, idx_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * idx_k_norm_rope_store -- the K producer: normalise, rotate, quantise and
  * write each new key into its cache slot.
  * Passage: vllm/models/deepseek_v41/amd/rocm.py, rocm_mxfp4_indexer_k_store

@@ -11,9 +11,11 @@ from ._binding import (  # noqa: F401
     FMT_MXFP4,
     IndexerError,
     idx_apply_candidate_mask,
+    idx_fill_logits_tail,
     idx_get_device_status,
     idx_mqa_logits,
     idx_paged_mqa_logits,
+    idx_row_ends,
     idx_topk,
     idx_topk_to_ragged_slots,
     lib,

@@ -54,6 +54,8 @@ _SIGNATURES = {
                          _P],
     "idx_get_device_status": [_P, ctypes.POINTER(ctypes.c_uint32)],
     "idx_debug_wait_expiry": [_I, ctypes.c_uint64, _P],
+    "idx_row_ends": [_P, _I, _I, _I, _I, _P, _P],
+    "idx_fill_logits_tail": [_P, _L, _I, _P, _I, _P],
 }
 
 
@@ -487,6 +489,38 @@ def idx_q_rope_quant(q, positions, cos_sin, rope_dim, weights, weight_scale, fmt
                      weights_out, q_scale_out=None, stream=None):
     prepare_q_rope_quant(q, positions, cos_sin, rope_dim, weights, weight_scale, fmt, q_out,
                          weights_out, q_scale_out)(stream)
+
+
+def prepare_row_ends(context_lens, next_n, max_model_len, row_ends, ctx_per_row=False):
+    """row_ends int32 [B * next_n]: each paged row's end ke from the context
+    lengths (the rule of the paged logits), computed on the device."""
+    _need(context_lens, torch.int32, "context_lens")
+    _need(row_ends, torch.int32, "row_ends")
+    rows = row_ends.numel()
+    if rows % next_n:
+        raise ValueError("row_ends must hold B * next_n entries")
+    B_ = rows // next_n
+    want = rows if ctx_per_row else B_
+    if context_lens.numel() != want:
+        raise ValueError(f"context_lens must hold {want} entries")
+    return Prepared("idx_row_ends", [_ptr(context_lens), 1 if ctx_per_row else 0, B_, next_n,
+                                     max_model_len, _ptr(row_ends)],
+                    (context_lens, row_ends))
+
+
+def idx_row_ends(context_lens, next_n, max_model_len, row_ends, ctx_per_row=False, stream=None):
+    prepare_row_ends(context_lens, next_n, max_model_len, row_ends, ctx_per_row)(stream)
+
+
+def idx_fill_logits_tail(logits, row_ends, width=None, stream=None):
+    """-inf over [row_ends[r], width) of every row of logits (fp32 [rows, ld])."""
+    if logits.dtype != torch.float32 or logits.stride(1) != 1:
+        raise ValueError("logits must be float32 with unit column stride")
+    _need(row_ends, torch.int32, "row_ends")
+    width = logits.shape[1] if width is None else width
+    _check(lib().idx_fill_logits_tail(_ptr(logits), logits.stride(0), logits.shape[0],
+                                      _ptr(row_ends), width, _stream(stream)),
+           "idx_fill_logits_tail")
 
 
 def idx_debug_wait_expiry(which: int, limit_ns: int, stream=None):

@@ -251,6 +251,7 @@ extern "C" idx_status idx_mqa_logits(const void *q, const void *q_scale, const f
                                      int64_t ld_logits, void *ws, size_t ws_bytes,
                                      idx_stream_t stream)
 {
+    IDX_NVTX_RANGE("idx_mqa_logits");
     (void)ws;
     (void)ws_bytes;
     if (M < 0 || N < 0 || H <= 0 || D <= 0 || !valid_fmt(fmt))
@@ -526,6 +527,7 @@ extern "C" idx_status idx_paged_mqa_logits(
     int num_cand, int cand_block, float *logits, int64_t ld_logits, int max_model_len,
     int num_ctas, void *ws, size_t ws_bytes, idx_stream_t stream)
 {
+    IDX_NVTX_RANGE("idx_paged_mqa_logits");
     return paged_logits(false, q, q_scale, weights, kv_pages, page_stride_bytes, num_pages,
                         block_table, bt_stride, context_lens, ctx_per_row, row_ks, B, next_n, H, D,
                         page_size, fmt, candidate_blocks, cand_stride, num_cand, cand_block, logits,
@@ -540,6 +542,7 @@ extern "C" idx_status idx_paged_mqa_logits_candidates(
     int num_cand, int cand_block, float *logits, int64_t ld_logits, int max_model_len,
     int num_ctas, void *ws, size_t ws_bytes, idx_stream_t stream)
 {
+    IDX_NVTX_RANGE("idx_paged_mqa_logits_candidates");
     if (!candidate_blocks || num_cand <= 0)
         return IDX_ERR_INVALID_ARG;
     return paged_logits(true, q, q_scale, weights, kv_pages, page_stride_bytes, num_pages,
@@ -555,6 +558,7 @@ extern "C" idx_status idx_paged_mqa_logits_block_max(
     int D, int page_size, idx_kv_format fmt, float *logits, int64_t ld_logits, int max_model_len,
     float *block_max, int64_t ld_block_max, int block_size, int num_ctas, idx_stream_t stream)
 {
+    IDX_NVTX_RANGE("idx_paged_mqa_logits_block_max");
     if (!block_max)
         return IDX_ERR_INVALID_ARG;
     BlockMaxOut bm;
@@ -576,6 +580,7 @@ extern "C" idx_status idx_paged_mqa_logits_topk(
     int32_t *out_idx, int64_t ld_out, int num_ctas, void *ws, size_t ws_bytes,
     idx_stream_t stream)
 {
+    IDX_NVTX_RANGE("idx_paged_mqa_logits_topk");
     if (B < 0 || next_n <= 0 || k < 0 || ld_out < k || ld_logits <= 0 || ld_logits > INT32_MAX)
         return IDX_ERR_INVALID_ARG;
     if (B == 0 || max_model_len == 0)
@@ -640,6 +645,7 @@ extern "C" size_t idx_paged_mqa_logits_workspace_size(int B, int next_n, int max
 
 extern "C" idx_status idx_get_device_status(idx_stream_t stream, uint32_t *out)
 {
+    IDX_NVTX_RANGE("idx_get_device_status");
     if (!out)
         return IDX_ERR_INVALID_ARG;
     unsigned int *p = device_status_ptr();

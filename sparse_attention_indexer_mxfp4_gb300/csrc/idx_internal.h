@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/idx.h"
+#include <nvtx3/nvToolsExt.h>
 
 namespace idx {
 
@@ -41,6 +42,18 @@ int topk_chunked_counts(void *ws, int rows, int64_t ld, uint32_t **hist, uint32_
                         uint32_t **cvalid);
 bool topk_takes_chunked(const float *logits, int64_t ld, int rows, int k, const void *ws,
                         size_t ws_bytes);
+
+// An NVTX range around one C-ABI call, named after the entry point, so a
+// profiler's timeline shows which call launched which kernels.  NVTX is
+// header-only: without a profiler attached a range costs a test of one
+// function pointer.
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
+#define IDX_NVTX_RANGE(name) ::idx::NvtxRange idx_nvtx_range_(name)
 
 inline idx_status launch_status(cudaError_t e)
 {

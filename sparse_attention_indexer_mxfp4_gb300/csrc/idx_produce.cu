@@ -292,6 +292,7 @@ extern "C" idx_status idx_k_norm_rope_store(const uint16_t *k_pre, int64_t ld_k,
                                             int page_size, const int64_t *slot_mapping,
                                             idx_stream_t stream)
 {
+    IDX_NVTX_RANGE("idx_k_norm_rope_store");
     if (T < 0 || D <= 0 || rope_dim < 0 || rope_dim % 2 != 0 || rope_dim > D ||
         num_positions < 0 || ld_cos_sin < rope_dim || page_size <= 0 || num_pages < 0 ||
         ld_k < D || !(eps >= 0.0f) ||
@@ -326,6 +327,7 @@ extern "C" idx_status idx_q_rope_quant(const uint16_t *q, const int32_t *positio
                                        uint8_t *q_out, void *q_scale_out, float *weights_out,
                                        idx_stream_t stream)
 {
+    IDX_NVTX_RANGE("idx_q_rope_quant");
     if (T < 0 || H <= 0 || D <= 0 || rope_dim < 0 || rope_dim % 2 != 0 || rope_dim > D ||
         num_positions < 0 || ld_cos_sin < rope_dim ||
         (fmt != IDX_KV_FP8_E4M3 && fmt != IDX_KV_MXFP4))

@@ -522,6 +522,7 @@ extern "C" idx_status idx_topk(const float *logits, int64_t ld, int rows, const 
                                int k, int32_t *out_idx, int64_t ld_out, void *ws, size_t ws_bytes,
                                idx_stream_t stream)
 {
+    IDX_NVTX_RANGE("idx_topk");
     if (rows < 0 || k < 0 || ld < 0 || ld_out < k || ld > INT32_MAX)
         return IDX_ERR_INVALID_ARG;
     if (rows == 0 || k == 0)
@@ -554,6 +555,7 @@ extern "C" idx_status idx_topk_candidates(const float *logits, int64_t ld, int r
                                           int num_cand, int block_size, int row_repeat, int k,
                                           int32_t *out_idx, int64_t ld_out, idx_stream_t stream)
 {
+    IDX_NVTX_RANGE("idx_topk_candidates");
     namespace T = idx::topk_cand;
     if (rows < 0 || k < 0 || ld < 0 || ld_out < k || ld > INT32_MAX || num_cand < 0 ||
         block_size <= 0 || row_repeat <= 0 || cand_stride < num_cand)
@@ -580,6 +582,7 @@ extern "C" idx_status idx_apply_candidate_mask(float *logits, int64_t ld, int ro
                                                int64_t cand_stride, int num_cand, int block_size,
                                                int row_repeat, idx_stream_t stream)
 {
+    IDX_NVTX_RANGE("idx_apply_candidate_mask");
     if (rows < 0 || width < 0 || ld < width || num_cand < 0 || block_size <= 0 ||
         row_repeat <= 0 || cand_stride < num_cand)
         return IDX_ERR_INVALID_ARG;
@@ -611,6 +614,7 @@ extern "C" idx_status idx_topk_to_ragged_slots(const int32_t *topk, int64_t ld, 
                                                int32_t *slots, int32_t *indptr, int32_t *lens,
                                                idx_stream_t stream)
 {
+    IDX_NVTX_RANGE("idx_topk_to_ragged_slots");
     if (rows < 0 || k < 0 || ld < k || page_size <= 0 || max_blocks < 0 || num_pages < 0 ||
         bt_stride < max_blocks || (!row_to_seq && next_n <= 0))
         return IDX_ERR_INVALID_ARG;
@@ -644,6 +648,97 @@ extern "C" idx_status idx_topk_to_ragged_slots(const int32_t *topk, int64_t ld, 
         e = launch_pdl(slot_write_kernel, dim3(rows), dim3(kSlotThreads), 0, s, topk, ld, rows, k,
                        row_to_seq, next_n, g, (const int32_t *)lens, indptr, scanned, slots);
     return launch_status(e);
+}
+
+// ------------------------------------------------ row ends and tail fill
+//
+// Row ends: ke of row j of sequence b is context_lens[b] - next_n + j + 1
+// (one length per sequence: each of the next_n query tokens of an MTP step
+// sees the context up to itself) or context_lens[b * next_n + j] (one
+// length per row), clamped to [0, width] -- the rule the paged logits
+// kernel applies to its own rows (vLLM page rocm_aiter_mla_sparse,
+// rocm_fp8_paged_mqa_logits_triton, ctx_per_row).  Tail fill: -inf over
+// [ke, width) of every row, as the stage-1 path of rocm_fp8_paged_mqa_logits
+// fills its whole workspace with -inf before scoring.
+
+namespace idx {
+
+__global__ void __launch_bounds__(256) row_ends_kernel(const int32_t *__restrict__ ctx,
+                                                       int ctx_per_row, int rows, int next_n,
+                                                       int width, int32_t *__restrict__ out)
+{
+    pdl_wait();  // out may still be read by the kernel before this one
+    pdl_launch_dependents();
+    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+    if (r >= rows)
+        return;
+    const int e = ctx_per_row ? ctx[r] : ctx[r / next_n] - next_n + r % next_n + 1;
+    out[r] = min(max(e, 0), width);
+}
+
+// Grid (column blocks, rows), both strided; four columns a store where the
+// row and the tail start allow it.
+__global__ void __launch_bounds__(256) fill_tail_kernel(float *__restrict__ logits, int64_t ld,
+                                                        int rows,
+                                                        const int32_t *__restrict__ row_ends,
+                                                        int width, int vec)
+{
+    for (int r = blockIdx.y; r < rows; r += gridDim.y) {
+        const int e = min(max(row_ends[r], 0), width);
+        float *row = logits + (size_t)r * ld;
+        // scalar up to a multiple of 4 (with four-column stores), else to the end
+        const int e4 = vec ? min((e + 3) & ~3, width) : width;
+        for (int t = e + blockIdx.x * 256 + threadIdx.x; t < e4; t += gridDim.x * 256)
+            row[t] = -INFINITY;
+        if (vec) {
+            const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            for (int t = e4 + 4 * (blockIdx.x * 256 + threadIdx.x); t + 4 <= width;
+                 t += 4 * gridDim.x * 256)
+                *reinterpret_cast<float4 *>(row + t) = ninf;
+            const int w4 = e4 + (width - e4) / 4 * 4;  // scalar tail past the last full quad
+            for (int t = w4 + blockIdx.x * 256 + threadIdx.x; t < width; t += gridDim.x * 256)
+                row[t] = -INFINITY;
+        }
+    }
+}
+
+} // namespace idx
+
+extern "C" idx_status idx_row_ends(const int32_t *context_lens, int ctx_per_row, int B,
+                                   int next_n, int max_model_len, int32_t *row_ends,
+                                   idx_stream_t stream)
+{
+    IDX_NVTX_RANGE("idx_row_ends");
+    if (B < 0 || next_n <= 0 || max_model_len < 0)
+        return IDX_ERR_INVALID_ARG;
+    const long long rows = (long long)B * next_n;
+    if (rows == 0)
+        return IDX_OK;
+    if (!context_lens || !row_ends || rows > INT32_MAX)
+        return IDX_ERR_INVALID_ARG;
+    return launch_status(launch_pdl(row_ends_kernel, dim3((unsigned)((rows + 255) / 256)),
+                                    dim3(256), 0, (cudaStream_t)stream, context_lens,
+                                    ctx_per_row ? 1 : 0, (int)rows, next_n, max_model_len,
+                                    row_ends));
+}
+
+extern "C" idx_status idx_fill_logits_tail(float *logits, int64_t ld, int rows,
+                                           const int32_t *row_ends, int width,
+                                           idx_stream_t stream)
+{
+    IDX_NVTX_RANGE("idx_fill_logits_tail");
+    if (rows < 0 || width < 0 || ld < width)
+        return IDX_ERR_INVALID_ARG;
+    if (rows == 0 || width == 0)
+        return IDX_OK;
+    if (!logits || !row_ends)
+        return IDX_ERR_INVALID_ARG;
+    const int vec = (ld % 4 == 0) && aligned16(logits);
+    const dim3 grid((unsigned)std::min(64, (width + 4 * 256 - 1) / (4 * 256)),
+                    (unsigned)std::min(rows, 65535));
+    fill_tail_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>(logits, ld, rows, row_ends, width,
+                                                              vec);
+    return launch_status(cudaGetLastError());
 }
 
 // ---------------------------------------------------- bounded-wait expiry
@@ -689,6 +784,7 @@ __global__ void wait_expiry_kernel(int which, uint64_t limit_ns, unsigned *statu
 
 extern "C" idx_status idx_debug_wait_expiry(int which, uint64_t limit_ns, idx_stream_t stream)
 {
+    IDX_NVTX_RANGE("idx_debug_wait_expiry");
     if ((which != 0 && which != 1) || limit_ns == 0 || limit_ns > 10000000000ull)
         return IDX_ERR_INVALID_ARG;
     unsigned int *status = device_status_ptr();
@@ -772,6 +868,7 @@ extern "C" idx_status idx_topk_noalloc(const float *logits, int64_t ld, int rows
                                        const int32_t *lengths, int k, int32_t *out_idx,
                                        int64_t ld_out, idx_stream_t stream)
 {
+    IDX_NVTX_RANGE("idx_topk_noalloc");
     if (rows < 0 || k < 0 || ld < 0 || ld_out < k || ld > INT32_MAX)
         return IDX_ERR_INVALID_ARG;
     if (rows == 0 || k == 0)

@@ -60,7 +60,9 @@ class IndexerStep:
             self.row_ks = _dev(case.row_ks, d)
             self.cand = _dev(case.cand, d)
             ke = np.clip(case.row_ends(), 0, case.width).astype(np.int32)
-            self.lengths = _dev(ke, d)
+            # each row's end, derived on the device from the context lengths
+            # by the library (idx_row_ends) at the head of every step
+            self.lengths = torch.empty(case.rows, dtype=torch.int32, device=d)
             self.rows, self.width = case.rows, case.width
             self.max_blocks = case.max_blocks
         else:
@@ -97,6 +99,14 @@ class IndexerStep:
         """Marshal every call of the step once; run() only launches."""
         c = self.case
         self._logits_calls = []
+        # the rows' ends: the logits kernel derives its own from the context
+        # lengths, so they are needed first by the top-k (by the logits call
+        # itself when it holds the top-k)
+        self._ends_call = (B.prepare_row_ends(self.context_lens, c.next_n, c.width, self.lengths,
+                                              ctx_per_row=c.ctx_per_row)
+                           if self.paged else None)
+        if self._ends_call is not None and self.fused_topk:
+            self._logits_calls.append(self._ends_call)
         fused = None
         if self.fused_topk:
             fused = B.prepare_paged_mqa_logits_topk(
@@ -156,6 +166,8 @@ class IndexerStep:
             call(stream)
 
     def topk_stage(self, stream=None):
+        if self._ends_call is not None and not self.fused_topk:
+            self._ends_call(stream)
         if self._topk_call is not None:
             self._topk_call(stream)
         if self._pool_call is not None:
@@ -180,10 +192,12 @@ class IndexerStep:
                            kv_copy=kv_copy)
 
     def input_names(self):
-        """The per-step inputs a caller copies in (the K cache is state)."""
-        names = ["q", "weights", "lengths"]
+        """The per-step inputs a caller copies in (the K cache is state; paged
+        row ends are derived on the device from the context lengths)."""
+        names = ["q", "weights"]
         if self.paged:
             return names + ["block_table", "context_lens"] + (
+                ["row_ks"] if self.row_ks is not None else []) + (
                 ["cand"] if self.cand is not None else [])
         return names + ["ks", "ke"]
 
@@ -194,6 +208,8 @@ class IndexerStep:
     @property
     def launches_per_step(self) -> int:
         calls = self._logits_calls + ([self._topk_call] if self._topk_call is not None else [])
+        if self._ends_call is not None and not self.fused_topk:
+            calls.append(self._ends_call)
         if self._pool_call is not None:
             calls.append(self._pool_call)
         if self._slots_call is not None:

@@ -181,6 +181,20 @@ def test_select_argument_checks():
     assert L.idx_get_device_status(None, None) == INVALID
 
 
+def test_row_helper_argument_checks():
+    L = B.lib()
+    r = L.idx_row_ends
+    assert r(FAKE, 0, -1, 1, 10, FAKE, None) == INVALID     # negative batch
+    assert r(FAKE, 0, 2, 0, 10, FAKE, None) == INVALID      # next_n <= 0
+    assert r(None, 0, 2, 1, 10, FAKE, None) == INVALID
+    assert r(FAKE, 0, 0, 2, 10, FAKE, None) == 0            # no rows
+    f = L.idx_fill_logits_tail
+    assert f(FAKE, 5, 2, FAKE, 10, None) == INVALID          # ld < width
+    assert f(FAKE, 10, -1, FAKE, 10, None) == INVALID
+    assert f(FAKE, 10, 2, None, 10, None) == INVALID
+    assert f(FAKE, 10, 0, FAKE, 10, None) == 0               # nothing to fill
+
+
 def test_topk_workspace_size_query():
     f = B.topk_workspace_size
     assert f(0, 1000, 10) == 0 and f(4, 0, 10) == 0
