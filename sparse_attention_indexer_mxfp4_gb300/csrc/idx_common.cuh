@@ -145,6 +145,14 @@ IDX_DEVFN void atomic_max_float(float *addr, float v)
         atomicMin(reinterpret_cast<unsigned int *>(addr), __float_as_uint(v));
 }
 
+// Prefetch of a global line into L2.  It returns no data, so it may run
+// before a programmatic wait: a later load after the wait still reads the
+// coherent value, from L2.
+IDX_DEVFN void prefetch_l2(const void *p)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
+}
+
 // -------------------------------------------------------------------- TMA
 
 IDX_DEVFN void tma_prefetch_desc(const void *desc)

@@ -237,8 +237,19 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
         tmem_alloc(tmem_slot, C::TM_COLS);
         tmem_relinquish();
     }
-    // everything above touches only this CTA's own resources; inputs and the
-    // logits buffer may still be in use by the previous kernel on the stream
+    // the schedule's first dependent loads (each row's context length and
+    // start) go to L2 while the previous kernel on the stream finishes
+    if (a.paged && warp == kMmaWarp + 1) {
+        const int nctx = a.ctx_per_row ? a.total_rows : a.num_groups;
+        for (int i = lane * 32; i < nctx; i += 32 * 32)
+            prefetch_l2(a.ctx + i);
+        if (a.row_ks)
+            for (int i = lane * 32; i < a.total_rows; i += 32 * 32)
+                prefetch_l2(a.row_ks + i);
+    }
+    // everything above touches only this CTA's own resources (and prefetches
+    // into L2); inputs and the logits buffer may still be in use by the
+    // previous kernel on the stream
     pdl_wait();
     pdl_launch_dependents();
     int g0, k0, n0;

@@ -5,11 +5,14 @@
 // Passage: vLLM page rocm_paged_mxfp4_indexer, _topk -- top-k over each
 // row's [0, lengths[row]), -1 padding.  The design is our own.
 //
-// A row is cut into chunks of 32768 keys; chunk c goes to the cluster's CTA
-// of rank c (clusters of C <= 8 CTAs of 1024 threads, one CTA per SM by
-// its shared memory).  Every CTA keeps its chunk as order-preserving keys
+// A row's keys [0, len) are cut into C equal chunks (a multiple of four keys
+// each, at most 32768); chunk c goes to the cluster's CTA of rank c
+// (clusters of C = ceil(ld / 32768) <= 8 CTAs of 1024 threads, one CTA per
+// SM by its shared memory), so a row shorter than the width still spreads
+// over the whole cluster.  Every CTA keeps its chunk as order-preserving keys
 // in shared memory, thread t holding positions 4 (1024 s + t) + e of the
-// chunk (s < 8, e < 4), so (rank, s, warp, lane, e) is index order.  The
+// chunk (s < 8, e < 4), so (rank, s, warp, lane, e) is index order; every
+// pass visits only the runs s that hold keys of the CTA's chunk.  The
 // 11/11/10-bit radix select runs on histograms each CTA builds over its own
 // keys; after a cluster barrier every CTA adds up the C histograms of the
 // digit through distributed shared memory and finds the same bin itself, so
@@ -99,8 +102,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const bool live = row < rows;
     const int len = live ? max(0, min(lengths[row], (int)ld)) : 0;
-    const int base = rank * kChunk;
-    const int end = max(0, min(len - base, kChunk));  // keys of this CTA's chunk
+    // the row's keys spread evenly over the cluster, whole quads per CTA (the
+    // chunk starts stay 16-byte aligned for vector loads)
+    const int per = min(kChunk, ((len + C - 1) / C + 3) & ~3);
+    const int base = rank * per;
+    const int end = max(0, min(len - base, per));        // keys of this CTA's chunk
+    const int nrun = (end + 4 * kThreads - 1) / (4 * kThreads);  // runs holding them
     const float *rowp = logits + (size_t)(live ? row : 0) * ld + base;
 
     // keys of this chunk into shared memory, the local digit-1 histogram
@@ -114,6 +121,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncthreads();
         #pragma unroll
         for (int s = 0; s < kSteps; ++s) {
+            if (s >= nrun)
+                break;
             sh.keys[s * kThreads + tid] = make_uint4(key[s][0], key[s][1], key[s][2], key[s][3]);
             #pragma unroll
             for (int e = 0; e < 4; ++e)
@@ -142,6 +151,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t krem = sh.sel[0][1];
         #pragma unroll
         for (int s = 0; s < kSteps; ++s) {
+            if (s >= nrun)
+                break;
             const uint4 v = run(s);
             const uint32_t kk[4] = {v.x, v.y, v.z, v.w};
             #pragma unroll
@@ -156,6 +167,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         krem = sh.sel[1][1];
         #pragma unroll
         for (int s = 0; s < kSteps; ++s) {
+            if (s >= nrun)
+                break;
             const uint4 v = run(s);
             const uint32_t kk[4] = {v.x, v.y, v.z, v.w};
             #pragma unroll
@@ -177,6 +190,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // when every key equal to T is taken) and keys equal to T
     #pragma unroll
     for (int s = 0; s < kSteps; ++s) {
+        if (s >= nrun) {  // runs without keys count nothing
+            if (lane == 0) {
+                sh.gt[s * kWarps + w] = 0u;
+                sh.eq[s * kWarps + w] = 0u;
+            }
+            continue;
+        }
         const uint4 v = run(s);
         const uint32_t kk[4] = {v.x, v.y, v.z, v.w};
         uint32_t ngt = 0, neq = 0;
@@ -217,6 +237,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (live) {
         #pragma unroll
         for (int s = 0; s < kSteps; ++s) {
+            if (s >= nrun)
+                break;
             const uint4 v = run(s);
             const uint32_t key[4] = {v.x, v.y, v.z, v.w};
             const uint32_t eq0 = eq_before + sh.eq[s * kWarps + w];

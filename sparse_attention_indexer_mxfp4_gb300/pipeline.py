@@ -100,12 +100,14 @@ class IndexerStep:
         c = self.case
         self._logits_calls = []
         # the rows' ends: the logits kernel derives its own from the context
-        # lengths, so they are needed first by the top-k (by the logits call
-        # itself when it holds the top-k)
+        # lengths, so they are needed first by the top-k -- or already in the
+        # logits stage, when it holds the top-k or the standalone candidate mask
         self._ends_call = (B.prepare_row_ends(self.context_lens, c.next_n, c.width, self.lengths,
                                               ctx_per_row=c.ctx_per_row)
                            if self.paged else None)
-        if self._ends_call is not None and self.fused_topk:
+        self._ends_first = self.paged and (
+            self.fused_topk or (self.cand is not None and not self.fused_mask))
+        if self._ends_call is not None and self._ends_first:
             self._logits_calls.append(self._ends_call)
         fused = None
         if self.fused_topk:
@@ -166,7 +168,7 @@ class IndexerStep:
             call(stream)
 
     def topk_stage(self, stream=None):
-        if self._ends_call is not None and not self.fused_topk:
+        if self._ends_call is not None and not self._ends_first:
             self._ends_call(stream)
         if self._topk_call is not None:
             self._topk_call(stream)
@@ -208,7 +210,7 @@ class IndexerStep:
     @property
     def launches_per_step(self) -> int:
         calls = self._logits_calls + ([self._topk_call] if self._topk_call is not None else [])
-        if self._ends_call is not None and not self.fused_topk:
+        if self._ends_call is not None and not self._ends_first:
             calls.append(self._ends_call)
         if self._pool_call is not None:
             calls.append(self._pool_call)
