@@ -89,10 +89,10 @@ def producer_bytes(case) -> float:
 # since and the traffic is reported as null.
 LOGITS_SOURCES = ["idx_logits_kernel.cuh", "idx_logits.cuh", "idx_common.cuh", "idx_api.cu"]
 NCU_TRAFFIC = {
-    4: {"bytes": 91136 + 189573632 + 8378112, "digest": "81d1e06d97682009",
-        "profile": "profiles/logits_kernel_paged_fp8_decode_b128_mtp2.md"},
-    6: {"bytes": 3840 + 413373184 + 21578496, "digest": "81d1e06d97682009",
-        "profile": "profiles/logits_kernel_candidate_source_b128_mtp2.md"},
+    3: {"bytes": 157692928 + 5200896, "digest": "e66ed00d05df2299",
+        "profile": "profiles/logits_kernel_paged_fp8_decode_b64.md"},
+    5: {"bytes": 285843712 + 14587392, "digest": "e66ed00d05df2299",
+        "profile": "profiles/logits_kernel_paged_mxfp4_decode_b32.md"},
 }
 
 
@@ -376,10 +376,13 @@ def measure(cfg: int, args, dev, world: int, rank: int, headline: bool) -> dict:
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
-    ms_per_step, logit_ms, topk_ms, mode = timing
+    ms_per_step, logit_ms, topk_ms, loop_ms, mode = timing
     assert idx_get_device_status() == 0, f"device status set during the timed steps (config {cfg})"
-    ms_per_step, logit_avg, topk_avg = max_over_ranks(
-        [ms_per_step, sum(logit_ms) / len(logit_ms), sum(topk_ms) / len(topk_ms)], dev, world)
+    logit_step = sum(logit_ms) / len(logit_ms)
+    topk_step = sum(topk_ms) / len(topk_ms)
+    ms_per_step, logit_step, topk_step, logit_avg, topk_avg = max_over_ranks(
+        [ms_per_step, logit_step, topk_step, loop_ms.get("logits_stage", logit_step),
+         loop_ms.get("topk_stage", topk_step)], dev, world)
 
     keys = _work(case) if prod else scored_keys(case)
     rows = case.rows if paged or prod else case.M
@@ -398,7 +401,7 @@ def measure(cfg: int, args, dev, world: int, rank: int, headline: bool) -> dict:
                 "unit": "TFLOP/s", "frac": round(ach / fp8_peak, 4), "traffic": None,
                 "peak_source": f"{src} bf16_tflops x 2 (fp8 dense)", "kernel": "logits_kernel",
                 "algorithmic_flops_per_launch": logits_flops(case),
-                "avg_launch_ms": round(logit_avg, 5)}
+                "avg_launch_ms": round(logit_avg, 5), "stage_ms_in_step": round(logit_step, 5)}
     else:
         lb = logits_bytes(case, cand_only=getattr(step, "cand_topk", False))
         if fused:  # the stage also holds the top-k: one more read of the live logits
@@ -414,7 +417,8 @@ def measure(cfg: int, args, dev, world: int, rank: int, headline: bool) -> dict:
                            "logits_kernel" if getattr(case, "cand", None) is not None
                            else "logits stage: bmax_fill_kernel + logits_kernel with block "
                            "maxima" if getattr(case, "source_block", 0) else "logits_kernel"),
-                "algorithmic_bytes_per_launch": lb, "avg_launch_ms": round(logit_avg, 5)}
+                "algorithmic_bytes_per_launch": lb, "avg_launch_ms": round(logit_avg, 5),
+                "stage_ms_in_step": round(logit_step, 5)}
     out = {
         "workload": WORKLOAD_NAMES[cfg], "config_id": cfg, "metric": metric,
         "value": round(job_value(world, keys, ms_per_step, div), 4), "unit": unit,
@@ -434,11 +438,14 @@ def measure(cfg: int, args, dev, world: int, rank: int, headline: bool) -> dict:
             "keys_scored_per_step": keys,
             "keys_dense_equivalent_per_step": case.keys_scored,
             "logits_ms": round(logit_avg, 5), "topk_ms": round(topk_avg, 5),
+            "logits_stage_ms_in_step": round(logit_step, 5),
+            "topk_stage_ms_in_step": round(topk_step, 5),
             "topk_rows_per_s": round(world * rows / (topk_avg * 1e-3), 1),
             "topk_roofline": {"bound": "hbm", "achieved": round(tach, 1), "peak": hbm,
                               "unit": "GB/s", "frac": round(tach / hbm, 4),
                               "algorithmic_bytes_per_launch": tb,
                               "avg_launch_ms": round(topk_avg, 5),
+                              "stage_ms_in_step": round(topk_step, 5),
                               "peak_source": f"{src} hbm_gbs"},
             "fused_topk": fused,
         })
@@ -564,6 +571,28 @@ def time_steps_graph(steps, K, flush, clock_soak_s=0.4):
         return g
 
     g_step, g_stages = capture(False), capture(True)
+
+    # per-launch time of each stage in steady state: K launches of the stage
+    # alone, back to back (rotating buffer sets), events only at the ends, so
+    # each launch overlaps the end of the one before as it does in a step
+    loop_ms = {}
+    if flush is None:
+        for name in ("logits_stage", "topk_stage"):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                for i in range(K):
+                    getattr(steps[i % len(steps)], name)()
+            torch.cuda.synchronize()
+            g.replay()
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(side):
+                e0.record()
+                g.replay()
+                e1.record()
+            torch.cuda.synchronize()
+            loop_ms[name] = e0.elapsed_time(e1) / K
     t_end = time.time() + clock_soak_s
     while time.time() < t_end:
         g_step.replay()
@@ -582,8 +611,10 @@ def time_steps_graph(steps, K, flush, clock_soak_s=0.4):
     logit_ms = [e[0].elapsed_time(e[1]) for e in evs]
     topk_ms = [e[1].elapsed_time(e[2]) for e in evs]
     ms = sum(step_ms) / K if flush is not None else total / K
-    return ms, logit_ms, topk_ms, ("cuda graph of the K steps, one replay (stage times from a "
-                                   "second replay with events between the stages)")
+    return ms, logit_ms, topk_ms, loop_ms, (
+        "cuda graph of the K steps, one replay; stage times in the step from a second replay "
+        "with events between the stages; per-launch stage times from graphs of K back-to-back "
+        "launches of each stage")
 
 
 def time_steps_eager(steps, K, flush):
@@ -605,7 +636,7 @@ def time_steps_eager(steps, K, flush):
     logit_ms = [e[0].elapsed_time(e[1]) for e in ev]
     topk_ms = [e[1].elapsed_time(e[2]) for e in ev]
     step_ms = [e[0].elapsed_time(e[3]) for e in ev]
-    return sum(step_ms) / K, logit_ms, topk_ms, "eager launches"
+    return sum(step_ms) / K, logit_ms, topk_ms, {}, "eager launches"
 
 
 def run_e2e(step, case, args, dev):
