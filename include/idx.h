@@ -117,7 +117,9 @@ idx_status idx_mqa_logits(const void *q, const void *q_scale, const float *weigh
  *   logits    fp32 [B * next_n, ld_logits], ld_logits >= max_model_len.  Only
  *             columns [0, ke) of each row are written; [ke, max_model_len) is
  *             left untouched (consumers read each row up to its length).
- *   num_ctas  0 = one persistent CTA per SM; otherwise the grid size.
+ *   num_ctas  0 = one persistent CTA per resident slot: the CTAs the
+ *             occupancy calculator places on an SM for the launched kernel and
+ *             its shared memory, times the SMs; otherwise the grid size.
  *   ws, ws_bytes  optional device scratch, 16-byte aligned.  With a fused
  *             candidate mask and ws_bytes >= idx_paged_mqa_logits_workspace_size
  *             (B, next_n, max_model_len, num_cand), a first kernel writes a

@@ -220,7 +220,8 @@ def prepare_paged_mqa_logits_block_max(q, q_scale, weights, kv_pages, block_tabl
     _need(weights, torch.float32, "weights")
     _need(block_table, torch.int32, "block_table")
     _need(context_lens, torch.int32, "context_lens")
-    _need(block_max, torch.float32, "block_max")
+    if block_max.dtype != torch.float32 or block_max.stride(1) != 1:
+        raise ValueError("block_max must be float32 with unit column stride")
     if kv_pages.dtype != torch.uint8 or kv_pages.dim() != 2 or kv_pages.stride(1) != 1:
         raise ValueError("kv_pages must be uint8 [num_pages, page_stride] with unit byte stride")
     args = (_ptr(q), _ptr(q_scale), _ptr(weights), _ptr(kv_pages), kv_pages.stride(0),

@@ -1,5 +1,6 @@
 // idx_api.cu -- C ABI entry points of the logits kernels, argument checks,
 // TMA descriptor encoding and the device status word.
+#include <climits>
 #include <cstdio>
 #include <cudaTypedefs.h>
 #include <mutex>
@@ -102,9 +103,13 @@ constexpr int kMaxSmemBytes = 227 * 1024;
 
 // BM: whether this instantiation also has the block-maxima variant (dense
 // walks of one- and two-row groups, the candidate source's shapes).
+// nctas: the grid size, or 0 for one persistent CTA per resident slot: the
+// CTAs the occupancy calculator places on an SM for this kernel and shared
+// memory, times the SMs (capped at max_ctas).
 template <int FMT, int H, int G, int S, int NA, int TK, bool BM>
 cudaError_t launch_logits_t(const LogitsArgs &a0, const CUtensorMap &tmK, const CUtensorMap &tmQ,
-                            const CUtensorMap &tmS, int nctas, cudaStream_t stream)
+                            const CUtensorMap &tmS, int nctas, long long max_ctas,
+                            cudaStream_t stream)
 {
     using C = LogitsCfg<FMT, H, G, S, NA, TK>;
     LogitsArgs a = a0;
@@ -145,6 +150,23 @@ cudaError_t launch_logits_t(const LogitsArgs &a0, const CUtensorMap &tmK, const 
             return e;
         configured[variant][dev] = 1;
     }
+    if (nctas <= 0) {
+        // resident CTAs per SM for this kernel and shared memory, cached per
+        // (variant, device) with the shared memory it was asked for
+        static int occ[5][kMaxDevices] = {};
+        static size_t occ_smem[5][kMaxDevices] = {};
+        if (!occ[variant][dev] || occ_smem[variant][dev] != smem) {
+            int n = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, C::THREADS, smem) !=
+                    cudaSuccess ||
+                n < 1)
+                return cudaErrorNotSupported;
+            occ[variant][dev] = n;
+            occ_smem[variant][dev] = smem;
+        }
+        const long long want = (long long)occ[variant][dev] * sm_count();
+        nctas = (int)std::max<long long>(1, std::min(want, max_ctas));
+    }
     return launch_pdl(kern, dim3(nctas), dim3(C::THREADS), smem, stream, a, tmK, tmQ, tmS);
 }
 
@@ -159,27 +181,27 @@ size_t logits_smem_t(int cand_words)
 // Dispatch on (format, heads, rows per group) to the compiled instantiations.
 cudaError_t launch_logits(int fmt, int H, int G, const LogitsArgs &a, const CUtensorMap &tmK,
                           const CUtensorMap &tmQ, const CUtensorMap &tmS, int nctas,
-                          cudaStream_t s, bool *supported)
+                          long long max_ctas, cudaStream_t s, bool *supported)
 {
     *supported = true;
     if (H == 64 && fmt == kFmtFp8) {
         switch (G) {
-        case 1: return launch_logits_t<kFmtFp8, 64, 1, 4, 2, 256, true>(a, tmK, tmQ, tmS, nctas, s);
+        case 1: return launch_logits_t<kFmtFp8, 64, 1, 4, 2, 256, true>(a, tmK, tmQ, tmS, nctas, max_ctas, s);
         case 2:
             // under a gather plan, 128-key tiles: candidate blocks of 128 keys
             // then fill whole tiles and stages
             if (a.plan)
-                return launch_logits_t<kFmtFp8, 64, 2, 6, 3, 128, false>(a, tmK, tmQ, tmS, nctas, s);
-            return launch_logits_t<kFmtFp8, 64, 2, 4, 2, 256, true>(a, tmK, tmQ, tmS, nctas, s);
+                return launch_logits_t<kFmtFp8, 64, 2, 6, 3, 128, false>(a, tmK, tmQ, tmS, nctas, max_ctas, s);
+            return launch_logits_t<kFmtFp8, 64, 2, 4, 2, 256, true>(a, tmK, tmQ, tmS, nctas, max_ctas, s);
         case 4:
             if (a.bmax)
                 break;  // no block-maxima variant for four-row groups
-            return launch_logits_t<kFmtFp8, 64, 4, 8, 2, 128, false>(a, tmK, tmQ, tmS, nctas, s);
+            return launch_logits_t<kFmtFp8, 64, 4, 8, 2, 128, false>(a, tmK, tmQ, tmS, nctas, max_ctas, s);
         }
     } else if (H == 64 && fmt == kFmtMxfp4) {
         switch (G) {
-        case 1: return launch_logits_t<kFmtMxfp4, 64, 1, 8, 2, 256, true>(a, tmK, tmQ, tmS, nctas, s);
-        case 2: return launch_logits_t<kFmtMxfp4, 64, 2, 12, 3, 128, true>(a, tmK, tmQ, tmS, nctas, s);
+        case 1: return launch_logits_t<kFmtMxfp4, 64, 1, 8, 2, 256, true>(a, tmK, tmQ, tmS, nctas, max_ctas, s);
+        case 2: return launch_logits_t<kFmtMxfp4, 64, 2, 12, 3, 128, true>(a, tmK, tmQ, tmS, nctas, max_ctas, s);
         }
     }
     *supported = false;
@@ -328,10 +350,9 @@ extern "C" idx_status idx_mqa_logits(const void *q, const void *q_scale, const f
     if (!a.status)
         return IDX_ERR_CUDA;
     const long long units = (long long)a.num_groups * T;
-    const int nctas = (int)(units < nsm ? units : nsm);
     bool supported = false;
-    cudaError_t e =
-        launch_logits(f, H, G, a, tmK, tmQ, tmS, nctas, (cudaStream_t)stream, &supported);
+    cudaError_t e = launch_logits(f, H, G, a, tmK, tmQ, tmS, 0, units, (cudaStream_t)stream,
+                                  &supported);
     if (!supported)
         return IDX_ERR_UNSUPPORTED;
     return launch_status(e);
@@ -481,7 +502,7 @@ static idx_status paged_logits(bool cand_only,
         return IDX_ERR_CUDA;
     if (check_only)  // every host check passed; nothing is launched
         return IDX_OK;
-    const int nctas = num_ctas > 0 ? num_ctas : sm_count();
+    const int nctas = num_ctas;  // 0: from the occupancy of the kernel launched
     // gather path: with a fused candidate mask and scratch for the plan, only
     // tiles and 64-key boxes that hold a candidate key are loaded and scored
     const size_t plan_need =
@@ -512,8 +533,8 @@ static idx_status paged_logits(bool cand_only,
             return IDX_ERR_CUDA;
     }
     bool supported = false;
-    cudaError_t e =
-        launch_logits(f, H, G, a, tmK, tmQ, tmS, nctas, (cudaStream_t)stream, &supported);
+    cudaError_t e = launch_logits(f, H, G, a, tmK, tmQ, tmS, nctas, LLONG_MAX, (cudaStream_t)stream,
+                                  &supported);
     if (!supported || e == cudaErrorNotSupported)
         return IDX_ERR_UNSUPPORTED;
     return launch_status(e);
