@@ -30,10 +30,12 @@ __global__ void candidate_mask_kernel(float *__restrict__ logits, int64_t ld, in
 {
     extern __shared__ uint32_t bm[];
     const int r = blockIdx.x;
-    if (r >= rows)
-        return;
     for (int i = threadIdx.x; i < words; i += blockDim.x)
         bm[i] = 0u;
+    pdl_wait();  // the logits, ranges and candidates may come from the kernel before this one
+    pdl_launch_dependents();
+    if (r >= rows)
+        return;
     __syncthreads();
     const int32_t *cr = cand + (size_t)(r / row_repeat) * cand_stride;
     for (int e = threadIdx.x; e < num_cand; e += blockDim.x) {
@@ -76,28 +78,33 @@ struct SlotGeom {
 constexpr int kSlotThreads = 256;
 constexpr int kSlotSteps = 8;  // entries per thread loaded before any is used
 
-// Slots of entries j = base + i * kSlotThreads + tid (i < kSlotSteps) of one
-// top-k row of sequence b: >= 0 a slot, -1 no entry (-1 or past k), -2 an
-// invalid position (logical page beyond max_blocks or page id outside the
-// pool).  The index loads are all issued first, then the block-table loads.
-__device__ __forceinline__ void row_slots(const int32_t *trow, int k, int base, int b,
-                                          const SlotGeom &g, int (&s)[kSlotSteps])
+// Top-k entries j = base + i * kSlotThreads + tid (i < kSlotSteps) of one
+// row, -1 past k; the loads are all issued before any is used.
+__device__ __forceinline__ void row_pos(const int32_t *trow, int k, int base,
+                                        int (&p)[kSlotSteps])
 {
-    int p[kSlotSteps];
     #pragma unroll
     for (int i = 0; i < kSlotSteps; ++i) {
         const int j = base + i * kSlotThreads + (int)threadIdx.x;
         p[i] = j < k ? __ldg(trow + j) : -1;
     }
-    int lp[kSlotSteps], pg[kSlotSteps];
+}
+
+// Slots of positions p of one sequence whose block-table row is btrow:
+// >= 0 a slot, -1 no entry, -2 an invalid position (logical page beyond
+// max_blocks or page id outside the pool).
+template <int N>
+__device__ __forceinline__ void pos_slots(const int (&p)[N], const int32_t *btrow,
+                                          const SlotGeom &g, int (&s)[N])
+{
+    int lp[N], pg[N];
     #pragma unroll
-    for (int i = 0; i < kSlotSteps; ++i) {
+    for (int i = 0; i < N; ++i) {
         lp[i] = p[i] < 0 ? -1 : (g.shift >= 0 ? p[i] >> g.shift : p[i] / g.P);
-        pg[i] = lp[i] >= 0 && lp[i] < g.max_blocks
-                    ? __ldg(g.bt + (size_t)b * g.bt_stride + lp[i]) : -1;
+        pg[i] = lp[i] >= 0 && lp[i] < g.max_blocks ? __ldg(btrow + lp[i]) : -1;
     }
     #pragma unroll
-    for (int i = 0; i < kSlotSteps; ++i) {
+    for (int i = 0; i < N; ++i) {
         if (p[i] < 0)
             s[i] = -1;
         else if (lp[i] >= g.max_blocks || pg[i] < 0 || pg[i] >= g.num_pages)
@@ -119,9 +126,11 @@ __global__ void __launch_bounds__(kSlotThreads)
     const int b = row_to_seq ? row_to_seq[r] : r / next_n;
     const int32_t *trow = topk + (size_t)r * ld;
     uint32_t cnt = 0, bad = 0;
+    const int32_t *btrow = g.bt + (size_t)b * g.bt_stride;
     for (int base = 0; base < k; base += kSlotSteps * kSlotThreads) {
-        int sl[kSlotSteps];
-        row_slots(trow, k, base, b, g, sl);
+        int p[kSlotSteps], sl[kSlotSteps];
+        row_pos(trow, k, base, p);
+        pos_slots(p, btrow, g, sl);
         #pragma unroll
         for (int i = 0; i < kSlotSteps; ++i) {
             cnt += sl[i] >= 0;
@@ -219,8 +228,10 @@ __global__ void __launch_bounds__(kSlotThreads)
     const uint32_t lt = (1u << lane) - 1u;
     const int32_t *trow = topk + (size_t)r * ld;
     // the first batch's loads go out before the offset is summed
-    int sl[kSlotSteps];
-    row_slots(trow, k, 0, b, g, sl);
+    const int32_t *btrow = g.bt + (size_t)b * g.bt_stride;
+    int p[kSlotSteps], sl[kSlotSteps];
+    row_pos(trow, k, 0, p);
+    pos_slots(p, btrow, g, sl);
     uint32_t off = 0;
     if (scanned) {
         off = (uint32_t)indptr[r];
@@ -244,8 +255,10 @@ __global__ void __launch_bounds__(kSlotThreads)
     int32_t *dst = slots + off;
     uint32_t written = 0;
     for (int base = 0; base < k; base += kSlotSteps * kSlotThreads) {
-        if (base > 0)
-            row_slots(trow, k, base, b, g, sl);
+        if (base > 0) {
+            row_pos(trow, k, base, p);
+            pos_slots(p, btrow, g, sl);
+        }
         uint32_t ball[kSlotSteps];
         #pragma unroll
         for (int i = 0; i < kSlotSteps; ++i) {
@@ -278,6 +291,139 @@ __global__ void __launch_bounds__(kSlotThreads)
     }
 }
 
+// Slot map in one launch, for the row counts of a decode step: one
+// thread-block cluster of C CTAs, CTA q taking rows [q R, q R + R).  Each CTA
+// stages its rows' block-table rows in shared memory, forms its rows' slots
+// (at most kScPairs per thread, in registers), counts the valid ones per
+// (row, step, warp) and scans them per row; after a cluster barrier each CTA
+// adds up the lower ranks' totals through distributed shared memory for its
+// first offset, then writes its rows' lens, indptr and slots in entry order.
+// A second barrier, arrived at once the totals are read and waited on at
+// the end, keeps every CTA's shared memory alive until the others are done
+// with it.  Entry e of a row is held by thread e % 1024 at step e / 1024;
+// pair u of a thread is (row u / E, step u % E).
+constexpr int kScThreads = 1024;
+constexpr int kScWarps = kScThreads / 32;
+constexpr int kScPairs = 4;            // (row, step) pairs per CTA
+constexpr int kScMaxBt = 32768;        // staged block-table words per CTA
+
+struct ScShared {
+    uint32_t tab[kScPairs * kScWarps];  // valid slots per (pair, warp), then offsets
+    uint32_t rowcnt[kScPairs];
+    uint32_t rowoff[kScPairs];  // offset of each row within the CTA's rows
+    uint32_t total;             // the CTA's valid slots (read by higher ranks)
+    uint32_t base;              // the lower ranks' valid slots
+};
+
+__global__ void __launch_bounds__(kScThreads, 1)
+    slot_cluster_kernel(const int32_t *__restrict__ topk, int64_t ld, int rows, int k,
+                        const int32_t *__restrict__ row_to_seq, int next_n, SlotGeom g, int R,
+                        int32_t *__restrict__ slots, int32_t *__restrict__ indptr,
+                        int32_t *__restrict__ lens, unsigned int *status)
+{
+    extern __shared__ __align__(16) uint8_t dsm[];
+    ScShared &sh = *reinterpret_cast<ScShared *>(dsm);
+    int32_t *sbt = reinterpret_cast<int32_t *>(dsm + sizeof(ScShared));  // [row][max_blocks]
+    cooperative_groups::cluster_group cl = cooperative_groups::this_cluster();
+    const int q = (int)cl.block_rank();
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int E = (k + kScThreads - 1) / kScThreads;
+    const int r0 = q * R, nr = max(0, min(R, rows - r0));
+    const int npair = nr * E;
+    pdl_wait();  // the top-k rows may come from the kernel before this one
+    pdl_launch_dependents();
+    int pos[kScPairs];
+    #pragma unroll
+    for (int u = 0; u < kScPairs; ++u) {
+        const int j = u / E, e = (u - j * E) * kScThreads + tid;
+        pos[u] = u < npair && e < k ? __ldg(topk + (size_t)(r0 + j) * ld + e) : -1;
+    }
+    // block-table rows of the CTA's rows, while the top-k entries are in flight
+    for (int j = 0; j < nr; ++j) {
+        const int b = row_to_seq ? __ldg(row_to_seq + r0 + j) : (r0 + j) / next_n;
+        const int32_t *btrow = g.bt + (size_t)b * g.bt_stride;
+        for (int i = tid; i < g.max_blocks; i += kScThreads)
+            sbt[j * g.max_blocks + i] = __ldg(btrow + i);
+    }
+    __syncthreads();
+    int sl[kScPairs];
+    uint32_t bad = 0;
+    #pragma unroll
+    for (int u = 0; u < kScPairs; ++u) {
+        const int j = u / E;
+        sl[u] = -1;
+        if (pos[u] >= 0) {
+            const int lp = g.shift >= 0 ? pos[u] >> g.shift : pos[u] / g.P;
+            const int pg = lp < g.max_blocks ? sbt[j * g.max_blocks + lp] : -1;
+            if (lp >= g.max_blocks || pg < 0 || pg >= g.num_pages)
+                bad = 1;
+            else
+                sl[u] = pg * g.P + (pos[u] - lp * g.P);
+        }
+        const uint32_t ball = __ballot_sync(0xffffffffu, sl[u] >= 0);
+        if (lane == 0 && u < npair)
+            sh.tab[u * kScWarps + w] = __popc(ball);
+    }
+    if (bad)
+        atomicOr(status, kDevBadPage);
+    __syncthreads();
+    // per row: exclusive offsets of its (step, warp) counts in that order
+    // (lane l holds entries l E .. l E + E - 1, E <= 4) and the row's count
+    if (w < nr) {
+        uint32_t *t = sh.tab + w * E * kScWarps;
+        uint32_t v[kScPairs], sum = 0;
+        #pragma unroll
+        for (int e = 0; e < kScPairs; ++e) {
+            v[e] = e < E ? t[lane * E + e] : 0u;
+            sum += v[e];
+        }
+        uint32_t tot;
+        uint32_t run = topk_detail::warp_excl(sum, lane, &tot);
+        #pragma unroll
+        for (int e = 0; e < kScPairs; ++e) {
+            if (e < E)
+                t[lane * E + e] = run;
+            run += v[e];
+        }
+        if (lane == 0)
+            sh.rowcnt[w] = tot;
+    }
+    __syncthreads();
+    if (w == 0) {
+        const uint32_t c = lane < nr ? sh.rowcnt[lane] : 0u;
+        uint32_t tot;
+        const uint32_t ex = topk_detail::warp_excl(c, lane, &tot);
+        if (lane < nr)
+            sh.rowoff[lane] = ex;
+        if (lane == 0)
+            sh.total = tot;
+    }
+    cl.sync();  // every CTA's total is published
+    if (w == 0) {
+        uint32_t v = lane < q ? *cl.map_shared_rank(&sh.total, lane) : 0u;
+        v = __reduce_add_sync(0xffffffffu, v);
+        if (lane == 0)
+            sh.base = v;
+    }
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");  // done reading others
+    __syncthreads();
+    const uint32_t base = sh.base;
+    if (tid < nr) {
+        lens[r0 + tid] = (int32_t)sh.rowcnt[tid];
+        indptr[r0 + tid + 1] = (int32_t)(base + sh.rowoff[tid] + sh.rowcnt[tid]);
+    }
+    if (q == 0 && tid == 0)
+        indptr[0] = 0;
+    const uint32_t lt = (1u << lane) - 1u;
+    #pragma unroll
+    for (int u = 0; u < kScPairs; ++u) {
+        const uint32_t ball = __ballot_sync(0xffffffffu, sl[u] >= 0);
+        if (sl[u] >= 0)
+            slots[base + sh.rowoff[u / E] + sh.tab[u * kScWarps + w] + __popc(ball & lt)] = sl[u];
+    }
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ top-k
 
 idx_status topk_launch_per_row(const float *logits, int64_t ld, int rows,
@@ -296,9 +442,8 @@ idx_status topk_launch_per_row(const float *logits, int64_t ld, int rows,
             return IDX_ERR_CUDA;
         configured[dev] = 1;
     }
-    T::topk_kernel<<<rows, T::kThreads, smem, s>>>(logits, ld, rows, lengths, k, out, ld_out,
-                                                   vec_ok);
-    return launch_status(cudaGetLastError());
+    return launch_status(launch_pdl(T::topk_kernel, dim3(rows), dim3(T::kThreads), smem, s,
+                                    logits, ld, rows, lengths, k, out, ld_out, vec_ok));
 }
 
 // Rows of at most 8192 keys: one 256-thread CTA per row, keys in registers.
@@ -306,9 +451,8 @@ idx_status topk_launch_short(const float *logits, int64_t ld, int rows, const in
                              int k, int32_t *out, int64_t ld_out, int vec_ok, cudaStream_t s)
 {
     namespace T = topk_short;
-    T::topk_short_kernel<<<rows, T::kThreads, 0, s>>>(logits, ld, rows, lengths, k, out, ld_out,
-                                                      vec_ok);
-    return launch_status(cudaGetLastError());
+    return launch_status(launch_pdl(T::topk_short_kernel, dim3(rows), dim3(T::kThreads), 0, s,
+                                    logits, ld, rows, lengths, k, out, ld_out, vec_ok));
 }
 
 // Rows of up to 262144 keys: one cluster of ceil(ld / 32768) CTAs per row,
@@ -337,11 +481,13 @@ idx_status topk_launch_cluster(const float *logits, int64_t ld, int rows, const 
             return IDX_ERR_CUDA;
         configured[dev] = 1;
     }
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)C;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(rows * C));
     cfg.blockDim = dim3(T::kThreads);
@@ -358,6 +504,7 @@ idx_status topk_launch_cluster(const float *logits, int64_t ld, int rows, const 
     }
     if (resident[dev][C] < 0)
         return IDX_ERR_UNSUPPORTED;
+    cfg.numAttrs = 2;  // launched programmatically after the kernel before it
     return launch_status(cudaLaunchKernelEx(&cfg, T::topk_cluster_kernel, logits, ld, rows,
                                             lengths, k, out, ld_out, vec_ok));
 }
@@ -601,11 +748,83 @@ extern "C" idx_status idx_apply_candidate_mask(float *logits, int64_t ld, int ro
         return IDX_ERR_CUDA;
     const int cols = (int)std::min<long long>(64, (width + 4095) / 4096);
     dim3 grid(rows, cols < 1 ? 1 : cols);
-    candidate_mask_kernel<<<grid, 256, smem, (cudaStream_t)stream>>>(
-        logits, ld, rows, width, row_ks, row_ke, candidate_blocks, cand_stride, num_cand,
-        block_size, row_repeat, words);
-    return launch_status(cudaGetLastError());
+    return launch_status(launch_pdl(candidate_mask_kernel, grid, dim3(256), smem,
+                                    (cudaStream_t)stream, logits, ld, rows, width, row_ks, row_ke,
+                                    candidate_blocks, cand_stride, num_cand, block_size,
+                                    row_repeat, words));
 }
+
+namespace idx {
+namespace {
+
+// The one-launch slot map, when its cluster holds the call: at most 4 (row,
+// 1024-entry step) pairs and 32768 staged block-table words per CTA, in
+// clusters of 16 CTAs where the device can hold them (else 8).  Past that
+// the count and write kernels, which spread the rows over the GPU, measured
+// faster (64 rows of 2048 entries: 7.6 us a step for the cluster at 8 pairs
+// a CTA against 6.0 us; 32 rows: 4.0 us against 6.2 us).
+// IDX_ERR_UNSUPPORTED otherwise.
+idx_status slots_launch_cluster(const int32_t *topk, int64_t ld, int rows, int k,
+                                const int32_t *row_to_seq, int next_n, const SlotGeom &g,
+                                int32_t *slots, int32_t *indptr, int32_t *lens,
+                                unsigned int *status, cudaStream_t s)
+{
+    static int cmax[64] = {};  // largest cluster the device holds: 16 or 8; -1 none
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return IDX_ERR_CUDA;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    const size_t smem_max = sizeof(ScShared) + (size_t)kScMaxBt * 4;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kScThreads);
+    cfg.dynamicSmemBytes = smem_max;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (!cmax[dev]) {
+        if (cudaFuncSetAttribute(slot_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem_max) != cudaSuccess)
+            return IDX_ERR_CUDA;
+        if (cudaFuncSetAttribute(slot_cluster_kernel,
+                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+            (void)cudaGetLastError();
+        cmax[dev] = -1;
+        for (int C : {16, 8}) {
+            attr[0].val.clusterDim.x = (unsigned)C;
+            cfg.gridDim = dim3((unsigned)C);
+            int n = 0;
+            const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, slot_cluster_kernel, &cfg);
+            if (e != cudaSuccess)
+                (void)cudaGetLastError();
+            if (e == cudaSuccess && n > 0) {
+                cmax[dev] = C;
+                break;
+            }
+        }
+    }
+    if (cmax[dev] < 0)
+        return IDX_ERR_UNSUPPORTED;
+    const int E = (k + kScThreads - 1) / kScThreads;
+    const int R = (rows + cmax[dev] - 1) / cmax[dev];
+    if (k < 1 || R * E > kScPairs || (long long)R * g.max_blocks > kScMaxBt)
+        return IDX_ERR_UNSUPPORTED;
+    const int C = (rows + R - 1) / R;
+    attr[0].val.clusterDim.x = (unsigned)C;
+    cfg.gridDim = dim3((unsigned)C);
+    cfg.dynamicSmemBytes = sizeof(ScShared) + (size_t)R * g.max_blocks * 4;
+    cfg.numAttrs = 2;  // launched programmatically after the kernel before it
+    return launch_status(cudaLaunchKernelEx(&cfg, slot_cluster_kernel, topk, ld, rows, k,
+                                            row_to_seq, next_n, g, R, slots, indptr, lens,
+                                            status));
+}
+
+} // namespace
+} // namespace idx
 
 extern "C" idx_status idx_topk_to_ragged_slots(const int32_t *topk, int64_t ld, int rows, int k,
                                                const int32_t *row_to_seq, int next_n,
@@ -638,6 +857,12 @@ extern "C" idx_status idx_topk_to_ragged_slots(const int32_t *topk, int64_t ld, 
         if ((1 << i) == page_size)
             g.shift = i;
     g.num_pages = num_pages;
+    {
+        const idx_status st = slots_launch_cluster(topk, ld, rows, k, row_to_seq, next_n, g,
+                                                   slots, indptr, lens, status, s);
+        if (st != IDX_ERR_UNSUPPORTED)
+            return st;
+    }
     cudaError_t e = launch_pdl(slot_count_kernel, dim3(rows), dim3(kSlotThreads), 0, s, topk, ld,
                                rows, k, row_to_seq, next_n, g, lens, status);
     const int scanned = rows > kSlotDirectRows;
@@ -683,6 +908,8 @@ __global__ void __launch_bounds__(256) fill_tail_kernel(float *__restrict__ logi
                                                         const int32_t *__restrict__ row_ends,
                                                         int width, int vec)
 {
+    pdl_wait();  // the logits and row ends may come from the kernel before this one
+    pdl_launch_dependents();
     for (int r = blockIdx.y; r < rows; r += gridDim.y) {
         const int e = min(max(row_ends[r], 0), width);
         float *row = logits + (size_t)r * ld;
@@ -736,9 +963,8 @@ extern "C" idx_status idx_fill_logits_tail(float *logits, int64_t ld, int rows,
     const int vec = (ld % 4 == 0) && aligned16(logits);
     const dim3 grid((unsigned)std::min(64, (width + 4 * 256 - 1) / (4 * 256)),
                     (unsigned)std::min(rows, 65535));
-    fill_tail_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>(logits, ld, rows, row_ends, width,
-                                                              vec);
-    return launch_status(cudaGetLastError());
+    return launch_status(launch_pdl(fill_tail_kernel, grid, dim3(256), 0, (cudaStream_t)stream,
+                                    logits, ld, rows, row_ends, width, vec));
 }
 
 // ---------------------------------------------------- bounded-wait expiry

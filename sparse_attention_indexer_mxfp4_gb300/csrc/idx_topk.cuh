@@ -177,8 +177,16 @@ __global__ void __launch_bounds__(kThreads, 2)
     extern __shared__ __align__(16) uint8_t dsm[];
     Shared &sh = *reinterpret_cast<Shared *>(dsm);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (row >= rows)
+    if (row >= rows) {
+        pdl_launch_dependents();
         return;
+    }
+    for (int i = tid; i < 2 * 2048; i += kThreads)
+        (&sh.hist[0][0])[i] = 0u;
+    if (tid == 0)
+        sh.ncand = 0;
+    pdl_wait();  // the logits and lengths may come from the kernel before this one
+    pdl_launch_dependents();
     const int len = max(0, min(lengths[row], (int)ld));
     // warp sub-slices, starts aligned to 4 elements
     const int wper = ((len + kWarps - 1) / kWarps + 3) & ~3;
@@ -186,11 +194,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int we = min(len, ws + wper);
     const float *rowp = logits + (size_t)row * ld;
     const bool vec = vec_ok != 0;
-
-    for (int i = tid; i < 2 * 2048; i += kThreads)
-        (&sh.hist[0][0])[i] = 0u;
-    if (tid == 0)
-        sh.ncand = 0;
     __syncthreads();
 
     // ---- pass 1: histogram of digit 1, count of valid keys

@@ -101,6 +101,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = blockIdx.x / C;  // the grid holds whole clusters: uniform per cluster
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const bool live = row < rows;
+    for (int i = tid; i < 2048 + 2048 + 1024; i += kThreads)
+        (i < 2048 ? sh.h1[i] : i < 4096 ? sh.h2[i - 2048] : sh.h3[i - 4096]) = 0u;
+    pdl_wait();  // the logits and lengths may come from the kernel before this one
+    pdl_launch_dependents();
     const int len = live ? max(0, min(lengths[row], (int)ld)) : 0;
     // the row's keys spread evenly over the cluster, whole quads per CTA (the
     // chunk starts stay 16-byte aligned for vector loads)
@@ -111,9 +115,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float *rowp = logits + (size_t)(live ? row : 0) * ld + base;
 
     // keys of this chunk into shared memory, the local digit-1 histogram
-    // from them as they are formed
-    for (int i = tid; i < 2048 + 2048 + 1024; i += kThreads)
-        (i < 2048 ? sh.h1[i] : i < 4096 ? sh.h2[i - 2048] : sh.h3[i - 4096]) = 0u;
+    // from them as they are formed (the histograms were cleared above)
     uint32_t nvalid = 0;
     {
         uint32_t key[kSteps][4];

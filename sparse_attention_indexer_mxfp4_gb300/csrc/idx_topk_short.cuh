@@ -282,6 +282,8 @@ __global__ void __launch_bounds__(kThreads, 3)
 {
     __shared__ __align__(16) regsel::Shared<kThreads, kSteps> sh;
     const int row = blockIdx.x, tid = threadIdx.x;
+    pdl_wait();  // the logits and lengths may come from the kernel before this one
+    pdl_launch_dependents();
     if (row >= rows)
         return;
     const int len = max(0, min(lengths[row], (int)ld));

@@ -157,15 +157,28 @@ def test_candidate_mask(width, blk, C, repeat):
 # ------------------------------------------------------------------ slot map
 
 
-# 4096 rows is the largest batch whose write kernel sums its own offsets;
-# 4097 and up run the scan kernel first
-@pytest.mark.parametrize("rows,k,P,next_n", [(1, 1, 64, 1), (6, 50, 16, 2), (256, 2048, 64, 2),
-                                             (1500, 300, 128, 1), (4096, 40, 16, 2),
-                                             (4097, 40, 16, 1), (9000, 17, 64, 3)])
-def test_slots(rows, k, P, next_n):
+# The one-launch cluster kernel takes calls with at most 4 (row, 1024-entry
+# step) pairs and 32768 block-table words per CTA of a 16-CTA cluster:
+# (1, 1), (6, 50), (12, 3000) with a partial third step, (16, 4096) with
+# four, (32, 2048) at two rows a CTA, (64, 1024) at four, (4, 100) with
+# 20000-entry block-table rows.  The count and write kernels take the rest:
+# (20, 3000) and (64, 2048) at six and eight pairs a CTA, (65, 1024),
+# (256, 2048), (64, 4096), (16, 4097), (40, 100) with 20000 entries (60000
+# words a CTA), (1500, 300); 4096 rows is the largest batch whose write
+# kernel sums its own offsets; 4097 and up run the scan kernel first.  (On a
+# device that holds no 16-CTA cluster the 8-CTA one takes the calls of up
+# to half the rows.)
+@pytest.mark.parametrize("rows,k,P,next_n,max_blocks", [
+    (1, 1, 64, 1, 40), (6, 50, 16, 2, 40), (12, 3000, 64, 2, 60), (16, 4096, 64, 1, 70),
+    (32, 2048, 64, 1, 40), (64, 1024, 16, 1, 70), (4, 100, 16, 2, 20000),
+    (20, 3000, 64, 2, 60), (64, 2048, 64, 1, 40), (65, 1024, 16, 1, 70),
+    (256, 2048, 64, 2, 40), (64, 4096, 64, 1, 70), (16, 4097, 64, 1, 70),
+    (40, 100, 16, 1, 20000), (1500, 300, 128, 1, 40),
+    (4096, 40, 16, 2, 40), (4097, 40, 16, 1, 40), (9000, 17, 64, 3, 40)])
+def test_slots(rows, k, P, next_n, max_blocks):
     rng = np.random.default_rng(rows + k)
     nseq = -(-rows // next_n)
-    num_pages, max_blocks = 5000, 40
+    num_pages = max(5000, max_blocks)
     bt = np.stack([rng.permutation(num_pages)[:max_blocks] for _ in range(nseq)]).astype(np.int32)
     topk = rng.integers(-1, max_blocks * P, size=(rows, k)).astype(np.int32)
     topk[rng.random((rows, k)) < 0.3] = -1
