@@ -51,7 +51,7 @@ struct Shared {
     uint32_t h3[1024];
     uint32_t mh[2048];  // the cluster's sum of the current digit's histograms
     uint32_t wbin[3][kWarps];
-    uint32_t sel[3][2];
+    uint32_t sel[3][3];
     uint32_t wred[kWarps];
     uint32_t cta[3];    // this CTA's finite keys, keys above T, keys equal to T
     uint32_t gt[kTab];  // keys above T (or taken) per (step, warp), then offsets
@@ -146,11 +146,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         total += cl.map_shared_rank(sh.cta, r)[0];
     merge_hist(cl, sh, sh.h1, 2048, C);
 
+    // T: the k-th largest key; every key at or above it is taken unless
+    // some_ties (then keys equal to T are taken lowest index first, ties of
+    // eq_total of them).  A digit's threshold bin whose keys are all taken
+    // ends the search with T its lowest key (the usual case after digit 2
+    // for rows of distinct values).  Every branch is cluster-uniform.
     uint32_t T = 0u, ties = 0u, eq_total = 0u;
-    if (total > (uint32_t)k) {  // cluster-uniform
+    bool some_ties = false;
+    if (total > (uint32_t)k) {
         regsel::find_bin<kThreads>(sh.mh, 2048, (uint32_t)k, sh.wbin[0], sh.sel[0]);
         const uint32_t b1 = sh.sel[0][0];
         uint32_t krem = sh.sel[0][1];
+        if (krem == sh.sel[0][2]) {
+            T = b1 << 21;
+            goto found;
+        }
         #pragma unroll
         for (int s = 0; s < kSteps; ++s) {
             if (s >= nrun)
@@ -167,6 +177,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         regsel::find_bin<kThreads>(sh.mh, 2048, krem, sh.wbin[1], sh.sel[1]);
         const uint32_t p2 = (b1 << 11) | sh.sel[1][0];
         krem = sh.sel[1][1];
+        if (krem == sh.sel[1][2]) {
+            T = p2 << 10;
+            goto found;
+        }
         #pragma unroll
         for (int s = 0; s < kSteps; ++s) {
             if (s >= nrun)
@@ -183,9 +197,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         regsel::find_bin<kThreads>(sh.mh, 1024, krem, sh.wbin[2], sh.sel[2]);
         T = (p2 << 10) | sh.sel[2][0];
         ties = sh.sel[2][1];
-        eq_total = sh.mh[T & 1023u];
+        eq_total = sh.sel[2][2];
+        some_ties = ties != eq_total;
     }
-    const bool all_ties = ties == eq_total;  // every key equal to T is taken (T = 0: none exist)
+found:
+    const bool all_ties = !some_ties;  // every key at or above tmin is taken
     const uint32_t tmin = T == 0u ? 1u : T;
 
     // per (step, warp): keys taken outright (above T, or at or above tmin
@@ -234,6 +250,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         gt_before += c[1];
         eq_before += c[2];
     }
+    // the last reads of other CTAs' shared memory are done: arrive at the
+    // barrier that keeps each CTA's shared memory alive until then (waited
+    // on at the end, so the writes below overlap it)
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
     const uint32_t lt = (1u << lane) - 1u;
     int32_t *orow = out + (size_t)(live ? row : 0) * ld_out;
     if (live) {
@@ -273,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 orow[j] = -1;
         }
     }
-    cl.sync();  // no CTA leaves while another may still read its shared memory
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 } // namespace topk_cluster

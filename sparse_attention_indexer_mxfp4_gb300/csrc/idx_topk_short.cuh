@@ -33,14 +33,14 @@ struct Shared {
     uint32_t hist[2][2048];
     uint32_t wvalid[kWarps];
     uint32_t wbin[3][kWarps];
-    uint32_t sel[3][2];
+    uint32_t sel[3][3];
     uint32_t gt[kTab];  // keys above T per (step, warp), then exclusive offsets
     uint32_t eq[kTab];  // keys equal to T per (step, warp), then exclusive offsets
 };
 
 // Descending-bin search over h[nb] (nb = 2048 or 1024): the bin where the
-// count from the top reaches krem, and the rank left inside it, go to
-// sel[0..1].  Reads h, writes wbin and sel only; two barriers.
+// count from the top reaches krem, the rank left inside it and the bin's
+// count go to sel[0..2].  Reads h, writes wbin and sel only; two barriers.
 template <int NT>
 __device__ __forceinline__ void find_bin(const uint32_t *h, int nb, uint32_t krem,
                                          uint32_t *wbin, uint32_t *sel)
@@ -72,6 +72,7 @@ __device__ __forceinline__ void find_bin(const uint32_t *h, int nb, uint32_t kre
         if (j < per && before < krem && before + loc[j] >= krem) {
             sel[0] = (uint32_t)(nb - 1 - (tid * per + j));
             sel[1] = krem - before;
+            sel[2] = loc[j];  // the bin's count
         }
         before += loc[j];
     }
@@ -143,6 +144,14 @@ __device__ __forceinline__ void select_write(Shared<NT, KS> &sh, const uint32_t 
         find_bin<NT>(sh.hist[0], 2048, (uint32_t)k, sh.wbin[0], sh.sel[0]);
         const uint32_t b1 = sh.sel[0][0];
         uint32_t krem = sh.sel[0][1];
+        // A digit's threshold bin whose keys are all taken ends the search:
+        // T is then the bin's lowest key and every key at or above it is
+        // taken (the k-th largest key is alone in its 22-bit bin for most
+        // rows of distinct values, so digit 3 is usually skipped).
+        if (krem == sh.sel[0][2]) {
+            T = b1 << 21;
+            goto found;
+        }
         // digit 2 (next 11 bits) of the keys in bin b1; digit 1's histogram
         // is cleared meanwhile for digit 3
         for (int i = tid; i < 1024 / 4; i += NT)
@@ -157,6 +166,10 @@ __device__ __forceinline__ void select_write(Shared<NT, KS> &sh, const uint32_t 
         find_bin<NT>(sh.hist[1], 2048, krem, sh.wbin[1], sh.sel[1]);
         const uint32_t p2 = (b1 << 11) | sh.sel[1][0];  // the top 22 bits of T
         krem = sh.sel[1][1];
+        if (krem == sh.sel[1][2]) {
+            T = p2 << 10;
+            goto found;
+        }
         // digit 3 (low 10 bits) of the keys matching the top 22 bits
         #pragma unroll
         for (int s = 0; s < KS; ++s)
@@ -170,6 +183,7 @@ __device__ __forceinline__ void select_write(Shared<NT, KS> &sh, const uint32_t 
         ties = sh.sel[2][1];
         all_ties = ties == sh.hist[0][T & 1023u];  // the keys equal to T
     }
+found:
     const uint32_t lt = (1u << lane) - 1u;
 
     if (all_ties) {

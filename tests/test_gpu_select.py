@@ -70,6 +70,38 @@ def test_topk_candidate_overflow(workspace):
     assert_topk_exact(got, oracle.topk(x, lengths, k))
 
 
+@pytest.mark.parametrize("width", [5000, 40000, 150000])
+@pytest.mark.parametrize("case", ["digit1_bin_taken", "digit2_bin_taken", "digit3_splits_bin"])
+def test_topk_threshold_bin(width, case):
+    """Where the radix select stops: the threshold bin of digit 1 wholly
+    taken (k equals the keys of the top bin), of digit 2 (distinct random
+    values), or split by digit 3 (consecutive floats fill whole 22-bit bins,
+    k ends inside one).  Register (5000) and cluster (40000, 150000) forms."""
+    rng = np.random.default_rng(width + len(case))
+    rows, k = 4, 2048
+    if case == "digit1_bin_taken":
+        # k keys in [64, 80) -- one digit-1 bin (sign, exponent, two mantissa
+        # bits) -- and the rest in [1, 2)
+        x = (1.0 + rng.random((rows, width))).astype(np.float32)
+        for r in range(rows):
+            top = rng.choice(width, size=k, replace=False)
+            x[r, top] = (64.0 + 16.0 * rng.random(k) * 0.999).astype(np.float32)
+    elif case == "digit2_bin_taken":
+        x = rng.standard_normal((rows, width)).astype(np.float32)
+    else:
+        base = np.float32(1.0).view(np.int32)
+        x = np.empty((rows, width), np.float32)
+        for r in range(rows):
+            # 4096 consecutive floats from 1.0, shuffled, the rest below 0.5;
+            # the 2048th largest falls inside the second 1024-key bin
+            v = (base + 700 + np.arange(4096, dtype=np.int32)).view(np.float32)
+            x[r] = (0.25 * rng.random(width)).astype(np.float32)
+            x[r, rng.choice(width, size=4096, replace=False)] = v
+    lengths = np.full(rows, width)
+    got = gpu_topk(x, lengths, k)
+    assert_topk_exact(got, oracle.topk(x, lengths, k))
+
+
 @pytest.mark.parametrize("width", [8192, 8191, 4099, 130])
 @pytest.mark.parametrize("kind", ["ties1", "ties3", "narrow", "normal"])
 def test_topk_short_rows(width, kind):
