@@ -89,10 +89,16 @@ def producer_bytes(case) -> float:
 # since and the traffic is reported as null.
 LOGITS_SOURCES = ["idx_logits_kernel.cuh", "idx_logits.cuh", "idx_common.cuh", "idx_api.cu"]
 NCU_TRAFFIC = {
-    3: {"bytes": 157692928 + 5200896, "digest": "e66ed00d05df2299",
-        "profile": "profiles/logits_kernel_paged_fp8_decode_b64.md"},
-    5: {"bytes": 285843712 + 14587392, "digest": "e66ed00d05df2299",
-        "profile": "profiles/logits_kernel_paged_mxfp4_decode_b32.md"},
+    2: {"bytes": 18604032 + 7564800, "digest": "43f3b2c3cb3a2f6b",
+        "profile": "profiles/logits_traffic_all_configs.md"},
+    3: {"bytes": 157701376 + 4563712, "digest": "43f3b2c3cb3a2f6b",
+        "profile": "profiles/logits_traffic_all_configs.md"},
+    4: {"bytes": 91392 + 189570304 + 5421824, "digest": "43f3b2c3cb3a2f6b",
+        "profile": "profiles/logits_traffic_all_configs.md"},
+    5: {"bytes": 285837568 + 14354432, "digest": "43f3b2c3cb3a2f6b",
+        "profile": "profiles/logits_traffic_all_configs.md"},
+    6: {"bytes": 3840 + 413286144 + 18357248, "digest": "43f3b2c3cb3a2f6b",
+        "profile": "profiles/logits_traffic_all_configs.md"},
 }
 
 
@@ -398,7 +404,8 @@ def measure(cfg: int, args, dev, world: int, rank: int, headline: bool) -> dict:
         fp8_peak = 2.0 * bf16  # dense fp8 rate = 2x bf16 on this part
         ach = logits_flops(case) / (logit_avg * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": fp8_peak,
-                "unit": "TFLOP/s", "frac": round(ach / fp8_peak, 4), "traffic": None,
+                "unit": "TFLOP/s", "frac": round(ach / fp8_peak, 4),
+                "traffic": logits_traffic(cfg),
                 "peak_source": f"{src} bf16_tflops x 2 (fp8 dense)", "kernel": "logits_kernel",
                 "algorithmic_flops_per_launch": logits_flops(case),
                 "avg_launch_ms": round(logit_avg, 5), "stage_ms_in_step": round(logit_step, 5)}
