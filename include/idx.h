@@ -28,6 +28,11 @@
  *     and cleared by idx_get_device_status().
  *   - Integers are int32 unless stated; row-major layouts; strides in elements
  *     unless the name ends in _bytes.
+ *   - Kernels are launched with programmatic stream serialisation: one may
+ *     start its set-up (barriers, tensor memory, shared-memory clears) while
+ *     the kernel ahead of it on the stream finishes, and waits for that
+ *     kernel to complete before it reads any argument array, so inputs that
+ *     the previous kernel writes are safe.
  */
 #ifndef IDX_H_
 #define IDX_H_
