@@ -70,19 +70,23 @@ __device__ __forceinline__ void load4(const float *row, int i0, int end, bool ve
 // and the row allows them, scalar loads for the rest.
 template <int U>
 __device__ __forceinline__ void load_keys(const float *row, int base, int stride, int end, bool vec,
-                                          uint32_t (&k)[U][4])
+                                          uint32_t (&k)[U][4], int nrun = U)
 {
+    // runs u >= nrun (the same in every thread of the caller) hold no key and
+    // issue no load
     float4 v[U];
     #pragma unroll
     for (int u = 0; u < U; ++u) {
         const int i0 = base + u * stride;
         v[u] = make_float4(NAN, NAN, NAN, NAN);
-        if (vec && i0 + 3 < end)
+        if (u < nrun && vec && i0 + 3 < end)
             v[u] = __ldg(reinterpret_cast<const float4 *>(row + i0));
     }
     #pragma unroll
     for (int u = 0; u < U; ++u) {
         const int i0 = base + u * stride;
+        if (u >= nrun)
+            break;
         if (!(vec && i0 + 3 < end)) {
             if (i0 < end)
                 v[u].x = __ldg(row + i0);

@@ -14,9 +14,10 @@
 // chunk (s < 8, e < 4), so (rank, s, warp, lane, e) is index order; every
 // pass visits only the runs s that hold keys of the CTA's chunk.  The
 // 11/11/10-bit radix select runs on histograms each CTA builds over its own
-// keys; after a cluster barrier every CTA adds up the C histograms of the
-// digit through distributed shared memory and finds the same bin itself, so
-// no reduction step or second barrier is needed per digit.  The write ranks
+// keys; after a cluster barrier every CTA's bin search adds up the C
+// histograms of the digit through distributed shared memory, bin by bin as
+// it scans, and finds the same bin itself, so no reduction step or second
+// barrier is needed per digit.  The write ranks
 // keys by (step, warp) tables inside the CTA, offset by the counts of the
 // lower-ranked CTAs (read remotely after one more barrier); keys equal to
 // the k-th largest are taken lowest index first across the whole row.
@@ -49,7 +50,6 @@ struct Shared {
     uint32_t h1[2048];  // this CTA's digit histograms, read by the cluster
     uint32_t h2[2048];
     uint32_t h3[1024];
-    uint32_t mh[2048];  // the cluster's sum of the current digit's histograms
     uint32_t wbin[3][kWarps];
     uint32_t sel[3][3];
     uint32_t wred[kWarps];
@@ -67,25 +67,24 @@ __device__ __forceinline__ uint32_t cta_sum(Shared &sh, uint32_t v)
     if (lane == 0)
         sh.wred[w] = v;
     __syncthreads();
-    uint32_t t = 0;
-    #pragma unroll 8
-    for (int i = 0; i < kWarps; ++i)
-        t += sh.wred[i];
-    return t;
+    static_assert(kWarps == 32, "one warp total per lane");
+    return __reduce_add_sync(0xffffffffu, sh.wred[lane]);
 }
 
-// mh[0, nb) = the sum of every cluster CTA's histogram h (nb <= 2048), then
-// a barrier.
-__device__ __forceinline__ void merge_hist(cg::cluster_group &cl, Shared &sh, uint32_t *h, int nb,
-                                           int C)
+// The bin search over the sum of every cluster CTA's histogram h (read
+// through distributed shared memory; each thread sums only the bins it
+// scans, so no merged copy and no barrier before the search).
+__device__ __forceinline__ void find_bin_cluster(cg::cluster_group &cl, Shared &sh, uint32_t *h,
+                                                 int nb, uint32_t krem, int C, int digit)
 {
-    for (int b = threadIdx.x; b < nb; b += kThreads) {
-        uint32_t v = 0;
-        for (int r = 0; r < C; ++r)
-            v += cl.map_shared_rank(h, r)[b];
-        sh.mh[b] = v;
-    }
-    __syncthreads();
+    regsel::find_bin_of<kThreads>(
+        [&](int b) -> uint32_t {
+            uint32_t v = 0;
+            for (int r = 0; r < C; ++r)
+                v += cl.map_shared_rank(h, r)[b];
+            return v;
+        },
+        nb, krem, sh.wbin[digit], sh.sel[digit]);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -119,7 +118,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t nvalid = 0;
     {
         uint32_t key[kSteps][4];
-        topk_detail::load_keys<kSteps>(rowp, 4 * tid, 4 * kThreads, end, vec_ok != 0, key);
+        topk_detail::load_keys<kSteps>(rowp, 4 * tid, 4 * kThreads, end, vec_ok != 0, key, nrun);
         __syncthreads();
         #pragma unroll
         for (int s = 0; s < kSteps; ++s) {
@@ -144,7 +143,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t total = 0;
     for (int r = 0; r < C; ++r)
         total += cl.map_shared_rank(sh.cta, r)[0];
-    merge_hist(cl, sh, sh.h1, 2048, C);
 
     // T: the k-th largest key; every key at or above it is taken unless
     // some_ties (then keys equal to T are taken lowest index first, ties of
@@ -154,7 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t T = 0u, ties = 0u, eq_total = 0u;
     bool some_ties = false;
     if (total > (uint32_t)k) {
-        regsel::find_bin<kThreads>(sh.mh, 2048, (uint32_t)k, sh.wbin[0], sh.sel[0]);
+        find_bin_cluster(cl, sh, sh.h1, 2048, (uint32_t)k, C, 0);
         const uint32_t b1 = sh.sel[0][0];
         uint32_t krem = sh.sel[0][1];
         if (krem == sh.sel[0][2]) {
@@ -172,9 +170,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (kk[e] >> 21 == b1)
                     atomicAdd(&sh.h2[(kk[e] >> 10) & 2047u], 1u);
         }
-        cl.sync();  // digit-2 histograms complete; every CTA is done with mh
-        merge_hist(cl, sh, sh.h2, 2048, C);
-        regsel::find_bin<kThreads>(sh.mh, 2048, krem, sh.wbin[1], sh.sel[1]);
+        cl.sync();  // digit-2 histograms complete
+        find_bin_cluster(cl, sh, sh.h2, 2048, krem, C, 1);
         const uint32_t p2 = (b1 << 11) | sh.sel[1][0];
         krem = sh.sel[1][1];
         if (krem == sh.sel[1][2]) {
@@ -193,8 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     atomicAdd(&sh.h3[kk[e] & 1023u], 1u);
         }
         cl.sync();  // digit-3 histograms complete
-        merge_hist(cl, sh, sh.h3, 1024, C);
-        regsel::find_bin<kThreads>(sh.mh, 1024, krem, sh.wbin[2], sh.sel[2]);
+        find_bin_cluster(cl, sh, sh.h3, 1024, krem, C, 2);
         T = (p2 << 10) | sh.sel[2][0];
         ties = sh.sel[2][1];
         eq_total = sh.sel[2][2];

@@ -38,12 +38,13 @@ struct Shared {
     uint32_t eq[kTab];  // keys equal to T per (step, warp), then exclusive offsets
 };
 
-// Descending-bin search over h[nb] (nb = 2048 or 1024): the bin where the
-// count from the top reaches krem, the rank left inside it and the bin's
-// count go to sel[0..2].  Reads h, writes wbin and sel only; two barriers.
-template <int NT>
-__device__ __forceinline__ void find_bin(const uint32_t *h, int nb, uint32_t krem,
-                                         uint32_t *wbin, uint32_t *sel)
+// Descending-bin search over nb bins (nb = 2048 or 1024) whose counts
+// count(b) returns: the bin where the count from the top reaches krem, the
+// rank left inside it and the bin's count go to sel[0..2].  Writes wbin and
+// sel only; two barriers.
+template <int NT, class Count>
+__device__ __forceinline__ void find_bin_of(Count count, int nb, uint32_t krem, uint32_t *wbin,
+                                            uint32_t *sel)
 {
     constexpr int MAXPER = 2048 / NT;
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -51,7 +52,7 @@ __device__ __forceinline__ void find_bin(const uint32_t *h, int nb, uint32_t kre
     uint32_t loc[MAXPER], lsum = 0;
     #pragma unroll
     for (int j = 0; j < MAXPER; ++j) {
-        loc[j] = j < per ? h[nb - 1 - (tid * per + j)] : 0u;
+        loc[j] = j < per ? count(nb - 1 - (tid * per + j)) : 0u;
         lsum += loc[j];
     }
     uint32_t wt;
@@ -77,6 +78,14 @@ __device__ __forceinline__ void find_bin(const uint32_t *h, int nb, uint32_t kre
         before += loc[j];
     }
     __syncthreads();
+}
+
+// find_bin_of over the histogram h[nb] in this CTA's shared memory.
+template <int NT>
+__device__ __forceinline__ void find_bin(const uint32_t *h, int nb, uint32_t krem,
+                                         uint32_t *wbin, uint32_t *sel)
+{
+    find_bin_of<NT>([h](int b) -> uint32_t { return h[b]; }, nb, krem, wbin, sel);
 }
 
 // In-place exclusive scan of an N-entry table (N a multiple of 32) by one
