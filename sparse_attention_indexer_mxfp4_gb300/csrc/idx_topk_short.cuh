@@ -113,11 +113,13 @@ __device__ __forceinline__ uint32_t scan_tab(uint32_t *tab, int lane)
 // Selects the k largest nonzero keys of the CTA (ties first in order) and
 // writes index_of(s, e) of each at its rank in order to orow[0, k), -1
 // after the last.  key[s][e] is the thread's key at order position
-// 4 NT s + 4 tid + e; 0 marks an empty or non-finite entry.  Uses every
-// thread of the CTA; begins by clearing the histograms.
+// 4 NT s + 4 tid + e; 0 marks an empty or non-finite entry, and every key of
+// the steps s >= ns (the same in every thread) is empty, so the passes stop
+// there.  Uses every thread of the CTA; begins by clearing the histograms.
 template <int NT, int KS, class IndexOf>
 __device__ __forceinline__ void select_write(Shared<NT, KS> &sh, const uint32_t (&key)[KS][4],
-                                             int k, int32_t *orow, IndexOf index_of)
+                                             int k, int32_t *orow, IndexOf index_of,
+                                             int ns = KS)
 {
     using S = Shared<NT, KS>;
     static_assert(S::kTab % 32 == 0, "tables are scanned 32 lanes wide");
@@ -129,13 +131,16 @@ __device__ __forceinline__ void select_write(Shared<NT, KS> &sh, const uint32_t 
     // digit 1 (top 11 bits) and the number of finite keys
     uint32_t nvalid = 0;
     #pragma unroll
-    for (int s = 0; s < KS; ++s)
+    for (int s = 0; s < KS; ++s) {
+        if (s >= ns)
+            break;
         #pragma unroll
         for (int e = 0; e < 4; ++e)
             if (key[s][e]) {
                 ++nvalid;
                 atomicAdd(&sh.hist[0][key[s][e] >> 21], 1u);
             }
+    }
     nvalid = __reduce_add_sync(0xffffffffu, nvalid);
     if (lane == 0)
         sh.wvalid[w] = nvalid;
@@ -166,11 +171,14 @@ __device__ __forceinline__ void select_write(Shared<NT, KS> &sh, const uint32_t 
         for (int i = tid; i < 1024 / 4; i += NT)
             reinterpret_cast<uint4 *>(sh.hist[0])[i] = make_uint4(0u, 0u, 0u, 0u);
         #pragma unroll
-        for (int s = 0; s < KS; ++s)
+        for (int s = 0; s < KS; ++s) {
+            if (s >= ns)
+                break;
             #pragma unroll
             for (int e = 0; e < 4; ++e)
                 if (key[s][e] >> 21 == b1)
                     atomicAdd(&sh.hist[1][(key[s][e] >> 10) & 2047u], 1u);
+        }
         __syncthreads();
         find_bin<NT>(sh.hist[1], 2048, krem, sh.wbin[1], sh.sel[1]);
         const uint32_t p2 = (b1 << 11) | sh.sel[1][0];  // the top 22 bits of T
@@ -181,11 +189,14 @@ __device__ __forceinline__ void select_write(Shared<NT, KS> &sh, const uint32_t 
         }
         // digit 3 (low 10 bits) of the keys matching the top 22 bits
         #pragma unroll
-        for (int s = 0; s < KS; ++s)
+        for (int s = 0; s < KS; ++s) {
+            if (s >= ns)
+                break;
             #pragma unroll
             for (int e = 0; e < 4; ++e)
                 if (key[s][e] >> 10 == p2)
                     atomicAdd(&sh.hist[0][key[s][e] & 1023u], 1u);
+        }
         __syncthreads();
         find_bin<NT>(sh.hist[0], 1024, krem, sh.wbin[2], sh.sel[2]);
         T = (p2 << 10) | sh.sel[2][0];
@@ -202,10 +213,12 @@ found:
         #pragma unroll
         for (int s = 0; s < KS; ++s) {
             uint32_t n = 0;
-            #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                n += key[s][e] >= tmin;
-            n = __reduce_add_sync(0xffffffffu, n);
+            if (s < ns) {
+                #pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    n += key[s][e] >= tmin;
+                n = __reduce_add_sync(0xffffffffu, n);
+            }
             if (lane == 0)
                 sh.gt[s * S::kWarps + w] = n;
         }
@@ -215,6 +228,8 @@ found:
         __syncthreads();
         #pragma unroll
         for (int s = 0; s < KS; ++s) {
+            if (s >= ns)
+                break;
             bool tk[4];
             uint32_t tk_below = 0;
             #pragma unroll
@@ -238,13 +253,15 @@ found:
     #pragma unroll
     for (int s = 0; s < KS; ++s) {
         uint32_t ngt = 0, neq = 0;
-        #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            ngt += key[s][e] > T;
-            neq += key[s][e] == T;
+        if (s < ns) {
+            #pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                ngt += key[s][e] > T;
+                neq += key[s][e] == T;
+            }
+            ngt = __reduce_add_sync(0xffffffffu, ngt);
+            neq = __reduce_add_sync(0xffffffffu, neq);
         }
-        ngt = __reduce_add_sync(0xffffffffu, ngt);
-        neq = __reduce_add_sync(0xffffffffu, neq);
         if (lane == 0) {
             sh.gt[s * S::kWarps + w] = ngt;
             sh.eq[s * S::kWarps + w] = neq;
@@ -261,6 +278,8 @@ found:
     // before it and the keys equal to T taken before it
     #pragma unroll
     for (int s = 0; s < KS; ++s) {
+        if (s >= ns)
+            break;
         const uint32_t eq0 = sh.eq[s * S::kWarps + w];
         uint32_t eq_below = 0;
         #pragma unroll
@@ -310,12 +329,13 @@ __global__ void __launch_bounds__(kThreads, 3)
     if (row >= rows)
         return;
     const int len = max(0, min(lengths[row], (int)ld));
+    const int nrun = (len + 4 * kThreads - 1) / (4 * kThreads);  // runs holding keys
     uint32_t key[kSteps][4];
     topk_detail::load_keys<kSteps>(logits + (size_t)row * ld, 4 * tid, 4 * kThreads, len,
-                                   vec_ok != 0, key);
+                                   vec_ok != 0, key, nrun);
     regsel::select_write<kThreads, kSteps>(
         sh, key, k, out + (size_t)row * ld_out,
-        [&](int s, int e) -> int32_t { return s * 4 * kThreads + 4 * tid + e; });
+        [&](int s, int e) -> int32_t { return s * 4 * kThreads + 4 * tid + e; }, nrun);
 }
 
 } // namespace topk_short
