@@ -246,6 +246,34 @@ def test_slots_row_to_seq_and_invalid_pages():
     np.testing.assert_array_equal(slots.cpu().numpy()[:ip[-1]], s)
 
 
+@pytest.mark.parametrize("rows,k", [(40, 1024), (48, 1000), (700, 300)])
+def test_slots_row_to_seq_invalid_pages_many_rows(rows, k):
+    """Invalid block-table entries and an explicit row-to-sequence map with
+    several rows per CTA: (40, 1024) and (48, 1000) take the one-launch
+    cluster kernel (three rows a CTA), (700, 300) the count and write
+    kernels."""
+    rng = np.random.default_rng(rows * 3 + k)
+    P, num_pages, max_blocks, nseq = 16, 3000, 64, 29
+    bt = np.stack([rng.permutation(num_pages)[:max_blocks] for _ in range(nseq)]).astype(np.int32)
+    bad = rng.random(bt.shape) < 0.02
+    bt[bad] = rng.choice([-1, num_pages, num_pages + 7], size=int(bad.sum()))
+    r2s = rng.integers(0, nseq, size=rows).astype(np.int32)
+    topk = rng.integers(-1, max_blocks * P + 40, size=(rows, k)).astype(np.int32)
+    topk[rng.random((rows, k)) < 0.2] = -1
+    slots = torch.empty(rows * k, dtype=torch.int32, device="cuda")
+    indptr = torch.empty(rows + 1, dtype=torch.int32, device="cuda")
+    lens = torch.empty(rows, dtype=torch.int32, device="cuda")
+    B.idx_get_device_status()
+    B.idx_topk_to_ragged_slots(_t(topk), _t(bt), P, num_pages, slots, indptr, lens,
+                               row_to_seq=_t(r2s))
+    torch.cuda.synchronize()
+    s_, ip, ln, nbad = oracle.topk_to_ragged_slots(topk, bt, P, num_pages, row_to_seq=r2s)
+    assert nbad > 0 and B.idx_get_device_status() & B.DEV_BAD_PAGE
+    np.testing.assert_array_equal(indptr.cpu().numpy(), ip)
+    np.testing.assert_array_equal(lens.cpu().numpy(), ln)
+    np.testing.assert_array_equal(slots.cpu().numpy()[:ip[-1]], s_)
+
+
 def _cand_case(rng, rows, width, num_cand, blk, row_repeat=1, ties=None):
     if ties == "narrow":
         # distinct values inside one bin of the first radix digit
