@@ -553,6 +553,7 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
         long long u = 0;    // units seen
         int slot = 0;
         int rks[G], rke[G];
+        int in_lo = 0, in_hi = 0;  // keys live in every row of the group: [in_lo, in_hi)
         constexpr int NSUB = C::NSUB;
         // histogram variant: this warpgroup's G x 2048 bins; the warp's
         // valid keys of each row in the 8192-key chunk it is in (flushed
@@ -567,11 +568,16 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
         for (; w.left > 0; walk_next<PLAN>(a, w), ++u) {
             if (w.first_in_group) {
                 slot = gq & 1;
+                in_lo = 0;
+                in_hi = 0x7fffffff;
                 for (int i = 0; i < G; ++i) {
                     rks[i] = 0;
                     rke[i] = 0;
-                    if (i < w.gi.nrows)
+                    if (i < w.gi.nrows) {
                         row_range(a, w.gi.row0 + i, rks[i], rke[i]);
+                        in_lo = max(in_lo, rks[i]);
+                        in_hi = min(in_hi, rke[i]);
+                    }
                 }
                 if (!mbar_wait(&q_full[slot], (gq >> 1) & 1, abort_flag, a.status))
                     break;
@@ -579,6 +585,9 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
             }
             const int t0 = (w.j << TSH) + kq;  // this thread's key in sub-tile 0
             const int wend = a.paged ? w.gi.hi : a.N;  // columns this group writes
+            // a tile whose every key is live in every row of the group (and
+            // no candidate mask): no range tests, unconditional stores
+            const bool interior = !a.cand && (w.j << TSH) >= in_lo && (w.j << TSH) + TK <= in_hi;
             const bool compute = unit_compute<PLAN>(w, TSH);
             bool mine;
             float val[NSUB][G];
@@ -608,7 +617,8 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
                 #pragma unroll
                 for (int sub = 0; sub < NSUB; ++sub) {
                     const int key = sub * kMmaM + kq, t = t0 + sub * kMmaM;
-                    live[sub] = t < w.gi.hi && t >= w.gi.lo && ((halves >> (key >> 6)) & 1u);
+                    live[sub] = (interior || (t < w.gi.hi && t >= w.gi.lo)) &&
+                                ((halves >> (key >> 6)) & 1u);
                     ksc[sub] = 1.0f;
                     if (FMT == kFmtFp8)
                         ksc[sub] = reinterpret_cast<const float *>(sd)[key];
@@ -761,6 +771,13 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
                 #pragma unroll
                 for (int sub = 0; sub < NSUB; ++sub) {
                     const int t = t0 + sub * kMmaM;
+                    if (interior) {
+                        if (!live[sub])
+                            #pragma unroll
+                            for (int i = 0; i < G; ++i)
+                                val[sub][i] = -INFINITY;
+                        continue;
+                    }
                     #pragma unroll
                     for (int i = 0; i < G; ++i) {
                         bool keep = live[sub] && t >= rks[i] && t < rke[i];
@@ -785,7 +802,7 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
                     #pragma unroll
                     for (int sub = 0; sub < NSUB; ++sub) {
                         const int t = t0 + sub * kMmaM;
-                        if (t < end)
+                        if (interior || t < end)
                             orow[t] = val[sub][i];
                     }
                 }
