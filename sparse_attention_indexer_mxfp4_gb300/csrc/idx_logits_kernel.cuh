@@ -554,6 +554,10 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
         int slot = 0;
         int rks[G], rke[G];
         int in_lo = 0, in_hi = 0;  // keys live in every row of the group: [in_lo, in_hi)
+        // one-row groups on 256-key tiles: the row's 64 head weights held in
+        // registers for the whole group
+        constexpr bool kWregs = G == 1 && C::NSUB == 2;
+        float4 wreg[kWregs ? 16 : 1];
         constexpr int NSUB = C::NSUB;
         // histogram variant: this warpgroup's G x 2048 bins; the warp's
         // valid keys of each row in the 8192-key chunk it is in (flushed
@@ -581,6 +585,13 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
                 }
                 if (!mbar_wait(&q_full[slot], (gq >> 1) & 1, abort_flag, a.status))
                     break;
+                if constexpr (kWregs) {
+                    const float4 *w4 =
+                        reinterpret_cast<const float4 *>(smem + C::OFF_W + slot * C::W_BYTES);
+                    #pragma unroll
+                    for (int q = 0; q < 16; ++q)
+                        wreg[q] = w4[q];
+                }
                 ++gq;
             }
             const int t0 = (w.j << TSH) + kq;  // this thread's key in sub-tile 0
@@ -637,9 +648,9 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
                     if (!use_qs && all_pos) {
                     // Common path of one-row groups on 256-key tiles: both
                     // sub-tiles' blocks of a half of the heads are loaded
-                    // together and summed side by side, so each weight is
-                    // read from shared memory once per tile and the two
-                    // sub-tiles' packed-FMA chains interleave.
+                    // together and summed side by side (the weights from
+                    // registers), so the two sub-tiles' packed-FMA chains
+                    // interleave.
                     float2 cc[2][4];
                     #pragma unroll
                     for (int half = 0; half < 2; ++half) {
@@ -652,11 +663,10 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
                             for (int jj = 0; jj < 4; ++jj)
                                 cc[0][jj] = cc[1][jj] = make_float2(0.0f, 0.0f);
                         }
-                        const float4 *w4 = reinterpret_cast<const float4 *>(wsm + half * 32);
                         #pragma unroll
                         for (int q = 0; q < 8; ++q) {
                             const int h4 = half * 8 + q;
-                            const float4 wv = w4[q];
+                            const float4 wv = wreg[kWregs ? h4 : 0];
                             const int jj = (h4 & 1) * 2;
                             #pragma unroll
                             for (int sb = 0; sb < 2; ++sb) {
