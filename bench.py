@@ -89,15 +89,15 @@ def producer_bytes(case) -> float:
 # since and the traffic is reported as null.
 LOGITS_SOURCES = ["idx_logits_kernel.cuh", "idx_logits.cuh", "idx_common.cuh", "idx_api.cu"]
 NCU_TRAFFIC = {
-    2: {"bytes": 18604032 + 7564800, "digest": "43f3b2c3cb3a2f6b",
+    2: {"bytes": 18571776 + 7147008, "digest": "9492c1f9c36411c5",
         "profile": "profiles/logits_traffic_all_configs.md"},
-    3: {"bytes": 157701376 + 4563712, "digest": "43f3b2c3cb3a2f6b",
+    3: {"bytes": 157696768 + 4282624, "digest": "9492c1f9c36411c5",
         "profile": "profiles/logits_traffic_all_configs.md"},
-    4: {"bytes": 91392 + 189570304 + 5421824, "digest": "43f3b2c3cb3a2f6b",
+    4: {"bytes": 91392 + 189562624 + 5358080, "digest": "9492c1f9c36411c5",
         "profile": "profiles/logits_traffic_all_configs.md"},
-    5: {"bytes": 285837568 + 14354432, "digest": "43f3b2c3cb3a2f6b",
+    5: {"bytes": 285832192 + 14259712, "digest": "9492c1f9c36411c5",
         "profile": "profiles/logits_traffic_all_configs.md"},
-    6: {"bytes": 3840 + 413286144 + 18357248, "digest": "43f3b2c3cb3a2f6b",
+    6: {"bytes": 4096 + 413298176 + 18445312, "digest": "9492c1f9c36411c5",
         "profile": "profiles/logits_traffic_all_configs.md"},
 }
 
