@@ -957,7 +957,6 @@ __global__ void __launch_bounds__(kPlanThreads) cand_plan_kernel(const __grid_co
 {
     extern __shared__ uint32_t pbits[];
     uint32_t *box = pbits, *tb = pbits + a.box_words;
-    __shared__ uint32_t red[kPlanThreads / 32];
     __shared__ int rks[8], rke[8];
     pdl_wait();
     pdl_launch_dependents();
@@ -1003,52 +1002,44 @@ __global__ void __launch_bounds__(kPlanThreads) cand_plan_kernel(const __grid_co
             continue;
         const int t_lo = (int)lo;
         const int t_hi = (int)min((long long)ke, lo + a.cand_block);
-        for (int b = t_lo / kHalfKeys; b <= (t_hi - 1) / kHalfKeys; ++b)
+        // the box bits, and the bits of the tiles holding those boxes (every
+        // such tile overlaps the group's live keys: the box lies in a row's
+        // [ks, ke))
+        constexpr int BSH = TSH - 6;  // log2 of the 64-key boxes per tile
+        for (int b = t_lo / kHalfKeys; b <= (t_hi - 1) / kHalfKeys; ++b) {
             atomicOr(&box[b >> 5], 1u << (b & 31));
-    }
-    __syncthreads();
-    // tile bits; thread t owns the contiguous tiles [t * per, (t + 1) * per)
-    constexpr int BPT = (1 << TSH) / kHalfKeys;  // boxes per tile
-    const int per = (gi.tiles + kPlanThreads - 1) / kPlanThreads;
-    uint32_t mine = 0;
-    for (int j = tid * per; j < min(gi.tiles, (tid + 1) * per); ++j) {
-        bool any = false;
-        #pragma unroll
-        for (int q = 0; q < BPT; ++q) {
-            const int b = j * BPT + q;
-            any = any || ((box[b >> 5] >> (b & 31)) & 1u);
-        }
-        if (any && tile_is_compute(gi, j, TSH)) {
-            atomicOr(&tb[j >> 5], 1u << (j & 31));
-            ++mine;
+            atomicOr(&tb[(b >> BSH) >> 5], 1u << ((b >> BSH) & 31));
         }
     }
     __syncthreads();
     if (slice == 0) {
-        // the tile list: exclusive prefix of the per-thread counts
-        const int lane = tid & 31, wi = tid >> 5;
-        uint32_t x = mine;
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t n = __shfl_up_sync(0xffffffffu, x, o);
-            if (lane >= o)
-                x += n;
-        }
-        if (lane == 31)
-            red[wi] = x;
-        __syncthreads();
-        uint32_t before = x - mine, total = 0;
-        for (int i = 0; i < kPlanThreads / 32; ++i) {
-            if (i < wi)
-                before += red[i];
-            total += red[i];
-        }
+        // the tile list in ascending order, by warp 0: each lane takes one
+        // word of tile bits per round, and a shuffle scan of the words' bit
+        // counts places its tiles
         uint32_t *dst = a.plan + (size_t)g * a.plan_words;
         uint32_t *list = dst + 1 + a.box_words;
-        for (int j = tid * per; j < min(gi.tiles, (tid + 1) * per); ++j)
-            if ((tb[j >> 5] >> (j & 31)) & 1u)
-                list[before++] = (uint32_t)j;
-        if (tid == 0)
-            dst[0] = total;
+        if (tid < 32) {
+            uint32_t run = 0;
+            for (int base = 0; base < tw; base += 32) {
+                uint32_t bits = base + tid < tw ? tb[base + tid] : 0u;
+                const uint32_t n = __popc(bits);
+                uint32_t x = n;
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+                    if (tid >= o)
+                        x += y;
+                }
+                uint32_t pos = run + x - n;
+                while (bits) {
+                    const int bit = __ffs(bits) - 1;
+                    list[pos++] = (uint32_t)((base + tid) * 32 + bit);
+                    bits &= bits - 1u;
+                }
+                run += __shfl_sync(0xffffffffu, x, 31);
+            }
+            if (tid == 0)
+                dst[0] = run;
+        }
         for (int i = tid; i < a.box_words; i += kPlanThreads)
             dst[1 + i] = box[i];
     }
