@@ -644,49 +644,61 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
                 const bool all_pos = __all_sync(0xffffffffu, pos);
                 const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * C::ACC_COLS;
                 bool summed = false;
-                if constexpr (G == 1 && NSUB == 2) {
+                if constexpr (NSUB == 2) {
                     if (!use_qs && all_pos) {
-                    // Common path of one-row groups on 256-key tiles: both
-                    // sub-tiles' blocks of a half of the heads are loaded
-                    // together and summed side by side (the weights from
-                    // registers), so the two sub-tiles' packed-FMA chains
-                    // interleave.
-                    float2 cc[2][4];
-                    #pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        uint32_t rb[2][32];
-                        tmem_ld_32x32b_x32(tbase + half * 32, rb[0]);
-                        tmem_ld_32x32b_x32(tbase + C::NCOLS + half * 32, rb[1]);
-                        tmem_ld_wait();
-                        if (half == 0) {
-                            #pragma unroll
-                            for (int jj = 0; jj < 4; ++jj)
-                                cc[0][jj] = cc[1][jj] = make_float2(0.0f, 0.0f);
-                        }
+                        // Common path on 256-key tiles: for each row, both
+                        // sub-tiles' blocks of a half of the heads are loaded
+                        // together and summed side by side, so each weight is
+                        // read once per tile (one-row groups hold them in
+                        // registers) and the two sub-tiles' packed-FMA chains
+                        // interleave.  Rows past the group's last are computed
+                        // and discarded.
                         #pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            const int h4 = half * 8 + q;
-                            const float4 wv = wreg[kWregs ? h4 : 0];
-                            const int jj = (h4 & 1) * 2;
+                        for (int i = 0; i < G; ++i) {
+                            float2 cc[2][4];
+                            #pragma unroll
+                            for (int half = 0; half < 2; ++half) {
+                                uint32_t rb[2][32];
+                                const uint32_t tcol = tbase + i * H + half * 32;
+                                tmem_ld_32x32b_x32(tcol, rb[0]);
+                                tmem_ld_32x32b_x32(tcol + C::NCOLS, rb[1]);
+                                tmem_ld_wait();
+                                if (half == 0) {
+                                    #pragma unroll
+                                    for (int jj = 0; jj < 4; ++jj)
+                                        cc[0][jj] = cc[1][jj] = make_float2(0.0f, 0.0f);
+                                }
+                                const float4 *w4 =
+                                    reinterpret_cast<const float4 *>(wsm + i * H + half * 32);
+                                #pragma unroll
+                                for (int q = 0; q < 8; ++q) {
+                                    const int h4 = half * 8 + q;
+                                    const float4 wv = kWregs ? wreg[kWregs ? h4 : 0] : w4[q];
+                                    const int jj = (h4 & 1) * 2;
+                                    #pragma unroll
+                                    for (int sb = 0; sb < 2; ++sb) {
+                                        const float *x =
+                                            reinterpret_cast<const float *>(&rb[sb][4 * q]);
+                                        cc[sb][jj] = fma2(
+                                            make_float2(wv.x, wv.y),
+                                            make_float2(fmaxf(x[0], 0.0f), fmaxf(x[1], 0.0f)),
+                                            cc[sb][jj]);
+                                        cc[sb][jj + 1] = fma2(
+                                            make_float2(wv.z, wv.w),
+                                            make_float2(fmaxf(x[2], 0.0f), fmaxf(x[3], 0.0f)),
+                                            cc[sb][jj + 1]);
+                                    }
+                                }
+                            }
                             #pragma unroll
                             for (int sb = 0; sb < 2; ++sb) {
-                                const float *x = reinterpret_cast<const float *>(&rb[sb][4 * q]);
-                                cc[sb][jj] = fma2(make_float2(wv.x, wv.y),
-                                                  make_float2(fmaxf(x[0], 0.0f), fmaxf(x[1], 0.0f)),
-                                                  cc[sb][jj]);
-                                cc[sb][jj + 1] = fma2(make_float2(wv.z, wv.w),
-                                                      make_float2(fmaxf(x[2], 0.0f), fmaxf(x[3], 0.0f)),
-                                                      cc[sb][jj + 1]);
+                                const float sum =
+                                    ((cc[sb][0].x + cc[sb][2].x) + (cc[sb][0].y + cc[sb][2].y)) +
+                                    ((cc[sb][1].x + cc[sb][3].x) + (cc[sb][1].y + cc[sb][3].y));
+                                val[sb][i] = fabsf(ksc[sb]) * sum;
                             }
                         }
-                    }
-                    #pragma unroll
-                    for (int sb = 0; sb < 2; ++sb) {
-                        const float sum = ((cc[sb][0].x + cc[sb][2].x) + (cc[sb][0].y + cc[sb][2].y)) +
-                                          ((cc[sb][1].x + cc[sb][3].x) + (cc[sb][1].y + cc[sb][3].y));
-                        val[sb][0] = fabsf(ksc[sb]) * sum;
-                    }
-                    summed = true;
+                        summed = true;
                     }
                 }
                 if (summed) {
