@@ -89,15 +89,15 @@ def producer_bytes(case) -> float:
 # since and the traffic is reported as null.
 LOGITS_SOURCES = ["idx_logits_kernel.cuh", "idx_logits.cuh", "idx_common.cuh", "idx_api.cu"]
 NCU_TRAFFIC = {
-    2: {"bytes": 18571776 + 7147008, "digest": "9492c1f9c36411c5",
+    2: {"bytes": 18639104 + 7703040, "digest": "e4994ba7d68ef8cd",
         "profile": "profiles/logits_traffic_all_configs.md"},
-    3: {"bytes": 157696768 + 4282624, "digest": "9492c1f9c36411c5",
+    3: {"bytes": 157699328 + 4484096, "digest": "e4994ba7d68ef8cd",
         "profile": "profiles/logits_traffic_all_configs.md"},
-    4: {"bytes": 91392 + 189562624 + 5358080, "digest": "9492c1f9c36411c5",
+    4: {"bytes": 87552 + 189587968 + 5689344, "digest": "e4994ba7d68ef8cd",
         "profile": "profiles/logits_traffic_all_configs.md"},
-    5: {"bytes": 285832192 + 14259712, "digest": "9492c1f9c36411c5",
+    5: {"bytes": 285839360 + 14535680, "digest": "e4994ba7d68ef8cd",
         "profile": "profiles/logits_traffic_all_configs.md"},
-    6: {"bytes": 4096 + 413298176 + 18445312, "digest": "9492c1f9c36411c5",
+    6: {"bytes": 4096 + 413282816 + 18372608, "digest": "e4994ba7d68ef8cd",
         "profile": "profiles/logits_traffic_all_configs.md"},
 }
 
