@@ -353,7 +353,8 @@ def measure(cfg: int, args, dev, world: int, rank: int, headline: bool) -> dict:
     case = _case(cfg, shard=rank)
     prod = _is_producer(case)
     step = (ProducerStep(case, device=dev) if prod else
-            IndexerStep(case, device=dev, fused_topk=args.fused_topk))
+            IndexerStep(case, device=dev, fused_topk=args.fused_topk,
+                        fused_slots=not args.split_slots))
     fused = getattr(step, "fused_topk", False)
     paged = isinstance(case, PagedCase)
     steps = [step] + ([step.twin(kv_copy=True), step.twin(kv_copy=True)] if paged else [])
@@ -477,7 +478,8 @@ def run_ours(args):
                                                           idx_get_device_status)
         case = _case(args.config, shard=rank)
         step = (ProducerStep(case, device=dev) if _is_producer(case) else
-                IndexerStep(case, device=dev, fused_topk=args.fused_topk))
+                IndexerStep(case, device=dev, fused_topk=args.fused_topk,
+                        fused_slots=not args.split_slots))
         for _ in range(args.warmup):
             step.run()
         torch.cuda.synchronize()
@@ -879,6 +881,9 @@ def main():
     p.add_argument("--fused-topk", action="store_true",
                    help="paged workloads without a candidate list: one call for the logits and "
                         "the row top-k (idx_paged_mqa_logits_topk)")
+    p.add_argument("--split-slots", action="store_true",
+                   help="paged workloads: the row top-k and the slot map as two calls "
+                        "(idx_topk, idx_topk_to_ragged_slots) instead of idx_topk_ragged_slots")
     args = p.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -378,6 +378,30 @@ idx_status idx_topk_to_ragged_slots(const int32_t *topk, int64_t ld, int rows, i
                                     idx_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * idx_topk_ragged_slots -- idx_topk, then idx_topk_to_ragged_slots of its
+ * result, in one call.
+ * Passage: as those two calls (rocm_paged_mxfp4_indexer, _topk;
+ * rocm_aiter_mla_sparse, build_prefill_topk_ragged_indices).
+ *
+ *   Arguments as idx_topk (logits .. ws_bytes), then as
+ *   idx_topk_to_ragged_slots for its topk = out_idx, ld = ld_out (row_to_seq
+ *   .. lens).  Every output is exactly what the two calls write.  Where the
+ *   top-k runs one thread-block cluster per row (8192 < ld <= 262144 and the
+ *   clusters fit the GPU) and the slot map would take its count-and-write
+ *   form (more than four (row, 1024-entry step) pairs or 32768 block-table
+ *   words a CTA of a 16-CTA cluster), the top-k kernel also counts each
+ *   row's valid slots as it writes the row, and the slot map runs only its
+ *   ordered write.
+ * Errors: as the two calls.
+ * ---------------------------------------------------------------------- */
+idx_status idx_topk_ragged_slots(const float *logits, int64_t ld, int rows,
+                                 const int32_t *lengths, int k, int32_t *out_idx, int64_t ld_out,
+                                 void *ws, size_t ws_bytes, const int32_t *row_to_seq, int next_n,
+                                 const int32_t *block_table, int64_t bt_stride, int max_blocks,
+                                 int page_size, int num_pages, int32_t *slots, int32_t *indptr,
+                                 int32_t *lens, idx_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * idx_row_ends -- each paged row's end ke, derived on the device from the
  * context lengths by the rule idx_paged_mqa_logits applies to its rows.
  * Passage: rocm_aiter_mla_sparse, rocm_fp8_paged_mqa_logits_triton (one

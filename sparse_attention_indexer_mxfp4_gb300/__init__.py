@@ -17,6 +17,7 @@ from ._binding import (  # noqa: F401
     idx_paged_mqa_logits,
     idx_row_ends,
     idx_topk,
+    idx_topk_ragged_slots,
     idx_topk_to_ragged_slots,
     lib,
     library_path,

@@ -45,6 +45,8 @@ _SIGNATURES = {
     "idx_topk_noalloc": [_P, _L, _I, _P, _I, _P, _L, _P],
     "idx_topk_candidates": [_P, _L, _I, _P, _P, _P, _L, _I, _I, _I, _I, _P, _L, _P],
     "idx_topk_to_ragged_slots": [_P, _L, _I, _I, _P, _I, _P, _L, _I, _I, _I, _P, _P, _P, _P],
+    "idx_topk_ragged_slots": [_P, _L, _I, _P, _I, _P, _L, _P, _S, _P, _I, _P, _L, _I, _I, _I, _P,
+                              _P, _P, _P],
     "idx_paged_mqa_logits_topk": [_P, _P, _P, _P, _L, _I, _P, _L, _P, _I, _P, _I, _I, _I, _I,
                                   _I, _I, _P, _L, _I, _P, _L, _I, _P, _I, _P, _L, _I, _P, _S,
                                   _P],
@@ -417,13 +419,55 @@ def prepare_topk_to_ragged_slots(topk, block_table, page_size, num_pages, slots,
             _ptr(lens))
     return Prepared("idx_topk_to_ragged_slots", args,
                     (topk, block_table, slots, indptr, lens, row_to_seq),
-                    2 + (rows > SLOT_DIRECT_ROWS))
+                    _slot_kernels(rows, k, mb))
+
+
+def _slot_kernels(rows, k, max_blocks):
+    """Kernels of one slot-map call: one 16-CTA cluster when each CTA holds
+    at most four (row, 1024-entry step) pairs and 32768 block-table words,
+    else a count and a write kernel (and a scan above SLOT_DIRECT_ROWS rows)."""
+    r = -(-rows // 16)
+    if k >= 1 and r * -(-k // 1024) <= 4 and r * max_blocks <= 32768:
+        return 1
+    return 2 + (rows > SLOT_DIRECT_ROWS)
 
 
 def idx_topk_to_ragged_slots(topk, block_table, page_size, num_pages, slots, indptr, lens,
                              next_n=1, row_to_seq=None, max_blocks=None, stream=None):
     prepare_topk_to_ragged_slots(topk, block_table, page_size, num_pages, slots, indptr, lens,
                                  next_n, row_to_seq, max_blocks)(stream)
+
+
+def prepare_topk_ragged_slots(logits, lengths, k, out, block_table, page_size, num_pages, slots,
+                              indptr, lens, next_n=1, row_to_seq=None, max_blocks=None,
+                              workspace=True):
+    """idx_topk into out, then idx_topk_to_ragged_slots of out, as one call
+    (the cluster top-k counts each row's valid slots as it writes the row
+    where the one-launch slot map does not take the call)."""
+    top = prepare_topk(logits, lengths, k, out, workspace)
+    _need(block_table, torch.int32, "block_table")
+    rows, ld = logits.shape[0], logits.stride(0)
+    mb = block_table.shape[1] if max_blocks is None else max_blocks
+    ws = top.keep[3]
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    args = (_ptr(logits), ld, rows, _ptr(lengths), k, _ptr(out), out.stride(0), _ptr(ws), nbytes,
+            _ptr(row_to_seq), next_n, _ptr(block_table), block_table.stride(0), mb, page_size,
+            num_pages, _ptr(slots), _ptr(indptr), _ptr(lens))
+    clusters = -(-ld // 32768)
+    fused = (rows > 0 and k > 0 and 8192 < ld <= TOPK_CLUSTER_MAX_LEN
+             and rows * clusters <= _sm_count(logits.device) and _slot_kernels(rows, k, mb) != 1)
+    kernels = 2 + (rows > SLOT_DIRECT_ROWS) if fused else (
+        top.kernels + _slot_kernels(rows, k, mb))
+    return Prepared("idx_topk_ragged_slots", args,
+                    (logits, lengths, out, ws, block_table, slots, indptr, lens, row_to_seq),
+                    kernels)
+
+
+def idx_topk_ragged_slots(logits, lengths, k, out, block_table, page_size, num_pages, slots,
+                          indptr, lens, next_n=1, row_to_seq=None, max_blocks=None, stream=None,
+                          workspace=True):
+    prepare_topk_ragged_slots(logits, lengths, k, out, block_table, page_size, num_pages, slots,
+                              indptr, lens, next_n, row_to_seq, max_blocks, workspace)(stream)
 
 
 def _bf16_bits(t):

@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(kSlotThreads)
     if ((threadIdx.x & 31) == 0)
         wsum[threadIdx.x >> 5] = cnt;
     if (bad)
-        atomicOr(status, 1u);
+        atomicOr(status, kDevBadPage);
     __syncthreads();
     if (threadIdx.x == 0) {
         uint32_t t = 0;
@@ -462,7 +462,8 @@ idx_status topk_launch_short(const float *logits, int64_t ld, int rows, const in
 // IDX_ERR_UNSUPPORTED when the call is outside that range or no such
 // cluster can be resident on the device.
 idx_status topk_launch_cluster(const float *logits, int64_t ld, int rows, const int32_t *lengths,
-                               int k, int32_t *out, int64_t ld_out, int vec_ok, cudaStream_t s)
+                               int k, int32_t *out, int64_t ld_out, int vec_ok, cudaStream_t s,
+                               const SlotCount *sc = nullptr)
 {
     namespace T = topk_cluster;
     const int C = (int)((ld + T::kChunk - 1) / T::kChunk);
@@ -505,8 +506,9 @@ idx_status topk_launch_cluster(const float *logits, int64_t ld, int rows, const 
     if (resident[dev][C] < 0)
         return IDX_ERR_UNSUPPORTED;
     cfg.numAttrs = 2;  // launched programmatically after the kernel before it
+    SlotCount none = {};
     return launch_status(cudaLaunchKernelEx(&cfg, T::topk_cluster_kernel, logits, ld, rows,
-                                            lengths, k, out, ld_out, vec_ok));
+                                            lengths, k, out, ld_out, vec_ok, sc ? *sc : none));
 }
 
 } // namespace
@@ -764,32 +766,29 @@ namespace {
 // faster (64 rows of 2048 entries: 7.6 us a step for the cluster at 8 pairs
 // a CTA against 6.0 us; 32 rows: 4.0 us against 6.2 us).
 // IDX_ERR_UNSUPPORTED otherwise.
-idx_status slots_launch_cluster(const int32_t *topk, int64_t ld, int rows, int k,
-                                const int32_t *row_to_seq, int next_n, const SlotGeom &g,
-                                int32_t *slots, int32_t *indptr, int32_t *lens,
-                                unsigned int *status, cudaStream_t s)
+// Largest slot_cluster_kernel cluster the current device holds (16, else
+// 8; -1 none; 0 when the device query fails), with cfg's shared memory,
+// block and attributes set up for it.
+int slot_cluster_max(cudaLaunchConfig_t &cfg, cudaLaunchAttribute (&attr)[2])
 {
-    static int cmax[64] = {};  // largest cluster the device holds: 16 or 8; -1 none
+    static int cmax[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
-        return IDX_ERR_CUDA;
-    cudaLaunchAttribute attr[2];
+        return 0;
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     const size_t smem_max = sizeof(ScShared) + (size_t)kScMaxBt * 4;
-    cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(kScThreads);
     cfg.dynamicSmemBytes = smem_max;
-    cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (!cmax[dev]) {
         if (cudaFuncSetAttribute(slot_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem_max) != cudaSuccess)
-            return IDX_ERR_CUDA;
+            return 0;
         if (cudaFuncSetAttribute(slot_cluster_kernel,
                                  cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
             (void)cudaGetLastError();
@@ -807,20 +806,97 @@ idx_status slots_launch_cluster(const int32_t *topk, int64_t ld, int rows, int k
             }
         }
     }
-    if (cmax[dev] < 0)
-        return IDX_ERR_UNSUPPORTED;
+    return cmax[dev];
+}
+
+// Rows per CTA of the one-launch slot map for this call: 0 when it does not
+// take the call (more than kScPairs (row, step) pairs or kScMaxBt staged
+// block-table words a CTA, or no such cluster on the device), -1 when the
+// device query fails.
+int slot_cluster_rows(int rows, int k, int max_blocks, cudaLaunchConfig_t &cfg,
+                      cudaLaunchAttribute (&attr)[2])
+{
+    const int cmax = slot_cluster_max(cfg, attr);
+    if (cmax == 0)
+        return -1;
+    if (cmax < 0 || k < 1)
+        return 0;
     const int E = (k + kScThreads - 1) / kScThreads;
-    const int R = (rows + cmax[dev] - 1) / cmax[dev];
-    if (k < 1 || R * E > kScPairs || (long long)R * g.max_blocks > kScMaxBt)
+    const int R = (rows + cmax - 1) / cmax;
+    return R * E > kScPairs || (long long)R * max_blocks > kScMaxBt ? 0 : R;
+}
+
+// The one-launch slot map; IDX_ERR_UNSUPPORTED where it does not take the
+// call (slot_cluster_rows).
+idx_status slots_launch_cluster(const int32_t *topk, int64_t ld, int rows, int k,
+                                const int32_t *row_to_seq, int next_n, const SlotGeom &g,
+                                int32_t *slots, int32_t *indptr, int32_t *lens,
+                                unsigned int *status, cudaStream_t s)
+{
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = {};
+    const int R = slot_cluster_rows(rows, k, g.max_blocks, cfg, attr);
+    if (R < 0)
+        return IDX_ERR_CUDA;
+    if (R == 0)
         return IDX_ERR_UNSUPPORTED;
     const int C = (rows + R - 1) / R;
     attr[0].val.clusterDim.x = (unsigned)C;
     cfg.gridDim = dim3((unsigned)C);
     cfg.dynamicSmemBytes = sizeof(ScShared) + (size_t)R * g.max_blocks * 4;
+    cfg.stream = s;
     cfg.numAttrs = 2;  // launched programmatically after the kernel before it
     return launch_status(cudaLaunchKernelEx(&cfg, slot_cluster_kernel, topk, ld, rows, k,
                                             row_to_seq, next_n, g, R, slots, indptr, lens,
                                             status));
+}
+
+} // namespace
+} // namespace idx
+
+namespace idx {
+namespace {
+
+// Checks and page geometry of a slot-map call (idx_topk_to_ragged_slots).
+idx_status slot_args(int64_t ld, int rows, int k, const int32_t *row_to_seq, int next_n,
+                     const int32_t *block_table, int64_t bt_stride, int max_blocks,
+                     int page_size, int num_pages, const int32_t *topk, int32_t *slots,
+                     int32_t *indptr, int32_t *lens, SlotGeom *g)
+{
+    if (rows < 0 || k < 0 || ld < k || page_size <= 0 || max_blocks < 0 || num_pages < 0 ||
+        bt_stride < max_blocks || (!row_to_seq && next_n <= 0))
+        return IDX_ERR_INVALID_ARG;
+    if (!indptr)
+        return IDX_ERR_INVALID_ARG;
+    if (rows > 0 && (!lens || (k > 0 && (!topk || !slots || !block_table))))
+        return IDX_ERR_INVALID_ARG;
+    g->bt = block_table;
+    g->bt_stride = bt_stride;
+    g->max_blocks = max_blocks;
+    g->P = page_size;
+    g->shift = -1;
+    for (int i = 0; i < 31; ++i)
+        if ((1 << i) == page_size)
+            g->shift = i;
+    g->num_pages = num_pages;
+    return IDX_OK;
+}
+
+// The ordered write of the slot map (with the scan kernel first above
+// kSlotDirectRows rows), after lens holds every row's valid slots.
+cudaError_t slots_launch_write(const int32_t *topk, int64_t ld, int rows, int k,
+                               const int32_t *row_to_seq, int next_n, const SlotGeom &g,
+                               int32_t *slots, int32_t *indptr, const int32_t *lens,
+                               cudaStream_t s)
+{
+    const int scanned = rows > kSlotDirectRows;
+    cudaError_t e = cudaSuccess;
+    if (scanned)
+        e = launch_pdl(indptr_scan_kernel, dim3(1), dim3(1024), 0, s, lens, rows, indptr);
+    if (e == cudaSuccess)
+        e = launch_pdl(slot_write_kernel, dim3(rows), dim3(kSlotThreads), 0, s, topk, ld, rows, k,
+                       row_to_seq, next_n, g, lens, indptr, scanned, slots);
+    return e;
 }
 
 } // namespace
@@ -834,29 +910,18 @@ extern "C" idx_status idx_topk_to_ragged_slots(const int32_t *topk, int64_t ld, 
                                                idx_stream_t stream)
 {
     IDX_NVTX_RANGE("idx_topk_to_ragged_slots");
-    if (rows < 0 || k < 0 || ld < k || page_size <= 0 || max_blocks < 0 || num_pages < 0 ||
-        bt_stride < max_blocks || (!row_to_seq && next_n <= 0))
-        return IDX_ERR_INVALID_ARG;
-    if (!indptr)
-        return IDX_ERR_INVALID_ARG;
+    SlotGeom g;
+    const idx_status st0 = slot_args(ld, rows, k, row_to_seq, next_n, block_table, bt_stride,
+                                     max_blocks, page_size, num_pages, topk, slots, indptr, lens,
+                                     &g);
+    if (st0 != IDX_OK)
+        return st0;
     cudaStream_t s = (cudaStream_t)stream;
     if (rows == 0)
         return launch_status(cudaMemsetAsync(indptr, 0, sizeof(int32_t), s));
-    if (!lens || (k > 0 && (!topk || !slots || !block_table)))
-        return IDX_ERR_INVALID_ARG;
     unsigned int *status = device_status_ptr();
     if (!status)
         return IDX_ERR_CUDA;
-    SlotGeom g;
-    g.bt = block_table;
-    g.bt_stride = bt_stride;
-    g.max_blocks = max_blocks;
-    g.P = page_size;
-    g.shift = -1;
-    for (int i = 0; i < 31; ++i)
-        if ((1 << i) == page_size)
-            g.shift = i;
-    g.num_pages = num_pages;
     {
         const idx_status st = slots_launch_cluster(topk, ld, rows, k, row_to_seq, next_n, g,
                                                    slots, indptr, lens, status, s);
@@ -865,14 +930,77 @@ extern "C" idx_status idx_topk_to_ragged_slots(const int32_t *topk, int64_t ld, 
     }
     cudaError_t e = launch_pdl(slot_count_kernel, dim3(rows), dim3(kSlotThreads), 0, s, topk, ld,
                                rows, k, row_to_seq, next_n, g, lens, status);
-    const int scanned = rows > kSlotDirectRows;
-    if (e == cudaSuccess && scanned)
-        e = launch_pdl(indptr_scan_kernel, dim3(1), dim3(1024), 0, s, (const int32_t *)lens, rows,
-                       indptr);
     if (e == cudaSuccess)
-        e = launch_pdl(slot_write_kernel, dim3(rows), dim3(kSlotThreads), 0, s, topk, ld, rows, k,
-                       row_to_seq, next_n, g, (const int32_t *)lens, indptr, scanned, slots);
+        e = slots_launch_write(topk, ld, rows, k, row_to_seq, next_n, g, slots, indptr,
+                               (const int32_t *)lens, s);
     return launch_status(e);
+}
+
+extern "C" idx_status idx_topk_ragged_slots(const float *logits, int64_t ld, int rows,
+                                            const int32_t *lengths, int k, int32_t *out_idx,
+                                            int64_t ld_out, void *ws, size_t ws_bytes,
+                                            const int32_t *row_to_seq, int next_n,
+                                            const int32_t *block_table, int64_t bt_stride,
+                                            int max_blocks, int page_size, int num_pages,
+                                            int32_t *slots, int32_t *indptr, int32_t *lens,
+                                            idx_stream_t stream)
+{
+    IDX_NVTX_RANGE("idx_topk_ragged_slots");
+    if (rows < 0 || k < 0 || ld < 0 || ld_out < k || ld > INT32_MAX)
+        return IDX_ERR_INVALID_ARG;
+    if (rows > 0 && k > 0 && (!logits || !lengths || !out_idx || ld <= 0))
+        return IDX_ERR_INVALID_ARG;
+    SlotGeom g;
+    const idx_status st0 = slot_args(ld_out, rows, k, row_to_seq, next_n, block_table, bt_stride,
+                                     max_blocks, page_size, num_pages, out_idx, slots, indptr,
+                                     lens, &g);
+    if (st0 != IDX_OK)
+        return st0;
+    cudaStream_t s = (cudaStream_t)stream;
+    // rows of 8193 .. 262144 keys on the cluster top-k, which counts each
+    // row's valid slots as it writes the row: then only the ordered write
+    // of the slot map runs (unless the one-launch slot map takes the call:
+    // it is the shorter of the two)
+    int sc_rows = 0;
+    if (rows > 0 && k > 0) {
+        cudaLaunchAttribute attr[2];
+        cudaLaunchConfig_t cfg = {};
+        sc_rows = slot_cluster_rows(rows, k, max_blocks, cfg, attr);
+        if (sc_rows < 0)
+            return IDX_ERR_CUDA;
+    }
+    if (rows > 0 && k > 0 && sc_rows == 0 && ld > topk_short::kMaxLen &&
+        ld <= topk_cluster::kMaxLen) {
+        unsigned int *status = device_status_ptr();
+        if (!status)
+            return IDX_ERR_CUDA;
+        SlotCount sc;
+        sc.bt = g.bt;
+        sc.bt_stride = g.bt_stride;
+        sc.max_blocks = g.max_blocks;
+        sc.P = g.P;
+        sc.shift = g.shift;
+        sc.num_pages = g.num_pages;
+        sc.row_to_seq = row_to_seq;
+        sc.next_n = next_n;
+        sc.lens = lens;
+        sc.status = status;
+        const int vec_ok = (ld % 4 == 0) && aligned16(logits);
+        const idx_status st = topk_launch_cluster(logits, ld, rows, lengths, k, out_idx, ld_out,
+                                                  vec_ok, s, &sc);
+        if (st == IDX_OK)
+            return launch_status(slots_launch_write(out_idx, ld_out, rows, k, row_to_seq, next_n,
+                                                    g, slots, indptr, (const int32_t *)lens, s));
+        if (st != IDX_ERR_UNSUPPORTED)
+            return st;
+    }
+    const idx_status st = idx_topk(logits, ld, rows, lengths, k, out_idx, ld_out, ws, ws_bytes,
+                                   stream);
+    if (st != IDX_OK)
+        return st;
+    return idx_topk_to_ragged_slots(out_idx, ld_out, rows, k, row_to_seq, next_n, block_table,
+                                    bt_stride, max_blocks, page_size, num_pages, slots, indptr,
+                                    lens, stream);
 }
 
 // ------------------------------------------------ row ends and tail fill

@@ -24,6 +24,31 @@
 #include "idx_common.cuh"
 
 namespace idx {
+// Slot counting in a top-k kernel that writes a row's indices (the fused
+// top-k -> ragged slots call): the slot of position p of sequence b is valid
+// when its logical page p / P is below max_blocks and bt[b, p / P] lies in
+// [0, num_pages).  bt == nullptr: no counting.  lens[row] receives the
+// row's valid slots; an invalid one sets kDevBadPage in *status.
+struct SlotCount {
+    const int32_t *bt;
+    int64_t bt_stride;
+    int max_blocks, P, shift, num_pages;  // shift = log2(P) when P is a power of two, else -1
+    const int32_t *row_to_seq;            // nullptr: row / next_n
+    int next_n;
+    int32_t *lens;
+    unsigned int *status;
+};
+
+// Whether the slot of position p of sequence b is valid (see SlotCount).
+__device__ __forceinline__ bool slot_valid(const SlotCount &sc, int b, int p)
+{
+    const int lp = sc.shift >= 0 ? p >> sc.shift : p / sc.P;
+    if (lp >= sc.max_blocks)
+        return false;
+    const int pg = __ldg(sc.bt + (size_t)b * sc.bt_stride + lp);
+    return pg >= 0 && pg < sc.num_pages;
+}
+
 namespace topk_detail {
 
 constexpr int kThreads = 512;

@@ -90,7 +90,7 @@ __device__ __forceinline__ void find_bin_cluster(cg::cluster_group &cl, Shared &
 __global__ void __launch_bounds__(kThreads, 1)
     topk_cluster_kernel(const float *__restrict__ logits, int64_t ld, int rows,
                         const int32_t *__restrict__ lengths, int k, int32_t *__restrict__ out,
-                        int64_t ld_out, int vec_ok)
+                        int64_t ld_out, int vec_ok, const SlotCount sc)
 {
     extern __shared__ __align__(16) uint8_t dsm[];
     Shared &sh = *reinterpret_cast<Shared *>(dsm);
@@ -104,6 +104,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         (i < 2048 ? sh.h1[i] : i < 4096 ? sh.h2[i - 2048] : sh.h3[i - 4096]) = 0u;
     pdl_wait();  // the logits and lengths may come from the kernel before this one
     pdl_launch_dependents();
+    // the row's slot count starts at 0 (ordered before every CTA's addition
+    // by the cluster barriers between)
+    if (sc.bt && live && rank == 0 && tid == 0)
+        sc.lens[row] = 0;
     const int len = live ? max(0, min(lengths[row], (int)ld)) : 0;
     // the row's keys spread evenly over the cluster, whole quads per CTA (the
     // chunk starts stay 16-byte aligned for vector loads)
@@ -252,6 +256,9 @@ found:
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
     const uint32_t lt = (1u << lane) - 1u;
     int32_t *orow = out + (size_t)(live ? row : 0) * ld_out;
+    uint32_t nslot = 0, nbad = 0;  // valid and invalid slots of this thread's taken keys
+    const int seq = sc.bt && live ? (sc.row_to_seq ? __ldg(sc.row_to_seq + row) : row / sc.next_n)
+                                  : 0;
     if (live) {
         #pragma unroll
         for (int s = 0; s < kSteps; ++s) {
@@ -280,13 +287,28 @@ found:
                            (all_ties ? 0u : min(eq0, ties)) + tk_below;
             #pragma unroll
             for (int e = 0; e < 4; ++e)
-                if (tk[e])
-                    orow[pos++] = base + 4 * (s * kThreads + tid) + e;
+                if (tk[e]) {
+                    const int p = base + 4 * (s * kThreads + tid) + e;
+                    orow[pos++] = p;
+                    if (sc.bt) {
+                        const bool ok = slot_valid(sc, seq, p);
+                        nslot += ok;
+                        nbad += !ok;
+                    }
+                }
         }
         if (rank == 0) {
             const int nsel = (int)min(total, (uint32_t)k);
             for (int j = nsel + tid; j < k; j += kThreads)
                 orow[j] = -1;
+        }
+        if (sc.bt) {
+            nslot = __reduce_add_sync(0xffffffffu, nslot);
+            nbad = __reduce_add_sync(0xffffffffu, nbad);
+            if (lane == 0 && nslot)
+                atomicAdd(sc.lens + row, (int32_t)nslot);
+            if (lane == 0 && nbad)
+                atomicOr(sc.status, kDevBadPage);
         }
     }
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");

@@ -33,11 +33,14 @@ class IndexerStep:
     instead (the same keys at other addresses).  ``fused_topk`` (paged, no candidate list) runs
     the logits and the row top-k as one idx_paged_mqa_logits_topk call, the
     logits kernel counting the top-k's first digit; its logits stage then
-    holds the top-k too."""
+    holds the top-k too.  ``fused_slots`` (paged, the row top-k as its own
+    call) runs the top-k and the slot map as one idx_topk_ragged_slots call,
+    the top-k counting each row's valid slots; its top-k stage then holds
+    the slot map too."""
 
     def __init__(self, case, device="cuda", fused_mask: bool = True, num_ctas: int = 0,
                  gather: bool = True, cand_topk: bool = True, kv_from=None,
-                 fused_topk: bool = False, kv_copy: bool = False):
+                 fused_topk: bool = False, kv_copy: bool = False, fused_slots: bool = True):
         self.case = case
         self.device = torch.device(device)
         self.fused_mask = fused_mask
@@ -45,6 +48,7 @@ class IndexerStep:
         self.cand_topk = bool(cand_topk and gather and fused_mask)
         self.fused_topk = bool(fused_topk and isinstance(case, PagedCase) and case.cand is None)
         self.num_ctas = num_ctas
+        self.fused_slots = fused_slots
         d = self.device
         self.paged = isinstance(case, PagedCase)
         self.q = _dev(case.q, d)
@@ -156,6 +160,12 @@ class IndexerStep:
                 row_ks=self.row_ks)
         elif fused is not None:
             self._topk_call = None  # inside the fused logits call
+        elif self.paged and self.fused_slots:
+            self._topk_call = B.prepare_topk_ragged_slots(
+                self.logits, self.lengths, self.k_top, self.topk, self.block_table, c.page_size,
+                c.num_pages, self.slots, self.indptr, self.lens, next_n=c.next_n,
+                max_blocks=self.max_blocks)
+            self._slots_call = None  # inside the top-k call
         else:
             self._topk_call = B.prepare_topk(self.logits, self.lengths, self.k_top, self.topk)
         # the candidate pool: the best blocks of each row, from the block maxima
@@ -191,7 +201,7 @@ class IndexerStep:
         return IndexerStep(self.case, device=self.device, fused_mask=self.fused_mask,
                            num_ctas=self.num_ctas, gather=self.gather,
                            cand_topk=self.cand_topk, kv_from=self, fused_topk=self.fused_topk,
-                           kv_copy=kv_copy)
+                           kv_copy=kv_copy, fused_slots=self.fused_slots)
 
     def input_names(self):
         """The per-step inputs a caller copies in (the K cache is state; paged

@@ -24,7 +24,8 @@ def _declared():
 def test_header_declares_the_five_operations():
     names = _declared()
     for n in ["idx_mqa_logits", "idx_paged_mqa_logits", "idx_apply_candidate_mask", "idx_topk",
-              "idx_topk_to_ragged_slots", "idx_get_device_status", "idx_version",
+              "idx_topk_to_ragged_slots", "idx_topk_ragged_slots", "idx_get_device_status",
+              "idx_version",
               "idx_topk_workspace_size"]:
         assert n in names
 
@@ -178,6 +179,17 @@ def test_select_argument_checks():
     assert g(FAKE, 4, 2, 8, None, 1, FAKE, 10, 10, 64, 100, FAKE, FAKE, FAKE, None) == INVALID
     assert g(FAKE, 8, 2, 8, None, 0, FAKE, 10, 10, 64, 100, FAKE, FAKE, FAKE, None) == INVALID
     assert g(FAKE, 8, 2, 8, None, 1, FAKE, 10, 10, 0, 100, FAKE, FAKE, FAKE, None) == INVALID
+    h = L.idx_topk_ragged_slots  # top-k checks, then the slot map's
+    assert h(FAKE, 100, 2, FAKE, 10, FAKE, 5, None, 0, None, 1, FAKE, 10, 10, 64, 100, FAKE,
+             FAKE, FAKE, None) == INVALID  # ld_out < k
+    assert h(None, 100, 2, FAKE, 10, FAKE, 10, None, 0, None, 1, FAKE, 10, 10, 64, 100, FAKE,
+             FAKE, FAKE, None) == INVALID
+    assert h(FAKE, 100, 2, FAKE, 10, FAKE, 10, None, 0, None, 0, FAKE, 10, 10, 64, 100, FAKE,
+             FAKE, FAKE, None) == INVALID  # next_n 0 without row_to_seq
+    assert h(FAKE, 100, 2, FAKE, 10, FAKE, 10, None, 0, None, 1, FAKE, 10, 10, 0, 100, FAKE,
+             FAKE, FAKE, None) == INVALID  # page_size 0
+    assert h(FAKE, 100, 2, FAKE, 10, FAKE, 10, None, 0, None, 1, FAKE, 10, 10, 64, 100, FAKE,
+             None, FAKE, None) == INVALID  # no indptr
     assert L.idx_get_device_status(None, None) == INVALID
 
 

@@ -274,6 +274,90 @@ def test_slots_row_to_seq_invalid_pages_many_rows(rows, k):
     np.testing.assert_array_equal(slots.cpu().numpy()[:ip[-1]], s_)
 
 
+def _ascending(ora_idx):
+    """The oracle's top-k rows in the library's layout: ascending indices,
+    then -1 padding (the slot map keeps the order of its top-k rows)."""
+    out = np.full_like(ora_idx, -1)
+    for r, row in enumerate(ora_idx):
+        v = np.sort(row[row >= 0])
+        out[r, :len(v)] = v
+    return out
+
+
+# idx_topk_ragged_slots.  The cluster top-k counting slots as it writes, where
+# the one-launch slot map does not take the call: (64, 65536, 2048) and
+# (40, 40000, 2048) at more than four (row, 1024-entry step) pairs a CTA of
+# its 16-CTA cluster, (2, 150000, 5000) at five steps a row, 4-token pages
+# of 150000 and 262144-key rows (over 32768 block-table words a CTA).  The
+# two-call forms: (12, 40000, 2048) (the one-launch slot map), 5000-key rows
+# (one CTA a row), 160 rows of 40000 (320 cluster CTAs: the chunked top-k),
+# 300001-key rows (past the cluster).  Beside each: an explicit
+# row-to-sequence map or next_n rows a sequence, block-table entries outside
+# the pool, positions past the table.
+@pytest.mark.parametrize("rows,width,k,P,next_n,r2s,ties", [
+    (64, 65536, 2048, 64, 1, False, None), (40, 40000, 2048, 64, 2, False, None),
+    (2, 150000, 5000, 64, 1, True, None), (6, 150000, 512, 4, 3, True, 4),
+    (3, 262144, 2048, 4, 1, False, None), (12, 40000, 2048, 64, 2, False, None),
+    (9, 5000, 2048, 64, 1, True, None), (160, 40000, 512, 64, 2, False, None),
+    (2, 300001, 2048, 64, 1, True, None)])
+def test_topk_ragged_slots_fused(rows, width, k, P, next_n, r2s, ties):
+    rng = np.random.default_rng(rows * 11 + width + k)
+    x = _random_logits(rng, rows, width, tie_levels=ties, neg_inf_frac=0.05)
+    lengths = rng.integers(0, width + 1, size=rows).astype(np.int32)
+    lengths[0] = width
+    nseq = -(-rows // next_n) if not r2s else max(2, rows // 3)
+    max_blocks = -(-width // P) - 3                 # the last pages' keys map past the row
+    num_pages = nseq * max_blocks + 100
+    bt = np.stack([rng.permutation(num_pages)[:max_blocks] for _ in range(nseq)]).astype(np.int32)
+    bad = rng.random(bt.shape) < 0.01
+    bt[bad] = rng.choice([-1, num_pages, num_pages + 5], size=int(bad.sum()))
+    bt[::2, 0] = -1                                  # first pages of every other sequence
+    row_to_seq = rng.integers(0, nseq, size=rows).astype(np.int32) if r2s else None
+    out = torch.full((rows, k), -7, dtype=torch.int32, device="cuda")
+    slots = torch.empty(rows * k, dtype=torch.int32, device="cuda")
+    indptr = torch.empty(rows + 1, dtype=torch.int32, device="cuda")
+    lens = torch.full((rows,), -9, dtype=torch.int32, device="cuda")
+    B.idx_get_device_status()
+    B.idx_topk_ragged_slots(_t(x), _t(lengths), k, out, _t(bt), P, num_pages, slots, indptr,
+                            lens, next_n=next_n,
+                            row_to_seq=None if row_to_seq is None else _t(row_to_seq))
+    torch.cuda.synchronize()
+    ora = oracle.topk(x, lengths, k)
+    assert_topk_exact(out.cpu().numpy(), ora)
+    s, ip, ln, nbad = oracle.topk_to_ragged_slots(_ascending(ora), bt, P, num_pages,
+                                                  next_n=next_n, row_to_seq=row_to_seq)
+    assert bool(B.idx_get_device_status() & B.DEV_BAD_PAGE) == (nbad > 0)
+    np.testing.assert_array_equal(lens.cpu().numpy(), ln)
+    np.testing.assert_array_equal(indptr.cpu().numpy(), ip)
+    np.testing.assert_array_equal(slots.cpu().numpy()[:ip[-1]], s)
+
+
+def test_topk_ragged_slots_fused_all_valid():
+    """No invalid slot: the device status stays clear (40 rows of 2048:
+    the cluster top-k counts the slots)."""
+    rng = np.random.default_rng(5)
+    rows, width, k, P = 40, 65536, 2048, 64
+    x = _random_logits(rng, rows, width)
+    lengths = rng.integers(width // 2, width + 1, size=rows).astype(np.int32)
+    max_blocks = width // P
+    bt = np.stack([rng.permutation(rows * max_blocks)[:max_blocks]
+                   for _ in range(rows)]).astype(np.int32)
+    out = torch.empty((rows, k), dtype=torch.int32, device="cuda")
+    slots = torch.empty(rows * k, dtype=torch.int32, device="cuda")
+    indptr = torch.empty(rows + 1, dtype=torch.int32, device="cuda")
+    lens = torch.empty(rows, dtype=torch.int32, device="cuda")
+    B.idx_get_device_status()
+    B.idx_topk_ragged_slots(_t(x), _t(lengths), k, out, _t(bt), P, rows * max_blocks, slots,
+                            indptr, lens)
+    torch.cuda.synchronize()
+    ora = oracle.topk(x, lengths, k)
+    s, ip, ln, nbad = oracle.topk_to_ragged_slots(_ascending(ora), bt, P, rows * max_blocks)
+    assert nbad == 0 and B.idx_get_device_status() == 0
+    assert (ln == k).all()
+    np.testing.assert_array_equal(indptr.cpu().numpy(), ip)
+    np.testing.assert_array_equal(slots.cpu().numpy()[:ip[-1]], s)
+
+
 def _cand_case(rng, rows, width, num_cand, blk, row_repeat=1, ties=None):
     if ties == "narrow":
         # distinct values inside one bin of the first radix digit
