@@ -44,6 +44,15 @@ IDX_DEVFN void mbar_arrive(uint64_t *bar)
                  : "memory");
 }
 
+// n arrivals at once (release semantics, as n single arrivals).
+IDX_DEVFN void mbar_arrive_cnt(uint64_t *bar, uint32_t n)
+{
+    asm volatile("{\n\t.reg .b64 st;\n\t"
+                 "mbarrier.arrive.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+                 "r"(n)
+                 : "memory");
+}
+
 IDX_DEVFN void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
 {
     asm volatile("{\n\t.reg .b64 st;\n\t"

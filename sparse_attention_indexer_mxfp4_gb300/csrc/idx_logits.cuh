@@ -337,6 +337,15 @@ __device__ __forceinline__ bool walk_last_in_group(const UnitWalk &w)
     return w.left == 1 || w.k + 1 >= w.n;
 }
 
+// At a group's first unit: whether the walk ends in this group.  It goes on
+// to another group only if units are left after this group's beyond the
+// next group's charged units (paged; walk_next charges them on entry).
+__device__ __forceinline__ bool walk_group_is_last(const LogitsArgs &a, const UnitWalk &w)
+{
+    const long long after = (long long)w.k + w.left - w.n;
+    return after <= (a.paged ? (long long)a.group_cost : 0LL);
+}
+
 // Next unit: the group's next one, else the first of the next group that
 // has units (after its charged units, paged).
 template <bool PLAN>

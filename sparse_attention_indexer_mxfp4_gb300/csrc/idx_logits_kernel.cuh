@@ -39,6 +39,32 @@ constexpr int kFmtMxfp4 = 1;
 // control warp and NA epilogue warps, and the per-tile issue cost of each
 // control role is split over two warps.
 constexpr int kFirstEpiWarp = 4;
+
+// Tile descriptor: {j, gq}, written by the MMA warp beside each tile it
+// issues (and {kDescDone, -} after the last one where the epilogue cannot
+// tell that it was the last), from which the accumulator's epilogue
+// warpgroup takes the tile's place: only the control warps walk the CTA's
+// unit range.  j: tile index within the group (keys [j TK, (j + 1) TK)); gq:
+// the CTA's count of the group (Q slot gq & 1, its q_full phase (gq >> 1) & 1).
+// Compute tiles go to the accumulators in turn (tile c to c % NA), so the
+// epilogue's use u of accumulator a is the CTA's compute tile a + u NA.
+constexpr int kDescDone = -1;
+
+// Group block: 16 words beside each Q slot, written by producer 0 before the
+// slot's q_full arrival: rows, ranges and the keys live in every row.
+enum GroupBlock : int {
+    kGrpNrows = 0,
+    kGrpRow0 = 1,
+    kGrpLo = 2,    // union of the rows' ranges [lo, hi)
+    kGrpHi = 3,
+    kGrpInLo = 4,  // keys live in every row: [in_lo, in_hi)
+    kGrpInHi = 5,
+    kGrpCEnd = 6,  // end of the group's compute tiles in the CTA's count
+    kGrpLast = 7,  // 1: the CTA's range ends in this group
+    kGrpRks = 8,   // rows' starts (four words), then ends (four words)
+    kGrpRke = 12,
+    kGrpWords = 16,
+};
 constexpr int kMmaWarp = 2;
 
 template <int FMT, int H, int G, int S, int NA, int TK>
@@ -68,11 +94,15 @@ struct LogitsCfg {
     static constexpr int OFF_Q = OFF_STAGE + S * STAGE_BYTES;
     static constexpr int OFF_W = OFF_Q + 2 * Q_BYTES;
     static constexpr int OFF_QS = OFF_W + 2 * W_BYTES;
-    static constexpr int OFF_QATOM = OFF_QS + 2 * QS_BYTES;
+    static constexpr int GRP_BYTES = 4 * kGrpWords;  // group block per Q slot
+    static constexpr int OFF_GRP = OFF_QS + 2 * QS_BYTES;
+    static constexpr int OFF_QATOM = OFF_GRP + 2 * GRP_BYTES;
     // per accumulator: the tile's key scales (FP8) and flags, copied out of
-    // the stage by the MMA warp so that the stage is free once the MMA is done
+    // the stage by the MMA warp so that the stage is free once the MMA is done,
+    // and the tile's descriptor (TileDesc words) for the epilogue
     static constexpr int SIDE_FLAGS = FMT == kFmtFp8 ? TK * 4 : 0;
-    static constexpr int SIDE_BYTES = SIDE_FLAGS + 16;
+    static constexpr int SIDE_DESC = SIDE_FLAGS + 16;
+    static constexpr int SIDE_BYTES = SIDE_DESC + 16;  // descriptor: two words, padded
     static constexpr int OFF_SIDE = OFF_QATOM + 4 * QATOM_BYTES;
     static constexpr int OFF_BAR = (OFF_SIDE + NA * SIDE_BYTES + 7) / 8 * 8;
     // full[S], empty[S], acc_full[NA], acc_empty[NA], q_full[2], q_empty[2]
@@ -94,6 +124,7 @@ struct LogitsCfg {
     static_assert(NCOLS % 16 == 0 && NCOLS >= 16 && NCOLS <= 256, "MMA N out of range");
     static_assert(H % 32 == 0, "heads are read from TMEM 32 columns at a time");
     static_assert(NA == 2 || NA == 3, "two or three epilogue warpgroups");
+    static_assert(G <= 4, "the group block holds four rows' ranges");
     static constexpr int EPI_WARPS = 4 * NA;
     static constexpr int THREADS = 32 * (kFirstEpiWarp + EPI_WARPS);
     // Tile c uses stage c % S.  S a multiple of 2 and of NA keeps every stage
@@ -190,6 +221,12 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
 {
     using C = LogitsCfg<FMT, H, G, S, NA, TK>;
     constexpr int TSH = TK == 256 ? 8 : 7;  // equals a.tile_shift
+    // Tile descriptors (only the control warps walk the units; the epilogue
+    // takes each tile from its descriptor) where the epilogue's arithmetic
+    // per tile is the largest: block maxima, four-row groups.  Elsewhere
+    // every warp walks the units, which keeps the control warps' work per
+    // tile, on those workloads the longer chain, at its least.
+    constexpr bool DESC = BMAX || G == 4;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // swizzled TMA tiles and MMA descriptors assume 1024-byte aligned tiles
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -282,7 +319,22 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
         int win0 = 0;      // first tile of the current page window
         HalfInfo cur = {}, nxt = {};
         bool cur_ok = false;
+        int nfill = 0;     // fill units seen (producer nfill & 1 writes each)
+        int fke = 0;       // lane i < nrows: row i's end
         for (; w.left > 0; walk_next<PLAN>(a, w)) {
+            int fks = 0;
+            if (w.first_in_group) {
+                // page window of this group: current and next, block-table
+                // loads in flight before anything else
+                win0 = w.k;
+                cur = half_info<C::NH, PLAN>(a, w, win0, lane);
+                nxt = half_info<C::NH, PLAN>(a, w, win0 + C::WIN_TILES, lane);
+                cur_ok = false;
+                // (descriptors) the rows' ranges, lane i holding row i's
+                fke = 0;
+                if (DESC && lane < w.gi.nrows)
+                    row_range(a, w.gi.row0 + lane, fks, fke);
+            }
             if (w.first_in_group && pw == 0) {
                 const int slot = gq & 1;
                 if (!mbar_wait(&q_empty[slot], ((gq >> 1) & 1) ^ 1, abort_flag, a.status))
@@ -303,6 +355,48 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
                         }
                     }
                     __syncwarp();
+                }
+                if constexpr (DESC) {
+                    // this CTA's compute tiles of the group: c .. cend - 1 (tile c to
+                    // accumulator c % NA); an accumulator that gets none of them is
+                    // done with the Q slot at once (its warpgroup's four arrivals)
+                    const long long kend = min((long long)w.n, (long long)w.k + w.left);
+                    long long ncomp;
+                    if constexpr (PLAN) {
+                        ncomp = kend - w.k;
+                    } else {
+                        const long long jlo = w.gi.hi > w.gi.lo ? (w.gi.lo >> TSH) : kend;
+                        const long long jhi = w.gi.hi > w.gi.lo ? ((w.gi.hi - 1) >> TSH) + 1 : kend;
+                        ncomp = max(0LL, min(kend, jhi) - max((long long)w.k, jlo));
+                    }
+                    const int cend = c + (int)ncomp;
+                    const int glast = walk_group_is_last(a, w);
+                    if (lane == 0)
+                        for (int acc = 0; acc < NA; ++acc)
+                            if (((acc - c % NA) + NA) % NA >= ncomp)
+                                mbar_arrive_cnt(&q_empty[slot], 4);
+                    {
+                        // the group block, published by the q_full arrival below
+                        const int in_lo = __reduce_max_sync(0xffffffffu, lane < nrows ? fks : 0);
+                        const int in_hi =
+                            __reduce_min_sync(0xffffffffu, lane < nrows ? fke : 0x7fffffff);
+                        const int rk = __shfl_sync(0xffffffffu, fks, (lane - kGrpRks) & 31);
+                        const int re = __shfl_sync(0xffffffffu, fke, (lane - kGrpRke) & 31);
+                        if (lane < kGrpWords)
+                            reinterpret_cast<int *>(smem + C::OFF_GRP + slot * C::GRP_BYTES)[lane] =
+                                lane == kGrpNrows   ? nrows
+                                : lane == kGrpRow0  ? w.gi.row0
+                                : lane == kGrpLo    ? w.gi.lo
+                                : lane == kGrpHi    ? w.gi.hi
+                                : lane == kGrpInLo  ? in_lo
+                                : lane == kGrpInHi  ? in_hi
+                                : lane == kGrpCEnd  ? cend
+                                : lane == kGrpLast  ? glast
+                                : lane >= kGrpRks && lane < kGrpRks + G ? rk
+                                : lane >= kGrpRke && lane < kGrpRke + G ? re
+                                                                         : 0;
+                        __syncwarp();
+                    }
                 }
                 if (lane == 0) {
                     uint32_t bytes = (uint32_t)(C::NCOLS * C::ROWB) + nrows * H * 4;
@@ -325,15 +419,27 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
                 __syncwarp();
                 ++gq;
             }
-            if (w.first_in_group) {
-                // page window of this group: current and next, loads in flight
-                win0 = w.k;
-                cur = half_info<C::NH, PLAN>(a, w, win0, lane);
-                nxt = half_info<C::NH, PLAN>(a, w, win0 + C::WIN_TILES, lane);
-                cur_ok = false;
-            }
-            if (!unit_compute<PLAN>(w, TSH))
+            if (!unit_compute<PLAN>(w, TSH)) {
+                // (descriptors) a fill unit: -inf over the tile for each row,
+                // up to its end; without descriptors the epilogue writes it
+                if (DESC && (nfill++ & 1) == pw) {
+                    const int t0 = w.j << TSH;
+                    const int wend = a.paged ? w.gi.hi : a.N;
+                    #pragma unroll 1
+                    for (int i = 0; i < w.gi.nrows; ++i) {
+                        const int ke = __shfl_sync(0xffffffffu, fke, i);
+                        const int end = min(wend, a.paged ? ke : a.N);
+                        float *orow = a.logits + (size_t)(w.gi.row0 + i) * a.ld;
+                        #pragma unroll
+                        for (int m = 0; m < TK / 32; ++m) {
+                            const int t = t0 + m * 32 + lane;
+                            if (t < end)
+                                orow[t] = -INFINITY;
+                        }
+                    }
+                }
                 continue;
+            }
             if ((c & 1) != pw) {  // the other producer's tile
                 ++c;
                 continue;
@@ -405,10 +511,14 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
         }
     } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
         // ------------------------------------------------------------ MMA issuers
-        const int mw = warp - kMmaWarp;  // issues the tiles with (c % NA) & 1 == mw
+        // MMA warp mw issues the tiles with (c % NA) & 1 == mw and writes
+        // each one's descriptor for the accumulator's epilogue warpgroup.
+        const int mw = warp - kMmaWarp;
         int gq = 0;
         int c = 0;
         int slot = 0;
+        uint32_t in_group = 0;  // accumulators with a compute tile in the current group
+        bool glast = false;     // the current group is the CTA's last
         for (; w.left > 0; walk_next<PLAN>(a, w)) {
             if (w.first_in_group) {
                 slot = gq & 1;
@@ -442,11 +552,34 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
                     }
                     __syncwarp();
                 }
+                if constexpr (DESC) {
+                    // which accumulators get a compute tile of the group (the
+                    // epilogue ends on the last group's last tile of each)
+                    const long long kend = min((long long)w.n, (long long)w.k + w.left);
+                    long long ncomp;
+                    if constexpr (PLAN) {
+                        ncomp = kend - w.k;
+                    } else {
+                        const long long jlo = w.gi.hi > w.gi.lo ? (w.gi.lo >> TSH) : kend;
+                        const long long jhi =
+                            w.gi.hi > w.gi.lo ? ((w.gi.hi - 1) >> TSH) + 1 : kend;
+                        ncomp = max(0LL, min(kend, jhi) - max((long long)w.k, jlo));
+                    }
+                    glast = walk_group_is_last(a, w);
+                    in_group = 0;
+                    for (int acc = 0; acc < NA; ++acc)
+                        if (((acc - c % NA) + NA) % NA < ncomp)
+                            in_group |= 1u << acc;
+                }
+                __syncwarp();
                 ++gq;
             }
-            if (unit_compute<PLAN>(w, TSH) && ((c % NA) & 1) != mw) {
+            const bool compute = unit_compute<PLAN>(w, TSH);
+            if (!compute) {
+                // a fill unit (the producers write it)
+            } else if (((c % NA) & 1) != mw) {
                 ++c;  // the other MMA warp's tile
-            } else if (unit_compute<PLAN>(w, TSH)) {
+            } else {
                 const int acc = c % NA;
                 const int s = C::stage(c);
                 if (!mbar_wait(&acc_empty[acc], (uint32_t)((c / NA) & 1) ^ 1, abort_flag, a.status))
@@ -454,9 +587,9 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
                 if (!mbar_wait(&full[s], C::phase(c), abort_flag, a.status))
                     break;
                 uint8_t *st = smem + C::OFF_STAGE + s * C::STAGE_BYTES;
+                uint8_t *sd = smem + C::OFF_SIDE + acc * C::SIDE_BYTES;
                 {
                     // the epilogue's key scales and flags, out of the stage
-                    uint8_t *sd = smem + C::OFF_SIDE + acc * C::SIDE_BYTES;
                     if constexpr (FMT == kFmtFp8) {
                         const float4 *src = reinterpret_cast<const float4 *>(st + C::A_BYTES);
                         #pragma unroll
@@ -518,9 +651,11 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
                             }
                         }
                     }
+                    if (DESC)
+                        *reinterpret_cast<int2 *>(sd + C::SIDE_DESC) = make_int2(w.j, gq - 1);
                     mma_commit(&empty[s]);
                     mma_commit(&acc_full[acc]);
-                    mbar_arrive(&acc_full[acc]);  // releases the side copy
+                    mbar_arrive(&acc_full[acc]);  // releases the side copy and descriptor
                 }
                 __syncwarp();
                 ++c;
@@ -528,6 +663,24 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
             if (walk_last_in_group(w)) {
                 if (lane == 0)
                     mma_commit(&q_empty[slot]);
+                __syncwarp();
+            }
+        }
+        if (DESC && !*abort_flag) {
+            // each of this warp's accumulators whose last tile the epilogue
+            // could not tell was the last (none in the CTA's last group): a
+            // descriptor without a tile, once the epilogue has drained it
+            for (int acc = mw; acc < NA; acc += 2) {
+                if (glast && ((in_group >> acc) & 1u))
+                    continue;
+                const int uses = c > acc ? (c - acc + NA - 1) / NA : 0;
+                if (!mbar_wait(&acc_empty[acc], (uint32_t)(uses & 1) ^ 1, abort_flag, a.status))
+                    break;
+                if (lane == 0) {
+                    uint8_t *sd = smem + C::OFF_SIDE + acc * C::SIDE_BYTES;
+                    reinterpret_cast<int *>(sd + C::SIDE_DESC)[0] = kDescDone;
+                    mbar_arrive_cnt(&acc_full[acc], 2);
+                }
                 __syncwarp();
             }
         }
@@ -542,18 +695,24 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
         }
     } else if (warp >= kFirstEpiWarp) {
         // ------------------------------------------------------------ epilogue
-        // NA warpgroups; warpgroup wg owns accumulator wg, i.e. the compute
-        // tiles with c % NA == wg, and the fill tiles with u % NA == wg.
+        // NA warpgroups; warpgroup wg drains accumulator wg.  With
+        // descriptors, every tile the MMA warp issues into it comes with one
+        // (the tile and its row group) and the group's rows, ranges and
+        // compute-tile end come from the group block beside its Q slot.
+        // Without, the warpgroup walks the units: it drains the compute
+        // tiles with c % NA == wg and writes the fill units with u % NA == wg.
         const int ew = warp - kFirstEpiWarp;
         const int wg = ew >> 2;
+        const int acc = wg;
         const int quad = warp & 3;            // TMEM lane quadrant of this warp
         const int kq = quad * 32 + lane;      // key of each 128-key MMA block this thread owns
-        int gq = 0;
-        int c = 0;          // compute tiles seen (all warpgroups')
-        long long u = 0;    // units seen
-        int slot = 0;
+        int gq = DESC ? -1 : 0;               // group of the last descriptor / groups started
+        int c = 0;                            // (walk) compute tiles seen, all warpgroups'
+        long long u = 0;                      // (walk) units seen
+        int slot = 0, nrows = 0, row0 = 0, glo = 0, ghi = 0;
+        int in_lo = 0, in_hi = 0;             // keys live in every row of the group
+        int cend = 0, glast = 0;              // the group's compute-tile end, last-group flag
         int rks[G], rke[G];
-        int in_lo = 0, in_hi = 0;  // keys live in every row of the group: [in_lo, in_hi)
         // one-row groups on 256-key tiles: the row's 64 head weights held in
         // registers for the whole group
         constexpr bool kWregs = G == 1 && C::NSUB == 2;
@@ -569,70 +728,139 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
         #pragma unroll
         for (int i = 0; i < G; ++i)
             vchunk_n[i] = vrow_n[i] = 0u;
-        for (; w.left > 0; walk_next<PLAN>(a, w), ++u) {
-            if (w.first_in_group) {
-                slot = gq & 1;
-                in_lo = 0;
-                in_hi = 0x7fffffff;
-                for (int i = 0; i < G; ++i) {
-                    rks[i] = 0;
-                    rke[i] = 0;
-                    if (i < w.gi.nrows) {
-                        row_range(a, w.gi.row0 + i, rks[i], rke[i]);
-                        in_lo = max(in_lo, rks[i]);
-                        in_hi = min(in_hi, rke[i]);
+        for (uint32_t use = 0;; ++use) {
+            bool compute = true, mine = true, last;
+            int j;
+            uint32_t halves = 0;
+            float ksc[NSUB];
+            if constexpr (DESC) {
+                if (!mbar_wait(&acc_full[acc], use & 1u, abort_flag, a.status))
+                    break;
+                tc_fence_after();
+                const uint8_t *sd = smem + C::OFF_SIDE + acc * C::SIDE_BYTES;
+                // the descriptor, box flags and key scales are read together,
+                // before any branch on them
+                const int2 d0 = *reinterpret_cast<const int2 *>(sd + C::SIDE_DESC);  // j, gq
+                halves = *reinterpret_cast<const uint32_t *>(sd + C::SIDE_FLAGS);
+                #pragma unroll
+                for (int sub = 0; sub < NSUB; ++sub)
+                    ksc[sub] = FMT == kFmtFp8
+                                   ? reinterpret_cast<const float *>(sd)[sub * kMmaM + kq]
+                                   : 1.0f;
+                if (d0.x == kDescDone)
+                    break;
+                if (d0.y != gq) {  // a new row group: its weights, rows and ranges
+                    gq = d0.y;
+                    slot = gq & 1;
+                    if (!mbar_wait(&q_full[slot], (gq >> 1) & 1, abort_flag, a.status))
+                        break;
+                    const int *gb =
+                        reinterpret_cast<const int *>(smem + C::OFF_GRP + slot * C::GRP_BYTES);
+                    const int4 g0v = *reinterpret_cast<const int4 *>(gb);
+                    const int4 g1v = *reinterpret_cast<const int4 *>(gb + 4);
+                    const int4 rs = *reinterpret_cast<const int4 *>(gb + kGrpRks);
+                    const int4 re = *reinterpret_cast<const int4 *>(gb + kGrpRke);
+                    nrows = g0v.x;
+                    row0 = g0v.y;
+                    glo = g0v.z;
+                    ghi = g0v.w;
+                    in_lo = g1v.x;
+                    in_hi = g1v.y;
+                    cend = g1v.z;
+                    glast = g1v.w;
+                    const int rsa[4] = {rs.x, rs.y, rs.z, rs.w};
+                    const int rea[4] = {re.x, re.y, re.z, re.w};
+                    #pragma unroll
+                    for (int i = 0; i < G; ++i) {
+                        rks[i] = rsa[i];
+                        rke[i] = rea[i];
+                    }
+                    if constexpr (kWregs) {
+                        const float4 *w4 =
+                            reinterpret_cast<const float4 *>(smem + C::OFF_W + slot * C::W_BYTES);
+                        #pragma unroll
+                        for (int q = 0; q < 16; ++q)
+                            wreg[q] = w4[q];
                     }
                 }
-                if (!mbar_wait(&q_full[slot], (gq >> 1) & 1, abort_flag, a.status))
+                j = d0.x;
+                // the group's last tile on this accumulator; in the CTA's last
+                // group, the accumulator's last tile
+                last = acc + (int)use * NA + NA >= cend;
+            } else {
+                if (w.left <= 0)
                     break;
-                if constexpr (kWregs) {
-                    const float4 *w4 =
-                        reinterpret_cast<const float4 *>(smem + C::OFF_W + slot * C::W_BYTES);
-                    #pragma unroll
-                    for (int q = 0; q < 16; ++q)
-                        wreg[q] = w4[q];
+                if (w.first_in_group) {
+                    slot = gq & 1;
+                    nrows = w.gi.nrows;
+                    row0 = w.gi.row0;
+                    glo = w.gi.lo;
+                    ghi = w.gi.hi;
+                    in_lo = 0;
+                    in_hi = 0x7fffffff;
+                    for (int i = 0; i < G; ++i) {
+                        rks[i] = 0;
+                        rke[i] = 0;
+                        if (i < nrows) {
+                            row_range(a, row0 + i, rks[i], rke[i]);
+                            in_lo = max(in_lo, rks[i]);
+                            in_hi = min(in_hi, rke[i]);
+                        }
+                    }
+                    if (!mbar_wait(&q_full[slot], (gq >> 1) & 1, abort_flag, a.status))
+                        break;
+                    if constexpr (kWregs) {
+                        const float4 *w4 =
+                            reinterpret_cast<const float4 *>(smem + C::OFF_W + slot * C::W_BYTES);
+                        #pragma unroll
+                        for (int q = 0; q < 16; ++q)
+                            wreg[q] = w4[q];
+                    }
+                    ++gq;
                 }
-                ++gq;
+                j = w.j;
+                compute = unit_compute<PLAN>(w, TSH);
+                if (compute) {
+                    mine = c % NA == wg;
+                    ++c;
+                } else {
+                    mine = (int)(u % NA) == wg;
+                }
+                last = walk_last_in_group(w);
             }
-            const int t0 = (w.j << TSH) + kq;  // this thread's key in sub-tile 0
-            const int wend = a.paged ? w.gi.hi : a.N;  // columns this group writes
             // a tile whose every key is live in every row of the group (and
             // no candidate mask): no range tests, unconditional stores
-            const bool interior = !a.cand && (w.j << TSH) >= in_lo && (w.j << TSH) + TK <= in_hi;
-            const bool compute = unit_compute<PLAN>(w, TSH);
-            bool mine;
+            const bool interior = !a.cand && (j << TSH) >= in_lo && (j << TSH) + TK <= in_hi;
+            const int t0 = (j << TSH) + kq;  // this thread's key in sub-tile 0
+            const int wend = a.paged ? ghi : a.N;  // columns this group writes
             float val[NSUB][G];
             #pragma unroll
             for (int sub = 0; sub < NSUB; ++sub)
                 #pragma unroll
                 for (int i = 0; i < G; ++i)
                     val[sub][i] = -INFINITY;
-            if (compute) {
-                mine = c % NA == wg;
-                ++c;
-            } else {
-                mine = (int)(u % NA) == wg;
-            }
             if (compute && mine) {
-                const int acc = wg;
-                const int use = (c - 1) / NA;  // uses of this accumulator so far
-                if (!mbar_wait(&acc_full[acc], (uint32_t)(use & 1), abort_flag, a.status))
-                    break;
-                tc_fence_after();
-                // key scales and box flags from the accumulator's side copy
-                const uint8_t *sd = smem + C::OFF_SIDE + acc * C::SIDE_BYTES;
-                const uint32_t halves = *reinterpret_cast<const uint32_t *>(sd + C::SIDE_FLAGS);
+                if constexpr (!DESC) {
+                    const int use_w = (c - 1) / NA;  // uses of this accumulator so far
+                    if (!mbar_wait(&acc_full[acc], (uint32_t)(use_w & 1), abort_flag, a.status))
+                        break;
+                    tc_fence_after();
+                    // key scales and box flags from the accumulator's side copy
+                    const uint8_t *sd = smem + C::OFF_SIDE + acc * C::SIDE_BYTES;
+                    halves = *reinterpret_cast<const uint32_t *>(sd + C::SIDE_FLAGS);
+                    #pragma unroll
+                    for (int sub = 0; sub < NSUB; ++sub)
+                        ksc[sub] = FMT == kFmtFp8
+                                       ? reinterpret_cast<const float *>(sd)[sub * kMmaM + kq]
+                                       : 1.0f;
+                }
                 bool live[NSUB];
-                float ksc[NSUB];
                 bool pos = true;
                 #pragma unroll
                 for (int sub = 0; sub < NSUB; ++sub) {
                     const int key = sub * kMmaM + kq, t = t0 + sub * kMmaM;
-                    live[sub] = (interior || (t < w.gi.hi && t >= w.gi.lo)) &&
+                    live[sub] = (interior || (t < ghi && t >= glo)) &&
                                 ((halves >> (key >> 6)) & 1u);
-                    ksc[sub] = 1.0f;
-                    if (FMT == kFmtFp8)
-                        ksc[sub] = reinterpret_cast<const float *>(sd)[key];
                     pos = pos && ksc[sub] >= 0.0f;
                 }
                 const float *wsm = reinterpret_cast<const float *>(smem + C::OFF_W + slot * C::W_BYTES);
@@ -755,7 +983,7 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
                         const float sgn = ksc[sub] >= 0.0f ? 1.0f : -1.0f;
                         #pragma unroll
                         for (int i = 0; i < G; ++i) {
-                            if (i >= w.gi.nrows)
+                            if (i >= nrows)
                                 break;
                             const uint32_t trow = tbase + sub * C::NCOLS + i * H;
                             const float4 *w4 = reinterpret_cast<const float4 *>(wsm + i * H);
@@ -817,10 +1045,10 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
             if (mine) {
                 #pragma unroll
                 for (int i = 0; i < G; ++i) {
-                    if (i >= w.gi.nrows)
+                    if (i >= nrows)
                         break;
                     const int end = min(wend, a.paged ? rke[i] : a.N);
-                    float *orow = a.logits + (size_t)(w.gi.row0 + i) * a.ld;
+                    float *orow = a.logits + (size_t)(row0 + i) * a.ld;
                     #pragma unroll
                     for (int sub = 0; sub < NSUB; ++sub) {
                         const int t = t0 + sub * kMmaM;
@@ -841,7 +1069,7 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
                                 #pragma unroll
                                 for (int i = 0; i < G; ++i)
                                     if (vchunk_n[i])
-                                        atomicAdd(a.cvalid + (size_t)(w.gi.row0 + i) * a.hist_P +
+                                        atomicAdd(a.cvalid + (size_t)(row0 + i) * a.hist_P +
                                                       vchunk, vchunk_n[i]);
                             #pragma unroll
                             for (int i = 0; i < G; ++i)
@@ -850,7 +1078,7 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
                         }
                         #pragma unroll
                         for (int i = 0; i < G; ++i) {
-                            if (i >= w.gi.nrows)
+                            if (i >= nrows)
                                 break;
                             const uint32_t key = order_key(val[sub][i]);
                             const uint32_t bin = key ? key >> 21 : 0xffffffffu;
@@ -869,9 +1097,9 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
                     // to memory with one atomic
                     #pragma unroll
                     for (int i = 0; i < G; ++i) {
-                        if (i >= w.gi.nrows)
+                        if (i >= nrows)
                             break;
-                        float *brow = a.bmax + (size_t)(w.gi.row0 + i) * a.ld_bmax;
+                        float *brow = a.bmax + (size_t)(row0 + i) * a.ld_bmax;
                         #pragma unroll
                         for (int sub = 0; sub < NSUB; ++sub) {
                             const int t = t0 + sub * kMmaM;
@@ -894,7 +1122,7 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
                     }
                 }
             }
-            if (walk_last_in_group(w)) {
+            if (last) {
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(&q_empty[slot]);
@@ -907,11 +1135,11 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
                     if (lane == 0)
                         #pragma unroll
                         for (int i = 0; i < G; ++i) {
-                            if (i < w.gi.nrows && vchunk_n[i])
-                                atomicAdd(a.cvalid + (size_t)(w.gi.row0 + i) * a.hist_P + vchunk,
+                            if (i < nrows && vchunk_n[i])
+                                atomicAdd(a.cvalid + (size_t)(row0 + i) * a.hist_P + vchunk,
                                           vchunk_n[i]);
-                            if (i < w.gi.nrows && vrow_n[i])
-                                atomicAdd(a.hvalid + w.gi.row0 + i, vrow_n[i]);
+                            if (i < nrows && vrow_n[i])
+                                atomicAdd(a.hvalid + row0 + i, vrow_n[i]);
                         }
                     #pragma unroll
                     for (int i = 0; i < G; ++i)
@@ -924,7 +1152,7 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
                     for (int b = quad * 32 + lane; b < G * 2048; b += 128) {
                         const uint32_t v = hs[b];
                         if (v) {
-                            atomicAdd(a.hist + (size_t)(w.gi.row0 + b / 2048) * 2048 + (b & 2047),
+                            atomicAdd(a.hist + (size_t)(row0 + b / 2048) * 2048 + (b & 2047),
                                       v);
                             hs[b] = 0u;
                         }
@@ -936,6 +1164,13 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
                         break;
                     hphase ^= 1u;
                 }
+            }
+            if constexpr (DESC) {
+                if (last && glast)
+                    break;
+            } else {
+                walk_next<PLAN>(a, w);
+                ++u;
             }
         }
     }
