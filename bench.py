@@ -89,15 +89,15 @@ def producer_bytes(case) -> float:
 # since and the traffic is reported as null.
 LOGITS_SOURCES = ["idx_logits_kernel.cuh", "idx_logits.cuh", "idx_common.cuh", "idx_api.cu"]
 NCU_TRAFFIC = {
-    2: {"bytes": 18639104 + 7703040, "digest": "e4994ba7d68ef8cd",
+    2: {"bytes": 18608128 + 7943424, "digest": "d326c333214ae894",
         "profile": "profiles/logits_traffic_all_configs.md"},
-    3: {"bytes": 157699328 + 4484096, "digest": "e4994ba7d68ef8cd",
+    3: {"bytes": 157696256 + 4502272, "digest": "d326c333214ae894",
         "profile": "profiles/logits_traffic_all_configs.md"},
-    4: {"bytes": 87552 + 189587968 + 5689344, "digest": "e4994ba7d68ef8cd",
+    4: {"bytes": 87808 + 189592576 + 5470464, "digest": "d326c333214ae894",
         "profile": "profiles/logits_traffic_all_configs.md"},
-    5: {"bytes": 285839360 + 14535680, "digest": "e4994ba7d68ef8cd",
+    5: {"bytes": 285835520 + 14193408, "digest": "d326c333214ae894",
         "profile": "profiles/logits_traffic_all_configs.md"},
-    6: {"bytes": 4096 + 413282816 + 18372608, "digest": "e4994ba7d68ef8cd",
+    6: {"bytes": 4352 + 413299968 + 18391552, "digest": "d326c333214ae894",
         "profile": "profiles/logits_traffic_all_configs.md"},
 }
 
