@@ -582,28 +582,14 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
             } else {
                 const int acc = c % NA;
                 const int s = C::stage(c);
-                if (!mbar_wait(&acc_empty[acc], (uint32_t)((c / NA) & 1) ^ 1, abort_flag, a.status))
-                    break;
-                if (!mbar_wait(&full[s], C::phase(c), abort_flag, a.status))
-                    break;
                 uint8_t *st = smem + C::OFF_STAGE + s * C::STAGE_BYTES;
                 uint8_t *sd = smem + C::OFF_SIDE + acc * C::SIDE_BYTES;
-                {
-                    // the epilogue's key scales and flags, out of the stage
-                    if constexpr (FMT == kFmtFp8) {
-                        const float4 *src = reinterpret_cast<const float4 *>(st + C::A_BYTES);
-                        #pragma unroll
-                        for (int i = lane; i < TK / 4; i += 32)
-                            reinterpret_cast<float4 *>(sd)[i] = src[i];
-                    }
-                    if (lane == 0)
-                        *reinterpret_cast<uint32_t *>(sd + C::SIDE_FLAGS) =
-                            *reinterpret_cast<const uint32_t *>(st + C::OFF_FLAGS);
-                    __syncwarp();
-                }
+                if (!mbar_wait(&full[s], C::phase(c), abort_flag, a.status))
+                    break;
                 if constexpr (FMT == kFmtMxfp4) {
                     // K scale words (key-major as loaded) -> one MMA-order atom
-                    // per 128 keys
+                    // per 128 keys, in the stage: built while the accumulator
+                    // may still be draining
                     const uint32_t *sw = reinterpret_cast<const uint32_t *>(st + C::A_BYTES);
                     #pragma unroll
                     for (int sub = 0; sub < C::NSUB; ++sub) {
@@ -616,6 +602,21 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
                                                    lane * 16) = v;
                     }
                     fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                if (!mbar_wait(&acc_empty[acc], (uint32_t)((c / NA) & 1) ^ 1, abort_flag, a.status))
+                    break;
+                {
+                    // the epilogue's key scales and flags, out of the stage
+                    if constexpr (FMT == kFmtFp8) {
+                        const float4 *src = reinterpret_cast<const float4 *>(st + C::A_BYTES);
+                        #pragma unroll
+                        for (int i = lane; i < TK / 4; i += 32)
+                            reinterpret_cast<float4 *>(sd)[i] = src[i];
+                    }
+                    if (lane == 0)
+                        *reinterpret_cast<uint32_t *>(sd + C::SIDE_FLAGS) =
+                            *reinterpret_cast<const uint32_t *>(st + C::OFF_FLAGS);
                     __syncwarp();
                 }
                 if (lane == 0) {
