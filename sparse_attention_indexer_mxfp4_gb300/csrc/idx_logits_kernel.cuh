@@ -222,11 +222,11 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
     using C = LogitsCfg<FMT, H, G, S, NA, TK>;
     constexpr int TSH = TK == 256 ? 8 : 7;  // equals a.tile_shift
     // Tile descriptors (only the control warps walk the units; the epilogue
-    // takes each tile from its descriptor) where the epilogue's arithmetic
-    // per tile is the largest: block maxima, four-row groups.  Elsewhere
-    // every warp walks the units, which keeps the control warps' work per
-    // tile, on those workloads the longer chain, at its least.
-    constexpr bool DESC = BMAX || G == 4;
+    // takes each tile from its descriptor) where they measured faster: block
+    // maxima, four-row groups, MXFP4.  On the FP8 decodes every warp walks
+    // the units, which keeps the control warps' work per tile, there the
+    // longer chain, at its least.
+    constexpr bool DESC = BMAX || G == 4 || FMT == kFmtMxfp4;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // swizzled TMA tiles and MMA descriptors assume 1024-byte aligned tiles
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
