@@ -89,15 +89,15 @@ def producer_bytes(case) -> float:
 # since and the traffic is reported as null.
 LOGITS_SOURCES = ["idx_logits_kernel.cuh", "idx_logits.cuh", "idx_common.cuh", "idx_api.cu"]
 NCU_TRAFFIC = {
-    2: {"bytes": 18608128 + 7943424, "digest": "d326c333214ae894",
+    2: {"bytes": 18590976 + 7609600, "digest": "e0cc2237a873a74a",
         "profile": "profiles/logits_traffic_all_configs.md"},
-    3: {"bytes": 157696256 + 4502272, "digest": "d326c333214ae894",
+    3: {"bytes": 157704192 + 4539392, "digest": "e0cc2237a873a74a",
         "profile": "profiles/logits_traffic_all_configs.md"},
-    4: {"bytes": 87808 + 189592576 + 5470464, "digest": "d326c333214ae894",
+    4: {"bytes": 87552 + 189610752 + 5420800, "digest": "e0cc2237a873a74a",
         "profile": "profiles/logits_traffic_all_configs.md"},
-    5: {"bytes": 285835520 + 14193408, "digest": "d326c333214ae894",
+    5: {"bytes": 285837056 + 14335744, "digest": "e0cc2237a873a74a",
         "profile": "profiles/logits_traffic_all_configs.md"},
-    6: {"bytes": 4352 + 413299968 + 18391552, "digest": "d326c333214ae894",
+    6: {"bytes": 3840 + 413299200 + 18456832, "digest": "e0cc2237a873a74a",
         "profile": "profiles/logits_traffic_all_configs.md"},
 }
 
