@@ -44,6 +44,7 @@ constexpr int kChunk = kSteps * kThreads * 4;    // 32768 keys per CTA
 constexpr int kMaxCluster = 8;                   // portable cluster size
 constexpr int kMaxLen = kChunk * kMaxCluster;    // 262144
 constexpr int kTab = kSteps * kWarps;            // (step, warp) entries
+constexpr int kBtStage = 2048;                   // block-table entries staged per CTA
 
 struct Shared {
     uint4 keys[kChunk / 4];
@@ -56,6 +57,7 @@ struct Shared {
     uint32_t cta[3];    // this CTA's finite keys, keys above T, keys equal to T
     uint32_t gt[kTab];  // keys above T (or taken) per (step, warp), then offsets
     uint32_t eq[kTab];  // keys equal to T per (step, warp), then offsets
+    int32_t bts[kBtStage];  // (slot count) the chunk's pages' block-table entries
 };
 
 // Sum over the CTA of one value per thread (every thread gets it); one
@@ -116,6 +118,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int end = max(0, min(len - base, per));        // keys of this CTA's chunk
     const int nrun = (end + 4 * kThreads - 1) / (4 * kThreads);  // runs holding them
     const float *rowp = logits + (size_t)(live ? row : 0) * ld + base;
+    // (slot count) the block-table entries of the chunk's pages go to shared
+    // memory while the keys load, when they fit (-1 past max_blocks)
+    const int seq = sc.bt && live ? (sc.row_to_seq ? __ldg(sc.row_to_seq + row) : row / sc.next_n)
+                                  : 0;
+    int bt_lo = 0;
+    bool bt_staged = false;
+    if (sc.bt && live && end > 0) {
+        const int lo = sc.shift >= 0 ? base >> sc.shift : base / sc.P;
+        const int hi = sc.shift >= 0 ? (base + end - 1) >> sc.shift : (base + end - 1) / sc.P;
+        if (hi - lo < kBtStage) {
+            bt_staged = true;
+            bt_lo = lo;
+            const int32_t *btrow = sc.bt + (size_t)seq * sc.bt_stride;
+            for (int i = tid; i <= hi - lo; i += kThreads)
+                sh.bts[i] = lo + i < sc.max_blocks ? __ldg(btrow + lo + i) : -1;
+        }
+    }
 
     // keys of this chunk into shared memory, the local digit-1 histogram
     // from them as they are formed (the histograms were cleared above)
@@ -257,8 +276,6 @@ found:
     const uint32_t lt = (1u << lane) - 1u;
     int32_t *orow = out + (size_t)(live ? row : 0) * ld_out;
     uint32_t nslot = 0, nbad = 0;  // valid and invalid slots of this thread's taken keys
-    const int seq = sc.bt && live ? (sc.row_to_seq ? __ldg(sc.row_to_seq + row) : row / sc.next_n)
-                                  : 0;
     if (live) {
         #pragma unroll
         for (int s = 0; s < kSteps; ++s) {
@@ -291,7 +308,14 @@ found:
                     const int p = base + 4 * (s * kThreads + tid) + e;
                     orow[pos++] = p;
                     if (sc.bt) {
-                        const bool ok = slot_valid(sc, seq, p);
+                        bool ok;
+                        if (bt_staged) {
+                            const int lp = sc.shift >= 0 ? p >> sc.shift : p / sc.P;
+                            const int pg = sh.bts[lp - bt_lo];
+                            ok = pg >= 0 && pg < sc.num_pages;
+                        } else {
+                            ok = slot_valid(sc, seq, p);
+                        }
                         nslot += ok;
                         nbad += !ok;
                     }

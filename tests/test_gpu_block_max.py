@@ -19,7 +19,7 @@ def _t(a):
     return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
 
-def _run(c, block):
+def _run(c, block, num_ctas=0):
     nb = -(-c.width // block)
     ld = nb + 3
     logits = torch.full((c.rows, c.width), float("nan"), dtype=torch.float32, device="cuda")
@@ -28,14 +28,15 @@ def _run(c, block):
     B.idx_paged_mqa_logits_block_max(_t(c.q), _t(c.q_scale), _t(c.weights), pages,
                                      _t(c.block_table), _t(c.context_lens), c.next_n,
                                      c.page_size, c.fmt, logits, c.width, bmax, block,
-                                     row_ks=_t(c.row_ks), ctx_per_row=c.ctx_per_row)
+                                     row_ks=_t(c.row_ks), ctx_per_row=c.ctx_per_row,
+                                     num_ctas=num_ctas)
     torch.cuda.synchronize()
     assert B.idx_get_device_status() == 0
     return logits.cpu().numpy(), bmax.cpu().numpy(), nb
 
 
-def _check(c, block):
-    gl, gb, nb = _run(c, block)
+def _check(c, block, num_ctas=0):
+    gl, gb, nb = _run(c, block, num_ctas)
     ref, bad = oracle.paged_mqa_logits(c.fmt, c.q, c.q_scale, c.weights, c.pages, c.page_stride,
                                        c.num_pages, c.block_table, c.context_lens,
                                        c.ctx_per_row, c.row_ks, c.B, c.next_n, c.H, c.D,
@@ -75,3 +76,13 @@ def test_block_max_mxfp4(next_n):
     c = synth.paged_case(80 + next_n, ctx, next_n, 64, 128, 64, 3072, fmt=synth.FMT_MXFP4,
                          pool_factor=1.2)
     _check(c, 128)
+
+
+@pytest.mark.parametrize("num_ctas", [1, 3, 7, 1000])
+def test_block_max_grid_sizes(num_ctas):
+    """The block-maxima kernel takes its tiles from descriptors: CTA ranges
+    that end inside a group, groups with fewer tiles than accumulators and
+    CTAs without units (1000) all end on the same outputs."""
+    ctx = [2, 63, 700, 2049, 130, 4000]
+    c = synth.paged_case(91, ctx, 2, 64, 128, 64, 4096, pool_factor=1.3)
+    _check(c, 128, num_ctas)

@@ -219,6 +219,17 @@ def test_paged_grid_sizes_agree(num_ctas):
     compare_paged(c, gpu_paged(c, num_ctas=num_ctas), ora_paged(c)[0])
 
 
+@pytest.mark.parametrize("next_n", [1, 2])
+@pytest.mark.parametrize("num_ctas", [1, 3, 7, 1000])
+def test_paged_mxfp4_grid_sizes_agree(next_n, num_ctas):
+    """MXFP4 kernels take their tiles from descriptors (one-row groups on two
+    accumulators, two-row groups on three): every split of the units over
+    the CTAs, empty CTAs included, gives the oracle's logits."""
+    c = synth.paged_case(72 + next_n, [900, 5, 333, 1200, 64], next_n, 64, 128, 64, 2048,
+                         fmt=synth.FMT_MXFP4, pool_factor=1.1)
+    compare_paged(c, gpu_paged(c, num_ctas=num_ctas), ora_paged(c)[0])
+
+
 def test_paged_bad_page_sets_status_and_masks():
     c = synth.paged_case(80, [300, 300], 1, 64, 128, 64, 512, pool_factor=1.0)
     c.block_table[1, 2] = c.num_pages + 5  # keys 128..191 of sequence 1
