@@ -322,11 +322,13 @@ def scored_keys(case) -> int:
     return case.keys_scored
 
 
-def topk_bytes(case) -> float:
+def topk_bytes(case, with_slots: bool = False) -> float:
     """Algorithmic bytes of one top-k stage: every logit the selection
     ranks read once (the live keys of each row, or only its candidate keys)
     and k int32 indices written per row; the candidate source also reads its
-    block maxima and writes its pool."""
+    block maxima and writes its pool.  with_slots (the stage also runs the
+    slot map, one idx_topk_ragged_slots call): k int32 slots, a row length
+    and an indptr entry written per row."""
     from sparse_attention_indexer_mxfp4_gb300.synth import PagedCase
     if isinstance(case, PagedCase):
         b = 4.0 * scored_keys(case) + 4.0 * case.rows * case.topk
@@ -335,6 +337,8 @@ def topk_bytes(case) -> float:
         if getattr(case, "source_block", 0):
             nb = -(-case.width // case.source_block)
             b += 4.0 * case.rows * (nb + case.source_cands)
+        if with_slots:
+            b += 4.0 * case.rows * (case.topk + 2) + 4.0
         return b
     return 4.0 * float(np.maximum(case.ke - case.ks, 0).sum()) + 4.0 * case.M * case.topk
 
@@ -440,7 +444,10 @@ def measure(cfg: int, args, dev, world: int, rank: int, headline: bool) -> dict:
         out.update({"tokens_per_step": case.T, "k_store_ms": round(logit_avg, 5),
                     "q_quant_ms": round(topk_avg, 5)})
     else:
-        tb = topk_bytes(case)
+        # the top-k stage holds the slot map when the step runs the two as
+        # one call (paged, the row top-k as its own call)
+        with_slots = bool(getattr(step, "_slots_call", 1) is None and paged)
+        tb = topk_bytes(case, with_slots)
         tach = tb / (topk_avg * 1e-3) / 1e9
         out.update({
             "keys_scored_per_step": keys,
@@ -449,7 +456,9 @@ def measure(cfg: int, args, dev, world: int, rank: int, headline: bool) -> dict:
             "logits_stage_ms_in_step": round(logit_step, 5),
             "topk_stage_ms_in_step": round(topk_step, 5),
             "topk_rows_per_s": round(world * rows / (topk_avg * 1e-3), 1),
-            "topk_roofline": {"bound": "hbm", "achieved": round(tach, 1), "peak": hbm,
+            "topk_roofline": {"stage": ("top-k + slot map (one call)" if with_slots
+                                        else "top-k"),
+                              "bound": "hbm", "achieved": round(tach, 1), "peak": hbm,
                               "unit": "GB/s", "frac": round(tach / hbm, 4),
                               "algorithmic_bytes_per_launch": tb,
                               "avg_launch_ms": round(topk_avg, 5),
