@@ -108,7 +108,9 @@ struct LogitsCfg {
     // full[S], empty[S], acc_full[NA], acc_empty[NA], q_full[2], q_empty[2]
     // + hist[NA][2]: a warpgroup's histogram hand-over (histogram variant)
     // + drain[2]: each MMA warp's last commit after an abort
-    static constexpr int NUM_BARS = 2 * S + 2 * NA + 4 + 2 * NA + 2;
+    // + acc_full2[NA], acc_empty2[NA]: the second column half of each
+    //   accumulator (split accumulators)
+    static constexpr int NUM_BARS = 2 * S + 2 * NA + 4 + 2 * NA + 2 + 2 * NA;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;  // tmem base, abort flag
     static constexpr int OFF_SCRATCH = (OFF_MISC + 16 + 7) / 8 * 8;  // 40 long longs
     static constexpr int OFF_BITMAP = OFF_SCRATCH + 40 * 8;
@@ -140,6 +142,11 @@ struct LogitsCfg {
     {
         return (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(NCOLS >> 3) << 17) |
                ((uint32_t)(kMmaM >> 4) << 24);
+    }
+    // the same with N = NCOLS / 2 (one column half of a split accumulator)
+    __host__ __device__ static constexpr uint32_t idesc_f8_half()
+    {
+        return (1u << 4) | ((uint32_t)(NCOLS >> 4) << 17) | ((uint32_t)(kMmaM >> 4) << 24);
     }
     // block-scaled e2m1 x e2m1 with ue8m0 scales; the scale-factor ids select
     // the byte of each 32-bit scale word the MMA starts from.
@@ -227,6 +234,11 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
     // the units, which keeps the control warps' work per tile, there the
     // longer chain, at its least.
     constexpr bool DESC = BMAX || G == 4 || FMT == kFmtMxfp4;
+    // Split accumulators (four-row FP8 groups, N = 256): each tile's MMA is
+    // issued as two N = 128 halves (rows 0-1 and 2-3 of the group) with
+    // their own full / empty barriers, so the next tile's first half runs
+    // while the epilogue drains the second half of this one.
+    constexpr bool SPLIT = DESC && FMT == kFmtFp8 && G == 4 && C::NSUB == 1;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // swizzled TMA tiles and MMA descriptors assume 1024-byte aligned tiles
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -236,6 +248,7 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
     uint64_t *q_full = acc_empty + NA, *q_empty = q_full + 2;
     uint64_t *hbar = q_empty + 2;  // [NA][2]: counts done, flush done
     uint64_t *drain = hbar + 2 * NA;  // [2]: MMA warps' commits after an abort
+    uint64_t *acc_full2 = drain + 2, *acc_empty2 = acc_full2 + NA;  // split accumulators
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
     long long *scratch = reinterpret_cast<long long *>(smem + C::OFF_SCRATCH);
@@ -252,6 +265,8 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
         for (int i = 0; i < NA; ++i) {
             mbar_init(&acc_full[i], 2);  // the MMA's commit + the MMA warp's side copy
             mbar_init(&acc_empty[i], 4);  // the owning warpgroup's warps
+            mbar_init(&acc_full2[i], 1);  // the second half's commit
+            mbar_init(&acc_empty2[i], 4);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&q_full[i], 1);
@@ -619,7 +634,22 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
                             *reinterpret_cast<const uint32_t *>(st + C::OFF_FLAGS);
                     __syncwarp();
                 }
-                if (lane == 0) {
+                if (SPLIT && lane == 0) {
+                    // the first column half: rows 0-1 of the group
+                    tc_fence_after();
+                    const uint32_t b_addr = smem_u32(smem + C::OFF_Q + slot * C::Q_BYTES);
+                    const uint32_t a_addr = smem_u32(st);
+                    #pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        uint64_t ad = make_smem_desc(a_addr + kk * 32, 16, 1024, kLayoutSw128);
+                        uint64_t bd = make_smem_desc(b_addr + kk * 32, 16, 1024, kLayoutSw128);
+                        mma_f8f6f4(tmem_base + acc * C::ACC_COLS, ad, bd, C::idesc_f8_half(),
+                                   kk > 0 ? 1u : 0u);
+                    }
+                    *reinterpret_cast<int2 *>(sd + C::SIDE_DESC) = make_int2(w.j, gq - 1);
+                    mma_commit(&acc_full[acc]);
+                    mbar_arrive(&acc_full[acc]);  // releases the side copy and descriptor
+                } else if (!SPLIT && lane == 0) {
                     tc_fence_after();
                     const uint32_t b_addr = smem_u32(smem + C::OFF_Q + slot * C::Q_BYTES);
                     #pragma unroll
@@ -659,6 +689,29 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
                     mbar_arrive(&acc_full[acc]);  // releases the side copy and descriptor
                 }
                 __syncwarp();
+                if constexpr (SPLIT) {
+                    // the second column half (rows 2-3), once the epilogue
+                    // has drained it of the accumulator's previous tile
+                    if (!mbar_wait(&acc_empty2[acc], (uint32_t)((c / NA) & 1) ^ 1, abort_flag,
+                                   a.status))
+                        break;
+                    if (lane == 0) {
+                        tc_fence_after();
+                        const uint32_t b_addr = smem_u32(smem + C::OFF_Q + slot * C::Q_BYTES) +
+                                                (uint32_t)(C::NCOLS / 2 * C::ROWB);
+                        const uint32_t a_addr = smem_u32(st);
+                        #pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            uint64_t ad = make_smem_desc(a_addr + kk * 32, 16, 1024, kLayoutSw128);
+                            uint64_t bd = make_smem_desc(b_addr + kk * 32, 16, 1024, kLayoutSw128);
+                            mma_f8f6f4(tmem_base + acc * C::ACC_COLS + C::NCOLS / 2, ad, bd,
+                                       C::idesc_f8_half(), kk > 0 ? 1u : 0u);
+                        }
+                        mma_commit(&empty[s]);
+                        mma_commit(&acc_full2[acc]);
+                    }
+                    __syncwarp();
+                }
                 ++c;
             }
             if (walk_last_in_group(w)) {
@@ -871,6 +924,7 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
                 // case skips the sign multiply.  Branches stay warp-uniform so
                 // the warp is converged at every tcgen05.ld.
                 const bool all_pos = __all_sync(0xffffffffu, pos);
+                bool h0_back = false;  // (split) the first column half handed back
                 const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * C::ACC_COLS;
                 bool summed = false;
                 if constexpr (NSUB == 2) {
@@ -946,7 +1000,9 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
                     #pragma unroll
                     for (int u = 0; u < NU; ++u) {
                         const int sub = u / (2 * G), i = (u / 2) % G, half = u & 1;
-                        if (u + 1 < NU) {
+                        // (split) the second column half is loaded only once
+                        // its MMA has landed, below
+                        if (u + 1 < NU && !(SPLIT && u + 1 == NU / 2)) {
                             const int s1 = (u + 1) / (2 * G), i1 = ((u + 1) / 2) % G,
                                       h1 = (u + 1) & 1;
                             tmem_ld_32x32b_x32(tbase + s1 * C::NCOLS + i1 * H + h1 * 32,
@@ -975,10 +1031,29 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
                                               ((cc[1].x + cc[3].x) + (cc[1].y + cc[3].y));
                             val[sub][i] = fabsf(ksc[sub]) * sum;
                         }
-                        if (u + 1 < NU)
+                        if (SPLIT && u + 1 == NU / 2) {
+                            // rows 0-1 done: their half goes back to the MMA
+                            // warp, then rows 2-3 once their half has landed
+                            // (after an abort the wait returns at once and the
+                            // tile's values are discarded)
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0)
+                                mbar_arrive(&acc_empty[acc]);
+                            h0_back = true;
+                            (void)mbar_wait(&acc_full2[acc], use & 1u, abort_flag, a.status);
+                            tc_fence_after();
+                            tmem_ld_32x32b_x32(tbase + C::NCOLS / 2, rb[(u + 1) & 1]);
                             tmem_ld_wait();
+                        } else if (u + 1 < NU) {
+                            tmem_ld_wait();
+                        }
                     }
                 } else {
+                    if constexpr (SPLIT) {  // both column halves first
+                        (void)mbar_wait(&acc_full2[acc], use & 1u, abort_flag, a.status);
+                        tc_fence_after();
+                    }
                     #pragma unroll
                     for (int sub = 0; sub < NSUB; ++sub) {
                         const float sgn = ksc[sub] >= 0.0f ? 1.0f : -1.0f;
@@ -1016,8 +1091,11 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&acc_empty[acc]);
+                if (lane == 0) {
+                    if (SPLIT && !h0_back)
+                        mbar_arrive(&acc_empty[acc]);
+                    mbar_arrive(SPLIT ? &acc_empty2[acc] : &acc_empty[acc]);
+                }
                 // masks
                 #pragma unroll
                 for (int sub = 0; sub < NSUB; ++sub) {
