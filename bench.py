@@ -89,15 +89,15 @@ def producer_bytes(case) -> float:
 # since and the traffic is reported as null.
 LOGITS_SOURCES = ["idx_logits_kernel.cuh", "idx_logits.cuh", "idx_common.cuh", "idx_api.cu"]
 NCU_TRAFFIC = {
-    2: {"bytes": 18590976 + 7609600, "digest": "e0cc2237a873a74a",
+    2: {"bytes": 18600192 + 7281152, "digest": "0123673903672453",
         "profile": "profiles/logits_traffic_all_configs.md"},
-    3: {"bytes": 157704192 + 4539392, "digest": "e0cc2237a873a74a",
+    3: {"bytes": 157698304 + 4448768, "digest": "0123673903672453",
         "profile": "profiles/logits_traffic_all_configs.md"},
-    4: {"bytes": 87552 + 189610752 + 5420800, "digest": "e0cc2237a873a74a",
+    4: {"bytes": 87552 + 189605888 + 5425408, "digest": "0123673903672453",
         "profile": "profiles/logits_traffic_all_configs.md"},
-    5: {"bytes": 285837056 + 14335744, "digest": "e0cc2237a873a74a",
+    5: {"bytes": 285834752 + 14224128, "digest": "0123673903672453",
         "profile": "profiles/logits_traffic_all_configs.md"},
-    6: {"bytes": 3840 + 413299200 + 18456832, "digest": "e0cc2237a873a74a",
+    6: {"bytes": 4352 + 413302272 + 18482432, "digest": "0123673903672453",
         "profile": "profiles/logits_traffic_all_configs.md"},
 }
 
