@@ -518,6 +518,10 @@ static idx_status paged_logits(bool cand_only,
         a.bmax = bm.out;
         a.ld_bmax = bm.ld;
         a.bmax_block = bm.block;
+        a.bmax_shift = -1;
+        for (int b = 0; b < 31; ++b)
+            if ((1 << b) == bm.block)
+                a.bmax_shift = b;
         const dim3 grid(std::min((bm_blocks + 255) / 256, 64), std::min(B * next_n, 65535));
         if (launch_pdl(bmax_fill_kernel, grid, dim3(256), 0, (cudaStream_t)stream, bm.out, bm.ld,
                        B * next_n, bm_blocks) != cudaSuccess)

@@ -141,6 +141,13 @@ IDX_DEVFN uint32_t order_key(float v)
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
+// The float of a nonzero order_key (the inverse of order_key on finite
+// values).
+IDX_DEVFN float key_float(uint32_t k)
+{
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
 // Float max into memory holding a float (prefilled, e.g. with -inf): values
 // with the sign bit clear order like their bits as signed integers and win by
 // atomicMax; values with it set order inversely to their bits as unsigned

@@ -73,6 +73,7 @@ struct LogitsArgs {
     float *bmax;
     int64_t ld_bmax;
     int bmax_block;
+    int bmax_shift;          // log2(bmax_block) if a power of two, else -1
     // Digit-1 histograms for a chunked top-k that runs next (nullable):
     // hist[r][2048] counts the written finite logits of row r by their
     // order-preserving key's top 11 bits, hvalid[r] and cvalid[r][hist_P]

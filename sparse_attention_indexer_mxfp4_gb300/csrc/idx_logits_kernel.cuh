@@ -1182,21 +1182,22 @@ __global__ void __launch_bounds__(LogitsCfg<FMT, H, G, S, NA, TK>::THREADS, 1)
                         #pragma unroll
                         for (int sub = 0; sub < NSUB; ++sub) {
                             const int t = t0 + sub * kMmaM;
-                            const int b = t >= rks[i] ? (t - rks[i]) / a.bmax_block : -1;
+                            const int d = t - rks[i];
+                            const int b = d < 0 ? -1
+                                          : a.bmax_shift >= 0 ? d >> a.bmax_shift
+                                                              : d / a.bmax_block;
                             const int b0 = __shfl_sync(0xffffffffu, b, 0);
                             const bool first = b == b0;
-                            float m0 = first ? val[sub][i] : -INFINITY;
-                            float m1 = first ? -INFINITY : val[sub][i];
-                            #pragma unroll
-                            for (int o = 16; o > 0; o >>= 1) {
-                                m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
-                                m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
-                            }
+                            // each part's maximum as an order-preserving key
+                            // (-inf: 0), one warp reduction each
+                            const uint32_t kv = order_key(val[sub][i]);
+                            const uint32_t k0 = __reduce_max_sync(0xffffffffu, first ? kv : 0u);
+                            const uint32_t k1 = __reduce_max_sync(0xffffffffu, first ? 0u : kv);
                             const uint32_t second = __ballot_sync(0xffffffffu, !first);
-                            if (lane == 0 && b0 >= 0 && m0 > -INFINITY)
-                                atomic_max_float(brow + b0, m0);
-                            if (second && lane == __ffs(second) - 1 && b >= 0 && m1 > -INFINITY)
-                                atomic_max_float(brow + b, m1);
+                            if (lane == 0 && b0 >= 0 && k0)
+                                atomic_max_float(brow + b0, key_float(k0));
+                            if (second && lane == __ffs(second) - 1 && b >= 0 && k1)
+                                atomic_max_float(brow + b, key_float(k1));
                         }
                     }
                 }
