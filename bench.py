@@ -89,15 +89,15 @@ def producer_bytes(case) -> float:
 # since and the traffic is reported as null.
 LOGITS_SOURCES = ["idx_logits_kernel.cuh", "idx_logits.cuh", "idx_common.cuh", "idx_api.cu"]
 NCU_TRAFFIC = {
-    2: {"bytes": 18600192 + 7281152, "digest": "0123673903672453",
+    2: {"bytes": 18609152 + 7529216, "digest": "0eb22f7a66d754d4",
         "profile": "profiles/logits_traffic_all_configs.md"},
-    3: {"bytes": 157698304 + 4448768, "digest": "0123673903672453",
+    3: {"bytes": 157697280 + 4507904, "digest": "0eb22f7a66d754d4",
         "profile": "profiles/logits_traffic_all_configs.md"},
-    4: {"bytes": 87552 + 189605888 + 5425408, "digest": "0123673903672453",
+    4: {"bytes": 87808 + 189602304 + 5477888, "digest": "0eb22f7a66d754d4",
         "profile": "profiles/logits_traffic_all_configs.md"},
-    5: {"bytes": 285834752 + 14224128, "digest": "0123673903672453",
+    5: {"bytes": 285833984 + 14241024, "digest": "0eb22f7a66d754d4",
         "profile": "profiles/logits_traffic_all_configs.md"},
-    6: {"bytes": 4352 + 413302272 + 18482432, "digest": "0123673903672453",
+    6: {"bytes": 4096 + 413308416 + 18571776, "digest": "0eb22f7a66d754d4",
         "profile": "profiles/logits_traffic_all_configs.md"},
 }
 
