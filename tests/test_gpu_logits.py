@@ -188,6 +188,19 @@ def test_paged_candidate_gather_plan(fmt, num_ctas):
     compare_paged(c, gpu_paged(c, num_ctas=num_ctas), ref)
 
 
+@pytest.mark.parametrize("num_ctas", [0, 7])
+def test_paged_candidate_gather_plan_four_rows(num_ctas):
+    """Four rows a sequence (next_n = 4) with candidates: the gather plan on
+    four-row groups, whose accumulators are split into two column halves."""
+    ctx = [40000, 9, 700, 16385, 260]
+    c = synth.paged_case(95, ctx, 4, 64, 128, 64, 40960, pool_factor=1.2, cand_num=6,
+                         cand_block=128)
+    c.cand[1, :] = -1     # a row without candidates
+    ref = ora_paged(c)[0]
+    compare_paged(c, gpu_paged(c, num_ctas=num_ctas), ref)
+    compare_paged(c, gpu_paged(c, num_ctas=num_ctas, gather=False), ref)
+
+
 @pytest.mark.parametrize("fmt", [synth.FMT_FP8, synth.FMT_MXFP4])
 def test_paged_candidates_only_writes_candidate_tiles(fmt):
     """idx_paged_mqa_logits_candidates: every candidate key is written and
